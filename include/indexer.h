@@ -1,0 +1,224 @@
+/*
+ * indexer.h -- C ABI of the GB300 (sm_103a) DeepSeek-V4.1 compressed-attention
+ * indexer: fp4 index-key publish, query prep, ReLU-weighted head-sum scoring with
+ * the causal mask, the two-level candidate-block filter and the position-ordered
+ * top-k.
+ *
+ * Sources (cited by page title and section):
+ *   [index-keys]  DeepSeek V4.1 / ... / attention / indexer / index-keys page:
+ *                 class Indexer (__init__, forward), SharedAttentionRuntime.
+ *   [compress]    "Module compress" API page (spark_model deepseek_v41_ref):
+ *                 fp4_quant_e8m0_inplace, to_e2m1_rne, yarn_freqs_cis,
+ *                 select_candidate_blocks, precision policy.
+ *   [attention.py] launcher/docker-images/dsv41-flash/patches/attention.py:
+ *                 _indexer_k_cache_head_dim (68-byte MXFP4 row),
+ *                 _fill_short_context_topk_indices, DeepseekV4Indexer.forward.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are caller-owned DEVICE memory unless stated otherwise.
+ *     The library never allocates, frees or keeps device memory, and keeps no
+ *     state between calls other than a thread-local error message.
+ *   - bf16 tensors are passed as their 16-bit patterns (indexer_bf16).
+ *   - Every call validates its arguments on the host before launching anything;
+ *     on failure it returns a negative INDEXER_ERR_* code, launches nothing and
+ *     sets indexer_last_error(). On success it returns INDEXER_OK after enqueuing
+ *     its kernels on `stream` (asynchronous; no implicit synchronisation).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   - Sizes: B sequences, S query rows per sequence (all at the same start_pos),
+ *     H = n_heads, D = head_dim = 128, rd = rope_dim, r = ratio,
+ *     T = (start_pos + S) / r keys visible to the last row,
+ *     vis(s) = (start_pos + s + 1) / r keys visible to row s (compress_lens).
+ *   - The key cache is k_cache[B][T_cap][68] bytes: per key 64 bytes of packed
+ *     e2m1 codes (element 2i in the low nibble of byte i, 2i+1 in the high nibble,
+ *     sign in bit 3 of each nibble) followed by 4 UE8M0 scale bytes, one per block
+ *     of 32 values ([attention.py] _indexer_k_cache_head_dim: 64 + 4 = 68).
+ *     T_cap must be a multiple of 4 and k_cache 16-byte aligned, so every
+ *     sequence's rows start on a 16-byte boundary.
+ *   - Device-side waits are bounded: a kernel whose wait runs out sets a bit in
+ *     the status word at the start of the workspace (indexer_status reads it).
+ */
+#ifndef INDEXER_H_
+#define INDEXER_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t indexer_bf16;          /* bf16 bit pattern */
+typedef struct CUstream_st* indexer_stream_t;   /* == cudaStream_t */
+
+#define INDEXER_OK                 0
+#define INDEXER_ERR_NULL          -1   /* a required pointer is NULL */
+#define INDEXER_ERR_ALIGN         -2   /* a pointer or stride breaks its alignment rule */
+#define INDEXER_ERR_DIMS          -3   /* unsupported n_heads / head_dim / rope_dim / ratio / sizes */
+#define INDEXER_ERR_RANGE         -4   /* positions, T > T_cap, table too short, bad start_pos */
+#define INDEXER_ERR_WORKSPACE     -5   /* workspace smaller than indexer_workspace_size() */
+#define INDEXER_ERR_ARCH          -6   /* current device is not sm_103 */
+#define INDEXER_ERR_CUDA          -7   /* a CUDA runtime call or launch failed */
+#define INDEXER_ERR_DEVICE_TIMEOUT -8  /* a bounded device-side wait ran out (indexer_status) */
+
+#define INDEXER_KEY_ROW_BYTES 68
+#define INDEXER_STATUS_BYTES 256       /* workspace header holding the status word */
+
+/* Indexer shape and selection parameters ([index-keys] Indexer.__init__). */
+typedef struct IndexerDims {
+    int32_t n_heads;           /* H = index_n_heads: 8, 16, 32, 64 or 128 */
+    int32_t head_dim;          /* D = index_head_dim: must be 128 */
+    int32_t rope_dim;          /* rd = rope_head_dim: even, 2..128 (RoPE on the last rd dims) */
+    int32_t ratio;             /* compress_ratio >= 1 */
+    int32_t index_topk;        /* output width (columns beyond min(topk, T) are -1) */
+    int32_t offset;            /* added to every emitted position */
+    int32_t cand_topk_blocks;  /* level one: blocks kept (0: no two-level filter) */
+    int32_t cand_block_size;   /* level one: compressed positions per block */
+    float norm_eps;            /* k_norm RMSNorm epsilon */
+} IndexerDims;
+
+/* YaRN parameters of the compressed layers ([compress] yarn_freqs_cis). */
+typedef struct IndexerYarn {
+    double theta;              /* compress_rope_theta */
+    double factor;             /* YaRN scaling factor */
+    int32_t original_seq_len;  /* YaRN applies when > 0 */
+    double beta_fast;
+    double beta_slow;
+} IndexerYarn;
+
+/* ---------------------------------------------------------------------------
+ * indexer_rope_table -- the RoPE table freqs_cis as (cos, sin) pairs.
+ * [compress] yarn_freqs_cis: precompute_freqs_cis WITH YaRN (original_seq_len > 0),
+ * [seqlen][dim/2] of (cos, sin); the cos_sin_cache the fused ops of [attention.py]
+ * take. NTK-by-parts YaRN: f_i = theta^(-2i/rd), ramp between the correction dims
+ * of beta_fast and beta_slow, f'_i = f_i/factor*ramp + f_i*(1-ramp), rounded to f32;
+ * angle = f32(pos) * f'_i in f32; cos/sin of that angle evaluated in f64 and
+ * rounded to f32.
+ *   table: device float[max_pos][rope_dim/2][2] (cos, sin), written.
+ *   max_pos >= 1; rope_dim even in [2, 128].
+ * ------------------------------------------------------------------------- */
+int indexer_rope_table(const IndexerYarn* yarn, int rope_dim, int max_pos, float* table,
+                       indexer_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * indexer_publish_k -- index-key publish ([index-keys] Indexer.forward, the
+ * owns_k branch; [attention.py] DeepseekV4Indexer._produce_k):
+ *   k = wk(latent)           bf16 Linear, exact sum rounded once to bf16
+ *   k = k_norm(k)            RMSNorm: bf16(w * k / sqrt(mean(k^2) + eps)), f64
+ *   RoPE(k[..., -rd:])       interleaved pairs, f32 rotation, rounded to bf16
+ *   fp4_act_quant(k, 32)     e2m1 (RNE, ties to even code) with e8m0 scales
+ *   k_cache[b][slot] = row
+ * Slots: start_pos == 0 (prefill) writes slots 0..G-1, group j at RoPE position
+ * j*r; start_pos > 0 (decode) needs G == 1 and (start_pos + 1) % r == 0 and
+ * writes slot start_pos / r at position start_pos + 1 - r.
+ *   latent:   bf16 [B][G][Din], 16-byte aligned, Din a multiple of 8 in [8, 1024]
+ *   wk:       bf16 [D][Din] (row o produces output dim o), 16-byte aligned
+ *   k_norm_w: bf16 [D]
+ *   rope_cs:  float [max_pos][rd/2][2]; every used position must be < max_pos
+ *   k_cache:  uint8 [B][T_cap][68]; last written slot must be < T_cap
+ * ------------------------------------------------------------------------- */
+int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B, int G, int Din,
+                      const indexer_bf16* wk, const indexer_bf16* k_norm_w, const float* rope_cs,
+                      int max_pos, int start_pos, uint8_t* k_cache, int T_cap, indexer_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * indexer_prep_q -- query prep ([index-keys] Indexer.forward: RoPE at the query's
+ * own position start_pos + s, fp4_act_quant; weights_proj(x) * softmax_scale *
+ * n_heads^-0.5 with softmax_scale = head_dim^-0.5; [attention.py]
+ * fused_indexer_q_rope_quant):
+ *   q:       bf16 [B][S][H][128] (post wq_b, pre-RoPE), 16-byte aligned
+ *   w:       bf16 [B][S][H] (weights_proj output)
+ *   q_rows:  uint8 [B][S][H][68] quantised query rows (same row format as keys)
+ *   w_prime: float [B][S][H] = w * 128^-0.5 * H^-0.5 (f32)
+ * ------------------------------------------------------------------------- */
+int indexer_prep_q(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
+                   int start_pos, const float* rope_cs, int max_pos, uint8_t* q_rows, float* w_prime,
+                   indexer_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * indexer_scores -- index scores of prepared queries against the key cache
+ * ([index-keys] Indexer.forward: einsum("bshd,btd->bsht"), relu, * weights,
+ * sum over heads; causal mask t >= vis(s) -> -inf; level two: -inf outside the
+ * candidate blocks):
+ *   score[b][s][t] = sum_h w'[b,s,h] * relu(sum_d qhat[b,s,h,d] * khat[b,t,d])
+ * over the dequantised fp4 values, products exact, f32 accumulation.
+ *   q_rows/w_prime as written by indexer_prep_q (q_rows 16-byte aligned)
+ *   cand_blocks: int32 [B][S][cand_topk_blocks] kept block ids (-1 = none), or
+ *                NULL for no candidate filter
+ *   scores: float [B][S][T] written (T = (start_pos + S) / r)
+ *   ws/ws_bytes: workspace of at least INDEXER_STATUS_BYTES (status word)
+ * ------------------------------------------------------------------------- */
+int indexer_scores(const IndexerDims* dims, const uint8_t* q_rows, const float* w_prime, int B, int S,
+                   int start_pos, const uint8_t* k_cache, int T_cap, const int32_t* cand_blocks,
+                   float* scores, void* ws, size_t ws_bytes, indexer_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * indexer_select_candidate_blocks -- level one of the two-level top-k
+ * ([compress] select_candidate_blocks; [index-keys] Indexer.forward). The pages
+ * give the signature only; this library's reading: blocks of cand_block_size
+ * positions, a block is eligible when it holds a position t < vis(s) with a
+ * finite score, its score is the max of those, the cand_topk_blocks best
+ * eligible blocks are kept (ties to the lower block index).
+ *   scores: float [B][S][T] as written by indexer_scores
+ *   blocks_out: int32 [B][S][cand_topk_blocks], kept block ids ascending, -1 pad
+ *   Needs T / cand_block_size + 1 <= 8192 blocks.
+ * ------------------------------------------------------------------------- */
+int indexer_select_candidate_blocks(const IndexerDims* dims, const float* scores, int B, int S,
+                                    int start_pos, int T, int32_t* blocks_out, indexer_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * indexer_topk -- top-k by score re-sorted into position order, offset added,
+ * -1 where unreachable ([index-keys] Indexer.forward, last three lines;
+ * [attention.py] topk_indices_buffer width and _fill_short_context_topk_indices).
+ * k_eff = min(index_topk, T). Among the finite scores at t < vis(s) the k_eff
+ * largest are kept (ties to the lower position) and written ascending as
+ * t + offset, then -1 up to index_topk columns. Rows with vis(s) <= k_eff
+ * and all scores finite reduce to [0 .. vis) + offset (short-context rule).
+ *   scores: float [B][S][T]; out: int32 [B][S][index_topk]
+ *   T <= 32768.
+ * ------------------------------------------------------------------------- */
+int indexer_topk(const IndexerDims* dims, const float* scores, int B, int S, int start_pos, int T,
+                 int32_t* out, indexer_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * indexer_forward -- the whole hot path after the key publish: query prep,
+ * scores, causal mask, optional level-one candidate publication (cand_out,
+ * the candidate source layer) or level-two filter (cand_in, a consumer layer),
+ * and the top-k ([index-keys] Indexer.forward). Either candidate pointer may be
+ * NULL; both non-NULL is allowed (filter by cand_in, publish from the
+ * unfiltered scores).
+ *   q, w, rope_cs, max_pos: as indexer_prep_q
+ *   k_cache, T_cap:         as indexer_scores
+ *   cand_in / cand_out:     int32 [B][S][cand_topk_blocks] or NULL
+ *   topk_out:               int32 [B][S][index_topk]
+ *   scores_out:             float [B][S][T] or NULL (the masked scores)
+ *   ws / ws_bytes:          workspace, at least indexer_workspace_size()
+ * ------------------------------------------------------------------------- */
+int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
+                    int start_pos, const float* rope_cs, int max_pos, const uint8_t* k_cache, int T_cap,
+                    const int32_t* cand_in, int32_t* cand_out, int32_t* topk_out, float* scores_out,
+                    void* ws, size_t ws_bytes, indexer_stream_t stream);
+
+/* Bytes of workspace indexer_forward needs for these sizes (0 on invalid dims).
+ * Layout: status header, quantised query rows, head weights, f32 scores. */
+size_t indexer_workspace_size(const IndexerDims* dims, int B, int S, int start_pos);
+
+/* Zeroes the status word at the start of a workspace (enqueued on `stream`). A
+ * workspace must be initialised once before its first use; kernels only ever OR
+ * bits into the word, and indexer_status clears it when it reads it. */
+int indexer_workspace_init(void* ws, size_t ws_bytes, indexer_stream_t stream);
+
+/* Synchronises `stream`, reads and clears the status word of `ws` and returns
+ * INDEXER_OK or INDEXER_ERR_DEVICE_TIMEOUT. For tests and diagnostics. */
+int indexer_status(void* ws, indexer_stream_t stream);
+
+/* Message of the last failure on this thread ("" if none). */
+const char* indexer_last_error(void);
+
+/* ABI version (major * 100 + minor). */
+int indexer_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* INDEXER_H_ */

@@ -1,0 +1,208 @@
+"""Python binding of the indexer C ABI (include/indexer.h).
+
+Argument marshalling only: every function takes torch tensors that already live
+on the GPU, checks dtype / shape / contiguity, and passes raw pointers and the
+current CUDA stream to the function of the same name in libindexer.so. All
+computation happens in the library's kernels; there is no fallback. If the
+library has not been built, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+__all__ = [
+    "IndexerDims", "IndexerYarn", "IndexerError", "load_library", "KEY_ROW_BYTES", "STATUS_BYTES",
+    "indexer_rope_table", "indexer_publish_k", "indexer_prep_q", "indexer_scores",
+    "indexer_select_candidate_blocks", "indexer_topk", "indexer_forward", "indexer_workspace_size",
+    "indexer_workspace_init", "indexer_status", "indexer_abi_version", "make_dims",
+]
+
+KEY_ROW_BYTES = 68
+STATUS_BYTES = 256
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libindexer.so")
+
+
+class IndexerDims(ctypes.Structure):
+    _fields_ = [
+        ("n_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("rope_dim", ctypes.c_int32),
+        ("ratio", ctypes.c_int32), ("index_topk", ctypes.c_int32), ("offset", ctypes.c_int32),
+        ("cand_topk_blocks", ctypes.c_int32), ("cand_block_size", ctypes.c_int32), ("norm_eps", ctypes.c_float),
+    ]
+
+
+class IndexerYarn(ctypes.Structure):
+    _fields_ = [
+        ("theta", ctypes.c_double), ("factor", ctypes.c_double), ("original_seq_len", ctypes.c_int32),
+        ("beta_fast", ctypes.c_double), ("beta_slow", ctypes.c_double),
+    ]
+
+
+class IndexerError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"indexer error {code}: {msg}")
+        self.code = code
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "indexer_rope_table": [ctypes.POINTER(IndexerYarn), _I, _I, _P, _P],
+    "indexer_publish_k": [ctypes.POINTER(IndexerDims), _P, _I, _I, _I, _P, _P, _P, _I, _I, _P, _I, _P],
+    "indexer_prep_q": [ctypes.POINTER(IndexerDims), _P, _P, _I, _I, _I, _P, _I, _P, _P, _P],
+    "indexer_scores": [ctypes.POINTER(IndexerDims), _P, _P, _I, _I, _I, _P, _I, _P, _P, _P, ctypes.c_size_t, _P],
+    "indexer_select_candidate_blocks": [ctypes.POINTER(IndexerDims), _P, _I, _I, _I, _I, _P, _P],
+    "indexer_topk": [ctypes.POINTER(IndexerDims), _P, _I, _I, _I, _I, _P, _P],
+    "indexer_forward": [ctypes.POINTER(IndexerDims), _P, _P, _I, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P, _P,
+                        ctypes.c_size_t, _P],
+    "indexer_workspace_init": [_P, ctypes.c_size_t, _P],
+    "indexer_status": [_P, _P],
+}
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libindexer.so (built by __graft_entry__.build()); raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    for name, args in _SIGS.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.indexer_workspace_size.argtypes = [ctypes.POINTER(IndexerDims), _I, _I, _I]
+    lib.indexer_workspace_size.restype = ctypes.c_size_t
+    lib.indexer_last_error.argtypes = []
+    lib.indexer_last_error.restype = ctypes.c_char_p
+    lib.indexer_abi_version.argtypes = []
+    lib.indexer_abi_version.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def make_dims(n_heads: int, ratio: int, index_topk: int, offset: int = 0, rope_dim: int = 64,
+              head_dim: int = 128, cand_topk_blocks: int = 0, cand_block_size: int = 0,
+              norm_eps: float = 1e-6) -> IndexerDims:
+    return IndexerDims(n_heads, head_dim, rope_dim, ratio, index_topk, offset, cand_topk_blocks, cand_block_size,
+                       norm_eps)
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise IndexerError(rc, load_library().indexer_last_error().decode())
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "tensor") -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def indexer_abi_version() -> int:
+    return load_library().indexer_abi_version()
+
+
+def indexer_rope_table(yarn: IndexerYarn, rope_dim: int, max_pos: int, table: torch.Tensor, stream=None):
+    """table: float32 [max_pos, rope_dim // 2, 2] (cos, sin)."""
+    if tuple(table.shape) != (max_pos, rope_dim // 2, 2):
+        raise ValueError("table must be [max_pos, rope_dim // 2, 2]")
+    _check(load_library().indexer_rope_table(ctypes.byref(yarn), rope_dim, max_pos,
+                                             _ptr(table, torch.float32, "table"), _stream(stream)))
+
+
+def indexer_publish_k(dims: IndexerDims, latent: torch.Tensor, wk: torch.Tensor, k_norm_w: torch.Tensor,
+                      rope_cs: torch.Tensor, start_pos: int, k_cache: torch.Tensor, stream=None):
+    """latent bf16 [B, G, Din]; wk bf16 [128, Din]; k_norm_w bf16 [128]; k_cache uint8 [B, T_cap, 68]."""
+    B, G, Din = latent.shape
+    if k_cache.dim() != 3 or k_cache.shape[0] != B or k_cache.shape[2] != KEY_ROW_BYTES:
+        raise ValueError("k_cache must be uint8 [B, T_cap, 68]")
+    _check(load_library().indexer_publish_k(
+        ctypes.byref(dims), _ptr(latent, torch.bfloat16, "latent"), B, G, Din, _ptr(wk, torch.bfloat16, "wk"),
+        _ptr(k_norm_w, torch.bfloat16, "k_norm_w"), _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0],
+        start_pos, _ptr(k_cache, torch.uint8, "k_cache"), k_cache.shape[1], _stream(stream)))
+
+
+def indexer_prep_q(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor, start_pos: int, rope_cs: torch.Tensor,
+                   q_rows: torch.Tensor, w_prime: torch.Tensor, stream=None):
+    """q bf16 [B, S, H, 128]; w bf16 [B, S, H]; q_rows uint8 [B, S, H, 68]; w_prime f32 [B, S, H]."""
+    B, S, H, _ = q.shape
+    _check(load_library().indexer_prep_q(
+        ctypes.byref(dims), _ptr(q, torch.bfloat16, "q"), _ptr(w, torch.bfloat16, "w"), B, S, start_pos,
+        _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(q_rows, torch.uint8, "q_rows"),
+        _ptr(w_prime, torch.float32, "w_prime"), _stream(stream)))
+
+
+def indexer_scores(dims: IndexerDims, q_rows: torch.Tensor, w_prime: torch.Tensor, start_pos: int,
+                   k_cache: torch.Tensor, scores: torch.Tensor, ws: torch.Tensor,
+                   cand_blocks: Optional[torch.Tensor] = None, stream=None):
+    """scores f32 [B, S, T]; ws uint8 workspace (>= 256 bytes, status word zeroed once)."""
+    B, S = q_rows.shape[:2]
+    _check(load_library().indexer_scores(
+        ctypes.byref(dims), _ptr(q_rows, torch.uint8, "q_rows"), _ptr(w_prime, torch.float32, "w_prime"), B, S,
+        start_pos, _ptr(k_cache, torch.uint8, "k_cache"), k_cache.shape[1],
+        _ptr(cand_blocks, torch.int32, "cand_blocks"), _ptr(scores, torch.float32, "scores"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def indexer_select_candidate_blocks(dims: IndexerDims, scores: torch.Tensor, start_pos: int,
+                                    blocks_out: torch.Tensor, stream=None):
+    """scores f32 [B, S, T]; blocks_out int32 [B, S, cand_topk_blocks]."""
+    B, S, T = scores.shape
+    _check(load_library().indexer_select_candidate_blocks(
+        ctypes.byref(dims), _ptr(scores, torch.float32, "scores"), B, S, start_pos, T,
+        _ptr(blocks_out, torch.int32, "blocks_out"), _stream(stream)))
+
+
+def indexer_topk(dims: IndexerDims, scores: torch.Tensor, start_pos: int, out: torch.Tensor, stream=None):
+    """scores f32 [B, S, T]; out int32 [B, S, index_topk]."""
+    B, S, T = scores.shape
+    _check(load_library().indexer_topk(ctypes.byref(dims), _ptr(scores, torch.float32, "scores"), B, S, start_pos,
+                                       T, _ptr(out, torch.int32, "out"), _stream(stream)))
+
+
+def indexer_workspace_size(dims: IndexerDims, B: int, S: int, start_pos: int) -> int:
+    return int(load_library().indexer_workspace_size(ctypes.byref(dims), B, S, start_pos))
+
+
+def indexer_workspace_init(ws: torch.Tensor, stream=None):
+    _check(load_library().indexer_workspace_init(_ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+                                                 _stream(stream)))
+
+
+def indexer_status(ws: torch.Tensor, stream=None):
+    """Synchronises the stream; raises IndexerError if a device wait ran out."""
+    _check(load_library().indexer_status(_ptr(ws, None, "ws"), _stream(stream)))
+
+
+def indexer_forward(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor, start_pos: int, rope_cs: torch.Tensor,
+                    k_cache: torch.Tensor, topk_out: torch.Tensor, ws: torch.Tensor,
+                    cand_in: Optional[torch.Tensor] = None, cand_out: Optional[torch.Tensor] = None,
+                    scores_out: Optional[torch.Tensor] = None, stream=None):
+    """The whole path after the key publish; see include/indexer.h."""
+    B, S = q.shape[:2]
+    _check(load_library().indexer_forward(
+        ctypes.byref(dims), _ptr(q, torch.bfloat16, "q"), _ptr(w, torch.bfloat16, "w"), B, S, start_pos,
+        _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(k_cache, torch.uint8, "k_cache"),
+        k_cache.shape[1], _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
+        _ptr(topk_out, torch.int32, "topk_out"), _ptr(scores_out, torch.float32, "scores_out"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))

@@ -1,0 +1,208 @@
+// Device helpers shared by the indexer kernels (sm_103a): exact rounding helpers
+// for the bf16 steps of the key/query path, and thin inline-PTX wrappers for
+// mbarriers, bulk (TMA) copies and the tcgen05 tensor-core / tensor-memory ops.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace indexer {
+
+constexpr int kHeadDim = 128;           // index_head_dim supported by the kernels
+constexpr int kRowBytes = 68;           // 64 packed e2m1 bytes + 4 UE8M0 scale bytes
+constexpr int kCodeBytes = 64;
+constexpr int kFp4Block = 32;
+
+// Status bits OR-ed into the workspace status word by kernels whose bounded waits ran out.
+constexpr uint32_t kStatusLoadTimeout = 1u;
+constexpr uint32_t kStatusMmaTimeout = 2u;
+// One second: a bounded wait gives up after this long and reports through the status word.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// ----------------------------------------------------------------------------- bf16 / rounding
+__device__ __forceinline__ float bf16_to_f32(uint32_t bits) { return __uint_as_float(bits << 16); }
+
+// Round an f32 to bf16 to nearest, ties to even (finite inputs).
+__device__ __forceinline__ uint32_t f32_to_bf16_rne(float f) {
+  const uint32_t b = __float_as_uint(f);
+  return (b + 0x7FFFu + ((b >> 16) & 1u)) >> 16;
+}
+
+// Round an f64 to bf16 once (no intermediate f32), to nearest with ties to even.
+// bf16 keeps 7 explicit mantissa bits; below 2^-126 the spacing is fixed at 2^-133.
+__device__ __forceinline__ uint32_t f64_to_bf16_rne(double x) {
+  const unsigned long long b = (unsigned long long)__double_as_longlong(x);
+  const uint32_t sign = (uint32_t)(b >> 48) & 0x8000u;
+  const unsigned long long a = b & 0x7FFFFFFFFFFFFFFFull;
+  if (a == 0) return sign;
+  const int e = (int)(a >> 52) - 1023;
+  if (e >= -126) {
+    const unsigned long long m = a & ((1ull << 52) - 1);
+    uint32_t keep = (uint32_t)(m >> 45);
+    const unsigned long long rest = m & ((1ull << 45) - 1);
+    const unsigned long long half = 1ull << 44;
+    int ee = e;
+    if (rest > half || (rest == half && (keep & 1u))) {
+      if (++keep == 128u) { keep = 0; ++ee; }
+    }
+    if (ee > 127) return sign | 0x7F80u;
+    return sign | ((uint32_t)(ee + 127) << 7) | keep;
+  }
+  // bf16 subnormal range: value = n * 2^-133 with n in [0, 128]; n = 128 is the
+  // smallest normal, whose bit pattern is exactly 128 as well.
+  const double scaled = __longlong_as_double((long long)a) * 0x1p133;
+  return sign | (uint32_t)__double2int_rn(scaled);
+}
+
+// Round (hi + lo) to bf16 correctly, where hi = fl32(hi + lo) (|lo| <= ulp(hi) / 2).
+// Only when hi sits exactly on a bf16 midpoint can lo change the result.
+__device__ __forceinline__ uint32_t f32pair_to_bf16_rne(float hi, float lo) {
+  const uint32_t hb = __float_as_uint(hi);
+  if ((hb & 0xFFFFu) == 0x8000u && lo != 0.0f) {
+    const bool away = (lo > 0.0f) == (hi > 0.0f);
+    return (hb >> 16) + (away ? 1u : 0u);
+  }
+  return f32_to_bf16_rne(hi);
+}
+
+// Error-free sum: s + e == a + b exactly (Knuth's TwoSum), no contraction.
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  const float z = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z));
+}
+
+// ----------------------------------------------------------------------------- e2m1 / e8m0
+// e8m0 exponent of a 32-block from its amax bit pattern (non-negative bf16): the
+// smallest e with 6 * 2^e >= max(amax, 6 * 2^-126). Writing amax = (1 + m/128) * 2^E,
+// 6 * 2^(E-2) = 1.5 * 2^E covers it iff m <= 64, else 6 * 2^(E-1) = 3 * 2^E does.
+__device__ __forceinline__ int e8m0_exponent(uint32_t amax_bits) {
+  const uint32_t a = amax_bits < 0x01C0u ? 0x01C0u : amax_bits;   // 0x01C0 = bf16 6 * 2^-126
+  const int E = (int)(a >> 7) - 127;
+  return E - ((a & 0x7Fu) <= 64u ? 2 : 1);
+}
+
+// 2^-e as an f32 (e in [-126, 126], so the result is a normal number).
+__device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
+
+// Two e2m1 codes in one byte: x0 -> low nibble, x1 -> high nibble; round to nearest
+// even on the e2m1 grid (hardware conversion); the sign bits are forced to the signs
+// of the inputs so that negative values rounding to zero keep their sign.
+__device__ __forceinline__ uint32_t e2m1x2(float x0, float x1) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }" : "=r"(r) : "f"(x1), "f"(x0));
+  r |= (__float_as_uint(x0) >> 28) & 0x8u;
+  r |= (__float_as_uint(x1) >> 24) & 0x80u;
+  return r;
+}
+
+// ----------------------------------------------------------------------------- PTX: mbarrier / bulk copy
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0u;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for the phase with the given parity to complete; false after kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
+  return true;
+}
+// Bulk (non-tensor TMA) copy global -> shared; dst, src and bytes multiples of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// ----------------------------------------------------------------------------- PTX: tcgen05
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T with block-32 UE8M0 scales from tensor memory,
+// both operands e2m1 packed two per byte (kind::mxf4, K = 64 per instruction).
+__device__ __forceinline__ void mma_mxf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p; }"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf4: A and B e2m1 (format 1, bits 7-9 / 10-12),
+// both K-major, N >> 3 in bits 17-22, UE8M0 scales (bit 23), M >> 7 in bits 27-28,
+// scale-factor data ids 0 (bytes 0 and 1 of each scale column), K = 64.
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N) {
+  return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 7) << 27);
+}
+
+// Shared-memory matrix descriptor, no swizzle, K-major: core matrices of 8 rows x 16 bytes
+// (128 contiguous bytes); lbo = byte step between core matrices along K, sbo = byte step
+// between 8-row groups along M/N; bits 46-48 hold the fixed value 0b001.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
+         (1ull << 46);
+}
+
+__device__ __forceinline__ void tmem_st_x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void tmem_st_x8(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3,
+                                           uint32_t v4, uint32_t v5, uint32_t v6, uint32_t v7) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+               ::"r"(taddr), "r"(v0), "r"(v1), "r"(v2), "r"(v3), "r"(v4), "r"(v5), "r"(v6), "r"(v7)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Load 32 consecutive columns of this warp's 32 lanes and wait for them (one asm
+// statement, so no use of the registers can be scheduled before the wait).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+}  // namespace indexer

@@ -1,0 +1,444 @@
+// C ABI of the indexer (declared in include/indexer.h): host-side validation, the
+// workspace layout and kernel launches. Every entry point validates all arguments
+// before it launches anything; the library holds no device memory of its own.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "../../include/indexer.h"
+#include "launch.h"
+
+using namespace indexer;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+int ok() {
+  g_last_error.clear();
+  return INDEXER_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(INDEXER_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t x, size_t m) { return (x + m - 1) / m * m; }
+
+// The kernels are built for sm_103a only.
+int check_arch() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int major = 0, minor = 0;
+  e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  if (major != 10 || minor != 3)
+    return fail(INDEXER_ERR_ARCH, "device %d is sm_%d%d; the indexer kernels are built for sm_103a", dev, major, minor);
+  return INDEXER_OK;
+}
+
+int check_dims(const IndexerDims* d) {
+  if (!d) return fail(INDEXER_ERR_NULL, "dims is NULL");
+  if (d->head_dim != 128) return fail(INDEXER_ERR_DIMS, "head_dim must be 128 (got %d)", d->head_dim);
+  const int h = d->n_heads;
+  if (h != 8 && h != 16 && h != 32 && h != 64 && h != 128)
+    return fail(INDEXER_ERR_DIMS, "n_heads must be 8, 16, 32, 64 or 128 (got %d)", h);
+  if (d->rope_dim < 2 || d->rope_dim > 128 || (d->rope_dim & 1))
+    return fail(INDEXER_ERR_DIMS, "rope_dim must be even in [2, 128] (got %d)", d->rope_dim);
+  if (d->ratio < 1) return fail(INDEXER_ERR_DIMS, "ratio must be >= 1 (got %d)", d->ratio);
+  if (d->index_topk < 1) return fail(INDEXER_ERR_DIMS, "index_topk must be >= 1 (got %d)", d->index_topk);
+  if (!(d->norm_eps >= 0.0f) || !std::isfinite(d->norm_eps))
+    return fail(INDEXER_ERR_DIMS, "norm_eps must be finite and >= 0");
+  return INDEXER_OK;
+}
+
+int check_cand_dims(const IndexerDims* d, int T) {
+  if (d->cand_topk_blocks < 1 || d->cand_block_size < 1)
+    return fail(INDEXER_ERR_DIMS, "candidate filter needs cand_topk_blocks >= 1 and cand_block_size >= 1");
+  const long long nblk = ((long long)T + d->cand_block_size - 1) / d->cand_block_size;
+  if (nblk > kCandMaxBlocks)
+    return fail(INDEXER_ERR_DIMS, "%lld candidate blocks exceed the limit of %d", nblk, kCandMaxBlocks);
+  return INDEXER_OK;
+}
+
+int check_rows(int B, int S, int start_pos) {
+  if (B < 1 || S < 1) return fail(INDEXER_ERR_DIMS, "B and S must be >= 1 (got %d, %d)", B, S);
+  if (start_pos < 0) return fail(INDEXER_ERR_RANGE, "start_pos must be >= 0 (got %d)", start_pos);
+  if ((long long)start_pos + S > (1LL << 30)) return fail(INDEXER_ERR_RANGE, "start_pos + S too large");
+  return INDEXER_OK;
+}
+
+struct WsLayout {
+  size_t q_rows, w_prime, scores, total;
+};
+
+WsLayout ws_layout(const IndexerDims* d, int B, int S, int start_pos) {
+  WsLayout l;
+  const size_t nvec = (size_t)B * S * d->n_heads;
+  const size_t T = (size_t)((start_pos + S) / d->ratio);
+  l.q_rows = INDEXER_STATUS_BYTES;
+  l.w_prime = l.q_rows + round_up(nvec * INDEXER_KEY_ROW_BYTES, 256);
+  l.scores = l.w_prime + round_up(nvec * sizeof(float), 256);
+  l.total = l.scores + round_up((size_t)B * S * T * sizeof(float), 256);
+  return l;
+}
+
+#define RETURN_IF(x)        \
+  do {                      \
+    int _rc = (x);          \
+    if (_rc != INDEXER_OK) return _rc; \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* indexer_last_error(void) { return g_last_error.c_str(); }
+
+int indexer_abi_version(void) { return 100; }
+
+// ---------------------------------------------------------------------------- RoPE table
+int indexer_rope_table(const IndexerYarn* y, int rope_dim, int max_pos, float* table, indexer_stream_t stream) {
+  if (!y) return fail(INDEXER_ERR_NULL, "yarn is NULL");
+  if (!table) return fail(INDEXER_ERR_NULL, "table is NULL");
+  if (!aligned(table, 8)) return fail(INDEXER_ERR_ALIGN, "table must be 8-byte aligned");
+  if (rope_dim < 2 || rope_dim > 128 || (rope_dim & 1))
+    return fail(INDEXER_ERR_DIMS, "rope_dim must be even in [2, 128] (got %d)", rope_dim);
+  if (max_pos < 1 || max_pos > (1 << 24)) return fail(INDEXER_ERR_RANGE, "max_pos must be in [1, 2^24]");
+  if (!(y->theta > 1.0) || !(y->factor > 0.0)) return fail(INDEXER_ERR_DIMS, "theta must be > 1 and factor > 0");
+  if (y->original_seq_len > 0 && (!(y->beta_fast > 0.0) || !(y->beta_slow > 0.0)))
+    return fail(INDEXER_ERR_DIMS, "beta_fast and beta_slow must be > 0");
+  RETURN_IF(check_arch());
+  // f'_i on the host in f64, rounded to f32 (NTK-by-parts YaRN, "Module compress" page,
+  // yarn_freqs_cis): ramp between the correction dims of beta_fast and beta_slow.
+  const int half = rope_dim / 2;
+  RopeFreqs f;
+  double low = 0.0, high = 0.0;
+  const bool yarn = y->original_seq_len > 0;
+  if (yarn) {
+    const double pi = 3.14159265358979323846;
+    auto corr = [&](double rot) {
+      return rope_dim * std::log((double)y->original_seq_len / (rot * 2.0 * pi)) / (2.0 * std::log(y->theta));
+    };
+    low = std::floor(corr(y->beta_fast));
+    high = std::ceil(corr(y->beta_slow));
+    if (low < 0.0) low = 0.0;
+    if (high > rope_dim - 1) high = rope_dim - 1;
+  }
+  const double span = high != low ? high - low : 0.001;
+  for (int i = 0; i < half; ++i) {
+    double fi = std::pow(y->theta, -2.0 * i / rope_dim);
+    if (yarn) {
+      double ramp = (i - low) / span;
+      ramp = ramp < 0.0 ? 0.0 : (ramp > 1.0 ? 1.0 : ramp);
+      fi = fi / y->factor * ramp + fi * (1.0 - ramp);
+    }
+    f.f[i] = (float)fi;
+  }
+  const cudaError_t e = launch_rope_table(f, half, max_pos, table, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
+  return ok();
+}
+
+// ---------------------------------------------------------------------------- key publish
+int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B, int G, int Din,
+                      const indexer_bf16* wk, const indexer_bf16* k_norm_w, const float* rope_cs, int max_pos,
+                      int start_pos, uint8_t* k_cache, int T_cap, indexer_stream_t stream) {
+  RETURN_IF(check_dims(dims));
+  if (!latent || !wk || !k_norm_w || !rope_cs || !k_cache) return fail(INDEXER_ERR_NULL, "a required pointer is NULL");
+  if (B < 1 || G < 1) return fail(INDEXER_ERR_DIMS, "B and G must be >= 1 (got %d, %d)", B, G);
+  if (Din < 8 || Din > 1024 || (Din % 8)) return fail(INDEXER_ERR_DIMS, "Din must be a multiple of 8 in [8, 1024]");
+  if (!aligned(latent, 16) || !aligned(wk, 16)) return fail(INDEXER_ERR_ALIGN, "latent and wk must be 16-byte aligned");
+  if (!aligned(rope_cs, 8)) return fail(INDEXER_ERR_ALIGN, "rope_cs must be 8-byte aligned");
+  if (T_cap < 1) return fail(INDEXER_ERR_DIMS, "T_cap must be >= 1");
+  if (start_pos < 0) return fail(INDEXER_ERR_RANGE, "start_pos must be >= 0");
+  const int r = dims->ratio;
+  PublishArgs a;
+  if (start_pos == 0) {
+    a.slot0 = 0;
+    a.pos0 = 0;
+    a.pos_step = r;
+  } else {
+    if (G != 1) return fail(INDEXER_ERR_RANGE, "decode publishes one key (G == 1), got G = %d", G);
+    if ((start_pos + 1) % r != 0)
+      return fail(INDEXER_ERR_RANGE, "start_pos %d does not complete a group of %d", start_pos, r);
+    a.slot0 = start_pos / r;
+    a.pos0 = start_pos + 1 - r;
+    a.pos_step = r;
+  }
+  if ((long long)a.slot0 + G > T_cap) return fail(INDEXER_ERR_RANGE, "slots up to %lld exceed T_cap %d", (long long)a.slot0 + G, T_cap);
+  if ((long long)a.pos0 + (long long)(G - 1) * a.pos_step >= max_pos)
+    return fail(INDEXER_ERR_RANGE, "RoPE position beyond the table (max_pos %d)", max_pos);
+  RETURN_IF(check_arch());
+  a.latent = latent;
+  a.wk = wk;
+  a.knorm = k_norm_w;
+  a.rope_cs = rope_cs;
+  a.k_cache = k_cache;
+  a.B = B;
+  a.G = G;
+  a.Din = Din;
+  a.rope_dim = dims->rope_dim;
+  a.T_cap = T_cap;
+  a.eps = dims->norm_eps;
+  const cudaError_t e = launch_publish(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "publish launch");
+  return ok();
+}
+
+// ---------------------------------------------------------------------------- query prep
+static int prep_q_checked(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
+                          int start_pos, const float* rope_cs, uint8_t* q_rows, float* w_prime,
+                          cudaStream_t stream) {
+  PrepArgs a;
+  a.q = q;
+  a.w = w;
+  a.rope_cs = rope_cs;
+  a.q_rows = q_rows;
+  a.w_prime = w_prime;
+  a.n_vec = (long long)B * S * dims->n_heads;
+  a.S = S;
+  a.H = dims->n_heads;
+  a.rope_dim = dims->rope_dim;
+  a.start_pos = start_pos;
+  a.w_scale = (float)(1.0 / std::sqrt((double)dims->head_dim) / std::sqrt((double)dims->n_heads));
+  const cudaError_t e = launch_prep_q(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "prep_q launch");
+  return INDEXER_OK;
+}
+
+static int check_prep_args(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
+                           int start_pos, const float* rope_cs, int max_pos) {
+  RETURN_IF(check_dims(dims));
+  RETURN_IF(check_rows(B, S, start_pos));
+  if (!q || !w || !rope_cs) return fail(INDEXER_ERR_NULL, "q, w and rope_cs must not be NULL");
+  if (!aligned(q, 16)) return fail(INDEXER_ERR_ALIGN, "q must be 16-byte aligned");
+  if (!aligned(rope_cs, 8)) return fail(INDEXER_ERR_ALIGN, "rope_cs must be 8-byte aligned");
+  if ((long long)start_pos + S > max_pos)
+    return fail(INDEXER_ERR_RANGE, "query positions up to %lld exceed the RoPE table (max_pos %d)",
+                (long long)start_pos + S - 1, max_pos);
+  return INDEXER_OK;
+}
+
+int indexer_prep_q(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S, int start_pos,
+                   const float* rope_cs, int max_pos, uint8_t* q_rows, float* w_prime, indexer_stream_t stream) {
+  RETURN_IF(check_prep_args(dims, q, w, B, S, start_pos, rope_cs, max_pos));
+  if (!q_rows || !w_prime) return fail(INDEXER_ERR_NULL, "q_rows and w_prime must not be NULL");
+  if (!aligned(q_rows, 4) || !aligned(w_prime, 4)) return fail(INDEXER_ERR_ALIGN, "q_rows and w_prime must be 4-byte aligned");
+  RETURN_IF(check_arch());
+  RETURN_IF(prep_q_checked(dims, q, w, B, S, start_pos, rope_cs, q_rows, w_prime, (cudaStream_t)stream));
+  return ok();
+}
+
+// ---------------------------------------------------------------------------- scores
+static int check_cache(const uint8_t* k_cache, int T_cap, int T) {
+  if (!k_cache) return fail(INDEXER_ERR_NULL, "k_cache is NULL");
+  if (!aligned(k_cache, 16)) return fail(INDEXER_ERR_ALIGN, "k_cache must be 16-byte aligned");
+  if (T_cap < 4 || (T_cap % 4)) return fail(INDEXER_ERR_ALIGN, "T_cap must be a positive multiple of 4 (got %d)", T_cap);
+  if (T > T_cap) return fail(INDEXER_ERR_RANGE, "T = %d keys exceed T_cap = %d", T, T_cap);
+  return INDEXER_OK;
+}
+
+int indexer_scores(const IndexerDims* dims, const uint8_t* q_rows, const float* w_prime, int B, int S, int start_pos,
+                   const uint8_t* k_cache, int T_cap, const int32_t* cand_blocks, float* scores, void* ws,
+                   size_t ws_bytes, indexer_stream_t stream) {
+  RETURN_IF(check_dims(dims));
+  RETURN_IF(check_rows(B, S, start_pos));
+  const int T = (start_pos + S) / dims->ratio;
+  RETURN_IF(check_cache(k_cache, T_cap, T));
+  if (!q_rows || !w_prime || !scores || !ws) return fail(INDEXER_ERR_NULL, "a required pointer is NULL");
+  if (!aligned(q_rows, 16) || !aligned(w_prime, 4) || !aligned(scores, 4) || !aligned(ws, 16))
+    return fail(INDEXER_ERR_ALIGN, "q_rows and ws must be 16-byte aligned, w_prime and scores 4-byte aligned");
+  if (ws_bytes < INDEXER_STATUS_BYTES) return fail(INDEXER_ERR_WORKSPACE, "workspace smaller than %d bytes", INDEXER_STATUS_BYTES);
+  if (cand_blocks) RETURN_IF(check_cand_dims(dims, T));
+  RETURN_IF(check_arch());
+  ScoreArgs a;
+  a.q_rows = q_rows;
+  a.w_prime = w_prime;
+  a.k_cache = k_cache;
+  a.scores = scores;
+  a.cand = cand_blocks;
+  a.status = static_cast<uint32_t*>(ws);
+  a.B = B;
+  a.S = S;
+  a.H = dims->n_heads;
+  a.T = T;
+  a.T_cap = T_cap;
+  a.start_pos = start_pos;
+  a.ratio = dims->ratio;
+  a.cbk = dims->cand_topk_blocks;
+  a.cbs = dims->cand_block_size > 0 ? dims->cand_block_size : 1;
+  a.fill_masked = 1;
+  const cudaError_t e = launch_scores(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "scores launch");
+  return ok();
+}
+
+// ---------------------------------------------------------------------------- selection
+int indexer_select_candidate_blocks(const IndexerDims* dims, const float* scores, int B, int S, int start_pos, int T,
+                                    int32_t* blocks_out, indexer_stream_t stream) {
+  RETURN_IF(check_dims(dims));
+  RETURN_IF(check_rows(B, S, start_pos));
+  if (!scores || !blocks_out) return fail(INDEXER_ERR_NULL, "scores and blocks_out must not be NULL");
+  if (T < 0 || T != (start_pos + S) / dims->ratio)
+    return fail(INDEXER_ERR_RANGE, "T must equal (start_pos + S) / ratio");
+  RETURN_IF(check_cand_dims(dims, T));
+  RETURN_IF(check_arch());
+  CandArgs a;
+  a.scores = scores;
+  a.blocks = blocks_out;
+  a.rows = B * S;
+  a.S = S;
+  a.T = T;
+  a.start_pos = start_pos;
+  a.ratio = dims->ratio;
+  a.cbk = dims->cand_topk_blocks;
+  a.cbs = dims->cand_block_size;
+  const cudaError_t e = launch_candidates(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "candidate launch");
+  return ok();
+}
+
+static int topk_checked(const IndexerDims* dims, const float* scores, int B, int S, int start_pos, int T,
+                        const int32_t* cand, int32_t* out, cudaStream_t stream) {
+  TopkArgs a;
+  a.scores = scores;
+  a.out = out;
+  a.cand = cand;
+  a.rows = B * S;
+  a.S = S;
+  a.T = T;
+  a.start_pos = start_pos;
+  a.ratio = dims->ratio;
+  a.topk = dims->index_topk;
+  a.offset = dims->offset;
+  a.cbk = dims->cand_topk_blocks;
+  a.cbs = dims->cand_block_size > 0 ? dims->cand_block_size : 1;
+  const cudaError_t e = launch_topk(a, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "topk launch");
+  return INDEXER_OK;
+}
+
+int indexer_topk(const IndexerDims* dims, const float* scores, int B, int S, int start_pos, int T, int32_t* out,
+                 indexer_stream_t stream) {
+  RETURN_IF(check_dims(dims));
+  RETURN_IF(check_rows(B, S, start_pos));
+  if (!scores || !out) return fail(INDEXER_ERR_NULL, "scores and out must not be NULL");
+  if (T < 0 || T != (start_pos + S) / dims->ratio)
+    return fail(INDEXER_ERR_RANGE, "T must equal (start_pos + S) / ratio");
+  if (T > kTopkMaxT) return fail(INDEXER_ERR_DIMS, "T = %d exceeds the top-k limit of %d", T, kTopkMaxT);
+  RETURN_IF(check_arch());
+  RETURN_IF(topk_checked(dims, scores, B, S, start_pos, T, nullptr, out, (cudaStream_t)stream));
+  return ok();
+}
+
+// ---------------------------------------------------------------------------- forward
+size_t indexer_workspace_size(const IndexerDims* dims, int B, int S, int start_pos) {
+  if (check_dims(dims) != INDEXER_OK || check_rows(B, S, start_pos) != INDEXER_OK) return 0;
+  return ws_layout(dims, B, S, start_pos).total;
+}
+
+int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
+                    int start_pos, const float* rope_cs, int max_pos, const uint8_t* k_cache, int T_cap,
+                    const int32_t* cand_in, int32_t* cand_out, int32_t* topk_out, float* scores_out, void* ws,
+                    size_t ws_bytes, indexer_stream_t stream) {
+  RETURN_IF(check_prep_args(dims, q, w, B, S, start_pos, rope_cs, max_pos));
+  const int T = (start_pos + S) / dims->ratio;
+  RETURN_IF(check_cache(k_cache, T_cap, T));
+  if (!topk_out || !ws) return fail(INDEXER_ERR_NULL, "topk_out and ws must not be NULL");
+  if (!aligned(ws, 256)) return fail(INDEXER_ERR_ALIGN, "ws must be 256-byte aligned");
+  if (scores_out && !aligned(scores_out, 4)) return fail(INDEXER_ERR_ALIGN, "scores_out must be 4-byte aligned");
+  if (T > kTopkMaxT) return fail(INDEXER_ERR_DIMS, "T = %d exceeds the top-k limit of %d", T, kTopkMaxT);
+  if (cand_in || cand_out) RETURN_IF(check_cand_dims(dims, T));
+  const WsLayout l = ws_layout(dims, B, S, start_pos);
+  if (ws_bytes < l.total) return fail(INDEXER_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, l.total);
+  RETURN_IF(check_arch());
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  uint8_t* q_rows = base + l.q_rows;
+  float* w_prime = reinterpret_cast<float*>(base + l.w_prime);
+  float* scores = scores_out ? scores_out : reinterpret_cast<float*>(base + l.scores);
+  RETURN_IF(prep_q_checked(dims, q, w, B, S, start_pos, rope_cs, q_rows, w_prime, st));
+  if (T > 0) {
+    ScoreArgs a;
+    a.q_rows = q_rows;
+    a.w_prime = w_prime;
+    a.k_cache = k_cache;
+    a.scores = scores;
+    a.cand = nullptr;   // the candidate filter is applied by the top-k (cand_out sees unfiltered scores)
+    a.status = reinterpret_cast<uint32_t*>(base);
+    a.B = B;
+    a.S = S;
+    a.H = dims->n_heads;
+    a.T = T;
+    a.T_cap = T_cap;
+    a.start_pos = start_pos;
+    a.ratio = dims->ratio;
+    a.cbk = dims->cand_topk_blocks;
+    a.cbs = dims->cand_block_size > 0 ? dims->cand_block_size : 1;
+    a.fill_masked = scores_out ? 1 : 0;
+    const cudaError_t e = launch_scores(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "scores launch");
+    if (cand_out) {
+      CandArgs c;
+      c.scores = scores;
+      c.blocks = cand_out;
+      c.rows = B * S;
+      c.S = S;
+      c.T = T;
+      c.start_pos = start_pos;
+      c.ratio = dims->ratio;
+      c.cbk = dims->cand_topk_blocks;
+      c.cbs = dims->cand_block_size;
+      const cudaError_t e2 = launch_candidates(c, st);
+      if (e2 != cudaSuccess) return cuda_fail(e2, "candidate launch");
+    }
+  }
+  RETURN_IF(topk_checked(dims, scores, B, S, start_pos, T, cand_in, topk_out, st));
+  return ok();
+}
+
+int indexer_workspace_init(void* ws, size_t ws_bytes, indexer_stream_t stream) {
+  if (!ws) return fail(INDEXER_ERR_NULL, "ws is NULL");
+  if (ws_bytes < INDEXER_STATUS_BYTES) return fail(INDEXER_ERR_WORKSPACE, "workspace smaller than %d bytes", INDEXER_STATUS_BYTES);
+  const cudaError_t e = cudaMemsetAsync(ws, 0, INDEXER_STATUS_BYTES, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace init");
+  return ok();
+}
+
+int indexer_status(void* ws, indexer_stream_t stream) {
+  if (!ws) return fail(INDEXER_ERR_NULL, "ws is NULL");
+  cudaStream_t st = (cudaStream_t)stream;
+  uint32_t word = 0;
+  cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof(word), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (word != 0u) {
+    e = cudaMemsetAsync(ws, 0, sizeof(word), st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    return fail(INDEXER_ERR_DEVICE_TIMEOUT, "device wait ran out (status 0x%x)", word);
+  }
+  return ok();
+}
+
+}  // extern "C"

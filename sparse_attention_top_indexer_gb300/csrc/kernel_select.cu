@@ -1,0 +1,229 @@
+// Per-row selection kernels: the position-ordered top-k and the level-one candidate
+// blocks. Both reduce to one CTA-wide primitive: among n order-preserving uint32 keys
+// (0 = not selectable) keep the k largest, ties to the lower index, and emit their
+// indices in ascending order.
+//
+// Selection is a most-significant-digit radix select (four 8-bit digits, shared-memory
+// histograms) that pins the k-th largest key K*, followed by an ordered compaction:
+// every key > K* and the first `need` keys equal to K* (in index order) are written at
+// their prefix-sum slot, so the output comes out sorted by position without a sort.
+#include <cuda_runtime.h>
+
+#include "device_common.cuh"
+#include "launch.h"
+
+namespace indexer {
+
+namespace {
+
+constexpr int kSelThreads = 1024;
+constexpr int kSelWarps = kSelThreads / 32;
+
+// Larger float -> larger key; every finite value maps to a key >= 0x00800000 > 0.
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+struct SelShared {
+  uint32_t hist[256];
+  uint32_t warp_tot[kSelWarps];
+  uint32_t bcast[4];
+};
+
+// Exclusive prefix sum over the CTA (1024 threads); returns this thread's exclusive
+// prefix and writes the total to *total.
+__device__ __forceinline__ uint32_t cta_exclusive_scan(uint32_t v, uint32_t* total, SelShared& sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) sh.warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t t = sh.warp_tot[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, t, off);
+      if (lane >= off) t += y;
+    }
+    sh.warp_tot[lane] = t;   // inclusive
+  }
+  __syncthreads();
+  const uint32_t before = (warp > 0 ? sh.warp_tot[warp - 1] : 0u) + x - v;
+  *total = sh.warp_tot[kSelWarps - 1];
+  __syncthreads();
+  return before;
+}
+
+// keys[0..n) in shared memory. Writes out[0..width): selected indices + offset in
+// ascending order, then -1. k >= 1.
+__device__ void cta_select(const uint32_t* keys, int n, int k, int32_t* out, int width, int offset,
+                           SelShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int per = (n + kSelThreads - 1) / kSelThreads;
+  const int lo = min(n, tid * per), hi = min(n, lo + per);
+
+  uint32_t nvalid_local = 0;
+  for (int i = lo; i < hi; ++i) nvalid_local += keys[i] != 0u;
+  uint32_t nvalid;
+  cta_exclusive_scan(nvalid_local, &nvalid, sh);
+
+  uint32_t kstar = 0u;        // select keys > kstar, plus `need` keys == kstar
+  uint32_t need = 0u;
+  if ((int)nvalid > k) {
+    uint32_t prefix = 0u, mask = 0u;
+    need = (uint32_t)k;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      if (tid < 256) sh.hist[tid] = 0u;
+      __syncthreads();
+      for (int i = lo; i < hi; ++i) {
+        const uint32_t key = keys[i];
+        if (key != 0u && (key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // lane L owns bins 8L .. 8L+7; find the bin holding the need-th largest key
+        uint32_t c[8], own = 0u;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          c[q] = sh.hist[lane * 8 + q];
+          own += c[q];
+        }
+        uint32_t incl = own;   // sum over lanes >= lane
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const uint32_t y = __shfl_down_sync(0xffffffffu, incl, off);
+          if (lane + off < 32) incl += y;
+        }
+        const uint32_t above = incl - own;
+        if (above < need && need <= incl) {
+          uint32_t acc = above;
+          for (int q = 7; q >= 0; --q) {
+            if (acc + c[q] >= need) {
+              sh.bcast[0] = (uint32_t)(lane * 8 + q);
+              sh.bcast[1] = acc;
+              break;
+            }
+            acc += c[q];
+          }
+        }
+      }
+      __syncthreads();
+      const uint32_t bin = sh.bcast[0];
+      need -= sh.bcast[1];
+      prefix |= bin << shift;
+      mask |= 255u << shift;
+      __syncthreads();
+    }
+    kstar = prefix;
+  }
+
+  // ordered compaction
+  uint32_t eq_local = 0u, gt_local = 0u;
+  for (int i = lo; i < hi; ++i) {
+    const uint32_t key = keys[i];
+    gt_local += key > kstar;
+    eq_local += (key == kstar && kstar != 0u);
+  }
+  uint32_t eq_total;
+  const uint32_t eq_before = cta_exclusive_scan(eq_local, &eq_total, sh);
+  const uint32_t eq_take = need > eq_before ? min(need - eq_before, eq_local) : 0u;
+  uint32_t sel_total;
+  uint32_t slot = cta_exclusive_scan(gt_local + eq_take, &sel_total, sh);
+  uint32_t eq_seen = 0u;
+  for (int i = lo; i < hi; ++i) {
+    const uint32_t key = keys[i];
+    bool take = key > kstar;
+    if (key == kstar && kstar != 0u) {
+      take = eq_seen < eq_take;
+      ++eq_seen;
+    }
+    if (take) out[slot++] = i + offset;
+  }
+  for (int i = (int)sel_total + tid; i < width; i += kSelThreads) out[i] = -1;
+}
+
+// One CTA per query row: keys of the finite scores at t < vis (and inside the kept
+// candidate blocks, if any), then cta_select. Rows with no candidate filter and
+// vis <= k_eff take the short-context fill [0 .. vis) directly.
+__global__ void __launch_bounds__(kSelThreads, 1) topk_kernel(const TopkArgs a) {
+  extern __shared__ __align__(16) uint32_t keys[];
+  __shared__ SelShared sh;
+  __shared__ uint32_t kept[kCandMaxBlocks / 32];
+  const int tid = threadIdx.x;
+  const int row = blockIdx.x;
+  const int s = row % a.S;
+  const int vis = min(a.T, (a.start_pos + s + 1) / a.ratio);
+  const int k_eff = min(a.topk, a.T);
+  int32_t* out = a.out + (size_t)row * a.topk;
+  if (a.cand == nullptr && vis <= k_eff) {
+    for (int i = tid; i < a.topk; i += kSelThreads) out[i] = i < vis ? i + a.offset : -1;
+    return;
+  }
+  const int nblk_words = a.cand ? ((a.T + a.cbs - 1) / a.cbs + 31) / 32 : 0;
+  if (a.cand) {
+    for (int i = tid; i < nblk_words; i += kSelThreads) kept[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < a.cbk; i += kSelThreads) {
+      const int blk = a.cand[(size_t)row * a.cbk + i];
+      if (blk >= 0 && blk < nblk_words * 32) atomicOr(&kept[blk >> 5], 1u << (blk & 31));
+    }
+    __syncthreads();
+  }
+  const float* src = a.scores + (size_t)row * a.T;
+  for (int t = tid; t < vis; t += kSelThreads) {
+    const float f = src[t];
+    bool ok = isfinite(f);
+    if (a.cand) {
+      const int blk = t / a.cbs;
+      ok = ok && ((kept[blk >> 5] >> (blk & 31)) & 1u);
+    }
+    keys[t] = ok ? order_key(f) : 0u;
+  }
+  __syncthreads();
+  cta_select(keys, vis, k_eff, out, a.topk, a.offset, sh);
+}
+
+// One CTA per query row: block score = max finite score over the block's positions
+// t < vis; ineligible blocks keep key 0; then cta_select over the blocks.
+__global__ void __launch_bounds__(kSelThreads, 1) cand_kernel(const CandArgs a) {
+  __shared__ uint32_t bkeys[kCandMaxBlocks];
+  __shared__ SelShared sh;
+  const int tid = threadIdx.x;
+  const int row = blockIdx.x;
+  const int s = row % a.S;
+  const int vis = min(a.T, (a.start_pos + s + 1) / a.ratio);
+  const int nblk = (a.T + a.cbs - 1) / a.cbs;
+  for (int i = tid; i < nblk; i += kSelThreads) bkeys[i] = 0u;
+  __syncthreads();
+  const float* src = a.scores + (size_t)row * a.T;
+  for (int t = tid; t < vis; t += kSelThreads) {
+    const float f = src[t];
+    if (isfinite(f)) atomicMax(&bkeys[t / a.cbs], order_key(f));
+  }
+  __syncthreads();
+  cta_select(bkeys, nblk, a.cbk, a.blocks + (size_t)row * a.cbk, a.cbk, 0, sh);
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
+  if (a.rows <= 0) return cudaSuccess;
+  const size_t smem = (size_t)(a.T > 0 ? a.T : 1) * sizeof(uint32_t);
+  cudaError_t err = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (err != cudaSuccess) return err;
+  topk_kernel<<<a.rows, kSelThreads, smem, stream>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_candidates(const CandArgs& a, cudaStream_t stream) {
+  if (a.rows <= 0) return cudaSuccess;
+  cand_kernel<<<a.rows, kSelThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace indexer

@@ -1,0 +1,98 @@
+"""Host-side checks of the C ABI: the library loads, exports every function that
+include/indexer.h declares, and rejects bad arguments before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def X():
+    import sparse_attention_top_indexer_gb300 as X
+    if not os.path.exists(X.LIB_PATH):
+        from sparse_attention_top_indexer_gb300.build import build
+        build()
+    X.load_library()
+    return X
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(indexer_\w+)\s*\(", text, re.M))
+    return names
+
+
+def test_every_declared_symbol_is_exported(X):
+    names = _declared()
+    assert {"indexer_publish_k", "indexer_scores", "indexer_topk", "indexer_forward"} <= names
+    lib = X.load_library()
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared but not exported"
+
+
+def test_struct_layouts_match_header(X):
+    assert ctypes.sizeof(X.IndexerDims) == 36
+    assert X.IndexerYarn.beta_slow.offset == 32
+
+
+def test_abi_version(X):
+    assert X.indexer_abi_version() == 100
+
+
+def test_workspace_size_host_only(X):
+    d = X.make_dims(n_heads=64, ratio=4, index_topk=2048)
+    n = X.indexer_workspace_size(d, 32, 1, 32767)
+    # status + q rows + w' + scores, each rounded to 256 bytes
+    assert n == 256 + 32 * 64 * 68 + 32 * 64 * 4 + 32 * 8192 * 4
+    bad = X.make_dims(n_heads=48, ratio=4, index_topk=2048)
+    assert X.indexer_workspace_size(bad, 32, 1, 32767) == 0
+
+
+def test_validation_rejects_without_launch(X):
+    lib = X.load_library()
+    d = X.make_dims(n_heads=64, ratio=4, index_topk=16)
+    # NULL dims
+    rc = lib.indexer_topk(None, None, 1, 1, 0, 0, None, None)
+    assert rc == -1 and b"dims" in lib.indexer_last_error()
+    # bad head_dim
+    d2 = X.make_dims(n_heads=64, ratio=4, index_topk=16, head_dim=96)
+    assert lib.indexer_topk(ctypes.byref(d2), 1, 1, 1, 0, 0, 1, None) == -3
+    # T inconsistent with start_pos / S / ratio
+    assert lib.indexer_topk(ctypes.byref(d), 16, 1, 8, 0, 5, 16, None) == -4
+    # misaligned q in forward
+    assert lib.indexer_forward(ctypes.byref(d), 0x1001, 0x2000, 1, 8, 0, 0x3000, 64, 0x4000, 64, None, None,
+                               0x5000, None, 0x6000, 1 << 20, None) == -2
+    # T beyond the cache
+    assert lib.indexer_forward(ctypes.byref(d), 0x1000, 0x2000, 1, 400, 0, 0x3000, 400, 0x4000, 64, None, None,
+                               0x5000, None, 0x6000, 1 << 20, None) == -4
+    # workspace too small
+    assert lib.indexer_forward(ctypes.byref(d), 0x1000, 0x2000, 1, 8, 0, 0x3000, 64, 0x4000, 64, None, None,
+                               0x5000, None, 0x6000, 16, None) == -5
+    # decode publish on a token that does not complete a group
+    assert lib.indexer_publish_k(ctypes.byref(d), 0x1000, 1, 1, 128, 0x2000, 0x3000, 0x4000, 100, 10, 0x5000, 64,
+                                 None) == -4
+    # RoPE positions beyond the table
+    assert lib.indexer_prep_q(ctypes.byref(d), 0x1000, 0x2000, 1, 8, 0, 0x3000, 4, 0x4000, 0x5000, None) == -4
+    # rope_dim odd
+    d3 = X.make_dims(n_heads=64, ratio=4, index_topk=16, rope_dim=63)
+    assert lib.indexer_prep_q(ctypes.byref(d3), 0x1000, 0x2000, 1, 8, 0, 0x3000, 64, 0x4000, 0x5000, None) == -3
+    # candidate filter with too many blocks
+    d4 = X.make_dims(n_heads=64, ratio=1, index_topk=16, cand_topk_blocks=4, cand_block_size=1)
+    assert lib.indexer_select_candidate_blocks(ctypes.byref(d4), 0x1000, 1, 1, 9999, 10000, 0x2000, None) == -3
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    import sparse_attention_top_indexer_gb300 as X
+    saved = X._lib
+    X._lib = None
+    try:
+        with pytest.raises(RuntimeError):
+            X.load_library(str(tmp_path / "nope.so"))
+    finally:
+        X._lib = saved
