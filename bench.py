@@ -1,0 +1,620 @@
+#!/usr/bin/env python3
+"""Indexer hot-path benchmark (one JSON line on rank 0).
+
+Default workload: decode -- 32 sequences, one query each at start_pos 32767
+(8192 compressed positions at ratio 4), 64 fp4 index heads, top-2048. One step
+is the whole hot path for that batch: publish the key of the group the token
+completes, then query prep + scores + causal mask + top-k (indexer_forward).
+
+  value        queries/s over all ranks, inputs resident in HBM, CUDA-graph
+               replay of the steps, CUDA events on the launching stream.
+               16 rotating key-cache copies (285 MB) keep the caches out of L2.
+  e2e          the same metric through the public C-ABI calls with pinned HOST
+               buffers: per step q/w/latent host->device, the calls, top-k
+               device->host, all inside the timed region.
+  roofline     the dominant kernel (scores): algorithmic bytes (or flops) per
+               launch / its average duration from CUDA events around each
+               kernel (split entry points, same graph replay), against the
+               measured peak in MEASURED_PEAKS.json.
+  cpu_baseline the CPU oracle, as it stands, on a bounded sample of the same
+               workload (rank 0, N=1).
+
+--impl reference times that oracle as the reference arm.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (decode
+shards by sequence, no data-path collective); the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from workloads import ROPE, WORKLOADS, Workload, normal_bf16  # noqa: E402
+
+METRIC = "indexer score+top-k queries/s and key-scores/s; % of HBM / FP4-MMA roofline"
+UNIT = "queries/s"
+FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense fp4 / bf16 tensor ratio of the part
+ROTATE = 16
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20000)
+    p.add_argument("--warmup", type=int, default=2000)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget for cpu_baseline")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+# ----------------------------------------------------------------------------- distributed
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            if torch.cuda.is_available():
+                self.pg.barrier(device_ids=[self.local])
+            else:
+                self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (50 ms) of SM clock and throttle reasons around the timed region."""
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device: int):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            self.uuid = ""
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        self.t0 = self.t1 = None
+
+    def region(self, t0, t1):
+        self.t0, self.t1 = t0, t1
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = []
+        for line in self.file.read().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, parts))
+            except Exception:
+                continue
+        os.unlink(self.file.name)
+        if self.uuid:
+            mine = [r for r in rows if self.uuid in r[1][1]]
+            rows = mine or rows
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
+        window = "timed" if inside else "warmup+timed"
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1][2]) for r in use if r[1][2].replace(".", "").isdigit()]
+        smax = [float(r[1][3]) for r in use if r[1][3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i in range(4) if r[1][6 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(use), "window": window}
+
+
+# ----------------------------------------------------------------------------- roofline inputs
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def profile_traffic(kernel_tag: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the kernel
+    source changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    if not os.path.exists(path):
+        return None
+    src = open(os.path.join(ROOT, "sparse_attention_top_indexer_gb300", "csrc", "kernel_score.cu"), "rb").read()
+    digest = hashlib.sha256(src).hexdigest()[:16]
+    vals = {}
+    for line in open(path):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != digest:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- our arm
+class Setup:
+    """Device tensors of one workload: RoPE table, weights, rotating caches and inputs."""
+
+    def __init__(self, wl: Workload, dev, rotate: int):
+        import sparse_attention_top_indexer_gb300 as X
+        self.X = X
+        self.wl = wl
+        self.dev = dev
+        X.load_library()
+        self.dims = X.make_dims(n_heads=wl.H, ratio=wl.ratio, index_topk=wl.topk, offset=wl.offset,
+                                rope_dim=wl.rope_dim, head_dim=wl.D, cand_topk_blocks=wl.cand_topk_blocks,
+                                cand_block_size=wl.cand_block_size, norm_eps=wl.norm_eps)
+        self.table = torch.empty((wl.max_pos, wl.rope_dim // 2, 2), dtype=torch.float32, device=dev)
+        X.indexer_rope_table(X.IndexerYarn(ROPE.theta, ROPE.factor, ROPE.original_seq_len, ROPE.beta_fast,
+                                           ROPE.beta_slow), wl.rope_dim, wl.max_pos, self.table)
+        self.wk, self.knw = wl.wk(dev), wl.k_norm_w(dev)
+        self.decode = wl.S == 1 and wl.start_pos > 0
+        self.rotate = rotate
+        if self.decode:
+            base = torch.zeros((wl.B, wl.T_cap, 68), dtype=torch.uint8, device=dev)
+            X.indexer_publish_k(self.dims, wl.latent(dev), self.wk, self.knw, self.table, 0, base)
+            self.caches = [base] + [base.clone() for _ in range(rotate - 1)]
+            self.lat = [normal_bf16(wl.seed, f"{wl.name}/latent_step/{i}", (wl.B, 1, wl.D), device=dev)
+                        for i in range(rotate)]
+        else:
+            self.caches = [torch.zeros((wl.B, wl.T_cap, 68), dtype=torch.uint8, device=dev) for _ in range(rotate)]
+            self.lat = [normal_bf16(wl.seed, f"{wl.name}/latent/{i}", (wl.B, wl.T, wl.D), device=dev)
+                        for i in range(rotate)]
+        tags = ["q1", "q2"] if wl.two_level else ["q"]
+        self.q = {t: [normal_bf16(wl.seed, f"{wl.name}/{t}/{i}", (wl.B, wl.S, wl.H, wl.D), device=dev)
+                      for i in range(rotate)] for t in tags}
+        self.w = {t: [normal_bf16(wl.seed, f"{wl.name}/w{t[1:]}/{i}", (wl.B, wl.S, wl.H), device=dev)
+                      for i in range(rotate)] for t in tags}
+        self.ws_bytes = X.indexer_workspace_size(self.dims, wl.B, wl.S, wl.start_pos)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        X.indexer_workspace_init(self.ws)
+        self.top = torch.empty((wl.B, wl.S, wl.topk), dtype=torch.int32, device=dev)
+        self.top1 = torch.empty_like(self.top)
+        self.cand = (torch.empty((wl.B, wl.S, wl.cand_topk_blocks), dtype=torch.int32, device=dev)
+                     if wl.two_level else None)
+        # split-entry buffers for the per-kernel breakdown
+        self.q_rows = torch.empty((wl.B, wl.S, wl.H, 68), dtype=torch.uint8, device=dev)
+        self.w_prime = torch.empty((wl.B, wl.S, wl.H), dtype=torch.float32, device=dev)
+        self.scores = torch.empty((wl.B, wl.S, wl.T), dtype=torch.float32, device=dev)
+
+    def publish(self, i):
+        wl = self.wl
+        self.X.indexer_publish_k(self.dims, self.lat[i], self.wk, self.knw, self.table,
+                                 wl.start_pos if self.decode else 0, self.caches[i])
+
+    def step(self, i):
+        """One pass of the whole hot path over batch i (forward entry point)."""
+        X, wl = self.X, self.wl
+        self.publish(i)
+        if wl.two_level:
+            X.indexer_forward(self.dims, self.q["q1"][i], self.w["q1"][i], wl.start_pos, self.table, self.caches[i],
+                              self.top1, self.ws, cand_out=self.cand)
+            X.indexer_forward(self.dims, self.q["q2"][i], self.w["q2"][i], wl.start_pos, self.table, self.caches[i],
+                              self.top, self.ws, cand_in=self.cand)
+        else:
+            X.indexer_forward(self.dims, self.q["q"][i], self.w["q"][i], wl.start_pos, self.table, self.caches[i],
+                              self.top, self.ws)
+
+    def launches_per_step(self) -> int:
+        return 1 + (7 if self.wl.two_level else 3)
+
+    def split_step(self, i, ev):
+        """The same kernels through the split entry points, an event after each.
+        Returns the labels of the intervals between consecutive events."""
+        X, wl = self.X, self.wl
+        labels = []
+        ev[0].record()
+        self.publish(i)
+        ev[1].record()
+        labels.append("publish")
+        passes = [("q1", True, None), ("q2", False, self.cand)] if wl.two_level else [("q", False, None)]
+        k = 1
+        for tag, want_cand, cand_in in passes:
+            X.indexer_prep_q(self.dims, self.q[tag][i], self.w[tag][i], wl.start_pos, self.table, self.q_rows,
+                             self.w_prime)
+            ev[k + 1].record()
+            labels.append("prep_q")
+            X.indexer_scores(self.dims, self.q_rows, self.w_prime, wl.start_pos, self.caches[i], self.scores, self.ws)
+            ev[k + 2].record()
+            labels.append("scores")
+            k += 2
+            if want_cand:
+                X.indexer_select_candidate_blocks(self.dims, self.scores, wl.start_pos, self.cand)
+                ev[k + 1].record()
+                labels.append("candidates")
+                k += 1
+            # (the level-two candidate filter rides inside indexer_forward's top-k; the split
+            # entry point selects over the same scores, same kernel and work)
+            X.indexer_topk(self.dims, self.scores, wl.start_pos, self.top)
+            ev[k + 1].record()
+            labels.append("topk")
+            k += 1
+        return labels
+
+
+def visible_pairs(wl: Workload) -> int:
+    vis = [min(wl.T, (wl.start_pos + s + 1) // wl.ratio) for s in range(wl.S)]
+    return wl.B * int(sum(vis))
+
+
+def score_units(wl: Workload):
+    """Algorithmic work of one scores launch: HBM bytes and tensor flops."""
+    pairs = visible_pairs(wl)
+    if wl.S == 1:   # decode: every key of a sequence is read once
+        key_bytes = wl.B * wl.T * 68
+    else:           # prefill: the sequence's keys are read once (they stay in L2 across query groups)
+        key_bytes = wl.B * wl.T * 68
+    q_bytes = wl.B * wl.S * wl.H * (68 + 4)
+    out_bytes = pairs * 4
+    flops = pairs * wl.H * wl.D * 2
+    return {"bytes": key_bytes + q_bytes + out_bytes, "flops": flops, "pairs": pairs}
+
+
+def capture(fn, n: int):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(n):
+            fn(i)
+    return g
+
+
+def run_ours(args, dist: Dist):
+    wl = WORKLOADS[args.workload]
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    big_inputs = wl.B * wl.S * wl.H * wl.D * 2 > 256 * 1024 * 1024
+    rotate = 1 if big_inputs else ROTATE
+    st = Setup(wl, dev, rotate)
+    for i in range(rotate):            # eager warm-up (also sets the kernels' attributes)
+        st.step(i)
+    torch.cuda.synchronize()
+    X = st.X
+    X.indexer_status(st.ws)
+
+    # graphs of `rotate` steps (+ remainders) replayed for the warm-up and the timed region
+    g_full = capture(st.step, rotate)
+    rem = args.steps % rotate
+    g_rem = capture(st.step, rem) if rem else None
+    n_full = args.steps // rotate
+    for _ in range(max(1, math.ceil(args.warmup / rotate))):
+        g_full.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(dist.local)
+    time.sleep(0.15)
+    dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
+    e0.record()
+    for _ in range(n_full):
+        g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    w1 = time.time()
+    dist.barrier()
+    sampler.region(w0, w1)
+    time.sleep(0.1)
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1)
+    ms_max = dist.max(ms)
+    X.indexer_status(st.ws)
+
+    queries = dist.world * wl.B * wl.S * args.steps
+    value = queries / (ms_max / 1e3)
+    units = score_units(wl)
+    key_scores = dist.world * units["pairs"] * args.steps / (ms_max / 1e3)
+
+    # per-kernel breakdown (split entry points, events between kernels, graph replay)
+    kernel_ms = breakdown(st, rotate)
+
+    # end to end through the public API with pinned host buffers
+    e2e = run_e2e(st, args, dist)
+
+    peaks = measured_peaks()
+    score_ms = kernel_ms.get("scores")
+    if wl.S == 1:
+        achieved = units["bytes"] / (score_ms / 1e3) / 1e9 if score_ms else None
+        peak = peaks["hbm_gbs"]
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak if achieved else None,
+                "traffic": profile_traffic(f"scores_{wl.name}"),
+                "algorithmic_bytes_per_launch": units["bytes"], "kernel": "score_kernel<64,1>",
+                "kernel_ms": score_ms, "peak_source": f"{peaks['source']} hbm_gbs"}
+    else:
+        achieved = units["flops"] / (score_ms / 1e3) / 1e12 if score_ms else None
+        peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak if achieved else None,
+                "traffic": profile_traffic(f"scores_{wl.name}"),
+                "algorithmic_flops_per_launch": units["flops"], "kernel": "score_kernel",
+                "kernel_ms": score_ms,
+                "peak_source": f"{peaks['source']} bf16_tflops x {FP4_OVER_BF16:g} (nominal fp4/bf16)"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e2m1 x e2m1 -> f32", "data": "synthetic",
+        "config": {"workload": describe(wl), "B": wl.B, "S": wl.S, "start_pos": wl.start_pos, "T": wl.T,
+                   "H": wl.H, "topk": wl.topk, "ratio": wl.ratio,
+                   "l2": (f"{rotate} rotating key caches / inputs ({rotate * wl.B * wl.T_cap * 68 / 1e6:.0f} MB)"
+                          if rotate > 1 else "inputs larger than L2"),
+                   "timing": "CUDA-graph replay, CUDA events on the launching stream"},
+        "key_scores_per_s": key_scores,
+        "kernel_ms": kernel_ms,
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": st.launches_per_step() * args.steps,
+        "clocks": clocks,
+    }
+    return line, wl
+
+
+def breakdown(st: Setup, rotate: int):
+    try:
+        ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(12)] for _ in range(rotate)]
+        external = True
+    except TypeError:
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(12)] for _ in range(rotate)]
+        external = False
+    labels = {}
+    sums, counts = {}, {}
+
+    def body(i):
+        labels[i] = st.split_step(i, ev[i])
+
+    if external:
+        g = capture(body, rotate)
+        runs = 8
+        for r in range(runs + 1):
+            g.replay()
+            torch.cuda.synchronize()
+            if r == 0:
+                continue
+            for i in range(rotate):
+                for j, lab in enumerate(labels[i]):
+                    sums[lab] = sums.get(lab, 0.0) + ev[i][j].elapsed_time(ev[i][j + 1])
+                    counts[lab] = counts.get(lab, 0) + 1
+    else:
+        for r in range(4):
+            torch.cuda._sleep(50_000_000)   # keep the GPU behind the host so the kernels run back to back
+            for i in range(rotate):
+                body(i)
+            torch.cuda.synchronize()
+            if r == 0:
+                continue
+            for i in range(rotate):
+                for j, lab in enumerate(labels[i]):
+                    sums[lab] = sums.get(lab, 0.0) + ev[i][j].elapsed_time(ev[i][j + 1])
+                    counts[lab] = counts.get(lab, 0) + 1
+    return {k: sums[k] / counts[k] for k in sums}
+
+
+def run_e2e(st: Setup, args, dist: Dist):
+    wl, X = st.wl, st.X
+    R = st.rotate
+    tag = "q2" if wl.two_level else "q"
+    qh = [t.cpu().pin_memory() for t in st.q[tag]]
+    wh = [t.cpu().pin_memory() for t in st.w[tag]]
+    lh = [t.cpu().pin_memory() for t in st.lat]
+    outh = [torch.empty(st.top.shape, dtype=torch.int32).pin_memory() for _ in range(R)]
+    qd, wd, ld = torch.empty_like(st.q[tag][0]), torch.empty_like(st.w[tag][0]), torch.empty_like(st.lat[0])
+    q1 = st.q.get("q1")
+    steps = args.steps if wl.S == 1 else min(args.steps, 64)
+
+    def one(i):
+        j = i % R
+        qd.copy_(qh[j], non_blocking=True)
+        wd.copy_(wh[j], non_blocking=True)
+        ld.copy_(lh[j], non_blocking=True)
+        X.indexer_publish_k(st.dims, ld, st.wk, st.knw, st.table, wl.start_pos if st.decode else 0, st.caches[j])
+        if wl.two_level:
+            X.indexer_forward(st.dims, q1[j], st.w["q1"][j], wl.start_pos, st.table, st.caches[j], st.top1, st.ws,
+                              cand_out=st.cand)
+            X.indexer_forward(st.dims, qd, wd, wl.start_pos, st.table, st.caches[j], st.top, st.ws, cand_in=st.cand)
+        else:
+            X.indexer_forward(st.dims, qd, wd, wl.start_pos, st.table, st.caches[j], st.top, st.ws)
+        outh[j].copy_(st.top, non_blocking=True)
+
+    for i in range(min(8, steps)):
+        one(i)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(steps):
+        one(i)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = dist.max(e0.elapsed_time(e1))
+    h2d = qh[0].numel() * 2 + wh[0].numel() * 2 + lh[0].numel() * 2
+    d2h = outh[0].numel() * 4
+    return {"value": dist.world * wl.B * wl.S * steps / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
+            "api": "indexer_publish_k + indexer_forward (eager Python/ctypes calls, pinned host buffers)"}
+
+
+def describe(wl: Workload) -> str:
+    kind = "decode" if wl.S == 1 else "prefill"
+    extra = f", two-level {wl.cand_topk_blocks}x{wl.cand_block_size} candidate blocks" if wl.two_level else ""
+    return (f"{wl.name}: {kind} B{wl.B} S{wl.S} start_pos {wl.start_pos}, ratio {wl.ratio} -> {wl.T} compressed "
+            f"positions, H{wl.H} fp4 heads, top-{wl.topk}, offset {wl.offset}{extra}")
+
+
+# ----------------------------------------------------------------------------- oracle arm / baseline
+class OracleSample:
+    """The CPU oracle on sequences of the workload (keys published once, untimed)."""
+
+    def __init__(self, wl: Workload, n_seq: int):
+        import oracle as O
+        self.O, self.wl = O, wl
+        from tests import cases as C
+        self.C = C
+        self.cos, self.sin = C.oracle_table(wl.max_pos, wl.rope_dim)
+        self.wk, self.knw = C.bits(wl.wk()), C.bits(wl.k_norm_w())
+        self.n_seq = min(n_seq, wl.B)
+        lat = wl.latent()
+        self.cache = []
+        for b in range(self.n_seq):
+            slots, rows, _ = O.publish_keys(C.bits(lat[b:b + 1]), self.wk, self.knw, self.cos, self.sin, 0, wl.ratio,
+                                            wl.rope_dim, wl.norm_eps)
+            c = np.zeros((1, wl.T_cap, 68), np.uint8)
+            c[0, slots] = rows[0]
+            self.cache.append(c)
+        self.q = C.bits(wl.q()[: self.n_seq])
+        self.w = C.bits(wl.w()[: self.n_seq])
+        self.dl = C.bits(wl.decode_latent()[: self.n_seq]) if wl.S == 1 else None
+
+    def query(self, b: int, key_frac: float = 1.0):
+        """Oracle step for sequence b's query row(s): step-key publish (decode), prep, scores, top-k."""
+        O, wl = self.O, self.wl
+        if self.dl is not None:
+            slots, rows, _ = O.publish_keys(self.dl[b:b + 1], self.wk, self.knw, self.cos, self.sin, wl.start_pos,
+                                            wl.ratio, wl.rope_dim, wl.norm_eps)
+            self.cache[b][0, slots] = rows[0]
+        T = max(1, int(math.ceil(wl.T * key_frac)))
+        rows_q, wprime, _ = O.prep_queries(self.q[b:b + 1], self.w[b:b + 1], self.cos, self.sin, wl.start_pos,
+                                           wl.rope_dim, wl.H)
+        vis = np.minimum(O.visible_lens(wl.start_pos, wl.S, wl.ratio), T)
+        sc = O.index_scores(rows_q, wprime, self.cache[b], T, vis)
+        O.topk_positions(sc[0], vis, max(1, int(math.ceil(wl.topk * key_frac))), wl.offset, T)
+
+
+def cpu_baseline(wl: Workload, seconds: float):
+    if wl.S != 1:
+        # prefill: one query row group of the workload per sample step (rows are independent)
+        wl_s = dataclasses_replace(wl, S=min(wl.S, 64), B=1)
+    else:
+        wl_s = wl
+    samp = OracleSample(wl_s, n_seq=4)
+    n = 0
+    c0, t0 = time.process_time(), time.perf_counter()
+    while True:
+        samp.query(n % samp.n_seq)
+        n += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    wall = time.perf_counter() - t0
+    cpu = time.process_time() - c0
+    queries = n * wl_s.S
+    return {"value": queries / wall, "unit": UNIT, "cores": max(1, round(cpu / wall)), "kind": "oracle",
+            "sample": f"{n} oracle steps of {wl_s.S} query row(s) each ({describe(wl_s)}), {wall:.1f} s wall, "
+                      f"keys published untimed; numpy f64 on {os.cpu_count()} host cores"}
+
+
+def dataclasses_replace(wl, **kw):
+    import dataclasses
+    return dataclasses.replace(wl, **kw)
+
+
+def run_reference(args, dist: Dist):
+    wl = WORKLOADS[args.workload]
+    if dist.rank != 0:
+        return None, wl
+    wl_s = wl if wl.S == 1 else dataclasses_replace(wl, S=min(wl.S, 64), B=1)
+    samp = OracleSample(wl_s, n_seq=2)
+    t = time.perf_counter()
+    samp.query(0)
+    t_q = time.perf_counter() - t
+    budget = 150.0 / max(1, args.steps + args.warmup)        # seconds per step so the run ends in minutes
+    frac = min(1.0, budget / max(t_q, 1e-6))
+    for i in range(args.warmup):
+        samp.query(i % samp.n_seq, frac)
+    c0, t0 = time.process_time(), time.perf_counter()
+    for i in range(args.steps):
+        samp.query(i % samp.n_seq, frac)
+    wall = time.perf_counter() - t0
+    cpu = time.process_time() - c0
+    value = args.steps * frac * wl_s.S / wall
+    sample = (f"each step: one sequence's {wl_s.S} query row(s) of {describe(wl_s)}, scored against "
+              f"{frac:.4f} of its keys (value scaled by that fraction); keys published untimed")
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": wall * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+        "config": {"workload": describe(wl), "B": wl.B, "S": wl.S, "start_pos": wl.start_pos, "T": wl.T, "H": wl.H,
+                   "topk": wl.topk, "ratio": wl.ratio},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": max(1, round(cpu / wall)), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line, wl
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            line, _ = run_reference(args, dist)
+        else:
+            line, wl = run_ours(args, dist)
+            if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
+                line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+        if dist.rank == 0 and line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

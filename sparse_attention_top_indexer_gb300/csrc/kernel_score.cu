@@ -42,9 +42,13 @@ struct ScoreCfg {
   static constexpr int N = QG * H;
   static constexpr int NP = round_up(N, 16);         // MMA N
   static constexpr int NCB = (NP + 31) / 32;         // scale columns per set
+  // Every scale-factor set starts on a 4-column boundary (an MMA given a scale set at an
+  // odd column faulted with a misaligned address).
+  static constexpr int SB = round_up(NCB, 4);        // column stride between the two B sets
   static constexpr int SFA_COL = NP;                 // 2 sets x 4 columns
-  static constexpr int SFB_COL = NP + 8;             // 2 sets x NCB columns
-  static constexpr int TMEM_NEED = NP + 8 + 2 * NCB;
+  static constexpr int SFB_COL = NP + 8;             // 2 sets x SB columns
+  static constexpr int TMEM_NEED = NP + 8 + 2 * SB;
+  static_assert(SFA_COL % 4 == 0 && SFB_COL % 4 == 0 && SB % 4 == 0, "scale sets must be 4-column aligned");
   static constexpr uint32_t TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128
                                         : TMEM_NEED <= 256 ? 256 : 512;
   static constexpr int OFF_QB = 0;
@@ -162,7 +166,7 @@ __global__ void __launch_bounds__(128, 1) score_kernel(const ScoreArgs a) {
   for (int j = 0; j < C::NCB; ++j) {
     const uint32_t wd = sfw[32 * j + lane];
     tmem_st_x1(tq + C::SFB_COL + j, wd & 0xFFFFu);
-    tmem_st_x1(tq + C::SFB_COL + C::NCB + j, wd >> 16);
+    tmem_st_x1(tq + C::SFB_COL + C::SB + j, wd >> 16);
   }
   if (tid == 0) issue_tile_load(a, b, tile0, stg_addr[0], bar_ld[0]);
 
@@ -210,7 +214,7 @@ __global__ void __launch_bounds__(128, 1) score_kernel(const ScoreArgs a) {
       mma_mxf4(tmem, smem_desc(ka_addr, 128, 512), smem_desc(qb_addr, 128, 512), idesc, tmem + C::SFA_COL,
                tmem + C::SFB_COL, 0u);
       mma_mxf4(tmem, smem_desc(ka_addr + 256, 128, 512), smem_desc(qb_addr + 256, 128, 512), idesc,
-               tmem + C::SFA_COL + 4, tmem + C::SFB_COL + C::NCB, 1u);
+               tmem + C::SFA_COL + 4, tmem + C::SFB_COL + C::SB, 1u);
       tc_commit(bar_mma);
     }
     if (tile + 1 < tile_vis) {

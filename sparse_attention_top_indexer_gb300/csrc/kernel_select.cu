@@ -20,8 +20,9 @@ constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
 
 // Larger float -> larger key; every finite value maps to a key >= 0x00800000 > 0.
+// -0.0 and +0.0 compare equal, so -0.0 is first folded onto +0.0 (x + 0 = +0 for x = -0).
 __device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = __float_as_uint(f);
+  const uint32_t u = __float_as_uint(__fadd_rn(f, 0.0f));
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
