@@ -198,6 +198,32 @@ int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexe
                     const int32_t* cand_in, int32_t* cand_out, int32_t* topk_out, float* scores_out,
                     void* ws, size_t ws_bytes, indexer_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * indexer_forward_noalloc -- indexer_forward for callers that cannot allocate
+ * device memory at call time. The pages have no counterpart: this is a deployment
+ * convenience of the library. Some hosts own all of the device's memory -- a
+ * plugin inside another runtime's memory pool, or a server whose memory budget is
+ * fixed at start-up -- and cannot hand this library a workspace. This entry point
+ * takes the same arguments as indexer_forward minus the workspace and uses a fixed
+ * scratch array inside the library's device memory instead:
+ *   - the scratch holds INDEXER_NOALLOC_SCRATCH_BYTES (8 MiB); sizes whose
+ *     indexer_workspace_size() exceeds it are rejected with INDEXER_ERR_WORKSPACE
+ *     and a message naming both sizes (nothing is launched);
+ *   - every GPU that loads the library keeps that array until the process exits;
+ *   - the first call on a device, with that device current, looks up the array's
+ *     device address (cudaGetSymbolAddress); make that first call before any stream
+ *     capture. The call allocates nothing and never calls cudaMalloc or cudaFree;
+ *   - all calls share the one array: calls that may run at the same time on the GPU
+ *     (different streams or host threads without ordering) race on it and must not
+ *     be issued; each call clears the status word it starts from;
+ *   - device-wait timeouts are not reported (the status word lives in the array).
+ * ------------------------------------------------------------------------- */
+#define INDEXER_NOALLOC_SCRATCH_BYTES (8 * 1024 * 1024)
+int indexer_forward_noalloc(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
+                            int start_pos, const float* rope_cs, int max_pos, const uint8_t* k_cache, int T_cap,
+                            const int32_t* cand_in, int32_t* cand_out, int32_t* topk_out, float* scores_out,
+                            indexer_stream_t stream);
+
 /* Bytes of workspace indexer_forward needs for these sizes (0 on invalid dims).
  * Layout: status header, quantised query rows, head weights, f32 scores. */
 size_t indexer_workspace_size(const IndexerDims* dims, int B, int S, int start_pos);

@@ -18,11 +18,13 @@ __all__ = [
     "IndexerDims", "IndexerYarn", "IndexerError", "load_library", "KEY_ROW_BYTES", "STATUS_BYTES",
     "indexer_rope_table", "indexer_publish_k", "indexer_prep_q", "indexer_scores",
     "indexer_select_candidate_blocks", "indexer_topk", "indexer_forward", "indexer_workspace_size",
-    "indexer_workspace_init", "indexer_status", "indexer_abi_version", "make_dims",
+    "indexer_workspace_init", "indexer_status", "indexer_abi_version", "make_dims", "indexer_forward_noalloc",
+    "NOALLOC_SCRATCH_BYTES",
 ]
 
 KEY_ROW_BYTES = 68
 STATUS_BYTES = 256
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libindexer.so")
 
@@ -61,6 +63,8 @@ _SIGS = {
     "indexer_topk": [ctypes.POINTER(IndexerDims), _P, _I, _I, _I, _I, _P, _P],
     "indexer_forward": [ctypes.POINTER(IndexerDims), _P, _P, _I, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P, _P,
                         ctypes.c_size_t, _P],
+    "indexer_forward_noalloc": [ctypes.POINTER(IndexerDims), _P, _P, _I, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P,
+                                _P],
     "indexer_workspace_init": [_P, ctypes.c_size_t, _P],
     "indexer_status": [_P, _P],
 }
@@ -206,3 +210,20 @@ def indexer_forward(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor, start_p
         k_cache.shape[1], _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
         _ptr(topk_out, torch.int32, "topk_out"), _ptr(scores_out, torch.float32, "scores_out"),
         _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def indexer_forward_noalloc(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor, start_pos: int,
+                            rope_cs: torch.Tensor, k_cache: torch.Tensor, topk_out: torch.Tensor,
+                            cand_in: Optional[torch.Tensor] = None, cand_out: Optional[torch.Tensor] = None,
+                            scores_out: Optional[torch.Tensor] = None, stream=None):
+    """indexer_forward without a workspace, for callers that cannot allocate device
+    memory when they call it (a plugin inside a runtime that owns the device's memory,
+    a server with a memory budget fixed at start-up). The library's fixed static
+    scratch is used instead; include/indexer.h states its size limit and why calls
+    that overlap on the GPU must not be issued."""
+    B, S = q.shape[:2]
+    _check(load_library().indexer_forward_noalloc(
+        ctypes.byref(dims), _ptr(q, torch.bfloat16, "q"), _ptr(w, torch.bfloat16, "w"), B, S, start_pos,
+        _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(k_cache, torch.uint8, "k_cache"),
+        k_cache.shape[1], _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
+        _ptr(topk_out, torch.int32, "topk_out"), _ptr(scores_out, torch.float32, "scores_out"), _stream(stream)))

@@ -110,6 +110,14 @@ WsLayout ws_layout(const IndexerDims* d, int B, int S, int start_pos) {
 
 }  // namespace
 
+namespace indexer {
+// Lets other translation units of the library report through indexer_last_error().
+int set_last_error(int code, const char* msg) {
+  g_last_error = msg;
+  return code;
+}
+}  // namespace indexer
+
 extern "C" {
 
 const char* indexer_last_error(void) { return g_last_error.c_str(); }

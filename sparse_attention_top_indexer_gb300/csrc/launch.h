@@ -69,6 +69,9 @@ struct CandArgs {
 };
 cudaError_t launch_candidates(const CandArgs& a, cudaStream_t stream);
 
+// Sets the thread-local message returned by indexer_last_error(); returns code.
+int set_last_error(int code, const char* msg);
+
 // Largest T the top-k kernel accepts (keys held in shared memory).
 constexpr int kTopkMaxT = 32768;
 constexpr int kCandMaxBlocks = 8192;
