@@ -13,9 +13,10 @@ completes, then query prep + scores + causal mask + top-k (indexer_forward).
                buffers: per step q/w/latent host->device, the calls, top-k
                device->host, all inside the timed region.
   roofline     the dominant kernel (scores): algorithmic bytes (or flops) per
-               launch / its average duration from CUDA events around each
-               kernel (split entry points, same graph replay), against the
-               measured peak in MEASURED_PEAKS.json.
+               launch / its average duration, from CUDA events around a graph
+               of back-to-back launches of that kernel alone (its own entry
+               point, rotating inputs), against the measured peak in
+               MEASURED_PEAKS.json.
   cpu_baseline the CPU oracle, as it stands, on a bounded sample of the same
                workload (rank 0, N=1).
 
@@ -208,13 +209,13 @@ class Setup:
         self.decode = wl.S == 1 and wl.start_pos > 0
         self.rotate = rotate
         if self.decode:
-            base = torch.zeros((wl.B, wl.T_cap, 68), dtype=torch.uint8, device=dev)
+            base = X.new_key_cache(wl.B, wl.T_cap, device=dev)
             X.indexer_publish_k(self.dims, wl.latent(dev), self.wk, self.knw, self.table, 0, base)
             self.caches = [base] + [base.clone() for _ in range(rotate - 1)]
             self.lat = [normal_bf16(wl.seed, f"{wl.name}/latent_step/{i}", (wl.B, 1, wl.D), device=dev)
                         for i in range(rotate)]
         else:
-            self.caches = [torch.zeros((wl.B, wl.T_cap, 68), dtype=torch.uint8, device=dev) for _ in range(rotate)]
+            self.caches = [X.new_key_cache(wl.B, wl.T_cap, device=dev) for _ in range(rotate)]
             self.lat = [normal_bf16(wl.seed, f"{wl.name}/latent/{i}", (wl.B, wl.T, wl.D), device=dev)
                         for i in range(rotate)]
         tags = ["q1", "q2"] if wl.two_level else ["q"]
@@ -255,38 +256,22 @@ class Setup:
     def launches_per_step(self) -> int:
         return 1 + (7 if self.wl.two_level else 3)
 
-    def split_step(self, i, ev):
-        """The same kernels through the split entry points, an event after each.
-        Returns the labels of the intervals between consecutive events."""
+    def kernel_kinds(self):
+        """One launch of each kernel of the step through its own entry point, on batch i."""
         X, wl = self.X, self.wl
-        labels = []
-        ev[0].record()
-        self.publish(i)
-        ev[1].record()
-        labels.append("publish")
-        passes = [("q1", True, None), ("q2", False, self.cand)] if wl.two_level else [("q", False, None)]
-        k = 1
-        for tag, want_cand, cand_in in passes:
-            X.indexer_prep_q(self.dims, self.q[tag][i], self.w[tag][i], wl.start_pos, self.table, self.q_rows,
-                             self.w_prime)
-            ev[k + 1].record()
-            labels.append("prep_q")
-            X.indexer_scores(self.dims, self.q_rows, self.w_prime, wl.start_pos, self.caches[i], self.scores, self.ws)
-            ev[k + 2].record()
-            labels.append("scores")
-            k += 2
-            if want_cand:
-                X.indexer_select_candidate_blocks(self.dims, self.scores, wl.start_pos, self.cand)
-                ev[k + 1].record()
-                labels.append("candidates")
-                k += 1
-            # (the level-two candidate filter rides inside indexer_forward's top-k; the split
-            # entry point selects over the same scores, same kernel and work)
-            X.indexer_topk(self.dims, self.scores, wl.start_pos, self.top)
-            ev[k + 1].record()
-            labels.append("topk")
-            k += 1
-        return labels
+        tag = "q2" if wl.two_level else "q"
+        kinds = {
+            "publish": lambda i: self.publish(i),
+            "prep_q": lambda i: X.indexer_prep_q(self.dims, self.q[tag][i], self.w[tag][i], wl.start_pos, self.table,
+                                                 self.q_rows, self.w_prime),
+            "scores": lambda i: X.indexer_scores(self.dims, self.q_rows, self.w_prime, wl.start_pos, self.caches[i],
+                                                 self.scores, self.ws),
+            "topk": lambda i: X.indexer_topk(self.dims, self.scores, wl.start_pos, self.top),
+        }
+        if wl.two_level:
+            kinds["candidates"] = lambda i: X.indexer_select_candidate_blocks(self.dims, self.scores, wl.start_pos,
+                                                                              self.cand)
+        return kinds
 
 
 def visible_pairs(wl: Workload) -> int:
@@ -409,44 +394,28 @@ def run_ours(args, dist: Dist):
     return line, wl
 
 
-def breakdown(st: Setup, rotate: int):
-    try:
-        ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(12)] for _ in range(rotate)]
-        external = True
-    except TypeError:
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(12)] for _ in range(rotate)]
-        external = False
-    labels = {}
-    sums, counts = {}, {}
-
-    def body(i):
-        labels[i] = st.split_step(i, ev[i])
-
-    if external:
-        g = capture(body, rotate)
-        runs = 8
-        for r in range(runs + 1):
+def breakdown(st: Setup, rotate: int, reps: int = 20):
+    """Average device time of each kernel of the step: a CUDA graph of `rotate`
+    back-to-back launches of that kernel alone (rotating inputs), replayed `reps` times
+    between CUDA events on the launching stream."""
+    out = {}
+    kinds = st.kernel_kinds()
+    for name in ["publish", "prep_q", "scores", "candidates", "topk"]:
+        if name not in kinds:
+            continue
+        g = capture(kinds[name], rotate)
+        for _ in range(3):
             g.replay()
-            torch.cuda.synchronize()
-            if r == 0:
-                continue
-            for i in range(rotate):
-                for j, lab in enumerate(labels[i]):
-                    sums[lab] = sums.get(lab, 0.0) + ev[i][j].elapsed_time(ev[i][j + 1])
-                    counts[lab] = counts.get(lab, 0) + 1
-    else:
-        for r in range(4):
-            torch.cuda._sleep(50_000_000)   # keep the GPU behind the host so the kernels run back to back
-            for i in range(rotate):
-                body(i)
-            torch.cuda.synchronize()
-            if r == 0:
-                continue
-            for i in range(rotate):
-                for j, lab in enumerate(labels[i]):
-                    sums[lab] = sums.get(lab, 0.0) + ev[i][j].elapsed_time(ev[i][j + 1])
-                    counts[lab] = counts.get(lab, 0) + 1
-    return {k: sums[k] / counts[k] for k in sums}
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        out[name] = e0.elapsed_time(e1) / (reps * rotate)
+    st.X.indexer_status(st.ws)
+    return out
 
 
 def run_e2e(st: Setup, args, dist: Dist):

@@ -28,12 +28,20 @@
  *     H = n_heads, D = head_dim = 128, rd = rope_dim, r = ratio,
  *     T = (start_pos + S) / r keys visible to the last row,
  *     vis(s) = (start_pos + s + 1) / r keys visible to row s (compress_lens).
- *   - The key cache is k_cache[B][T_cap][68] bytes: per key 64 bytes of packed
- *     e2m1 codes (element 2i in the low nibble of byte i, 2i+1 in the high nibble,
- *     sign in bit 3 of each nibble) followed by 4 UE8M0 scale bytes, one per block
- *     of 32 values ([attention.py] _indexer_k_cache_head_dim: 64 + 4 = 68).
- *     T_cap must be a multiple of 4 and k_cache 16-byte aligned, so every
- *     sequence's rows start on a 16-byte boundary.
+ *   - Every quantised 128-vector (a key, or a query head) is 68 bytes: 64 bytes of
+ *     packed e2m1 codes (element 2i in the low nibble of byte i, 2i+1 in the high
+ *     nibble, sign in bit 3 of each nibble) and 4 UE8M0 scale bytes, one per block of
+ *     32 values, block 0 in the lowest byte ([attention.py] _indexer_k_cache_head_dim:
+ *     64 + 4 = 68). Query rows (q_rows) are stored as such 68-byte rows.
+ *   - The key cache is paged, 128 keys (INDEXER_PAGE_KEYS) per page of
+ *     INDEXER_PAGE_BYTES = 8704 bytes, still 68 bytes per key: k_cache[B][T_cap/128]
+ *     [8704]. Within a page, key m's code byte j sits at
+ *         (m/8)*512 + (j/16)*128 + (m%8)*16 + (j%16)          (bytes 0 .. 8191)
+ *     -- the tensor cores' K-major core-matrix order, so a page is an MMA operand as it
+ *     lies -- and its 4 scale bytes form the 32-bit word at
+ *         8192 + ((m%32)*4 + m/32)*4                          (bytes 8192 .. 8703)
+ *     -- the order tcgen05.cp expects for 128 rows. T_cap must be a multiple of 128
+ *     and k_cache 16-byte aligned.
  *   - Device-side waits are bounded: a kernel whose wait runs out sets a bit in
  *     the status word at the start of the workspace (indexer_status reads it).
  */
@@ -61,6 +69,8 @@ typedef struct CUstream_st* indexer_stream_t;   /* == cudaStream_t */
 #define INDEXER_ERR_DEVICE_TIMEOUT -8  /* a bounded device-side wait ran out (indexer_status) */
 
 #define INDEXER_KEY_ROW_BYTES 68
+#define INDEXER_PAGE_KEYS 128
+#define INDEXER_PAGE_BYTES 8704        /* 128 keys x 68 bytes */
 #define INDEXER_STATUS_BYTES 256       /* workspace header holding the status word */
 
 /* Indexer shape and selection parameters ([index-keys] Indexer.__init__). */
@@ -106,7 +116,7 @@ int indexer_rope_table(const IndexerYarn* yarn, int rope_dim, int max_pos, float
  *   k = k_norm(k)            RMSNorm: bf16(w * k / sqrt(mean(k^2) + eps)), f64
  *   RoPE(k[..., -rd:])       interleaved pairs, f32 rotation, rounded to bf16
  *   fp4_act_quant(k, 32)     e2m1 (RNE, ties to even code) with e8m0 scales
- *   k_cache[b][slot] = row
+ *   key slot s of sequence b: page s / 128, key s % 128 of k_cache[b]
  * Slots: start_pos == 0 (prefill) writes slots 0..G-1, group j at RoPE position
  * j*r; start_pos > 0 (decode) needs G == 1 and (start_pos + 1) % r == 0 and
  * writes slot start_pos / r at position start_pos + 1 - r.
@@ -114,7 +124,7 @@ int indexer_rope_table(const IndexerYarn* yarn, int rope_dim, int max_pos, float
  *   wk:       bf16 [D][Din] (row o produces output dim o), 16-byte aligned
  *   k_norm_w: bf16 [D]
  *   rope_cs:  float [max_pos][rd/2][2]; every used position must be < max_pos
- *   k_cache:  uint8 [B][T_cap][68]; last written slot must be < T_cap
+ *   k_cache:  uint8 [B][T_cap/128][8704] (paged, see above); last slot < T_cap
  * ------------------------------------------------------------------------- */
 int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B, int G, int Din,
                       const indexer_bf16* wk, const indexer_bf16* k_norm_w, const float* rope_cs,
@@ -141,7 +151,8 @@ int indexer_prep_q(const IndexerDims* dims, const indexer_bf16* q, const indexer
  * candidate blocks):
  *   score[b][s][t] = sum_h w'[b,s,h] * relu(sum_d qhat[b,s,h,d] * khat[b,t,d])
  * over the dequantised fp4 values, products exact, f32 accumulation.
- *   q_rows/w_prime as written by indexer_prep_q (q_rows 16-byte aligned)
+ *   q_rows/w_prime as written by indexer_prep_q (both 16-byte aligned)
+ *   k_cache/T_cap: the paged key cache (T_cap a multiple of 128)
  *   cand_blocks: int32 [B][S][cand_topk_blocks] kept block ids (-1 = none), or
  *                NULL for no candidate filter
  *   scores: float [B][S][T] written (T = (start_pos + S) / r)

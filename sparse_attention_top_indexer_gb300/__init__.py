@@ -15,7 +15,8 @@ from typing import Optional
 import torch
 
 __all__ = [
-    "IndexerDims", "IndexerYarn", "IndexerError", "load_library", "KEY_ROW_BYTES", "STATUS_BYTES",
+    "IndexerDims", "IndexerYarn", "IndexerError", "load_library", "KEY_ROW_BYTES", "STATUS_BYTES", "PAGE_KEYS",
+    "PAGE_BYTES", "new_key_cache",
     "indexer_rope_table", "indexer_publish_k", "indexer_prep_q", "indexer_scores",
     "indexer_select_candidate_blocks", "indexer_topk", "indexer_forward", "indexer_workspace_size",
     "indexer_workspace_init", "indexer_status", "indexer_abi_version", "make_dims", "indexer_forward_noalloc",
@@ -23,6 +24,8 @@ __all__ = [
 ]
 
 KEY_ROW_BYTES = 68
+PAGE_KEYS = 128
+PAGE_BYTES = PAGE_KEYS * KEY_ROW_BYTES    # 8704
 STATUS_BYTES = 256
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -99,6 +102,19 @@ def make_dims(n_heads: int, ratio: int, index_topk: int, offset: int = 0, rope_d
                        norm_eps)
 
 
+def new_key_cache(B: int, T_cap: int, device="cuda") -> torch.Tensor:
+    """A zeroed paged key cache: uint8 [B, T_cap / 128, 8704] (T_cap a multiple of 128)."""
+    if T_cap % PAGE_KEYS:
+        raise ValueError("T_cap must be a multiple of 128")
+    return torch.zeros((B, T_cap // PAGE_KEYS, PAGE_BYTES), dtype=torch.uint8, device=device)
+
+
+def _cache_tcap(k_cache: torch.Tensor) -> int:
+    if k_cache.dim() != 3 or k_cache.shape[2] != PAGE_BYTES:
+        raise ValueError("k_cache must be the paged uint8 [B, T_cap / 128, 8704] cache")
+    return k_cache.shape[1] * PAGE_KEYS
+
+
 def _check(rc: int):
     if rc != 0:
         raise IndexerError(rc, load_library().indexer_last_error().decode())
@@ -136,14 +152,15 @@ def indexer_rope_table(yarn: IndexerYarn, rope_dim: int, max_pos: int, table: to
 
 def indexer_publish_k(dims: IndexerDims, latent: torch.Tensor, wk: torch.Tensor, k_norm_w: torch.Tensor,
                       rope_cs: torch.Tensor, start_pos: int, k_cache: torch.Tensor, stream=None):
-    """latent bf16 [B, G, Din]; wk bf16 [128, Din]; k_norm_w bf16 [128]; k_cache uint8 [B, T_cap, 68]."""
+    """latent bf16 [B, G, Din]; wk bf16 [128, Din]; k_norm_w bf16 [128]; k_cache uint8 [B, T_cap/128, 8704]."""
     B, G, Din = latent.shape
-    if k_cache.dim() != 3 or k_cache.shape[0] != B or k_cache.shape[2] != KEY_ROW_BYTES:
-        raise ValueError("k_cache must be uint8 [B, T_cap, 68]")
+    T_cap = _cache_tcap(k_cache)
+    if k_cache.shape[0] != B:
+        raise ValueError("k_cache batch differs from latent")
     _check(load_library().indexer_publish_k(
         ctypes.byref(dims), _ptr(latent, torch.bfloat16, "latent"), B, G, Din, _ptr(wk, torch.bfloat16, "wk"),
         _ptr(k_norm_w, torch.bfloat16, "k_norm_w"), _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0],
-        start_pos, _ptr(k_cache, torch.uint8, "k_cache"), k_cache.shape[1], _stream(stream)))
+        start_pos, _ptr(k_cache, torch.uint8, "k_cache"), T_cap, _stream(stream)))
 
 
 def indexer_prep_q(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor, start_pos: int, rope_cs: torch.Tensor,
@@ -163,7 +180,7 @@ def indexer_scores(dims: IndexerDims, q_rows: torch.Tensor, w_prime: torch.Tenso
     B, S = q_rows.shape[:2]
     _check(load_library().indexer_scores(
         ctypes.byref(dims), _ptr(q_rows, torch.uint8, "q_rows"), _ptr(w_prime, torch.float32, "w_prime"), B, S,
-        start_pos, _ptr(k_cache, torch.uint8, "k_cache"), k_cache.shape[1],
+        start_pos, _ptr(k_cache, torch.uint8, "k_cache"), _cache_tcap(k_cache),
         _ptr(cand_blocks, torch.int32, "cand_blocks"), _ptr(scores, torch.float32, "scores"),
         _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
 
@@ -207,7 +224,7 @@ def indexer_forward(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor, start_p
     _check(load_library().indexer_forward(
         ctypes.byref(dims), _ptr(q, torch.bfloat16, "q"), _ptr(w, torch.bfloat16, "w"), B, S, start_pos,
         _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(k_cache, torch.uint8, "k_cache"),
-        k_cache.shape[1], _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
+        _cache_tcap(k_cache), _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
         _ptr(topk_out, torch.int32, "topk_out"), _ptr(scores_out, torch.float32, "scores_out"),
         _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
 
@@ -225,5 +242,5 @@ def indexer_forward_noalloc(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor,
     _check(load_library().indexer_forward_noalloc(
         ctypes.byref(dims), _ptr(q, torch.bfloat16, "q"), _ptr(w, torch.bfloat16, "w"), B, S, start_pos,
         _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(k_cache, torch.uint8, "k_cache"),
-        k_cache.shape[1], _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
+        _cache_tcap(k_cache), _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
         _ptr(topk_out, torch.int32, "topk_out"), _ptr(scores_out, torch.float32, "scores_out"), _stream(stream)))

@@ -12,6 +12,18 @@ constexpr int kHeadDim = 128;           // index_head_dim supported by the kerne
 constexpr int kRowBytes = 68;           // 64 packed e2m1 bytes + 4 UE8M0 scale bytes
 constexpr int kCodeBytes = 64;
 constexpr int kFp4Block = 32;
+constexpr int kPageKeys = 128;          // keys per page of the paged key cache
+constexpr int kPageBytes = kPageKeys * kRowBytes;   // 8704: 8192 code bytes + 512 scale bytes
+
+// Byte offset, within its page, of code byte j (0..63) of key m (0..127): the K-major
+// core-matrix order of the tensor cores (8 rows x 16 bytes per core matrix, 128 bytes
+// between core matrices along K, 512 bytes between 8-row groups).
+__host__ __device__ __forceinline__ int page_code_offset(int m, int j) {
+  return (m >> 3) * 512 + (j >> 4) * 128 + (m & 7) * 16 + (j & 15);
+}
+// Byte offset, within its page, of the 32-bit scale word of key m: lane m % 32, column
+// m / 32 of a 32 x 4 word block (the layout tcgen05.cp copies to 128 lanes).
+__host__ __device__ __forceinline__ int page_scale_offset(int m) { return 8192 + ((m & 31) * 4 + (m >> 5)) * 4; }
 
 // Status bits OR-ed into the workspace status word by kernels whose bounded waits ran out.
 constexpr uint32_t kStatusLoadTimeout = 1u;
@@ -133,6 +145,23 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Named barrier over `n` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// Named barrier that also returns the AND of `v` over its `n` threads, so that every
+// thread of a warpgroup takes the same branch after a bounded wait.
+__device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t n, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.and.pred q, %2, %3, p; selp.u32 %0, 1, 0, q; }"
+      : "=r"(r) : "r"((uint32_t)v), "r"(id), "r"(n) : "memory");
+  return r != 0u;
+}
 
 // ----------------------------------------------------------------------------- PTX: tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {

@@ -177,7 +177,9 @@ int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B
   if (Din < 8 || Din > 1024 || (Din % 8)) return fail(INDEXER_ERR_DIMS, "Din must be a multiple of 8 in [8, 1024]");
   if (!aligned(latent, 16) || !aligned(wk, 16)) return fail(INDEXER_ERR_ALIGN, "latent and wk must be 16-byte aligned");
   if (!aligned(rope_cs, 8)) return fail(INDEXER_ERR_ALIGN, "rope_cs must be 8-byte aligned");
-  if (T_cap < 1) return fail(INDEXER_ERR_DIMS, "T_cap must be >= 1");
+  if (T_cap < INDEXER_PAGE_KEYS || (T_cap % INDEXER_PAGE_KEYS))
+    return fail(INDEXER_ERR_ALIGN, "T_cap must be a positive multiple of %d (got %d)", INDEXER_PAGE_KEYS, T_cap);
+  if (!aligned(k_cache, 16)) return fail(INDEXER_ERR_ALIGN, "k_cache must be 16-byte aligned");
   if (start_pos < 0) return fail(INDEXER_ERR_RANGE, "start_pos must be >= 0");
   const int r = dims->ratio;
   PublishArgs a;
@@ -261,7 +263,8 @@ int indexer_prep_q(const IndexerDims* dims, const indexer_bf16* q, const indexer
 static int check_cache(const uint8_t* k_cache, int T_cap, int T) {
   if (!k_cache) return fail(INDEXER_ERR_NULL, "k_cache is NULL");
   if (!aligned(k_cache, 16)) return fail(INDEXER_ERR_ALIGN, "k_cache must be 16-byte aligned");
-  if (T_cap < 4 || (T_cap % 4)) return fail(INDEXER_ERR_ALIGN, "T_cap must be a positive multiple of 4 (got %d)", T_cap);
+  if (T_cap < INDEXER_PAGE_KEYS || (T_cap % INDEXER_PAGE_KEYS))
+    return fail(INDEXER_ERR_ALIGN, "T_cap must be a positive multiple of %d (got %d)", INDEXER_PAGE_KEYS, T_cap);
   if (T > T_cap) return fail(INDEXER_ERR_RANGE, "T = %d keys exceed T_cap = %d", T, T_cap);
   return INDEXER_OK;
 }
@@ -274,8 +277,8 @@ int indexer_scores(const IndexerDims* dims, const uint8_t* q_rows, const float* 
   const int T = (start_pos + S) / dims->ratio;
   RETURN_IF(check_cache(k_cache, T_cap, T));
   if (!q_rows || !w_prime || !scores || !ws) return fail(INDEXER_ERR_NULL, "a required pointer is NULL");
-  if (!aligned(q_rows, 16) || !aligned(w_prime, 4) || !aligned(scores, 4) || !aligned(ws, 16))
-    return fail(INDEXER_ERR_ALIGN, "q_rows and ws must be 16-byte aligned, w_prime and scores 4-byte aligned");
+  if (!aligned(q_rows, 16) || !aligned(w_prime, 16) || !aligned(scores, 4) || !aligned(ws, 16))
+    return fail(INDEXER_ERR_ALIGN, "q_rows, w_prime and ws must be 16-byte aligned, scores 4-byte aligned");
   if (ws_bytes < INDEXER_STATUS_BYTES) return fail(INDEXER_ERR_WORKSPACE, "workspace smaller than %d bytes", INDEXER_STATUS_BYTES);
   if (cand_blocks) RETURN_IF(check_cand_dims(dims, T));
   RETURN_IF(check_arch());

@@ -5,23 +5,29 @@
 // times weights, sum over heads), with t >= vis(s) = (start_pos + s + 1) / ratio
 // masked to -inf and, for a level-two layer, -inf outside the candidate blocks.
 //
-// One CTA (128 threads) takes a group of QG query rows of one sequence and a run of
-// 128-key tiles:
-//   * A operand (M = 128): the key tile. Its 68-byte cache rows arrive by one bulk TMA
-//     copy (cp.async.bulk) into a staging buffer; thread m rewrites row m into the
-//     K-major no-swizzle core-matrix layout (8 rows x 16 bytes per core matrix) and
-//     its 4 UE8M0 scale bytes into tensor memory.
-//   * B operand (N = QG * H, padded to 16): the group's quantised query heads, loaded
-//     once per CTA in the same layout; scales in tensor memory.
-//   * Two MMAs (K = 64 each, scale blocks {0,1} then {2,3}) accumulate the 128 x N f32
-//     head dot products in tensor memory; the next tile's copy is in flight meanwhile.
-//   * Epilogue: thread m owns key t0 + m (TMEM lane m) and reads its N head scores with
-//     tcgen05.ld; for every query row it forms sum_h w' * max(dot, 0) in f32 -- the
-//     head reduction needs no shuffles because keys, not heads, sit on the lanes.
+// One CTA (256 threads) takes a group of QG query rows of one sequence and a run of
+// 128-key pages of the paged key cache. A page already holds its codes in the tensor
+// cores' K-major core-matrix order, so the MMA reads the A operand straight from the
+// stage buffer the page was bulk-copied into:
+//   * producer (warp 1, lane 0): one bulk copy (cp.async.bulk) per page into a ring of
+//     NSTAGE stage buffers; the first NSTAGE pages are requested at kernel start, the rest
+//     as soon as the MMA that read a stage has completed;
+//   * MMA issuer (warp 0, lane 0): per page, two block-scaled MMAs (K = 64 each) from the
+//     stage buffer into one of NACC f32 accumulators, committed to an mbarrier;
+//   * epilogue (warps 4-7): thread m owns key t0 + m (TMEM lane m); it reads the N head
+//     dot products with tcgen05.ld and forms sum_h w' * max(dot, 0) per query row in f32
+//     -- no shuffles, because keys, not heads, sit on the lanes. Having drained
+//     accumulator c it also writes, with tcgen05.st, the A scale factors of the next page
+//     that will use c (its key's scale word, from that page's stage buffer), then
+//     releases c to the MMA issuer.
+// B operand (N = QG * H, padded to 16): the group's quantised query rows, rewritten once
+// per CTA into the same core-matrix order; their scale factors go to tensor memory.
 //
-// Scale-factor placement in tensor memory (per 32-bit column, bytes 0/1 = the two
-// scale blocks of one K = 64 MMA): B row n = 32j + i sits in column j of lane i of every
-// 32-lane quadrant; A row m is written to lane m of all four columns of its set.
+// Tensor-memory scale layout: the MMA reads the scale factors of A row m from lane m,
+// column m / 32 of the scale set, and those of B row n = 32 j + i from column j, lane i of
+// any 32-lane quadrant. Each 32-bit column holds the two UE8M0 scales an MMA of K = 64
+// needs in its low two bytes (scale-factor id 0), so a key's scale word is split into
+// bytes 0/1 (first MMA) and bytes 2/3 (second MMA) in two 4-column halves of its set.
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -31,48 +37,61 @@ namespace indexer {
 
 namespace {
 
-constexpr int kTileKeys = 128;
-constexpr int kStageBytes = kTileKeys * kRowBytes;   // 8704
-constexpr int kABytes = kTileKeys * kCodeBytes;      // 8192
+constexpr int kTileKeys = kPageKeys;                 // one MMA M-tile per page
+constexpr int kStageStride = 9216;                   // page (8704 B) padded to a 1 KB multiple
+constexpr int kThreads = 256;
+constexpr int kEpiThreads = 128;                     // warps 4-7
 
 __host__ __device__ constexpr int round_up(int x, int m) { return (x + m - 1) / m * m; }
+__host__ __device__ constexpr uint32_t pow2_cols(int n) {
+  return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : n <= 256 ? 256u : 512u;
+}
 
 template <int H, int QG>
 struct ScoreCfg {
   static constexpr int N = QG * H;
-  static constexpr int NP = round_up(N, 16);         // MMA N
-  static constexpr int NCB = (NP + 31) / 32;         // scale columns per set
-  // Every scale-factor set starts on a 4-column boundary (an MMA given a scale set at an
-  // odd column faulted with a misaligned address).
-  static constexpr int SB = round_up(NCB, 4);        // column stride between the two B sets
-  static constexpr int SFA_COL = NP;                 // 2 sets x 4 columns
-  static constexpr int SFB_COL = NP + 8;             // 2 sets x SB columns
-  static constexpr int TMEM_NEED = NP + 8 + 2 * SB;
-  static_assert(SFA_COL % 4 == 0 && SFB_COL % 4 == 0 && SB % 4 == 0, "scale sets must be 4-column aligned");
-  static constexpr uint32_t TMEM_COLS = TMEM_NEED <= 32 ? 32 : TMEM_NEED <= 64 ? 64 : TMEM_NEED <= 128 ? 128
-                                        : TMEM_NEED <= 256 ? 256 : 512;
+  static constexpr int NP = round_up(N, 16);                 // MMA N
+  static constexpr int NCB = (NP + 31) / 32;                 // B scale columns per half
+  static constexpr int SB = round_up(NCB, 4);
+  // tensor memory: NACC accumulators of NP columns, NACC A scale sets of 8 columns, two
+  // halves of SB B scale columns; every scale address is a multiple of 4 columns
+  static constexpr int NACC = (2 * NP + 16 + 2 * SB <= 512) ? 2 : 1;
+  static constexpr int SFA_COL = NACC * NP;
+  static constexpr int SFB_COL = SFA_COL + 8 * NACC;
+  static constexpr int TMEM_NEED = SFB_COL + 2 * SB;
+  static constexpr uint32_t TMEM_COLS = pow2_cols(TMEM_NEED);
+  static constexpr int NSTAGE = 8;
   static constexpr int OFF_QB = 0;
-  static constexpr int OFF_KA = round_up(NP * kCodeBytes, 1024);
-  static constexpr int OFF_STG = OFF_KA + kABytes;
-  static constexpr int OFF_W = OFF_STG + 2 * kStageBytes;
+  static constexpr int OFF_STG = round_up(NP * kCodeBytes, 1024);
+  static constexpr int OFF_W = OFF_STG + NSTAGE * kStageStride;
   static constexpr int OFF_SFW = OFF_W + round_up(N * 4, 16);
-  static constexpr int OFF_BAR = OFF_SFW + NCB * 32 * 4;
-  static constexpr int OFF_TSLOT = OFF_BAR + 3 * 8;
-  static constexpr int OFF_CAND = round_up(OFF_TSLOT + 4, 16);
+  static constexpr int NBAR = 2 * NSTAGE + 2 * NACC;                          // full, free, done, empty
+  static constexpr int OFF_BAR = round_up(OFF_SFW + NCB * 32 * 4, 8);
+  static constexpr int OFF_INFO = OFF_BAR + NBAR * 8;                         // tmem base, counters
+  static constexpr int OFF_CAND = round_up(OFF_INFO + 16, 16);
   static_assert(N <= 256, "MMA N is at most 256");
+  static_assert(SFA_COL % 4 == 0 && SFB_COL % 4 == 0 && SB % 4 == 0, "scale sets must be 4-column aligned");
+  static_assert(TMEM_NEED <= (int)TMEM_COLS && TMEM_COLS <= 512u, "tensor memory budget");
 };
 
-__device__ __forceinline__ void issue_tile_load(const ScoreArgs& a, int b, int tile, uint32_t stage_addr,
+__device__ __forceinline__ void issue_page_load(const ScoreArgs& a, int b, int tile, uint32_t stage_addr,
                                                 uint32_t bar) {
-  const int t0 = tile * kTileKeys;
-  const int nv = min(kTileKeys, a.T - t0);
-  const uint32_t bytes = (uint32_t)(round_up(nv, 4) * kRowBytes);   // multiple of 16; stays below T_cap
-  mbar_arrive_expect_tx(bar, bytes);
-  bulk_g2s(stage_addr, a.k_cache + ((size_t)b * a.T_cap + t0) * kRowBytes, bytes, bar);
+  mbar_arrive_expect_tx(bar, (uint32_t)kPageBytes);
+  bulk_g2s(stage_addr, a.k_cache + ((size_t)b * (a.T_cap / kPageKeys) + tile) * kPageBytes, (uint32_t)kPageBytes,
+           bar);
+}
+
+// Epilogue thread et: the A scale factors of key et of the page in stage `st` into scale
+// set c (bytes 0/1 of its scale word in columns 0-3, bytes 2/3 in columns 4-7 of lane et).
+__device__ __forceinline__ void write_sfa(uint32_t tq_set, const uint8_t* page, int et) {
+  const uint32_t w = *reinterpret_cast<const uint32_t*>(page + page_scale_offset(et));
+  const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
+  tmem_st_x8(tq_set, lo, lo, lo, lo, hi, hi, hi, hi);
 }
 
 template <int H, int QG>
-__global__ void __launch_bounds__(128, 1) score_kernel(const ScoreArgs a) {
+__global__ void __launch_bounds__(kThreads, ScoreCfg<H, QG>::TMEM_COLS <= 256 ? 2 : 1)
+    score_kernel(const ScoreArgs a) {
   using C = ScoreCfg<H, QG>;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1024-byte aligned base
@@ -81,51 +100,56 @@ __global__ void __launch_bounds__(128, 1) score_kernel(const ScoreArgs a) {
   const int s0 = blockIdx.y * QG;
   const int nq = min(QG, a.S - s0);
   const int ntiles = (a.T + kTileKeys - 1) / kTileKeys;
-  const int tiles_per_cta = (ntiles + gridDim.x - 1) / gridDim.x;
-  const int tile0 = blockIdx.x * tiles_per_cta;
-  const int tile1 = min(tile0 + tiles_per_cta, ntiles);
+  const int tile0 = blockIdx.x * a.tiles_per_cta;
+  const int tile1 = min(tile0 + a.tiles_per_cta, ntiles);
   if (nq <= 0 || tile0 >= tile1) return;
-  // keys the group's last row can see; tiles at or past it are fully masked
+  // keys the group's last row can see; pages at or past it are fully masked
   const int vis_hi = min(a.T, (a.start_pos + s0 + nq) / a.ratio);
   const int tile_vis = min(tile1, (vis_hi + kTileKeys - 1) / kTileKeys);
   if (a.fill_masked) {
     const int t_begin = max(tile0, tile_vis) * kTileKeys, t_end = min(tile1 * kTileKeys, a.T);
     for (int qi = 0; qi < nq; ++qi) {
       float* dst = a.scores + ((size_t)b * a.S + s0 + qi) * a.T;
-      for (int t = t_begin + tid; t < t_end; t += 128) dst[t] = -__int_as_float(0x7f800000);
+      for (int t = t_begin + tid; t < t_end; t += kThreads) dst[t] = -__int_as_float(0x7f800000);
     }
   }
   if (tile_vis <= tile0) return;
+  const int nt = tile_vis - tile0;   // pages this CTA scores
 
   uint8_t* qB = smem + C::OFF_QB;
-  uint8_t* kA = smem + C::OFF_KA;
-  uint8_t* stg = smem + C::OFF_STG;
+  const uint8_t* stg = smem + C::OFF_STG;
   float* wq = reinterpret_cast<float*>(smem + C::OFF_W);
   uint32_t* sfw = reinterpret_cast<uint32_t*>(smem + C::OFF_SFW);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + C::OFF_TSLOT);
+  uint32_t* info = reinterpret_cast<uint32_t*>(smem + C::OFF_INFO);   // [0] tmem, [1] issued, [2] mma issued
   uint32_t* cand_bits = reinterpret_cast<uint32_t*>(smem + C::OFF_CAND);
-  const uint32_t bar_ld[2] = {smem_u32(&bars[0]), smem_u32(&bars[1])};
-  const uint32_t bar_mma = smem_u32(&bars[2]);
-  const uint32_t stg_addr[2] = {smem_u32(stg), smem_u32(stg + kStageBytes)};
+  const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
+  auto bar_full = [&](int st) { return bar0 + 8u * (uint32_t)st; };
+  auto bar_free = [&](int st) { return bar0 + 8u * (uint32_t)(C::NSTAGE + st); };
+  auto bar_done = [&](int c) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + c); };
+  auto bar_empty = [&](int c) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + C::NACC + c); };
+  const uint32_t stg0 = smem_u32(stg);
 
   if (tid == 0) {
-    mbar_init(bar_ld[0], 1);
-    mbar_init(bar_ld[1], 1);
-    mbar_init(bar_mma, 1);
+    for (int i = 0; i < 2 * C::NSTAGE + C::NACC; ++i) mbar_init(bar0 + 8u * i, 1);
+    for (int c = 0; c < C::NACC; ++c) mbar_init(bar_empty(c), kEpiThreads);
     fence_mbar_init();
+    const int first = min(nt, C::NSTAGE);
+    for (int i = 0; i < first; ++i) issue_page_load(a, b, tile0 + i, stg0 + i * kStageStride, bar_full(i));
+    info[1] = (uint32_t)first;
+    info[2] = 0u;
   }
+  __syncwarp();
   if (warp == 0) {
-    tmem_alloc(smem_u32(tslot), C::TMEM_COLS);
+    tmem_alloc(smem_u32(&info[0]), C::TMEM_COLS);
     tmem_relinquish();
   }
   // head weights of the group (0 for rows past S)
-  for (int n = tid; n < C::N; n += 128) {
+  for (int n = tid; n < C::N; n += kThreads) {
     const int qi = n / H;
     wq[n] = qi < nq ? a.w_prime[((size_t)b * a.S + s0 + qi) * H + (n % H)] : 0.f;
   }
-  // quantised query rows -> B operand (core-matrix layout) and scale words
-  for (int n = tid; n < C::NCB * 32; n += 128) {
+  // quantised query rows -> B operand (core-matrix order) and scale words
+  for (int n = tid; n < C::NCB * 32; n += kThreads) {
     uint32_t w[16];
     uint32_t sc = 0x7F7F7F7Fu;
     if (n < C::N && n / H < nq) {
@@ -149,9 +173,9 @@ __global__ void __launch_bounds__(128, 1) score_kernel(const ScoreArgs a) {
   // level-two candidate filter: one bit per block of cbs positions, per query row
   const int cand_words = a.cand ? ((a.T + a.cbs - 1) / a.cbs + 31) / 32 : 0;
   if (a.cand) {
-    for (int i = tid; i < QG * cand_words; i += 128) cand_bits[i] = 0u;
+    for (int i = tid; i < QG * cand_words; i += kThreads) cand_bits[i] = 0u;
     __syncthreads();
-    for (int i = tid; i < nq * a.cbk; i += 128) {
+    for (int i = tid; i < nq * a.cbk; i += kThreads) {
       const int qi = i / a.cbk;
       const int blk = a.cand[((size_t)b * a.S + s0 + qi) * a.cbk + (i % a.cbk)];
       if (blk >= 0 && blk < cand_words * 32) atomicOr(&cand_bits[qi * cand_words + (blk >> 5)], 1u << (blk & 31));
@@ -160,117 +184,178 @@ __global__ void __launch_bounds__(128, 1) score_kernel(const ScoreArgs a) {
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tslot;
-  const uint32_t tq = tmem + ((uint32_t)(warp * 32) << 16);   // this warp's lane quadrant
+  const uint32_t tmem = info[0];
+  const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);   // this warp's lane quadrant
+  if (warp < 4) {
+    __syncwarp();
 #pragma unroll
-  for (int j = 0; j < C::NCB; ++j) {
-    const uint32_t wd = sfw[32 * j + lane];
-    tmem_st_x1(tq + C::SFB_COL + j, wd & 0xFFFFu);
-    tmem_st_x1(tq + C::SFB_COL + C::SB + j, wd >> 16);
-  }
-  if (tid == 0) issue_tile_load(a, b, tile0, stg_addr[0], bar_ld[0]);
-
-  const uint32_t idesc = idesc_mxf4(128, C::NP);
-  const uint32_t qb_addr = smem_u32(qB), ka_addr = smem_u32(kA);
-  bool load_pending = true;   // tile0's copy
-  int pending_stage = 0, pending_parity = 0;
-  bool ok = true;
-  int it = 0;
-  for (int tile = tile0; tile < tile_vis; ++tile, ++it) {
-    const int st = it & 1;
-    const int t0 = tile * kTileKeys;
-    const int nv = min(kTileKeys, a.T - t0);
-    const bool got = mbar_wait(bar_ld[st], (it >> 1) & 1);
-    if (__syncthreads_and(got) == 0) {
-      if (tid == 0) atomicOr(a.status, kStatusLoadTimeout);
-      ok = false;
-      break;
+    for (int j = 0; j < C::NCB; ++j) {
+      const uint32_t wd = sfw[32 * j + lane];
+      tmem_st_x1(tq + C::SFB_COL + j, wd & 0xFFFFu);
+      tmem_st_x1(tq + C::SFB_COL + C::SB + j, wd >> 16);
     }
-    load_pending = false;
-    // A operand: key row tid -> core-matrix layout; scale word -> tensor memory
-    uint32_t w[17];
-    if (tid < nv) {
-      const uint32_t* raw = reinterpret_cast<const uint32_t*>(stg + st * kStageBytes + tid * kRowBytes);
-#pragma unroll
-      for (int i = 0; i < 17; ++i) w[i] = raw[i];
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = 0u;
-      w[16] = 0x7F7F7F7Fu;
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      *reinterpret_cast<uint4*>(kA + (tid >> 3) * 512 + c * 128 + (tid & 7) * 16) =
-          make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-    const uint32_t s01 = w[16] & 0xFFFFu, s23 = w[16] >> 16;
-    tmem_st_x8(tq + C::SFA_COL, s01, s01, s01, s01, s23, s23, s23, s23);
     tmem_wait_st();
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0) {
-      if (tile + 1 < tile_vis) issue_tile_load(a, b, tile + 1, stg_addr[st ^ 1], bar_ld[st ^ 1]);
-      mma_mxf4(tmem, smem_desc(ka_addr, 128, 512), smem_desc(qb_addr, 128, 512), idesc, tmem + C::SFA_COL,
-               tmem + C::SFB_COL, 0u);
-      mma_mxf4(tmem, smem_desc(ka_addr + 256, 128, 512), smem_desc(qb_addr + 256, 128, 512), idesc,
-               tmem + C::SFA_COL + 4, tmem + C::SFB_COL + C::SB, 1u);
-      tc_commit(bar_mma);
-    }
-    if (tile + 1 < tile_vis) {
-      load_pending = true;
-      pending_stage = st ^ 1;
-      pending_parity = ((it + 1) >> 1) & 1;
-    }
-    const bool done = mbar_wait(bar_mma, it & 1);
-    if (__syncthreads_and(done) == 0) {
-      if (tid == 0) atomicOr(a.status, kStatusMmaTimeout);
-      ok = false;
-      mbar_wait(bar_mma, it & 1);   // one more bounded wait before the tensor memory is released
-      break;
-    }
-    tc_fence_after();
+  }
+  fence_proxy_async_smem();   // the B operand was written by ordinary stores
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
-    // epilogue: key t0 + tid, all N head scores of the group
-    float acc[QG];
-#pragma unroll
-    for (int qi = 0; qi < QG; ++qi) acc[qi] = 0.f;
-#pragma unroll
-    for (int c = 0; c < C::NCB; ++c) {
-      float v[32];
-      tmem_ld32(tq + 32 * c, v);
-#pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const int n = 32 * c + jj;
-        if (n < C::N) acc[n / H] = fmaf(wq[n], fmaxf(v[jj], 0.f), acc[n / H]);
+  // Role loops are warp-uniform: every lane of a role warp runs the loop and takes the
+  // same branches (waits are made uniform with __all_sync), and only lane 0 issues the
+  // copies, MMAs and commits. No warp reaches a CTA-wide barrier partly diverged.
+  bool failed = false;
+  if (warp == 0) {
+    // ------------------------------------------------------------ MMA issuer (lane 0)
+    const uint32_t idesc = idesc_mxf4(128, C::NP);
+    const uint32_t qb = smem_u32(qB);
+    for (int i = 0; i < nt; ++i) {
+      const int st = i % C::NSTAGE, c = i % C::NACC;
+      // the page has landed, and accumulator c is drained and holds this page's A scales
+      bool ok = mbar_wait(bar_full(st), (uint32_t)(i / C::NSTAGE) & 1u);
+      ok = ok && mbar_wait(bar_empty(c), (uint32_t)(i / C::NACC) & 1u);
+      if (!__all_sync(0xffffffffu, ok)) {
+        failed = true;
+        break;
       }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t pa = stg0 + (uint32_t)(st * kStageStride);
+        const uint32_t acc = tmem + (uint32_t)(c * C::NP);
+        const uint32_t sfa = tmem + (uint32_t)(C::SFA_COL + 8 * c);
+        mma_mxf4(acc, smem_desc(pa, 128, 512), smem_desc(qb, 128, 512), idesc, sfa, tmem + C::SFB_COL, 0u);
+        mma_mxf4(acc, smem_desc(pa + 256, 128, 512), smem_desc(qb + 256, 128, 512), idesc, sfa + 4,
+                 tmem + C::SFB_COL + C::SB, 1u);
+        tc_commit(bar_done(c));
+        if (i + C::NSTAGE < nt) tc_commit(bar_free(st));
+        info[2] = (uint32_t)(i + 1);
+      }
+      __syncwarp();
     }
-    if (tid < nv) {
-      const int t = t0 + tid;
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ producer (lane 0): stage refills
+    for (int j = C::NSTAGE; j < nt; ++j) {
+      const int st = j % C::NSTAGE;
+      const bool ok = mbar_wait(bar_free(st), (uint32_t)((j - C::NSTAGE) / C::NSTAGE) & 1u);
+      if (!__all_sync(0xffffffffu, ok)) {
+        failed = true;
+        break;
+      }
+      if (lane == 0) {
+        issue_page_load(a, b, tile0 + j, stg0 + st * kStageStride, bar_full(st));
+        info[1] = (uint32_t)(j + 1);
+      }
+      __syncwarp();
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ epilogue
+    constexpr int P = H >= 32 ? 4 : (H >= 16 ? 2 : 1);   // independent partial sums per row
+    const int et = tid - 128;   // key within the page == TMEM lane
+    // A scales of the first NACC pages, one scale set per accumulator
+    for (int p = 0; p < min(nt, C::NACC); ++p) {
+      const bool ok = mbar_wait(bar_full(p), 0u);
+      if (!__all_sync(0xffffffffu, ok)) {
+        failed = true;
+        break;
+      }
+      write_sfa(tq + (uint32_t)(C::SFA_COL + 8 * p), stg + p * kStageStride, et);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_empty(p));
+    }
+    for (int i = 0; i < nt && !failed; ++i) {
+      const int c = i % C::NACC;
+      const bool ok = mbar_wait(bar_done(c), (uint32_t)(i / C::NACC) & 1u);
+      if (!__all_sync(0xffffffffu, ok)) {
+        failed = true;
+        break;
+      }
+      tc_fence_after();
+      float part[QG][P];
 #pragma unroll
-      for (int qi = 0; qi < QG; ++qi) {
-        if (qi < nq) {
-          const int s = s0 + qi;
-          const int vis = min(a.T, (a.start_pos + s + 1) / a.ratio);
-          bool keep = t < vis;
-          if (a.cand) {
-            const int blk = t / a.cbs;
-            keep = keep && ((cand_bits[qi * cand_words + (blk >> 5)] >> (blk & 31)) & 1u);
-          }
-          a.scores[((size_t)b * a.S + s) * a.T + t] = keep ? acc[qi] : -__int_as_float(0x7f800000);
+      for (int qi = 0; qi < QG; ++qi)
+#pragma unroll
+        for (int p = 0; p < P; ++p) part[qi][p] = 0.f;
+#pragma unroll
+      for (int k = 0; k < C::NCB; ++k) {
+        float v[32];
+        tmem_ld32(tq + (uint32_t)(c * C::NP + 32 * k), v);
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int n = 32 * k + jj;
+          if (n < C::N) part[n / H][n % P] = fmaf(wq[n], fmaxf(v[jj], 0.f), part[n / H][n % P]);
         }
       }
+      const int inext = i + C::NACC;   // the next page to use accumulator c
+      if (inext < nt) {
+        const int sn = inext % C::NSTAGE;
+        const bool okn = mbar_wait(bar_full(sn), (uint32_t)(inext / C::NSTAGE) & 1u);
+        if (!__all_sync(0xffffffffu, okn)) {
+          failed = true;
+          break;
+        }
+        write_sfa(tq + (uint32_t)(C::SFA_COL + 8 * c), stg + sn * kStageStride, et);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      if (inext < nt) mbar_arrive(bar_empty(c));   // accumulator c drained, next scales in place
+      const int t0 = (tile0 + i) * kTileKeys;
+      const int nv = min(kTileKeys, a.T - t0);
+      if (et < nv) {
+        const int t = t0 + et;
+#pragma unroll
+        for (int qi = 0; qi < QG; ++qi) {
+          if (qi < nq) {
+            float acc = part[qi][0];
+#pragma unroll
+            for (int p = 1; p < P; ++p) acc += part[qi][p];
+            const int s = s0 + qi;
+            const int vis = min(a.T, (a.start_pos + s + 1) / a.ratio);
+            bool keep = t < vis;
+            if (a.cand) {
+              const int blk = t / a.cbs;
+              keep = keep && ((cand_bits[qi * cand_words + (blk >> 5)] >> (blk & 31)) & 1u);
+            }
+            a.scores[((size_t)b * a.S + s) * a.T + t] = keep ? acc : -__int_as_float(0x7f800000);
+          }
+        }
+      }
+      __syncwarp();
     }
-    tc_fence_before();
   }
-  if (!ok && load_pending) mbar_wait(bar_ld[pending_stage], pending_parity);   // bounded
+  if (failed && (tid == 0 || tid == 32 || tid == 128))
+    atomicOr(a.status, tid == 128 ? kStatusMmaTimeout : kStatusLoadTimeout);
+  __syncwarp();
+  __syncthreads();
+  if (tid == 0) {
+    // bounded waits for copies and MMAs still in flight before shared and tensor memory go away
+    const int issued = (int)info[1], mmas = (int)info[2];
+    for (int st = 0; st < C::NSTAGE && st < issued; ++st) {
+      const int last = st + ((issued - 1 - st) / C::NSTAGE) * C::NSTAGE;   // last page loaded into st
+      mbar_wait(bar_full(st), (uint32_t)(last / C::NSTAGE) & 1u);
+    }
+    if (mmas > 0) mbar_wait(bar_done((mmas - 1) % C::NACC), (uint32_t)((mmas - 1) / C::NACC) & 1u);
+  }
+  __syncwarp();
   __syncthreads();
   tc_fence_after();
   if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 template <int H, int QG>
-cudaError_t launch_cfg(const ScoreArgs& a, cudaStream_t stream) {
+cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
   using C = ScoreCfg<H, QG>;
   const int cand_words = a.cand ? ((a.T + a.cbs - 1) / a.cbs + 31) / 32 : 0;
   const size_t smem = (size_t)C::OFF_CAND + (size_t)QG * cand_words * 4 + 1024;   // + base alignment slack
@@ -278,16 +363,22 @@ cudaError_t launch_cfg(const ScoreArgs& a, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   const int ntiles = (a.T + kTileKeys - 1) / kTileKeys;
   const int groups = (a.S + QG - 1) / QG;
-  // decode-like shapes (few query groups): split the keys of a sequence over CTAs
-  int chunks = 1;
-  const long long base_ctas = (long long)groups * a.B;
-  if (base_ctas < 600) {
-    chunks = (int)((600 + base_ctas - 1) / base_ctas);
-    if (chunks > ntiles) chunks = ntiles;
-    if (chunks < 1) chunks = 1;
+  // resident CTAs per SM: tensor memory (512 columns) and shared memory (227 KB) both bound it
+  const int by_tmem = 512 / (int)C::TMEM_COLS;
+  const int by_smem = (int)((227 * 1024) / (smem + 1024));
+  const int per_sm = by_tmem < by_smem ? by_tmem : by_smem;
+  const long long target = (long long)sm_count() * (per_sm > 0 ? per_sm : 1);
+  const long long base = (long long)groups * a.B;
+  // few query groups (decode): split each sequence's pages over CTAs, one wave in total
+  int tpc = ntiles;
+  if (base < target) {
+    tpc = (int)((ntiles * base + target - 1) / target);
+    if (tpc < 1) tpc = 1;
+    while (tpc < ntiles && (long long)((ntiles + tpc - 1) / tpc) * base > target) ++tpc;
   }
-  dim3 grid(chunks, groups, a.B);
-  score_kernel<H, QG><<<grid, 128, smem, stream>>>(a);
+  a.tiles_per_cta = tpc;
+  dim3 grid((ntiles + tpc - 1) / tpc, groups, a.B);
+  score_kernel<H, QG><<<grid, kThreads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -38,16 +38,21 @@ cudaError_t launch_rope_table(const RopeFreqs& freqs, int half, int max_pos, flo
 // ---------------------------------------------------------------------------- key publish
 // One CTA of 128 threads per key; thread o owns output dim o.
 //  1. k_pre[o] = bf16( sum_i wk[o][i] * latent[i] ): bf16*bf16 products are exact in f32,
-//     their sum is carried error-free (TwoSum) in four interleaved accumulators and
+//     their sum is carried error-free (TwoSum) in eight interleaved accumulators and
 //     rounded once to bf16 ("DeepSeek V4.1" index-keys page, Indexer: wk bf16 Linear).
-//  2. RMSNorm in f64: y = bf16( (w[o] * k_pre[o]) * (1 / sqrt(sum(k_pre^2) / 128 + eps)) ).
+//     The thread's wk row is fetched 128 elements at a time with all loads issued
+//     before any is used, so a 128-wide row costs one memory round trip.
+//  2. RMSNorm in f64: y = bf16( (w[o] * k_pre[o]) * (1 / sqrt(sum(k_pre^2) / 128 + eps)) );
+//     the reciprocal square root is formed once per key.
 //  3. RoPE on the last rope_dim dims at the group position: interleaved pair (2i, 2i+1)
 //     rotated by table entry i with the f32 sequence x0*c - x1*s, x0*s + x1*c, then bf16.
-//  4. e2m1/e8m0 quantisation per 32-block (warp w owns block w) into the 68-byte row.
+//  4. e2m1/e8m0 quantisation per 32-block (warp w owns block w); the 64 code bytes and
+//     4 scale bytes go to the key's places in its 128-key page.
 __global__ void __launch_bounds__(128) publish_kernel(PublishArgs a) {
   __shared__ float lat[1024];
   __shared__ float kv[kHeadDim];
   __shared__ double wsum[4];
+  __shared__ double rinv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int key = blockIdx.x;
   const int b = key / a.G, j = key % a.G;
@@ -57,26 +62,39 @@ __global__ void __launch_bounds__(128) publish_kernel(PublishArgs a) {
 
   // 1. exact dot product, rounded once
   const uint16_t* wrow = a.wk + (size_t)tid * a.Din;
-  float s[4] = {0.f, 0.f, 0.f, 0.f}, c[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int i0 = 0; i0 < a.Din; i0 += 8) {
-    const uint4 w8 = *reinterpret_cast<const uint4*>(wrow + i0);
-    const uint32_t ww[4] = {w8.x, w8.y, w8.z, w8.w};
+  constexpr int kAcc = 8;
+  float s[kAcc], c[kAcc];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float p0 = __fmul_rn(bf16_to_f32(ww[k] & 0xFFFFu), lat[i0 + 2 * k]);
-      const float p1 = __fmul_rn(bf16_to_f32(ww[k] >> 16), lat[i0 + 2 * k + 1]);
-      float t, e;
-      two_sum(s[k], p0, t, e);
-      s[k] = t;
-      c[k] = __fadd_rn(c[k], e);
-      two_sum(s[k], p1, t, e);
-      s[k] = t;
-      c[k] = __fadd_rn(c[k], e);
+  for (int k = 0; k < kAcc; ++k) s[k] = c[k] = 0.f;
+  for (int i0 = 0; i0 < a.Din; i0 += 128) {
+    uint4 w8[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      w8[u] = (i0 + 8 * u < a.Din) ? *reinterpret_cast<const uint4*>(wrow + i0 + 8 * u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const uint32_t ww[4] = {w8[u].x, w8[u].y, w8[u].z, w8[u].w};
+      const int e0 = i0 + 8 * u;
+      if (e0 < a.Din) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int acc = (2 * k) & (kAcc - 1), acc2 = (2 * k + 1) & (kAcc - 1);
+          const float p0 = __fmul_rn(bf16_to_f32(ww[k] & 0xFFFFu), lat[e0 + 2 * k]);
+          const float p1 = __fmul_rn(bf16_to_f32(ww[k] >> 16), lat[e0 + 2 * k + 1]);
+          float t, e;
+          two_sum(s[acc], p0, t, e);
+          s[acc] = t;
+          c[acc] = __fadd_rn(c[acc], e);
+          two_sum(s[acc2], p1, t, e);
+          s[acc2] = t;
+          c[acc2] = __fadd_rn(c[acc2], e);
+        }
+      }
     }
   }
   float hi = s[0], lo = c[0];
 #pragma unroll
-  for (int k = 1; k < 4; ++k) {
+  for (int k = 1; k < kAcc; ++k) {
     float t, e;
     two_sum(hi, s[k], t, e);
     hi = t;
@@ -97,10 +115,13 @@ __global__ void __launch_bounds__(128) publish_kernel(PublishArgs a) {
   for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
   if (lane == 0) wsum[warp] = ss;
   __syncthreads();
-  const double ms = ((wsum[0] + wsum[1]) + (wsum[2] + wsum[3])) / (double)kHeadDim;
-  const double r = 1.0 / sqrt(ms + (double)a.eps);
+  if (tid == 0) {
+    const double ms = ((wsum[0] + wsum[1]) + (wsum[2] + wsum[3])) / (double)kHeadDim;
+    rinv = 1.0 / sqrt(ms + (double)a.eps);
+  }
+  __syncthreads();
   const float wx = __fmul_rn(bf16_to_f32(a.knorm[tid]), x);   // exact (bf16 * bf16)
-  float y = bf16_to_f32(f64_to_bf16_rne((double)wx * r));
+  float y = bf16_to_f32(f64_to_bf16_rne((double)wx * rinv));
 
   // 3. RoPE
   kv[tid] = y;
@@ -118,15 +139,17 @@ __global__ void __launch_bounds__(128) publish_kernel(PublishArgs a) {
   }
 
   // 4. quantise: warp w holds block w, one value per lane
-  uint32_t amax = __float_as_uint(y) >> 16 & 0x7FFFu;
+  uint32_t amax = (__float_as_uint(y) >> 16) & 0x7FFFu;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, off));
   const int e = e8m0_exponent(amax);
   const float yq = __fmul_rn(y, pow2_neg(e));
   const float partner = __shfl_down_sync(0xffffffffu, yq, 1);
-  uint8_t* row = a.k_cache + ((size_t)b * a.T_cap + a.slot0 + j) * kRowBytes;
-  if ((lane & 1) == 0) row[(warp * 32 + lane) >> 1] = (uint8_t)e2m1x2(yq, partner);
-  if (lane == 0) row[kCodeBytes + warp] = (uint8_t)(e + 127);
+  const int slot = a.slot0 + j;
+  const int m = slot % kPageKeys;
+  uint8_t* page = a.k_cache + ((size_t)b * (a.T_cap / kPageKeys) + slot / kPageKeys) * kPageBytes;
+  if ((lane & 1) == 0) page[page_code_offset(m, (warp * 32 + lane) >> 1)] = (uint8_t)e2m1x2(yq, partner);
+  if (lane == 0) page[page_scale_offset(m) + warp] = (uint8_t)(e + 127);
 }
 
 cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream) {

@@ -51,6 +51,7 @@ struct ScoreArgs {
   uint32_t* status;
   int B, S, H, T, T_cap, start_pos, ratio, cbk, cbs;
   int fill_masked;          // write -inf over key tiles no row of the group can see
+  int tiles_per_cta;        // set by the launcher
 };
 cudaError_t launch_scores(const ScoreArgs& a, cudaStream_t stream);
 

@@ -60,13 +60,25 @@ def gpu_cache(wl: Workload, table: torch.Tensor, latent=None, decode_latent=None
     the key of the group completed at start_pos."""
     import sparse_attention_top_indexer_gb300 as X
     lat = wl.latent("cuda") if latent is None else latent
-    cache = torch.zeros((wl.B, wl.T_cap, 68), dtype=torch.uint8, device="cuda")
+    cache = X.new_key_cache(wl.B, wl.T_cap)
     d = dims_of(wl)
     X.indexer_publish_k(d, lat, wl.wk("cuda"), wl.k_norm_w("cuda"), table, 0, cache)
     if publishes_step_key(wl):
         dl = wl.decode_latent("cuda") if decode_latent is None else decode_latent
         X.indexer_publish_k(d, dl, wl.wk("cuda"), wl.k_norm_w("cuda"), table, wl.start_pos, cache)
     return cache
+
+
+def pages_to_rows(pages) -> np.ndarray:
+    """The paged key cache [B, P, 8704] as 68-byte key rows [B, P*128, 68]: within a page,
+    key m's code byte j sits at (m/8)*512 + (j/16)*128 + (m%8)*16 + j%16 and its scale
+    word at 8192 + ((m%32)*4 + m/32)*4 (a pure reordering of bytes)."""
+    if isinstance(pages, torch.Tensor):
+        pages = pages.cpu().numpy()
+    B, P, _ = pages.shape
+    codes = pages[:, :, :8192].reshape(B, P, 16, 4, 8, 16).transpose(0, 1, 2, 4, 3, 5).reshape(B, P, 128, 64)
+    sc = pages[:, :, 8192:].reshape(B, P, 32, 4, 4).transpose(0, 1, 3, 2, 4).reshape(B, P, 128, 4)
+    return np.concatenate([codes, sc], axis=-1).reshape(B, P * 128, 68)
 
 
 def oracle_cache(wl: Workload, cos, sin, latent=None, decode_latent=None) -> np.ndarray:

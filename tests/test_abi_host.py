@@ -69,13 +69,16 @@ def test_validation_rejects_without_launch(X):
     assert lib.indexer_forward(ctypes.byref(d), 0x1001, 0x2000, 1, 8, 0, 0x3000, 64, 0x4000, 64, None, None,
                                0x5000, None, 0x6000, 1 << 20, None) == -2
     # T beyond the cache
-    assert lib.indexer_forward(ctypes.byref(d), 0x1000, 0x2000, 1, 400, 0, 0x3000, 400, 0x4000, 64, None, None,
+    assert lib.indexer_forward(ctypes.byref(d), 0x1000, 0x2000, 1, 1000, 0, 0x3000, 1000, 0x4000, 128, None, None,
                                0x5000, None, 0x6000, 1 << 20, None) == -4
-    # workspace too small
+    # cache capacity that is not a whole number of 128-key pages
     assert lib.indexer_forward(ctypes.byref(d), 0x1000, 0x2000, 1, 8, 0, 0x3000, 64, 0x4000, 64, None, None,
+                               0x5000, None, 0x6000, 1 << 20, None) == -2
+    # workspace too small
+    assert lib.indexer_forward(ctypes.byref(d), 0x1000, 0x2000, 1, 8, 0, 0x3000, 64, 0x4000, 128, None, None,
                                0x5000, None, 0x6000, 16, None) == -5
     # decode publish on a token that does not complete a group
-    assert lib.indexer_publish_k(ctypes.byref(d), 0x1000, 1, 1, 128, 0x2000, 0x3000, 0x4000, 100, 10, 0x5000, 64,
+    assert lib.indexer_publish_k(ctypes.byref(d), 0x1000, 1, 1, 128, 0x2000, 0x3000, 0x4000, 100, 10, 0x5000, 128,
                                  None) == -4
     # RoPE positions beyond the table
     assert lib.indexer_prep_q(ctypes.byref(d), 0x1000, 0x2000, 1, 8, 0, 0x3000, 4, 0x4000, 0x5000, None) == -4

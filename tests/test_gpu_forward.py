@@ -56,7 +56,7 @@ def test_forward_full_compare(X, name):
     cos, sin = C.oracle_table(wl.max_pos)
     cache = C.gpu_cache(wl, table)
     ref_cache = C.oracle_cache(wl, cos, sin)
-    assert np.array_equal(cache.cpu().numpy(), ref_cache)
+    assert np.array_equal(C.pages_to_rows(cache), ref_cache)
     q, w = wl.q("cuda"), wl.w("cuda")
     top, _, sc = _run_forward(X, wl, q, w, table, cache)
     ref_top, _, ref_sc = O.forward(C.bits(q), C.bits(w), ref_cache, cos, sin, wl.start_pos, wl.ratio, wl.rope_dim,
@@ -74,7 +74,7 @@ def test_forward_two_level_decode(X):
     cos, sin = C.oracle_table(wl.max_pos)
     cache = C.gpu_cache(wl, table)
     ref_cache = C.oracle_cache(wl, cos, sin)
-    assert np.array_equal(cache.cpu().numpy(), ref_cache)
+    assert np.array_equal(C.pages_to_rows(cache), ref_cache)
     # level one: the candidate source layer (its own q, w) publishes its blocks and its top-k
     q1, w1 = wl.q("cuda", tag="q1"), wl.w("cuda", tag="w1")
     top1, cand, sc1 = _run_forward(X, wl, q1, w1, table, cache, want_cand=True)
@@ -126,7 +126,7 @@ def test_forward_prefill_sampled(X, name, n_rand):
     cos, sin = C.oracle_table(wl.max_pos)
     cache = C.gpu_cache(wl, table)
     ref_cache = C.oracle_cache(wl, cos, sin)
-    assert np.array_equal(cache.cpu().numpy(), ref_cache)
+    assert np.array_equal(C.pages_to_rows(cache), ref_cache)
     q, w = wl.q("cuda"), wl.w("cuda")
     top, _, sc = _run_forward(X, wl, q, w, table, cache, want_scores=(name == "prefill"))
     top_np = top.cpu().numpy()
@@ -158,12 +158,12 @@ def test_forward_edges(X, S, start, topk):
                              H=32)
     table = C.gpu_table(max(wl.max_pos, 8))
     cos, sin = C.oracle_table(max(wl.max_pos, 8))
-    T_cap = max(4, wl.T_cap)
-    cache = torch.zeros((wl.B, T_cap, 68), dtype=torch.uint8, device="cuda")
+    T_cap = max(128, wl.T_cap)
+    cache = X.new_key_cache(wl.B, T_cap)
     ref_cache = np.zeros((wl.B, T_cap, 68), np.uint8)
     if wl.T > 0:
-        cache[:, :wl.T_cap] = C.gpu_cache(wl, table)
-        ref_cache[:, :wl.T_cap] = C.oracle_cache(wl, cos, sin)
+        cache = C.gpu_cache(wl, table)
+        ref_cache = C.oracle_cache(wl, cos, sin)
     q, w = wl.q("cuda"), wl.w("cuda")
     top, _, sc = _run_forward(X, wl, q, w, table, cache, want_scores=wl.T > 0)
     ref_top, _, ref_sc = O.forward(C.bits(q), C.bits(w), ref_cache, cos, sin, wl.start_pos, wl.ratio, wl.rope_dim,

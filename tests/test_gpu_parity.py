@@ -45,7 +45,7 @@ def test_publish_prefill_bit_exact(X, B, G):
     wl = dataclasses.replace(WORKLOADS["tiny_prefill"], name=f"pub{B}x{G}", B=B, S=G * 4)
     table = C.gpu_table(wl.max_pos)
     cos, sin = C.oracle_table(wl.max_pos)
-    got = C.gpu_cache(wl, table).cpu().numpy()
+    got = C.pages_to_rows(C.gpu_cache(wl, table))
     ref = C.oracle_cache(wl, cos, sin)
     assert np.array_equal(got, ref), f"{np.sum(np.any(got != ref, axis=-1))} rows differ"
 
@@ -54,10 +54,10 @@ def test_publish_decode_slot(X):
     wl = dataclasses.replace(WORKLOADS["decode"], B=2, name="pubdec")
     table = C.gpu_table(wl.max_pos)
     cos, sin = C.oracle_table(wl.max_pos)
-    cache = torch.zeros((wl.B, wl.T_cap, 68), dtype=torch.uint8, device="cuda")
+    cache = X.new_key_cache(wl.B, wl.T_cap)
     lat = wl.decode_latent("cuda")
     X.indexer_publish_k(C.dims_of(wl), lat, wl.wk("cuda"), wl.k_norm_w("cuda"), table, wl.start_pos, cache)
-    got = cache.cpu().numpy()
+    got = C.pages_to_rows(cache)
     slots, rows, _ = O.publish_keys(C.bits(lat), C.bits(wl.wk()), C.bits(wl.k_norm_w()), cos, sin, wl.start_pos,
                                     wl.ratio, wl.rope_dim, wl.norm_eps)
     assert list(slots) == [8191]
@@ -100,7 +100,7 @@ def _scores_case(X, wl: Workload, cand=None):
     cos, sin = C.oracle_table(wl.max_pos)
     cache = C.gpu_cache(wl, table)
     ref_cache = C.oracle_cache(wl, cos, sin)
-    assert np.array_equal(cache.cpu().numpy(), ref_cache)
+    assert np.array_equal(C.pages_to_rows(cache), ref_cache)
     q, w = wl.q("cuda"), wl.w("cuda")
     d = C.dims_of(wl)
     rows = torch.empty((wl.B, wl.S, wl.H, 68), dtype=torch.uint8, device="cuda")

@@ -69,7 +69,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(X):
     q = torch.zeros((wl.B, wl.S, wl.H, wl.D), dtype=torch.bfloat16, device="cuda")
     w = torch.zeros((wl.B, wl.S, wl.H), dtype=torch.bfloat16, device="cuda")
     table = torch.zeros((wl.max_pos, 32, 2), dtype=torch.float32, device="cuda")
-    cache = torch.zeros((wl.B, wl.T_cap, 68), dtype=torch.uint8, device="cuda")
+    cache = X.new_key_cache(wl.B, wl.T_cap)
     top = torch.empty((wl.B, wl.S, wl.topk), dtype=torch.int32, device="cuda")
     with pytest.raises(X.IndexerError) as err:
         X.indexer_forward_noalloc(d, q, w, 0, table, cache, top)
