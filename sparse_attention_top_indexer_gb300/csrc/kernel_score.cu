@@ -8,20 +8,19 @@
 // One CTA (256 threads) takes a group of QG query rows of one sequence and a run of
 // 128-key pages of the paged key cache. A page already holds its codes in the tensor
 // cores' K-major core-matrix order, so the MMA reads the A operand straight from the
-// stage buffer the page was bulk-copied into:
-//   * producer (warp 1, lane 0): one bulk copy (cp.async.bulk) per page into a ring of
-//     NSTAGE stage buffers; the first NSTAGE pages are requested at kernel start, the rest
-//     as soon as the MMA that read a stage has completed;
-//   * MMA issuer (warp 0, lane 0): per page, two block-scaled MMAs (K = 64 each) from the
-//     stage buffer into one of NACC f32 accumulators, committed to an mbarrier;
-//   * epilogue (warps 4-7): thread m owns key t0 + m (TMEM lane m); it reads the N head
-//     dot products with tcgen05.ld and forms sum_h w' * max(dot, 0) per query row in f32
-//     -- no shuffles, because keys, not heads, sit on the lanes. Having drained
-//     accumulator c it also writes, with tcgen05.st, the A scale factors of the next page
-//     that will use c (its key's scale word, from that page's stage buffer), then
-//     releases c to the MMA issuer.
-// B operand (N = QG * H, padded to 16): the group's quantised query rows, rewritten once
-// per CTA into the same core-matrix order; their scale factors go to tensor memory.
+// stage buffer the page was bulk-copied into (cp.async.bulk, one copy per page, into a
+// ring of NSTAGE stages):
+//   * MMA warpgroup (warps 0-3): rewrites the group's quantised query rows into the same
+//     core-matrix order once (the B operand, N = QG * H padded to 16) and stores their
+//     scale factors in tensor memory; then, per page, each warp stores the A scale factors
+//     of its 32 keys (tcgen05.st into its lane quadrant), the four warps meet at a named
+//     barrier, and one thread issues two block-scaled MMAs (K = 64 each) into one of NACC
+//     f32 accumulators, committed to an mbarrier;
+//   * epilogue warpgroup (warps 4-7): thread m owns key t0 + m (TMEM lane m); it reads the
+//     N head dot products with tcgen05.ld, releases the accumulator, and forms
+//     sum_h w' * max(dot, 0) per query row in f32 -- no shuffles, because keys, not heads,
+//     sit on the lanes. Once a page's MMA has completed, its stage is refilled from here.
+// Only lane 0 of a warp polls an mbarrier; the warp follows through __syncwarp.
 //
 // Tensor-memory scale layout: the MMA reads the scale factors of A row m from lane m,
 // column m / 32 of the scale set, and those of B row n = 32 j + i from column j, lane i of
@@ -47,6 +46,13 @@ __host__ __device__ constexpr uint32_t pow2_cols(int n) {
   return n <= 32 ? 32u : n <= 64 ? 64u : n <= 128 ? 128u : n <= 256 ? 256u : 512u;
 }
 
+// most accumulators (at most 4) whose columns, with their A scale sets and the B
+// scales, fit in `budget` tensor-memory columns
+__host__ __device__ constexpr int max_acc(int NP, int SB, int budget) {
+  return 4 * (NP + 8) + 2 * SB <= budget ? 4 : 3 * (NP + 8) + 2 * SB <= budget ? 3
+       : 2 * (NP + 8) + 2 * SB <= budget ? 2 : 1 * (NP + 8) + 2 * SB <= budget ? 1 : 0;
+}
+
 template <int H, int QG>
 struct ScoreCfg {
   static constexpr int N = QG * H;
@@ -54,8 +60,9 @@ struct ScoreCfg {
   static constexpr int NCB = (NP + 31) / 32;                 // B scale columns per half
   static constexpr int SB = round_up(NCB, 4);
   // tensor memory: NACC accumulators of NP columns, NACC A scale sets of 8 columns, two
-  // halves of SB B scale columns; every scale address is a multiple of 4 columns
-  static constexpr int NACC = (2 * NP + 16 + 2 * SB <= 512) ? 2 : 1;
+  // halves of SB B scale columns; every scale address is a multiple of 4 columns. Two or
+  // more accumulators within 256 columns let two CTAs share an SM.
+  static constexpr int NACC = max_acc(NP, SB, 256) >= 2 ? max_acc(NP, SB, 256) : max_acc(NP, SB, 512);
   static constexpr int SFA_COL = NACC * NP;
   static constexpr int SFB_COL = SFA_COL + 8 * NACC;
   static constexpr int TMEM_NEED = SFB_COL + 2 * SB;
@@ -63,13 +70,16 @@ struct ScoreCfg {
   static constexpr int NSTAGE = 8;
   static constexpr int OFF_QB = 0;
   static constexpr int OFF_STG = round_up(NP * kCodeBytes, 1024);
-  static constexpr int OFF_W = OFF_STG + NSTAGE * kStageStride;
+  static constexpr int OFF_QSTG = OFF_STG + NSTAGE * kStageStride;          // raw query rows
+  static constexpr int OFF_W = OFF_QSTG + round_up(N * kRowBytes, 16);
   static constexpr int OFF_SFW = OFF_W + round_up(N * 4, 16);
-  static constexpr int NBAR = 2 * NSTAGE + 2 * NACC;                          // full, free, done, empty
+  static constexpr int NBAR = NSTAGE + 2 * NACC + 1;                          // full, done, empty, q
   static constexpr int OFF_BAR = round_up(OFF_SFW + NCB * 32 * 4, 8);
   static constexpr int OFF_INFO = OFF_BAR + NBAR * 8;                         // tmem base, counters
   static constexpr int OFF_CAND = round_up(OFF_INFO + 16, 16);
   static_assert(N <= 256, "MMA N is at most 256");
+  static_assert(NACC >= 1, "tensor memory budget");
+  static_assert(NBAR <= 32, "barriers are initialised by the lanes of one warp");
   static_assert(SFA_COL % 4 == 0 && SFB_COL % 4 == 0 && SB % 4 == 0, "scale sets must be 4-column aligned");
   static_assert(TMEM_NEED <= (int)TMEM_COLS && TMEM_COLS <= 512u, "tensor memory budget");
 };
@@ -81,12 +91,13 @@ __device__ __forceinline__ void issue_page_load(const ScoreArgs& a, int b, int t
            bar);
 }
 
-// Epilogue thread et: the A scale factors of key et of the page in stage `st` into scale
-// set c (bytes 0/1 of its scale word in columns 0-3, bytes 2/3 in columns 4-7 of lane et).
-__device__ __forceinline__ void write_sfa(uint32_t tq_set, const uint8_t* page, int et) {
-  const uint32_t w = *reinterpret_cast<const uint32_t*>(page + page_scale_offset(et));
-  const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
-  tmem_st_x8(tq_set, lo, lo, lo, lo, hi, hi, hi, hi);
+// Lane 0 waits (bounded) for the phase; the warp follows it. Warp-uniform result.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok = 1u;
+  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity) ? 1u : 0u;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0u;
 }
 
 template <int H, int QG>
@@ -118,108 +129,109 @@ __global__ void __launch_bounds__(kThreads, ScoreCfg<H, QG>::TMEM_COLS <= 256 ? 
 
   uint8_t* qB = smem + C::OFF_QB;
   const uint8_t* stg = smem + C::OFF_STG;
+  const uint8_t* qstg = smem + C::OFF_QSTG;
   float* wq = reinterpret_cast<float*>(smem + C::OFF_W);
   uint32_t* sfw = reinterpret_cast<uint32_t*>(smem + C::OFF_SFW);
-  uint32_t* info = reinterpret_cast<uint32_t*>(smem + C::OFF_INFO);   // [0] tmem, [1] issued, [2] mma issued
+  uint32_t* info = reinterpret_cast<uint32_t*>(smem + C::OFF_INFO);   // [0] tmem, [1] pages issued, [2] mma issued
   uint32_t* cand_bits = reinterpret_cast<uint32_t*>(smem + C::OFF_CAND);
   const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
   auto bar_full = [&](int st) { return bar0 + 8u * (uint32_t)st; };
-  auto bar_free = [&](int st) { return bar0 + 8u * (uint32_t)(C::NSTAGE + st); };
-  auto bar_done = [&](int c) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + c); };
-  auto bar_empty = [&](int c) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + C::NACC + c); };
+  auto bar_done = [&](int c) { return bar0 + 8u * (uint32_t)(C::NSTAGE + c); };
+  auto bar_empty = [&](int c) { return bar0 + 8u * (uint32_t)(C::NSTAGE + C::NACC + c); };
+  const uint32_t bar_q = bar0 + 8u * (uint32_t)(C::NSTAGE + 2 * C::NACC);
   const uint32_t stg0 = smem_u32(stg);
 
-  if (tid == 0) {
-    for (int i = 0; i < 2 * C::NSTAGE + C::NACC; ++i) mbar_init(bar0 + 8u * i, 1);
-    for (int c = 0; c < C::NACC; ++c) mbar_init(bar_empty(c), kEpiThreads);
-    fence_mbar_init();
-    const int first = min(nt, C::NSTAGE);
-    for (int i = 0; i < first; ++i) issue_page_load(a, b, tile0 + i, stg0 + i * kStageStride, bar_full(i));
-    info[1] = (uint32_t)first;
-    info[2] = 0u;
-  }
-  __syncwarp();
+  // Setup: warp 0 initialises the barriers and requests the group's query rows and head
+  // weights, then the first NSTAGE pages (one lane per page); warp 1 allocates tensor
+  // memory meanwhile.
+  const size_t qrow0 = ((size_t)b * a.S + s0) * H;   // first query row of the group
+  const int first = min(nt, C::NSTAGE);
   if (warp == 0) {
+    if (lane < C::NBAR) {
+      const bool empty_bar = lane >= C::NSTAGE + C::NACC && lane < C::NSTAGE + 2 * C::NACC;
+      mbar_init(bar0 + 8u * (uint32_t)lane, empty_bar ? (uint32_t)kEpiThreads : 1u);
+      fence_mbar_init();
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t qbytes = (uint32_t)(nq * H * kRowBytes), wbytes = (uint32_t)(nq * H * 4);
+      mbar_arrive_expect_tx(bar_q, qbytes + wbytes);
+      bulk_g2s(smem_u32(qstg), a.q_rows + qrow0 * kRowBytes, qbytes, bar_q);
+      bulk_g2s(smem_u32(wq), a.w_prime + qrow0, wbytes, bar_q);
+      info[1] = (uint32_t)first;
+      info[2] = 0u;
+    }
+    __syncwarp();
+    if (lane < first) issue_page_load(a, b, tile0 + lane, stg0 + lane * kStageStride, bar_full(lane));
+    __syncwarp();
+  } else if (warp == 1) {
     tmem_alloc(smem_u32(&info[0]), C::TMEM_COLS);
     tmem_relinquish();
-  }
-  // head weights of the group (0 for rows past S)
-  for (int n = tid; n < C::N; n += kThreads) {
-    const int qi = n / H;
-    wq[n] = qi < nq ? a.w_prime[((size_t)b * a.S + s0 + qi) * H + (n % H)] : 0.f;
-  }
-  // quantised query rows -> B operand (core-matrix order) and scale words
-  for (int n = tid; n < C::NCB * 32; n += kThreads) {
-    uint32_t w[16];
-    uint32_t sc = 0x7F7F7F7Fu;
-    if (n < C::N && n / H < nq) {
-      const uint32_t* src =
-          reinterpret_cast<const uint32_t*>(a.q_rows + (((size_t)b * a.S + s0 + n / H) * H + (n % H)) * kRowBytes);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = src[i];
-      sc = src[16];
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) w[i] = 0u;
-    }
-    if (n < C::NP) {
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        *reinterpret_cast<uint4*>(qB + (n >> 3) * 512 + c * 128 + (n & 7) * 16) =
-            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-    }
-    sfw[n] = sc;
-  }
-  // level-two candidate filter: one bit per block of cbs positions, per query row
-  const int cand_words = a.cand ? ((a.T + a.cbs - 1) / a.cbs + 31) / 32 : 0;
-  if (a.cand) {
-    for (int i = tid; i < QG * cand_words; i += kThreads) cand_bits[i] = 0u;
-    __syncthreads();
-    for (int i = tid; i < nq * a.cbk; i += kThreads) {
-      const int qi = i / a.cbk;
-      const int blk = a.cand[((size_t)b * a.S + s0 + qi) * a.cbk + (i % a.cbk)];
-      if (blk >= 0 && blk < cand_words * 32) atomicOr(&cand_bits[qi * cand_words + (blk >> 5)], 1u << (blk & 31));
-    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = info[0];
   const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);   // this warp's lane quadrant
-  if (warp < 4) {
-    __syncwarp();
-#pragma unroll
-    for (int j = 0; j < C::NCB; ++j) {
-      const uint32_t wd = sfw[32 * j + lane];
-      tmem_st_x1(tq + C::SFB_COL + j, wd & 0xFFFFu);
-      tmem_st_x1(tq + C::SFB_COL + C::SB + j, wd >> 16);
-    }
-    tmem_wait_st();
-  }
-  fence_proxy_async_smem();   // the B operand was written by ordinary stores
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
 
-  // Role loops are warp-uniform: every lane of a role warp runs the loop and takes the
-  // same branches (waits are made uniform with __all_sync), and only lane 0 issues the
-  // copies, MMAs and commits. No warp reaches a CTA-wide barrier partly diverged.
   bool failed = false;
-  if (warp == 0) {
-    // ------------------------------------------------------------ MMA issuer (lane 0)
+  if (warp < 4) {
+    // ------------------------------------------------------------ MMA warpgroup
+    // query rows -> B operand (core-matrix order) and B scales
+    failed = !named_bar_and(1, 128, warp_wait(bar_q, 0u));
+    if (!failed) {
+      for (int n = tid; n < C::NCB * 32; n += 128) {
+        uint32_t w[16];
+        uint32_t sc = 0x7F7F7F7Fu;
+        if (n < nq * H) {
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(qstg + n * kRowBytes);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = src[i];
+          sc = src[16];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = 0u;
+        }
+        if (n < C::NP) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(qB + (n >> 3) * 512 + c * 128 + (n & 7) * 16) =
+                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        }
+        sfw[n] = sc;
+      }
+      fence_proxy_async_smem();   // the B operand was written by ordinary stores
+      named_bar_sync(1, 128);
+#pragma unroll
+      for (int j = 0; j < C::NCB; ++j) {
+        const uint32_t wd = sfw[32 * j + lane];
+        tmem_st_x1(tq + C::SFB_COL + j, wd & 0xFFFFu);
+        tmem_st_x1(tq + C::SFB_COL + C::SB + j, wd >> 16);
+      }
+    }
     const uint32_t idesc = idesc_mxf4(128, C::NP);
     const uint32_t qb = smem_u32(qB);
-    for (int i = 0; i < nt; ++i) {
+    const int key = (warp << 5) | lane;   // this thread's key (TMEM lane) within a page
+    for (int i = 0; i < nt && !failed; ++i) {
       const int st = i % C::NSTAGE, c = i % C::NACC;
-      // the page has landed, and accumulator c is drained and holds this page's A scales
-      bool ok = mbar_wait(bar_full(st), (uint32_t)(i / C::NSTAGE) & 1u);
-      ok = ok && mbar_wait(bar_empty(c), (uint32_t)(i / C::NACC) & 1u);
-      if (!__all_sync(0xffffffffu, ok)) {
+      // the page has landed, and accumulator c (with its scale set) has been drained
+      bool ok = warp_wait(bar_full(st), (uint32_t)(i / C::NSTAGE) & 1u);
+      if (ok && i >= C::NACC) ok = warp_wait(bar_empty(c), (uint32_t)((i - C::NACC) / C::NACC) & 1u);
+      if (!named_bar_and(1, 128, ok)) {
         failed = true;
         break;
       }
       tc_fence_after();
-      if (lane == 0) {
+      {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(stg + st * kStageStride + page_scale_offset(key));
+        const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
+        tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * c), lo, lo, lo, lo, hi, hi, hi, hi);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      named_bar_sync(1, 128);
+      if (tid == 0) {
+        tc_fence_after();
         const uint32_t pa = stg0 + (uint32_t)(st * kStageStride);
         const uint32_t acc = tmem + (uint32_t)(c * C::NP);
         const uint32_t sfa = tmem + (uint32_t)(C::SFA_COL + 8 * c);
@@ -227,46 +239,33 @@ __global__ void __launch_bounds__(kThreads, ScoreCfg<H, QG>::TMEM_COLS <= 256 ? 
         mma_mxf4(acc, smem_desc(pa + 256, 128, 512), smem_desc(qb + 256, 128, 512), idesc, sfa + 4,
                  tmem + C::SFB_COL + C::SB, 1u);
         tc_commit(bar_done(c));
-        if (i + C::NSTAGE < nt) tc_commit(bar_free(st));
         info[2] = (uint32_t)(i + 1);
       }
       __syncwarp();
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ producer (lane 0): stage refills
-    for (int j = C::NSTAGE; j < nt; ++j) {
-      const int st = j % C::NSTAGE;
-      const bool ok = mbar_wait(bar_free(st), (uint32_t)((j - C::NSTAGE) / C::NSTAGE) & 1u);
-      if (!__all_sync(0xffffffffu, ok)) {
-        failed = true;
-        break;
-      }
-      if (lane == 0) {
-        issue_page_load(a, b, tile0 + j, stg0 + st * kStageStride, bar_full(st));
-        info[1] = (uint32_t)(j + 1);
-      }
-      __syncwarp();
-    }
-  } else if (warp >= 4) {
-    // ------------------------------------------------------------ epilogue
+  } else {
+    // ------------------------------------------------------------ epilogue warpgroup
     constexpr int P = H >= 32 ? 4 : (H >= 16 ? 2 : 1);   // independent partial sums per row
     const int et = tid - 128;   // key within the page == TMEM lane
-    // A scales of the first NACC pages, one scale set per accumulator
-    for (int p = 0; p < min(nt, C::NACC); ++p) {
-      const bool ok = mbar_wait(bar_full(p), 0u);
-      if (!__all_sync(0xffffffffu, ok)) {
-        failed = true;
-        break;
+    // level-two candidate filter: one bit per block of cbs positions, per query row
+    const int cand_words = a.cand ? ((a.T + a.cbs - 1) / a.cbs + 31) / 32 : 0;
+    if (a.cand) {
+      for (int i = et; i < QG * cand_words; i += kEpiThreads) cand_bits[i] = 0u;
+      named_bar_sync(2, kEpiThreads);
+      for (int i = et; i < nq * a.cbk; i += kEpiThreads) {
+        const int qi = i / a.cbk;
+        const int blk = a.cand[((size_t)b * a.S + s0 + qi) * a.cbk + (i % a.cbk)];
+        if (blk >= 0 && blk < cand_words * 32) atomicOr(&cand_bits[qi * cand_words + (blk >> 5)], 1u << (blk & 31));
       }
-      write_sfa(tq + (uint32_t)(C::SFA_COL + 8 * p), stg + p * kStageStride, et);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_empty(p));
     }
+    // head weights (rows past S weigh nothing)
+    failed = !warp_wait(bar_q, 0u);
+    if (!failed)
+      for (int n = nq * H + et; n < C::N; n += kEpiThreads) wq[n] = 0.f;
+    named_bar_sync(2, kEpiThreads);
     for (int i = 0; i < nt && !failed; ++i) {
       const int c = i % C::NACC;
-      const bool ok = mbar_wait(bar_done(c), (uint32_t)(i / C::NACC) & 1u);
-      if (!__all_sync(0xffffffffu, ok)) {
+      if (!warp_wait(bar_done(c), (uint32_t)(i / C::NACC) & 1u)) {
         failed = true;
         break;
       }
@@ -276,29 +275,41 @@ __global__ void __launch_bounds__(kThreads, ScoreCfg<H, QG>::TMEM_COLS <= 256 ? 
       for (int qi = 0; qi < QG; ++qi)
 #pragma unroll
         for (int p = 0; p < P; ++p) part[qi][p] = 0.f;
+      if constexpr (C::NCB <= 2) {
+        // small N: read the whole accumulator, release it, then reduce
+        float v[C::NCB][32];
 #pragma unroll
-      for (int k = 0; k < C::NCB; ++k) {
-        float v[32];
-        tmem_ld32(tq + (uint32_t)(c * C::NP + 32 * k), v);
+        for (int k = 0; k < C::NCB; ++k) tmem_ld32(tq + (uint32_t)(c * C::NP + 32 * k), v[k]);
+        tc_fence_before();
+        mbar_arrive(bar_empty(c));   // accumulator c and its scale set may be reused
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int n = 32 * k + jj;
-          if (n < C::N) part[n / H][n % P] = fmaf(wq[n], fmaxf(v[jj], 0.f), part[n / H][n % P]);
+        for (int k = 0; k < C::NCB; ++k)
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int n = 32 * k + jj;
+            if (n < C::N) part[n / H][n % P] = fmaf(wq[n], fmaxf(v[k][jj], 0.f), part[n / H][n % P]);
+          }
+      } else {
+        // large N: reduce 32 columns at a time, release after the last read
+#pragma unroll
+        for (int k = 0; k < C::NCB; ++k) {
+          float v[32];
+          tmem_ld32(tq + (uint32_t)(c * C::NP + 32 * k), v);
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int n = 32 * k + jj;
+            if (n < C::N) part[n / H][n % P] = fmaf(wq[n], fmaxf(v[jj], 0.f), part[n / H][n % P]);
+          }
         }
+        tc_fence_before();
+        mbar_arrive(bar_empty(c));
       }
-      const int inext = i + C::NACC;   // the next page to use accumulator c
-      if (inext < nt) {
-        const int sn = inext % C::NSTAGE;
-        const bool okn = mbar_wait(bar_full(sn), (uint32_t)(inext / C::NSTAGE) & 1u);
-        if (!__all_sync(0xffffffffu, okn)) {
-          failed = true;
-          break;
-        }
-        write_sfa(tq + (uint32_t)(C::SFA_COL + 8 * c), stg + sn * kStageStride, et);
-        tmem_wait_st();
+      if (et == 0 && i + C::NSTAGE < nt) {
+        // the MMA that read this page's stage has completed: refill it
+        issue_page_load(a, b, tile0 + i + C::NSTAGE, stg0 + (i % C::NSTAGE) * kStageStride,
+                        bar_full(i % C::NSTAGE));
+        info[1] = (uint32_t)(i + C::NSTAGE + 1);
       }
-      tc_fence_before();
-      if (inext < nt) mbar_arrive(bar_empty(c));   // accumulator c drained, next scales in place
       const int t0 = (tile0 + i) * kTileKeys;
       const int nv = min(kTileKeys, a.T - t0);
       if (et < nv) {
@@ -323,23 +334,24 @@ __global__ void __launch_bounds__(kThreads, ScoreCfg<H, QG>::TMEM_COLS <= 256 ? 
       __syncwarp();
     }
   }
-  if (failed && (tid == 0 || tid == 32 || tid == 128))
-    atomicOr(a.status, tid == 128 ? kStatusMmaTimeout : kStatusLoadTimeout);
   __syncwarp();
-  __syncthreads();
-  if (tid == 0) {
-    // bounded waits for copies and MMAs still in flight before shared and tensor memory go away
-    const int issued = (int)info[1], mmas = (int)info[2];
-    for (int st = 0; st < C::NSTAGE && st < issued; ++st) {
-      const int last = st + ((issued - 1 - st) / C::NSTAGE) * C::NSTAGE;   // last page loaded into st
-      mbar_wait(bar_full(st), (uint32_t)(last / C::NSTAGE) & 1u);
+  if (failed && (tid == 0 || tid == 128)) atomicOr(a.status, tid == 0 ? kStatusLoadTimeout : kStatusMmaTimeout);
+  // On success every copy and MMA has been waited for by its consumer; after a failure,
+  // bounded waits for whatever may still be in flight before shared and tensor memory go.
+  if (__syncthreads_or(failed)) {
+    if (tid == 0) {
+      const int issued = (int)info[1], mmas = (int)info[2];
+      mbar_wait(bar_q, 0u);
+      for (int st = 0; st < C::NSTAGE && st < issued; ++st) {
+        const int last = st + ((issued - 1 - st) / C::NSTAGE) * C::NSTAGE;   // last page loaded into st
+        mbar_wait(bar_full(st), (uint32_t)(last / C::NSTAGE) & 1u);
+      }
+      if (mmas > 0) mbar_wait(bar_done((mmas - 1) % C::NACC), (uint32_t)((mmas - 1) / C::NACC) & 1u);
     }
-    if (mmas > 0) mbar_wait(bar_done((mmas - 1) % C::NACC), (uint32_t)((mmas - 1) / C::NACC) & 1u);
+    __syncthreads();
   }
-  __syncwarp();
-  __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 int sm_count() {
