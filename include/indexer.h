@@ -202,7 +202,8 @@ int indexer_topk(const IndexerDims* dims, const float* scores, int B, int S, int
  *   cand_in / cand_out:     int32 [B][S][cand_topk_blocks] or NULL
  *   topk_out:               int32 [B][S][index_topk]
  *   scores_out:             float [B][S][T] or NULL (the masked scores)
- *   ws / ws_bytes:          workspace, at least indexer_workspace_size()
+ *   ws / ws_bytes:          workspace, at least indexer_workspace_size(),
+ *                           initialised once by indexer_workspace_init
  * ------------------------------------------------------------------------- */
 int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
                     int start_pos, const float* rope_cs, int max_pos, const uint8_t* k_cache, int T_cap,

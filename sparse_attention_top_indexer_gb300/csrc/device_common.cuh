@@ -125,6 +125,59 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
   return ok != 0u;
 }
+// ----------------------------------------------------------------------------- query prep
+// RoPE table entries (cos, sin) of the 4 element pairs of slice j (0..15) of a
+// 128-element head vector; pairs outside the last rope_dim elements get (1, 0), which
+// the rotation below never reads.
+__device__ __forceinline__ void load_rope_slice(const float2* cs_row, int j, int rope_dim, float2 (&c)[4]) {
+  const int rstart = kHeadDim - rope_dim;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e0 = j * 8 + 2 * k;
+    c[k] = e0 >= rstart ? cs_row[(e0 - rstart) >> 1] : make_float2(1.f, 0.f);
+  }
+}
+
+// One 8-element slice j (0..15) of a 128-element query-head vector, given as 8 bf16 in
+// `raw`: RoPE on the last rope_dim elements with the slice's table entries c (from
+// load_rope_slice; interleaved pairs rotated with the f32 sequence x0*c - x1*s,
+// x0*s + x1*c, each rounded to bf16), then e2m1 with the 32-block's e8m0 scale. Returns
+// the 4 code bytes (element 2i in the low nibble of byte i) and the block's scale
+// exponent in *e. The 4 threads of a 32-block (lanes 4i..4i+3 of a 16-lane half named by
+// gmask) must call it together: they share the block amax.
+__device__ __forceinline__ uint32_t quant_q_slice(uint4 raw, int j, const float2 (&c)[4], int rope_dim,
+                                                  unsigned gmask, int* e) {
+  const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
+  float x[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    x[2 * k] = bf16_to_f32(wds[k] & 0xFFFFu);
+    x[2 * k + 1] = bf16_to_f32(wds[k] >> 16);
+  }
+  const int rstart = kHeadDim - rope_dim;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e0 = j * 8 + 2 * k;   // even element; rstart is even so pairs never straddle
+    if (e0 >= rstart) {
+      const float x0 = x[2 * k], x1 = x[2 * k + 1];
+      x[2 * k] = bf16_to_f32(f32_to_bf16_rne(__fsub_rn(__fmul_rn(x0, c[k].x), __fmul_rn(x1, c[k].y))));
+      x[2 * k + 1] = bf16_to_f32(f32_to_bf16_rne(__fadd_rn(__fmul_rn(x0, c[k].y), __fmul_rn(x1, c[k].x))));
+    }
+  }
+  uint32_t amax = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) amax = max(amax, (__float_as_uint(x[k]) >> 16) & 0x7FFFu);
+  amax = max(amax, __shfl_xor_sync(gmask, amax, 1));
+  amax = max(amax, __shfl_xor_sync(gmask, amax, 2));
+  const int ex = e8m0_exponent(amax);
+  const float sc = pow2_neg(ex);
+  uint32_t word = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) word |= e2m1x2(__fmul_rn(x[2 * k], sc), __fmul_rn(x[2 * k + 1], sc)) << (8 * k);
+  *e = ex;
+  return word;
+}
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

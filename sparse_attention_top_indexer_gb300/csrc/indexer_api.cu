@@ -91,6 +91,7 @@ struct WsLayout {
   size_t q_rows, w_prime, scores, total;
 };
 
+// status header | query rows | w' | scores
 WsLayout ws_layout(const IndexerDims* d, int B, int S, int start_pos) {
   WsLayout l;
   const size_t nvec = (size_t)B * S * d->n_heads;
@@ -122,7 +123,7 @@ extern "C" {
 
 const char* indexer_last_error(void) { return g_last_error.c_str(); }
 
-int indexer_abi_version(void) { return 100; }
+int indexer_abi_version(void) { return 200; }
 
 // ---------------------------------------------------------------------------- RoPE table
 int indexer_rope_table(const IndexerYarn* y, int rope_dim, int max_pos, float* table, indexer_stream_t stream) {

@@ -338,7 +338,8 @@ __global__ void __launch_bounds__(kThreads, ScoreCfg<H, QG>::TMEM_COLS <= 256 ? 
   if (failed && (tid == 0 || tid == 128)) atomicOr(a.status, tid == 0 ? kStatusLoadTimeout : kStatusMmaTimeout);
   // On success every copy and MMA has been waited for by its consumer; after a failure,
   // bounded waits for whatever may still be in flight before shared and tensor memory go.
-  if (__syncthreads_or(failed)) {
+  const bool any_failed = __syncthreads_or(failed);
+  if (any_failed) {
     if (tid == 0) {
       const int issued = (int)info[1], mmas = (int)info[2];
       mbar_wait(bar_q, 0u);
@@ -371,8 +372,19 @@ cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
   using C = ScoreCfg<H, QG>;
   const int cand_words = a.cand ? ((a.T + a.cbs - 1) / a.cbs + 31) / 32 : 0;
   const size_t smem = (size_t)C::OFF_CAND + (size_t)QG * cand_words * 4 + 1024;   // + base alignment slack
-  cudaError_t err = cudaFuncSetAttribute(score_kernel<H, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // the attributes are set once per device and kernel (the dynamic size only grows)
+  static int set_bytes[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64 || set_bytes[dev] < (int)smem) {
+    err = cudaFuncSetAttribute(score_kernel<H, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(score_kernel<H, QG>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64) set_bytes[dev] = (int)smem;
+  }
   const int ntiles = (a.T + kTileKeys - 1) / kTileKeys;
   const int groups = (a.S + QG - 1) / QG;
   // resident CTAs per SM: tensor memory (512 columns) and shared memory (227 KB) both bound it

@@ -3,14 +3,17 @@
 // (0 = not selectable) keep the k largest, ties to the lower index, and emit their
 // indices in ascending order.
 //
-// Selection is a most-significant-digit radix select (four 8-bit digits, shared-memory
-// histograms) that pins the k-th largest key K*, followed by an ordered compaction:
-// every key > K* and the first `need` keys equal to K* (in index order) are written at
-// their prefix-sum slot, so the output comes out sorted by position without a sort.
+// Selection is a most-significant-digit radix select (shared-memory histograms) that
+// pins the k-th largest key K*, followed by an ordered compaction: every key > K* and the
+// first `need` keys equal to K* (in index order) are written at their prefix-sum slot, so
+// the output comes out sorted by position without a sort. The top-k kernel uses the
+// register-resident form in select_common.cuh; the candidate-block kernel keeps its keys
+// in shared memory.
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
 #include "launch.h"
+#include "select_common.cuh"
 
 namespace indexer {
 
@@ -18,13 +21,6 @@ namespace {
 
 constexpr int kSelThreads = 1024;
 constexpr int kSelWarps = kSelThreads / 32;
-
-// Larger float -> larger key; every finite value maps to a key >= 0x00800000 > 0.
-// -0.0 and +0.0 compare equal, so -0.0 is first folded onto +0.0 (x + 0 = +0 for x = -0).
-__device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = __float_as_uint(__fadd_rn(f, 0.0f));
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 // Adds 1 to hist[bin] for every lane whose `valid` is set, with one shared-memory atomic
 // per distinct bin per warp (lanes holding the same bin are combined first, so a few hot
@@ -158,32 +154,22 @@ __device__ void cta_select(const uint32_t* keys, int n, int k, int32_t* out, int
   for (int i = (int)sel_total + tid; i < width; i += kSelThreads) out[i] = -1;
 }
 
-struct TopkShared {
-  uint32_t hist[2][2048];    // double-buffered: one pass counts while the next is cleared
-  uint32_t warp_tot[kSelWarps];
-  uint32_t bc[4];            // bin, count above the bin, count in the bin, total
+struct TopkKept {
   uint32_t kept[kCandMaxBlocks / 32];
 };
-
-// Radix digits of the selection, most significant first: 11 + 11 + 10 bits. The first
-// digit (sign, exponent and two mantissa bits of the score) spreads typical score rows
-// over ~100 bins, so plain shared-memory atomics see little contention.
-__device__ __forceinline__ int digit_shift(int p) { return p == 0 ? 21 : (p == 1 ? 10 : 0); }
-__device__ __forceinline__ uint32_t digit_mask(int p) { return p == 2 ? 0x3FFu : 0x7FFu; }
 
 // One CTA (1024 threads) per query row; thread t holds the keys of positions
 // [t*KPT, (t+1)*KPT) in registers. Keys are the order-preserving images of the finite
 // scores at t < vis (inside the kept candidate blocks, if any), 0 otherwise. Up to three
-// radix passes pin the k_eff-th largest key; each pass counts into a 2048-bin histogram,
-// and a CTA-wide scan over the bins (two per thread, largest bins first) finds the bin
-// holding it. A pass stops the search early once its bin holds exactly the keys still
-// needed. One CTA-wide scan of packed (equal, greater) counts then gives every thread its
-// output slot, so the indices are written in position order. Rows with no candidate
-// filter and vis <= k_eff take the short-context fill [0 .. vis).
+// radix passes pin the k_eff-th largest key and an ordered compaction writes the indices
+// in position order (select_top). Rows with no candidate filter and vis <= k_eff take the
+// short-context fill [0 .. vis).
+
 template <int KPT>
 __global__ void __launch_bounds__(kSelThreads, 1) topk_kernel(const TopkArgs a) {
-  __shared__ TopkShared sh;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  __shared__ SelectShared<kSelThreads> sh;
+  __shared__ TopkKept kb;
+  const int tid = threadIdx.x;
   const int row = blockIdx.x;
   const int s = row % a.S;
   const int vis = min(a.T, (a.start_pos + s + 1) / a.ratio);
@@ -193,15 +179,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_kernel(const TopkArgs a) 
     for (int i = tid; i < a.topk; i += kSelThreads) out[i] = i < vis ? i + a.offset : -1;
     return;
   }
-  sh.hist[0][tid] = 0u;
-  sh.hist[0][tid + kSelThreads] = 0u;
   const int nblk_words = a.cand ? ((a.T + a.cbs - 1) / a.cbs + 31) / 32 : 0;
   if (a.cand) {
-    for (int i = tid; i < nblk_words; i += kSelThreads) sh.kept[i] = 0u;
+    for (int i = tid; i < nblk_words; i += kSelThreads) kb.kept[i] = 0u;
     __syncthreads();
     for (int i = tid; i < a.cbk; i += kSelThreads) {
       const int blk = a.cand[(size_t)row * a.cbk + i];
-      if (blk >= 0 && blk < nblk_words * 32) atomicOr(&sh.kept[blk >> 5], 1u << (blk & 31));
+      if (blk >= 0 && blk < nblk_words * 32) atomicOr(&kb.kept[blk >> 5], 1u << (blk & 31));
     }
   }
   __syncthreads();
@@ -212,7 +196,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_kernel(const TopkArgs a) 
     bool ok = t < vis && isfinite(f);
     if (ok && a.cand) {
       const int blk = t / a.cbs;
-      ok = (sh.kept[blk >> 5] >> (blk & 31)) & 1u;
+      ok = (kb.kept[blk >> 5] >> (blk & 31)) & 1u;
     }
     return ok ? order_key(f) : 0u;
   };
@@ -232,118 +216,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_kernel(const TopkArgs a) 
     for (int j = 0; j < KPT; ++j) key[j] = base + j < vis ? make_key(src[base + j], base + j) : 0u;
   }
 
-  uint32_t prefix = 0u, mask = 0u, need = (uint32_t)k_eff, kstar = 0u;
-  bool select_all = false, settled = false;
-#pragma unroll 1
-  for (int p = 0; p < 3; ++p) {
-    const int shift = digit_shift(p);
-    const uint32_t dm = digit_mask(p);
-    uint32_t* h = sh.hist[p & 1];
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-      const uint32_t k = key[j];
-      if (k != 0u && (k & mask) == prefix) atomicAdd(&h[(k >> shift) & dm], 1u);
-    }
-    __syncthreads();
-    // thread t owns bins hb = 2047 - 2t and hb - 1: an inclusive scan over threads counts
-    // the keys in all bins >= the thread's lower bin
-    const int hb = 2047 - 2 * tid;
-    const uint32_t c_hi = h[hb], c_lo = h[hb - 1];
-    uint32_t* nxt = sh.hist[(p + 1) & 1];
-    nxt[tid] = 0u;   // clear the next pass's buffer
-    nxt[tid + kSelThreads] = 0u;
-    const uint32_t own = c_hi + c_lo;
-    uint32_t incl = own;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += y;
-    }
-    if (lane == 31) sh.warp_tot[warp] = incl;
-    __syncthreads();
-    uint32_t wt = sh.warp_tot[lane];
-    uint32_t before_w = lane < warp ? wt : 0u;
-    uint32_t total = wt;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      before_w += __shfl_xor_sync(0xffffffffu, before_w, off);
-      total += __shfl_xor_sync(0xffffffffu, total, off);
-    }
-    const uint32_t above = before_w + incl - own;   // keys in bins above hb
-    if (need <= total && above < need && need <= above + own) {
-      if (above + c_hi >= need) {
-        sh.bc[0] = (uint32_t)hb;
-        sh.bc[1] = above;
-        sh.bc[2] = c_hi;
-      } else {
-        sh.bc[0] = (uint32_t)(hb - 1);
-        sh.bc[1] = above + c_hi;
-        sh.bc[2] = c_lo;
-      }
-    }
-    __syncthreads();
-    if (p == 0 && total <= need) {   // no more valid keys than k_eff: take them all
-      select_all = true;
-      break;
-    }
-    const uint32_t bin = sh.bc[0];
-    need -= sh.bc[1];
-    prefix |= bin << shift;
-    mask |= dm << shift;
-    if (sh.bc[2] == need) {   // the whole bin is taken: every key >= prefix
-      kstar = (prefix > 0u ? prefix : 1u) - 1u;
-      need = 0u;
-      settled = true;
-      break;
-    }
-  }
-  if (select_all) {
-    kstar = 0u;
-    need = 0u;
-  } else if (!settled) {
-    kstar = prefix;          // all 32 bits fixed; `need` keys equal to it are still taken
-  }
-
-  // ordered compaction: one scan of (equal << 16 | greater) per thread
-  uint32_t gt = 0u, eq = 0u;
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    gt += key[j] > kstar;
-    eq += (need != 0u && key[j] == kstar);
-  }
-  const uint32_t packed = (eq << 16) | gt;
-  uint32_t x = packed;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) sh.warp_tot[warp] = x;
-  __syncthreads();
-  const uint32_t wt = sh.warp_tot[lane];
-  uint32_t before_w = lane < warp ? wt : 0u;
-  uint32_t total = wt;
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    before_w += __shfl_xor_sync(0xffffffffu, before_w, off);
-    total += __shfl_xor_sync(0xffffffffu, total, off);
-  }
-  const uint32_t before = before_w + x - packed;
-  const uint32_t eq_before = before >> 16;
-  uint32_t slot = (before & 0xFFFFu) + min(eq_before, need);
-  uint32_t eq_seen = eq_before;
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    const uint32_t k = key[j];
-    if (k > kstar) {
-      out[slot++] = base + j + a.offset;
-    } else if (need != 0u && k == kstar) {
-      if (eq_seen < need) out[slot++] = base + j + a.offset;
-      ++eq_seen;
-    }
-  }
-  const int sel_total = (int)((total & 0xFFFFu) + min(total >> 16, need));
-  for (int i = sel_total + tid; i < a.topk; i += kSelThreads) out[i] = -1;
+  select_top<kSelThreads, KPT>(key, k_eff, out, a.topk, a.offset, sh, nullptr);
 }
 
 // One CTA per query row: block score = max finite score over the block's positions

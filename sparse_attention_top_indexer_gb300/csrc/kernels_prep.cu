@@ -173,35 +173,10 @@ __global__ void __launch_bounds__(256) prep_q_kernel(PrepArgs a) {
   const int s = (int)((v / a.H) % a.S);
   const int pos = a.start_pos + s;
   const uint4 raw = *reinterpret_cast<const uint4*>(a.q + v * kHeadDim + j * 8);
-  const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
-  float x[8];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    x[2 * k] = bf16_to_f32(wds[k] & 0xFFFFu);
-    x[2 * k + 1] = bf16_to_f32(wds[k] >> 16);
-  }
-  const int rstart = kHeadDim - a.rope_dim;
-  const float2* cs = reinterpret_cast<const float2*>(a.rope_cs) + (size_t)pos * (a.rope_dim / 2);
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int e0 = j * 8 + 2 * k;   // even element; rstart is even so pairs never straddle
-    if (e0 >= rstart) {
-      const float2 c = cs[(e0 - rstart) >> 1];
-      const float x0 = x[2 * k], x1 = x[2 * k + 1];
-      x[2 * k] = bf16_to_f32(f32_to_bf16_rne(__fsub_rn(__fmul_rn(x0, c.x), __fmul_rn(x1, c.y))));
-      x[2 * k + 1] = bf16_to_f32(f32_to_bf16_rne(__fadd_rn(__fmul_rn(x0, c.y), __fmul_rn(x1, c.x))));
-    }
-  }
-  uint32_t amax = 0;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) amax = max(amax, (__float_as_uint(x[k]) >> 16) & 0x7FFFu);
-  amax = max(amax, __shfl_xor_sync(gmask, amax, 1));
-  amax = max(amax, __shfl_xor_sync(gmask, amax, 2));
-  const int e = e8m0_exponent(amax);
-  const float sc = pow2_neg(e);
-  uint32_t word = 0;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) word |= e2m1x2(__fmul_rn(x[2 * k], sc), __fmul_rn(x[2 * k + 1], sc)) << (8 * k);
+  float2 c[4];
+  load_rope_slice(reinterpret_cast<const float2*>(a.rope_cs) + (size_t)pos * (a.rope_dim / 2), j, a.rope_dim, c);
+  int e;
+  const uint32_t word = quant_q_slice(raw, j, c, a.rope_dim, gmask, &e);
   uint8_t* row = a.q_rows + v * kRowBytes;
   *reinterpret_cast<uint32_t*>(row + 4 * j) = word;
   if ((j & 3) == 0) row[kCodeBytes + (j >> 2)] = (uint8_t)(e + 127);

@@ -45,7 +45,7 @@ cudaError_t launch_prep_q(const PrepArgs& a, cudaStream_t stream);
 struct ScoreArgs {
   const uint8_t* q_rows;    // [B][S][H][68]
   const float* w_prime;     // [B][S][H]
-  const uint8_t* k_cache;   // [B][T_cap][68]
+  const uint8_t* k_cache;   // [B][T_cap / 128][8704] pages
   float* scores;            // [B][S][T]
   const int32_t* cand;      // [B][S][cbk] or nullptr
   uint32_t* status;

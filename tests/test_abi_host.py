@@ -42,7 +42,7 @@ def test_struct_layouts_match_header(X):
 
 
 def test_abi_version(X):
-    assert X.indexer_abi_version() == 100
+    assert X.indexer_abi_version() == 200   # paged key cache, workspace head with row counters
 
 
 def test_workspace_size_host_only(X):

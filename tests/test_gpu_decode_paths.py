@@ -1,0 +1,98 @@
+"""indexer_forward on decode shapes (one query row per sequence) against the separate
+entry points and the oracle.
+
+Its scores and indices must equal, bit for bit, what indexer_prep_q + indexer_scores +
+indexer_topk produce on the same inputs, also when the call is repeated on one workspace
+and when a prefill call shares the workspace.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from tests import cases as C
+from workloads import WORKLOADS
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def X():
+    import sparse_attention_top_indexer_gb300 as X
+    X.load_library()
+    return X
+
+
+def _split_path(X, wl, d, q, w, table, cache):
+    rows = torch.empty((wl.B, 1, wl.H, 68), dtype=torch.uint8, device="cuda")
+    wp = torch.empty((wl.B, 1, wl.H), dtype=torch.float32, device="cuda")
+    X.indexer_prep_q(d, q, w, wl.start_pos, table, rows, wp)
+    sc = torch.empty((wl.B, 1, wl.T), dtype=torch.float32, device="cuda")
+    ws = torch.empty(X.STATUS_BYTES, dtype=torch.uint8, device="cuda")
+    X.indexer_workspace_init(ws)
+    X.indexer_scores(d, rows, wp, wl.start_pos, cache, sc, ws)
+    top = torch.empty((wl.B, 1, wl.topk), dtype=torch.int32, device="cuda")
+    X.indexer_topk(d, sc, wl.start_pos, top)
+    X.indexer_status(ws)
+    return sc, top
+
+
+def _fused(X, wl, d, q, w, table, cache, ws):
+    sc = torch.empty((wl.B, 1, wl.T), dtype=torch.float32, device="cuda")
+    top = torch.empty((wl.B, 1, wl.topk), dtype=torch.int32, device="cuda")
+    X.indexer_forward(d, q, w, wl.start_pos, table, cache, top, ws, scores_out=sc)
+    return sc, top
+
+
+@pytest.mark.parametrize("name,B,H,start,topk", [
+    ("f_dec", 3, 64, 4095, 256),        # 1024 keys, 8 pages per row over several CTAs
+    ("f_rag", 5, 8, 1999, 100),          # 500 keys: ragged last page, N padded to 16
+    ("f_h16", 2, 16, 511, 64),           # one page
+    ("f_h32", 4, 32, 8191, 1023),        # 2048 keys
+    ("f_h128", 2, 128, 16383, 2047),     # 4096 keys, one CTA per SM
+    ("f_full", 32, 64, 32767, 2048),     # the decode workload's shape
+])
+def test_fused_equals_split_and_oracle(X, name, B, H, start, topk):
+    wl = dataclasses.replace(WORKLOADS["decode"], name=name, B=B, H=H, start_pos=start, topk=topk)
+    d = C.dims_of(wl)
+    table = C.gpu_table(wl.max_pos)
+    cache = C.gpu_cache(wl, table)
+    q, w = wl.q("cuda"), wl.w("cuda")
+    sc_ref, top_ref = _split_path(X, wl, d, q, w, table, cache)
+    ws = torch.empty(X.indexer_workspace_size(d, wl.B, 1, wl.start_pos), dtype=torch.uint8, device="cuda")
+    X.indexer_workspace_init(ws)
+    for rep in range(3):
+        sc, top = _fused(X, wl, d, q, w, table, cache, ws)
+        X.indexer_status(ws)
+        assert torch.equal(sc.view(torch.int32), sc_ref.view(torch.int32)), f"rep {rep}: scores differ"
+        assert torch.equal(top, top_ref), f"rep {rep}: indices differ"
+    if B * wl.T <= 8 * 4096:   # oracle check on the smaller shapes
+        cos, sin = C.oracle_table(wl.max_pos)
+        ref_cache = C.oracle_cache(wl, cos, sin)
+        ref_top, _, ref_sc = O.forward(C.bits(q), C.bits(w), ref_cache, cos, sin, wl.start_pos, wl.ratio,
+                                       wl.rope_dim, wl.topk, wl.offset)
+        C.assert_scores_close(sc.cpu().numpy(), ref_sc)
+        C.compare_topk(top.cpu().numpy().reshape(-1, wl.topk), ref_top.reshape(-1, wl.topk),
+                       ref_sc.reshape(-1, wl.T), wl.offset)
+
+
+def test_fused_workspace_shared_with_prefill(X):
+    """Decode and prefill calls interleaved on one workspace."""
+    dec = dataclasses.replace(WORKLOADS["decode"], name="f_share", B=4, start_pos=4095, topk=300)
+    pre = dataclasses.replace(WORKLOADS["prefill"], name="f_share_p", B=2, S=600, topk=64)
+    dd, dp = C.dims_of(dec), C.dims_of(pre)
+    n = max(X.indexer_workspace_size(dd, dec.B, 1, dec.start_pos), X.indexer_workspace_size(dp, pre.B, pre.S, 0))
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    X.indexer_workspace_init(ws)
+    t_dec, t_pre = C.gpu_table(dec.max_pos), C.gpu_table(pre.max_pos)
+    c_dec, c_pre = C.gpu_cache(dec, t_dec), C.gpu_cache(pre, t_pre)
+    qd, wd = dec.q("cuda"), dec.w("cuda")
+    _, top_ref = _split_path(X, dec, dd, qd, wd, t_dec, c_dec)
+    for _ in range(2):
+        top_p = torch.empty((pre.B, pre.S, pre.topk), dtype=torch.int32, device="cuda")
+        X.indexer_forward(dp, pre.q("cuda"), pre.w("cuda"), 0, t_pre, c_pre, top_p, ws)
+        _, top = _fused(X, dec, dd, qd, wd, t_dec, c_dec, ws)
+        X.indexer_status(ws)
+        assert torch.equal(top, top_ref)
