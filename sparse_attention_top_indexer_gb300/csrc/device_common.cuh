@@ -178,6 +178,16 @@ __device__ __forceinline__ uint32_t quant_q_slice(uint4 raw, int j, const float2
   return word;
 }
 
+// ----------------------------------------------------------------------------- launch overlap
+// Every kernel of the library is launched with programmatic stream serialisation: it may
+// start while the kernel before it on the stream is still running. pdl_allow_next() lets
+// the next kernel start in turn; pdl_wait() blocks until every earlier kernel on the
+// stream has completed and its memory is visible, and each kernel calls it before its
+// first global-memory access (read or write), so only shared-memory set-up overlaps.
+// Both are no-ops for a kernel launched without that attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_allow_next() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(kThreads, ScoreCfg<H, QG>::TMEM_COLS <= 256 ? 
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1024-byte aligned base
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_allow_next();
   const int b = blockIdx.z;
   const int s0 = blockIdx.y * QG;
   const int nq = min(QG, a.S - s0);
@@ -117,6 +118,7 @@ __global__ void __launch_bounds__(kThreads, ScoreCfg<H, QG>::TMEM_COLS <= 256 ? 
   // keys the group's last row can see; pages at or past it are fully masked
   const int vis_hi = min(a.T, (a.start_pos + s0 + nq) / a.ratio);
   const int tile_vis = min(tile1, (vis_hi + kTileKeys - 1) / kTileKeys);
+  pdl_wait();   // the query rows, weights and pages of the kernels before are complete
   if (a.fill_masked) {
     const int t_begin = max(tile0, tile_vis) * kTileKeys, t_end = min(tile1 * kTileKeys, a.T);
     for (int qi = 0; qi < nq; ++qi) {
@@ -402,8 +404,7 @@ cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
   }
   a.tiles_per_cta = tpc;
   dim3 grid((ntiles + tpc - 1) / tpc, groups, a.B);
-  score_kernel<H, QG><<<grid, kThreads, smem, stream>>>(a);
-  return cudaGetLastError();
+  return launch_overlapped(score_kernel<H, QG>, grid, dim3(kThreads), smem, stream, a);
 }
 
 }  // namespace

@@ -165,25 +165,27 @@ struct TopkKept {
 // in position order (select_top). Rows with no candidate filter and vis <= k_eff take the
 // short-context fill [0 .. vis).
 
-template <int KPT>
-__global__ void __launch_bounds__(kSelThreads, 1) topk_kernel(const TopkArgs a) {
-  __shared__ SelectShared<kSelThreads> sh;
+template <int NT, int KPT>
+__global__ void __launch_bounds__(NT, 1) topk_kernel(const TopkArgs a) {
+  __shared__ SelectShared<NT> sh;
   __shared__ TopkKept kb;
   const int tid = threadIdx.x;
+  pdl_allow_next();
+  pdl_wait();
   const int row = blockIdx.x;
   const int s = row % a.S;
   const int vis = min(a.T, (a.start_pos + s + 1) / a.ratio);
   const int k_eff = min(a.topk, a.T);
   int32_t* out = a.out + (size_t)row * a.topk;
   if (a.cand == nullptr && vis <= k_eff) {
-    for (int i = tid; i < a.topk; i += kSelThreads) out[i] = i < vis ? i + a.offset : -1;
+    for (int i = tid; i < a.topk; i += NT) out[i] = i < vis ? i + a.offset : -1;
     return;
   }
   const int nblk_words = a.cand ? ((a.T + a.cbs - 1) / a.cbs + 31) / 32 : 0;
   if (a.cand) {
-    for (int i = tid; i < nblk_words; i += kSelThreads) kb.kept[i] = 0u;
+    for (int i = tid; i < nblk_words; i += NT) kb.kept[i] = 0u;
     __syncthreads();
-    for (int i = tid; i < a.cbk; i += kSelThreads) {
+    for (int i = tid; i < a.cbk; i += NT) {
       const int blk = a.cand[(size_t)row * a.cbk + i];
       if (blk >= 0 && blk < nblk_words * 32) atomicOr(&kb.kept[blk >> 5], 1u << (blk & 31));
     }
@@ -216,7 +218,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) topk_kernel(const TopkArgs a) 
     for (int j = 0; j < KPT; ++j) key[j] = base + j < vis ? make_key(src[base + j], base + j) : 0u;
   }
 
-  select_top<kSelThreads, KPT>(key, k_eff, out, a.topk, a.offset, sh, nullptr);
+  select_top<NT, KPT>(key, k_eff, out, a.topk, a.offset, sh, nullptr);
 }
 
 // One CTA per query row: block score = max finite score over the block's positions
@@ -225,6 +227,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) cand_kernel(const CandArgs a) 
   __shared__ uint32_t bkeys[kCandMaxBlocks];
   __shared__ SelShared sh;
   const int tid = threadIdx.x;
+  pdl_allow_next();
+  pdl_wait();
   const int row = blockIdx.x;
   const int s = row % a.S;
   const int vis = min(a.T, (a.start_pos + s + 1) / a.ratio);
@@ -245,21 +249,18 @@ __global__ void __launch_bounds__(kSelThreads, 1) cand_kernel(const CandArgs a) 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   if (a.rows <= 0) return cudaSuccess;
   if (a.T <= kSelThreads * 8) {
-    topk_kernel<8><<<a.rows, kSelThreads, 0, stream>>>(a);
+    return launch_overlapped(topk_kernel<kSelThreads, 8>, dim3(a.rows), dim3(kSelThreads), 0, stream, a);
   } else if (a.T <= kSelThreads * 16) {
-    topk_kernel<16><<<a.rows, kSelThreads, 0, stream>>>(a);
+    return launch_overlapped(topk_kernel<kSelThreads, 16>, dim3(a.rows), dim3(kSelThreads), 0, stream, a);
   } else if (a.T <= kSelThreads * 32) {
-    topk_kernel<32><<<a.rows, kSelThreads, 0, stream>>>(a);
-  } else {
-    return cudaErrorInvalidValue;
+    return launch_overlapped(topk_kernel<kSelThreads, 32>, dim3(a.rows), dim3(kSelThreads), 0, stream, a);
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_candidates(const CandArgs& a, cudaStream_t stream) {
   if (a.rows <= 0) return cudaSuccess;
-  cand_kernel<<<a.rows, kSelThreads, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_overlapped(cand_kernel, dim3(a.rows), dim3(kSelThreads), 0, stream, a);
 }
 
 }  // namespace indexer

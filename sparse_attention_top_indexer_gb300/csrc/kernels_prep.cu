@@ -17,6 +17,8 @@ namespace indexer {
 // table[pos][i] = (cos, sin) of angle f32(pos) * f'_i (f32 product), evaluated in f64
 // and rounded to f32 ("Module compress" page, yarn_freqs_cis).
 __global__ void rope_table_kernel(RopeFreqs freqs, int half, int max_pos, float2* table) {
+  pdl_allow_next();
+  pdl_wait();
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)max_pos * half) return;
   const int pos = (int)(idx / half);
@@ -31,8 +33,8 @@ cudaError_t launch_rope_table(const RopeFreqs& freqs, int half, int max_pos, flo
   const long long n = (long long)max_pos * half;
   const int threads = 256;
   const long long blocks = (n + threads - 1) / threads;
-  rope_table_kernel<<<(unsigned)blocks, threads, 0, stream>>>(freqs, half, max_pos, reinterpret_cast<float2*>(table));
-  return cudaGetLastError();
+  return launch_overlapped(rope_table_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, freqs, half, max_pos,
+                           reinterpret_cast<float2*>(table));
 }
 
 // ---------------------------------------------------------------------------- key publish
@@ -54,6 +56,8 @@ __global__ void __launch_bounds__(128) publish_kernel(PublishArgs a) {
   __shared__ double wsum[4];
   __shared__ double rinv;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_allow_next();
+  pdl_wait();
   const int key = blockIdx.x;
   const int b = key / a.G, j = key % a.G;
   const uint16_t* src = a.latent + ((size_t)b * a.G + j) * a.Din;
@@ -154,8 +158,7 @@ __global__ void __launch_bounds__(128) publish_kernel(PublishArgs a) {
 
 cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream) {
   const long long keys = (long long)a.B * a.G;
-  publish_kernel<<<(unsigned)keys, 128, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_overlapped(publish_kernel, dim3((unsigned)keys), dim3(128), 0, stream, a);
 }
 
 // ---------------------------------------------------------------------------- query prep
@@ -164,6 +167,8 @@ cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream) {
 // 32-block share its amax by shuffles; each thread writes 4 code bytes, the first
 // thread of a block its scale byte. w' = f32(w) * head_dim^-0.5 * H^-0.5.
 __global__ void __launch_bounds__(256) prep_q_kernel(PrepArgs a) {
+  pdl_allow_next();
+  pdl_wait();
   const int tid = threadIdx.x;
   const long long v = (long long)blockIdx.x * 16 + (tid >> 4);
   const int j = tid & 15;
@@ -185,8 +190,7 @@ __global__ void __launch_bounds__(256) prep_q_kernel(PrepArgs a) {
 
 cudaError_t launch_prep_q(const PrepArgs& a, cudaStream_t stream) {
   const long long blocks = (a.n_vec + 15) / 16;
-  prep_q_kernel<<<(unsigned)blocks, 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_overlapped(prep_q_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, a);
 }
 
 }  // namespace indexer
