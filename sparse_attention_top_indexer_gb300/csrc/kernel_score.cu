@@ -38,8 +38,7 @@ namespace {
 
 constexpr int kTileKeys = kPageKeys;                 // one MMA M-tile per page
 constexpr int kStageStride = 9216;                   // page (8704 B) padded to a 1 KB multiple
-constexpr int kThreads = 256;
-constexpr int kEpiThreads = 128;                     // warps 4-7
+constexpr int kEpiThreads = 128;                     // one epilogue warpgroup
 
 __host__ __device__ constexpr int round_up(int x, int m) { return (x + m - 1) / m * m; }
 __host__ __device__ constexpr uint32_t pow2_cols(int n) {
@@ -53,8 +52,10 @@ __host__ __device__ constexpr int max_acc(int NP, int SB, int budget) {
        : 2 * (NP + 8) + 2 * SB <= budget ? 2 : 1 * (NP + 8) + 2 * SB <= budget ? 1 : 0;
 }
 
-template <int H, int QG>
+// EPI epilogue warpgroups (warps 4 .. 4*EPI+3) take alternate pages.
+template <int H, int QG, int EPI>
 struct ScoreCfg {
+  static constexpr int THREADS = 128 * (1 + EPI);
   static constexpr int N = QG * H;
   static constexpr int NP = round_up(N, 16);                 // MMA N
   static constexpr int NCB = (NP + 31) / 32;                 // B scale columns per half
@@ -62,12 +63,12 @@ struct ScoreCfg {
   // tensor memory: NACC accumulators of NP columns, NACC A scale sets of 8 columns, two
   // halves of SB B scale columns; every scale address is a multiple of 4 columns. Two or
   // more accumulators within 256 columns let two CTAs share an SM.
+  static constexpr int NSTAGE = 8;
   static constexpr int NACC = max_acc(NP, SB, 256) >= 2 ? max_acc(NP, SB, 256) : max_acc(NP, SB, 512);
   static constexpr int SFA_COL = NACC * NP;
   static constexpr int SFB_COL = SFA_COL + 8 * NACC;
   static constexpr int TMEM_NEED = SFB_COL + 2 * SB;
   static constexpr uint32_t TMEM_COLS = pow2_cols(TMEM_NEED);
-  static constexpr int NSTAGE = 8;
   static constexpr int OFF_QB = 0;
   static constexpr int OFF_STG = round_up(NP * kCodeBytes, 1024);
   static constexpr int OFF_QSTG = OFF_STG + NSTAGE * kStageStride;          // raw query rows
@@ -100,10 +101,10 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return ok != 0u;
 }
 
-template <int H, int QG>
-__global__ void __launch_bounds__(kThreads, ScoreCfg<H, QG>::TMEM_COLS <= 256 ? 2 : 1)
+template <int H, int QG, int EPI>
+__global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG, EPI>::TMEM_COLS <= 256 ? 2 : 1)
     score_kernel(const ScoreArgs a) {
-  using C = ScoreCfg<H, QG>;
+  using C = ScoreCfg<H, QG, EPI>;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1024-byte aligned base
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -119,14 +120,19 @@ __global__ void __launch_bounds__(kThreads, ScoreCfg<H, QG>::TMEM_COLS <= 256 ? 
   const int vis_hi = min(a.T, (a.start_pos + s0 + nq) / a.ratio);
   const int tile_vis = min(tile1, (vis_hi + kTileKeys - 1) / kTileKeys);
   pdl_wait();   // the query rows, weights and pages of the kernels before are complete
-  if (a.fill_masked) {
+  // -inf over the pages no row of the group can see (by the epilogue warps while they wait
+  // for the first accumulator, or here when the CTA has nothing to score)
+  auto fill_masked = [&](int first_thread, int nthreads) {
     const int t_begin = max(tile0, tile_vis) * kTileKeys, t_end = min(tile1 * kTileKeys, a.T);
     for (int qi = 0; qi < nq; ++qi) {
       float* dst = a.scores + ((size_t)b * a.S + s0 + qi) * a.T;
-      for (int t = t_begin + tid; t < t_end; t += kThreads) dst[t] = -__int_as_float(0x7f800000);
+      for (int t = t_begin + first_thread; t < t_end; t += nthreads) dst[t] = -__int_as_float(0x7f800000);
     }
+  };
+  if (tile_vis <= tile0) {
+    if (a.fill_masked) fill_masked(tid, C::THREADS);
+    return;
   }
-  if (tile_vis <= tile0) return;
   const int nt = tile_vis - tile0;   // pages this CTA scores
 
   uint8_t* qB = smem + C::OFF_QB;
@@ -247,14 +253,17 @@ __global__ void __launch_bounds__(kThreads, ScoreCfg<H, QG>::TMEM_COLS <= 256 ? 
     }
   } else {
     // ------------------------------------------------------------ epilogue warpgroup
-    constexpr int P = H >= 32 ? 4 : (H >= 16 ? 2 : 1);   // independent partial sums per row
-    const int et = tid - 128;   // key within the page == TMEM lane
+    constexpr int P = H >= 32 ? 4 : 2;   // independent partial sums per row (pairs of heads)
+    static_assert(C::N % 4 == 0 && H % 4 == 0 && C::NCB <= 4, "epilogue column grouping");
+    const int grp = (warp - 4) >> 2;              // this warp's epilogue warpgroup
+    const int et = (tid - 128) & (kEpiThreads - 1);   // key within the page == TMEM lane
+    const int ge = tid - 128;                     // index among all epilogue threads
     // level-two candidate filter: one bit per block of cbs positions, per query row
     const int cand_words = a.cand ? ((a.T + a.cbs - 1) / a.cbs + 31) / 32 : 0;
     if (a.cand) {
-      for (int i = et; i < QG * cand_words; i += kEpiThreads) cand_bits[i] = 0u;
-      named_bar_sync(2, kEpiThreads);
-      for (int i = et; i < nq * a.cbk; i += kEpiThreads) {
+      for (int i = ge; i < QG * cand_words; i += EPI * kEpiThreads) cand_bits[i] = 0u;
+      named_bar_sync(2, EPI * kEpiThreads);
+      for (int i = ge; i < nq * a.cbk; i += EPI * kEpiThreads) {
         const int qi = i / a.cbk;
         const int blk = a.cand[((size_t)b * a.S + s0 + qi) * a.cbk + (i % a.cbk)];
         if (blk >= 0 && blk < cand_words * 32) atomicOr(&cand_bits[qi * cand_words + (blk >> 5)], 1u << (blk & 31));
@@ -263,54 +272,43 @@ __global__ void __launch_bounds__(kThreads, ScoreCfg<H, QG>::TMEM_COLS <= 256 ? 
     // head weights (rows past S weigh nothing)
     failed = !warp_wait(bar_q, 0u);
     if (!failed)
-      for (int n = nq * H + et; n < C::N; n += kEpiThreads) wq[n] = 0.f;
-    named_bar_sync(2, kEpiThreads);
-    for (int i = 0; i < nt && !failed; ++i) {
+      for (int n = nq * H + ge; n < C::N; n += EPI * kEpiThreads) wq[n] = 0.f;
+    named_bar_sync(2, EPI * kEpiThreads);
+    if (a.fill_masked) fill_masked(ge, EPI * kEpiThreads);
+    for (int i = grp; i < nt && !failed; i += EPI) {   // this group's pages
       const int c = i % C::NACC;
       if (!warp_wait(bar_done(c), (uint32_t)(i / C::NACC) & 1u)) {
         failed = true;
         break;
       }
       tc_fence_after();
+      // the whole accumulator in one tensor-memory read, then release it
+      float v[C::NCB * 32];
+      if constexpr (C::NCB == 1) tmem_ld32(tq + (uint32_t)(c * C::NP), v);
+      else if constexpr (C::NCB == 2) tmem_ld64(tq + (uint32_t)(c * C::NP), v);
+      else tmem_ld128(tq + (uint32_t)(c * C::NP), v);
+      tc_fence_before();
+      mbar_arrive(bar_empty(c));   // accumulator c and its scale set may be reused
+      // sum_h w' * max(dot, 0) per query row: column pairs (two heads of one row) with packed
+      // f32x2 FMAs into P independent partial sums per row
       float part[QG][P];
 #pragma unroll
       for (int qi = 0; qi < QG; ++qi)
 #pragma unroll
         for (int p = 0; p < P; ++p) part[qi][p] = 0.f;
-      if constexpr (C::NCB <= 2) {
-        // small N: read the whole accumulator, release it, then reduce
-        float v[C::NCB][32];
 #pragma unroll
-        for (int k = 0; k < C::NCB; ++k) tmem_ld32(tq + (uint32_t)(c * C::NP + 32 * k), v[k]);
-        tc_fence_before();
-        mbar_arrive(bar_empty(c));   // accumulator c and its scale set may be reused
-#pragma unroll
-        for (int k = 0; k < C::NCB; ++k)
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int n = 32 * k + jj;
-            if (n < C::N) part[n / H][n % P] = fmaf(wq[n], fmaxf(v[k][jj], 0.f), part[n / H][n % P]);
-          }
-      } else {
-        // large N: reduce 32 columns at a time, release after the last read
-#pragma unroll
-        for (int k = 0; k < C::NCB; ++k) {
-          float v[32];
-          tmem_ld32(tq + (uint32_t)(c * C::NP + 32 * k), v);
-#pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int n = 32 * k + jj;
-            if (n < C::N) part[n / H][n % P] = fmaf(wq[n], fmaxf(v[jj], 0.f), part[n / H][n % P]);
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(bar_empty(c));
+      for (int n = 0; n < C::N; n += 4) {
+        const float4 w4 = *reinterpret_cast<const float4*>(wq + n);
+        const int qi = n / H, p0 = (n % P), p1 = ((n + 2) % P);
+        ffma2(part[qi][p0], part[qi][p0 + 1], w4.x, w4.y, fmaxf(v[n], 0.f), fmaxf(v[n + 1], 0.f));
+        ffma2(part[(n + 2) / H][p1], part[(n + 2) / H][p1 + 1], w4.z, w4.w, fmaxf(v[n + 2], 0.f),
+              fmaxf(v[n + 3], 0.f));
       }
       if (et == 0 && i + C::NSTAGE < nt) {
         // the MMA that read this page's stage has completed: refill it
         issue_page_load(a, b, tile0 + i + C::NSTAGE, stg0 + (i % C::NSTAGE) * kStageStride,
                         bar_full(i % C::NSTAGE));
-        info[1] = (uint32_t)(i + C::NSTAGE + 1);
+        atomicMax(&info[1], (uint32_t)(i + C::NSTAGE + 1));
       }
       const int t0 = (tile0 + i) * kTileKeys;
       const int nv = min(kTileKeys, a.T - t0);
@@ -369,9 +367,9 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int H, int QG>
+template <int H, int QG, int EPI>
 cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
-  using C = ScoreCfg<H, QG>;
+  using C = ScoreCfg<H, QG, EPI>;
   const int cand_words = a.cand ? ((a.T + a.cbs - 1) / a.cbs + 31) / 32 : 0;
   const size_t smem = (size_t)C::OFF_CAND + (size_t)QG * cand_words * 4 + 1024;   // + base alignment slack
   // the attributes are set once per device and kernel (the dynamic size only grows)
@@ -380,9 +378,9 @@ cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64 || set_bytes[dev] < (int)smem) {
-    err = cudaFuncSetAttribute(score_kernel<H, QG>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    err = cudaFuncSetAttribute(score_kernel<H, QG, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(score_kernel<H, QG>, cudaFuncAttributePreferredSharedMemoryCarveout,
+      err = cudaFuncSetAttribute(score_kernel<H, QG, EPI>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) set_bytes[dev] = (int)smem;
@@ -404,7 +402,7 @@ cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
   }
   a.tiles_per_cta = tpc;
   dim3 grid((ntiles + tpc - 1) / tpc, groups, a.B);
-  return launch_overlapped(score_kernel<H, QG>, grid, dim3(kThreads), smem, stream, a);
+  return launch_overlapped(score_kernel<H, QG, EPI>, grid, dim3(C::THREADS), smem, stream, a);
 }
 
 }  // namespace
@@ -413,11 +411,13 @@ cudaError_t launch_scores(const ScoreArgs& a, cudaStream_t stream) {
   if (a.T <= 0) return cudaSuccess;
   const bool single = a.S == 1;
   switch (a.H) {
-    case 8: return single ? launch_cfg<8, 1>(a, stream) : launch_cfg<8, 32>(a, stream);
-    case 16: return single ? launch_cfg<16, 1>(a, stream) : launch_cfg<16, 16>(a, stream);
-    case 32: return single ? launch_cfg<32, 1>(a, stream) : launch_cfg<32, 8>(a, stream);
-    case 64: return single ? launch_cfg<64, 1>(a, stream) : launch_cfg<64, 4>(a, stream);
-    case 128: return single ? launch_cfg<128, 1>(a, stream) : launch_cfg<128, 2>(a, stream);
+    // decode: one query row, N = H, two CTAs per SM; several rows: N = 128 (three
+    // accumulators in 512 columns) and two epilogue warpgroups
+    case 8: return single ? launch_cfg<8, 1, 1>(a, stream) : launch_cfg<8, 16, 2>(a, stream);
+    case 16: return single ? launch_cfg<16, 1, 1>(a, stream) : launch_cfg<16, 8, 2>(a, stream);
+    case 32: return single ? launch_cfg<32, 1, 1>(a, stream) : launch_cfg<32, 4, 2>(a, stream);
+    case 64: return single ? launch_cfg<64, 1, 1>(a, stream) : launch_cfg<64, 2, 2>(a, stream);
+    case 128: return single ? launch_cfg<128, 1, 1>(a, stream) : launch_cfg<128, 1, 2>(a, stream);
     default: return cudaErrorInvalidValue;
   }
 }
