@@ -38,79 +38,115 @@ cudaError_t launch_rope_table(const RopeFreqs& freqs, int half, int max_pos, flo
 }
 
 // ---------------------------------------------------------------------------- key publish
-// One CTA of 128 threads per key; thread o owns output dim o.
+// One CTA per key: 128 x TPO threads (TPO = 4 for a few keys, 1 for many).
 //  1. k_pre[o] = bf16( sum_i wk[o][i] * latent[i] ): bf16*bf16 products are exact in f32,
-//     their sum is carried error-free (TwoSum) in eight interleaved accumulators and
-//     rounded once to bf16 ("DeepSeek V4.1" index-keys page, Indexer: wk bf16 Linear).
-//     The thread's wk row is fetched 128 elements at a time with all loads issued
-//     before any is used, so a 128-wide row costs one memory round trip.
+//     their sum is carried error-free (TwoSum) and rounded once to bf16 ("DeepSeek V4.1"
+//     index-keys page, Indexer: wk bf16 Linear). Output o's products are split over four
+//     consecutive threads (four accumulators each), whose parts are merged with TwoSum
+//     across the lanes; every global read is issued at entry. From step 2 on, thread
+//     o < 128 owns output dim o.
 //  2. RMSNorm in f64: y = bf16( (w[o] * k_pre[o]) * (1 / sqrt(sum(k_pre^2) / 128 + eps)) );
 //     the reciprocal square root is formed once per key.
 //  3. RoPE on the last rope_dim dims at the group position: interleaved pair (2i, 2i+1)
 //     rotated by table entry i with the f32 sequence x0*c - x1*s, x0*s + x1*c, then bf16.
 //  4. e2m1/e8m0 quantisation per 32-block (warp w owns block w); the 64 code bytes and
 //     4 scale bytes go to the key's places in its 128-key page.
-__global__ void __launch_bounds__(128) publish_kernel(PublishArgs a) {
+template <int TPO>   // threads per output dimension (1 or 4)
+__global__ void __launch_bounds__(kHeadDim * TPO) publish_kernel(PublishArgs a) {
+  constexpr int NT = kHeadDim * TPO;
   __shared__ float lat[1024];
+  __shared__ float kx[kHeadDim];
   __shared__ float kv[kHeadDim];
   __shared__ double wsum[4];
   __shared__ double rinv;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
   pdl_allow_next();
   pdl_wait();
   const int key = blockIdx.x;
   const int b = key / a.G, j = key % a.G;
+  const int o = tid / TPO, part = tid % TPO;
+  // every global read of the key is issued before the first is used
+  const int span = ((a.Din + 8 * TPO - 1) / (8 * TPO)) * 8;   // elements per part, a multiple of 8
+  const int e_begin = part * span, e_end = min(a.Din, e_begin + span);
+  const uint16_t* wrow = a.wk + (size_t)o * a.Din;
+  constexpr int kPre = 128 / TPO / 8;   // 16-byte chunks fetched up front (the first 128 / TPO elements)
+  uint4 wpre[kPre];
+#pragma unroll
+  for (int u = 0; u < kPre; ++u)
+    wpre[u] = (e_begin + 8 * u < e_end) ? *reinterpret_cast<const uint4*>(wrow + e_begin + 8 * u) : make_uint4(0, 0, 0, 0);
+  const uint32_t knorm_bits = tid < kHeadDim ? a.knorm[tid] : 0u;
+  const int rstart = kHeadDim - a.rope_dim;
+  float2 cs = make_float2(1.f, 0.f);
+  if (tid < kHeadDim && tid >= rstart)
+    cs = reinterpret_cast<const float2*>(a.rope_cs)[(size_t)(a.pos0 + j * a.pos_step) * (a.rope_dim / 2) +
+                                                    ((tid - rstart) >> 1)];
   const uint16_t* src = a.latent + ((size_t)b * a.G + j) * a.Din;
-  for (int i = tid; i < a.Din; i += 128) lat[i] = bf16_to_f32(src[i]);
+  for (int i = tid; i < a.Din; i += NT) lat[i] = bf16_to_f32(src[i]);
   __syncthreads();
 
-  // 1. exact dot product, rounded once
-  const uint16_t* wrow = a.wk + (size_t)tid * a.Din;
-  constexpr int kAcc = 8;
-  float s[kAcc], c[kAcc];
+  // 1. exact dot product, rounded once: output o's products are split over TPO consecutive
+  //    threads, each carrying its part error-free in four (sum, error) pairs; the parts are
+  //    merged with TwoSum across the lanes
+  {
+    constexpr int kAcc = 4;
+    float s[kAcc], c[kAcc];
 #pragma unroll
-  for (int k = 0; k < kAcc; ++k) s[k] = c[k] = 0.f;
-  for (int i0 = 0; i0 < a.Din; i0 += 128) {
-    uint4 w8[16];
+    for (int k = 0; k < kAcc; ++k) s[k] = c[k] = 0.f;
+    for (int e0 = e_begin; e0 < e_end; e0 += 8 * kPre) {
+      uint4 w8[kPre];
 #pragma unroll
-    for (int u = 0; u < 16; ++u)
-      w8[u] = (i0 + 8 * u < a.Din) ? *reinterpret_cast<const uint4*>(wrow + i0 + 8 * u) : make_uint4(0, 0, 0, 0);
+      for (int u = 0; u < kPre; ++u)
+        w8[u] = e0 == e_begin ? wpre[u]
+                              : ((e0 + 8 * u < e_end) ? *reinterpret_cast<const uint4*>(wrow + e0 + 8 * u)
+                                                      : make_uint4(0, 0, 0, 0));
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      const uint32_t ww[4] = {w8[u].x, w8[u].y, w8[u].z, w8[u].w};
-      const int e0 = i0 + 8 * u;
-      if (e0 < a.Din) {
+      for (int u = 0; u < kPre; ++u) {
+        const uint32_t ww[4] = {w8[u].x, w8[u].y, w8[u].z, w8[u].w};
+        const int eu = e0 + 8 * u;
+        if (eu < e_end) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int acc = (2 * k) & (kAcc - 1), acc2 = (2 * k + 1) & (kAcc - 1);
-          const float p0 = __fmul_rn(bf16_to_f32(ww[k] & 0xFFFFu), lat[e0 + 2 * k]);
-          const float p1 = __fmul_rn(bf16_to_f32(ww[k] >> 16), lat[e0 + 2 * k + 1]);
-          float t, e;
-          two_sum(s[acc], p0, t, e);
-          s[acc] = t;
-          c[acc] = __fadd_rn(c[acc], e);
-          two_sum(s[acc2], p1, t, e);
-          s[acc2] = t;
-          c[acc2] = __fadd_rn(c[acc2], e);
+          for (int k = 0; k < 4; ++k) {
+            const float p0 = __fmul_rn(bf16_to_f32(ww[k] & 0xFFFFu), lat[eu + 2 * k]);
+            const float p1 = __fmul_rn(bf16_to_f32(ww[k] >> 16), lat[eu + 2 * k + 1]);
+            float t, e;
+            two_sum(s[k], p0, t, e);
+            s[k] = t;
+            c[k] = __fadd_rn(c[k], e);
+            two_sum(s[k], p1, t, e);
+            s[k] = t;
+            c[k] = __fadd_rn(c[k], e);
+          }
         }
       }
     }
-  }
-  float hi = s[0], lo = c[0];
+    float hi = s[0], lo = c[0];
 #pragma unroll
-  for (int k = 1; k < kAcc; ++k) {
-    float t, e;
-    two_sum(hi, s[k], t, e);
-    hi = t;
-    lo = __fadd_rn(__fadd_rn(lo, c[k]), e);
+    for (int k = 1; k < kAcc; ++k) {
+      float t, e;
+      two_sum(hi, s[k], t, e);
+      hi = t;
+      lo = __fadd_rn(__fadd_rn(lo, c[k]), e);
+    }
+#pragma unroll
+    for (int off = 1; off < TPO; off <<= 1) {
+      const float ohi = __shfl_xor_sync(0xffffffffu, hi, off), olo = __shfl_xor_sync(0xffffffffu, lo, off);
+      float t, e;
+      two_sum(hi, ohi, t, e);
+      hi = t;
+      lo = __fadd_rn(__fadd_rn(lo, olo), e);
+    }
+    {
+      float t, e;
+      two_sum(hi, lo, t, e);   // normalise: |e| <= ulp(t) / 2
+      hi = t;
+      lo = e;
+    }
+    if (part == 0) kx[o] = bf16_to_f32(f32pair_to_bf16_rne(hi, lo));
   }
-  {
-    float t, e;
-    two_sum(hi, lo, t, e);   // normalise: |e| <= ulp(t) / 2
-    hi = t;
-    lo = e;
-  }
-  const float x = bf16_to_f32(f32pair_to_bf16_rne(hi, lo));
+  __syncthreads();
+  if (tid >= kHeadDim) return;   // one thread per output dimension from here on
+  const int warp = tid >> 5, lane = tid & 31;
+  const float x = kx[tid];
 
   // 2. RMSNorm in f64 (the squares of bf16 values are exact; the sum is exact for any
   //    realistic dynamic range, so its order does not matter)
@@ -118,27 +154,23 @@ __global__ void __launch_bounds__(128) publish_kernel(PublishArgs a) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
   if (lane == 0) wsum[warp] = ss;
-  __syncthreads();
+  named_bar_sync(1, kHeadDim);
   if (tid == 0) {
     const double ms = ((wsum[0] + wsum[1]) + (wsum[2] + wsum[3])) / (double)kHeadDim;
     rinv = 1.0 / sqrt(ms + (double)a.eps);
   }
-  __syncthreads();
-  const float wx = __fmul_rn(bf16_to_f32(a.knorm[tid]), x);   // exact (bf16 * bf16)
+  named_bar_sync(1, kHeadDim);
+  const float wx = __fmul_rn(bf16_to_f32(knorm_bits), x);   // exact (bf16 * bf16)
   float y = bf16_to_f32(f64_to_bf16_rne((double)wx * rinv));
 
   // 3. RoPE
   kv[tid] = y;
-  __syncthreads();
-  const int rstart = kHeadDim - a.rope_dim;
+  named_bar_sync(1, kHeadDim);
   if (tid >= rstart) {
-    const int rel = tid - rstart;
-    const int pair = rel >> 1;
-    const int pos = a.pos0 + j * a.pos_step;
-    const float2 cs = reinterpret_cast<const float2*>(a.rope_cs)[(size_t)pos * (a.rope_dim / 2) + pair];
+    const int pair = (tid - rstart) >> 1;
     const float x0 = kv[rstart + 2 * pair], x1 = kv[rstart + 2 * pair + 1];
-    const float r0 = (rel & 1) == 0 ? __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y))
-                                    : __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x));
+    const float r0 = ((tid - rstart) & 1) == 0 ? __fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y))
+                                              : __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x));
     y = bf16_to_f32(f32_to_bf16_rne(r0));
   }
 
@@ -158,7 +190,10 @@ __global__ void __launch_bounds__(128) publish_kernel(PublishArgs a) {
 
 cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream) {
   const long long keys = (long long)a.B * a.G;
-  return launch_overlapped(publish_kernel, dim3((unsigned)keys), dim3(128), 0, stream, a);
+  // few keys (a decode step): four threads per output dimension for a shorter chain;
+  // many keys (prefill): one, for throughput
+  if (keys < 512) return launch_overlapped(publish_kernel<4>, dim3((unsigned)keys), dim3(4 * kHeadDim), 0, stream, a);
+  return launch_overlapped(publish_kernel<1>, dim3((unsigned)keys), dim3(kHeadDim), 0, stream, a);
 }
 
 // ---------------------------------------------------------------------------- query prep
