@@ -6,9 +6,8 @@
 // Selection is a most-significant-digit radix select (shared-memory histograms) that
 // pins the k-th largest key K*, followed by an ordered compaction: every key > K* and the
 // first `need` keys equal to K* (in index order) are written at their prefix-sum slot, so
-// the output comes out sorted by position without a sort. The top-k kernel uses the
-// register-resident form in select_common.cuh; the candidate-block kernel keeps its keys
-// in shared memory.
+// the output comes out sorted by position without a sort. Both kernels use the
+// register-resident form in select_common.cuh.
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -20,139 +19,6 @@ namespace indexer {
 namespace {
 
 constexpr int kSelThreads = 1024;
-constexpr int kSelWarps = kSelThreads / 32;
-
-// Adds 1 to hist[bin] for every lane whose `valid` is set, with one shared-memory atomic
-// per distinct bin per warp (lanes holding the same bin are combined first, so a few hot
-// bins do not serialise 32 atomics each). All 32 lanes of the warp must call it.
-__device__ __forceinline__ void hist_add_warp(uint32_t* hist, uint32_t bin, bool valid) {
-  const uint32_t tag = valid ? bin : 0xFFFFFFFFu;
-  const uint32_t peers = __match_any_sync(0xffffffffu, tag);
-  if (valid && (__ffs(peers) - 1) == (int)(threadIdx.x & 31)) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
-}
-
-struct SelShared {
-  uint32_t hist[256];
-  uint32_t warp_tot[kSelWarps];
-  uint32_t bcast[4];
-};
-
-// Exclusive prefix sum over the CTA (1024 threads); returns this thread's exclusive
-// prefix and writes the total to *total.
-__device__ __forceinline__ uint32_t cta_exclusive_scan(uint32_t v, uint32_t* total, SelShared& sh) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t x = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
-    if (lane >= off) x += y;
-  }
-  if (lane == 31) sh.warp_tot[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    uint32_t t = sh.warp_tot[lane];
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t y = __shfl_up_sync(0xffffffffu, t, off);
-      if (lane >= off) t += y;
-    }
-    sh.warp_tot[lane] = t;   // inclusive
-  }
-  __syncthreads();
-  const uint32_t before = (warp > 0 ? sh.warp_tot[warp - 1] : 0u) + x - v;
-  *total = sh.warp_tot[kSelWarps - 1];
-  __syncthreads();
-  return before;
-}
-
-// keys[0..n) in shared memory. Writes out[0..width): selected indices + offset in
-// ascending order, then -1. k >= 1.
-__device__ void cta_select(const uint32_t* keys, int n, int k, int32_t* out, int width, int offset,
-                           SelShared& sh) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int per = (n + kSelThreads - 1) / kSelThreads;
-  const int lo = min(n, tid * per), hi = min(n, lo + per);
-
-  uint32_t nvalid_local = 0;
-  for (int i = lo; i < hi; ++i) nvalid_local += keys[i] != 0u;
-  uint32_t nvalid;
-  cta_exclusive_scan(nvalid_local, &nvalid, sh);
-
-  uint32_t kstar = 0u;        // select keys > kstar, plus `need` keys == kstar
-  uint32_t need = 0u;
-  if ((int)nvalid > k) {
-    uint32_t prefix = 0u, mask = 0u;
-    need = (uint32_t)k;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      if (tid < 256) sh.hist[tid] = 0u;
-      __syncthreads();
-      for (int j = 0; j < per; ++j) {
-        const int i = lo + j;
-        const uint32_t key = i < hi ? keys[i] : 0u;
-        hist_add_warp(sh.hist, (key >> shift) & 255u, key != 0u && (key & mask) == prefix);
-      }
-      __syncthreads();
-      if (warp == 0) {
-        // lane L owns bins 8L .. 8L+7; find the bin holding the need-th largest key
-        uint32_t c[8], own = 0u;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          c[q] = sh.hist[lane * 8 + q];
-          own += c[q];
-        }
-        uint32_t incl = own;   // sum over lanes >= lane
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-          const uint32_t y = __shfl_down_sync(0xffffffffu, incl, off);
-          if (lane + off < 32) incl += y;
-        }
-        const uint32_t above = incl - own;
-        if (above < need && need <= incl) {
-          uint32_t acc = above;
-          for (int q = 7; q >= 0; --q) {
-            if (acc + c[q] >= need) {
-              sh.bcast[0] = (uint32_t)(lane * 8 + q);
-              sh.bcast[1] = acc;
-              break;
-            }
-            acc += c[q];
-          }
-        }
-      }
-      __syncthreads();
-      const uint32_t bin = sh.bcast[0];
-      need -= sh.bcast[1];
-      prefix |= bin << shift;
-      mask |= 255u << shift;
-      __syncthreads();
-    }
-    kstar = prefix;
-  }
-
-  // ordered compaction
-  uint32_t eq_local = 0u, gt_local = 0u;
-  for (int i = lo; i < hi; ++i) {
-    const uint32_t key = keys[i];
-    gt_local += key > kstar;
-    eq_local += (key == kstar && kstar != 0u);
-  }
-  uint32_t eq_total;
-  const uint32_t eq_before = cta_exclusive_scan(eq_local, &eq_total, sh);
-  const uint32_t eq_take = need > eq_before ? min(need - eq_before, eq_local) : 0u;
-  uint32_t sel_total;
-  uint32_t slot = cta_exclusive_scan(gt_local + eq_take, &sel_total, sh);
-  uint32_t eq_seen = 0u;
-  for (int i = lo; i < hi; ++i) {
-    const uint32_t key = keys[i];
-    bool take = key > kstar;
-    if (key == kstar && kstar != 0u) {
-      take = eq_seen < eq_take;
-      ++eq_seen;
-    }
-    if (take) out[slot++] = i + offset;
-  }
-  for (int i = (int)sel_total + tid; i < width; i += kSelThreads) out[i] = -1;
-}
 
 struct TopkKept {
   uint32_t kept[kCandMaxBlocks / 32];
@@ -218,14 +84,23 @@ __global__ void __launch_bounds__(NT, 1) topk_kernel(const TopkArgs a) {
     for (int j = 0; j < KPT; ++j) key[j] = base + j < vis ? make_key(src[base + j], base + j) : 0u;
   }
 
-  select_top<NT, KPT>(key, k_eff, out, a.topk, a.offset, sh, nullptr);
+  select_top<NT, KPT>(key, k_eff, out, a.topk, a.offset, sh);
 }
 
-// One CTA per query row: block score = max finite score over the block's positions
-// t < vis; ineligible blocks keep key 0; then cta_select over the blocks.
+// One CTA per query row. Block score = max finite score over the block's positions
+// t < vis; a block with none keeps key 0 (ineligible). Thread t loads the PPT positions
+// [t*PPT, (t+1)*PPT) at once, folds them into a running maximum per block and merges each
+// block it touches with one shared-memory atomicMax. The blocks' keys then go to
+// registers (BPT consecutive blocks per thread) and select_top keeps the cbk best, ties to
+// the lower block, in ascending block order.
+union CandShared {
+  uint32_t bkeys[kCandMaxBlocks];
+  SelectShared<kSelThreads> sel;   // reused once the block keys are in registers
+};
+
+template <int PPT, int BPT>
 __global__ void __launch_bounds__(kSelThreads, 1) cand_kernel(const CandArgs a) {
-  __shared__ uint32_t bkeys[kCandMaxBlocks];
-  __shared__ SelShared sh;
+  __shared__ CandShared sh;
   const int tid = threadIdx.x;
   pdl_allow_next();
   pdl_wait();
@@ -233,15 +108,51 @@ __global__ void __launch_bounds__(kSelThreads, 1) cand_kernel(const CandArgs a) 
   const int s = row % a.S;
   const int vis = min(a.T, (a.start_pos + s + 1) / a.ratio);
   const int nblk = (a.T + a.cbs - 1) / a.cbs;
-  for (int i = tid; i < nblk; i += kSelThreads) bkeys[i] = 0u;
+  for (int i = tid; i < nblk; i += kSelThreads) sh.bkeys[i] = 0u;
   __syncthreads();
   const float* src = a.scores + (size_t)row * a.T;
-  for (int t = tid; t < vis; t += kSelThreads) {
-    const float f = src[t];
-    if (isfinite(f)) atomicMax(&bkeys[t / a.cbs], order_key(f));
+  const int t_begin = tid * PPT;
+  uint32_t pk[PPT];   // this thread's position keys (0 = not a candidate value)
+  if ((a.T & 3) == 0) {   // rows start 16-byte aligned: float4 loads
+#pragma unroll
+    for (int j = 0; j < PPT; j += 4) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t_begin + j < vis) v = *reinterpret_cast<const float4*>(src + t_begin + j);
+      const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) pk[j + u] = (t_begin + j + u < vis && isfinite(f[u])) ? order_key(f[u]) : 0u;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < PPT; ++j) {
+      const float f = t_begin + j < vis ? src[t_begin + j] : 0.f;
+      pk[j] = (t_begin + j < vis && isfinite(f)) ? order_key(f) : 0u;
+    }
+  }
+  if (t_begin < vis) {
+    int blk = t_begin / a.cbs, bnd = (blk + 1) * a.cbs;   // positions advance by one: one boundary at a time
+    uint32_t run = 0u;
+#pragma unroll
+    for (int j = 0; j < PPT; ++j) {
+      if (t_begin + j >= bnd) {
+        if (run) atomicMax(&sh.bkeys[blk], run);
+        ++blk;
+        bnd += a.cbs;
+        run = 0u;
+      }
+      run = max(run, pk[j]);
+    }
+    if (run) atomicMax(&sh.bkeys[blk], run);
   }
   __syncthreads();
-  cta_select(bkeys, nblk, a.cbk, a.blocks + (size_t)row * a.cbk, a.cbk, 0, sh);
+  uint32_t key[BPT];
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    const int bi = tid * BPT + j;
+    key[j] = bi < nblk ? sh.bkeys[bi] : 0u;
+  }
+  __syncthreads();   // the block keys are in registers: the shared memory is reused below
+  select_top<kSelThreads, BPT>(key, min(a.cbk, nblk), a.blocks + (size_t)row * a.cbk, a.cbk, 0, sh.sel);
 }
 
 }  // namespace
@@ -258,9 +169,23 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   return cudaErrorInvalidValue;
 }
 
+template <int PPT>
+cudaError_t launch_cand_ppt(const CandArgs& a, int nblk, cudaStream_t stream) {
+  const dim3 grid(a.rows), block(kSelThreads);
+  if (nblk <= kSelThreads) return launch_overlapped(cand_kernel<PPT, 1>, grid, block, 0, stream, a);
+  if (nblk <= 2 * kSelThreads) return launch_overlapped(cand_kernel<PPT, 2>, grid, block, 0, stream, a);
+  if (nblk <= 4 * kSelThreads) return launch_overlapped(cand_kernel<PPT, 4>, grid, block, 0, stream, a);
+  if (nblk <= 8 * kSelThreads) return launch_overlapped(cand_kernel<PPT, 8>, grid, block, 0, stream, a);
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_candidates(const CandArgs& a, cudaStream_t stream) {
   if (a.rows <= 0) return cudaSuccess;
-  return launch_overlapped(cand_kernel, dim3(a.rows), dim3(kSelThreads), 0, stream, a);
+  const int nblk = (a.T + a.cbs - 1) / a.cbs;
+  if (a.T <= kSelThreads * 8) return launch_cand_ppt<8>(a, nblk, stream);
+  if (a.T <= kSelThreads * 16) return launch_cand_ppt<16>(a, nblk, stream);
+  if (a.T <= kSelThreads * 32) return launch_cand_ppt<32>(a, nblk, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace indexer

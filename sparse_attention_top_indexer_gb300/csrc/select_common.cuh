@@ -23,7 +23,6 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 constexpr int kHistBins = 2048;
-constexpr int kDigit0Shift = 21;   // the first digit: sign, exponent and two mantissa bits
 
 // Radix digits of the selection, most significant first: 11 + 11 + 10 bits. The first
 // digit spreads typical score rows over ~100 bins, so plain shared-memory atomics see
@@ -64,13 +63,11 @@ __device__ __forceinline__ uint32_t cta_scan(uint32_t v, uint32_t& total, Select
   return before_w + incl - v;
 }
 
-// hist0: the first digit's histogram of the row's keys when it is already known (global
-// memory, 2048 16-bit counters: bins 2i and 2i+1 in the low and high half of word i),
-// else nullptr. All NT threads must call it; it ends with every
-// output written by its thread (no trailing barrier).
+// All NT threads must call it; it ends with every output written by its thread (no
+// trailing barrier).
 template <int NT, int KPT>
 __device__ void select_top(const uint32_t (&key)[KPT], int k_eff, int32_t* out, int width, int offset,
-                           SelectShared<NT>& sh, const uint32_t* hist0) {
+                           SelectShared<NT>& sh) {
   constexpr int BPT = kHistBins / NT;   // histogram bins per thread
   static_assert(BPT >= 1 && kHistBins % NT == 0, "thread count must divide the bin count");
   const int tid = threadIdx.x;
@@ -88,14 +85,7 @@ __device__ void select_top(const uint32_t (&key)[KPT], int k_eff, int32_t* out, 
     const int shift = digit_shift(p);
     const uint32_t dm = digit_mask(p);
     uint32_t c[BPT];
-    if (p == 0 && hist0 != nullptr) {
-#pragma unroll
-      for (int q = 0; q < BPT; ++q) {
-        const int bin = hb - q;
-        const uint32_t w2 = __ldcg(hist0 + (bin >> 1));
-        c[q] = (bin & 1) ? (w2 >> 16) : (w2 & 0xFFFFu);
-      }
-    } else {
+    {
       uint32_t* h = sh.hist[p & 1];
 #pragma unroll
       for (int j = 0; j < KPT; ++j) {
