@@ -159,13 +159,16 @@ __global__ void __launch_bounds__(kSelThreads, 1) cand_kernel(const CandArgs a) 
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   if (a.rows <= 0) return cudaSuccess;
-  if (a.T <= kSelThreads * 8) {
-    return launch_overlapped(topk_kernel<kSelThreads, 8>, dim3(a.rows), dim3(kSelThreads), 0, stream, a);
-  } else if (a.T <= kSelThreads * 16) {
-    return launch_overlapped(topk_kernel<kSelThreads, 16>, dim3(a.rows), dim3(kSelThreads), 0, stream, a);
-  } else if (a.T <= kSelThreads * 32) {
-    return launch_overlapped(topk_kernel<kSelThreads, 32>, dim3(a.rows), dim3(kSelThreads), 0, stream, a);
-  }
+  const dim3 grid(a.rows);
+  // eight keys per thread and no more threads than keys up to 8192 positions
+  if (a.T <= 256 * 8) return launch_overlapped(topk_kernel<256, 8>, grid, dim3(256), 0, stream, a);
+  if (a.T <= 512 * 8) return launch_overlapped(topk_kernel<512, 8>, grid, dim3(512), 0, stream, a);
+  if (a.T <= kSelThreads * 8)
+    return launch_overlapped(topk_kernel<kSelThreads, 8>, grid, dim3(kSelThreads), 0, stream, a);
+  if (a.T <= kSelThreads * 16)
+    return launch_overlapped(topk_kernel<kSelThreads, 16>, grid, dim3(kSelThreads), 0, stream, a);
+  if (a.T <= kSelThreads * 32)
+    return launch_overlapped(topk_kernel<kSelThreads, 32>, grid, dim3(kSelThreads), 0, stream, a);
   return cudaErrorInvalidValue;
 }
 
