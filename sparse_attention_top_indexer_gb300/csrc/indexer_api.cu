@@ -283,7 +283,7 @@ int indexer_scores(const IndexerDims* dims, const uint8_t* q_rows, const float* 
   if (ws_bytes < INDEXER_STATUS_BYTES) return fail(INDEXER_ERR_WORKSPACE, "workspace smaller than %d bytes", INDEXER_STATUS_BYTES);
   if (cand_blocks) RETURN_IF(check_cand_dims(dims, T));
   RETURN_IF(check_arch());
-  ScoreArgs a;
+  ScoreArgs a{};
   a.q_rows = q_rows;
   a.w_prime = w_prime;
   a.k_cache = k_cache;
@@ -315,7 +315,7 @@ int indexer_select_candidate_blocks(const IndexerDims* dims, const float* scores
     return fail(INDEXER_ERR_RANGE, "T must equal (start_pos + S) / ratio");
   RETURN_IF(check_cand_dims(dims, T));
   RETURN_IF(check_arch());
-  CandArgs a;
+  CandArgs a{};
   a.scores = scores;
   a.blocks = blocks_out;
   a.rows = B * S;
@@ -331,8 +331,8 @@ int indexer_select_candidate_blocks(const IndexerDims* dims, const float* scores
 }
 
 static int topk_checked(const IndexerDims* dims, const float* scores, int B, int S, int start_pos, int T,
-                        const int32_t* cand, int32_t* out, cudaStream_t stream) {
-  TopkArgs a;
+                        const int32_t* cand, int32_t* out, cudaStream_t stream, bool sparse = false) {
+  TopkArgs a{};
   a.scores = scores;
   a.out = out;
   a.cand = cand;
@@ -345,6 +345,7 @@ static int topk_checked(const IndexerDims* dims, const float* scores, int B, int
   a.offset = dims->offset;
   a.cbk = dims->cand_topk_blocks;
   a.cbs = dims->cand_block_size > 0 ? dims->cand_block_size : 1;
+  a.sparse = sparse ? 1 : 0;
   const cudaError_t e = launch_topk(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "topk launch");
   return INDEXER_OK;
@@ -390,13 +391,19 @@ int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexe
   float* w_prime = reinterpret_cast<float*>(base + l.w_prime);
   float* scores = scores_out ? scores_out : reinterpret_cast<float*>(base + l.scores);
   RETURN_IF(prep_q_checked(dims, q, w, B, S, start_pos, rope_cs, q_rows, w_prime, st));
+  // level two with one query row and no score output: only the kept blocks' keys are
+  // scored and ranked (the other positions of the workspace scores are never read)
+  const bool sparse2 = cand_in && !cand_out && !scores_out && S == 1 && T <= 32768 &&
+                       (long long)dims->cand_topk_blocks * dims->cand_block_size <= 8192;
   if (T > 0) {
-    ScoreArgs a;
+    ScoreArgs a{};
     a.q_rows = q_rows;
     a.w_prime = w_prime;
     a.k_cache = k_cache;
     a.scores = scores;
-    a.cand = nullptr;   // the candidate filter is applied by the top-k (cand_out sees unfiltered scores)
+    // otherwise the candidate filter is applied by the top-k (cand_out sees unfiltered scores)
+    a.cand = sparse2 ? cand_in : nullptr;
+    a.sparse_pages = sparse2 ? 1 : 0;
     a.status = reinterpret_cast<uint32_t*>(base);
     a.B = B;
     a.S = S;
@@ -411,7 +418,7 @@ int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexe
     const cudaError_t e = launch_scores(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "scores launch");
     if (cand_out) {
-      CandArgs c;
+      CandArgs c{};
       c.scores = scores;
       c.blocks = cand_out;
       c.rows = B * S;
@@ -425,7 +432,7 @@ int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexe
       if (e2 != cudaSuccess) return cuda_fail(e2, "candidate launch");
     }
   }
-  RETURN_IF(topk_checked(dims, scores, B, S, start_pos, T, cand_in, topk_out, st));
+  RETURN_IF(topk_checked(dims, scores, B, S, start_pos, T, cand_in, topk_out, st, sparse2 && T > 0));
   return ok();
 }
 

@@ -39,6 +39,7 @@ namespace {
 constexpr int kTileKeys = kPageKeys;                 // one MMA M-tile per page
 constexpr int kStageStride = 9216;                   // page (8704 B) padded to a 1 KB multiple
 constexpr int kEpiThreads = 128;                     // one epilogue warpgroup
+constexpr int kMaxPages = 32768 / kPageKeys;         // pages of the longest row a sparse launch takes
 
 __host__ __device__ constexpr int round_up(int x, int m) { return (x + m - 1) / m * m; }
 __host__ __device__ constexpr uint32_t pow2_cols(int n) {
@@ -77,7 +78,8 @@ struct ScoreCfg {
   static constexpr int NBAR = NSTAGE + 2 * NACC + 1;                          // full, done, empty, q
   static constexpr int OFF_BAR = round_up(OFF_SFW + NCB * 32 * 4, 8);
   static constexpr int OFF_INFO = OFF_BAR + NBAR * 8;                         // tmem base, counters
-  static constexpr int OFF_CAND = round_up(OFF_INFO + 16, 16);
+  static constexpr int OFF_PLIST = round_up(OFF_INFO + 16, 16);   // sparse: the row's pages (+ bitmap)
+  static constexpr int OFF_CAND = OFF_PLIST + (QG == 1 ? kMaxPages * 4 + kMaxPages / 8 : 0);
   static_assert(N <= 256, "MMA N is at most 256");
   static_assert(NACC >= 1, "tensor memory budget");
   static_assert(NBAR <= 32, "barriers are initialised by the lanes of one warp");
@@ -112,13 +114,56 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
   const int b = blockIdx.z;
   const int s0 = blockIdx.y * QG;
   const int nq = min(QG, a.S - s0);
-  const int ntiles = (a.T + kTileKeys - 1) / kTileKeys;
+  int* plist = reinterpret_cast<int*>(smem + C::OFF_PLIST);   // sparse: logical page -> page
+  uint32_t* info = reinterpret_cast<uint32_t*>(smem + C::OFF_INFO);   // [0] tmem, [1] pages issued, [2] mma issued,
+                                                                       // [3] sparse: pages of the row
+  int ntiles = (a.T + kTileKeys - 1) / kTileKeys;
+  if (QG == 1 && a.sparse_pages) {
+    // level two with one query row: only the pages holding a kept candidate block are
+    // scored. Warp 0 marks them in a bitmap and lists them in ascending order.
+    pdl_wait();
+    if (warp == 0) {
+      uint32_t* bits = reinterpret_cast<uint32_t*>(plist + kMaxPages);
+      const int nw = (ntiles + 31) / 32;
+      for (int i = lane; i < nw; i += 32) bits[i] = 0u;
+      __syncwarp();
+      const int32_t* cand = a.cand + (size_t)b * a.cbk;
+      for (int e = lane; e < a.cbk; e += 32) {
+        const int blk = cand[e];
+        if (blk < 0 || (long long)blk * a.cbs >= a.T) continue;
+        const int p0 = (int)(((long long)blk * a.cbs) / kTileKeys);
+        const int p1 = (int)(min((long long)(blk + 1) * a.cbs, (long long)a.T) - 1) / kTileKeys;
+        for (int pg = p0; pg <= p1; ++pg) atomicOr(&bits[pg >> 5], 1u << (pg & 31));
+      }
+      __syncwarp();
+      int total = 0;
+      for (int w0 = 0; w0 < nw; w0 += 32) {
+        const uint32_t word = w0 + lane < nw ? bits[w0 + lane] : 0u;
+        const int cnt = __popc(word);
+        int incl = cnt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, off);
+          if (lane >= off) incl += y;
+        }
+        int slot = total + incl - cnt;
+        for (uint32_t w = word; w; w &= w - 1) plist[slot++] = (w0 + lane) * 32 + (__ffs(w) - 1);
+        total += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) info[3] = (uint32_t)total;
+    }
+    __syncthreads();
+    ntiles = (int)info[3];
+  }
+  const bool sparse = QG == 1 && a.sparse_pages;
+  auto page_of = [&](int logical) { return sparse ? plist[logical] : logical; };
   const int tile0 = blockIdx.x * a.tiles_per_cta;
   const int tile1 = min(tile0 + a.tiles_per_cta, ntiles);
   if (nq <= 0 || tile0 >= tile1) return;
-  // keys the group's last row can see; pages at or past it are fully masked
+  // keys the group's last row can see; pages at or past it are fully masked (a sparse
+  // launch has one row, which sees every key)
   const int vis_hi = min(a.T, (a.start_pos + s0 + nq) / a.ratio);
-  const int tile_vis = min(tile1, (vis_hi + kTileKeys - 1) / kTileKeys);
+  const int tile_vis = sparse ? tile1 : min(tile1, (vis_hi + kTileKeys - 1) / kTileKeys);
   pdl_wait();   // the query rows, weights and pages of the kernels before are complete
   // -inf over the pages no row of the group can see (by the epilogue warps while they wait
   // for the first accumulator, or here when the CTA has nothing to score)
@@ -140,7 +185,6 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
   const uint8_t* qstg = smem + C::OFF_QSTG;
   float* wq = reinterpret_cast<float*>(smem + C::OFF_W);
   uint32_t* sfw = reinterpret_cast<uint32_t*>(smem + C::OFF_SFW);
-  uint32_t* info = reinterpret_cast<uint32_t*>(smem + C::OFF_INFO);   // [0] tmem, [1] pages issued, [2] mma issued
   uint32_t* cand_bits = reinterpret_cast<uint32_t*>(smem + C::OFF_CAND);
   const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
   auto bar_full = [&](int st) { return bar0 + 8u * (uint32_t)st; };
@@ -170,7 +214,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
       info[2] = 0u;
     }
     __syncwarp();
-    if (lane < first) issue_page_load(a, b, tile0 + lane, stg0 + lane * kStageStride, bar_full(lane));
+    if (lane < first) issue_page_load(a, b, page_of(tile0 + lane), stg0 + lane * kStageStride, bar_full(lane));
     __syncwarp();
   } else if (warp == 1) {
     tmem_alloc(smem_u32(&info[0]), C::TMEM_COLS);
@@ -306,11 +350,11 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
       }
       if (et == 0 && i + C::NSTAGE < nt) {
         // the MMA that read this page's stage has completed: refill it
-        issue_page_load(a, b, tile0 + i + C::NSTAGE, stg0 + (i % C::NSTAGE) * kStageStride,
+        issue_page_load(a, b, page_of(tile0 + i + C::NSTAGE), stg0 + (i % C::NSTAGE) * kStageStride,
                         bar_full(i % C::NSTAGE));
         atomicMax(&info[1], (uint32_t)(i + C::NSTAGE + 1));
       }
-      const int t0 = (tile0 + i) * kTileKeys;
+      const int t0 = page_of(tile0 + i) * kTileKeys;
       const int nv = min(kTileKeys, a.T - t0);
       if (et < nv) {
         const int t = t0 + et;
@@ -372,6 +416,8 @@ cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
   using C = ScoreCfg<H, QG, EPI>;
   const int cand_words = a.cand ? ((a.T + a.cbs - 1) / a.cbs + 31) / 32 : 0;
   const size_t smem = (size_t)C::OFF_CAND + (size_t)QG * cand_words * 4 + 1024;   // + base alignment slack
+  if (a.sparse_pages && (QG != 1 || a.S != 1 || a.cand == nullptr || (a.T + kTileKeys - 1) / kTileKeys > kMaxPages))
+    return cudaErrorInvalidValue;
   // the attributes are set once per device and kernel (the dynamic size only grows)
   static int set_bytes[64] = {0};
   int dev = 0;
@@ -385,7 +431,11 @@ cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) set_bytes[dev] = (int)smem;
   }
-  const int ntiles = (a.T + kTileKeys - 1) / kTileKeys;
+  int ntiles = (a.T + kTileKeys - 1) / kTileKeys;
+  if (a.sparse_pages) {   // at most the pages of the kept blocks
+    const long long per_block = (a.cbs + kTileKeys - 1) / kTileKeys + 1;
+    ntiles = (int)min((long long)ntiles, (long long)a.cbk * per_block);
+  }
   const int groups = (a.S + QG - 1) / QG;
   // resident CTAs per SM: tensor memory (512 columns) and shared memory (227 KB) both bound it
   const int by_tmem = 512 / (int)C::TMEM_COLS;

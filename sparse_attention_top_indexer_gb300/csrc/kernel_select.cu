@@ -87,6 +87,81 @@ __global__ void __launch_bounds__(NT, 1) topk_kernel(const TopkArgs a) {
   select_top<NT, KPT>(key, k_eff, out, a.topk, a.offset, sh);
 }
 
+// Level two with one query row: the top-k over the kept candidate blocks only. The row's
+// kept blocks (deduplicated, ascending) are gathered into a list of E = nb * cbs
+// positions; thread t takes list entries [t*KPT, (t+1)*KPT) -- still in position order --
+// and select_top returns list indices, which are then mapped back to positions. The
+// selection equals topk_kernel's with the same filter: same keys, same order.
+template <int NT>
+struct SparseShared {
+  SelectShared<NT> sel;
+  uint32_t bits[kCandMaxBlocks / 32];
+  int blist[kCandMaxBlocks];
+  int nb;
+};
+
+template <int NT, int KPT>
+__global__ void __launch_bounds__(NT, 1) topk_sparse_kernel(const TopkArgs a) {
+  __shared__ SparseShared<NT> sh;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_allow_next();
+  pdl_wait();
+  const int row = blockIdx.x;
+  const int s = row % a.S;
+  const int vis = min(a.T, (a.start_pos + s + 1) / a.ratio);
+  const int k_eff = min(a.topk, a.T);
+  int32_t* out = a.out + (size_t)row * a.topk;
+  const int nblk = (a.T + a.cbs - 1) / a.cbs;
+  const int nw = (nblk + 31) / 32;
+  for (int i = tid; i < nw; i += NT) sh.bits[i] = 0u;
+  __syncthreads();
+  for (int i = tid; i < a.cbk; i += NT) {
+    const int blk = a.cand[(size_t)row * a.cbk + i];
+    if (blk >= 0 && blk < nblk) atomicOr(&sh.bits[blk >> 5], 1u << (blk & 31));
+  }
+  __syncthreads();
+  if (warp == 0) {   // ascending list of the kept blocks
+    int total = 0;
+    for (int w0 = 0; w0 < nw; w0 += 32) {
+      const uint32_t word = w0 + lane < nw ? sh.bits[w0 + lane] : 0u;
+      const int cnt = __popc(word);
+      int incl = cnt;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += y;
+      }
+      int slot = total + incl - cnt;
+      for (uint32_t w = word; w; w &= w - 1) sh.blist[slot++] = (w0 + lane) * 32 + (__ffs(w) - 1);
+      total += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) sh.nb = total;
+  }
+  __syncthreads();
+  const int E = sh.nb * a.cbs;
+  const float* src = a.scores + (size_t)row * a.T;
+  auto pos_of = [&](int e) { return sh.blist[e / a.cbs] * a.cbs + e % a.cbs; };
+  uint32_t key[KPT];
+#pragma unroll
+  for (int j = 0; j < KPT; ++j) {
+    const int e = tid * KPT + j;
+    key[j] = 0u;
+    if (e < E) {
+      const int t = pos_of(e);
+      if (t < vis) {
+        const float f = src[t];
+        if (isfinite(f)) key[j] = order_key(f);
+      }
+    }
+  }
+  select_top<NT, KPT>(key, k_eff, out, a.topk, 0, sh.sel);
+  __syncthreads();   // every list index is written
+  for (int i = tid; i < a.topk; i += NT) {
+    const int g = out[i];
+    if (g >= 0) out[i] = pos_of(g) + a.offset;
+  }
+}
+
 // One CTA per query row. Block score = max finite score over the block's positions
 // t < vis; a block with none keeps key 0 (ineligible). Thread t loads the PPT positions
 // [t*PPT, (t+1)*PPT) at once, folds them into a running maximum per block and merges each
@@ -160,6 +235,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) cand_kernel(const CandArgs a) 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   if (a.rows <= 0) return cudaSuccess;
   const dim3 grid(a.rows);
+  if (a.sparse) {   // kept positions only: at most cbk * cbs of them
+    const long long E = (long long)a.cbk * a.cbs;
+    if (a.cand == nullptr || E > (long long)kSelThreads * 8) return cudaErrorInvalidValue;
+    if (E <= 256 * 8) return launch_overlapped(topk_sparse_kernel<256, 8>, grid, dim3(256), 0, stream, a);
+    if (E <= 512 * 8) return launch_overlapped(topk_sparse_kernel<512, 8>, grid, dim3(512), 0, stream, a);
+    return launch_overlapped(topk_sparse_kernel<kSelThreads, 8>, grid, dim3(kSelThreads), 0, stream, a);
+  }
   // eight keys per thread and no more threads than keys up to 8192 positions
   if (a.T <= 256 * 8) return launch_overlapped(topk_kernel<256, 8>, grid, dim3(256), 0, stream, a);
   if (a.T <= 512 * 8) return launch_overlapped(topk_kernel<512, 8>, grid, dim3(512), 0, stream, a);

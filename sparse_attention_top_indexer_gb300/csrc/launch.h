@@ -69,6 +69,8 @@ struct ScoreArgs {
   uint32_t* status;
   int B, S, H, T, T_cap, start_pos, ratio, cbk, cbs;
   int fill_masked;          // write -inf over key tiles no row of the group can see
+  int sparse_pages;         // one query row (S == 1): score only the pages of its kept blocks
+                            // (cand); keys outside them are not written
   int tiles_per_cta;        // set by the launcher
 };
 cudaError_t launch_scores(const ScoreArgs& a, cudaStream_t stream);
@@ -78,6 +80,7 @@ struct TopkArgs {
   int32_t* out;             // [rows][topk]
   const int32_t* cand;      // [rows][cbk] or nullptr
   int rows, S, T, start_pos, ratio, topk, offset, cbk, cbs;
+  int sparse;               // consider only the positions of the kept blocks (cand), cbk * cbs <= 8192
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
 

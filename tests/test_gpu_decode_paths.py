@@ -96,3 +96,45 @@ def test_fused_workspace_shared_with_prefill(X):
         _, top = _fused(X, dec, dd, qd, wd, t_dec, c_dec, ws)
         X.indexer_status(ws)
         assert torch.equal(top, top_ref)
+
+
+@pytest.mark.parametrize("B,start,cbk,cbs,topk", [
+    (8, 131071, 64, 64, 2048),   # the two-level workload's shape: 64 blocks of 64 of 32768 keys
+    (3, 8191, 20, 48, 300),      # blocks straddling page boundaries
+    (2, 4095, 7, 100, 64),       # few kept keys (700) for top-64
+    (4, 32767, 16, 128, 2047),   # kept keys (2048) just above k
+])
+def test_level_two_kept_blocks_only(X, B, start, cbk, cbs, topk):
+    """Level two with one query row and no score output scores and ranks only the kept
+    blocks' keys; its indices must equal the full-width path's (scores_out given)."""
+    wl = dataclasses.replace(WORKLOADS["two_level_decode"], name=f"sp{B}_{cbs}", B=B, start_pos=start, topk=topk,
+                             cand_topk_blocks=cbk, cand_block_size=cbs)
+    d = C.dims_of(wl)
+    table = C.gpu_table(wl.max_pos)
+    cache = C.gpu_cache(wl, table)
+    q, w = wl.q("cuda", tag="q2"), wl.w("cuda", tag="w2")
+    nblk = -(-wl.T // cbs)
+    rng = np.random.default_rng(B * 1000 + cbs)
+    cand = np.full((B, 1, cbk), -1, np.int32)
+    for b in range(B):
+        n = cbk if b % 2 == 0 else cbk // 2          # some rows padded with -1
+        cand[b, 0, :n] = np.sort(rng.choice(nblk, n, replace=False))
+    if B > 2:                                         # one row unsorted, with a repeated block
+        cand[1, 0, :3] = cand[1, 0, [2, 0, 0]]
+    cand_t = torch.from_numpy(cand).cuda()
+    ws = torch.empty(X.indexer_workspace_size(d, wl.B, 1, wl.start_pos), dtype=torch.uint8, device="cuda")
+    X.indexer_workspace_init(ws)
+    sc = torch.empty((wl.B, 1, wl.T), dtype=torch.float32, device="cuda")
+    top_full = torch.empty((wl.B, 1, wl.topk), dtype=torch.int32, device="cuda")
+    X.indexer_forward(d, q, w, wl.start_pos, table, cache, top_full, ws, cand_in=cand_t, scores_out=sc)
+    top_kept = torch.empty_like(top_full)
+    X.indexer_forward(d, q, w, wl.start_pos, table, cache, top_kept, ws, cand_in=cand_t)
+    X.indexer_status(ws)
+    assert torch.equal(top_kept, top_full)
+    if B * wl.T <= 16384:
+        cos, sin = C.oracle_table(wl.max_pos)
+        ref_cache = C.oracle_cache(wl, cos, sin)
+        ref_top, _, ref_sc = O.forward(C.bits(q), C.bits(w), ref_cache, cos, sin, wl.start_pos, wl.ratio, wl.rope_dim,
+                                       wl.topk, wl.offset, cand_in=cand, cand_block_size=cbs)
+        C.compare_topk(top_kept.cpu().numpy().reshape(-1, wl.topk), ref_top.reshape(-1, wl.topk),
+                       ref_sc.reshape(-1, wl.T), wl.offset)
