@@ -33,15 +33,23 @@
  *     nibble, sign in bit 3 of each nibble) and 4 UE8M0 scale bytes, one per block of
  *     32 values, block 0 in the lowest byte ([attention.py] _indexer_k_cache_head_dim:
  *     64 + 4 = 68). Query rows (q_rows) are stored as such 68-byte rows.
- *   - The key cache is paged, 128 keys (INDEXER_PAGE_KEYS) per page of
- *     INDEXER_PAGE_BYTES = 8704 bytes, still 68 bytes per key: k_cache[B][T_cap/128]
- *     [8704]. Within a page, key m's code byte j sits at
- *         (m/8)*512 + (j/16)*128 + (m%8)*16 + (j%16)          (bytes 0 .. 8191)
- *     -- the tensor cores' K-major core-matrix order, so a page is an MMA operand as it
- *     lies -- and its 4 scale bytes form the 32-bit word at
- *         8192 + ((m%32)*4 + m/32)*4                          (bytes 8192 .. 8703)
- *     -- the order tcgen05.cp expects for 128 rows. T_cap must be a multiple of 128
- *     and k_cache 16-byte aligned.
+ *   - Keys live in pages of 64 keys (INDEXER_PAGE_KEYS), INDEXER_PAGE_BYTES = 4352
+ *     bytes each, still 68 bytes per key. A page is 8 groups of 8 keys, 544 bytes per
+ *     group: the group's 512 code bytes, then its keys' 4-byte scale words. Key m's
+ *     code byte j sits at
+ *         (m/8)*544 + (j/16)*128 + (m%8)*16 + (j%16)
+ *     -- the tensor cores' K-major core-matrix order, so two pages side by side are one
+ *     128-row MMA operand as they lie -- and its scale word at
+ *         (m/8)*544 + 512 + (m%8)*4
+ *     (the scale of block i in byte i). Two ways to hold them:
+ *       * sequence-major: k_cache[B][T_cap/64][4352], sequence b's key t in page t/64
+ *         of its own run (T_cap a multiple of 64, k_cache 16-byte aligned);
+ *       * a page pool k_pool[num_pages][4352] shared by many sequences, with a block
+ *         table giving each sequence's pages (the paged entry points below); slot x of
+ *         the pool is key x % 64 of page x / 64.
+ *   - Score buffers that the selection kernels read (scores of indexer_topk and
+ *     indexer_select_candidate_blocks, scores_out of the forward calls) are 16-byte
+ *     aligned.
  *   - Device-side waits are bounded: a kernel whose wait runs out sets a bit in
  *     the status word at the start of the workspace (indexer_status reads it).
  */
@@ -67,10 +75,13 @@ typedef struct CUstream_st* indexer_stream_t;   /* == cudaStream_t */
 #define INDEXER_ERR_ARCH          -6   /* current device is not sm_103 */
 #define INDEXER_ERR_CUDA          -7   /* a CUDA runtime call or launch failed */
 #define INDEXER_ERR_DEVICE_TIMEOUT -8  /* a bounded device-side wait ran out (indexer_status) */
+/* indexer_status also returns INDEXER_ERR_RANGE when device-side metadata (a block table,
+ * slot mapping, positions or row table) was out of range; the affected keys or rows were
+ * skipped */
 
 #define INDEXER_KEY_ROW_BYTES 68
-#define INDEXER_PAGE_KEYS 128
-#define INDEXER_PAGE_BYTES 8704        /* 128 keys x 68 bytes */
+#define INDEXER_PAGE_KEYS 64
+#define INDEXER_PAGE_BYTES 4352        /* 64 keys x 68 bytes */
 #define INDEXER_STATUS_BYTES 256       /* workspace header holding the status word */
 
 /* Indexer shape and selection parameters ([index-keys] Indexer.__init__). */
@@ -116,7 +127,7 @@ int indexer_rope_table(const IndexerYarn* yarn, int rope_dim, int max_pos, float
  *   k = k_norm(k)            RMSNorm: bf16(w * k / sqrt(mean(k^2) + eps)), f64
  *   RoPE(k[..., -rd:])       interleaved pairs, f32 rotation, rounded to bf16
  *   fp4_act_quant(k, 32)     e2m1 (RNE, ties to even code) with e8m0 scales
- *   key slot s of sequence b: page s / 128, key s % 128 of k_cache[b]
+ *   key slot s of sequence b: page s / 64, key s % 64 of k_cache[b]
  * Slots: start_pos == 0 (prefill) writes slots 0..G-1, group j at RoPE position
  * j*r; start_pos > 0 (decode) needs G == 1 and (start_pos + 1) % r == 0 and
  * writes slot start_pos / r at position start_pos + 1 - r.
@@ -124,7 +135,7 @@ int indexer_rope_table(const IndexerYarn* yarn, int rope_dim, int max_pos, float
  *   wk:       bf16 [D][Din] (row o produces output dim o), 16-byte aligned
  *   k_norm_w: bf16 [D]
  *   rope_cs:  float [max_pos][rd/2][2]; every used position must be < max_pos
- *   k_cache:  uint8 [B][T_cap/128][8704] (paged, see above); last slot < T_cap
+ *   k_cache:  uint8 [B][T_cap/64][4352] (sequence-major, see above); last slot < T_cap
  * ------------------------------------------------------------------------- */
 int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B, int G, int Din,
                       const indexer_bf16* wk, const indexer_bf16* k_norm_w, const float* rope_cs,
@@ -152,7 +163,7 @@ int indexer_prep_q(const IndexerDims* dims, const indexer_bf16* q, const indexer
  *   score[b][s][t] = sum_h w'[b,s,h] * relu(sum_d qhat[b,s,h,d] * khat[b,t,d])
  * over the dequantised fp4 values, products exact, f32 accumulation.
  *   q_rows/w_prime as written by indexer_prep_q (both 16-byte aligned)
- *   k_cache/T_cap: the paged key cache (T_cap a multiple of 128)
+ *   k_cache/T_cap: the sequence-major key cache (T_cap a multiple of 64)
  *   cand_blocks: int32 [B][S][cand_topk_blocks] kept block ids (-1 = none), or
  *                NULL for no candidate filter
  *   scores: float [B][S][T] written (T = (start_pos + S) / r)
@@ -201,7 +212,7 @@ int indexer_topk(const IndexerDims* dims, const float* scores, int B, int S, int
  *   k_cache, T_cap:         as indexer_scores
  *   cand_in / cand_out:     int32 [B][S][cand_topk_blocks] or NULL
  *   topk_out:               int32 [B][S][index_topk]
- *   scores_out:             float [B][S][T] or NULL (the masked scores)
+ *   scores_out:             float [B][S][T] or NULL (the masked scores), 16-byte aligned
  *   ws / ws_bytes:          workspace, at least indexer_workspace_size(),
  *                           initialised once by indexer_workspace_init
  * ------------------------------------------------------------------------- */
@@ -235,6 +246,57 @@ int indexer_forward_noalloc(const IndexerDims* dims, const indexer_bf16* q, cons
                             int start_pos, const float* rope_cs, int max_pos, const uint8_t* k_cache, int T_cap,
                             const int32_t* cand_in, int32_t* cand_out, int32_t* topk_out, float* scores_out,
                             indexer_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Page pool and mixed batches: a server's form of the same path ([attention.py]
+ * DeepseekV4IndexerCache: paged indexer cache of 64-state pages through a slot
+ * mapping; DeepseekV4Indexer.forward over batches that mix decode rows and prefill
+ * chunks). All per-key and per-sequence metadata is DEVICE memory, read by the kernels,
+ * so the calls can be captured in a CUDA graph; the host passes bounds only. Metadata
+ * that is out of range is not dereferenced: the kernel skips the key or row and sets a
+ * status bit that indexer_status reports as INDEXER_ERR_RANGE.
+ * ------------------------------------------------------------------------- */
+
+/* indexer_publish_k_paged -- the key publish of indexer_publish_k for N keys that each
+ * name their own pool slot and RoPE position:
+ *   latent:       bf16 [N][Din], 16-byte aligned (Din a multiple of 8 in [8, 1024])
+ *   positions:    int32 [N], RoPE position of key i (in [0, max_pos))
+ *   slot_mapping: int32 [N], pool slot of key i (page * 64 + key in page); < 0: skipped
+ *   k_pool:       uint8 [num_pages][4352], 16-byte aligned
+ *   ws/ws_bytes:  status word (INDEXER_STATUS_BYTES), initialised by indexer_workspace_init */
+int indexer_publish_k_paged(const IndexerDims* dims, const indexer_bf16* latent, int N, int Din,
+                            const indexer_bf16* wk, const indexer_bf16* k_norm_w, const float* rope_cs, int max_pos,
+                            const int32_t* positions, const int32_t* slot_mapping, uint8_t* k_pool, int num_pages,
+                            void* ws, size_t ws_bytes, indexer_stream_t stream);
+
+/* indexer_forward_paged -- indexer_forward over a batch of n_seq sequences with their own
+ * start positions and query-row counts, keys in a page pool:
+ *   q:           bf16 [Q][H][128] query rows of all sequences, 16-byte aligned
+ *   w:           bf16 [Q][H]
+ *   seq_pos:     int32 [n_seq], start_pos of each sequence
+ *   q_start:     int32 [n_seq + 1], ascending; sequence b owns rows q_start[b] ..
+ *                q_start[b+1]-1, its row s at position seq_pos[b] + s, and sees
+ *                T_b = (seq_pos[b] + S_b) / ratio keys, row s vis(s) of them
+ *   T_max:       a bound on every T_b (the row width of scores_out), <= 32768
+ *   k_pool:      uint8 [num_pages][4352]
+ *   block_table: int32 [n_seq][bt_stride], pool page of each of a sequence's logical
+ *                pages (key t in logical page t / 64); bt_stride >= ceil(T_max / 64)
+ *   cand_in / cand_out: int32 [Q][cand_topk_blocks] or NULL (as indexer_forward)
+ *   topk_out:    int32 [Q][index_topk]
+ *   scores_out:  float [Q][T_max] or NULL; positions >= T_b of a row are not written
+ *   ws/ws_bytes: workspace of at least indexer_workspace_size_paged(), initialised once
+ * Rows that no sequence owns (q_start[0] > 0 or q_start[n_seq] < Q) get all -1. At most
+ * 4096 sequences per call. */
+int indexer_forward_paged(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int Q, int n_seq,
+                          const int32_t* seq_pos, const int32_t* q_start, int T_max, const float* rope_cs,
+                          int max_pos, const uint8_t* k_pool, int num_pages, const int32_t* block_table,
+                          int bt_stride, const int32_t* cand_in, int32_t* cand_out, int32_t* topk_out,
+                          float* scores_out, void* ws, size_t ws_bytes, indexer_stream_t stream);
+
+/* Bytes of workspace indexer_forward_paged needs (0 on invalid sizes). Layout: status
+ * header, quantised query rows, head weights, f32 scores [Q][T_max], row metadata, row
+ * groups. */
+size_t indexer_workspace_size_paged(const IndexerDims* dims, int Q, int n_seq, int T_max);
 
 /* Bytes of workspace indexer_forward needs for these sizes (0 on invalid dims).
  * Layout: status header, quantised query rows, head weights, f32 scores. */

@@ -16,7 +16,8 @@ import torch
 
 __all__ = [
     "IndexerDims", "IndexerYarn", "IndexerError", "load_library", "KEY_ROW_BYTES", "STATUS_BYTES", "PAGE_KEYS",
-    "PAGE_BYTES", "new_key_cache",
+    "PAGE_BYTES", "new_key_cache", "new_key_pool", "indexer_publish_k_paged", "indexer_forward_paged",
+    "indexer_workspace_size_paged",
     "indexer_rope_table", "indexer_publish_k", "indexer_prep_q", "indexer_scores",
     "indexer_select_candidate_blocks", "indexer_topk", "indexer_forward", "indexer_workspace_size",
     "indexer_workspace_init", "indexer_status", "indexer_abi_version", "make_dims", "indexer_forward_noalloc",
@@ -24,8 +25,8 @@ __all__ = [
 ]
 
 KEY_ROW_BYTES = 68
-PAGE_KEYS = 128
-PAGE_BYTES = PAGE_KEYS * KEY_ROW_BYTES    # 8704
+PAGE_KEYS = 64
+PAGE_BYTES = PAGE_KEYS * KEY_ROW_BYTES    # 4352
 STATUS_BYTES = 256
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -69,6 +70,10 @@ _SIGS = {
     "indexer_forward_noalloc": [ctypes.POINTER(IndexerDims), _P, _P, _I, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P,
                                 _P],
     "indexer_workspace_init": [_P, ctypes.c_size_t, _P],
+    "indexer_publish_k_paged": [ctypes.POINTER(IndexerDims), _P, _I, _I, _P, _P, _P, _I, _P, _P, _P, _I, _P,
+                                ctypes.c_size_t, _P],
+    "indexer_forward_paged": [ctypes.POINTER(IndexerDims), _P, _P, _I, _I, _P, _P, _I, _P, _I, _P, _I, _P, _I,
+                              _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "indexer_status": [_P, _P],
 }
 
@@ -87,6 +92,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         fn.restype = ctypes.c_int
     lib.indexer_workspace_size.argtypes = [ctypes.POINTER(IndexerDims), _I, _I, _I]
     lib.indexer_workspace_size.restype = ctypes.c_size_t
+    lib.indexer_workspace_size_paged.argtypes = [ctypes.POINTER(IndexerDims), _I, _I, _I]
+    lib.indexer_workspace_size_paged.restype = ctypes.c_size_t
     lib.indexer_last_error.argtypes = []
     lib.indexer_last_error.restype = ctypes.c_char_p
     lib.indexer_abi_version.argtypes = []
@@ -103,16 +110,27 @@ def make_dims(n_heads: int, ratio: int, index_topk: int, offset: int = 0, rope_d
 
 
 def new_key_cache(B: int, T_cap: int, device="cuda") -> torch.Tensor:
-    """A zeroed paged key cache: uint8 [B, T_cap / 128, 8704] (T_cap a multiple of 128)."""
+    """A zeroed sequence-major key cache: uint8 [B, T_cap / 64, 4352] (T_cap a multiple of 64)."""
     if T_cap % PAGE_KEYS:
-        raise ValueError("T_cap must be a multiple of 128")
+        raise ValueError("T_cap must be a multiple of 64")
     return torch.zeros((B, T_cap // PAGE_KEYS, PAGE_BYTES), dtype=torch.uint8, device=device)
+
+
+def new_key_pool(num_pages: int, device="cuda") -> torch.Tensor:
+    """A zeroed page pool: uint8 [num_pages, 4352], 64 keys per page."""
+    return torch.zeros((num_pages, PAGE_BYTES), dtype=torch.uint8, device=device)
 
 
 def _cache_tcap(k_cache: torch.Tensor) -> int:
     if k_cache.dim() != 3 or k_cache.shape[2] != PAGE_BYTES:
-        raise ValueError("k_cache must be the paged uint8 [B, T_cap / 128, 8704] cache")
+        raise ValueError("k_cache must be the sequence-major uint8 [B, T_cap / 64, 4352] cache")
     return k_cache.shape[1] * PAGE_KEYS
+
+
+def _pool_pages(k_pool: torch.Tensor) -> int:
+    if k_pool.dim() != 2 or k_pool.shape[1] != PAGE_BYTES:
+        raise ValueError("k_pool must be the uint8 [num_pages, 4352] page pool")
+    return k_pool.shape[0]
 
 
 def _check(rc: int):
@@ -152,7 +170,7 @@ def indexer_rope_table(yarn: IndexerYarn, rope_dim: int, max_pos: int, table: to
 
 def indexer_publish_k(dims: IndexerDims, latent: torch.Tensor, wk: torch.Tensor, k_norm_w: torch.Tensor,
                       rope_cs: torch.Tensor, start_pos: int, k_cache: torch.Tensor, stream=None):
-    """latent bf16 [B, G, Din]; wk bf16 [128, Din]; k_norm_w bf16 [128]; k_cache uint8 [B, T_cap/128, 8704]."""
+    """latent bf16 [B, G, Din]; wk bf16 [128, Din]; k_norm_w bf16 [128]; k_cache uint8 [B, T_cap/64, 4352]."""
     B, G, Din = latent.shape
     T_cap = _cache_tcap(k_cache)
     if k_cache.shape[0] != B:
@@ -244,3 +262,47 @@ def indexer_forward_noalloc(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor,
         _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(k_cache, torch.uint8, "k_cache"),
         _cache_tcap(k_cache), _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
         _ptr(topk_out, torch.int32, "topk_out"), _ptr(scores_out, torch.float32, "scores_out"), _stream(stream)))
+
+
+def indexer_publish_k_paged(dims: IndexerDims, latent: torch.Tensor, wk: torch.Tensor, k_norm_w: torch.Tensor,
+                            rope_cs: torch.Tensor, positions: torch.Tensor, slot_mapping: torch.Tensor,
+                            k_pool: torch.Tensor, ws: torch.Tensor, stream=None):
+    """latent bf16 [N, Din]; positions int32 [N] (RoPE position of each key); slot_mapping
+    int32 [N] (pool slot = page * 64 + key in page, < 0 skipped); k_pool uint8 [num_pages, 4352];
+    ws holds the status word."""
+    N, Din = latent.shape
+    if tuple(positions.shape) != (N,) or tuple(slot_mapping.shape) != (N,):
+        raise ValueError("positions and slot_mapping must be [N]")
+    _check(load_library().indexer_publish_k_paged(
+        ctypes.byref(dims), _ptr(latent, torch.bfloat16, "latent"), N, Din, _ptr(wk, torch.bfloat16, "wk"),
+        _ptr(k_norm_w, torch.bfloat16, "k_norm_w"), _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0],
+        _ptr(positions, torch.int32, "positions"), _ptr(slot_mapping, torch.int32, "slot_mapping"),
+        _ptr(k_pool, torch.uint8, "k_pool"), _pool_pages(k_pool), _ptr(ws, None, "ws"),
+        ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def indexer_workspace_size_paged(dims: IndexerDims, Q: int, n_seq: int, T_max: int) -> int:
+    return int(load_library().indexer_workspace_size_paged(ctypes.byref(dims), Q, n_seq, T_max))
+
+
+def indexer_forward_paged(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor, seq_pos: torch.Tensor,
+                          q_start: torch.Tensor, T_max: int, rope_cs: torch.Tensor, k_pool: torch.Tensor,
+                          block_table: torch.Tensor, topk_out: torch.Tensor, ws: torch.Tensor,
+                          cand_in: Optional[torch.Tensor] = None, cand_out: Optional[torch.Tensor] = None,
+                          scores_out: Optional[torch.Tensor] = None, stream=None):
+    """A batch of sequences with their own start positions and query rows, keys in a page
+    pool: q bf16 [Q, H, 128]; w bf16 [Q, H]; seq_pos int32 [n_seq]; q_start int32 [n_seq + 1];
+    block_table int32 [n_seq, bt_stride]; topk_out int32 [Q, index_topk]; scores_out f32
+    [Q, T_max]; see include/indexer.h."""
+    Q = q.shape[0]
+    n_seq = seq_pos.shape[0]
+    if tuple(q_start.shape) != (n_seq + 1,) or block_table.dim() != 2 or block_table.shape[0] != n_seq:
+        raise ValueError("q_start must be [n_seq + 1] and block_table [n_seq, bt_stride]")
+    _check(load_library().indexer_forward_paged(
+        ctypes.byref(dims), _ptr(q, torch.bfloat16, "q"), _ptr(w, torch.bfloat16, "w"), Q, n_seq,
+        _ptr(seq_pos, torch.int32, "seq_pos"), _ptr(q_start, torch.int32, "q_start"), T_max,
+        _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(k_pool, torch.uint8, "k_pool"),
+        _pool_pages(k_pool), _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
+        _ptr(topk_out, torch.int32, "topk_out"), _ptr(scores_out, torch.float32, "scores_out"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))

@@ -12,22 +12,30 @@ constexpr int kHeadDim = 128;           // index_head_dim supported by the kerne
 constexpr int kRowBytes = 68;           // 64 packed e2m1 bytes + 4 UE8M0 scale bytes
 constexpr int kCodeBytes = 64;
 constexpr int kFp4Block = 32;
-constexpr int kPageKeys = 128;          // keys per page of the paged key cache
-constexpr int kPageBytes = kPageKeys * kRowBytes;   // 8704: 8192 code bytes + 512 scale bytes
+constexpr int kPageKeys = 64;           // keys per page of the key cache (a page pool)
+constexpr int kGroupBytes = 544;        // 8 keys: 512 code bytes + 32 scale bytes
+constexpr int kPageBytes = kPageKeys * kRowBytes;   // 4352 = 8 groups of 544 bytes
 
-// Byte offset, within its page, of code byte j (0..63) of key m (0..127): the K-major
-// core-matrix order of the tensor cores (8 rows x 16 bytes per core matrix, 128 bytes
-// between core matrices along K, 512 bytes between 8-row groups).
+// Byte offset, within its page, of code byte j (0..63) of key m: 8-key groups of 544
+// bytes; in a group, the keys' codes in the K-major core-matrix order of the tensor cores
+// (8 rows x 16 bytes per core matrix, 128 bytes between core matrices along K), then
+// the keys' 4-byte scale words. Two pages side by side are one 128-row MMA operand
+// (544 bytes between 8-row groups), so both formulas also hold for m in 64..127 counted
+// from the first of two adjacent pages.
 __host__ __device__ __forceinline__ int page_code_offset(int m, int j) {
-  return (m >> 3) * 512 + (j >> 4) * 128 + (m & 7) * 16 + (j & 15);
+  return (m >> 3) * kGroupBytes + (j >> 4) * 128 + (m & 7) * 16 + (j & 15);
 }
-// Byte offset, within its page, of the 32-bit scale word of key m: lane m % 32, column
-// m / 32 of a 32 x 4 word block (the layout tcgen05.cp copies to 128 lanes).
-__host__ __device__ __forceinline__ int page_scale_offset(int m) { return 8192 + ((m & 31) * 4 + (m >> 5)) * 4; }
+// Byte offset, within its page, of the 32-bit scale word of key m (scale of block i in
+// byte i).
+__host__ __device__ __forceinline__ int page_scale_offset(int m) { return (m >> 3) * kGroupBytes + 512 + (m & 7) * 4; }
 
 // Status bits OR-ed into the workspace status word by kernels whose bounded waits ran out.
 constexpr uint32_t kStatusLoadTimeout = 1u;
 constexpr uint32_t kStatusMmaTimeout = 2u;
+// Status bit of invalid device-side metadata (a block-table entry outside the page pool, a
+// slot or position out of range, inconsistent per-sequence rows): the affected keys or
+// rows are skipped.
+constexpr uint32_t kStatusBadMeta = 4u;
 // One second: a bounded wait gives up after this long and reports through the status word.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 

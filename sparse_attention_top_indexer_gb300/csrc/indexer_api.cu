@@ -10,6 +10,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/indexer.h"
+#include "device_common.cuh"
 #include "launch.h"
 
 using namespace indexer;
@@ -103,6 +104,27 @@ WsLayout ws_layout(const IndexerDims* d, int B, int S, int start_pos) {
   return l;
 }
 
+struct PagedWsLayout {
+  size_t q_rows, w_prime, scores, rows, groups, total;
+  int qg, n_groups;
+};
+
+// status header | query rows | w' | scores [Q][T_max] | row metadata | row groups
+PagedWsLayout paged_ws_layout(const IndexerDims* d, int Q, int n_seq, int T_max) {
+  PagedWsLayout l;
+  const size_t nvec = (size_t)Q * d->n_heads;
+  l.qg = score_group_rows(d->n_heads, Q <= n_seq);
+  const long long g = ((long long)Q + l.qg - 1) / l.qg + n_seq;
+  l.n_groups = (int)(g < Q ? g : Q);
+  l.q_rows = INDEXER_STATUS_BYTES;
+  l.w_prime = l.q_rows + round_up(nvec * INDEXER_KEY_ROW_BYTES, 256);
+  l.scores = l.w_prime + round_up(nvec * sizeof(float), 256);
+  l.rows = l.scores + round_up((size_t)Q * T_max * sizeof(float), 256);
+  l.groups = l.rows + round_up((size_t)Q * sizeof(RowInfo), 256);
+  l.total = l.groups + round_up((size_t)l.n_groups * sizeof(RowGroup), 256);
+  return l;
+}
+
 #define RETURN_IF(x)        \
   do {                      \
     int _rc = (x);          \
@@ -123,7 +145,7 @@ extern "C" {
 
 const char* indexer_last_error(void) { return g_last_error.c_str(); }
 
-int indexer_abi_version(void) { return 200; }
+int indexer_abi_version(void) { return 300; }
 
 // ---------------------------------------------------------------------------- RoPE table
 int indexer_rope_table(const IndexerYarn* y, int rope_dim, int max_pos, float* table, indexer_stream_t stream) {
@@ -183,7 +205,7 @@ int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B
   if (!aligned(k_cache, 16)) return fail(INDEXER_ERR_ALIGN, "k_cache must be 16-byte aligned");
   if (start_pos < 0) return fail(INDEXER_ERR_RANGE, "start_pos must be >= 0");
   const int r = dims->ratio;
-  PublishArgs a;
+  PublishArgs a{};
   if (start_pos == 0) {
     a.slot0 = 0;
     a.pos0 = 0;
@@ -204,7 +226,12 @@ int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B
   a.wk = wk;
   a.knorm = k_norm_w;
   a.rope_cs = rope_cs;
-  a.k_cache = k_cache;
+  a.k_pool = k_cache;
+  a.status = nullptr;
+  a.slots = nullptr;
+  a.positions = nullptr;
+  a.num_pages = 0;
+  a.max_pos = max_pos;
   a.B = B;
   a.G = G;
   a.Din = Din;
@@ -220,7 +247,7 @@ int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B
 static int prep_q_checked(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
                           int start_pos, const float* rope_cs, uint8_t* q_rows, float* w_prime,
                           cudaStream_t stream) {
-  PrepArgs a;
+  PrepArgs a{};
   a.q = q;
   a.w = w;
   a.rope_cs = rope_cs;
@@ -286,15 +313,16 @@ int indexer_scores(const IndexerDims* dims, const uint8_t* q_rows, const float* 
   ScoreArgs a{};
   a.q_rows = q_rows;
   a.w_prime = w_prime;
-  a.k_cache = k_cache;
+  a.k_pool = k_cache;
+  a.pages_per_seq = T_cap / INDEXER_PAGE_KEYS;
   a.scores = scores;
+  a.ld = T;
   a.cand = cand_blocks;
   a.status = static_cast<uint32_t*>(ws);
   a.B = B;
   a.S = S;
   a.H = dims->n_heads;
   a.T = T;
-  a.T_cap = T_cap;
   a.start_pos = start_pos;
   a.ratio = dims->ratio;
   a.cbk = dims->cand_topk_blocks;
@@ -311,6 +339,7 @@ int indexer_select_candidate_blocks(const IndexerDims* dims, const float* scores
   RETURN_IF(check_dims(dims));
   RETURN_IF(check_rows(B, S, start_pos));
   if (!scores || !blocks_out) return fail(INDEXER_ERR_NULL, "scores and blocks_out must not be NULL");
+  if (!aligned(scores, 16)) return fail(INDEXER_ERR_ALIGN, "scores must be 16-byte aligned");
   if (T < 0 || T != (start_pos + S) / dims->ratio)
     return fail(INDEXER_ERR_RANGE, "T must equal (start_pos + S) / ratio");
   RETURN_IF(check_cand_dims(dims, T));
@@ -321,6 +350,7 @@ int indexer_select_candidate_blocks(const IndexerDims* dims, const float* scores
   a.rows = B * S;
   a.S = S;
   a.T = T;
+  a.ld = T;
   a.start_pos = start_pos;
   a.ratio = dims->ratio;
   a.cbk = dims->cand_topk_blocks;
@@ -339,6 +369,7 @@ static int topk_checked(const IndexerDims* dims, const float* scores, int B, int
   a.rows = B * S;
   a.S = S;
   a.T = T;
+  a.ld = T;
   a.start_pos = start_pos;
   a.ratio = dims->ratio;
   a.topk = dims->index_topk;
@@ -356,6 +387,7 @@ int indexer_topk(const IndexerDims* dims, const float* scores, int B, int S, int
   RETURN_IF(check_dims(dims));
   RETURN_IF(check_rows(B, S, start_pos));
   if (!scores || !out) return fail(INDEXER_ERR_NULL, "scores and out must not be NULL");
+  if (!aligned(scores, 16)) return fail(INDEXER_ERR_ALIGN, "scores must be 16-byte aligned");
   if (T < 0 || T != (start_pos + S) / dims->ratio)
     return fail(INDEXER_ERR_RANGE, "T must equal (start_pos + S) / ratio");
   if (T > kTopkMaxT) return fail(INDEXER_ERR_DIMS, "T = %d exceeds the top-k limit of %d", T, kTopkMaxT);
@@ -379,7 +411,7 @@ int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexe
   RETURN_IF(check_cache(k_cache, T_cap, T));
   if (!topk_out || !ws) return fail(INDEXER_ERR_NULL, "topk_out and ws must not be NULL");
   if (!aligned(ws, 256)) return fail(INDEXER_ERR_ALIGN, "ws must be 256-byte aligned");
-  if (scores_out && !aligned(scores_out, 4)) return fail(INDEXER_ERR_ALIGN, "scores_out must be 4-byte aligned");
+  if (scores_out && !aligned(scores_out, 16)) return fail(INDEXER_ERR_ALIGN, "scores_out must be 16-byte aligned");
   if (T > kTopkMaxT) return fail(INDEXER_ERR_DIMS, "T = %d exceeds the top-k limit of %d", T, kTopkMaxT);
   if (cand_in || cand_out) RETURN_IF(check_cand_dims(dims, T));
   const WsLayout l = ws_layout(dims, B, S, start_pos);
@@ -399,8 +431,10 @@ int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexe
     ScoreArgs a{};
     a.q_rows = q_rows;
     a.w_prime = w_prime;
-    a.k_cache = k_cache;
+    a.k_pool = k_cache;
+    a.pages_per_seq = T_cap / INDEXER_PAGE_KEYS;
     a.scores = scores;
+    a.ld = T;
     // otherwise the candidate filter is applied by the top-k (cand_out sees unfiltered scores)
     a.cand = sparse2 ? cand_in : nullptr;
     a.sparse_pages = sparse2 ? 1 : 0;
@@ -409,7 +443,6 @@ int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexe
     a.S = S;
     a.H = dims->n_heads;
     a.T = T;
-    a.T_cap = T_cap;
     a.start_pos = start_pos;
     a.ratio = dims->ratio;
     a.cbk = dims->cand_topk_blocks;
@@ -424,6 +457,7 @@ int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexe
       c.rows = B * S;
       c.S = S;
       c.T = T;
+      c.ld = T;
       c.start_pos = start_pos;
       c.ratio = dims->ratio;
       c.cbk = dims->cand_topk_blocks;
@@ -433,6 +467,196 @@ int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexe
     }
   }
   RETURN_IF(topk_checked(dims, scores, B, S, start_pos, T, cand_in, topk_out, st, sparse2 && T > 0));
+  return ok();
+}
+
+// ---------------------------------------------------------------------------- page pool
+int indexer_publish_k_paged(const IndexerDims* dims, const indexer_bf16* latent, int N, int Din,
+                            const indexer_bf16* wk, const indexer_bf16* k_norm_w, const float* rope_cs, int max_pos,
+                            const int32_t* positions, const int32_t* slot_mapping, uint8_t* k_pool, int num_pages,
+                            void* ws, size_t ws_bytes, indexer_stream_t stream) {
+  RETURN_IF(check_dims(dims));
+  if (!latent || !wk || !k_norm_w || !rope_cs || !positions || !slot_mapping || !k_pool || !ws)
+    return fail(INDEXER_ERR_NULL, "a required pointer is NULL");
+  if (N < 0) return fail(INDEXER_ERR_DIMS, "N must be >= 0 (got %d)", N);
+  if (Din < 8 || Din > 1024 || (Din % 8)) return fail(INDEXER_ERR_DIMS, "Din must be a multiple of 8 in [8, 1024]");
+  if (!aligned(latent, 16) || !aligned(wk, 16)) return fail(INDEXER_ERR_ALIGN, "latent and wk must be 16-byte aligned");
+  if (!aligned(rope_cs, 8)) return fail(INDEXER_ERR_ALIGN, "rope_cs must be 8-byte aligned");
+  if (!aligned(positions, 4) || !aligned(slot_mapping, 4)) return fail(INDEXER_ERR_ALIGN, "positions and slot_mapping must be 4-byte aligned");
+  if (!aligned(k_pool, 16)) return fail(INDEXER_ERR_ALIGN, "k_pool must be 16-byte aligned");
+  if (num_pages < 1 || (long long)num_pages * INDEXER_PAGE_KEYS > (1LL << 31) - 1)
+    return fail(INDEXER_ERR_DIMS, "num_pages must be in [1, 2^31 / %d)", INDEXER_PAGE_KEYS);
+  if (max_pos < 1) return fail(INDEXER_ERR_RANGE, "max_pos must be >= 1");
+  if (ws_bytes < INDEXER_STATUS_BYTES) return fail(INDEXER_ERR_WORKSPACE, "workspace smaller than %d bytes", INDEXER_STATUS_BYTES);
+  if (!aligned(ws, 16)) return fail(INDEXER_ERR_ALIGN, "ws must be 16-byte aligned");
+  RETURN_IF(check_arch());
+  if (N == 0) return ok();
+  PublishArgs a{};
+  a.latent = latent;
+  a.wk = wk;
+  a.knorm = k_norm_w;
+  a.rope_cs = rope_cs;
+  a.k_pool = k_pool;
+  a.status = static_cast<uint32_t*>(ws);
+  a.B = 1;
+  a.G = N;
+  a.Din = Din;
+  a.rope_dim = dims->rope_dim;
+  a.slots = slot_mapping;
+  a.positions = positions;
+  a.num_pages = num_pages;
+  a.max_pos = max_pos;
+  a.eps = dims->norm_eps;
+  const cudaError_t e = launch_publish(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "publish launch");
+  return ok();
+}
+
+static int check_batch(const IndexerDims* d, int Q, int n_seq, int T_max) {
+  if (Q < 1 || n_seq < 1) return fail(INDEXER_ERR_DIMS, "Q and n_seq must be >= 1 (got %d, %d)", Q, n_seq);
+  if (n_seq > kPlanMaxSeq) return fail(INDEXER_ERR_DIMS, "n_seq = %d exceeds the limit of %d", n_seq, kPlanMaxSeq);
+  if (T_max < 1) return fail(INDEXER_ERR_DIMS, "T_max must be >= 1 (got %d)", T_max);
+  if (T_max > kTopkMaxT) return fail(INDEXER_ERR_DIMS, "T_max = %d exceeds the top-k limit of %d", T_max, kTopkMaxT);
+  if ((long long)Q * d->n_heads > (1LL << 31) / 128) return fail(INDEXER_ERR_DIMS, "Q * n_heads too large");
+  return INDEXER_OK;
+}
+
+size_t indexer_workspace_size_paged(const IndexerDims* dims, int Q, int n_seq, int T_max) {
+  if (check_dims(dims) != INDEXER_OK || check_batch(dims, Q, n_seq, T_max) != INDEXER_OK) return 0;
+  return paged_ws_layout(dims, Q, n_seq, T_max).total;
+}
+
+int indexer_forward_paged(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int Q, int n_seq,
+                          const int32_t* seq_pos, const int32_t* q_start, int T_max, const float* rope_cs,
+                          int max_pos, const uint8_t* k_pool, int num_pages, const int32_t* block_table,
+                          int bt_stride, const int32_t* cand_in, int32_t* cand_out, int32_t* topk_out,
+                          float* scores_out, void* ws, size_t ws_bytes, indexer_stream_t stream) {
+  RETURN_IF(check_dims(dims));
+  RETURN_IF(check_batch(dims, Q, n_seq, T_max));
+  if (!q || !w || !seq_pos || !q_start || !rope_cs || !k_pool || !block_table || !topk_out || !ws)
+    return fail(INDEXER_ERR_NULL, "a required pointer is NULL");
+  if (!aligned(q, 16)) return fail(INDEXER_ERR_ALIGN, "q must be 16-byte aligned");
+  if (!aligned(rope_cs, 8)) return fail(INDEXER_ERR_ALIGN, "rope_cs must be 8-byte aligned");
+  if (!aligned(k_pool, 16)) return fail(INDEXER_ERR_ALIGN, "k_pool must be 16-byte aligned");
+  if (!aligned(ws, 256)) return fail(INDEXER_ERR_ALIGN, "ws must be 256-byte aligned");
+  if (!aligned(seq_pos, 4) || !aligned(q_start, 4) || !aligned(block_table, 4))
+    return fail(INDEXER_ERR_ALIGN, "seq_pos, q_start and block_table must be 4-byte aligned");
+  if (scores_out && !aligned(scores_out, 16)) return fail(INDEXER_ERR_ALIGN, "scores_out must be 16-byte aligned");
+  if (max_pos < 1) return fail(INDEXER_ERR_RANGE, "max_pos must be >= 1");
+  if (num_pages < 1) return fail(INDEXER_ERR_DIMS, "num_pages must be >= 1");
+  const int pages_max = (T_max + INDEXER_PAGE_KEYS - 1) / INDEXER_PAGE_KEYS;
+  if (bt_stride < pages_max)
+    return fail(INDEXER_ERR_DIMS, "bt_stride %d < %d pages of T_max = %d keys", bt_stride, pages_max, T_max);
+  if (cand_in || cand_out) RETURN_IF(check_cand_dims(dims, T_max));
+  const PagedWsLayout l = paged_ws_layout(dims, Q, n_seq, T_max);
+  if (ws_bytes < l.total) return fail(INDEXER_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, l.total);
+  RETURN_IF(check_arch());
+  cudaStream_t st = (cudaStream_t)stream;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  uint32_t* status = reinterpret_cast<uint32_t*>(base);
+  uint8_t* q_rows = base + l.q_rows;
+  float* w_prime = reinterpret_cast<float*>(base + l.w_prime);
+  // scores rows are T_max wide; a 16-byte row stride keeps the selection kernels' vector loads
+  const int ld = T_max;
+  float* scores = scores_out ? scores_out : reinterpret_cast<float*>(base + l.scores);
+  RowInfo* rows = reinterpret_cast<RowInfo*>(base + l.rows);
+  RowGroup* groups = reinterpret_cast<RowGroup*>(base + l.groups);
+  {
+    PlanArgs p{};
+    p.seq_pos = seq_pos;
+    p.q_start = q_start;
+    p.rows = rows;
+    p.groups = groups;
+    p.status = status;
+    p.n_seq = n_seq;
+    p.n_rows = Q;
+    p.n_groups = l.n_groups;
+    p.qg = l.qg;
+    p.ratio = dims->ratio;
+    p.T_max = T_max;
+    p.max_pos = max_pos;
+    const cudaError_t e = launch_plan(p, st);
+    if (e != cudaSuccess) return cuda_fail(e, "plan launch");
+  }
+  {
+    PrepArgs a{};
+    a.q = q;
+    a.w = w;
+    a.rope_cs = rope_cs;
+    a.q_rows = q_rows;
+    a.w_prime = w_prime;
+    a.rows = rows;
+    a.n_vec = (long long)Q * dims->n_heads;
+    a.S = 1;
+    a.H = dims->n_heads;
+    a.rope_dim = dims->rope_dim;
+    a.w_scale = (float)(1.0 / std::sqrt((double)dims->head_dim) / std::sqrt((double)dims->n_heads));
+    const cudaError_t e = launch_prep_q(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "prep_q launch");
+  }
+  const bool single = l.qg == 1 && Q <= n_seq;
+  const bool sparse2 = cand_in && !cand_out && !scores_out && single &&
+                       (long long)dims->cand_topk_blocks * dims->cand_block_size <= 8192;
+  {
+    ScoreArgs a{};
+    a.q_rows = q_rows;
+    a.w_prime = w_prime;
+    a.k_pool = k_pool;
+    a.block_table = block_table;
+    a.bt_stride = bt_stride;
+    a.num_pages = num_pages;
+    a.groups = groups;
+    a.n_groups = l.n_groups;
+    a.scores = scores;
+    a.ld = ld;
+    a.cand = sparse2 ? cand_in : nullptr;
+    a.sparse_pages = sparse2 ? 1 : 0;
+    a.status = status;
+    a.B = n_seq;
+    a.S = single ? 1 : 2;   // selects the single-row (decode) kernel, matching l.qg
+    a.H = dims->n_heads;
+    a.T = T_max;
+    a.ratio = dims->ratio;
+    a.cbk = dims->cand_topk_blocks;
+    a.cbs = dims->cand_block_size > 0 ? dims->cand_block_size : 1;
+    a.fill_masked = scores_out ? 1 : 0;
+    const cudaError_t e = launch_scores(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "scores launch");
+  }
+  if (cand_out) {
+    CandArgs c{};
+    c.scores = scores;
+    c.blocks = cand_out;
+    c.rinfo = rows;
+    c.rows = Q;
+    c.S = 1;
+    c.T = T_max;
+    c.ld = ld;
+    c.ratio = dims->ratio;
+    c.cbk = dims->cand_topk_blocks;
+    c.cbs = dims->cand_block_size;
+    const cudaError_t e = launch_candidates(c, st);
+    if (e != cudaSuccess) return cuda_fail(e, "candidate launch");
+  }
+  {
+    TopkArgs a{};
+    a.scores = scores;
+    a.out = topk_out;
+    a.cand = cand_in;
+    a.rinfo = rows;
+    a.rows = Q;
+    a.S = 1;
+    a.T = T_max;
+    a.ld = ld;
+    a.ratio = dims->ratio;
+    a.topk = dims->index_topk;
+    a.offset = dims->offset;
+    a.cbk = dims->cand_topk_blocks;
+    a.cbs = dims->cand_block_size > 0 ? dims->cand_block_size : 1;
+    a.sparse = sparse2 ? 1 : 0;
+    const cudaError_t e = launch_topk(a, st);
+    if (e != cudaSuccess) return cuda_fail(e, "topk launch");
+  }
   return ok();
 }
 
@@ -455,6 +679,9 @@ int indexer_status(void* ws, indexer_stream_t stream) {
     e = cudaMemsetAsync(ws, 0, sizeof(word), st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(e, "status clear");
+    if (word & kStatusBadMeta)
+      return fail(INDEXER_ERR_RANGE, "device-side metadata out of range: a block-table entry, slot, position or "
+                  "row table was invalid and its keys or rows were skipped (status 0x%x)", word);
     return fail(INDEXER_ERR_DEVICE_TIMEOUT, "device wait ran out (status 0x%x)", word);
   }
   return ok();

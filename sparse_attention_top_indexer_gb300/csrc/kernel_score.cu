@@ -36,10 +36,11 @@ namespace indexer {
 
 namespace {
 
-constexpr int kTileKeys = kPageKeys;                 // one MMA M-tile per page
-constexpr int kStageStride = 9216;                   // page (8704 B) padded to a 1 KB multiple
+constexpr int kTileKeys = 2 * kPageKeys;             // one MMA M-tile: two 64-key pages side by side
+constexpr int kStageStride = 9216;                   // two pages (8704 B) padded to a 1 KB multiple
 constexpr int kEpiThreads = 128;                     // one epilogue warpgroup
 constexpr int kMaxPages = 32768 / kPageKeys;         // pages of the longest row a sparse launch takes
+constexpr int kMaxTilesCta = 256;                    // tiles one CTA takes at most
 
 __host__ __device__ constexpr int round_up(int x, int m) { return (x + m - 1) / m * m; }
 __host__ __device__ constexpr uint32_t pow2_cols(int n) {
@@ -78,7 +79,8 @@ struct ScoreCfg {
   static constexpr int NBAR = NSTAGE + 2 * NACC + 1;                          // full, done, empty, q
   static constexpr int OFF_BAR = round_up(OFF_SFW + NCB * 32 * 4, 8);
   static constexpr int OFF_INFO = OFF_BAR + NBAR * 8;                         // tmem base, counters
-  static constexpr int OFF_PLIST = round_up(OFF_INFO + 16, 16);   // sparse: the row's pages (+ bitmap)
+  static constexpr int OFF_PTAB = round_up(OFF_INFO + 16, 16);   // pool page of each half of this CTA's tiles
+  static constexpr int OFF_PLIST = OFF_PTAB + 2 * kMaxTilesCta * 4;   // sparse: the row's pages (+ bitmap)
   static constexpr int OFF_CAND = OFF_PLIST + (QG == 1 ? kMaxPages * 4 + kMaxPages / 8 : 0);
   static_assert(N <= 256, "MMA N is at most 256");
   static_assert(NACC >= 1, "tensor memory budget");
@@ -87,11 +89,22 @@ struct ScoreCfg {
   static_assert(TMEM_NEED <= (int)TMEM_COLS && TMEM_COLS <= 512u, "tensor memory budget");
 };
 
-__device__ __forceinline__ void issue_page_load(const ScoreArgs& a, int b, int tile, uint32_t stage_addr,
+// Pool page of logical page lp of sequence b: through the block table, or the sequence's
+// own run of pages. -1: no page (lp < 0); -2: a block-table entry outside the pool.
+__device__ __forceinline__ int pool_page(const ScoreArgs& a, int b, int lp) {
+  if (lp < 0) return -1;
+  if (a.block_table == nullptr) return b * a.pages_per_seq + lp;
+  const int p = a.block_table[(size_t)b * a.bt_stride + lp];
+  return (p >= 0 && p < a.num_pages) ? p : -2;
+}
+
+// Requests the two pages of a tile into a stage (a missing half is not copied; its keys
+// are never stored).
+__device__ __forceinline__ void issue_tile_load(const ScoreArgs& a, int p0, int p1, uint32_t stage_addr,
                                                 uint32_t bar) {
-  mbar_arrive_expect_tx(bar, (uint32_t)kPageBytes);
-  bulk_g2s(stage_addr, a.k_cache + ((size_t)b * (a.T_cap / kPageKeys) + tile) * kPageBytes, (uint32_t)kPageBytes,
-           bar);
+  mbar_arrive_expect_tx(bar, (uint32_t)((p0 >= 0 ? kPageBytes : 0) + (p1 >= 0 ? kPageBytes : 0)));
+  if (p0 >= 0) bulk_g2s(stage_addr, a.k_pool + (size_t)p0 * kPageBytes, (uint32_t)kPageBytes, bar);
+  if (p1 >= 0) bulk_g2s(stage_addr + kPageBytes, a.k_pool + (size_t)p1 * kPageBytes, (uint32_t)kPageBytes, bar);
 }
 
 // Lane 0 waits (bounded) for the phase; the warp follows it. Warp-uniform result.
@@ -111,28 +124,48 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1024-byte aligned base
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_allow_next();
-  const int b = blockIdx.z;
-  const int s0 = blockIdx.y * QG;
-  const int nq = min(QG, a.S - s0);
-  int* plist = reinterpret_cast<int*>(smem + C::OFF_PLIST);   // sparse: logical page -> page
-  uint32_t* info = reinterpret_cast<uint32_t*>(smem + C::OFF_INFO);   // [0] tmem, [1] pages issued, [2] mma issued,
+  // this CTA's query rows: nq consecutive rows (row0 ..) of sequence b, the first at
+  // position pos0; the sequence has Tb keys
+  int b, row0, nq, pos0, Tb;
+  if (a.groups == nullptr) {
+    b = blockIdx.z;
+    const int s0 = blockIdx.y * QG;
+    nq = min(QG, a.S - s0);
+    row0 = b * a.S + s0;
+    pos0 = a.start_pos + s0;
+    Tb = a.T;
+  } else {
+    const int g = blockIdx.z * gridDim.y + blockIdx.y;
+    if (g >= a.n_groups) return;
+    pdl_wait();   // the groups were written by the kernels before
+    const RowGroup rg = a.groups[g];
+    b = rg.b;
+    row0 = rg.row0;
+    nq = min(rg.nq, QG);
+    pos0 = rg.pos0;
+    Tb = min(rg.T, a.T);
+  }
+  int* plist = reinterpret_cast<int*>(smem + C::OFF_PLIST);   // sparse: the row's pages, ascending
+  int* ptab = reinterpret_cast<int*>(smem + C::OFF_PTAB);     // pool page of each half of this CTA's tiles
+  uint32_t* info = reinterpret_cast<uint32_t*>(smem + C::OFF_INFO);   // [0] tmem, [1] tiles issued, [2] mma issued,
                                                                        // [3] sparse: pages of the row
-  int ntiles = (a.T + kTileKeys - 1) / kTileKeys;
-  if (QG == 1 && a.sparse_pages) {
+  const bool sparse = QG == 1 && a.sparse_pages;
+  int npages = (Tb + kPageKeys - 1) / kPageKeys;   // logical pages to score, two per tile
+  if (sparse) {
     // level two with one query row: only the pages holding a kept candidate block are
     // scored. Warp 0 marks them in a bitmap and lists them in ascending order.
     pdl_wait();
     if (warp == 0) {
       uint32_t* bits = reinterpret_cast<uint32_t*>(plist + kMaxPages);
-      const int nw = (ntiles + 31) / 32;
+      const int nw = (npages + 31) / 32;
       for (int i = lane; i < nw; i += 32) bits[i] = 0u;
       __syncwarp();
-      const int32_t* cand = a.cand + (size_t)b * a.cbk;
+      const int32_t* cand = a.cand + (size_t)row0 * a.cbk;
       for (int e = lane; e < a.cbk; e += 32) {
         const int blk = cand[e];
-        if (blk < 0 || (long long)blk * a.cbs >= a.T) continue;
-        const int p0 = (int)(((long long)blk * a.cbs) / kTileKeys);
-        const int p1 = (int)(min((long long)(blk + 1) * a.cbs, (long long)a.T) - 1) / kTileKeys;
+        if (blk < 0 || (long long)blk * a.cbs >= Tb) continue;
+        const int p0 = (int)(((long long)blk * a.cbs) / kPageKeys);
+        const int p1 = (int)(min((long long)(blk + 1) * a.cbs, (long long)Tb) - 1) / kPageKeys;
         for (int pg = p0; pg <= p1; ++pg) atomicOr(&bits[pg >> 5], 1u << (pg & 31));
       }
       __syncwarp();
@@ -153,24 +186,29 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
       if (lane == 0) info[3] = (uint32_t)total;
     }
     __syncthreads();
-    ntiles = (int)info[3];
+    npages = (int)info[3];
   }
-  const bool sparse = QG == 1 && a.sparse_pages;
-  auto page_of = [&](int logical) { return sparse ? plist[logical] : logical; };
+  const int ntiles = (npages + 1) / 2;
   const int tile0 = blockIdx.x * a.tiles_per_cta;
   const int tile1 = min(tile0 + a.tiles_per_cta, ntiles);
   if (nq <= 0 || tile0 >= tile1) return;
-  // keys the group's last row can see; pages at or past it are fully masked (a sparse
+  // logical page of half h of tile i (-1: none)
+  auto lpage = [&](int i, int h) {
+    const int k = 2 * i + h;
+    return k < npages ? (sparse ? plist[k] : k) : -1;
+  };
+  // keys the group's last row can see; tiles at or past it are fully masked (a sparse
   // launch has one row, which sees every key)
-  const int vis_hi = min(a.T, (a.start_pos + s0 + nq) / a.ratio);
+  const int vis_hi = min(Tb, (pos0 + nq) / a.ratio);
   const int tile_vis = sparse ? tile1 : min(tile1, (vis_hi + kTileKeys - 1) / kTileKeys);
   pdl_wait();   // the query rows, weights and pages of the kernels before are complete
-  // -inf over the pages no row of the group can see (by the epilogue warps while they wait
+  // -inf over the tiles no row of the group can see (by the epilogue warps while they wait
   // for the first accumulator, or here when the CTA has nothing to score)
   auto fill_masked = [&](int first_thread, int nthreads) {
-    const int t_begin = max(tile0, tile_vis) * kTileKeys, t_end = min(tile1 * kTileKeys, a.T);
+    if (sparse) return;
+    const int t_begin = max(tile0, tile_vis) * kTileKeys, t_end = min(tile1 * kTileKeys, Tb);
     for (int qi = 0; qi < nq; ++qi) {
-      float* dst = a.scores + ((size_t)b * a.S + s0 + qi) * a.T;
+      float* dst = a.scores + (size_t)(row0 + qi) * a.ld;
       for (int t = t_begin + first_thread; t < t_end; t += nthreads) dst[t] = -__int_as_float(0x7f800000);
     }
   };
@@ -178,7 +216,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
     if (a.fill_masked) fill_masked(tid, C::THREADS);
     return;
   }
-  const int nt = tile_vis - tile0;   // pages this CTA scores
+  const int nt = tile_vis - tile0;   // tiles this CTA scores
 
   uint8_t* qB = smem + C::OFF_QB;
   const uint8_t* stg = smem + C::OFF_STG;
@@ -192,11 +230,23 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
   auto bar_empty = [&](int c) { return bar0 + 8u * (uint32_t)(C::NSTAGE + C::NACC + c); };
   const uint32_t bar_q = bar0 + 8u * (uint32_t)(C::NSTAGE + 2 * C::NACC);
   const uint32_t stg0 = smem_u32(stg);
+  // pool pages of tile i's halves into ptab (an entry outside the pool is reported and its
+  // keys score -inf)
+  auto fill_ptab = [&](int i) {
+    int p[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      p[h] = pool_page(a, b, lpage(tile0 + i, h));
+      if (p[h] == -2) atomicOr(a.status, kStatusBadMeta);
+      ptab[2 * i + h] = p[h];
+    }
+    return make_int2(p[0], p[1]);
+  };
 
   // Setup: warp 0 initialises the barriers and requests the group's query rows and head
-  // weights, then the first NSTAGE pages (one lane per page); warp 1 allocates tensor
-  // memory meanwhile.
-  const size_t qrow0 = ((size_t)b * a.S + s0) * H;   // first query row of the group
+  // weights, then the first NSTAGE tiles (one lane per tile); warp 1 allocates tensor
+  // memory meanwhile; warps 2-3 look up the pool pages of the remaining tiles.
+  const size_t qrow0 = (size_t)row0 * H;   // first query-head row of the group
   const int first = min(nt, C::NSTAGE);
   if (warp == 0) {
     if (lane < C::NBAR) {
@@ -214,11 +264,16 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
       info[2] = 0u;
     }
     __syncwarp();
-    if (lane < first) issue_page_load(a, b, page_of(tile0 + lane), stg0 + lane * kStageStride, bar_full(lane));
+    if (lane < first) {
+      const int2 p = fill_ptab(lane);
+      issue_tile_load(a, max(p.x, -1), max(p.y, -1), stg0 + lane * kStageStride, bar_full(lane));
+    }
     __syncwarp();
   } else if (warp == 1) {
     tmem_alloc(smem_u32(&info[0]), C::TMEM_COLS);
     tmem_relinquish();
+  } else if (warp < 4) {
+    for (int i = first + tid - 64; i < nt; i += 64) fill_ptab(i);
   }
   tc_fence_before();
   __syncthreads();
@@ -287,8 +342,8 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
         const uint32_t pa = stg0 + (uint32_t)(st * kStageStride);
         const uint32_t acc = tmem + (uint32_t)(c * C::NP);
         const uint32_t sfa = tmem + (uint32_t)(C::SFA_COL + 8 * c);
-        mma_mxf4(acc, smem_desc(pa, 128, 512), smem_desc(qb, 128, 512), idesc, sfa, tmem + C::SFB_COL, 0u);
-        mma_mxf4(acc, smem_desc(pa + 256, 128, 512), smem_desc(qb + 256, 128, 512), idesc, sfa + 4,
+        mma_mxf4(acc, smem_desc(pa, 128, kGroupBytes), smem_desc(qb, 128, 512), idesc, sfa, tmem + C::SFB_COL, 0u);
+        mma_mxf4(acc, smem_desc(pa + 256, 128, kGroupBytes), smem_desc(qb + 256, 128, 512), idesc, sfa + 4,
                  tmem + C::SFB_COL + C::SB, 1u);
         tc_commit(bar_done(c));
         info[2] = (uint32_t)(i + 1);
@@ -309,7 +364,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
       named_bar_sync(2, EPI * kEpiThreads);
       for (int i = ge; i < nq * a.cbk; i += EPI * kEpiThreads) {
         const int qi = i / a.cbk;
-        const int blk = a.cand[((size_t)b * a.S + s0 + qi) * a.cbk + (i % a.cbk)];
+        const int blk = a.cand[(size_t)(row0 + qi) * a.cbk + (i % a.cbk)];
         if (blk >= 0 && blk < cand_words * 32) atomicOr(&cand_bits[qi * cand_words + (blk >> 5)], 1u << (blk & 31));
       }
     }
@@ -350,28 +405,30 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
       }
       if (et == 0 && i + C::NSTAGE < nt) {
         // the MMA that read this page's stage has completed: refill it
-        issue_page_load(a, b, page_of(tile0 + i + C::NSTAGE), stg0 + (i % C::NSTAGE) * kStageStride,
+        const int nx = i + C::NSTAGE;
+        issue_tile_load(a, max(ptab[2 * nx], -1), max(ptab[2 * nx + 1], -1), stg0 + (i % C::NSTAGE) * kStageStride,
                         bar_full(i % C::NSTAGE));
         atomicMax(&info[1], (uint32_t)(i + C::NSTAGE + 1));
       }
-      const int t0 = page_of(tile0 + i) * kTileKeys;
-      const int nv = min(kTileKeys, a.T - t0);
-      if (et < nv) {
-        const int t = t0 + et;
+      // this thread's key: key et % 64 of the tile's half et / 64
+      const int h = et >> 6;
+      const int lp = lpage(tile0 + i, h);
+      const int t = lp * kPageKeys + (et & (kPageKeys - 1));
+      if (lp >= 0 && t < Tb) {
+        const bool present = ptab[2 * i + h] >= 0;   // else a block-table entry outside the pool
 #pragma unroll
         for (int qi = 0; qi < QG; ++qi) {
           if (qi < nq) {
             float acc = part[qi][0];
 #pragma unroll
             for (int p = 1; p < P; ++p) acc += part[qi][p];
-            const int s = s0 + qi;
-            const int vis = min(a.T, (a.start_pos + s + 1) / a.ratio);
-            bool keep = t < vis;
+            const int vis = min(Tb, (pos0 + qi + 1) / a.ratio);
+            bool keep = present && t < vis;
             if (a.cand) {
               const int blk = t / a.cbs;
               keep = keep && ((cand_bits[qi * cand_words + (blk >> 5)] >> (blk & 31)) & 1u);
             }
-            a.scores[((size_t)b * a.S + s) * a.T + t] = keep ? acc : -__int_as_float(0x7f800000);
+            a.scores[(size_t)(row0 + qi) * a.ld + t] = keep ? acc : -__int_as_float(0x7f800000);
           }
         }
       }
@@ -416,7 +473,8 @@ cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
   using C = ScoreCfg<H, QG, EPI>;
   const int cand_words = a.cand ? ((a.T + a.cbs - 1) / a.cbs + 31) / 32 : 0;
   const size_t smem = (size_t)C::OFF_CAND + (size_t)QG * cand_words * 4 + 1024;   // + base alignment slack
-  if (a.sparse_pages && (QG != 1 || a.S != 1 || a.cand == nullptr || (a.T + kTileKeys - 1) / kTileKeys > kMaxPages))
+  if (a.sparse_pages && (QG != 1 || (a.groups == nullptr && a.S != 1) || a.cand == nullptr ||
+                         (a.T + kPageKeys - 1) / kPageKeys > kMaxPages))
     return cudaErrorInvalidValue;
   // the attributes are set once per device and kernel (the dynamic size only grows)
   static int set_bytes[64] = {0};
@@ -432,26 +490,34 @@ cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
     if (dev >= 0 && dev < 64) set_bytes[dev] = (int)smem;
   }
   int ntiles = (a.T + kTileKeys - 1) / kTileKeys;
-  if (a.sparse_pages) {   // at most the pages of the kept blocks
-    const long long per_block = (a.cbs + kTileKeys - 1) / kTileKeys + 1;
-    ntiles = (int)min((long long)ntiles, (long long)a.cbk * per_block);
+  if (a.sparse_pages) {   // at most the pages of the kept blocks, two per tile
+    const long long pages = (long long)a.cbk * ((a.cbs + kPageKeys - 1) / kPageKeys + 1);
+    ntiles = (int)min((long long)ntiles, (pages + 1) / 2);
   }
-  const int groups = (a.S + QG - 1) / QG;
+  const long long base = a.groups ? (long long)a.n_groups : (long long)((a.S + QG - 1) / QG) * a.B;
+  if (base <= 0) return cudaSuccess;
   // resident CTAs per SM: tensor memory (512 columns) and shared memory (227 KB) both bound it
   const int by_tmem = 512 / (int)C::TMEM_COLS;
   const int by_smem = (int)((227 * 1024) / (smem + 1024));
   const int per_sm = by_tmem < by_smem ? by_tmem : by_smem;
   const long long target = (long long)sm_count() * (per_sm > 0 ? per_sm : 1);
-  const long long base = (long long)groups * a.B;
-  // few query groups (decode): split each sequence's pages over CTAs, one wave in total
+  // few query groups (decode): split each sequence's tiles over CTAs, one wave in total
   int tpc = ntiles;
   if (base < target) {
     tpc = (int)((ntiles * base + target - 1) / target);
     if (tpc < 1) tpc = 1;
     while (tpc < ntiles && (long long)((ntiles + tpc - 1) / tpc) * base > target) ++tpc;
   }
+  if (tpc > kMaxTilesCta) tpc = kMaxTilesCta;
   a.tiles_per_cta = tpc;
-  dim3 grid((ntiles + tpc - 1) / tpc, groups, a.B);
+  dim3 grid((ntiles + tpc - 1) / tpc, 1, 1);
+  if (a.groups) {   // group g = blockIdx.z * gridDim.y + blockIdx.y
+    grid.y = (unsigned)min(base, 65535ll);
+    grid.z = (unsigned)((base + grid.y - 1) / grid.y);
+  } else {
+    grid.y = (unsigned)((a.S + QG - 1) / QG);
+    grid.z = (unsigned)a.B;
+  }
   return launch_overlapped(score_kernel<H, QG, EPI>, grid, dim3(C::THREADS), smem, stream, a);
 }
 
@@ -459,6 +525,8 @@ cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
 
 cudaError_t launch_scores(const ScoreArgs& a, cudaStream_t stream) {
   if (a.T <= 0) return cudaSuccess;
+  // S == 1: one query row per group (a uniform batch of single rows, or row groups planned
+  // with score_group_rows(H, true))
   const bool single = a.S == 1;
   switch (a.H) {
     // decode: one query row, N = H, two CTAs per SM; several rows: N = 128 (three
@@ -469,6 +537,17 @@ cudaError_t launch_scores(const ScoreArgs& a, cudaStream_t stream) {
     case 64: return single ? launch_cfg<64, 1, 1>(a, stream) : launch_cfg<64, 2, 2>(a, stream);
     case 128: return single ? launch_cfg<128, 1, 1>(a, stream) : launch_cfg<128, 1, 2>(a, stream);
     default: return cudaErrorInvalidValue;
+  }
+}
+
+int score_group_rows(int H, bool single) {
+  if (single) return 1;
+  switch (H) {
+    case 8: return 16;
+    case 16: return 8;
+    case 32: return 4;
+    case 64: return 2;
+    default: return 1;
   }
 }
 

@@ -20,6 +20,17 @@ namespace {
 
 constexpr int kSelThreads = 1024;
 
+// (vis, T) of a row: keys it may see and keys of its sequence, from the per-row metadata
+// of a batch with per-sequence positions, or from the uniform S / start_pos.
+__device__ __forceinline__ int2 row_extent(const RowInfo* ri, int row, int S, int T, int start_pos, int ratio) {
+  if (ri != nullptr) {
+    const RowInfo r = ri[row];
+    const int t = max(0, min(r.T, T));
+    return make_int2(max(0, min(r.vis, t)), t);
+  }
+  return make_int2(min(T, (start_pos + row % S + 1) / ratio), T);
+}
+
 struct TopkKept {
   uint32_t kept[kCandMaxBlocks / 32];
 };
@@ -39,9 +50,9 @@ __global__ void __launch_bounds__(NT, 1) topk_kernel(const TopkArgs a) {
   pdl_allow_next();
   pdl_wait();
   const int row = blockIdx.x;
-  const int s = row % a.S;
-  const int vis = min(a.T, (a.start_pos + s + 1) / a.ratio);
-  const int k_eff = min(a.topk, a.T);
+  const int2 ext = row_extent(a.rinfo, row, a.S, a.T, a.start_pos, a.ratio);
+  const int vis = ext.x;
+  const int k_eff = min(a.topk, ext.y);
   int32_t* out = a.out + (size_t)row * a.topk;
   if (a.cand == nullptr && vis <= k_eff) {
     for (int i = tid; i < a.topk; i += NT) out[i] = i < vis ? i + a.offset : -1;
@@ -59,7 +70,7 @@ __global__ void __launch_bounds__(NT, 1) topk_kernel(const TopkArgs a) {
   __syncthreads();
 
   const int base = tid * KPT;
-  const float* src = a.scores + (size_t)row * a.T;
+  const float* src = a.scores + (size_t)row * a.ld;
   auto make_key = [&](float f, int t) -> uint32_t {
     bool ok = t < vis && isfinite(f);
     if (ok && a.cand) {
@@ -69,7 +80,7 @@ __global__ void __launch_bounds__(NT, 1) topk_kernel(const TopkArgs a) {
     return ok ? order_key(f) : 0u;
   };
   uint32_t key[KPT];
-  if ((a.T & 3) == 0) {   // rows start 16-byte aligned: float4 loads
+  if ((a.ld & 3) == 0) {   // rows start 16-byte aligned: float4 loads
 #pragma unroll
     for (int j = 0; j < KPT; j += 4) {
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -107,9 +118,9 @@ __global__ void __launch_bounds__(NT, 1) topk_sparse_kernel(const TopkArgs a) {
   pdl_allow_next();
   pdl_wait();
   const int row = blockIdx.x;
-  const int s = row % a.S;
-  const int vis = min(a.T, (a.start_pos + s + 1) / a.ratio);
-  const int k_eff = min(a.topk, a.T);
+  const int2 ext = row_extent(a.rinfo, row, a.S, a.T, a.start_pos, a.ratio);
+  const int vis = ext.x;
+  const int k_eff = min(a.topk, ext.y);
   int32_t* out = a.out + (size_t)row * a.topk;
   const int nblk = (a.T + a.cbs - 1) / a.cbs;
   const int nw = (nblk + 31) / 32;
@@ -139,7 +150,7 @@ __global__ void __launch_bounds__(NT, 1) topk_sparse_kernel(const TopkArgs a) {
   }
   __syncthreads();
   const int E = sh.nb * a.cbs;
-  const float* src = a.scores + (size_t)row * a.T;
+  const float* src = a.scores + (size_t)row * a.ld;
   auto pos_of = [&](int e) { return sh.blist[e / a.cbs] * a.cbs + e % a.cbs; };
   uint32_t key[KPT];
 #pragma unroll
@@ -180,15 +191,14 @@ __global__ void __launch_bounds__(kSelThreads, 1) cand_kernel(const CandArgs a) 
   pdl_allow_next();
   pdl_wait();
   const int row = blockIdx.x;
-  const int s = row % a.S;
-  const int vis = min(a.T, (a.start_pos + s + 1) / a.ratio);
+  const int vis = row_extent(a.rinfo, row, a.S, a.T, a.start_pos, a.ratio).x;
   const int nblk = (a.T + a.cbs - 1) / a.cbs;
   for (int i = tid; i < nblk; i += kSelThreads) sh.bkeys[i] = 0u;
   __syncthreads();
-  const float* src = a.scores + (size_t)row * a.T;
+  const float* src = a.scores + (size_t)row * a.ld;
   const int t_begin = tid * PPT;
   uint32_t pk[PPT];   // this thread's position keys (0 = not a candidate value)
-  if ((a.T & 3) == 0) {   // rows start 16-byte aligned: float4 loads
+  if ((a.ld & 3) == 0) {   // rows start 16-byte aligned: float4 loads
 #pragma unroll
     for (int j = 0; j < PPT; j += 4) {
       float4 v = make_float4(0.f, 0.f, 0.f, 0.f);

@@ -50,7 +50,7 @@ cudaError_t launch_rope_table(const RopeFreqs& freqs, int half, int max_pos, flo
 //  3. RoPE on the last rope_dim dims at the group position: interleaved pair (2i, 2i+1)
 //     rotated by table entry i with the f32 sequence x0*c - x1*s, x0*s + x1*c, then bf16.
 //  4. e2m1/e8m0 quantisation per 32-block (warp w owns block w); the 64 code bytes and
-//     4 scale bytes go to the key's places in its 128-key page.
+//     4 scale bytes go to the key's places in its 64-key page of the pool.
 template <int TPO>   // threads per output dimension (1 or 4)
 __global__ void __launch_bounds__(kHeadDim * TPO) publish_kernel(PublishArgs a) {
   constexpr int NT = kHeadDim * TPO;
@@ -64,6 +64,18 @@ __global__ void __launch_bounds__(kHeadDim * TPO) publish_kernel(PublishArgs a) 
   pdl_wait();
   const int key = blockIdx.x;
   const int b = key / a.G, j = key % a.G;
+  // the key's slot in the page pool and its RoPE position
+  long long slot = (long long)b * a.T_cap + a.slot0 + j;
+  int pos = a.pos0 + j * a.pos_step;
+  if (a.slots != nullptr) {
+    slot = a.slots[key];
+    pos = a.positions[key];
+    if (slot < 0) return;   // a padding entry: nothing to publish
+    if (slot >= (long long)a.num_pages * kPageKeys || pos < 0 || pos >= a.max_pos) {
+      if (tid == 0) atomicOr(a.status, kStatusBadMeta);
+      return;
+    }
+  }
   const int o = tid / TPO, part = tid % TPO;
   // every global read of the key is issued before the first is used
   const int span = ((a.Din + 8 * TPO - 1) / (8 * TPO)) * 8;   // elements per part, a multiple of 8
@@ -78,8 +90,7 @@ __global__ void __launch_bounds__(kHeadDim * TPO) publish_kernel(PublishArgs a) 
   const int rstart = kHeadDim - a.rope_dim;
   float2 cs = make_float2(1.f, 0.f);
   if (tid < kHeadDim && tid >= rstart)
-    cs = reinterpret_cast<const float2*>(a.rope_cs)[(size_t)(a.pos0 + j * a.pos_step) * (a.rope_dim / 2) +
-                                                    ((tid - rstart) >> 1)];
+    cs = reinterpret_cast<const float2*>(a.rope_cs)[(size_t)pos * (a.rope_dim / 2) + ((tid - rstart) >> 1)];
   const uint16_t* src = a.latent + ((size_t)b * a.G + j) * a.Din;
   for (int i = tid; i < a.Din; i += NT) lat[i] = bf16_to_f32(src[i]);
   __syncthreads();
@@ -181,9 +192,8 @@ __global__ void __launch_bounds__(kHeadDim * TPO) publish_kernel(PublishArgs a) 
   const int e = e8m0_exponent(amax);
   const float yq = __fmul_rn(y, pow2_neg(e));
   const float partner = __shfl_down_sync(0xffffffffu, yq, 1);
-  const int slot = a.slot0 + j;
-  const int m = slot % kPageKeys;
-  uint8_t* page = a.k_cache + ((size_t)b * (a.T_cap / kPageKeys) + slot / kPageKeys) * kPageBytes;
+  const int m = (int)(slot % kPageKeys);
+  uint8_t* page = a.k_pool + (size_t)(slot / kPageKeys) * kPageBytes;
   if ((lane & 1) == 0) page[page_code_offset(m, (warp * 32 + lane) >> 1)] = (uint8_t)e2m1x2(yq, partner);
   if (lane == 0) page[page_scale_offset(m) + warp] = (uint8_t)(e + 127);
 }
@@ -198,7 +208,8 @@ cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream) {
 
 // ---------------------------------------------------------------------------- query prep
 // 16 threads per query-head vector, 8 consecutive bf16 each (one 16-byte load); RoPE
-// at position start_pos + s with the same f32 rotation as the keys; the 4 threads of a
+// at the row's position (start_pos + s of its sequence) with the same f32 rotation as
+// the keys; the 4 threads of a
 // 32-block share its amax by shuffles; each thread writes 4 code bytes, the first
 // thread of a block its scale byte. w' = f32(w) * head_dim^-0.5 * H^-0.5.
 __global__ void __launch_bounds__(256) prep_q_kernel(PrepArgs a) {
@@ -210,8 +221,7 @@ __global__ void __launch_bounds__(256) prep_q_kernel(PrepArgs a) {
   if (v >= a.n_vec) return;   // whole 16-lane groups leave together
   const int lane = tid & 31;
   const unsigned gmask = 0xFFFFu << (lane & 16);
-  const int s = (int)((v / a.H) % a.S);
-  const int pos = a.start_pos + s;
+  const int pos = a.rows ? a.rows[v / a.H].pos : a.start_pos + (int)((v / a.H) % a.S);
   const uint4 raw = *reinterpret_cast<const uint4*>(a.q + v * kHeadDim + j * 8);
   float2 c[4];
   load_rope_slice(reinterpret_cast<const float2*>(a.rope_cs) + (size_t)pos * (a.rope_dim / 2), j, a.rope_dim, c);
@@ -226,6 +236,143 @@ __global__ void __launch_bounds__(256) prep_q_kernel(PrepArgs a) {
 cudaError_t launch_prep_q(const PrepArgs& a, cudaStream_t stream) {
   const long long blocks = (a.n_vec + 15) / 16;
   return launch_overlapped(prep_q_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, a);
+}
+
+// ---------------------------------------------------------------------------- batch plan
+// A batch of n_seq sequences; sequence b owns rows q_start[b] .. q_start[b+1]-1, row s of
+// it at position seq_pos[b] + s, and sees (seq_pos[b] + S_b) / ratio keys. The plan writes
+// each row's metadata (position, visible keys, keys of its sequence) and the row groups
+// of up to qg consecutive rows of one sequence that the score kernel's CTAs take. Every
+// CTA loads the sequence table into shared memory and prefix-sums the group counts;
+// thread i then describes row i and group i by binary search. A sequence whose rows or
+// positions are inconsistent (rows outside [0, n_rows) or in decreasing order, a negative
+// position, positions past the RoPE table, more keys than T_max) is reported in the status
+// word and has no rows; rows no sequence owns see no keys.
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanPerThread = kPlanMaxSeq / kPlanThreads;
+
+__device__ __forceinline__ int last_le(const int* v, int n, int x) {   // largest i < n with v[i] <= x, or -1
+  int lo = 0, hi = n;   // answer in [lo - 1, hi - 1]
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (v[mid] <= x) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo - 1;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(PlanArgs a) {
+  __shared__ int qs[kPlanMaxSeq + 1];   // first row of each sequence
+  __shared__ int gs[kPlanMaxSeq + 1];   // first group of each sequence
+  __shared__ uint32_t ok[kPlanMaxSeq / 32];
+  __shared__ int wsum[kPlanThreads / 32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_allow_next();
+  pdl_wait();
+  // 1. per sequence: validity and group count (kPlanPerThread consecutive sequences a
+  //    thread). Rows must be ascending across the whole table, else no sequence has rows.
+  int q0v[kPlanPerThread], q1v[kPlanPerThread], spv[kPlanPerThread];
+  bool rows_bad = false;
+  for (int i = tid; i < kPlanMaxSeq / 32; i += kPlanThreads) ok[i] = 0u;
+#pragma unroll
+  for (int u = 0; u < kPlanPerThread; ++u) {
+    const int b = tid * kPlanPerThread + u;
+    q0v[u] = q1v[u] = spv[u] = 0;
+    if (b < a.n_seq) {
+      q0v[u] = a.q_start[b];
+      q1v[u] = a.q_start[b + 1];
+      spv[u] = a.seq_pos[b];
+      rows_bad = rows_bad || q0v[u] < 0 || q1v[u] < q0v[u] || q1v[u] > a.n_rows;
+    }
+  }
+  rows_bad = __syncthreads_or(rows_bad) != 0;
+  int cnt[kPlanPerThread];
+  int tsum = 0;
+#pragma unroll
+  for (int u = 0; u < kPlanPerThread; ++u) {
+    const int b = tid * kPlanPerThread + u;
+    cnt[u] = 0;
+    if (b < a.n_seq) {
+      const long long last = (long long)spv[u] + (q1v[u] - q0v[u]);   // one past the last row's position
+      const bool valid = !rows_bad && spv[u] >= 0 && last <= (long long)a.max_pos &&
+                         last / a.ratio <= (long long)a.T_max;
+      qs[b] = q0v[u];
+      if (valid) {
+        atomicOr(&ok[b >> 5], 1u << (b & 31));
+        cnt[u] = (q1v[u] - q0v[u] + a.qg - 1) / a.qg;
+      } else if (blockIdx.x == 0) {
+        atomicOr(a.status, kStatusBadMeta);
+      }
+    }
+    tsum += cnt[u];
+  }
+  // 2. exclusive prefix of the group counts
+  int incl = tsum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = wsum[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, off);
+      if (lane >= off) w += y;
+    }
+    wsum[lane] = w;   // inclusive over warps
+  }
+  __syncthreads();
+  int run = (warp > 0 ? wsum[warp - 1] : 0) + incl - tsum;
+#pragma unroll
+  for (int u = 0; u < kPlanPerThread; ++u) {
+    const int b = tid * kPlanPerThread + u;
+    if (b < a.n_seq) gs[b] = run;
+    run += cnt[u];
+  }
+  if (tid == 0) {
+    gs[a.n_seq] = wsum[kPlanThreads / 32 - 1];
+    qs[a.n_seq] = a.n_rows;
+  }
+  __syncthreads();
+  const int i = blockIdx.x * kPlanThreads + tid;
+  // 3. row i
+  if (i < a.n_rows) {
+    RowInfo r = {0, 0, 0, -1};
+    const int b = last_le(qs, a.n_seq, i);
+    if (b >= 0 && ((ok[b >> 5] >> (b & 31)) & 1u) && i < a.q_start[b + 1]) {
+      const int sp = a.seq_pos[b], S_b = a.q_start[b + 1] - qs[b];
+      r.pos = sp + (i - qs[b]);
+      r.T = (sp + S_b) / a.ratio;
+      r.vis = min(r.T, (r.pos + 1) / a.ratio);
+      r.b = b;
+    }
+    a.rows[i] = r;
+  }
+  // 4. group i
+  if (i < a.n_groups) {
+    RowGroup g = {0, 0, 0, 0, 0, 0, 0, 0};
+    if (i < gs[a.n_seq]) {
+      const int b = last_le(gs, a.n_seq, i);
+      const int k = i - gs[b];
+      const int sp = a.seq_pos[b], S_b = a.q_start[b + 1] - qs[b];
+      g.b = b;
+      g.row0 = qs[b] + k * a.qg;
+      g.nq = min(a.qg, S_b - k * a.qg);
+      g.pos0 = sp + k * a.qg;
+      g.T = (sp + S_b) / a.ratio;
+    }
+    a.groups[i] = g;
+  }
+}
+
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream) {
+  const int n = a.n_rows > a.n_groups ? a.n_rows : a.n_groups;
+  if (n <= 0) return cudaSuccess;
+  return launch_overlapped(plan_kernel, dim3((unsigned)((n + kPlanThreads - 1) / kPlanThreads)), dim3(kPlanThreads),
+                           0, stream, a);
 }
 
 }  // namespace indexer

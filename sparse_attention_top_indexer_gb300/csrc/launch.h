@@ -35,59 +35,106 @@ struct RopeFreqs {
 
 cudaError_t launch_rope_table(const RopeFreqs& freqs, int half, int max_pos, float* table, cudaStream_t stream);
 
+// Key slots: a key cache is a pool of 64-key pages ([num_pages][4352] bytes). Slot x is
+// key x % 64 of pool page x / 64. A sequence-major cache k_cache[B][T_cap / 64][4352] is
+// the pool whose sequence b owns pages b * T_cap / 64 onwards, so key t of sequence b sits
+// in slot b * T_cap + t.
 struct PublishArgs {
-  const uint16_t* latent;   // [B][G][Din]
+  const uint16_t* latent;   // [n_keys][Din] (sequence-major: [B][G][Din])
   const uint16_t* wk;       // [128][Din]
   const uint16_t* knorm;    // [128]
   const float* rope_cs;     // [max_pos][rd/2][2]
-  uint8_t* k_cache;         // [B][T_cap][68]
+  uint8_t* k_pool;          // [num_pages][4352]
+  uint32_t* status = nullptr;   // status word (paged publish) or nullptr
   int B, G, Din, rope_dim, T_cap;
-  int slot0;                // cache slot of group 0
-  int pos0, pos_step;       // RoPE position of group j: pos0 + j * pos_step
+  int slot0;                // sequence-major: slot of group 0 within its sequence
+  int pos0, pos_step;       // sequence-major: RoPE position of group j is pos0 + j * pos_step
+  // paged publish (slots != nullptr): key i goes to slot slots[i] (< 0: skipped) at RoPE
+  // position positions[i]; B = 1, G = n_keys
+  const int32_t* slots = nullptr;
+  const int32_t* positions = nullptr;
+  int num_pages, max_pos;
   float eps;
 };
 cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream);
 
+// Per-row metadata of a batch of sequences with their own start positions and query-row
+// counts, built on the device by the plan kernel.
+struct alignas(16) RowInfo {
+  int pos;   // RoPE position of the row (start_pos_b + s)
+  int vis;   // keys it may see: min(T_b, (pos + 1) / ratio)
+  int T;     // keys of its sequence: min(T_max, (start_pos_b + S_b) / ratio)
+  int b;     // its sequence
+};
+// A group of up to QG consecutive rows of one sequence (one score CTA row).
+struct alignas(16) RowGroup {
+  int b, row0, nq, pos0;   // sequence, first row, rows, position of the first row
+  int T, pad0, pad1, pad2;  // keys of the sequence
+};
+
+struct PlanArgs {
+  const int32_t* seq_pos;   // [n_seq] start position of each sequence
+  const int32_t* q_start;   // [n_seq + 1] first query row of each sequence
+  RowInfo* rows;            // [n_rows]
+  RowGroup* groups;         // [n_groups]
+  uint32_t* status;
+  int n_seq, n_rows, n_groups, qg, ratio, T_max, max_pos;
+};
+cudaError_t launch_plan(const PlanArgs& a, cudaStream_t stream);
+constexpr int kPlanMaxSeq = 4096;   // sequences one batch may hold
+
 struct PrepArgs {
-  const uint16_t* q;        // [B][S][H][128]
-  const uint16_t* w;        // [B][S][H]
+  const uint16_t* q;        // [rows][H][128]
+  const uint16_t* w;        // [rows][H]
   const float* rope_cs;
-  uint8_t* q_rows;          // [B][S][H][68]
-  float* w_prime;           // [B][S][H]
-  long long n_vec;          // B * S * H
+  uint8_t* q_rows;          // [rows][H][68]
+  float* w_prime;           // [rows][H]
+  const RowInfo* rows = nullptr;   // per-row positions, or nullptr: row r is at start_pos + r % S
+  long long n_vec;          // rows * H
   int S, H, rope_dim, start_pos;
   float w_scale;            // head_dim^-0.5 * H^-0.5
 };
 cudaError_t launch_prep_q(const PrepArgs& a, cudaStream_t stream);
 
 struct ScoreArgs {
-  const uint8_t* q_rows;    // [B][S][H][68]
-  const float* w_prime;     // [B][S][H]
-  const uint8_t* k_cache;   // [B][T_cap / 128][8704] pages
-  float* scores;            // [B][S][T]
-  const int32_t* cand;      // [B][S][cbk] or nullptr
+  const uint8_t* q_rows;    // [rows][H][68]
+  const float* w_prime;     // [rows][H]
+  const uint8_t* k_pool;    // [num_pages][4352]
+  const int32_t* block_table = nullptr;   // [B][bt_stride] pool page of each logical page, or nullptr:
+                                // sequence b owns pages b * pages_per_seq onwards
+  int bt_stride, num_pages, pages_per_seq;
+  const RowGroup* groups = nullptr;   // row groups of a batch with per-sequence positions, or nullptr:
+                            // B sequences of S rows at start_pos
+  float* scores;            // [rows][ld]
+  int ld;
+  const int32_t* cand = nullptr;   // [rows][cbk] or nullptr
   uint32_t* status;
-  int B, S, H, T, T_cap, start_pos, ratio, cbk, cbs;
+  int B, S, H, T, start_pos, ratio, cbk, cbs;   // with groups: T = T_max, S unused
+  int n_groups;             // with groups
   int fill_masked;          // write -inf over key tiles no row of the group can see
-  int sparse_pages;         // one query row (S == 1): score only the pages of its kept blocks
-                            // (cand); keys outside them are not written
+  int sparse_pages;         // one query row per group: score only the pages of its kept
+                            // blocks (cand); keys outside them are not written
   int tiles_per_cta;        // set by the launcher
 };
 cudaError_t launch_scores(const ScoreArgs& a, cudaStream_t stream);
+// Query rows per score CTA (QG) for n_heads H: 1 for single rows (decode), else 128 / H.
+int score_group_rows(int H, bool single);
 
 struct TopkArgs {
-  const float* scores;      // [rows][T]
+  const float* scores;      // [rows][ld]
   int32_t* out;             // [rows][topk]
-  const int32_t* cand;      // [rows][cbk] or nullptr
-  int rows, S, T, start_pos, ratio, topk, offset, cbk, cbs;
+  const int32_t* cand = nullptr;     // [rows][cbk] or nullptr
+  const RowInfo* rinfo = nullptr;    // per-row vis / T, or nullptr (uniform S, T, start_pos)
+  int rows, S, T, ld, start_pos, ratio, topk, offset, cbk, cbs;
   int sparse;               // consider only the positions of the kept blocks (cand), cbk * cbs <= 8192
 };
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream);
 
 struct CandArgs {
-  const float* scores;      // [rows][T]
+  const float* scores;      // [rows][ld]
   int32_t* blocks;          // [rows][cbk]
-  int rows, S, T, start_pos, ratio, cbk, cbs;
+  const RowInfo* rinfo = nullptr;    // per-row vis / T, or nullptr
+  int rows, S, T, ld, start_pos, ratio, cbk, cbs;
 };
 cudaError_t launch_candidates(const CandArgs& a, cudaStream_t stream);
 

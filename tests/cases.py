@@ -70,15 +70,27 @@ def gpu_cache(wl: Workload, table: torch.Tensor, latent=None, decode_latent=None
 
 
 def pages_to_rows(pages) -> np.ndarray:
-    """The paged key cache [B, P, 8704] as 68-byte key rows [B, P*128, 68]: within a page,
-    key m's code byte j sits at (m/8)*512 + (j/16)*128 + (m%8)*16 + j%16 and its scale
-    word at 8192 + ((m%32)*4 + m/32)*4 (a pure reordering of bytes)."""
+    """Key pages [..., P, 4352] as 68-byte key rows [..., P*64, 68]: a page is 8 groups of
+    544 bytes; in group g, key m = 8g + r has code byte j at (j/16)*128 + r*16 + j%16 and
+    its scale word at 512 + r*4 (a pure reordering of bytes)."""
     if isinstance(pages, torch.Tensor):
         pages = pages.cpu().numpy()
-    B, P, _ = pages.shape
-    codes = pages[:, :, :8192].reshape(B, P, 16, 4, 8, 16).transpose(0, 1, 2, 4, 3, 5).reshape(B, P, 128, 64)
-    sc = pages[:, :, 8192:].reshape(B, P, 32, 4, 4).transpose(0, 1, 3, 2, 4).reshape(B, P, 128, 4)
-    return np.concatenate([codes, sc], axis=-1).reshape(B, P * 128, 68)
+    lead, P = pages.shape[:-2], pages.shape[-2]
+    g = pages.reshape(-1, P, 8, 544)
+    n = g.shape[0]
+    codes = g[..., :512].reshape(n, P, 8, 4, 8, 16).transpose(0, 1, 2, 4, 3, 5).reshape(n, P, 64, 64)
+    sc = g[..., 512:].reshape(n, P, 64, 4)
+    return np.concatenate([codes, sc], axis=-1).reshape(*lead, P * 64, 68)
+
+
+def pool_to_rows(pool, block_table_row, n_keys: int) -> np.ndarray:
+    """The first n_keys key rows [n_keys, 68] of one sequence of a page pool [num_pages, 4352],
+    following its block-table row (pool page of each logical page)."""
+    if isinstance(pool, torch.Tensor):
+        pool = pool.cpu().numpy()
+    bt = np.asarray(block_table_row.cpu() if isinstance(block_table_row, torch.Tensor) else block_table_row)
+    npages = (n_keys + 63) // 64
+    return pages_to_rows(pool[bt[:npages]])[:n_keys]
 
 
 def oracle_cache(wl: Workload, cos, sin, latent=None, decode_latent=None) -> np.ndarray:

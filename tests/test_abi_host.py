@@ -42,7 +42,7 @@ def test_struct_layouts_match_header(X):
 
 
 def test_abi_version(X):
-    assert X.indexer_abi_version() == 200   # paged key cache, workspace head with row counters
+    assert X.indexer_abi_version() == 300   # 64-key pages, page pool + mixed batches
 
 
 def test_workspace_size_host_only(X):
@@ -71,8 +71,8 @@ def test_validation_rejects_without_launch(X):
     # T beyond the cache
     assert lib.indexer_forward(ctypes.byref(d), 0x1000, 0x2000, 1, 1000, 0, 0x3000, 1000, 0x4000, 128, None, None,
                                0x5000, None, 0x6000, 1 << 20, None) == -4
-    # cache capacity that is not a whole number of 128-key pages
-    assert lib.indexer_forward(ctypes.byref(d), 0x1000, 0x2000, 1, 8, 0, 0x3000, 64, 0x4000, 64, None, None,
+    # cache capacity that is not a whole number of 64-key pages
+    assert lib.indexer_forward(ctypes.byref(d), 0x1000, 0x2000, 1, 8, 0, 0x3000, 64, 0x4000, 96, None, None,
                                0x5000, None, 0x6000, 1 << 20, None) == -2
     # workspace too small
     assert lib.indexer_forward(ctypes.byref(d), 0x1000, 0x2000, 1, 8, 0, 0x3000, 64, 0x4000, 128, None, None,
@@ -88,6 +88,45 @@ def test_validation_rejects_without_launch(X):
     # candidate filter with too many blocks
     d4 = X.make_dims(n_heads=64, ratio=1, index_topk=16, cand_topk_blocks=4, cand_block_size=1)
     assert lib.indexer_select_candidate_blocks(ctypes.byref(d4), 0x1000, 1, 1, 9999, 10000, 0x2000, None) == -3
+
+
+def test_paged_workspace_size_host_only(X):
+    d = X.make_dims(n_heads=64, ratio=4, index_topk=2048)
+    r = lambda x: (x + 255) // 256 * 256
+    # 40 rows of 8 sequences (a prefill chunk and decode rows), T_max 8192: status, q rows,
+    # w', scores, row metadata (16 B), row groups (32 B; at most ceil(40 / 2) + 8 = 28)
+    n = X.indexer_workspace_size_paged(d, 40, 8, 8192)
+    assert n == 256 + r(40 * 64 * 68) + r(40 * 64 * 4) + r(40 * 8192 * 4) + r(40 * 16) + r(28 * 32)
+    # decode only (one row per sequence): one group per row
+    n1 = X.indexer_workspace_size_paged(d, 8, 8, 8192)
+    assert n1 == 256 + r(8 * 64 * 68) + r(8 * 64 * 4) + r(8 * 8192 * 4) + r(8 * 16) + r(8 * 32)
+    assert X.indexer_workspace_size_paged(d, 8, 4097, 8192) == 0     # too many sequences
+    assert X.indexer_workspace_size_paged(d, 8, 8, 40000) == 0       # beyond the top-k width
+
+
+def test_paged_validation_rejects_without_launch(X):
+    lib = X.load_library()
+    d = X.make_dims(n_heads=64, ratio=4, index_topk=16)
+    ws = 1 << 24
+    args = dict(q=0x1000, w=0x2000, Q=8, n_seq=2, seq_pos=0x3000, q_start=0x3100, T_max=1024, rope=0x4000,
+                max_pos=4096, pool=0x5000, num_pages=64, bt=0x6000, bt_stride=16, topk=0x7000, ws=0x8000)
+
+    def fwd(**kw):
+        a = dict(args, **kw)
+        return lib.indexer_forward_paged(ctypes.byref(d), a["q"], a["w"], a["Q"], a["n_seq"], a["seq_pos"],
+                                         a["q_start"], a["T_max"], a["rope"], a["max_pos"], a["pool"],
+                                         a["num_pages"], a["bt"], a["bt_stride"], None, None, a["topk"], None,
+                                         a["ws"], ws, None)
+    assert fwd(bt=None) == -1                        # block table required
+    assert fwd(pool=0x5008) == -2                    # pool not 16-byte aligned
+    assert fwd(bt_stride=15) == -3                   # fewer table columns than pages of T_max
+    assert fwd(n_seq=5000) == -3                     # too many sequences
+    assert fwd(T_max=40000) == -3                    # beyond the top-k width
+    # paged publish: a status workspace is required, the pool must be aligned
+    assert lib.indexer_publish_k_paged(ctypes.byref(d), 0x1000, 4, 128, 0x2000, 0x3000, 0x4000, 100, 0x5000,
+                                       0x6000, 0x7000, 8, None, 0, None) == -1
+    assert lib.indexer_publish_k_paged(ctypes.byref(d), 0x1000, 4, 128, 0x2000, 0x3000, 0x4000, 100, 0x5000,
+                                       0x6000, 0x7008, 8, 0x8000, 256, None) == -2
 
 
 def test_missing_library_fails_loudly(tmp_path):

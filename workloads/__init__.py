@@ -232,3 +232,117 @@ WORKLOADS = {
                  heavy_frac=0.05, heavy_scale=8.0),
     ]
 }
+
+
+@dataclasses.dataclass(frozen=True)
+class MixedBatch:
+    """A server batch: sequences with their own start position and query-row count (decode
+    rows and prefill chunks), their keys in one shared pool of 64-key pages assigned in a
+    seeded random order. Sequence b holds keys 0 .. T_b - 1 (key j published at RoPE
+    position j * ratio, as a prefill publishes it) with T_b = (start_pos_b + S_b) // ratio;
+    its rows are q_start[b] .. q_start[b+1] - 1 of the flat query batch."""
+    name: str
+    seqs: tuple            # ((start_pos, S), ...)
+    ratio: int
+    H: int
+    topk: int
+    offset: int = 0
+    D: int = 128
+    rope_dim: int = 64
+    cand_topk_blocks: int = 0
+    cand_block_size: int = 0
+    spare_pages: int = 8   # pool pages no sequence owns
+    norm_eps: float = 1e-6
+    seed: int = 0
+
+    @property
+    def n_seq(self) -> int:
+        return len(self.seqs)
+
+    @property
+    def Q(self) -> int:
+        return sum(S for _, S in self.seqs)
+
+    @property
+    def q_start(self) -> list:
+        out = [0]
+        for _, S in self.seqs:
+            out.append(out[-1] + S)
+        return out
+
+    @property
+    def T_list(self) -> list:
+        return [(sp + S) // self.ratio for sp, S in self.seqs]
+
+    @property
+    def T_max(self) -> int:
+        return max(max(self.T_list), 1)
+
+    @property
+    def max_pos(self) -> int:
+        return max(sp + S for sp, S in self.seqs)
+
+    @property
+    def pages(self) -> list:
+        return [(t + 63) // 64 for t in self.T_list]
+
+    @property
+    def num_pages(self) -> int:
+        return sum(self.pages) + self.spare_pages
+
+    @property
+    def bt_stride(self) -> int:
+        return max((self.T_max + 63) // 64, 1)
+
+    def block_table(self) -> torch.Tensor:
+        """int32 [n_seq, bt_stride]: a seeded permutation of the pool's pages dealt to the
+        sequences in order; unused entries -1."""
+        u = uniform_f64(self.seed, f"{self.name}/pages", (self.num_pages,))
+        perm = torch.argsort(u).to(torch.int32)
+        bt = torch.full((self.n_seq, self.bt_stride), -1, dtype=torch.int32)
+        k = 0
+        for b, n in enumerate(self.pages):
+            bt[b, :n] = perm[k:k + n]
+            k += n
+        return bt
+
+    def q(self, device="cpu", tag: str = "q") -> torch.Tensor:
+        return normal_bf16(self.seed, f"{self.name}/{tag}", (self.Q, self.H, self.D), device=device)
+
+    def w(self, device="cpu", tag: str = "w") -> torch.Tensor:
+        return normal_bf16(self.seed, f"{self.name}/{tag}", (self.Q, self.H), device=device)
+
+    def latent(self, b: int, device="cpu") -> torch.Tensor:
+        """Latents of sequence b's keys 0 .. T_b - 1, [T_b, D]."""
+        return normal_bf16(self.seed, f"{self.name}/latent/{b}", (self.T_list[b], self.D), device=device)
+
+    def wk(self, device="cpu") -> torch.Tensor:
+        return normal_bf16(self.seed, f"{self.name}/wk", (self.D, self.D), std=self.D ** -0.5, device=device)
+
+    def k_norm_w(self, device="cpu") -> torch.Tensor:
+        return normal_bf16(self.seed, f"{self.name}/k_norm_w", (self.D,), std=math.sqrt(0.1), mean=1.0,
+                           device=device)
+
+
+def _server_step_seqs() -> tuple:
+    """64 decode rows with context lengths spread over 4k .. 32k positions (each a group end,
+    start_pos + 1 a multiple of 4) and two 512-row prefill chunks at 16384 and 24576."""
+    u = uniform_f64(0, "server_step/lengths", (64,))
+    dec = tuple((int(4096 + x * 28672) // 4 * 4 + 3, 1) for x in u.tolist())
+    return dec + ((16384, 512), (24576, 512))
+
+
+MIXED = {
+    m.name: m
+    for m in [
+        # a small batch for parity: a chunked prefill, decode rows, a prefill from 0, an
+        # empty sequence, a one-key sequence and a 2048-key sequence
+        MixedBatch("mixed_small", seqs=((1024, 64), (4095, 1), (511, 1), (0, 40), (300, 0), (6, 1), (8191, 1)),
+                   ratio=4, H=64, topk=128),
+        # decode only (one row per sequence): the single-row score kernel over the pool
+        MixedBatch("mixed_decode", seqs=tuple((4 * (256 + 97 * i) + 3, 1) for i in range(24)), ratio=4, H=64,
+                   topk=256),
+        # a server step: 64 decode rows + two 512-row prefill chunks
+        MixedBatch("server_step", seqs=_server_step_seqs(), ratio=4, H=64, topk=2048),
+    ]
+}
