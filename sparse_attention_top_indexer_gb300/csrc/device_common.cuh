@@ -268,6 +268,13 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N) {
   return (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 7) << 27);
 }
 
+// Warms L2 with [gptr, gptr + bytes) (16-byte aligned, a multiple of 16 bytes). A hint
+// only: the data is not delivered anywhere and a later write to the lines by another
+// kernel keeps L2 coherent, so it may be issued before pdl_wait().
+__device__ __forceinline__ void prefetch_l2_bulk(const void* gptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gptr), "r"(bytes) : "memory");
+}
+
 // Shared-memory matrix descriptor, no swizzle, K-major: core matrices of 8 rows x 16 bytes
 // (128 contiguous bytes); lbo = byte step between core matrices along K, sbo = byte step
 // between 8-row groups along M/N; bits 46-48 hold the fixed value 0b001.

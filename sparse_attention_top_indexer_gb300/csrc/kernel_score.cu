@@ -99,10 +99,14 @@ __device__ __forceinline__ int pool_page(const ScoreArgs& a, int b, int lp) {
 }
 
 // Requests the two pages of a tile into a stage (a missing half is not copied; its keys
-// are never stored).
+// are never stored); adjacent pool pages come in one copy.
 __device__ __forceinline__ void issue_tile_load(const ScoreArgs& a, int p0, int p1, uint32_t stage_addr,
                                                 uint32_t bar) {
   mbar_arrive_expect_tx(bar, (uint32_t)((p0 >= 0 ? kPageBytes : 0) + (p1 >= 0 ? kPageBytes : 0)));
+  if (p0 >= 0 && p1 == p0 + 1) {
+    bulk_g2s(stage_addr, a.k_pool + (size_t)p0 * kPageBytes, (uint32_t)(2 * kPageBytes), bar);
+    return;
+  }
   if (p0 >= 0) bulk_g2s(stage_addr, a.k_pool + (size_t)p0 * kPageBytes, (uint32_t)kPageBytes, bar);
   if (p1 >= 0) bulk_g2s(stage_addr + kPageBytes, a.k_pool + (size_t)p1 * kPageBytes, (uint32_t)kPageBytes, bar);
 }
@@ -201,6 +205,14 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
   // launch has one row, which sees every key)
   const int vis_hi = min(Tb, (pos0 + nq) / a.ratio);
   const int tile_vis = sparse ? tile1 : min(tile1, (vis_hi + kTileKeys - 1) / kTileKeys);
+  if (!sparse && a.groups == nullptr && a.block_table == nullptr && warp == 0) {
+    // the CTA's pages are known before the kernels before finish: warm L2 with them
+    // while they run (a hint; the copies below read after pdl_wait)
+    for (int i = tile0 + lane; i < tile_vis; i += 32) {
+      const int lp = 2 * i, n = min(2, npages - lp);
+      prefetch_l2_bulk(a.k_pool + ((size_t)b * a.pages_per_seq + lp) * kPageBytes, (uint32_t)(n * kPageBytes));
+    }
+  }
   pdl_wait();   // the query rows, weights and pages of the kernels before are complete
   // -inf over the tiles no row of the group can see (by the epilogue warps while they wait
   // for the first accumulator, or here when the CTA has nothing to score)

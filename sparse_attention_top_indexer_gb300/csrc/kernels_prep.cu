@@ -61,6 +61,9 @@ __global__ void __launch_bounds__(kHeadDim * TPO) publish_kernel(PublishArgs a) 
   __shared__ double rinv;
   const int tid = threadIdx.x;
   pdl_allow_next();
+  if (tid == 0 && blockIdx.x < 4) {   // warm L2 with wk while the kernels before run: four CTAs, 32 rows each
+    prefetch_l2_bulk(a.wk + (size_t)blockIdx.x * 32 * a.Din, (uint32_t)(32 * a.Din * 2));
+  }
   pdl_wait();
   const int key = blockIdx.x;
   const int b = key / a.G, j = key % a.G;
@@ -214,8 +217,13 @@ cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream) {
 // thread of a block its scale byte. w' = f32(w) * head_dim^-0.5 * H^-0.5.
 __global__ void __launch_bounds__(256) prep_q_kernel(PrepArgs a) {
   pdl_allow_next();
-  pdl_wait();
   const int tid = threadIdx.x;
+  if (tid == 0) {   // warm L2 with the CTA's 16 query-head vectors while the kernels before run
+    const long long v0 = (long long)blockIdx.x * 16;
+    const long long nv = a.n_vec - v0 < 16 ? a.n_vec - v0 : 16;
+    prefetch_l2_bulk(a.q + v0 * kHeadDim, (uint32_t)(nv * kHeadDim * 2));
+  }
+  pdl_wait();
   const long long v = (long long)blockIdx.x * 16 + (tid >> 4);
   const int j = tid & 15;
   if (v >= a.n_vec) return;   // whole 16-lane groups leave together
