@@ -44,7 +44,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-from workloads import ROPE, WORKLOADS, Workload, normal_bf16  # noqa: E402
+from workloads import MIXED, ROPE, WORKLOADS, MixedBatch, Workload, normal_bf16  # noqa: E402
 
 METRIC = "indexer score+top-k queries/s and key-scores/s; % of HBM / FP4-MMA roofline"
 UNIT = "queries/s"
@@ -58,7 +58,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=20000)
     p.add_argument("--warmup", type=int, default=2000)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="decode", choices=sorted(WORKLOADS))
+    p.add_argument("--workload", default="decode", choices=sorted(WORKLOADS) + sorted(MIXED))
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
@@ -394,6 +394,171 @@ def run_ours(args, dist: Dist):
     return line, wl
 
 
+# ----------------------------------------------------------------------------- mixed batches
+class MixedSetup:
+    """A server step over a page pool: every sequence's keys before this step are
+    published once; a step publishes the keys its rows complete (slot mapping) and runs
+    indexer_forward_paged over the whole batch. `rotate` pool copies and inputs."""
+
+    def __init__(self, m: MixedBatch, dev, rotate: int):
+        import sparse_attention_top_indexer_gb300 as X
+        self.X, self.m, self.dev, self.rotate = X, m, dev, rotate
+        X.load_library()
+        self.dims = X.make_dims(n_heads=m.H, ratio=m.ratio, index_topk=m.topk, offset=m.offset,
+                                rope_dim=m.rope_dim, head_dim=m.D, cand_topk_blocks=m.cand_topk_blocks,
+                                cand_block_size=m.cand_block_size, norm_eps=m.norm_eps)
+        self.table = torch.empty((m.max_pos, m.rope_dim // 2, 2), dtype=torch.float32, device=dev)
+        X.indexer_rope_table(X.IndexerYarn(ROPE.theta, ROPE.factor, ROPE.original_seq_len, ROPE.beta_fast,
+                                           ROPE.beta_slow), m.rope_dim, m.max_pos, self.table)
+        self.wk, self.knw = m.wk(dev), m.k_norm_w(dev)
+        bt = m.block_table()
+        self.bt = bt.to(dev)
+        # keys before the step (published once) and the keys the step's rows complete
+        old_pos, old_slot, new_pos, new_slot = [], [], [], []
+        for b, (sp, S) in enumerate(m.seqs):
+            t_old, t_new = sp // m.ratio, m.T_list[b]
+            for lo, hi, pos, slot in ((0, t_old, old_pos, old_slot), (t_old, t_new, new_pos, new_slot)):
+                j = torch.arange(lo, hi)
+                pos.append(j * m.ratio)
+                slot.append(bt[b, j // 64].long() * 64 + j % 64)
+        i32 = lambda xs: torch.cat(xs).to(torch.int32).to(dev)
+        self.old_pos, self.old_slot = i32(old_pos), i32(old_slot)
+        self.new_pos, self.new_slot = i32(new_pos), i32(new_slot)
+        self.n_new = int(self.new_pos.numel())
+        self.status = torch.empty(X.STATUS_BYTES, dtype=torch.uint8, device=dev)
+        X.indexer_workspace_init(self.status)
+        base = X.new_key_pool(m.num_pages, device=dev)
+        n_old = int(self.old_pos.numel())
+        lat_old = normal_bf16(m.seed, f"{m.name}/latent_old", (n_old, m.D), device=dev)
+        X.indexer_publish_k_paged(self.dims, lat_old, self.wk, self.knw, self.table, self.old_pos, self.old_slot,
+                                  base, self.status)
+        self.pools = [base] + [base.clone() for _ in range(rotate - 1)]
+        self.lat = [normal_bf16(m.seed, f"{m.name}/latent_new/{i}", (self.n_new, m.D), device=dev)
+                    for i in range(rotate)]
+        self.q = [normal_bf16(m.seed, f"{m.name}/q/{i}", (m.Q, m.H, m.D), device=dev) for i in range(rotate)]
+        self.w = [normal_bf16(m.seed, f"{m.name}/w/{i}", (m.Q, m.H), device=dev) for i in range(rotate)]
+        self.seq_pos = torch.tensor([sp for sp, _ in m.seqs], dtype=torch.int32, device=dev)
+        self.q_start = torch.tensor(m.q_start, dtype=torch.int32, device=dev)
+        self.ws = torch.empty(X.indexer_workspace_size_paged(self.dims, m.Q, m.n_seq, m.T_max), dtype=torch.uint8,
+                              device=dev)
+        X.indexer_workspace_init(self.ws)
+        self.top = torch.empty((m.Q, m.topk), dtype=torch.int32, device=dev)
+
+    def publish(self, i):
+        self.X.indexer_publish_k_paged(self.dims, self.lat[i], self.wk, self.knw, self.table, self.new_pos,
+                                       self.new_slot, self.pools[i], self.status)
+
+    def forward(self, i):
+        m = self.m
+        self.X.indexer_forward_paged(self.dims, self.q[i], self.w[i], self.seq_pos, self.q_start, m.T_max,
+                                     self.table, self.pools[i], self.bt, self.top, self.ws)
+
+    def step(self, i):
+        self.publish(i)
+        self.forward(i)
+
+
+def mixed_units(m: MixedBatch):
+    """Algorithmic work of one forward over the batch: every key of a sequence read once,
+    query rows in, indices out; tensor flops of every visible (row, key) pair."""
+    pairs = 0
+    for (sp, S), T in zip(m.seqs, m.T_list):
+        pairs += sum(min(T, (sp + s + 1) // m.ratio) for s in range(S))
+    key_bytes = sum(m.T_list) * 68
+    q_bytes = m.Q * m.H * (m.D * 2 + 2)
+    out_bytes = m.Q * m.topk * 4
+    return {"bytes": key_bytes + q_bytes + out_bytes, "flops": pairs * m.H * m.D * 2, "pairs": pairs}
+
+
+def run_mixed(args, dist: Dist):
+    m = MIXED[args.workload]
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    rotate = ROTATE
+    st = MixedSetup(m, dev, rotate)
+    for i in range(rotate):
+        st.step(i)
+    torch.cuda.synchronize()
+    X = st.X
+    X.indexer_status(st.ws)
+    X.indexer_status(st.status)
+    g_full = capture(st.step, rotate)
+    n_full = max(1, args.steps // rotate)
+    steps = n_full * rotate
+    for _ in range(max(1, math.ceil(args.warmup / rotate))):
+        g_full.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(dist.local)
+    time.sleep(0.15)
+    dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
+    e0.record()
+    for _ in range(n_full):
+        g_full.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    w1 = time.time()
+    dist.barrier()
+    sampler.region(w0, w1)
+    time.sleep(0.1)
+    clocks = sampler.stop()
+    ms_max = dist.max(e0.elapsed_time(e1))
+    X.indexer_status(st.ws)
+    X.indexer_status(st.status)
+    # the step's two calls alone (graphs of back-to-back launches, events around them)
+    kernel_ms = {}
+    for name, fn in (("publish_paged", st.publish), ("forward_paged", st.forward)):
+        g = capture(fn, rotate)
+        g.replay()
+        torch.cuda.synchronize()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record()
+        for _ in range(10):
+            g.replay()
+        a1.record()
+        torch.cuda.synchronize()
+        kernel_ms[name] = a0.elapsed_time(a1) / (10 * rotate)
+    units = mixed_units(m)
+    peaks = measured_peaks()
+    fwd = kernel_ms["forward_paged"]
+    t_hbm = units["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    t_mma = units["flops"] / (peaks["bf16_tflops"] * FP4_OVER_BF16 * 1e12)
+    if t_hbm >= t_mma:
+        achieved = units["bytes"] / (fwd / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                "algorithmic_bytes_per_launch": units["bytes"],
+                "kernel": "indexer_forward_paged (plan, query prep, scores, top-k)", "kernel_ms": fwd,
+                "peak_source": f"{peaks['source']} hbm_gbs"}
+    else:
+        achieved = units["flops"] / (fwd / 1e3) / 1e12
+        peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": None, "algorithmic_flops_per_launch": units["flops"],
+                "kernel": "indexer_forward_paged (plan, query prep, scores, top-k)", "kernel_ms": fwd,
+                "peak_source": f"{peaks['source']} bf16_tflops x {FP4_OVER_BF16:g} (nominal fp4/bf16)"}
+    n_dec = sum(1 for _, S in m.seqs if S == 1)
+    line = {
+        "metric": METRIC, "value": dist.world * m.Q * steps / (ms_max / 1e3), "unit": UNIT, "n_gpus": dist.world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms_max / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "e2m1 x e2m1 -> f32", "data": "synthetic",
+        "config": {"workload": (f"{m.name}: mixed batch of {m.n_seq} sequences ({n_dec} decode rows, "
+                                f"{m.n_seq - n_dec} prefill chunks), {m.Q} query rows, T_max {m.T_max}, H{m.H}, "
+                                f"top-{m.topk}, keys in a pool of {m.num_pages} 64-key pages"),
+                   "Q": m.Q, "n_seq": m.n_seq, "T_max": m.T_max, "H": m.H, "topk": m.topk, "ratio": m.ratio,
+                   "l2": f"{rotate} rotating page pools / inputs ({rotate * m.num_pages * 4352 / 1e6:.0f} MB)",
+                   "timing": "CUDA-graph replay, CUDA events on the launching stream"},
+        "key_scores_per_s": dist.world * units["pairs"] * steps / (ms_max / 1e3),
+        "kernel_ms": kernel_ms,
+        "roofline": roof,
+        "gpu_launches": 5 * steps,
+        "clocks": clocks,
+    }
+    return line
+
+
 def breakdown(st: Setup, rotate: int, reps: int = 20):
     """Average device time of each kernel of the step: a CUDA graph of `rotate`
     back-to-back launches of that kernel alone (rotating inputs), replayed `reps` times
@@ -536,6 +701,10 @@ def dataclasses_replace(wl, **kw):
 
 
 def run_reference(args, dist: Dist):
+    if args.workload in MIXED:
+        return ({"impl": "reference", "unavailable": "the oracle reference arm times the uniform workloads; "
+                 "mixed page-pool batches are compared with the oracle per sequence in the tests"}
+                if dist.rank == 0 else None), None
     wl = WORKLOADS[args.workload]
     if dist.rank != 0:
         return None, wl
@@ -575,6 +744,8 @@ def main():
     try:
         if args.impl == "reference":
             line, _ = run_reference(args, dist)
+        elif args.workload in MIXED:
+            line = run_mixed(args, dist)
         else:
             line, wl = run_ours(args, dist)
             if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
