@@ -167,7 +167,8 @@ int indexer_prep_q(const IndexerDims* dims, const indexer_bf16* q, const indexer
  *   cand_blocks: int32 [B][S][cand_topk_blocks] kept block ids (-1 = none), or
  *                NULL for no candidate filter
  *   scores: float [B][S][T] written (T = (start_pos + S) / r)
- *   ws/ws_bytes: workspace of at least INDEXER_STATUS_BYTES (status word)
+ *   ws/ws_bytes: workspace of at least INDEXER_STATUS_BYTES (the status word and the
+ *                scoring kernels' work counter), initialised once by indexer_workspace_init
  * ------------------------------------------------------------------------- */
 int indexer_scores(const IndexerDims* dims, const uint8_t* q_rows, const float* w_prime, int B, int S,
                    int start_pos, const uint8_t* k_cache, int T_cap, const int32_t* cand_blocks,

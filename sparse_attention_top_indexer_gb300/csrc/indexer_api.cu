@@ -17,6 +17,10 @@ using namespace indexer;
 
 namespace {
 
+// Word of the workspace header holding the several-row score kernel's group counter (two
+// words, zeroed by indexer_workspace_init and left zero by every launch).
+constexpr int kSchedWord = 32;
+
 thread_local std::string g_last_error;
 
 int fail(int code, const char* fmt, ...) {
@@ -319,6 +323,7 @@ int indexer_scores(const IndexerDims* dims, const uint8_t* q_rows, const float* 
   a.ld = T;
   a.cand = cand_blocks;
   a.status = static_cast<uint32_t*>(ws);
+  a.sched = static_cast<uint32_t*>(ws) + kSchedWord;
   a.B = B;
   a.S = S;
   a.H = dims->n_heads;
@@ -439,6 +444,7 @@ int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexe
     a.cand = sparse2 ? cand_in : nullptr;
     a.sparse_pages = sparse2 ? 1 : 0;
     a.status = reinterpret_cast<uint32_t*>(base);
+    a.sched = reinterpret_cast<uint32_t*>(base) + kSchedWord;
     a.B = B;
     a.S = S;
     a.H = dims->n_heads;
@@ -612,6 +618,7 @@ int indexer_forward_paged(const IndexerDims* dims, const indexer_bf16* q, const 
     a.cand = sparse2 ? cand_in : nullptr;
     a.sparse_pages = sparse2 ? 1 : 0;
     a.status = status;
+    a.sched = status + kSchedWord;
     a.B = n_seq;
     a.S = single ? 1 : 2;   // selects the single-row (decode) kernel, matching l.qg
     a.H = dims->n_heads;

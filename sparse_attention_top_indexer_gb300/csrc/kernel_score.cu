@@ -468,6 +468,417 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
   if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
+// ============================================================================ several rows
+// Query groups of several rows (prefill, chunked prefill, mixed batches): a persistent CTA
+// per SM runs one pipeline over many groups, so the set-up (barriers, tensor memory, the
+// first pages' latency) is paid once per SM instead of once per group. Groups are fetched
+// from a counter in the workspace (a uniform batch hands out the groups with the most
+// visible keys first), which balances the causal triangle across SMs.
+//   * producer warp (the last warp): fetches the next group, writes its descriptor and
+//     requests its query rows and w' into one of two query buffers (once the MMA warpgroup
+//     and the epilogue have released the buffer's previous group), then streams the group's
+//     tiles through a ring
+//     of NSTAGE stages, each stage refilled once the MMA that read it has completed;
+//   * scale warpgroup (warps 0-3): per group, rewrites the query rows into the B operand
+//     (core-matrix order, one of two buffers) and stores their scales in tensor memory (one
+//     of two sets); per tile, once the accumulator's previous use has been drained, the
+//     four warps store the tile's A scales (each warp its own lane quadrant) and signal the
+//     MMA warp through the accumulator's "scales ready" mbarrier;
+//   * MMA warp: per tile, one thread issues the two block-scaled MMAs into one of NACC
+//     accumulators and commits to the accumulator's and the stage's mbarriers, so the scale
+//     stores of the next tiles overlap the issue of this one;
+//   * EPI epilogue warpgroups take alternate tiles (over the whole sequence of groups): read
+//     the accumulator in 64-column halves, release it, form sum_h w' * max(dot, 0) per row
+//     and store; after its last tile of a group every epilogue thread releases the query
+//     buffer of that group.
+template <int H, int QG, int EPI>
+struct RowsCfg {
+  static constexpr int THREADS = 128 * (1 + EPI) + 64;
+  static constexpr int MMA_WARP = 4 * (1 + EPI);
+  static constexpr int PRODUCER_WARP = MMA_WARP + 1;
+  static constexpr int QFREE_COUNT = 128 * (1 + EPI) + 32;   // scale warpgroup, epilogue, MMA warp
+  static constexpr int N = QG * H;
+  static constexpr int NP = round_up(N, 16);
+  static constexpr int NCB = (NP + 31) / 32;
+  static constexpr int SB = round_up(NCB, 4);
+  static constexpr int NSTAGE = 12;
+  // NACC accumulators with their A scale sets, and two B scale sets (two query buffers)
+  static constexpr int NACC = 3 * (NP + 8) + 4 * SB <= 512 ? 3 : 2 * (NP + 8) + 4 * SB <= 512 ? 2 : 1;
+  static constexpr int SFA_COL = NACC * NP;
+  static constexpr int SFB_COL = SFA_COL + 8 * NACC;   // set q: columns SFB_COL + 2*SB*q ..
+  static constexpr int TMEM_NEED = SFB_COL + 4 * SB;
+  static constexpr uint32_t TMEM_COLS = pow2_cols(TMEM_NEED);
+  static constexpr int QB_STRIDE = round_up(NP * kCodeBytes, 1024);
+  static constexpr int QSTG_STRIDE = round_up(N * kRowBytes, 16);
+  static constexpr int W_STRIDE = round_up(N * 4, 16);
+  static constexpr int OFF_QB = 0;
+  static constexpr int OFF_STG = 2 * QB_STRIDE;
+  static constexpr int OFF_QSTG = OFF_STG + NSTAGE * kStageStride;
+  static constexpr int OFF_W = OFF_QSTG + 2 * QSTG_STRIDE;
+  static constexpr int OFF_SFW = OFF_W + 2 * W_STRIDE;
+  static constexpr int OFF_GD = round_up(OFF_SFW + NCB * 32 * 4, 16);   // two group descriptors
+  static constexpr int NBAR = 2 * NSTAGE + 3 * NACC + 4;   // full, free, done, empty, qfull, qfree, ready
+  static constexpr int OFF_BAR = OFF_GD + 2 * 32;
+  static constexpr int OFF_INFO = OFF_BAR + NBAR * 8;                     // tmem, tiles, mmas, q phases
+  static constexpr int SMEM = OFF_INFO + 16;
+  static_assert(N <= 256 && NCB * 32 % 64 == 0, "epilogue reads 64-column halves");
+  static_assert(TMEM_NEED <= (int)TMEM_COLS && TMEM_COLS <= 512u, "tensor memory budget");
+  static_assert(SFA_COL % 4 == 0 && SFB_COL % 4 == 0 && SB % 4 == 0, "scale sets must be 4-column aligned");
+  static_assert(NBAR <= 64, "barriers are initialised by the lanes of two passes of one warp");
+  static_assert(QFREE_COUNT < (1 << 20), "mbarrier arrival count");
+};
+
+struct GroupDesc {   // one query group, as the producer hands it to the other roles
+  int b, row0, nq, pos0;
+  int Tb, nt, ntiles, live;   // keys of the sequence, tiles to score, tiles of the sequence, 0 = no more groups
+};
+
+template <int H, int QG, int EPI>
+__global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_kernel(const ScoreArgs a) {
+  using C = RowsCfg<H, QG, EPI>;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_allow_next();
+  GroupDesc* gdesc = reinterpret_cast<GroupDesc*>(smem + C::OFF_GD);
+  uint32_t* info = reinterpret_cast<uint32_t*>(smem + C::OFF_INFO);   // [0] tmem, [1] tiles issued, [2] mmas, [3] q phases
+  const uint8_t* stg = smem + C::OFF_STG;
+  const uint32_t stg0 = smem_u32(stg);
+  uint32_t* sfw = reinterpret_cast<uint32_t*>(smem + C::OFF_SFW);
+  const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
+  auto bar_full = [&](int st) { return bar0 + 8u * (uint32_t)st; };
+  auto bar_free = [&](int st) { return bar0 + 8u * (uint32_t)(C::NSTAGE + st); };
+  auto bar_done = [&](int c) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + c); };
+  auto bar_empty = [&](int c) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + C::NACC + c); };
+  auto bar_qfull = [&](int q) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + 2 * C::NACC + q); };
+  auto bar_qfree = [&](int q) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + 2 * C::NACC + 2 + q); };
+  auto bar_ready = [&](int c) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + 2 * C::NACC + 4 + c); };
+  if (warp == 0) {
+    for (int i = lane; i < C::NBAR; i += 32) {
+      const bool empty_bar = i >= 2 * C::NSTAGE + C::NACC && i < 2 * C::NSTAGE + 2 * C::NACC;
+      const bool qfree_bar = i >= 2 * C::NSTAGE + 2 * C::NACC + 2 && i < 2 * C::NSTAGE + 2 * C::NACC + 4;
+      const bool ready_bar = i >= 2 * C::NSTAGE + 2 * C::NACC + 4;
+      // a query buffer is released by the scale warpgroup and the MMA warp (once they have
+      // read it) and by every epilogue thread (once the group's last accumulator has been
+      // read); an accumulator's scales are ready once the four scale warps have stored them
+      mbar_init(bar0 + 8u * (uint32_t)i, empty_bar || ready_bar ? (uint32_t)kEpiThreads
+                                         : qfree_bar ? (uint32_t)C::QFREE_COUNT : 1u);
+    }
+    fence_mbar_init();
+    if (lane == 0) info[1] = info[2] = info[3] = 0u;
+  } else if (warp == 1) {
+    tmem_alloc(smem_u32(&info[0]), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = info[0];
+  bool failed = false;
+
+  if (warp == C::PRODUCER_WARP) {
+    // ------------------------------------------------------------ producer warp
+    pdl_wait();   // query rows, w', pages and the group list of the kernels before are complete
+    const int gps = (a.S + QG - 1) / QG;                       // uniform batch: groups per sequence
+    const long long total = a.groups ? (long long)a.n_groups : (long long)gps * a.B;
+    uint32_t j = 0;                                            // tiles issued
+    for (int k = 0;; ++k) {
+      const int qb = k & 1;
+      if (k >= 2 && !warp_wait(bar_qfree(qb), (uint32_t)((k - 2) >> 1) & 1u)) {
+        failed = true;
+        break;
+      }
+      // next group with rows (the lanes agree through lane 0's fetch)
+      GroupDesc d{};
+      for (;;) {
+        uint32_t f = 0u;
+        if (lane == 0) f = atomicAdd(a.sched, 1u);
+        f = __shfl_sync(0xffffffffu, f, 0);
+        if ((long long)f >= total) break;
+        if (a.groups == nullptr) {
+          const int si = gps - 1 - (int)(f / (uint32_t)a.B);   // most visible keys first
+          d.b = (int)(f % (uint32_t)a.B);
+          const int s0 = si * QG;
+          d.nq = min(QG, a.S - s0);
+          d.row0 = d.b * a.S + s0;
+          d.pos0 = a.start_pos + s0;
+          d.Tb = a.T;
+        } else {
+          const RowGroup rg = a.groups[f];
+          d.b = rg.b;
+          d.row0 = rg.row0;
+          d.nq = min(rg.nq, QG);
+          d.pos0 = rg.pos0;
+          d.Tb = min(rg.T, a.T);
+        }
+        if (d.nq > 0) {
+          d.live = 1;
+          break;
+        }
+      }
+      if (d.live) {
+        d.ntiles = (d.Tb + kTileKeys - 1) / kTileKeys;
+        const int vis_hi = min(d.Tb, (d.pos0 + d.nq) / a.ratio);
+        d.nt = min(d.ntiles, (vis_hi + kTileKeys - 1) / kTileKeys);
+      }
+      if (lane == 0) {
+        gdesc[qb] = d;
+        if (d.live) {
+          const uint32_t qbytes = (uint32_t)(d.nq * H * kRowBytes), wbytes = (uint32_t)(d.nq * H * 4);
+          mbar_arrive_expect_tx(bar_qfull(qb), qbytes + wbytes);
+          bulk_g2s(smem_u32(smem + C::OFF_QSTG + qb * C::QSTG_STRIDE), a.q_rows + (size_t)d.row0 * H * kRowBytes,
+                   qbytes, bar_qfull(qb));
+          bulk_g2s(smem_u32(smem + C::OFF_W + qb * C::W_STRIDE), a.w_prime + (size_t)d.row0 * H, wbytes,
+                   bar_qfull(qb));
+        } else {
+          mbar_arrive(bar_qfull(qb));   // no more groups: the other roles stop here
+        }
+        info[3] = (uint32_t)(k + 1);
+      }
+      __syncwarp();
+      if (!d.live) break;
+      const int npages = (d.Tb + kPageKeys - 1) / kPageKeys;
+      for (int i0 = 0; i0 < d.nt && !failed; i0 += 32) {
+        int p0 = -1, p1 = -1;   // this lane's tile: its two pool pages (looked up in parallel)
+        if (i0 + lane < d.nt) {
+          const int lp = 2 * (i0 + lane);
+          p0 = pool_page(a, d.b, lp);
+          p1 = pool_page(a, d.b, lp + 1 < npages ? lp + 1 : -1);
+          if (p0 == -2 || p1 == -2) atomicOr(a.status, kStatusBadMeta);
+        }
+        const int n = min(32, d.nt - i0);
+        for (int u = 0; u < n; ++u, ++j) {
+          const int st = (int)(j % C::NSTAGE);
+          if (j >= (uint32_t)C::NSTAGE && !warp_wait(bar_free(st), ((j / C::NSTAGE) - 1) & 1u)) {
+            failed = true;
+            break;
+          }
+          const int q0 = __shfl_sync(0xffffffffu, p0, u), q1 = __shfl_sync(0xffffffffu, p1, u);
+          if (lane == 0) {
+            issue_tile_load(a, max(q0, -1), max(q1, -1), stg0 + st * kStageStride, bar_full(st));
+            info[1] = j + 1;
+          }
+          __syncwarp();
+        }
+      }
+      if (failed) break;
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ scale warpgroup
+    const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);   // this warp's lane quadrant
+    const int key = tid;   // this thread's key (TMEM lane) within a tile
+    uint32_t j = 0;
+    for (int k = 0; !failed; ++k) {
+      const int qb = k & 1;
+      if (!named_bar_and(1, 128, warp_wait(bar_qfull(qb), (uint32_t)(k >> 1) & 1u))) {
+        failed = true;
+        break;
+      }
+      const GroupDesc d = gdesc[qb];
+      if (!d.live) break;
+      if (d.nt == 0) {
+        mbar_arrive(bar_qfree(qb));
+        continue;
+      }
+      // query rows -> B operand buffer qb (core-matrix order) and B scale set qb
+      uint8_t* qB = smem + C::OFF_QB + qb * C::QB_STRIDE;
+      const uint8_t* qstg = smem + C::OFF_QSTG + qb * C::QSTG_STRIDE;
+      for (int n = tid; n < C::NCB * 32; n += 128) {
+        uint32_t w[16];
+        uint32_t sc = 0x7F7F7F7Fu;
+        if (n < d.nq * H) {
+          const uint32_t* src = reinterpret_cast<const uint32_t*>(qstg + n * kRowBytes);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = src[i];
+          sc = src[16];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) w[i] = 0u;
+        }
+        if (n < C::NP) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            *reinterpret_cast<uint4*>(qB + (n >> 3) * 512 + c * 128 + (n & 7) * 16) =
+                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+        }
+        sfw[n] = sc;
+      }
+      fence_proxy_async_smem();   // the B operand was written by ordinary stores
+      named_bar_sync(1, 128);
+      // done with the buffer's descriptor and raw rows (the B operand itself stays in use
+      // until the group's MMAs complete, which the epilogue's release covers)
+      mbar_arrive(bar_qfree(qb));
+      const uint32_t sfb = (uint32_t)(C::SFB_COL + qb * 2 * C::SB);
+#pragma unroll
+      for (int jj = 0; jj < C::NCB; ++jj) {
+        const uint32_t wd = sfw[32 * jj + lane];
+        tmem_st_x1(tq + sfb + jj, wd & 0xFFFFu);
+        tmem_st_x1(tq + sfb + C::SB + jj, wd >> 16);
+      }
+      for (int i = 0; i < d.nt; ++i, ++j) {
+        const int st = (int)(j % C::NSTAGE), c = (int)(j % C::NACC);
+        // the tile has landed, and accumulator c (with its scale set) has been drained
+        bool ok = warp_wait(bar_full(st), (j / C::NSTAGE) & 1u);
+        if (ok && j >= (uint32_t)C::NACC) ok = warp_wait(bar_empty(c), ((j - C::NACC) / C::NACC) & 1u);
+        if (!named_bar_and(1, 128, ok)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(stg + st * kStageStride + page_scale_offset(key));
+        const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
+        tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * c), lo, lo, lo, lo, hi, hi, hi, hi);
+        tmem_wait_st();   // (also the group's B scales, for its first tile)
+        tc_fence_before();
+        mbar_arrive(bar_ready(c));
+      }
+    }
+  } else if (warp == C::MMA_WARP) {
+    // ------------------------------------------------------------ MMA warp
+    const uint32_t idesc = idesc_mxf4(128, C::NP);
+    uint32_t j = 0;
+    for (int k = 0; !failed; ++k) {
+      const int qb = k & 1;
+      if (!warp_wait(bar_qfull(qb), (uint32_t)(k >> 1) & 1u)) {
+        failed = true;
+        break;
+      }
+      const GroupDesc d = gdesc[qb];
+      if (!d.live) break;
+      mbar_arrive(bar_qfree(qb));   // the descriptor is in registers
+      const uint32_t qbaddr = smem_u32(smem + C::OFF_QB + qb * C::QB_STRIDE);
+      const uint32_t sfb = (uint32_t)(C::SFB_COL + qb * 2 * C::SB);
+      for (int i = 0; i < d.nt; ++i, ++j) {
+        const int st = (int)(j % C::NSTAGE), c = (int)(j % C::NACC);
+        bool ok = warp_wait(bar_ready(c), (j / C::NACC) & 1u);
+        if (ok) ok = warp_wait(bar_full(st), (j / C::NSTAGE) & 1u);
+        if (!ok) {
+          failed = true;
+          break;
+        }
+        if (lane == 0) {
+          tc_fence_after();
+          const uint32_t pa = stg0 + (uint32_t)(st * kStageStride);
+          const uint32_t acc = tmem + (uint32_t)(c * C::NP);
+          const uint32_t sfa = tmem + (uint32_t)(C::SFA_COL + 8 * c);
+          mma_mxf4(acc, smem_desc(pa, 128, kGroupBytes), smem_desc(qbaddr, 128, 512), idesc, sfa, tmem + sfb, 0u);
+          mma_mxf4(acc, smem_desc(pa + 256, 128, kGroupBytes), smem_desc(qbaddr + 256, 128, 512), idesc, sfa + 4,
+                   tmem + sfb + C::SB, 1u);
+          tc_commit(bar_done(c));
+          tc_commit(bar_free(st));
+          info[2] = j + 1;
+        }
+        __syncwarp();
+      }
+    }
+  } else if (warp < C::PRODUCER_WARP) {
+    // ------------------------------------------------------------ epilogue warpgroups
+    constexpr int P = H >= 32 ? 4 : 2;   // independent partial sums per row (pairs of heads)
+    const int grp = (warp - 4) >> 2;
+    const int et = (tid - 128) & (kEpiThreads - 1);   // key within the tile == TMEM lane
+    const int ge = tid - 128;
+    const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    pdl_wait();   // the scores of the kernels before have been read
+    uint32_t j = 0;
+    for (int k = 0; !failed; ++k) {
+      const int qb = k & 1;
+      if (!warp_wait(bar_qfull(qb), (uint32_t)(k >> 1) & 1u)) {
+        failed = true;
+        break;
+      }
+      const GroupDesc d = gdesc[qb];
+      if (!d.live) break;
+      const float* wq = reinterpret_cast<const float*>(smem + C::OFF_W + qb * C::W_STRIDE);
+      if (a.fill_masked) {   // -inf over the tiles no row of the group can see
+        const int t_begin = d.nt * kTileKeys;
+        for (int qi = 0; qi < d.nq; ++qi) {
+          float* dst = a.scores + (size_t)(d.row0 + qi) * a.ld;
+          for (int t = t_begin + ge; t < d.Tb; t += EPI * kEpiThreads) dst[t] = -__int_as_float(0x7f800000);
+        }
+      }
+      for (int i = 0; i < d.nt && !failed; ++i, ++j) {
+        if ((int)(j % EPI) != grp) continue;
+        const int c = (int)(j % C::NACC);
+        if (!warp_wait(bar_done(c), (j / C::NACC) & 1u)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        float part[QG][P];
+#pragma unroll
+        for (int qi = 0; qi < QG; ++qi)
+#pragma unroll
+          for (int p = 0; p < P; ++p) part[qi][p] = 0.f;
+#pragma unroll
+        for (int h = 0; h < C::NCB * 32 / 64; ++h) {   // 64-column halves of the accumulator
+          float v[64];
+          tmem_ld64(tq + (uint32_t)(c * C::NP + 64 * h), v);
+          if (h == C::NCB * 32 / 64 - 1) {
+            tc_fence_before();
+            mbar_arrive(bar_empty(c));   // accumulator c and its scale set may be reused
+          }
+#pragma unroll
+          for (int u = 0; u < 64; u += 4) {
+            const int n = 64 * h + u;
+            if (n < C::N) {
+              const float4 w4 = *reinterpret_cast<const float4*>(wq + n);
+              const int qi = n / H, p0 = (n % P), p1 = ((n + 2) % P);
+              ffma2(part[qi][p0], part[qi][p0 + 1], w4.x, w4.y, fmaxf(v[u], 0.f), fmaxf(v[u + 1], 0.f));
+              ffma2(part[(n + 2) / H][p1], part[(n + 2) / H][p1 + 1], w4.z, w4.w, fmaxf(v[u + 2], 0.f),
+                    fmaxf(v[u + 3], 0.f));
+            }
+          }
+        }
+        const int t = i * kTileKeys + et;
+        if (t < d.Tb) {
+#pragma unroll
+          for (int qi = 0; qi < QG; ++qi) {
+            if (qi < d.nq) {
+              float acc = part[qi][0];
+#pragma unroll
+              for (int p = 1; p < P; ++p) acc += part[qi][p];
+              const int vis = min(d.Tb, (d.pos0 + qi + 1) / a.ratio);
+              a.scores[(size_t)(d.row0 + qi) * a.ld + t] = t < vis ? acc : -__int_as_float(0x7f800000);
+            }
+          }
+        }
+        __syncwarp();
+      }
+      if (failed) break;
+      mbar_arrive(bar_qfree(qb));   // this thread is done with the group's query buffer
+    }
+  }
+  __syncwarp();
+  if (failed && lane == 0)
+    atomicOr(a.status, warp < 4 || warp >= C::MMA_WARP ? kStatusLoadTimeout : kStatusMmaTimeout);
+  // on failure, bounded waits for whatever may still be in flight before shared and tensor
+  // memory go
+  const bool any_failed = __syncthreads_or(failed);
+  if (any_failed && tid == 0) {
+    const int issued = (int)info[1], mmas = (int)info[2], qph = (int)info[3];
+    for (int st = 0; st < C::NSTAGE && st < issued; ++st) {
+      const int last = st + ((issued - 1 - st) / C::NSTAGE) * C::NSTAGE;
+      mbar_wait(bar_full(st), (uint32_t)(last / C::NSTAGE) & 1u);
+    }
+    for (int q = 0; q < 2 && q < qph; ++q) {
+      const int last = q + ((qph - 1 - q) / 2) * 2;
+      mbar_wait(bar_qfull(q), (uint32_t)(last >> 1) & 1u);
+    }
+    if (mmas > 0) mbar_wait(bar_done((mmas - 1) % C::NACC), (uint32_t)((mmas - 1) / C::NACC) & 1u);
+  }
+  __syncthreads();
+  if (tid == 0) {   // the last CTA to finish rewinds the group counter for the next launch
+    __threadfence();
+    if (atomicAdd(a.sched + 1, 1u) == gridDim.x - 1) {
+      a.sched[0] = 0u;
+      a.sched[1] = 0u;
+      __threadfence();
+    }
+  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
 int sm_count() {
   static int cached[64] = {0};
   int dev = 0;
@@ -533,6 +944,28 @@ cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
   return launch_overlapped(score_kernel<H, QG, EPI>, grid, dim3(C::THREADS), smem, stream, a);
 }
 
+template <int H, int QG, int EPI>
+cudaError_t launch_rows(ScoreArgs a, cudaStream_t stream) {
+  using C = RowsCfg<H, QG, EPI>;
+  const size_t smem = (size_t)C::SMEM + 1024;   // + base alignment slack
+  static int set_bytes[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64 || set_bytes[dev] < (int)smem) {
+    err = cudaFuncSetAttribute(score_rows_kernel<H, QG, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(score_rows_kernel<H, QG, EPI>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 (int)cudaSharedmemCarveoutMaxShared);
+    if (err != cudaSuccess) return err;
+    if (dev >= 0 && dev < 64) set_bytes[dev] = (int)smem;
+  }
+  const long long groups = a.groups ? (long long)a.n_groups : (long long)((a.S + QG - 1) / QG) * a.B;
+  if (groups <= 0) return cudaSuccess;
+  const long long ctas = groups < sm_count() ? groups : sm_count();   // one persistent CTA per SM
+  return launch_overlapped(score_rows_kernel<H, QG, EPI>, dim3((unsigned)ctas), dim3(C::THREADS), smem, stream, a);
+}
+
 }  // namespace
 
 cudaError_t launch_scores(const ScoreArgs& a, cudaStream_t stream) {
@@ -540,9 +973,20 @@ cudaError_t launch_scores(const ScoreArgs& a, cudaStream_t stream) {
   // S == 1: one query row per group (a uniform batch of single rows, or row groups planned
   // with score_group_rows(H, true))
   const bool single = a.S == 1;
+  if (!single && a.cand == nullptr && a.sched != nullptr) {
+    // several rows per group: the persistent kernel (N = 128, two epilogue warpgroups)
+    switch (a.H) {
+      case 8: return launch_rows<8, 16, 2>(a, stream);
+      case 16: return launch_rows<16, 8, 2>(a, stream);
+      case 32: return launch_rows<32, 4, 2>(a, stream);
+      case 64: return launch_rows<64, 2, 2>(a, stream);
+      case 128: return launch_rows<128, 1, 2>(a, stream);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (a.H) {
-    // decode: one query row, N = H, two CTAs per SM; several rows: N = 128 (three
-    // accumulators in 512 columns) and two epilogue warpgroups
+    // decode: one query row, N = H, two CTAs per SM; several rows with a level-two filter:
+    // N = 128 (three accumulators in 512 columns) and two epilogue warpgroups
     case 8: return single ? launch_cfg<8, 1, 1>(a, stream) : launch_cfg<8, 16, 2>(a, stream);
     case 16: return single ? launch_cfg<16, 1, 1>(a, stream) : launch_cfg<16, 8, 2>(a, stream);
     case 32: return single ? launch_cfg<32, 1, 1>(a, stream) : launch_cfg<32, 4, 2>(a, stream);

@@ -109,6 +109,8 @@ struct ScoreArgs {
   int ld;
   const int32_t* cand = nullptr;   // [rows][cbk] or nullptr
   uint32_t* status;
+  uint32_t* sched = nullptr;        // two words, zero between launches: the several-row kernel's
+                                    // group counter and its count of finished CTAs
   int B, S, H, T, start_pos, ratio, cbk, cbs;   // with groups: T = T_max, S unused
   int n_groups;             // with groups
   int fill_masked;          // write -inf over key tiles no row of the group can see
