@@ -485,8 +485,9 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
 //     four warps store the tile's A scales (each warp its own lane quadrant) and signal the
 //     MMA warp through the accumulator's "scales ready" mbarrier;
 //   * MMA warp: per tile, one thread issues the two block-scaled MMAs into one of NACC
-//     accumulators and commits to the accumulator's and the stage's mbarriers, so the scale
-//     stores of the next tiles overlap the issue of this one;
+//     accumulators and commits to the stage's mbarrier (which frees the stage for the
+//     producer and hands the accumulator to the epilogue), so the scale stores of the next
+//     tiles overlap the issue of this one;
 //   * EPI epilogue warpgroups take alternate tiles (over the whole sequence of groups): read
 //     the accumulator in 64-column halves, release it, form sum_h w' * max(dot, 0) per row
 //     and store; after its last tile of a group every epilogue thread releases the query
@@ -526,6 +527,7 @@ struct RowsCfg {
   static_assert(SFA_COL % 4 == 0 && SFB_COL % 4 == 0 && SB % 4 == 0, "scale sets must be 4-column aligned");
   static_assert(NBAR <= 64, "barriers are initialised by the lanes of two passes of one warp");
   static_assert(QFREE_COUNT < (1 << 20), "mbarrier arrival count");
+  static_assert(NSTAGE > NACC, "the epilogue waits on a stage's barrier for its accumulator");
 };
 
 struct GroupDesc {   // one query group, as the producer hands it to the other roles
@@ -668,9 +670,11 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
     const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);   // this warp's lane quadrant
     const int key = tid;   // this thread's key (TMEM lane) within a tile
     uint32_t j = 0;
-    for (int k = 0; !failed; ++k) {
+    for (int k = 0;; ++k) {
       const int qb = k & 1;
-      if (!named_bar_and(1, 128, warp_wait(bar_qfull(qb), (uint32_t)(k >> 1) & 1u))) {
+      // the four warps agree at every group start (a warp that gave up inside the previous
+      // group has skipped its remaining waits and arrives here with failed set)
+      if (!named_bar_and(1, 128, !failed && warp_wait(bar_qfull(qb), (uint32_t)(k >> 1) & 1u))) {
         failed = true;
         break;
       }
@@ -716,13 +720,15 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
         tmem_st_x1(tq + sfb + C::SB + jj, wd >> 16);
       }
       for (int i = 0; i < d.nt; ++i, ++j) {
+        if (failed) continue;   // no more waits; the next group start reports it
         const int st = (int)(j % C::NSTAGE), c = (int)(j % C::NACC);
-        // the tile has landed, and accumulator c (with its scale set) has been drained
+        // the tile has landed, and accumulator c (with its scale set) has been drained; each
+        // warp goes on by itself and arrives on the accumulator's "ready" barrier
         bool ok = warp_wait(bar_full(st), (j / C::NSTAGE) & 1u);
         if (ok && j >= (uint32_t)C::NACC) ok = warp_wait(bar_empty(c), ((j - C::NACC) / C::NACC) & 1u);
-        if (!named_bar_and(1, 128, ok)) {
+        if (!ok) {
           failed = true;
-          break;
+          continue;
         }
         tc_fence_after();
         const uint32_t w = *reinterpret_cast<const uint32_t*>(stg + st * kStageStride + page_scale_offset(key));
@@ -764,8 +770,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
           mma_mxf4(acc, smem_desc(pa, 128, kGroupBytes), smem_desc(qbaddr, 128, 512), idesc, sfa, tmem + sfb, 0u);
           mma_mxf4(acc, smem_desc(pa + 256, 128, kGroupBytes), smem_desc(qbaddr + 256, 128, 512), idesc, sfa + 4,
                    tmem + sfb + C::SB, 1u);
-          tc_commit(bar_done(c));
-          tc_commit(bar_free(st));
+          tc_commit(bar_free(st));   // the stage may be refilled and the accumulator read
           info[2] = j + 1;
         }
         __syncwarp();
@@ -796,10 +801,16 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
           for (int t = t_begin + ge; t < d.Tb; t += EPI * kEpiThreads) dst[t] = -__int_as_float(0x7f800000);
         }
       }
+      // keys each row of the group may see
+      int visq[QG];
+#pragma unroll
+      for (int qi = 0; qi < QG; ++qi) visq[qi] = min(d.Tb, (d.pos0 + qi + 1) / a.ratio);
       for (int i = 0; i < d.nt && !failed; ++i, ++j) {
         if ((int)(j % EPI) != grp) continue;
         const int c = (int)(j % C::NACC);
-        if (!warp_wait(bar_done(c), (j / C::NACC) & 1u)) {
+        // tile j's MMA has completed (its stage's barrier; the stage cannot be refilled and
+        // complete again before this accumulator is released, as NSTAGE > NACC)
+        if (!warp_wait(bar_free((int)(j % C::NSTAGE)), (j / C::NSTAGE) & 1u)) {
           failed = true;
           break;
         }
@@ -837,8 +848,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
               float acc = part[qi][0];
 #pragma unroll
               for (int p = 1; p < P; ++p) acc += part[qi][p];
-              const int vis = min(d.Tb, (d.pos0 + qi + 1) / a.ratio);
-              a.scores[(size_t)(d.row0 + qi) * a.ld + t] = t < vis ? acc : -__int_as_float(0x7f800000);
+              a.scores[(size_t)(d.row0 + qi) * a.ld + t] = t < visq[qi] ? acc : -__int_as_float(0x7f800000);
             }
           }
         }
@@ -864,7 +874,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
       const int last = q + ((qph - 1 - q) / 2) * 2;
       mbar_wait(bar_qfull(q), (uint32_t)(last >> 1) & 1u);
     }
-    if (mmas > 0) mbar_wait(bar_done((mmas - 1) % C::NACC), (uint32_t)((mmas - 1) / C::NACC) & 1u);
+    if (mmas > 0) mbar_wait(bar_free((mmas - 1) % C::NSTAGE), (uint32_t)((mmas - 1) / C::NSTAGE) & 1u);
   }
   __syncthreads();
   if (tid == 0) {   // the last CTA to finish rewinds the group counter for the next launch
