@@ -148,7 +148,8 @@ int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B
  * fused_indexer_q_rope_quant):
  *   q:       bf16 [B][S][H][128] (post wq_b, pre-RoPE), 16-byte aligned
  *   w:       bf16 [B][S][H] (weights_proj output)
- *   q_rows:  uint8 [B][S][H][68] quantised query rows (same row format as keys)
+ *   q_rows:  uint8 [B][S][H][68] quantised query rows (same row format as keys), 16-byte
+ *            aligned
  *   w_prime: float [B][S][H] = w * 128^-0.5 * H^-0.5 (f32)
  * ------------------------------------------------------------------------- */
 int indexer_prep_q(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,

@@ -250,8 +250,9 @@ int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B
 // ---------------------------------------------------------------------------- query prep
 static int prep_q_checked(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
                           int start_pos, const float* rope_cs, uint8_t* q_rows, float* w_prime,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, uint32_t* status = nullptr) {
   PrepArgs a{};
+  a.status = status;
   a.q = q;
   a.w = w;
   a.rope_cs = rope_cs;
@@ -260,6 +261,7 @@ static int prep_q_checked(const IndexerDims* dims, const indexer_bf16* q, const 
   a.n_vec = (long long)B * S * dims->n_heads;
   a.S = S;
   a.H = dims->n_heads;
+  a.h_shift = __builtin_ctz((unsigned)dims->n_heads);
   a.rope_dim = dims->rope_dim;
   a.start_pos = start_pos;
   a.w_scale = (float)(1.0 / std::sqrt((double)dims->head_dim) / std::sqrt((double)dims->n_heads));
@@ -285,7 +287,8 @@ int indexer_prep_q(const IndexerDims* dims, const indexer_bf16* q, const indexer
                    const float* rope_cs, int max_pos, uint8_t* q_rows, float* w_prime, indexer_stream_t stream) {
   RETURN_IF(check_prep_args(dims, q, w, B, S, start_pos, rope_cs, max_pos));
   if (!q_rows || !w_prime) return fail(INDEXER_ERR_NULL, "q_rows and w_prime must not be NULL");
-  if (!aligned(q_rows, 4) || !aligned(w_prime, 4)) return fail(INDEXER_ERR_ALIGN, "q_rows and w_prime must be 4-byte aligned");
+  if (!aligned(q_rows, 16) || !aligned(w_prime, 4))
+    return fail(INDEXER_ERR_ALIGN, "q_rows must be 16-byte aligned and w_prime 4-byte aligned");
   RETURN_IF(check_arch());
   RETURN_IF(prep_q_checked(dims, q, w, B, S, start_pos, rope_cs, q_rows, w_prime, (cudaStream_t)stream));
   return ok();
@@ -427,7 +430,8 @@ int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexe
   uint8_t* q_rows = base + l.q_rows;
   float* w_prime = reinterpret_cast<float*>(base + l.w_prime);
   float* scores = scores_out ? scores_out : reinterpret_cast<float*>(base + l.scores);
-  RETURN_IF(prep_q_checked(dims, q, w, B, S, start_pos, rope_cs, q_rows, w_prime, st));
+  RETURN_IF(prep_q_checked(dims, q, w, B, S, start_pos, rope_cs, q_rows, w_prime, st,
+                           reinterpret_cast<uint32_t*>(base)));
   // level two with one query row and no score output: only the kept blocks' keys are
   // scored and ranked (the other positions of the workspace scores are never read)
   const bool sparse2 = cand_in && !cand_out && !scores_out && S == 1 && T <= 32768 &&
@@ -592,9 +596,11 @@ int indexer_forward_paged(const IndexerDims* dims, const indexer_bf16* q, const 
     a.q_rows = q_rows;
     a.w_prime = w_prime;
     a.rows = rows;
+    a.status = status;
     a.n_vec = (long long)Q * dims->n_heads;
     a.S = 1;
     a.H = dims->n_heads;
+    a.h_shift = __builtin_ctz((unsigned)dims->n_heads);
     a.rope_dim = dims->rope_dim;
     a.w_scale = (float)(1.0 / std::sqrt((double)dims->head_dim) / std::sqrt((double)dims->n_heads));
     const cudaError_t e = launch_prep_q(a, st);

@@ -252,6 +252,12 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
     if (E <= 512 * 8) return launch_overlapped(topk_sparse_kernel<512, 8>, grid, dim3(512), 0, stream, a);
     return launch_overlapped(topk_sparse_kernel<kSelThreads, 8>, grid, dim3(kSelThreads), 0, stream, a);
   }
+  if (a.rows >= 4096 && a.T > 256 * 8 && a.T <= 256 * 32) {
+    // many rows (prefill): 256 threads per row with up to 32 keys each, so several rows
+    // share an SM; the latency of one row matters less than the rows per second
+    if (a.T <= 256 * 16) return launch_overlapped(topk_kernel<256, 16>, grid, dim3(256), 0, stream, a);
+    return launch_overlapped(topk_kernel<256, 32>, grid, dim3(256), 0, stream, a);
+  }
   // eight keys per thread and no more threads than keys up to 8192 positions
   if (a.T <= 256 * 8) return launch_overlapped(topk_kernel<256, 8>, grid, dim3(256), 0, stream, a);
   if (a.T <= 512 * 8) return launch_overlapped(topk_kernel<512, 8>, grid, dim3(512), 0, stream, a);

@@ -229,7 +229,8 @@ __global__ void __launch_bounds__(256) prep_q_kernel(PrepArgs a) {
   if (v >= a.n_vec) return;   // whole 16-lane groups leave together
   const int lane = tid & 31;
   const unsigned gmask = 0xFFFFu << (lane & 16);
-  const int pos = a.rows ? a.rows[v / a.H].pos : a.start_pos + (int)((v / a.H) % a.S);
+  const int qrow = (int)(v >> a.h_shift);   // H is a power of two
+  const int pos = a.rows ? a.rows[qrow].pos : a.start_pos + qrow % a.S;
   const uint4 raw = *reinterpret_cast<const uint4*>(a.q + v * kHeadDim + j * 8);
   float2 c[4];
   load_rope_slice(reinterpret_cast<const float2*>(a.rope_cs) + (size_t)pos * (a.rope_dim / 2), j, a.rope_dim, c);
@@ -241,9 +242,81 @@ __global__ void __launch_bounds__(256) prep_q_kernel(PrepArgs a) {
   if (j == 0) a.w_prime[v] = bf16_to_f32(a.w[v]) * a.w_scale;
 }
 
+// Many vectors (prefill): a CTA takes 64 vectors, brings their 16 KB of bf16 q into shared
+// memory with one bulk copy (so the copy engine, not registers, holds the bytes in flight),
+// quantises them with the same per-slice arithmetic, stages the 68-byte rows and w' and
+// writes them out as whole 16-byte chunks.
+constexpr int kPrepBulkVecs = 64;
+
+__global__ void __launch_bounds__(256) prep_q_bulk_kernel(PrepArgs a) {
+  constexpr int NV = kPrepBulkVecs;
+  __shared__ __align__(128) uint16_t sq[NV * kHeadDim];
+  __shared__ __align__(16) uint8_t srow[NV * kRowBytes];
+  __shared__ __align__(16) float sw[NV];
+  __shared__ __align__(8) uint64_t bar;
+  pdl_allow_next();
+  const int tid = threadIdx.x;
+  const long long v0 = (long long)blockIdx.x * NV;
+  const int nv = (int)(a.n_vec - v0 < NV ? a.n_vec - v0 : NV);
+  const uint32_t b = smem_u32(&bar);
+  if (tid == 0) {
+    mbar_init(b, 1u);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  if (tid == 0) {
+    const uint32_t qbytes = (uint32_t)(nv * kHeadDim * 2);
+    mbar_arrive_expect_tx(b, qbytes);
+    bulk_g2s(smem_u32(sq), a.q + v0 * kHeadDim, qbytes, b);
+  }
+  uint32_t wbits = 0u;
+  if (tid < nv) wbits = a.w[v0 + tid];
+  if (!__syncthreads_and(warp_wait_bounded(b, 0u))) {   // the copy did not land in time: report and leave
+    if (tid == 0) {
+      if (a.status) atomicOr(a.status, kStatusLoadTimeout);
+      mbar_wait(b, 0u);   // one more bounded wait for the copy before shared memory goes
+    }
+    return;
+  }
+  const int g = tid >> 4, j = tid & 15;
+  const int lane = tid & 31;
+  const unsigned gmask = 0xFFFFu << (lane & 16);
+#pragma unroll
+  for (int p = 0; p < NV / 16; ++p) {
+    const int vi = 16 * p + g;
+    if (vi < nv) {   // the 16 lanes of a group agree
+      const long long v = v0 + vi;
+      const int qrow = (int)(v >> a.h_shift);   // H is a power of two
+      const int pos = a.rows ? a.rows[qrow].pos : a.start_pos + qrow % a.S;
+      float2 c[4];
+      load_rope_slice(reinterpret_cast<const float2*>(a.rope_cs) + (size_t)pos * (a.rope_dim / 2), j, a.rope_dim, c);
+      const uint4 raw = *reinterpret_cast<const uint4*>(sq + vi * kHeadDim + j * 8);
+      int e;
+      const uint32_t word = quant_q_slice(raw, j, c, a.rope_dim, gmask, &e);
+      *reinterpret_cast<uint32_t*>(srow + vi * kRowBytes + 4 * j) = word;
+      if ((j & 3) == 0) srow[vi * kRowBytes + kCodeBytes + (j >> 2)] = (uint8_t)(e + 127);
+    }
+  }
+  if (tid < nv) sw[tid] = bf16_to_f32(wbits) * a.w_scale;
+  __syncthreads();
+  uint8_t* dst = a.q_rows + v0 * kRowBytes;   // 16-byte aligned: 64 * 68 is a multiple of 16
+  const int bytes = nv * kRowBytes, whole = bytes & ~15;
+  for (int o = tid * 16; o < whole; o += 256 * 16)
+    *reinterpret_cast<uint4*>(dst + o) = *reinterpret_cast<const uint4*>(srow + o);
+  for (int o = whole + tid * 4; o < bytes; o += 256 * 4)
+    *reinterpret_cast<uint32_t*>(dst + o) = *reinterpret_cast<const uint32_t*>(srow + o);
+  for (int i = tid; i < nv; i += 256) a.w_prime[v0 + i] = sw[i];
+}
+
 cudaError_t launch_prep_q(const PrepArgs& a, cudaStream_t stream) {
-  const long long blocks = (a.n_vec + 15) / 16;
-  return launch_overlapped(prep_q_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, a);
+  // few vectors (decode): one per 16-thread group, for the shortest chain; many: bulk copies
+  if (a.n_vec <= 16384) {
+    const long long blocks = (a.n_vec + 15) / 16;
+    return launch_overlapped(prep_q_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, a);
+  }
+  const long long blocks = (a.n_vec + kPrepBulkVecs - 1) / kPrepBulkVecs;
+  return launch_overlapped(prep_q_bulk_kernel, dim3((unsigned)blocks), dim3(256), 0, stream, a);
 }
 
 // ---------------------------------------------------------------------------- batch plan

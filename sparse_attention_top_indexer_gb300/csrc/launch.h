@@ -90,8 +90,10 @@ struct PrepArgs {
   uint8_t* q_rows;          // [rows][H][68]
   float* w_prime;           // [rows][H]
   const RowInfo* rows = nullptr;   // per-row positions, or nullptr: row r is at start_pos + r % S
+  uint32_t* status = nullptr;      // status word for a bounded wait that ran out, or nullptr
   long long n_vec;          // rows * H
   int S, H, rope_dim, start_pos;
+  int h_shift;              // log2(H)
   float w_scale;            // head_dim^-0.5 * H^-0.5
 };
 cudaError_t launch_prep_q(const PrepArgs& a, cudaStream_t stream);

@@ -119,16 +119,21 @@ def _sample_rows(wl: Workload, n_rand: int, seed: int):
     return rows
 
 
-@pytest.mark.parametrize("name,n_rand", [("prefill", 40), ("large_prefill", 24)])
+# prefill_t4096: 16384 rows over 4096 keys, the many-rows top-k with 16 keys per thread
+_SAMPLED = {"prefill": WORKLOADS["prefill"], "large_prefill": WORKLOADS["large_prefill"],
+            "prefill_t4096": dataclasses.replace(WORKLOADS["prefill"], name="prefill_t4096", S=16384, topk=1024)}
+
+
+@pytest.mark.parametrize("name,n_rand", [("prefill", 40), ("large_prefill", 24), ("prefill_t4096", 24)])
 def test_forward_prefill_sampled(X, name, n_rand):
-    wl = WORKLOADS[name]
+    wl = _SAMPLED[name]
     table = C.gpu_table(wl.max_pos)
     cos, sin = C.oracle_table(wl.max_pos)
     cache = C.gpu_cache(wl, table)
     ref_cache = C.oracle_cache(wl, cos, sin)
     assert np.array_equal(C.pages_to_rows(cache), ref_cache)
     q, w = wl.q("cuda"), wl.w("cuda")
-    top, _, sc = _run_forward(X, wl, q, w, table, cache, want_scores=(name == "prefill"))
+    top, _, sc = _run_forward(X, wl, q, w, table, cache, want_scores=(name != "large_prefill"))
     top_np = top.cpu().numpy()
     _check_properties(top_np, wl)
     w_cpu = w.cpu()
