@@ -17,6 +17,8 @@ __all__ = [
     "rope_interleaved", "fp4_quant_e8m0", "pack_row68", "unpack_row68", "dequant_row68",
     "key_slots", "publish_keys", "prep_queries", "visible_lens", "index_scores",
     "select_candidate_blocks", "candidate_mask", "topk_positions", "forward",
+    "FP8_BLOCK", "E4M3_GRID", "FP8_SCALE_FLOOR", "FP8_ROW_BYTES", "fp8_quant_ue8m0", "pack_row132",
+    "dequant_row132", "dequant_row", "quantise_rows",
 ]
 
 # fp4_block_size (compress module page, constant FP4_BLOCK).
@@ -220,6 +222,83 @@ def dequant_row68(rows: np.ndarray, head_dim: int = 128) -> np.ndarray:
     return sign * np.ldexp(mag, e_full)
 
 
+# ----------------------------------------------------------------------------- FP8 rows
+# The FP8 indexer cache row (attention.py patch page, _indexer_k_cache_head_dim, FP8
+# branch: "128 fp8 + 4 fp32 scale" = 132 bytes for head_dim 128; DeepseekV4Indexer:
+# scale_fmt "ue8m0", quant_block_size 128). Readings: one block of 128 values per
+# row; the scale is a power of two (UE8M0), the ceiling of amax / 448 (448 = largest
+# e4m3 magnitude) with amax floored at 448 * 2**-126, stored as an f32; values x / scale
+# rounded to the nearest e4m3 value, ties to the even code, keeping the sign; codes
+# element i in byte i, then the f32 scale (little-endian).
+FP8_BLOCK = 128
+FP8_MAX = 448.0
+FP8_SCALE_FLOOR = FP8_MAX * 2.0 ** -126
+FP8_ROW_BYTES = 128 + 4
+# e4m3 (the OCP "fn" variant: no infinities, code 0x7F is NaN) magnitudes by 7-bit code:
+# exponent field E = code >> 3, mantissa M = code & 7; E = 0: M/8 * 2**-6 (subnormal),
+# else (1 + M/8) * 2**(E - 7). Codes 0..126 ascend.
+E4M3_GRID = np.array([((c & 7) / 8.0) * 2.0 ** -6 if (c >> 3) == 0 else (1.0 + (c & 7) / 8.0) * 2.0 ** ((c >> 3) - 7)
+                      for c in range(127)])
+
+
+def _ue8m0_exponent_fp8(amax: np.ndarray) -> np.ndarray:
+    """Smallest integer e with 448 * 2**e >= max(amax, 448 * 2**-126)."""
+    a = np.maximum(amax, FP8_SCALE_FLOOR)
+    e = np.ceil(np.log2(a / FP8_MAX)).astype(np.int64)   # first guess, then made exact
+    e = np.where(np.ldexp(FP8_MAX, e - 1) >= a, e - 1, e)
+    e = np.where(np.ldexp(FP8_MAX, e) < a, e + 1, e)
+    return e
+
+
+def fp8_quant_ue8m0(x_bits: np.ndarray):
+    """Per 128-value row: scale 2**e (e from _ue8m0_exponent_fp8 of the row's amax),
+    x / 2**e (exact) rounded to the nearest e4m3 magnitude, ties to the even code,
+    sign in bit 7. Returns (codes uint8 [..., 128], exponents int64 [...], dequantised
+    f64 values [..., 128])."""
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    x = bf16_to_f64(x_bits)
+    neg = ((x_bits >> 15) & 1).astype(np.uint8)
+    e = _ue8m0_exponent_fp8(np.max(np.abs(x), axis=-1))
+    y = np.ldexp(np.abs(x), -e[..., None])                   # exact, <= 448
+    hi = np.clip(np.searchsorted(E4M3_GRID, y, side="left"), 0, len(E4M3_GRID) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_hi, d_lo = E4M3_GRID[hi] - y, y - E4M3_GRID[lo]
+    take_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (lo % 2 == 0))
+    mag = np.where(take_lo, lo, hi).astype(np.uint8)
+    codes = mag | (neg << 7)
+    deq = np.where(neg == 1, -1.0, 1.0) * np.ldexp(E4M3_GRID[mag], e[..., None])
+    return codes, e, deq
+
+
+def pack_row132(codes: np.ndarray, e: np.ndarray) -> np.ndarray:
+    """128 code bytes then the f32 scale 2**e, little-endian."""
+    sc = np.ldexp(np.ones(e.shape, dtype=np.float32), e.astype(np.int32)).astype("<f4")
+    return np.concatenate([codes.astype(np.uint8), sc[..., None].view(np.uint8)], axis=-1)
+
+
+def dequant_row132(rows: np.ndarray) -> np.ndarray:
+    """Exact f64 values of FP8 rows: sign * e4m3 magnitude * scale."""
+    rows = np.asarray(rows, dtype=np.uint8)
+    codes = rows[..., :128]
+    sc = np.ascontiguousarray(rows[..., 128:132]).view("<f4")[..., 0].astype(np.float64)
+    mag = E4M3_GRID[np.minimum(codes & 0x7F, 126)]
+    return np.where(codes & 0x80, -1.0, 1.0) * mag * sc[..., None]
+
+
+def dequant_row(rows: np.ndarray) -> np.ndarray:
+    """Dequantised values of 68-byte (MXFP4) or 132-byte (FP8) rows."""
+    return dequant_row132(rows) if rows.shape[-1] == FP8_ROW_BYTES else dequant_row68(rows)
+
+
+def quantise_rows(x_bits: np.ndarray, fmt: str = "mxfp4") -> np.ndarray:
+    """The cache row of each 128-value vector in the given format."""
+    if fmt == "fp8":
+        codes, e, _ = fp8_quant_ue8m0(x_bits)
+        return pack_row132(codes, e)
+    codes, scales, _ = fp4_quant_e8m0(x_bits)
+    return pack_row68(codes, scales)
+
+
 def key_slots(start_pos: int, G: int, ratio: int):
     """Cache slots and RoPE positions of the G keys published by one forward
     (index-keys page, Indexer.forward, key publish): prefill (start_pos == 0)
@@ -235,7 +314,7 @@ def key_slots(start_pos: int, G: int, ratio: int):
 
 
 def publish_keys(latent_bits, wk_bits, knorm_bits, cos, sin, start_pos: int, ratio: int,
-                 rope_dim: int, eps: float):
+                 rope_dim: int, eps: float, fmt: str = "mxfp4"):
     """Key publish (index-keys page, Indexer.forward): k = k_norm(wk(latent)),
     RoPE on the last rope_dim dims at the group position, fp4_act_quant, and the
     row written at slot start_pos//ratio + j. Returns (slots, rows [B, G, 68],
@@ -245,12 +324,11 @@ def publish_keys(latent_bits, wk_bits, knorm_bits, cos, sin, start_pos: int, rat
     k = linear_bf16(latent_bits, wk_bits)
     k = rmsnorm_bf16(k, knorm_bits, eps)
     k = rope_interleaved(k, cos, sin, positions[None, :], rope_dim)
-    codes, scales, _ = fp4_quant_e8m0(k)
-    return slots, pack_row68(codes, scales), k
+    return slots, quantise_rows(k, fmt), k
 
 
 def prep_queries(q_bits, w_bits, cos, sin, start_pos: int, rope_dim: int, n_heads: int,
-                 row_positions: Optional[np.ndarray] = None):
+                 row_positions: Optional[np.ndarray] = None, fmt: str = "mxfp4"):
     """Query prep (index-keys page, Indexer.forward and __init__): RoPE at the
     query's own position start_pos + s, fp4_act_quant, and head weights scaled by
     softmax_scale * n_heads**-0.5 with softmax_scale = index_head_dim**-0.5.
@@ -261,9 +339,8 @@ def prep_queries(q_bits, w_bits, cos, sin, start_pos: int, rope_dim: int, n_head
     B, S, H, D = q_bits.shape
     pos = (start_pos + np.arange(S)) if row_positions is None else np.asarray(row_positions)
     qr = rope_interleaved(q_bits, cos, sin, np.broadcast_to(pos[None, :, None], (B, S, H)), rope_dim)
-    codes, scales, _ = fp4_quant_e8m0(qr)
     wprime = bf16_to_f64(w_bits) * (D ** -0.5 * n_heads ** -0.5)
-    return pack_row68(codes, scales), wprime, qr
+    return quantise_rows(qr, fmt), wprime, qr
 
 
 def visible_lens(start_pos: int, S: int, ratio: int, row_positions: Optional[np.ndarray] = None):
@@ -278,15 +355,15 @@ def index_scores(q_rows, wprime, k_rows, T: int, vis: np.ndarray, chunk: int = 2
     """score[b,s,t] = sum_h w'[b,s,h] * relu(sum_d q[b,s,h,d] * k[b,t,d]) over the
     dequantised fp4 values (index-keys page, Indexer.forward: einsum bshd,btd->bsht,
     relu, times weights, sum over heads), with t >= vis[s] set to -inf (causal
-    mask). f64 throughout; q rows [B,S,H,68], k rows [B,>=T,68], vis [S]."""
+    mask). f64 throughout; q rows [B,S,H,68 or 132], k rows [B,>=T,same width], vis [S]."""
     B, S, H, _ = q_rows.shape
-    kd = dequant_row68(k_rows[:, :T])                       # [B, T, D]
+    kd = dequant_row(k_rows[:, :T])                         # [B, T, D]
     out = np.empty((B, S, T), dtype=np.float64)
     t = np.arange(T)
     for b in range(B):
         for s0 in range(0, S, chunk):
             s1 = min(S, s0 + chunk)
-            qd = dequant_row68(q_rows[b, s0:s1])            # [s, H, D]
+            qd = dequant_row(q_rows[b, s0:s1])              # [s, H, D]
             dots = np.einsum("shd,td->sht", qd, kd[b])
             sc = np.einsum("sht,sh->st", np.maximum(dots, 0.0), wprime[b, s0:s1])
             sc[t[None, :] >= vis[s0:s1, None]] = -np.inf
@@ -365,7 +442,7 @@ def topk_positions(scores: np.ndarray, vis: np.ndarray, index_topk: int, offset:
 
 def forward(q_bits, w_bits, k_rows, cos, sin, start_pos: int, ratio: int, rope_dim: int, index_topk: int,
             offset: int, cand_in: Optional[np.ndarray] = None, cand_topk_blocks: int = 0,
-            cand_block_size: int = 0, want_candidates: bool = False):
+            cand_block_size: int = 0, want_candidates: bool = False, fmt: Optional[str] = None):
     """Indexer.forward after the key publish (index-keys page): query prep,
     scores, causal mask, optional level-one candidate publication (source layer)
     or level-two candidate mask (consumer), then top-k. k_rows is the cache
@@ -373,7 +450,9 @@ def forward(q_bits, w_bits, k_rows, cos, sin, start_pos: int, ratio: int, rope_d
     candidate blocks [B,S,cbk] or None, masked scores [B,S,T])."""
     B, S, H, D = q_bits.shape
     T = (start_pos + S) // ratio
-    q_rows, wprime, _ = prep_queries(q_bits, w_bits, cos, sin, start_pos, rope_dim, H)
+    if fmt is None:   # the queries take the keys' format
+        fmt = "fp8" if k_rows.shape[-1] == FP8_ROW_BYTES else "mxfp4"
+    q_rows, wprime, _ = prep_queries(q_bits, w_bits, cos, sin, start_pos, rope_dim, H, fmt=fmt)
     vis = visible_lens(start_pos, S, ratio)
     sc = index_scores(q_rows, wprime, k_rows, T, vis)
     cand_out = None

@@ -494,3 +494,94 @@ def test_forward_tiny_composition():
         assert np.all(top[0, s, :n] >= 0) and np.all(top[0, s, n:] == -1)
         if vis[s] <= 16:
             assert list(top[0, s, :n]) == list(range(n))
+
+
+# ----------------------------------------------------------------------------- FP8 rows
+def _torch_e4m3_codes(x_f32: np.ndarray) -> np.ndarray:
+    """PyTorch's float32 -> float8_e4m3fn conversion (round to nearest even) as bytes."""
+    torch = pytest.importorskip("torch")
+    return torch.from_numpy(np.ascontiguousarray(x_f32, dtype=np.float32)).to(torch.float8_e4m3fn) \
+        .view(torch.uint8).numpy()
+
+
+def test_e4m3_rounding_exhaustive_against_torch():
+    """Every finite bf16 value in [-448, 448] (which includes every e4m3 midpoint, so every
+    tie) rounds like PyTorch's float8_e4m3fn conversion, sign kept for values that round
+    to zero. Each row carries 448 so that its scale is 2**0."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    v = O.bf16_to_f64(bits)
+    ok = np.isfinite(v) & (np.abs(v) <= 448.0)
+    vals = bits[ok]
+    n = (len(vals) + 126) // 127 * 127
+    padded = np.concatenate([vals, np.zeros(n - len(vals), np.uint16)]).reshape(-1, 127)
+    rows = np.concatenate([np.full((padded.shape[0], 1), O.f32_to_bf16(np.float32(448.0)), np.uint16), padded],
+                          axis=1)
+    codes, e, _ = O.fp8_quant_ue8m0(rows)
+    assert np.all(e == 0)
+    ref = _torch_e4m3_codes(O.bf16_to_f64(rows).astype(np.float32))
+    assert np.array_equal(codes, ref)
+
+
+def test_e4m3_golden_ties():
+    """Hand-worked ties between neighbouring e4m3 values go to the even code."""
+    cases = {1.0625: 1.0, 1.1875: 1.25, 17.0: 16.0, 19.0: 20.0, 0.0029296875: 0.00390625, 0.0009765625: 0.0,
+             -0.0009765625: -0.0, 440.0: 448.0, 424.0: 416.0}
+    for x, want in cases.items():
+        row = np.zeros(128, np.uint16)
+        row[0] = O.f32_to_bf16(np.float32(448.0))
+        row[1] = O.f32_to_bf16(np.float32(x))
+        _, e, deq = O.fp8_quant_ue8m0(row[None])
+        assert e[0] == 0 and deq[0, 1] == want and math.copysign(1.0, deq[0, 1]) == math.copysign(1.0, want), x
+
+
+def test_ue8m0_fp8_closed_forms():
+    """The scale is the smallest power of two 2**e with 448 * 2**e >= amax; all-zero rows
+    take the floor 2**-126."""
+    for amax, want in [(448.0, 0), (450.0, 1), (224.0, -1), (225.0, 0), (0.875, -9), (0.0, -126), (2.0 ** -127, -126),
+                       (3.5 * 2.0 ** 100, 93)]:
+        row = np.zeros(128, np.uint16)
+        row[5] = O.f32_to_bf16(np.float32(amax))
+        assert O.bf16_to_f64(row[5]) == amax, amax
+        _, e, _ = O.fp8_quant_ue8m0(row[None])
+        assert e[0] == want, (amax, e[0], want)
+
+
+def test_fp8_error_bound_and_row_bytes():
+    """|x - deq| is within half an e4m3 step: 2**-4 |x| for normal values, 2**(e-10) at the
+    subnormal end; the row is the 128 codes then the f32 scale little-endian."""
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal((64, 128)) * np.exp(rng.uniform(-20, 20, (64, 1)))).astype(np.float32)
+    bits = O.f32_to_bf16(x)
+    codes, e, deq = O.fp8_quant_ue8m0(bits)
+    xv = O.bf16_to_f64(bits)
+    assert np.all(np.abs(xv - deq) <= np.maximum(np.abs(xv) * 2.0 ** -4, np.ldexp(1.0, e[:, None] - 10)))
+    rows = O.pack_row132(codes, e)
+    assert rows.shape == (64, 132) and np.array_equal(rows[:, :128], codes)
+    sc = rows[:, 128:].copy().view("<f4")[:, 0]
+    assert np.array_equal(sc.astype(np.float64), np.ldexp(1.0, e))
+    one = O.pack_row132(np.zeros((1, 128), np.uint8), np.array([0]))
+    assert list(one[0, 128:]) == [0x00, 0x00, 0x80, 0x3F]
+    assert np.array_equal(O.dequant_row132(rows), deq)
+
+
+def test_fp8_scores_against_torch_dequantisation():
+    """index_scores on FP8 rows equals sum_h w' relu(q . k) with q and k dequantised by
+    PyTorch's e4m3 conversion times the rows' scales (one head with w' = 1 reduces to
+    relu(q . k))."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(5)
+    q = O.f32_to_bf16(rng.standard_normal((1, 3, 4, 128)).astype(np.float32))
+    k = O.f32_to_bf16((rng.standard_normal((1, 9, 128)) * 3).astype(np.float32))
+    qr, kr = O.quantise_rows(q, "fp8"), O.quantise_rows(k, "fp8")
+    w = rng.standard_normal((1, 3, 4))
+
+    def deq(rows):
+        vals = torch.from_numpy(np.ascontiguousarray(rows[..., :128])).view(torch.float8_e4m3fn).float().numpy()
+        sc = np.ascontiguousarray(rows[..., 128:]).view("<f4")[..., 0]
+        return vals.astype(np.float64) * sc[..., None]
+    dq, dk = deq(qr), deq(kr)
+    ref = np.einsum("sht,sh->st", np.maximum(np.einsum("shd,td->sht", dq[0], dk[0]), 0.0), w[0])
+    got = O.index_scores(qr, w, kr, 9, np.full(3, 9))[0]
+    assert np.allclose(got, ref, rtol=0, atol=1e-12 * np.abs(ref).max())
+    one = O.index_scores(qr[:, :, :1], np.ones((1, 3, 1)), kr, 9, np.full(3, 9))[0]
+    assert np.allclose(one, np.maximum(dq[0, :, 0] @ dk[0].T, 0.0), rtol=0, atol=1e-12)
