@@ -49,6 +49,14 @@ from workloads import MIXED, ROPE, WORKLOADS, MixedBatch, Workload, normal_bf16 
 METRIC = "indexer score+top-k queries/s and key-scores/s; % of HBM / FP4-MMA roofline"
 UNIT = "queries/s"
 FP4_OVER_BF16 = 13.5 / 2.25          # nominal dense fp4 / bf16 tensor ratio of the part
+FP8_OVER_BF16 = 4.5 / 2.25           # nominal dense fp8 / bf16 tensor ratio of the part
+
+
+def fmt_of(wl) -> dict:
+    """Row format of a workload: MXFP4 (68-byte rows) or FP8 (132-byte rows)."""
+    if getattr(wl, "key_format", 0) == 1:
+        return {"name": "fp8", "row": 132, "dtype": "e4m3 x e4m3 -> f32", "ratio": FP8_OVER_BF16, "label": "fp8"}
+    return {"name": "mxfp4", "row": 68, "dtype": "e2m1 x e2m1 -> f32", "ratio": FP4_OVER_BF16, "label": "fp4"}
 ROTATE = 16
 
 
@@ -201,7 +209,7 @@ class Setup:
         X.load_library()
         self.dims = X.make_dims(n_heads=wl.H, ratio=wl.ratio, index_topk=wl.topk, offset=wl.offset,
                                 rope_dim=wl.rope_dim, head_dim=wl.D, cand_topk_blocks=wl.cand_topk_blocks,
-                                cand_block_size=wl.cand_block_size, norm_eps=wl.norm_eps)
+                                cand_block_size=wl.cand_block_size, norm_eps=wl.norm_eps, key_format=wl.key_format)
         self.table = torch.empty((wl.max_pos, wl.rope_dim // 2, 2), dtype=torch.float32, device=dev)
         X.indexer_rope_table(X.IndexerYarn(ROPE.theta, ROPE.factor, ROPE.original_seq_len, ROPE.beta_fast,
                                            ROPE.beta_slow), wl.rope_dim, wl.max_pos, self.table)
@@ -209,13 +217,14 @@ class Setup:
         self.decode = wl.S == 1 and wl.start_pos > 0
         self.rotate = rotate
         if self.decode:
-            base = X.new_key_cache(wl.B, wl.T_cap, device=dev)
+            base = X.new_key_cache(wl.B, wl.T_cap, device=dev, key_format=wl.key_format)
             X.indexer_publish_k(self.dims, wl.latent(dev), self.wk, self.knw, self.table, 0, base)
             self.caches = [base] + [base.clone() for _ in range(rotate - 1)]
             self.lat = [normal_bf16(wl.seed, f"{wl.name}/latent_step/{i}", (wl.B, 1, wl.D), device=dev)
                         for i in range(rotate)]
         else:
-            self.caches = [X.new_key_cache(wl.B, wl.T_cap, device=dev) for _ in range(rotate)]
+            self.caches = [X.new_key_cache(wl.B, wl.T_cap, device=dev, key_format=wl.key_format)
+                           for _ in range(rotate)]
             self.lat = [normal_bf16(wl.seed, f"{wl.name}/latent/{i}", (wl.B, wl.T, wl.D), device=dev)
                         for i in range(rotate)]
         tags = ["q1", "q2"] if wl.two_level else ["q"]
@@ -231,7 +240,7 @@ class Setup:
         self.cand = (torch.empty((wl.B, wl.S, wl.cand_topk_blocks), dtype=torch.int32, device=dev)
                      if wl.two_level else None)
         # split-entry buffers for the per-kernel breakdown
-        self.q_rows = torch.empty((wl.B, wl.S, wl.H, 68), dtype=torch.uint8, device=dev)
+        self.q_rows = torch.empty((wl.B, wl.S, wl.H, X.row_bytes(wl.key_format)), dtype=torch.uint8, device=dev)
         self.w_prime = torch.empty((wl.B, wl.S, wl.H), dtype=torch.float32, device=dev)
         self.scores = torch.empty((wl.B, wl.S, wl.T), dtype=torch.float32, device=dev)
 
@@ -282,11 +291,10 @@ def visible_pairs(wl: Workload) -> int:
 def score_units(wl: Workload):
     """Algorithmic work of one scores launch: HBM bytes and tensor flops."""
     pairs = visible_pairs(wl)
-    if wl.S == 1:   # decode: every key of a sequence is read once
-        key_bytes = wl.B * wl.T * 68
-    else:           # prefill: the sequence's keys are read once (they stay in L2 across query groups)
-        key_bytes = wl.B * wl.T * 68
-    q_bytes = wl.B * wl.S * wl.H * (68 + 4)
+    rb = 132 if wl.key_format == 1 else 68   # bytes per key / query-head row
+    # every key of a sequence is read once (prefill: they stay in L2 across query groups)
+    key_bytes = wl.B * wl.T * rb
+    q_bytes = wl.B * wl.S * wl.H * (rb + 4)
     out_bytes = pairs * 4
     flops = pairs * wl.H * wl.D * 2
     return {"bytes": key_bytes + q_bytes + out_bytes, "flops": flops, "pairs": pairs}
@@ -363,25 +371,27 @@ def run_ours(args, dist: Dist):
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak if achieved else None,
                 "traffic": profile_traffic(f"scores_{wl.name}"),
-                "algorithmic_bytes_per_launch": units["bytes"], "kernel": "score_kernel<64,1>",
+                "algorithmic_bytes_per_launch": units["bytes"], "kernel": f"score_kernel<{wl.H},1,1,{fmt_of(wl)['name']}>",
                 "kernel_ms": score_ms, "peak_source": f"{peaks['source']} hbm_gbs"}
     else:
         achieved = units["flops"] / (score_ms / 1e3) / 1e12 if score_ms else None
-        peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+        fm = fmt_of(wl)
+        peak = peaks["bf16_tflops"] * fm["ratio"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak if achieved else None,
                 "traffic": profile_traffic(f"scores_{wl.name}"),
-                "algorithmic_flops_per_launch": units["flops"], "kernel": "score_kernel",
+                "algorithmic_flops_per_launch": units["flops"], "kernel": "score_rows_kernel",
                 "kernel_ms": score_ms,
-                "peak_source": f"{peaks['source']} bf16_tflops x {FP4_OVER_BF16:g} (nominal fp4/bf16)"}
+                "peak_source": f"{peaks['source']} bf16_tflops x {fm['ratio']:g} (nominal {fm['label']}/bf16)"}
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e2m1 x e2m1 -> f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": fmt_of(wl)["dtype"], "data": "synthetic",
         "config": {"workload": describe(wl), "B": wl.B, "S": wl.S, "start_pos": wl.start_pos, "T": wl.T,
                    "H": wl.H, "topk": wl.topk, "ratio": wl.ratio,
-                   "l2": (f"{rotate} rotating key caches / inputs ({rotate * wl.B * wl.T_cap * 68 / 1e6:.0f} MB)"
+                   "l2": (f"{rotate} rotating key caches / inputs "
+                          f"({rotate * wl.B * wl.T_cap * (132 if wl.key_format == 1 else 68) / 1e6:.0f} MB)"
                           if rotate > 1 else "inputs larger than L2"),
                    "timing": "CUDA-graph replay, CUDA events on the launching stream"},
         "key_scores_per_s": key_scores,
@@ -631,7 +641,7 @@ def describe(wl: Workload) -> str:
     kind = "decode" if wl.S == 1 else "prefill"
     extra = f", two-level {wl.cand_topk_blocks}x{wl.cand_block_size} candidate blocks" if wl.two_level else ""
     return (f"{wl.name}: {kind} B{wl.B} S{wl.S} start_pos {wl.start_pos}, ratio {wl.ratio} -> {wl.T} compressed "
-            f"positions, H{wl.H} fp4 heads, top-{wl.topk}, offset {wl.offset}{extra}")
+            f"positions, H{wl.H} {fmt_of(wl)['label']} heads, top-{wl.topk}, offset {wl.offset}{extra}")
 
 
 # ----------------------------------------------------------------------------- oracle arm / baseline
@@ -650,8 +660,8 @@ class OracleSample:
         self.cache = []
         for b in range(self.n_seq):
             slots, rows, _ = O.publish_keys(C.bits(lat[b:b + 1]), self.wk, self.knw, self.cos, self.sin, 0, wl.ratio,
-                                            wl.rope_dim, wl.norm_eps)
-            c = np.zeros((1, wl.T_cap, 68), np.uint8)
+                                            wl.rope_dim, wl.norm_eps, fmt=fmt_of(wl)["name"])
+            c = np.zeros((1, wl.T_cap, fmt_of(wl)["row"]), np.uint8)
             c[0, slots] = rows[0]
             self.cache.append(c)
         self.q = C.bits(wl.q()[: self.n_seq])
@@ -663,11 +673,11 @@ class OracleSample:
         O, wl = self.O, self.wl
         if self.dl is not None:
             slots, rows, _ = O.publish_keys(self.dl[b:b + 1], self.wk, self.knw, self.cos, self.sin, wl.start_pos,
-                                            wl.ratio, wl.rope_dim, wl.norm_eps)
+                                            wl.ratio, wl.rope_dim, wl.norm_eps, fmt=fmt_of(wl)["name"])
             self.cache[b][0, slots] = rows[0]
         T = max(1, int(math.ceil(wl.T * key_frac)))
         rows_q, wprime, _ = O.prep_queries(self.q[b:b + 1], self.w[b:b + 1], self.cos, self.sin, wl.start_pos,
-                                           wl.rope_dim, wl.H)
+                                           wl.rope_dim, wl.H, fmt=fmt_of(wl)["name"])
         vis = np.minimum(O.visible_lens(wl.start_pos, wl.S, wl.ratio), T)
         sc = O.index_scores(rows_q, wprime, self.cache[b], T, vis)
         O.topk_positions(sc[0], vis, max(1, int(math.ceil(wl.topk * key_frac))), wl.offset, T)

@@ -47,6 +47,15 @@
  *       * a page pool k_pool[num_pages][4352] shared by many sequences, with a block
  *         table giving each sequence's pages (the paged entry points below); slot x of
  *         the pool is key x % 64 of page x / 64.
+ *   - FP8 rows (key_format = INDEXER_KEY_FP8; the attention.py page's FP8 indexer cache,
+ *     "128 fp8 + 4 fp32 scale" = 132 bytes, scale_fmt ue8m0, block 128): 128 e4m3 codes
+ *     (element i in byte i) then an f32 scale 2^e, e the power-of-two ceiling of
+ *     amax / 448 with amax floored at 448 * 2^-126; codes round x / 2^e to nearest even,
+ *     keeping the sign. Query heads use the same row. FP8 pages hold 64 keys in 8448
+ *     bytes as 8 groups of 1056: the group's 1024 code bytes (key m's byte j at
+ *     (m/8)*1056 + (j/16)*128 + (m%8)*16 + j%16), then its keys' f32 scales at
+ *     (m/8)*1056 + 1024 + (m%8)*4. Every cache and q_rows buffer takes the row and page
+ *     size of dims->key_format; the score is sum_h w' * relu(s_q * s_k * qcodes . kcodes).
  *   - Score buffers that the selection kernels read (scores of indexer_topk and
  *     indexer_select_candidate_blocks, scores_out of the forward calls) are 16-byte
  *     aligned.
@@ -82,6 +91,10 @@ typedef struct CUstream_st* indexer_stream_t;   /* == cudaStream_t */
 #define INDEXER_KEY_ROW_BYTES 68
 #define INDEXER_PAGE_KEYS 64
 #define INDEXER_PAGE_BYTES 4352        /* 64 keys x 68 bytes */
+#define INDEXER_KEY_MXFP4 0
+#define INDEXER_KEY_FP8 1
+#define INDEXER_KEY_ROW_BYTES_FP8 132
+#define INDEXER_PAGE_BYTES_FP8 8448    /* 64 keys x 132 bytes */
 #define INDEXER_STATUS_BYTES 256       /* workspace header holding the status word */
 
 /* Indexer shape and selection parameters ([index-keys] Indexer.__init__). */
@@ -95,6 +108,8 @@ typedef struct IndexerDims {
     int32_t cand_topk_blocks;  /* level one: blocks kept (0: no two-level filter) */
     int32_t cand_block_size;   /* level one: compressed positions per block */
     float norm_eps;            /* k_norm RMSNorm epsilon */
+    int32_t key_format;        /* INDEXER_KEY_MXFP4 (0) or INDEXER_KEY_FP8 (1): the row format of
+                                  keys and quantised queries, see below */
 } IndexerDims;
 
 /* YaRN parameters of the compressed layers ([compress] yarn_freqs_cis). */

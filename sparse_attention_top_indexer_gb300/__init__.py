@@ -16,7 +16,8 @@ import torch
 
 __all__ = [
     "IndexerDims", "IndexerYarn", "IndexerError", "load_library", "KEY_ROW_BYTES", "STATUS_BYTES", "PAGE_KEYS",
-    "PAGE_BYTES", "new_key_cache", "new_key_pool", "indexer_publish_k_paged", "indexer_forward_paged",
+    "PAGE_BYTES", "KEY_MXFP4", "KEY_FP8", "ROW_BYTES_FP8", "PAGE_BYTES_FP8", "row_bytes", "page_bytes",
+    "new_key_cache", "new_key_pool", "indexer_publish_k_paged", "indexer_forward_paged",
     "indexer_workspace_size_paged",
     "indexer_rope_table", "indexer_publish_k", "indexer_prep_q", "indexer_scores",
     "indexer_select_candidate_blocks", "indexer_topk", "indexer_forward", "indexer_workspace_size",
@@ -27,6 +28,9 @@ __all__ = [
 KEY_ROW_BYTES = 68
 PAGE_KEYS = 64
 PAGE_BYTES = PAGE_KEYS * KEY_ROW_BYTES    # 4352
+KEY_MXFP4, KEY_FP8 = 0, 1
+ROW_BYTES_FP8 = 132
+PAGE_BYTES_FP8 = PAGE_KEYS * ROW_BYTES_FP8   # 8448
 STATUS_BYTES = 256
 NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -38,6 +42,7 @@ class IndexerDims(ctypes.Structure):
         ("n_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("rope_dim", ctypes.c_int32),
         ("ratio", ctypes.c_int32), ("index_topk", ctypes.c_int32), ("offset", ctypes.c_int32),
         ("cand_topk_blocks", ctypes.c_int32), ("cand_block_size", ctypes.c_int32), ("norm_eps", ctypes.c_float),
+        ("key_format", ctypes.c_int32),
     ]
 
 
@@ -104,32 +109,44 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 
 def make_dims(n_heads: int, ratio: int, index_topk: int, offset: int = 0, rope_dim: int = 64,
               head_dim: int = 128, cand_topk_blocks: int = 0, cand_block_size: int = 0,
-              norm_eps: float = 1e-6) -> IndexerDims:
+              norm_eps: float = 1e-6, key_format: int = KEY_MXFP4) -> IndexerDims:
     return IndexerDims(n_heads, head_dim, rope_dim, ratio, index_topk, offset, cand_topk_blocks, cand_block_size,
-                       norm_eps)
+                       norm_eps, key_format)
 
 
-def new_key_cache(B: int, T_cap: int, device="cuda") -> torch.Tensor:
-    """A zeroed sequence-major key cache: uint8 [B, T_cap / 64, 4352] (T_cap a multiple of 64)."""
+def row_bytes(key_format: int = KEY_MXFP4) -> int:
+    """Bytes of one quantised key or query-head row: 68 (MXFP4) or 132 (FP8)."""
+    return ROW_BYTES_FP8 if key_format == KEY_FP8 else KEY_ROW_BYTES
+
+
+def page_bytes(key_format: int = KEY_MXFP4) -> int:
+    """Bytes of one 64-key page: 4352 (MXFP4) or 8448 (FP8)."""
+    return PAGE_BYTES_FP8 if key_format == KEY_FP8 else PAGE_BYTES
+
+
+def new_key_cache(B: int, T_cap: int, device="cuda", key_format: int = KEY_MXFP4) -> torch.Tensor:
+    """A zeroed sequence-major key cache: uint8 [B, T_cap / 64, page bytes] (T_cap a multiple of 64)."""
     if T_cap % PAGE_KEYS:
         raise ValueError("T_cap must be a multiple of 64")
-    return torch.zeros((B, T_cap // PAGE_KEYS, PAGE_BYTES), dtype=torch.uint8, device=device)
+    return torch.zeros((B, T_cap // PAGE_KEYS, page_bytes(key_format)), dtype=torch.uint8, device=device)
 
 
-def new_key_pool(num_pages: int, device="cuda") -> torch.Tensor:
-    """A zeroed page pool: uint8 [num_pages, 4352], 64 keys per page."""
-    return torch.zeros((num_pages, PAGE_BYTES), dtype=torch.uint8, device=device)
+def new_key_pool(num_pages: int, device="cuda", key_format: int = KEY_MXFP4) -> torch.Tensor:
+    """A zeroed page pool: uint8 [num_pages, page bytes], 64 keys per page."""
+    return torch.zeros((num_pages, page_bytes(key_format)), dtype=torch.uint8, device=device)
 
 
-def _cache_tcap(k_cache: torch.Tensor) -> int:
-    if k_cache.dim() != 3 or k_cache.shape[2] != PAGE_BYTES:
-        raise ValueError("k_cache must be the sequence-major uint8 [B, T_cap / 64, 4352] cache")
+def _cache_tcap(k_cache: torch.Tensor, dims: Optional[IndexerDims] = None) -> int:
+    pb = page_bytes(dims.key_format) if dims is not None else k_cache.shape[-1]
+    if k_cache.dim() != 3 or k_cache.shape[2] != pb or pb not in (PAGE_BYTES, PAGE_BYTES_FP8):
+        raise ValueError(f"k_cache must be the sequence-major uint8 [B, T_cap / 64, {pb}] cache of the dims' format")
     return k_cache.shape[1] * PAGE_KEYS
 
 
-def _pool_pages(k_pool: torch.Tensor) -> int:
-    if k_pool.dim() != 2 or k_pool.shape[1] != PAGE_BYTES:
-        raise ValueError("k_pool must be the uint8 [num_pages, 4352] page pool")
+def _pool_pages(k_pool: torch.Tensor, dims: Optional[IndexerDims] = None) -> int:
+    pb = page_bytes(dims.key_format) if dims is not None else k_pool.shape[-1]
+    if k_pool.dim() != 2 or k_pool.shape[1] != pb or pb not in (PAGE_BYTES, PAGE_BYTES_FP8):
+        raise ValueError(f"k_pool must be the uint8 [num_pages, {pb}] page pool of the dims' format")
     return k_pool.shape[0]
 
 
@@ -172,7 +189,7 @@ def indexer_publish_k(dims: IndexerDims, latent: torch.Tensor, wk: torch.Tensor,
                       rope_cs: torch.Tensor, start_pos: int, k_cache: torch.Tensor, stream=None):
     """latent bf16 [B, G, Din]; wk bf16 [128, Din]; k_norm_w bf16 [128]; k_cache uint8 [B, T_cap/64, 4352]."""
     B, G, Din = latent.shape
-    T_cap = _cache_tcap(k_cache)
+    T_cap = _cache_tcap(k_cache, dims)
     if k_cache.shape[0] != B:
         raise ValueError("k_cache batch differs from latent")
     _check(load_library().indexer_publish_k(
@@ -198,7 +215,7 @@ def indexer_scores(dims: IndexerDims, q_rows: torch.Tensor, w_prime: torch.Tenso
     B, S = q_rows.shape[:2]
     _check(load_library().indexer_scores(
         ctypes.byref(dims), _ptr(q_rows, torch.uint8, "q_rows"), _ptr(w_prime, torch.float32, "w_prime"), B, S,
-        start_pos, _ptr(k_cache, torch.uint8, "k_cache"), _cache_tcap(k_cache),
+        start_pos, _ptr(k_cache, torch.uint8, "k_cache"), _cache_tcap(k_cache, dims),
         _ptr(cand_blocks, torch.int32, "cand_blocks"), _ptr(scores, torch.float32, "scores"),
         _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
 
@@ -242,7 +259,7 @@ def indexer_forward(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor, start_p
     _check(load_library().indexer_forward(
         ctypes.byref(dims), _ptr(q, torch.bfloat16, "q"), _ptr(w, torch.bfloat16, "w"), B, S, start_pos,
         _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(k_cache, torch.uint8, "k_cache"),
-        _cache_tcap(k_cache), _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
+        _cache_tcap(k_cache, dims), _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
         _ptr(topk_out, torch.int32, "topk_out"), _ptr(scores_out, torch.float32, "scores_out"),
         _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
 
@@ -260,7 +277,7 @@ def indexer_forward_noalloc(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor,
     _check(load_library().indexer_forward_noalloc(
         ctypes.byref(dims), _ptr(q, torch.bfloat16, "q"), _ptr(w, torch.bfloat16, "w"), B, S, start_pos,
         _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(k_cache, torch.uint8, "k_cache"),
-        _cache_tcap(k_cache), _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
+        _cache_tcap(k_cache, dims), _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
         _ptr(topk_out, torch.int32, "topk_out"), _ptr(scores_out, torch.float32, "scores_out"), _stream(stream)))
 
 
@@ -277,7 +294,7 @@ def indexer_publish_k_paged(dims: IndexerDims, latent: torch.Tensor, wk: torch.T
         ctypes.byref(dims), _ptr(latent, torch.bfloat16, "latent"), N, Din, _ptr(wk, torch.bfloat16, "wk"),
         _ptr(k_norm_w, torch.bfloat16, "k_norm_w"), _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0],
         _ptr(positions, torch.int32, "positions"), _ptr(slot_mapping, torch.int32, "slot_mapping"),
-        _ptr(k_pool, torch.uint8, "k_pool"), _pool_pages(k_pool), _ptr(ws, None, "ws"),
+        _ptr(k_pool, torch.uint8, "k_pool"), _pool_pages(k_pool, dims), _ptr(ws, None, "ws"),
         ws.numel() * ws.element_size(), _stream(stream)))
 
 
@@ -302,7 +319,7 @@ def indexer_forward_paged(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor, s
         ctypes.byref(dims), _ptr(q, torch.bfloat16, "q"), _ptr(w, torch.bfloat16, "w"), Q, n_seq,
         _ptr(seq_pos, torch.int32, "seq_pos"), _ptr(q_start, torch.int32, "q_start"), T_max,
         _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(k_pool, torch.uint8, "k_pool"),
-        _pool_pages(k_pool), _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
+        _pool_pages(k_pool, dims), _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
         _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
         _ptr(topk_out, torch.int32, "topk_out"), _ptr(scores_out, torch.float32, "scores_out"),
         _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))

@@ -29,6 +29,22 @@ __host__ __device__ __forceinline__ int page_code_offset(int m, int j) {
 // byte i).
 __host__ __device__ __forceinline__ int page_scale_offset(int m) { return (m >> 3) * kGroupBytes + 512 + (m & 7) * 4; }
 
+// FP8 rows (the FP8 indexer cache of the attention.py page: 128 fp8 values + a 4-byte
+// f32 scale = 132 bytes): 128 e4m3 codes (element i in byte i), then the f32 scale, a
+// power of two. FP8 pages hold 64 keys as 8 groups of 1056 bytes: the group's 1024 code
+// bytes in the same core-matrix order (8 core matrices of 128 bytes along K), then its
+// keys' f32 scales; two pages side by side are again one 128-row MMA operand.
+constexpr int kRowBytesFp8 = 132;
+constexpr int kCodeBytesFp8 = 128;
+constexpr int kGroupBytesFp8 = 1056;
+constexpr int kPageBytesFp8 = kPageKeys * kRowBytesFp8;   // 8448 = 8 groups of 1056 bytes
+__host__ __device__ __forceinline__ int page_code_offset_fp8(int m, int j) {
+  return (m >> 3) * kGroupBytesFp8 + (j >> 4) * 128 + (m & 7) * 16 + (j & 15);
+}
+__host__ __device__ __forceinline__ int page_scale_offset_fp8(int m) {
+  return (m >> 3) * kGroupBytesFp8 + 1024 + (m & 7) * 4;
+}
+
 // Status bits OR-ed into the workspace status word by kernels whose bounded waits ran out.
 constexpr uint32_t kStatusLoadTimeout = 1u;
 constexpr uint32_t kStatusMmaTimeout = 2u;
@@ -104,6 +120,27 @@ __device__ __forceinline__ int e8m0_exponent(uint32_t amax_bits) {
 
 // 2^-e as an f32 (e in [-126, 126], so the result is a normal number).
 __device__ __forceinline__ float pow2_neg(int e) { return __uint_as_float((uint32_t)(127 - e) << 23); }
+
+// FP8 rows: smallest e with 448 * 2^e >= max(amax, 448 * 2^-126), from the bf16 bits of
+// amax (sign cleared). 448 = 1.75 * 2^8, so with amax = (1 + m/128) * 2^E, e = E - 8
+// when 1 + m/128 <= 1.75 (m <= 96), else E - 7; 0x04E0 is the bf16 pattern of the floor.
+__device__ __forceinline__ int fp8_exponent(uint32_t amax_bits) {
+  const uint32_t a = amax_bits < 0x04E0u ? 0x04E0u : amax_bits;
+  const int E = (int)(a >> 7) - 127;
+  return E - ((a & 0x7Fu) <= 96u ? 8 : 7);
+}
+__device__ __forceinline__ float pow2(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// Two e4m3 codes: x0 -> low byte, x1 -> high byte; round to nearest even (hardware
+// conversion; the scaled values never exceed 448, so nothing saturates); the sign bits
+// are forced to the signs of the inputs so that negative values rounding to zero keep it.
+__device__ __forceinline__ uint32_t e4m3x2(float x0, float x1) {
+  uint32_t r;
+  asm("{ .reg .b16 t; cvt.rn.satfinite.e4m3x2.f32 t, %1, %2; cvt.u32.u16 %0, t; }" : "=r"(r) : "f"(x1), "f"(x0));
+  r |= (__float_as_uint(x0) >> 24) & 0x80u;
+  r |= (__float_as_uint(x1) >> 16) & 0x8000u;
+  return r;
+}
 
 // Two e2m1 codes in one byte: x0 -> low nibble, x1 -> high nibble; round to nearest
 // even on the e2m1 grid (hardware conversion); the sign bits are forced to the signs
@@ -184,6 +221,42 @@ __device__ __forceinline__ uint32_t quant_q_slice(uint4 raw, int j, const float2
   for (int k = 0; k < 4; ++k) word |= e2m1x2(__fmul_rn(x[2 * k], sc), __fmul_rn(x[2 * k + 1], sc)) << (8 * k);
   *e = ex;
   return word;
+}
+
+// FP8 query slice: the same RoPE as quant_q_slice, then the row's 128-value amax over the
+// 16 lanes of the group, the power-of-two scale and eight e4m3 codes (returned as two
+// words, element j*8 in the lowest byte); *e receives the scale exponent.
+__device__ __forceinline__ uint2 quant_q_slice_fp8(uint4 raw, int j, const float2 (&c)[4], int rope_dim,
+                                                   unsigned gmask, int* e) {
+  const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
+  float x[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    x[2 * k] = bf16_to_f32(wds[k] & 0xFFFFu);
+    x[2 * k + 1] = bf16_to_f32(wds[k] >> 16);
+  }
+  const int rstart = kHeadDim - rope_dim;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int e0 = j * 8 + 2 * k;
+    if (e0 >= rstart) {
+      const float x0 = x[2 * k], x1 = x[2 * k + 1];
+      x[2 * k] = bf16_to_f32(f32_to_bf16_rne(__fsub_rn(__fmul_rn(x0, c[k].x), __fmul_rn(x1, c[k].y))));
+      x[2 * k + 1] = bf16_to_f32(f32_to_bf16_rne(__fadd_rn(__fmul_rn(x0, c[k].y), __fmul_rn(x1, c[k].x))));
+    }
+  }
+  uint32_t amax = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) amax = max(amax, (__float_as_uint(x[k]) >> 16) & 0x7FFFu);
+#pragma unroll
+  for (int off = 1; off < 16; off <<= 1) amax = max(amax, __shfl_xor_sync(gmask, amax, off));
+  const int ex = fp8_exponent(amax);
+  const float sc = pow2(-ex);
+  uint2 out;
+  out.x = e4m3x2(__fmul_rn(x[0], sc), __fmul_rn(x[1], sc)) | (e4m3x2(__fmul_rn(x[2], sc), __fmul_rn(x[3], sc)) << 16);
+  out.y = e4m3x2(__fmul_rn(x[4], sc), __fmul_rn(x[5], sc)) | (e4m3x2(__fmul_rn(x[6], sc), __fmul_rn(x[7], sc)) << 16);
+  *e = ex;
+  return out;
 }
 
 // ----------------------------------------------------------------------------- launch overlap
@@ -281,6 +354,21 @@ __host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N) {
 // kernel keeps L2 coherent, so it may be issued before pdl_wait().
 __device__ __forceinline__ void prefetch_l2_bulk(const void* gptr, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gptr), "r"(bytes) : "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, both e4m3 (kind::f8f6f4, K = 32 per instruction).
+__device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p; }"
+      ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Instruction descriptor of kind::f8f6f4: f32 accumulator (bits 4-5 = 1), A and B e4m3
+// (bits 7-9 and 10-12 = 0), both K-major, N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+__host__ __device__ constexpr uint32_t idesc_f8(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // Shared-memory matrix descriptor, no swizzle, K-major: core matrices of 8 rows x 16 bytes

@@ -73,8 +73,16 @@ int check_dims(const IndexerDims* d) {
   if (d->index_topk < 1) return fail(INDEXER_ERR_DIMS, "index_topk must be >= 1 (got %d)", d->index_topk);
   if (!(d->norm_eps >= 0.0f) || !std::isfinite(d->norm_eps))
     return fail(INDEXER_ERR_DIMS, "norm_eps must be finite and >= 0");
+  if (d->key_format != INDEXER_KEY_MXFP4 && d->key_format != INDEXER_KEY_FP8)
+    return fail(INDEXER_ERR_DIMS, "key_format must be INDEXER_KEY_MXFP4 or INDEXER_KEY_FP8 (got %d)", d->key_format);
   return INDEXER_OK;
 }
+
+// Bytes of one quantised row / one 64-key page in the dims' key format.
+size_t row_bytes(const IndexerDims* d) {
+  return d->key_format == INDEXER_KEY_FP8 ? INDEXER_KEY_ROW_BYTES_FP8 : INDEXER_KEY_ROW_BYTES;
+}
+bool is_fp8(const IndexerDims* d) { return d->key_format == INDEXER_KEY_FP8; }
 
 int check_cand_dims(const IndexerDims* d, int T) {
   if (d->cand_topk_blocks < 1 || d->cand_block_size < 1)
@@ -102,7 +110,7 @@ WsLayout ws_layout(const IndexerDims* d, int B, int S, int start_pos) {
   const size_t nvec = (size_t)B * S * d->n_heads;
   const size_t T = (size_t)((start_pos + S) / d->ratio);
   l.q_rows = INDEXER_STATUS_BYTES;
-  l.w_prime = l.q_rows + round_up(nvec * INDEXER_KEY_ROW_BYTES, 256);
+  l.w_prime = l.q_rows + round_up(nvec * row_bytes(d), 256);
   l.scores = l.w_prime + round_up(nvec * sizeof(float), 256);
   l.total = l.scores + round_up((size_t)B * S * T * sizeof(float), 256);
   return l;
@@ -121,7 +129,7 @@ PagedWsLayout paged_ws_layout(const IndexerDims* d, int Q, int n_seq, int T_max)
   const long long g = ((long long)Q + l.qg - 1) / l.qg + n_seq;
   l.n_groups = (int)(g < Q ? g : Q);
   l.q_rows = INDEXER_STATUS_BYTES;
-  l.w_prime = l.q_rows + round_up(nvec * INDEXER_KEY_ROW_BYTES, 256);
+  l.w_prime = l.q_rows + round_up(nvec * row_bytes(d), 256);
   l.scores = l.w_prime + round_up(nvec * sizeof(float), 256);
   l.rows = l.scores + round_up((size_t)Q * T_max * sizeof(float), 256);
   l.groups = l.rows + round_up((size_t)Q * sizeof(RowInfo), 256);
@@ -149,7 +157,7 @@ extern "C" {
 
 const char* indexer_last_error(void) { return g_last_error.c_str(); }
 
-int indexer_abi_version(void) { return 300; }
+int indexer_abi_version(void) { return 400; }
 
 // ---------------------------------------------------------------------------- RoPE table
 int indexer_rope_table(const IndexerYarn* y, int rope_dim, int max_pos, float* table, indexer_stream_t stream) {
@@ -241,6 +249,7 @@ int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B
   a.Din = Din;
   a.rope_dim = dims->rope_dim;
   a.T_cap = T_cap;
+  a.fp8 = is_fp8(dims) ? 1 : 0;
   a.eps = dims->norm_eps;
   const cudaError_t e = launch_publish(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "publish launch");
@@ -262,6 +271,7 @@ static int prep_q_checked(const IndexerDims* dims, const indexer_bf16* q, const 
   a.S = S;
   a.H = dims->n_heads;
   a.h_shift = __builtin_ctz((unsigned)dims->n_heads);
+  a.fp8 = is_fp8(dims) ? 1 : 0;
   a.rope_dim = dims->rope_dim;
   a.start_pos = start_pos;
   a.w_scale = (float)(1.0 / std::sqrt((double)dims->head_dim) / std::sqrt((double)dims->n_heads));
@@ -336,6 +346,7 @@ int indexer_scores(const IndexerDims* dims, const uint8_t* q_rows, const float* 
   a.cbk = dims->cand_topk_blocks;
   a.cbs = dims->cand_block_size > 0 ? dims->cand_block_size : 1;
   a.fill_masked = 1;
+  a.fp8 = is_fp8(dims) ? 1 : 0;
   const cudaError_t e = launch_scores(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "scores launch");
   return ok();
@@ -458,6 +469,7 @@ int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexe
     a.cbk = dims->cand_topk_blocks;
     a.cbs = dims->cand_block_size > 0 ? dims->cand_block_size : 1;
     a.fill_masked = scores_out ? 1 : 0;
+    a.fp8 = is_fp8(dims) ? 1 : 0;
     const cudaError_t e = launch_scores(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "scores launch");
     if (cand_out) {
@@ -516,6 +528,7 @@ int indexer_publish_k_paged(const IndexerDims* dims, const indexer_bf16* latent,
   a.positions = positions;
   a.num_pages = num_pages;
   a.max_pos = max_pos;
+  a.fp8 = is_fp8(dims) ? 1 : 0;
   a.eps = dims->norm_eps;
   const cudaError_t e = launch_publish(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "publish launch");
@@ -601,6 +614,7 @@ int indexer_forward_paged(const IndexerDims* dims, const indexer_bf16* q, const 
     a.S = 1;
     a.H = dims->n_heads;
     a.h_shift = __builtin_ctz((unsigned)dims->n_heads);
+    a.fp8 = is_fp8(dims) ? 1 : 0;
     a.rope_dim = dims->rope_dim;
     a.w_scale = (float)(1.0 / std::sqrt((double)dims->head_dim) / std::sqrt((double)dims->n_heads));
     const cudaError_t e = launch_prep_q(a, st);
@@ -633,6 +647,7 @@ int indexer_forward_paged(const IndexerDims* dims, const indexer_bf16* q, const 
     a.cbk = dims->cand_topk_blocks;
     a.cbs = dims->cand_block_size > 0 ? dims->cand_block_size : 1;
     a.fill_masked = scores_out ? 1 : 0;
+    a.fp8 = is_fp8(dims) ? 1 : 0;
     const cudaError_t e = launch_scores(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "scores launch");
   }

@@ -37,7 +37,18 @@ namespace indexer {
 namespace {
 
 constexpr int kTileKeys = 2 * kPageKeys;             // one MMA M-tile: two 64-key pages side by side
-constexpr int kStageStride = 9216;                   // two pages (8704 B) padded to a 1 KB multiple
+// Key formats: MXFP4 rows (68 bytes; block-scaled MMA, scales in tensor memory) and FP8
+// rows (132 bytes; e4m3 MMA, the per-row scales multiply in the epilogue).
+struct FmtMxfp4 {
+  static constexpr bool kFp8 = false;
+  static constexpr int kCode = kCodeBytes, kRow = kRowBytes, kPage = kPageBytes, kGroup = kGroupBytes;
+  static constexpr int kStage = 9216;    // two pages (8704 B) padded to a 1 KB multiple
+};
+struct FmtFp8 {
+  static constexpr bool kFp8 = true;
+  static constexpr int kCode = kCodeBytesFp8, kRow = kRowBytesFp8, kPage = kPageBytesFp8, kGroup = kGroupBytesFp8;
+  static constexpr int kStage = 17408;   // two pages (16896 B) padded to a 1 KB multiple
+};
 constexpr int kEpiThreads = 128;                     // one epilogue warpgroup
 constexpr int kMaxPages = 32768 / kPageKeys;         // pages of the longest row a sparse launch takes
 constexpr int kMaxTilesCta = 256;                    // tiles one CTA takes at most
@@ -54,8 +65,14 @@ __host__ __device__ constexpr int max_acc(int NP, int SB, int budget) {
        : 2 * (NP + 8) + 2 * SB <= budget ? 2 : 1 * (NP + 8) + 2 * SB <= budget ? 1 : 0;
 }
 
+// FP8 accumulators: at most 4; N <= 64 keeps them within 256 columns (two CTAs per SM),
+// larger N takes the 512 columns of one CTA per SM (its epilogue reads 128 columns at once)
+__host__ __device__ constexpr int acc_f8(int NP) {
+  return NP <= 64 ? (256 / NP < 4 ? 256 / NP : 4) : (512 / NP < 4 ? 512 / NP : 4);
+}
+
 // EPI epilogue warpgroups (warps 4 .. 4*EPI+3) take alternate pages.
-template <int H, int QG, int EPI>
+template <int H, int QG, int EPI, class F>
 struct ScoreCfg {
   static constexpr int THREADS = 128 * (1 + EPI);
   static constexpr int N = QG * H;
@@ -65,16 +82,17 @@ struct ScoreCfg {
   // tensor memory: NACC accumulators of NP columns, NACC A scale sets of 8 columns, two
   // halves of SB B scale columns; every scale address is a multiple of 4 columns. Two or
   // more accumulators within 256 columns let two CTAs share an SM.
-  static constexpr int NSTAGE = 8;
-  static constexpr int NACC = max_acc(NP, SB, 256) >= 2 ? max_acc(NP, SB, 256) : max_acc(NP, SB, 512);
+  static constexpr int NSTAGE = F::kFp8 ? 5 : 8;
+  static constexpr int NACC = F::kFp8 ? acc_f8(NP)
+                                      : max_acc(NP, SB, 256) >= 2 ? max_acc(NP, SB, 256) : max_acc(NP, SB, 512);
   static constexpr int SFA_COL = NACC * NP;
   static constexpr int SFB_COL = SFA_COL + 8 * NACC;
-  static constexpr int TMEM_NEED = SFB_COL + 2 * SB;
+  static constexpr int TMEM_NEED = F::kFp8 ? NACC * NP : SFB_COL + 2 * SB;
   static constexpr uint32_t TMEM_COLS = pow2_cols(TMEM_NEED);
   static constexpr int OFF_QB = 0;
-  static constexpr int OFF_STG = round_up(NP * kCodeBytes, 1024);
-  static constexpr int OFF_QSTG = OFF_STG + NSTAGE * kStageStride;          // raw query rows
-  static constexpr int OFF_W = OFF_QSTG + round_up(N * kRowBytes, 16);
+  static constexpr int OFF_STG = round_up(NP * F::kCode, 1024);
+  static constexpr int OFF_QSTG = OFF_STG + NSTAGE * F::kStage;             // raw query rows
+  static constexpr int OFF_W = OFF_QSTG + round_up(N * F::kRow, 16);
   static constexpr int OFF_SFW = OFF_W + round_up(N * 4, 16);
   static constexpr int NBAR = NSTAGE + 2 * NACC + 1;                          // full, done, empty, q
   static constexpr int OFF_BAR = round_up(OFF_SFW + NCB * 32 * 4, 8);
@@ -100,15 +118,63 @@ __device__ __forceinline__ int pool_page(const ScoreArgs& a, int b, int lp) {
 
 // Requests the two pages of a tile into a stage (a missing half is not copied; its keys
 // are never stored); adjacent pool pages come in one copy.
+template <class F>
 __device__ __forceinline__ void issue_tile_load(const ScoreArgs& a, int p0, int p1, uint32_t stage_addr,
                                                 uint32_t bar) {
-  mbar_arrive_expect_tx(bar, (uint32_t)((p0 >= 0 ? kPageBytes : 0) + (p1 >= 0 ? kPageBytes : 0)));
+  constexpr int PB = F::kPage;
+  mbar_arrive_expect_tx(bar, (uint32_t)((p0 >= 0 ? PB : 0) + (p1 >= 0 ? PB : 0)));
   if (p0 >= 0 && p1 == p0 + 1) {
-    bulk_g2s(stage_addr, a.k_pool + (size_t)p0 * kPageBytes, (uint32_t)(2 * kPageBytes), bar);
+    bulk_g2s(stage_addr, a.k_pool + (size_t)p0 * PB, (uint32_t)(2 * PB), bar);
     return;
   }
-  if (p0 >= 0) bulk_g2s(stage_addr, a.k_pool + (size_t)p0 * kPageBytes, (uint32_t)kPageBytes, bar);
-  if (p1 >= 0) bulk_g2s(stage_addr + kPageBytes, a.k_pool + (size_t)p1 * kPageBytes, (uint32_t)kPageBytes, bar);
+  if (p0 >= 0) bulk_g2s(stage_addr, a.k_pool + (size_t)p0 * PB, (uint32_t)PB, bar);
+  if (p1 >= 0) bulk_g2s(stage_addr + PB, a.k_pool + (size_t)p1 * PB, (uint32_t)PB, bar);
+}
+
+// The query rows of a group -> the MMA's B operand (core-matrix order: 8-row groups of
+// 8 * code bytes, 16-byte core-matrix rows 128 bytes apart along K) and, for MXFP4, each
+// row's scale word into sfw (rows past nrows are zero, their scales 2^0).
+template <class F, int NCB32, int NP>
+__device__ __forceinline__ void build_b_operand(const uint8_t* qstg, uint8_t* qB, uint32_t* sfw, int nrows,
+                                                int tid) {
+  for (int n = tid; n < NCB32; n += 128) {
+    uint32_t w[F::kCode / 4];
+    uint32_t sc = 0x7F7F7F7Fu;
+    if (n < nrows) {
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(qstg + n * F::kRow);
+#pragma unroll
+      for (int i = 0; i < F::kCode / 4; ++i) w[i] = src[i];
+      if (!F::kFp8) sc = src[F::kCode / 4];
+    } else {
+#pragma unroll
+      for (int i = 0; i < F::kCode / 4; ++i) w[i] = 0u;
+    }
+    if (n < NP) {
+#pragma unroll
+      for (int c = 0; c < F::kCode / 16; ++c)
+        *reinterpret_cast<uint4*>(qB + (n >> 3) * (8 * F::kCode) + c * 128 + (n & 7) * 16) =
+            make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    }
+    if (!F::kFp8) sfw[n] = sc;
+  }
+}
+
+// One tile's MMAs: MXFP4 -- two block-scaled MMAs of K = 64; FP8 -- four e4m3 MMAs of K = 32.
+template <class F, int NP>
+__device__ __forceinline__ void issue_tile_mma(uint32_t acc, uint32_t pa, uint32_t qb, uint32_t sfa, uint32_t sfb,
+                                               int SB) {
+  if constexpr (F::kFp8) {
+    const uint32_t idesc = idesc_f8(128, NP);
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      mma_f8(acc, smem_desc(pa + 256 * k, 128, F::kGroup), smem_desc(qb + 256 * k, 128, 8 * F::kCode), idesc,
+             k > 0 ? 1u : 0u);
+  } else {
+    const uint32_t idesc = idesc_mxf4(128, NP);
+    mma_mxf4(acc, smem_desc(pa, 128, F::kGroup), smem_desc(qb, 128, 8 * F::kCode), idesc, sfa, sfb, 0u);
+    mma_mxf4(acc, smem_desc(pa + 256, 128, F::kGroup), smem_desc(qb + 256, 128, 8 * F::kCode), idesc, sfa + 4,
+             sfb + SB, 1u);
+  }
 }
 
 // Lane 0 waits (bounded) for the phase; the warp follows it. Warp-uniform result.
@@ -120,10 +186,12 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return ok != 0u;
 }
 
-template <int H, int QG, int EPI>
-__global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG, EPI>::TMEM_COLS <= 256 ? 2 : 1)
+template <int H, int QG, int EPI, class F>
+__global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
+                                  ScoreCfg<H, QG, EPI, F>::TMEM_COLS <= 256 && ScoreCfg<H, QG, EPI, F>::THREADS <= 256
+                                      ? 2 : 1)
     score_kernel(const ScoreArgs a) {
-  using C = ScoreCfg<H, QG, EPI>;
+  using C = ScoreCfg<H, QG, EPI, F>;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);   // 1024-byte aligned base
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -210,7 +278,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
     // while they run (a hint; the copies below read after pdl_wait)
     for (int i = tile0 + lane; i < tile_vis; i += 32) {
       const int lp = 2 * i, n = min(2, npages - lp);
-      prefetch_l2_bulk(a.k_pool + ((size_t)b * a.pages_per_seq + lp) * kPageBytes, (uint32_t)(n * kPageBytes));
+      prefetch_l2_bulk(a.k_pool + ((size_t)b * a.pages_per_seq + lp) * F::kPage, (uint32_t)(n * F::kPage));
     }
   }
   pdl_wait();   // the query rows, weights and pages of the kernels before are complete
@@ -268,9 +336,9 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
     }
     __syncwarp();
     if (lane == 0) {
-      const uint32_t qbytes = (uint32_t)(nq * H * kRowBytes), wbytes = (uint32_t)(nq * H * 4);
+      const uint32_t qbytes = (uint32_t)(nq * H * F::kRow), wbytes = (uint32_t)(nq * H * 4);
       mbar_arrive_expect_tx(bar_q, qbytes + wbytes);
-      bulk_g2s(smem_u32(qstg), a.q_rows + qrow0 * kRowBytes, qbytes, bar_q);
+      bulk_g2s(smem_u32(qstg), a.q_rows + qrow0 * F::kRow, qbytes, bar_q);
       bulk_g2s(smem_u32(wq), a.w_prime + qrow0, wbytes, bar_q);
       info[1] = (uint32_t)first;
       info[2] = 0u;
@@ -278,7 +346,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
     __syncwarp();
     if (lane < first) {
       const int2 p = fill_ptab(lane);
-      issue_tile_load(a, max(p.x, -1), max(p.y, -1), stg0 + lane * kStageStride, bar_full(lane));
+      issue_tile_load<F>(a, max(p.x, -1), max(p.y, -1), stg0 + lane * F::kStage, bar_full(lane));
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -299,36 +367,18 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
     // query rows -> B operand (core-matrix order) and B scales
     failed = !named_bar_and(1, 128, warp_wait(bar_q, 0u));
     if (!failed) {
-      for (int n = tid; n < C::NCB * 32; n += 128) {
-        uint32_t w[16];
-        uint32_t sc = 0x7F7F7F7Fu;
-        if (n < nq * H) {
-          const uint32_t* src = reinterpret_cast<const uint32_t*>(qstg + n * kRowBytes);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = src[i];
-          sc = src[16];
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = 0u;
-        }
-        if (n < C::NP) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(qB + (n >> 3) * 512 + c * 128 + (n & 7) * 16) =
-                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-        }
-        sfw[n] = sc;
-      }
+      build_b_operand<F, C::NCB * 32, C::NP>(qstg, qB, sfw, nq * H, tid);
       fence_proxy_async_smem();   // the B operand was written by ordinary stores
       named_bar_sync(1, 128);
+      if constexpr (!F::kFp8) {
 #pragma unroll
-      for (int j = 0; j < C::NCB; ++j) {
-        const uint32_t wd = sfw[32 * j + lane];
-        tmem_st_x1(tq + C::SFB_COL + j, wd & 0xFFFFu);
-        tmem_st_x1(tq + C::SFB_COL + C::SB + j, wd >> 16);
+        for (int j = 0; j < C::NCB; ++j) {
+          const uint32_t wd = sfw[32 * j + lane];
+          tmem_st_x1(tq + C::SFB_COL + j, wd & 0xFFFFu);
+          tmem_st_x1(tq + C::SFB_COL + C::SB + j, wd >> 16);
+        }
       }
     }
-    const uint32_t idesc = idesc_mxf4(128, C::NP);
     const uint32_t qb = smem_u32(qB);
     const int key = (warp << 5) | lane;   // this thread's key (TMEM lane) within a page
     for (int i = 0; i < nt && !failed; ++i) {
@@ -341,8 +391,8 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
         break;
       }
       tc_fence_after();
-      {
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(stg + st * kStageStride + page_scale_offset(key));
+      if constexpr (!F::kFp8) {   // the tile's A scales
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(stg + st * F::kStage + page_scale_offset(key));
         const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
         tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * c), lo, lo, lo, lo, hi, hi, hi, hi);
       }
@@ -351,12 +401,10 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
       named_bar_sync(1, 128);
       if (tid == 0) {
         tc_fence_after();
-        const uint32_t pa = stg0 + (uint32_t)(st * kStageStride);
+        const uint32_t pa = stg0 + (uint32_t)(st * F::kStage);
         const uint32_t acc = tmem + (uint32_t)(c * C::NP);
         const uint32_t sfa = tmem + (uint32_t)(C::SFA_COL + 8 * c);
-        mma_mxf4(acc, smem_desc(pa, 128, kGroupBytes), smem_desc(qb, 128, 512), idesc, sfa, tmem + C::SFB_COL, 0u);
-        mma_mxf4(acc, smem_desc(pa + 256, 128, kGroupBytes), smem_desc(qb + 256, 128, 512), idesc, sfa + 4,
-                 tmem + C::SFB_COL + C::SB, 1u);
+        issue_tile_mma<F, C::NP>(acc, pa, qb, sfa, tmem + C::SFB_COL, C::SB);
         tc_commit(bar_done(c));
         info[2] = (uint32_t)(i + 1);
       }
@@ -382,13 +430,23 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
     }
     // head weights (rows past S weigh nothing)
     failed = !warp_wait(bar_q, 0u);
-    if (!failed)
+    if (!failed) {
       for (int n = nq * H + ge; n < C::N; n += EPI * kEpiThreads) wq[n] = 0.f;
+      if constexpr (F::kFp8)   // fold each query row's scale into its head weight
+        for (int n = ge; n < nq * H; n += EPI * kEpiThreads)
+          wq[n] *= *reinterpret_cast<const float*>(qstg + n * F::kRow + F::kCode);
+    }
     named_bar_sync(2, EPI * kEpiThreads);
     if (a.fill_masked) fill_masked(ge, EPI * kEpiThreads);
     for (int i = grp; i < nt && !failed; i += EPI) {   // this group's pages
       const int c = i % C::NACC;
-      if (!warp_wait(bar_done(c), (uint32_t)(i / C::NACC) & 1u)) {
+      bool ok = warp_wait(bar_done(c), (uint32_t)(i / C::NACC) & 1u);
+      float sk = 1.f;   // FP8: this key's scale, read before the stage is refilled
+      if constexpr (F::kFp8) {
+        if (ok) sk = *reinterpret_cast<const float*>(stg + (i % C::NSTAGE) * F::kStage + page_scale_offset_fp8(et));
+        ok = named_bar_and(3 + grp, kEpiThreads, ok);   // the warpgroup agrees (and has read its scales)
+      }
+      if (!ok) {
         failed = true;
         break;
       }
@@ -418,7 +476,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
       if (et == 0 && i + C::NSTAGE < nt) {
         // the MMA that read this page's stage has completed: refill it
         const int nx = i + C::NSTAGE;
-        issue_tile_load(a, max(ptab[2 * nx], -1), max(ptab[2 * nx + 1], -1), stg0 + (i % C::NSTAGE) * kStageStride,
+        issue_tile_load<F>(a, max(ptab[2 * nx], -1), max(ptab[2 * nx + 1], -1), stg0 + (i % C::NSTAGE) * F::kStage,
                         bar_full(i % C::NSTAGE));
         atomicMax(&info[1], (uint32_t)(i + C::NSTAGE + 1));
       }
@@ -440,6 +498,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
               const int blk = t / a.cbs;
               keep = keep && ((cand_bits[qi * cand_words + (blk >> 5)] >> (blk & 31)) & 1u);
             }
+            if constexpr (F::kFp8) acc *= sk;
             a.scores[(size_t)(row0 + qi) * a.ld + t] = keep ? acc : -__int_as_float(0x7f800000);
           }
         }
@@ -492,7 +551,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI>::THREADS, ScoreCfg<H, QG,
 //     the accumulator in 64-column halves, release it, form sum_h w' * max(dot, 0) per row
 //     and store; after its last tile of a group every epilogue thread releases the query
 //     buffer of that group.
-template <int H, int QG, int EPI>
+template <int H, int QG, int EPI, class F>
 struct RowsCfg {
   static constexpr int THREADS = 128 * (1 + EPI) + 64;
   static constexpr int MMA_WARP = 4 * (1 + EPI);
@@ -502,23 +561,27 @@ struct RowsCfg {
   static constexpr int NP = round_up(N, 16);
   static constexpr int NCB = (NP + 31) / 32;
   static constexpr int SB = round_up(NCB, 4);
-  static constexpr int NSTAGE = 12;
-  // NACC accumulators with their A scale sets, and two B scale sets (two query buffers)
-  static constexpr int NACC = 3 * (NP + 8) + 4 * SB <= 512 ? 3 : 2 * (NP + 8) + 4 * SB <= 512 ? 2 : 1;
+  static constexpr int NSTAGE = F::kFp8 ? 8 : 12;
+  // NACC accumulators (MXFP4: with their A scale sets, and two B scale sets, one per
+  // query buffer; FP8: no scale sets)
+  static constexpr int NACC = F::kFp8 ? (512 / NP < 4 ? 512 / NP : 4)
+                            : 3 * (NP + 8) + 4 * SB <= 512 ? 3 : 2 * (NP + 8) + 4 * SB <= 512 ? 2 : 1;
   static constexpr int SFA_COL = NACC * NP;
   static constexpr int SFB_COL = SFA_COL + 8 * NACC;   // set q: columns SFB_COL + 2*SB*q ..
-  static constexpr int TMEM_NEED = SFB_COL + 4 * SB;
+  static constexpr int TMEM_NEED = F::kFp8 ? NACC * NP : SFB_COL + 4 * SB;
   static constexpr uint32_t TMEM_COLS = pow2_cols(TMEM_NEED);
-  static constexpr int QB_STRIDE = round_up(NP * kCodeBytes, 1024);
-  static constexpr int QSTG_STRIDE = round_up(N * kRowBytes, 16);
+  static constexpr int QB_STRIDE = round_up(NP * F::kCode, 1024);
+  static constexpr int QSTG_STRIDE = round_up(N * F::kRow, 16);
   static constexpr int W_STRIDE = round_up(N * 4, 16);
   static constexpr int OFF_QB = 0;
   static constexpr int OFF_STG = 2 * QB_STRIDE;
-  static constexpr int OFF_QSTG = OFF_STG + NSTAGE * kStageStride;
+  static constexpr int OFF_QSTG = OFF_STG + NSTAGE * F::kStage;
   static constexpr int OFF_W = OFF_QSTG + 2 * QSTG_STRIDE;
-  static constexpr int OFF_SFW = OFF_W + 2 * W_STRIDE;
+  static constexpr int OFF_WS = OFF_W + 2 * W_STRIDE;                    // FP8: w' times the row's scale
+  static constexpr int OFF_SFW = OFF_WS + (F::kFp8 ? 2 * W_STRIDE : 0);
   static constexpr int OFF_GD = round_up(OFF_SFW + NCB * 32 * 4, 16);   // two group descriptors
-  static constexpr int NBAR = 2 * NSTAGE + 3 * NACC + 4;   // full, free, done, empty, qfull, qfree, ready
+  // full, free, done, empty, qfull, qfree, ready; FP8: scales read (per stage), scaled w' ready
+  static constexpr int NBAR = 2 * NSTAGE + 3 * NACC + 4 + (F::kFp8 ? NSTAGE + 2 : 0);
   static constexpr int OFF_BAR = OFF_GD + 2 * 32;
   static constexpr int OFF_INFO = OFF_BAR + NBAR * 8;                     // tmem, tiles, mmas, q phases
   static constexpr int SMEM = OFF_INFO + 16;
@@ -528,6 +591,7 @@ struct RowsCfg {
   static_assert(NBAR <= 64, "barriers are initialised by the lanes of two passes of one warp");
   static_assert(QFREE_COUNT < (1 << 20), "mbarrier arrival count");
   static_assert(NSTAGE > NACC, "the epilogue waits on a stage's barrier for its accumulator");
+  static_assert(OFF_GD + 64 + NBAR * 8 + 16 + 1024 <= 227 * 1024, "shared memory budget");
 };
 
 struct GroupDesc {   // one query group, as the producer hands it to the other roles
@@ -535,9 +599,9 @@ struct GroupDesc {   // one query group, as the producer hands it to the other r
   int Tb, nt, ntiles, live;   // keys of the sequence, tiles to score, tiles of the sequence, 0 = no more groups
 };
 
-template <int H, int QG, int EPI>
-__global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_kernel(const ScoreArgs a) {
-  using C = RowsCfg<H, QG, EPI>;
+template <int H, int QG, int EPI, class F>
+__global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows_kernel(const ScoreArgs a) {
+  using C = RowsCfg<H, QG, EPI, F>;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -555,16 +619,23 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
   auto bar_qfull = [&](int q) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + 2 * C::NACC + q); };
   auto bar_qfree = [&](int q) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + 2 * C::NACC + 2 + q); };
   auto bar_ready = [&](int c) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + 2 * C::NACC + 4 + c); };
+  auto bar_sread = [&](int st) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + 3 * C::NACC + 4 + st); };
+  auto bar_wsready = [&](int q) { return bar0 + 8u * (uint32_t)(3 * C::NSTAGE + 3 * C::NACC + 4 + q); };
   if (warp == 0) {
     for (int i = lane; i < C::NBAR; i += 32) {
       const bool empty_bar = i >= 2 * C::NSTAGE + C::NACC && i < 2 * C::NSTAGE + 2 * C::NACC;
       const bool qfree_bar = i >= 2 * C::NSTAGE + 2 * C::NACC + 2 && i < 2 * C::NSTAGE + 2 * C::NACC + 4;
-      const bool ready_bar = i >= 2 * C::NSTAGE + 2 * C::NACC + 4;
+      const bool ready_bar = i >= 2 * C::NSTAGE + 2 * C::NACC + 4 && i < 2 * C::NSTAGE + 3 * C::NACC + 4;
+      const bool sread_bar = i >= 2 * C::NSTAGE + 3 * C::NACC + 4 && i < 3 * C::NSTAGE + 3 * C::NACC + 4;
+      const bool ws_bar = i >= 3 * C::NSTAGE + 3 * C::NACC + 4;
       // a query buffer is released by the scale warpgroup and the MMA warp (once they have
       // read it) and by every epilogue thread (once the group's last accumulator has been
-      // read); an accumulator's scales are ready once the four scale warps have stored them
-      mbar_init(bar0 + 8u * (uint32_t)i, empty_bar || ready_bar ? (uint32_t)kEpiThreads
-                                         : qfree_bar ? (uint32_t)C::QFREE_COUNT : 1u);
+      // read); an accumulator's scales are ready once the four scale warps have stored them;
+      // FP8: a stage's key scales have been read by the epilogue warpgroup of its tile, and
+      // a query buffer's scaled head weights have been written by all epilogue threads
+      mbar_init(bar0 + 8u * (uint32_t)i, empty_bar || ready_bar || sread_bar ? (uint32_t)kEpiThreads
+                                         : qfree_bar ? (uint32_t)C::QFREE_COUNT
+                                         : ws_bar ? (uint32_t)(EPI * kEpiThreads) : 1u);
     }
     fence_mbar_init();
     if (lane == 0) info[1] = info[2] = info[3] = 0u;
@@ -626,9 +697,9 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
       if (lane == 0) {
         gdesc[qb] = d;
         if (d.live) {
-          const uint32_t qbytes = (uint32_t)(d.nq * H * kRowBytes), wbytes = (uint32_t)(d.nq * H * 4);
+          const uint32_t qbytes = (uint32_t)(d.nq * H * F::kRow), wbytes = (uint32_t)(d.nq * H * 4);
           mbar_arrive_expect_tx(bar_qfull(qb), qbytes + wbytes);
-          bulk_g2s(smem_u32(smem + C::OFF_QSTG + qb * C::QSTG_STRIDE), a.q_rows + (size_t)d.row0 * H * kRowBytes,
+          bulk_g2s(smem_u32(smem + C::OFF_QSTG + qb * C::QSTG_STRIDE), a.q_rows + (size_t)d.row0 * H * F::kRow,
                    qbytes, bar_qfull(qb));
           bulk_g2s(smem_u32(smem + C::OFF_W + qb * C::W_STRIDE), a.w_prime + (size_t)d.row0 * H, wbytes,
                    bar_qfull(qb));
@@ -651,13 +722,15 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
         const int n = min(32, d.nt - i0);
         for (int u = 0; u < n; ++u, ++j) {
           const int st = (int)(j % C::NSTAGE);
-          if (j >= (uint32_t)C::NSTAGE && !warp_wait(bar_free(st), ((j / C::NSTAGE) - 1) & 1u)) {
+          // the stage's previous tile: its MMA has completed (FP8: and its key scales were read)
+          if (j >= (uint32_t)C::NSTAGE &&
+              !warp_wait(F::kFp8 ? bar_sread(st) : bar_free(st), ((j / C::NSTAGE) - 1) & 1u)) {
             failed = true;
             break;
           }
           const int q0 = __shfl_sync(0xffffffffu, p0, u), q1 = __shfl_sync(0xffffffffu, p1, u);
           if (lane == 0) {
-            issue_tile_load(a, max(q0, -1), max(q1, -1), stg0 + st * kStageStride, bar_full(st));
+            issue_tile_load<F>(a, max(q0, -1), max(q1, -1), stg0 + st * F::kStage, bar_full(st));
             info[1] = j + 1;
           }
           __syncwarp();
@@ -687,37 +760,20 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
       // query rows -> B operand buffer qb (core-matrix order) and B scale set qb
       uint8_t* qB = smem + C::OFF_QB + qb * C::QB_STRIDE;
       const uint8_t* qstg = smem + C::OFF_QSTG + qb * C::QSTG_STRIDE;
-      for (int n = tid; n < C::NCB * 32; n += 128) {
-        uint32_t w[16];
-        uint32_t sc = 0x7F7F7F7Fu;
-        if (n < d.nq * H) {
-          const uint32_t* src = reinterpret_cast<const uint32_t*>(qstg + n * kRowBytes);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = src[i];
-          sc = src[16];
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = 0u;
-        }
-        if (n < C::NP) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            *reinterpret_cast<uint4*>(qB + (n >> 3) * 512 + c * 128 + (n & 7) * 16) =
-                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-        }
-        sfw[n] = sc;
-      }
+      build_b_operand<F, C::NCB * 32, C::NP>(qstg, qB, sfw, d.nq * H, tid);
       fence_proxy_async_smem();   // the B operand was written by ordinary stores
       named_bar_sync(1, 128);
       // done with the buffer's descriptor and raw rows (the B operand itself stays in use
       // until the group's MMAs complete, which the epilogue's release covers)
       mbar_arrive(bar_qfree(qb));
       const uint32_t sfb = (uint32_t)(C::SFB_COL + qb * 2 * C::SB);
+      if constexpr (!F::kFp8) {
 #pragma unroll
-      for (int jj = 0; jj < C::NCB; ++jj) {
-        const uint32_t wd = sfw[32 * jj + lane];
-        tmem_st_x1(tq + sfb + jj, wd & 0xFFFFu);
-        tmem_st_x1(tq + sfb + C::SB + jj, wd >> 16);
+        for (int jj = 0; jj < C::NCB; ++jj) {
+          const uint32_t wd = sfw[32 * jj + lane];
+          tmem_st_x1(tq + sfb + jj, wd & 0xFFFFu);
+          tmem_st_x1(tq + sfb + C::SB + jj, wd >> 16);
+        }
       }
       for (int i = 0; i < d.nt; ++i, ++j) {
         if (failed) continue;   // no more waits; the next group start reports it
@@ -731,9 +787,11 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
           continue;
         }
         tc_fence_after();
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(stg + st * kStageStride + page_scale_offset(key));
-        const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
-        tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * c), lo, lo, lo, lo, hi, hi, hi, hi);
+        if constexpr (!F::kFp8) {   // the tile's A scales
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(stg + st * F::kStage + page_scale_offset(key));
+          const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
+          tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * c), lo, lo, lo, lo, hi, hi, hi, hi);
+        }
         tmem_wait_st();   // (also the group's B scales, for its first tile)
         tc_fence_before();
         mbar_arrive(bar_ready(c));
@@ -741,7 +799,6 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
     }
   } else if (warp == C::MMA_WARP) {
     // ------------------------------------------------------------ MMA warp
-    const uint32_t idesc = idesc_mxf4(128, C::NP);
     uint32_t j = 0;
     for (int k = 0; !failed; ++k) {
       const int qb = k & 1;
@@ -764,12 +821,10 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
         }
         if (lane == 0) {
           tc_fence_after();
-          const uint32_t pa = stg0 + (uint32_t)(st * kStageStride);
+          const uint32_t pa = stg0 + (uint32_t)(st * F::kStage);
           const uint32_t acc = tmem + (uint32_t)(c * C::NP);
           const uint32_t sfa = tmem + (uint32_t)(C::SFA_COL + 8 * c);
-          mma_mxf4(acc, smem_desc(pa, 128, kGroupBytes), smem_desc(qbaddr, 128, 512), idesc, sfa, tmem + sfb, 0u);
-          mma_mxf4(acc, smem_desc(pa + 256, 128, kGroupBytes), smem_desc(qbaddr + 256, 128, 512), idesc, sfa + 4,
-                   tmem + sfb + C::SB, 1u);
+          issue_tile_mma<F, C::NP>(acc, pa, qbaddr, sfa, tmem + sfb, C::SB);
           tc_commit(bar_free(st));   // the stage may be refilled and the accumulator read
           info[2] = j + 1;
         }
@@ -794,6 +849,20 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
       const GroupDesc d = gdesc[qb];
       if (!d.live) break;
       const float* wq = reinterpret_cast<const float*>(smem + C::OFF_W + qb * C::W_STRIDE);
+      if constexpr (F::kFp8) {
+        // w' times each query row's scale, written by all epilogue threads (bounded wait
+        // on the buffer's barrier before use)
+        float* ws = reinterpret_cast<float*>(smem + C::OFF_WS + qb * C::W_STRIDE);
+        const uint8_t* qstg = smem + C::OFF_QSTG + qb * C::QSTG_STRIDE;
+        for (int n = ge; n < C::N; n += EPI * kEpiThreads)
+          ws[n] = n < d.nq * H ? wq[n] * *reinterpret_cast<const float*>(qstg + n * F::kRow + F::kCode) : 0.f;
+        mbar_arrive(bar_wsready(qb));
+        if (!warp_wait(bar_wsready(qb), (uint32_t)(k >> 1) & 1u)) {
+          failed = true;
+          break;
+        }
+        wq = ws;
+      }
       if (a.fill_masked) {   // -inf over the tiles no row of the group can see
         const int t_begin = d.nt * kTileKeys;
         for (int qi = 0; qi < d.nq; ++qi) {
@@ -810,9 +879,15 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
         const int c = (int)(j % C::NACC);
         // tile j's MMA has completed (its stage's barrier; the stage cannot be refilled and
         // complete again before this accumulator is released, as NSTAGE > NACC)
-        if (!warp_wait(bar_free((int)(j % C::NSTAGE)), (j / C::NSTAGE) & 1u)) {
+        const int st = (int)(j % C::NSTAGE);
+        if (!warp_wait(bar_free(st), (j / C::NSTAGE) & 1u)) {
           failed = true;
           break;
+        }
+        float sk = 1.f;   // FP8: this key's scale; the stage may be refilled once all are read
+        if constexpr (F::kFp8) {
+          sk = *reinterpret_cast<const float*>(stg + st * F::kStage + page_scale_offset_fp8(et));
+          mbar_arrive(bar_sread(st));
         }
         tc_fence_after();
         float part[QG][P];
@@ -848,6 +923,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI>::THREADS, 1) score_rows_ke
               float acc = part[qi][0];
 #pragma unroll
               for (int p = 1; p < P; ++p) acc += part[qi][p];
+              if constexpr (F::kFp8) acc *= sk;
               a.scores[(size_t)(d.row0 + qi) * a.ld + t] = t < visq[qi] ? acc : -__int_as_float(0x7f800000);
             }
           }
@@ -901,9 +977,9 @@ int sm_count() {
   return cached[dev];
 }
 
-template <int H, int QG, int EPI>
+template <int H, int QG, int EPI, class F>
 cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
-  using C = ScoreCfg<H, QG, EPI>;
+  using C = ScoreCfg<H, QG, EPI, F>;
   const int cand_words = a.cand ? ((a.T + a.cbs - 1) / a.cbs + 31) / 32 : 0;
   const size_t smem = (size_t)C::OFF_CAND + (size_t)QG * cand_words * 4 + 1024;   // + base alignment slack
   if (a.sparse_pages && (QG != 1 || (a.groups == nullptr && a.S != 1) || a.cand == nullptr ||
@@ -915,9 +991,9 @@ cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64 || set_bytes[dev] < (int)smem) {
-    err = cudaFuncSetAttribute(score_kernel<H, QG, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    err = cudaFuncSetAttribute(score_kernel<H, QG, EPI, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(score_kernel<H, QG, EPI>, cudaFuncAttributePreferredSharedMemoryCarveout,
+      err = cudaFuncSetAttribute(score_kernel<H, QG, EPI, F>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) set_bytes[dev] = (int)smem;
@@ -951,21 +1027,22 @@ cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
     grid.y = (unsigned)((a.S + QG - 1) / QG);
     grid.z = (unsigned)a.B;
   }
-  return launch_overlapped(score_kernel<H, QG, EPI>, grid, dim3(C::THREADS), smem, stream, a);
+  return launch_overlapped(score_kernel<H, QG, EPI, F>, grid, dim3(C::THREADS), smem, stream, a);
 }
 
-template <int H, int QG, int EPI>
+template <int H, int QG, int EPI, class F>
 cudaError_t launch_rows(ScoreArgs a, cudaStream_t stream) {
-  using C = RowsCfg<H, QG, EPI>;
+  using C = RowsCfg<H, QG, EPI, F>;
   const size_t smem = (size_t)C::SMEM + 1024;   // + base alignment slack
   static int set_bytes[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64 || set_bytes[dev] < (int)smem) {
-    err = cudaFuncSetAttribute(score_rows_kernel<H, QG, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    err = cudaFuncSetAttribute(score_rows_kernel<H, QG, EPI, F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)smem);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(score_rows_kernel<H, QG, EPI>, cudaFuncAttributePreferredSharedMemoryCarveout,
+      err = cudaFuncSetAttribute(score_rows_kernel<H, QG, EPI, F>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) set_bytes[dev] = (int)smem;
@@ -973,37 +1050,43 @@ cudaError_t launch_rows(ScoreArgs a, cudaStream_t stream) {
   const long long groups = a.groups ? (long long)a.n_groups : (long long)((a.S + QG - 1) / QG) * a.B;
   if (groups <= 0) return cudaSuccess;
   const long long ctas = groups < sm_count() ? groups : sm_count();   // one persistent CTA per SM
-  return launch_overlapped(score_rows_kernel<H, QG, EPI>, dim3((unsigned)ctas), dim3(C::THREADS), smem, stream, a);
+  return launch_overlapped(score_rows_kernel<H, QG, EPI, F>, dim3((unsigned)ctas), dim3(C::THREADS), smem, stream,
+                           a);
 }
 
-}  // namespace
-
-cudaError_t launch_scores(const ScoreArgs& a, cudaStream_t stream) {
-  if (a.T <= 0) return cudaSuccess;
+template <class F>
+cudaError_t launch_scores_fmt(const ScoreArgs& a, cudaStream_t stream) {
   // S == 1: one query row per group (a uniform batch of single rows, or row groups planned
   // with score_group_rows(H, true))
   const bool single = a.S == 1;
   if (!single && a.cand == nullptr && a.sched != nullptr) {
     // several rows per group: the persistent kernel (N = 128, two epilogue warpgroups)
     switch (a.H) {
-      case 8: return launch_rows<8, 16, 2>(a, stream);
-      case 16: return launch_rows<16, 8, 2>(a, stream);
-      case 32: return launch_rows<32, 4, 2>(a, stream);
-      case 64: return launch_rows<64, 2, 2>(a, stream);
-      case 128: return launch_rows<128, 1, 2>(a, stream);
+      case 8: return launch_rows<8, 16, 2, F>(a, stream);
+      case 16: return launch_rows<16, 8, 2, F>(a, stream);
+      case 32: return launch_rows<32, 4, 2, F>(a, stream);
+      case 64: return launch_rows<64, 2, 2, F>(a, stream);
+      case 128: return launch_rows<128, 1, 2, F>(a, stream);
       default: return cudaErrorInvalidValue;
     }
   }
   switch (a.H) {
     // decode: one query row, N = H, two CTAs per SM; several rows with a level-two filter:
-    // N = 128 (three accumulators in 512 columns) and two epilogue warpgroups
-    case 8: return single ? launch_cfg<8, 1, 1>(a, stream) : launch_cfg<8, 16, 2>(a, stream);
-    case 16: return single ? launch_cfg<16, 1, 1>(a, stream) : launch_cfg<16, 8, 2>(a, stream);
-    case 32: return single ? launch_cfg<32, 1, 1>(a, stream) : launch_cfg<32, 4, 2>(a, stream);
-    case 64: return single ? launch_cfg<64, 1, 1>(a, stream) : launch_cfg<64, 2, 2>(a, stream);
-    case 128: return single ? launch_cfg<128, 1, 1>(a, stream) : launch_cfg<128, 1, 2>(a, stream);
+    // N = 128 and two epilogue warpgroups
+    case 8: return single ? launch_cfg<8, 1, 1, F>(a, stream) : launch_cfg<8, 16, 2, F>(a, stream);
+    case 16: return single ? launch_cfg<16, 1, 1, F>(a, stream) : launch_cfg<16, 8, 2, F>(a, stream);
+    case 32: return single ? launch_cfg<32, 1, 1, F>(a, stream) : launch_cfg<32, 4, 2, F>(a, stream);
+    case 64: return single ? launch_cfg<64, 1, 1, F>(a, stream) : launch_cfg<64, 2, 2, F>(a, stream);
+    case 128: return single ? launch_cfg<128, 1, 1, F>(a, stream) : launch_cfg<128, 1, 2, F>(a, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+}  // namespace
+
+cudaError_t launch_scores(const ScoreArgs& a, cudaStream_t stream) {
+  if (a.T <= 0) return cudaSuccess;
+  return a.fp8 ? launch_scores_fmt<FmtFp8>(a, stream) : launch_scores_fmt<FmtMxfp4>(a, stream);
 }
 
 int score_group_rows(int H, bool single) {

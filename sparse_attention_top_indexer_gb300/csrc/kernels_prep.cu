@@ -188,14 +188,29 @@ __global__ void __launch_bounds__(kHeadDim * TPO) publish_kernel(PublishArgs a) 
     y = bf16_to_f32(f32_to_bf16_rne(r0));
   }
 
-  // 4. quantise: warp w holds block w, one value per lane
+  // 4. quantise: MXFP4 -- warp w holds block w, one value per lane; FP8 -- one block of
+  //    128 values (amax over the four warps), one e4m3 byte per value
   uint32_t amax = (__float_as_uint(y) >> 16) & 0x7FFFu;
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  const int m = (int)(slot % kPageKeys);
+  if (a.fp8) {
+    __shared__ uint32_t wmax[4];
+    if (lane == 0) wmax[warp] = amax;
+    named_bar_sync(1, kHeadDim);
+    const uint32_t am = max(max(wmax[0], wmax[1]), max(wmax[2], wmax[3]));
+    const int e = fp8_exponent(am);
+    const float yq = __fmul_rn(y, pow2(-e));
+    const float partner = __shfl_down_sync(0xffffffffu, yq, 1);
+    uint8_t* page = a.k_pool + (size_t)(slot / kPageKeys) * kPageBytesFp8;
+    if ((lane & 1) == 0)   // elements tid, tid + 1: two adjacent bytes of one core-matrix row
+      *reinterpret_cast<uint16_t*>(page + page_code_offset_fp8(m, tid)) = (uint16_t)e4m3x2(yq, partner);
+    if (tid == 0) *reinterpret_cast<float*>(page + page_scale_offset_fp8(m)) = pow2(e);
+    return;
+  }
   const int e = e8m0_exponent(amax);
   const float yq = __fmul_rn(y, pow2_neg(e));
   const float partner = __shfl_down_sync(0xffffffffu, yq, 1);
-  const int m = (int)(slot % kPageKeys);
   uint8_t* page = a.k_pool + (size_t)(slot / kPageKeys) * kPageBytes;
   if ((lane & 1) == 0) page[page_code_offset(m, (warp * 32 + lane) >> 1)] = (uint8_t)e2m1x2(yq, partner);
   if (lane == 0) page[page_scale_offset(m) + warp] = (uint8_t)(e + 127);
@@ -235,10 +250,18 @@ __global__ void __launch_bounds__(256) prep_q_kernel(PrepArgs a) {
   float2 c[4];
   load_rope_slice(reinterpret_cast<const float2*>(a.rope_cs) + (size_t)pos * (a.rope_dim / 2), j, a.rope_dim, c);
   int e;
-  const uint32_t word = quant_q_slice(raw, j, c, a.rope_dim, gmask, &e);
-  uint8_t* row = a.q_rows + v * kRowBytes;
-  *reinterpret_cast<uint32_t*>(row + 4 * j) = word;
-  if ((j & 3) == 0) row[kCodeBytes + (j >> 2)] = (uint8_t)(e + 127);
+  if (a.fp8) {
+    const uint2 codes = quant_q_slice_fp8(raw, j, c, a.rope_dim, gmask, &e);
+    uint8_t* row = a.q_rows + v * kRowBytesFp8;   // 132-byte rows: 4-byte aligned only
+    *reinterpret_cast<uint32_t*>(row + 8 * j) = codes.x;
+    *reinterpret_cast<uint32_t*>(row + 8 * j + 4) = codes.y;
+    if (j == 0) *reinterpret_cast<float*>(row + kCodeBytesFp8) = pow2(e);
+  } else {
+    const uint32_t word = quant_q_slice(raw, j, c, a.rope_dim, gmask, &e);
+    uint8_t* row = a.q_rows + v * kRowBytes;
+    *reinterpret_cast<uint32_t*>(row + 4 * j) = word;
+    if ((j & 3) == 0) row[kCodeBytes + (j >> 2)] = (uint8_t)(e + 127);
+  }
   if (j == 0) a.w_prime[v] = bf16_to_f32(a.w[v]) * a.w_scale;
 }
 
@@ -251,7 +274,7 @@ constexpr int kPrepBulkVecs = 64;
 __global__ void __launch_bounds__(256) prep_q_bulk_kernel(PrepArgs a) {
   constexpr int NV = kPrepBulkVecs;
   __shared__ __align__(128) uint16_t sq[NV * kHeadDim];
-  __shared__ __align__(16) uint8_t srow[NV * kRowBytes];
+  __shared__ __align__(16) uint8_t srow[NV * kRowBytesFp8];   // MXFP4 rows use the first NV * 68 bytes
   __shared__ __align__(16) float sw[NV];
   __shared__ __align__(8) uint64_t bar;
   pdl_allow_next();
@@ -293,15 +316,23 @@ __global__ void __launch_bounds__(256) prep_q_bulk_kernel(PrepArgs a) {
       load_rope_slice(reinterpret_cast<const float2*>(a.rope_cs) + (size_t)pos * (a.rope_dim / 2), j, a.rope_dim, c);
       const uint4 raw = *reinterpret_cast<const uint4*>(sq + vi * kHeadDim + j * 8);
       int e;
-      const uint32_t word = quant_q_slice(raw, j, c, a.rope_dim, gmask, &e);
-      *reinterpret_cast<uint32_t*>(srow + vi * kRowBytes + 4 * j) = word;
-      if ((j & 3) == 0) srow[vi * kRowBytes + kCodeBytes + (j >> 2)] = (uint8_t)(e + 127);
+      if (a.fp8) {
+        const uint2 codes = quant_q_slice_fp8(raw, j, c, a.rope_dim, gmask, &e);
+        *reinterpret_cast<uint32_t*>(srow + vi * kRowBytesFp8 + 8 * j) = codes.x;   // 4-byte aligned rows
+        *reinterpret_cast<uint32_t*>(srow + vi * kRowBytesFp8 + 8 * j + 4) = codes.y;
+        if (j == 0) *reinterpret_cast<float*>(srow + vi * kRowBytesFp8 + kCodeBytesFp8) = pow2(e);
+      } else {
+        const uint32_t word = quant_q_slice(raw, j, c, a.rope_dim, gmask, &e);
+        *reinterpret_cast<uint32_t*>(srow + vi * kRowBytes + 4 * j) = word;
+        if ((j & 3) == 0) srow[vi * kRowBytes + kCodeBytes + (j >> 2)] = (uint8_t)(e + 127);
+      }
     }
   }
   if (tid < nv) sw[tid] = bf16_to_f32(wbits) * a.w_scale;
   __syncthreads();
-  uint8_t* dst = a.q_rows + v0 * kRowBytes;   // 16-byte aligned: 64 * 68 is a multiple of 16
-  const int bytes = nv * kRowBytes, whole = bytes & ~15;
+  const int rb = a.fp8 ? kRowBytesFp8 : kRowBytes;
+  uint8_t* dst = a.q_rows + v0 * rb;   // 16-byte aligned: 64 * 68 and 64 * 132 are multiples of 16
+  const int bytes = nv * rb, whole = bytes & ~15;
   for (int o = tid * 16; o < whole; o += 256 * 16)
     *reinterpret_cast<uint4*>(dst + o) = *reinterpret_cast<const uint4*>(srow + o);
   for (int o = whole + tid * 4; o < bytes; o += 256 * 4)

@@ -54,6 +54,7 @@ struct PublishArgs {
   const int32_t* slots = nullptr;
   const int32_t* positions = nullptr;
   int num_pages, max_pos;
+  int fp8;                  // FP8 rows (132 bytes, 8448-byte pages) instead of MXFP4
   float eps;
 };
 cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream);
@@ -94,6 +95,7 @@ struct PrepArgs {
   long long n_vec;          // rows * H
   int S, H, rope_dim, start_pos;
   int h_shift;              // log2(H)
+  int fp8;                  // FP8 rows ([rows][H][132]) instead of MXFP4 ([rows][H][68])
   float w_scale;            // head_dim^-0.5 * H^-0.5
 };
 cudaError_t launch_prep_q(const PrepArgs& a, cudaStream_t stream);
@@ -119,6 +121,7 @@ struct ScoreArgs {
   int sparse_pages;         // one query row per group: score only the pages of its kept
                             // blocks (cand); keys outside them are not written
   int tiles_per_cta;        // set by the launcher
+  int fp8;                  // FP8 key and query rows (132 bytes, 8448-byte pages) instead of MXFP4
 };
 cudaError_t launch_scores(const ScoreArgs& a, cudaStream_t stream);
 // Query rows per score CTA (QG) for n_heads H: 1 for single rows (decode), else 128 / H.

@@ -45,7 +45,7 @@ def dims_of(wl: Workload, **over):
     import sparse_attention_top_indexer_gb300 as X
     kw = dict(n_heads=wl.H, ratio=wl.ratio, index_topk=wl.topk, offset=wl.offset, rope_dim=wl.rope_dim,
               head_dim=wl.D, cand_topk_blocks=wl.cand_topk_blocks, cand_block_size=wl.cand_block_size,
-              norm_eps=wl.norm_eps)
+              norm_eps=wl.norm_eps, key_format=wl.key_format)
     kw.update(over)
     return X.make_dims(**kw)
 
@@ -60,7 +60,7 @@ def gpu_cache(wl: Workload, table: torch.Tensor, latent=None, decode_latent=None
     the key of the group completed at start_pos."""
     import sparse_attention_top_indexer_gb300 as X
     lat = wl.latent("cuda") if latent is None else latent
-    cache = X.new_key_cache(wl.B, wl.T_cap)
+    cache = X.new_key_cache(wl.B, wl.T_cap, key_format=wl.key_format)
     d = dims_of(wl)
     X.indexer_publish_k(d, lat, wl.wk("cuda"), wl.k_norm_w("cuda"), table, 0, cache)
     if publishes_step_key(wl):
@@ -83,6 +83,25 @@ def pages_to_rows(pages) -> np.ndarray:
     return np.concatenate([codes, sc], axis=-1).reshape(*lead, P * 64, 68)
 
 
+def fp8_pages_to_rows(pages) -> np.ndarray:
+    """FP8 key pages [..., P, 8448] as 132-byte rows [..., P*64, 132]: a page is 8 groups of
+    1056 bytes; in group g, key m = 8g + r has code byte j at (j/16)*128 + r*16 + j%16 and
+    its f32 scale at 1024 + r*4 (a pure reordering of bytes)."""
+    if isinstance(pages, torch.Tensor):
+        pages = pages.cpu().numpy()
+    lead, P = pages.shape[:-2], pages.shape[-2]
+    g = pages.reshape(-1, P, 8, 1056)
+    n = g.shape[0]
+    codes = g[..., :1024].reshape(n, P, 8, 8, 8, 16).transpose(0, 1, 2, 4, 3, 5).reshape(n, P, 64, 128)
+    sc = g[..., 1024:].reshape(n, P, 64, 4)
+    return np.concatenate([codes, sc], axis=-1).reshape(*lead, P * 64, 132)
+
+
+def any_pages_to_rows(pages) -> np.ndarray:
+    """Key rows of MXFP4 (4352-byte) or FP8 (8448-byte) pages."""
+    return fp8_pages_to_rows(pages) if pages.shape[-1] == 8448 else pages_to_rows(pages)
+
+
 def pool_to_rows(pool, block_table_row, n_keys: int) -> np.ndarray:
     """The first n_keys key rows [n_keys, 68] of one sequence of a page pool [num_pages, 4352],
     following its block-table row (pool page of each logical page)."""
@@ -90,19 +109,22 @@ def pool_to_rows(pool, block_table_row, n_keys: int) -> np.ndarray:
         pool = pool.cpu().numpy()
     bt = np.asarray(block_table_row.cpu() if isinstance(block_table_row, torch.Tensor) else block_table_row)
     npages = (n_keys + 63) // 64
-    return pages_to_rows(pool[bt[:npages]])[:n_keys]
+    return any_pages_to_rows(pool[bt[:npages]])[:n_keys]
 
 
 def oracle_cache(wl: Workload, cos, sin, latent=None, decode_latent=None) -> np.ndarray:
     lat = bits(wl.latent() if latent is None else latent)
     wk, knw = bits(wl.wk()), bits(wl.k_norm_w())
-    cache = np.zeros((wl.B, wl.T_cap, 68), np.uint8)
+    fmt = "fp8" if wl.key_format == 1 else "mxfp4"
+    cache = np.zeros((wl.B, wl.T_cap, 132 if fmt == "fp8" else 68), np.uint8)
     for b in range(wl.B):   # one sequence at a time keeps the oracle's temporaries small
-        slots, rows, _ = O.publish_keys(lat[b:b + 1], wk, knw, cos, sin, 0, wl.ratio, wl.rope_dim, wl.norm_eps)
+        slots, rows, _ = O.publish_keys(lat[b:b + 1], wk, knw, cos, sin, 0, wl.ratio, wl.rope_dim, wl.norm_eps,
+                                        fmt=fmt)
         cache[b, slots] = rows[0]
     if publishes_step_key(wl):
         dl = bits(wl.decode_latent() if decode_latent is None else decode_latent)
-        slots, rows, _ = O.publish_keys(dl, wk, knw, cos, sin, wl.start_pos, wl.ratio, wl.rope_dim, wl.norm_eps)
+        slots, rows, _ = O.publish_keys(dl, wk, knw, cos, sin, wl.start_pos, wl.ratio, wl.rope_dim, wl.norm_eps,
+                                        fmt=fmt)
         cache[:, slots] = rows
     return cache
 

@@ -37,12 +37,12 @@ def test_every_declared_symbol_is_exported(X):
 
 
 def test_struct_layouts_match_header(X):
-    assert ctypes.sizeof(X.IndexerDims) == 36
+    assert ctypes.sizeof(X.IndexerDims) == 40
     assert X.IndexerYarn.beta_slow.offset == 32
 
 
 def test_abi_version(X):
-    assert X.indexer_abi_version() == 300   # 64-key pages, page pool + mixed batches
+    assert X.indexer_abi_version() == 400   # key_format field: MXFP4 or FP8 rows
 
 
 def test_workspace_size_host_only(X):

@@ -157,6 +157,7 @@ class Workload:
     heavy_scale: float = 1.0
     norm_eps: float = 1e-6
     seed: int = 0
+    key_format: int = 0       # 0: MXFP4 rows (68 bytes), 1: FP8 rows (132 bytes)
 
     @property
     def end_pos(self) -> int:
@@ -230,6 +231,9 @@ WORKLOADS = {
                  cand_topk_blocks=64, cand_block_size=64),
         Workload("large_prefill", B=2, S=32768, start_pos=0, ratio=4, H=64, topk=2048, offset=8192,
                  heavy_frac=0.05, heavy_scale=8.0),
+        # the FP8 key format (132-byte rows) on the decode and prefill shapes
+        Workload("decode_fp8", B=32, S=1, start_pos=32767, ratio=4, H=64, topk=2048, key_format=1),
+        Workload("prefill_fp8", B=1, S=8192, start_pos=0, ratio=4, H=64, topk=512, key_format=1),
     ]
 }
 
@@ -254,6 +258,7 @@ class MixedBatch:
     spare_pages: int = 8   # pool pages no sequence owns
     norm_eps: float = 1e-6
     seed: int = 0
+    key_format: int = 0       # 0: MXFP4 rows (68 bytes), 1: FP8 rows (132 bytes)
 
     @property
     def n_seq(self) -> int:
