@@ -250,20 +250,24 @@ class Setup:
                                  wl.start_pos if self.decode else 0, self.caches[i])
 
     def step(self, i):
-        """One pass of the whole hot path over batch i (forward entry point)."""
+        """One pass of the whole hot path over batch i: the step's key publish and the forward
+        in one call (indexer_forward_publish); a two-level step's consumer layer follows."""
         X, wl = self.X, self.wl
-        self.publish(i)
+        sp = wl.start_pos if self.decode else 0
         if wl.two_level:
-            X.indexer_forward(self.dims, self.q["q1"][i], self.w["q1"][i], wl.start_pos, self.table, self.caches[i],
-                              self.top1, self.ws, cand_out=self.cand)
+            X.indexer_forward_publish(self.dims, self.lat[i], self.wk, self.knw, self.q["q1"][i], self.w["q1"][i], sp,
+                                      self.table, self.caches[i], self.top1, self.ws, cand_out=self.cand)
             X.indexer_forward(self.dims, self.q["q2"][i], self.w["q2"][i], wl.start_pos, self.table, self.caches[i],
                               self.top, self.ws, cand_in=self.cand)
         else:
-            X.indexer_forward(self.dims, self.q["q"][i], self.w["q"][i], wl.start_pos, self.table, self.caches[i],
-                              self.top, self.ws)
+            X.indexer_forward_publish(self.dims, self.lat[i], self.wk, self.knw, self.q["q"][i], self.w["q"][i], sp,
+                                      self.table, self.caches[i], self.top, self.ws)
 
     def launches_per_step(self) -> int:
-        return 1 + (7 if self.wl.two_level else 3)
+        # decode: publish + query prep in one launch, scores, top-k; prefill: separate
+        # publish and query prep launches
+        small = self.decode and self.wl.B * self.wl.S * self.wl.H <= 16384
+        return (3 if small else 4) + (4 if self.wl.two_level else 0)
 
     def kernel_kinds(self):
         """One launch of each kernel of the step through its own entry point, on batch i."""
@@ -610,13 +614,13 @@ def run_e2e(st: Setup, args, dist: Dist):
         qd.copy_(qh[j], non_blocking=True)
         wd.copy_(wh[j], non_blocking=True)
         ld.copy_(lh[j], non_blocking=True)
-        X.indexer_publish_k(st.dims, ld, st.wk, st.knw, st.table, wl.start_pos if st.decode else 0, st.caches[j])
+        sp = wl.start_pos if st.decode else 0
         if wl.two_level:
-            X.indexer_forward(st.dims, q1[j], st.w["q1"][j], wl.start_pos, st.table, st.caches[j], st.top1, st.ws,
-                              cand_out=st.cand)
+            X.indexer_forward_publish(st.dims, ld, st.wk, st.knw, q1[j], st.w["q1"][j], sp, st.table, st.caches[j],
+                                      st.top1, st.ws, cand_out=st.cand)
             X.indexer_forward(st.dims, qd, wd, wl.start_pos, st.table, st.caches[j], st.top, st.ws, cand_in=st.cand)
         else:
-            X.indexer_forward(st.dims, qd, wd, wl.start_pos, st.table, st.caches[j], st.top, st.ws)
+            X.indexer_forward_publish(st.dims, ld, st.wk, st.knw, qd, wd, sp, st.table, st.caches[j], st.top, st.ws)
         outh[j].copy_(st.top, non_blocking=True)
 
     for i in range(min(8, steps)):
@@ -634,7 +638,7 @@ def run_e2e(st: Setup, args, dist: Dist):
     d2h = outh[0].numel() * 4
     return {"value": dist.world * wl.B * wl.S * steps / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
-            "api": "indexer_publish_k + indexer_forward (eager Python/ctypes calls, pinned host buffers)"}
+            "api": "indexer_forward_publish (eager Python/ctypes calls, pinned host buffers)"}
 
 
 def describe(wl: Workload) -> str:

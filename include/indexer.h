@@ -239,6 +239,22 @@ int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexe
                     void* ws, size_t ws_bytes, indexer_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * indexer_forward_publish -- indexer_publish_k followed by indexer_forward, in one call
+ * ([index-keys] Indexer.forward publishes the keys its tokens complete before scoring;
+ * [attention.py] DeepseekV4Indexer.forward: _produce_k, then the query path). The step's
+ * keys are written before any score is computed. The publish and the query prep are
+ * independent, so for a decode step (fewer than 512 keys and 16384 query-head vectors)
+ * they run in one launch. Arguments: those of indexer_publish_k (latent [B][G][Din], wk,
+ * k_norm_w, the start_pos rule for G) and of indexer_forward; k_cache is written.
+ * ------------------------------------------------------------------------- */
+int indexer_forward_publish(const IndexerDims* dims, const indexer_bf16* latent, int G, int Din,
+                            const indexer_bf16* wk, const indexer_bf16* k_norm_w, const indexer_bf16* q,
+                            const indexer_bf16* w, int B, int S, int start_pos, const float* rope_cs, int max_pos,
+                            uint8_t* k_cache, int T_cap, const int32_t* cand_in, int32_t* cand_out,
+                            int32_t* topk_out, float* scores_out, void* ws, size_t ws_bytes,
+                            indexer_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * indexer_forward_noalloc -- indexer_forward for callers that cannot allocate
  * device memory at call time. The pages have no counterpart: this is a deployment
  * convenience of the library. Some hosts own all of the device's memory -- a

@@ -18,7 +18,7 @@ __all__ = [
     "IndexerDims", "IndexerYarn", "IndexerError", "load_library", "KEY_ROW_BYTES", "STATUS_BYTES", "PAGE_KEYS",
     "PAGE_BYTES", "KEY_MXFP4", "KEY_FP8", "ROW_BYTES_FP8", "PAGE_BYTES_FP8", "row_bytes", "page_bytes",
     "new_key_cache", "new_key_pool", "indexer_publish_k_paged", "indexer_forward_paged",
-    "indexer_workspace_size_paged",
+    "indexer_workspace_size_paged", "indexer_forward_publish",
     "indexer_rope_table", "indexer_publish_k", "indexer_prep_q", "indexer_scores",
     "indexer_select_candidate_blocks", "indexer_topk", "indexer_forward", "indexer_workspace_size",
     "indexer_workspace_init", "indexer_status", "indexer_abi_version", "make_dims", "indexer_forward_noalloc",
@@ -74,6 +74,8 @@ _SIGS = {
                         ctypes.c_size_t, _P],
     "indexer_forward_noalloc": [ctypes.POINTER(IndexerDims), _P, _P, _I, _I, _I, _P, _I, _P, _I, _P, _P, _P, _P,
                                 _P],
+    "indexer_forward_publish": [ctypes.POINTER(IndexerDims), _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _I,
+                                _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "indexer_workspace_init": [_P, ctypes.c_size_t, _P],
     "indexer_publish_k_paged": [ctypes.POINTER(IndexerDims), _P, _I, _I, _P, _P, _P, _I, _P, _P, _P, _I, _P,
                                 ctypes.c_size_t, _P],
@@ -321,5 +323,24 @@ def indexer_forward_paged(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor, s
         _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(k_pool, torch.uint8, "k_pool"),
         _pool_pages(k_pool, dims), _ptr(block_table, torch.int32, "block_table"), block_table.shape[1],
         _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
+        _ptr(topk_out, torch.int32, "topk_out"), _ptr(scores_out, torch.float32, "scores_out"),
+        _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def indexer_forward_publish(dims: IndexerDims, latent: torch.Tensor, wk: torch.Tensor, k_norm_w: torch.Tensor,
+                            q: torch.Tensor, w: torch.Tensor, start_pos: int, rope_cs: torch.Tensor,
+                            k_cache: torch.Tensor, topk_out: torch.Tensor, ws: torch.Tensor,
+                            cand_in: Optional[torch.Tensor] = None, cand_out: Optional[torch.Tensor] = None,
+                            scores_out: Optional[torch.Tensor] = None, stream=None):
+    """indexer_publish_k(latent [B, G, Din]) then indexer_forward(q [B, S, H, 128]) in one call."""
+    B, G, Din = latent.shape
+    S = q.shape[1]
+    if q.shape[0] != B or k_cache.shape[0] != B:
+        raise ValueError("latent, q and k_cache must share the batch")
+    _check(load_library().indexer_forward_publish(
+        ctypes.byref(dims), _ptr(latent, torch.bfloat16, "latent"), G, Din, _ptr(wk, torch.bfloat16, "wk"),
+        _ptr(k_norm_w, torch.bfloat16, "k_norm_w"), _ptr(q, torch.bfloat16, "q"), _ptr(w, torch.bfloat16, "w"), B, S,
+        start_pos, _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(k_cache, torch.uint8, "k_cache"),
+        _cache_tcap(k_cache, dims), _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
         _ptr(topk_out, torch.int32, "topk_out"), _ptr(scores_out, torch.float32, "scores_out"),
         _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))

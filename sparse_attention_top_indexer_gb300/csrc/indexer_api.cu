@@ -203,9 +203,10 @@ int indexer_rope_table(const IndexerYarn* y, int rope_dim, int max_pos, float* t
 }
 
 // ---------------------------------------------------------------------------- key publish
-int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B, int G, int Din,
-                      const indexer_bf16* wk, const indexer_bf16* k_norm_w, const float* rope_cs, int max_pos,
-                      int start_pos, uint8_t* k_cache, int T_cap, indexer_stream_t stream) {
+// Validates a sequence-major key publish and fills its launch arguments (no launch).
+static int build_publish(const IndexerDims* dims, const indexer_bf16* latent, int B, int G, int Din,
+                         const indexer_bf16* wk, const indexer_bf16* k_norm_w, const float* rope_cs, int max_pos,
+                         int start_pos, uint8_t* k_cache, int T_cap, PublishArgs* out) {
   RETURN_IF(check_dims(dims));
   if (!latent || !wk || !k_norm_w || !rope_cs || !k_cache) return fail(INDEXER_ERR_NULL, "a required pointer is NULL");
   if (B < 1 || G < 1) return fail(INDEXER_ERR_DIMS, "B and G must be >= 1 (got %d, %d)", B, G);
@@ -233,7 +234,6 @@ int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B
   if ((long long)a.slot0 + G > T_cap) return fail(INDEXER_ERR_RANGE, "slots up to %lld exceed T_cap %d", (long long)a.slot0 + G, T_cap);
   if ((long long)a.pos0 + (long long)(G - 1) * a.pos_step >= max_pos)
     return fail(INDEXER_ERR_RANGE, "RoPE position beyond the table (max_pos %d)", max_pos);
-  RETURN_IF(check_arch());
   a.latent = latent;
   a.wk = wk;
   a.knorm = k_norm_w;
@@ -251,15 +251,25 @@ int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B
   a.T_cap = T_cap;
   a.fp8 = is_fp8(dims) ? 1 : 0;
   a.eps = dims->norm_eps;
+  *out = a;
+  return INDEXER_OK;
+}
+
+int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B, int G, int Din,
+                      const indexer_bf16* wk, const indexer_bf16* k_norm_w, const float* rope_cs, int max_pos,
+                      int start_pos, uint8_t* k_cache, int T_cap, indexer_stream_t stream) {
+  PublishArgs a{};
+  RETURN_IF(build_publish(dims, latent, B, G, Din, wk, k_norm_w, rope_cs, max_pos, start_pos, k_cache, T_cap, &a));
+  RETURN_IF(check_arch());
   const cudaError_t e = launch_publish(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "publish launch");
   return ok();
 }
 
 // ---------------------------------------------------------------------------- query prep
-static int prep_q_checked(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
-                          int start_pos, const float* rope_cs, uint8_t* q_rows, float* w_prime,
-                          cudaStream_t stream, uint32_t* status = nullptr) {
+static PrepArgs make_prep_args(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
+                               int start_pos, const float* rope_cs, uint8_t* q_rows, float* w_prime,
+                               uint32_t* status) {
   PrepArgs a{};
   a.status = status;
   a.q = q;
@@ -275,6 +285,13 @@ static int prep_q_checked(const IndexerDims* dims, const indexer_bf16* q, const 
   a.rope_dim = dims->rope_dim;
   a.start_pos = start_pos;
   a.w_scale = (float)(1.0 / std::sqrt((double)dims->head_dim) / std::sqrt((double)dims->n_heads));
+  return a;
+}
+
+static int prep_q_checked(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
+                          int start_pos, const float* rope_cs, uint8_t* q_rows, float* w_prime,
+                          cudaStream_t stream, uint32_t* status = nullptr) {
+  const PrepArgs a = make_prep_args(dims, q, w, B, S, start_pos, rope_cs, q_rows, w_prime, status);
   const cudaError_t e = launch_prep_q(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "prep_q launch");
   return INDEXER_OK;
@@ -421,10 +438,12 @@ size_t indexer_workspace_size(const IndexerDims* dims, int B, int S, int start_p
   return ws_layout(dims, B, S, start_pos).total;
 }
 
-int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
-                    int start_pos, const float* rope_cs, int max_pos, const uint8_t* k_cache, int T_cap,
-                    const int32_t* cand_in, int32_t* cand_out, int32_t* topk_out, float* scores_out, void* ws,
-                    size_t ws_bytes, indexer_stream_t stream) {
+// The forward of indexer_forward; with `pub`, the step's key publish runs first (in the same
+// launch as the query prep when both are small).
+static int forward_impl(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
+                        int start_pos, const float* rope_cs, int max_pos, const uint8_t* k_cache, int T_cap,
+                        const int32_t* cand_in, int32_t* cand_out, int32_t* topk_out, float* scores_out, void* ws,
+                        size_t ws_bytes, indexer_stream_t stream, const PublishArgs* pub) {
   RETURN_IF(check_prep_args(dims, q, w, B, S, start_pos, rope_cs, max_pos));
   const int T = (start_pos + S) / dims->ratio;
   RETURN_IF(check_cache(k_cache, T_cap, T));
@@ -441,8 +460,15 @@ int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexe
   uint8_t* q_rows = base + l.q_rows;
   float* w_prime = reinterpret_cast<float*>(base + l.w_prime);
   float* scores = scores_out ? scores_out : reinterpret_cast<float*>(base + l.scores);
-  RETURN_IF(prep_q_checked(dims, q, w, B, S, start_pos, rope_cs, q_rows, w_prime, st,
-                           reinterpret_cast<uint32_t*>(base)));
+  if (pub) {
+    const PrepArgs pa = make_prep_args(dims, q, w, B, S, start_pos, rope_cs, q_rows, w_prime,
+                                       reinterpret_cast<uint32_t*>(base));
+    const cudaError_t e = launch_publish_prep(*pub, pa, st);
+    if (e != cudaSuccess) return cuda_fail(e, "publish / prep_q launch");
+  } else {
+    RETURN_IF(prep_q_checked(dims, q, w, B, S, start_pos, rope_cs, q_rows, w_prime, st,
+                             reinterpret_cast<uint32_t*>(base)));
+  }
   // level two with one query row and no score output: only the kept blocks' keys are
   // scored and ranked (the other positions of the workspace scores are never read)
   const bool sparse2 = cand_in && !cand_out && !scores_out && S == 1 && T <= 32768 &&
@@ -686,6 +712,26 @@ int indexer_forward_paged(const IndexerDims* dims, const indexer_bf16* q, const 
     if (e != cudaSuccess) return cuda_fail(e, "topk launch");
   }
   return ok();
+}
+
+int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
+                    int start_pos, const float* rope_cs, int max_pos, const uint8_t* k_cache, int T_cap,
+                    const int32_t* cand_in, int32_t* cand_out, int32_t* topk_out, float* scores_out, void* ws,
+                    size_t ws_bytes, indexer_stream_t stream) {
+  return forward_impl(dims, q, w, B, S, start_pos, rope_cs, max_pos, k_cache, T_cap, cand_in, cand_out, topk_out,
+                      scores_out, ws, ws_bytes, stream, nullptr);
+}
+
+int indexer_forward_publish(const IndexerDims* dims, const indexer_bf16* latent, int G, int Din,
+                            const indexer_bf16* wk, const indexer_bf16* k_norm_w, const indexer_bf16* q,
+                            const indexer_bf16* w, int B, int S, int start_pos, const float* rope_cs, int max_pos,
+                            uint8_t* k_cache, int T_cap, const int32_t* cand_in, int32_t* cand_out,
+                            int32_t* topk_out, float* scores_out, void* ws, size_t ws_bytes,
+                            indexer_stream_t stream) {
+  PublishArgs pa{};
+  RETURN_IF(build_publish(dims, latent, B, G, Din, wk, k_norm_w, rope_cs, max_pos, start_pos, k_cache, T_cap, &pa));
+  return forward_impl(dims, q, w, B, S, start_pos, rope_cs, max_pos, k_cache, T_cap, cand_in, cand_out, topk_out,
+                      scores_out, ws, ws_bytes, stream, &pa);
 }
 
 int indexer_workspace_init(void* ws, size_t ws_bytes, indexer_stream_t stream) {

@@ -51,8 +51,14 @@ cudaError_t launch_rope_table(const RopeFreqs& freqs, int half, int max_pos, flo
 //     rotated by table entry i with the f32 sequence x0*c - x1*s, x0*s + x1*c, then bf16.
 //  4. e2m1/e8m0 quantisation per 32-block (warp w owns block w); the 64 code bytes and
 //     4 scale bytes go to the key's places in its 64-key page of the pool.
-template <int TPO>   // threads per output dimension (1 or 4)
-__global__ void __launch_bounds__(kHeadDim * TPO) publish_kernel(PublishArgs a) {
+// Warms L2 with wk (CTAs 0..3 of a launch, 32 rows each) while the kernels before run.
+__device__ __forceinline__ void prefetch_wk(const PublishArgs& a, int cta) {
+  if (threadIdx.x == 0 && cta < 4) prefetch_l2_bulk(a.wk + (size_t)cta * 32 * a.Din, (uint32_t)(32 * a.Din * 2));
+}
+
+// The whole publish of key `key` by the CTA's kHeadDim * TPO threads.
+template <int TPO>
+__device__ __forceinline__ void publish_key(const PublishArgs& a, int key) {
   constexpr int NT = kHeadDim * TPO;
   __shared__ float lat[1024];
   __shared__ float kx[kHeadDim];
@@ -60,12 +66,6 @@ __global__ void __launch_bounds__(kHeadDim * TPO) publish_kernel(PublishArgs a) 
   __shared__ double wsum[4];
   __shared__ double rinv;
   const int tid = threadIdx.x;
-  pdl_allow_next();
-  if (tid == 0 && blockIdx.x < 4) {   // warm L2 with wk while the kernels before run: four CTAs, 32 rows each
-    prefetch_l2_bulk(a.wk + (size_t)blockIdx.x * 32 * a.Din, (uint32_t)(32 * a.Din * 2));
-  }
-  pdl_wait();
-  const int key = blockIdx.x;
   const int b = key / a.G, j = key % a.G;
   // the key's slot in the page pool and its RoPE position
   long long slot = (long long)b * a.T_cap + a.slot0 + j;
@@ -216,6 +216,14 @@ __global__ void __launch_bounds__(kHeadDim * TPO) publish_kernel(PublishArgs a) 
   if (lane == 0) page[page_scale_offset(m) + warp] = (uint8_t)(e + 127);
 }
 
+template <int TPO>   // threads per output dimension (1 or 4)
+__global__ void __launch_bounds__(kHeadDim * TPO) publish_kernel(PublishArgs a) {
+  pdl_allow_next();
+  prefetch_wk(a, blockIdx.x);
+  pdl_wait();
+  publish_key<TPO>(a, blockIdx.x);
+}
+
 cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream) {
   const long long keys = (long long)a.B * a.G;
   // few keys (a decode step): four threads per output dimension for a shorter chain;
@@ -230,16 +238,18 @@ cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream) {
 // the keys; the 4 threads of a
 // 32-block share its amax by shuffles; each thread writes 4 code bytes, the first
 // thread of a block its scale byte. w' = f32(w) * head_dim^-0.5 * H^-0.5.
-__global__ void __launch_bounds__(256) prep_q_kernel(PrepArgs a) {
-  pdl_allow_next();
-  const int tid = threadIdx.x;
-  if (tid == 0) {   // warm L2 with the CTA's 16 query-head vectors while the kernels before run
-    const long long v0 = (long long)blockIdx.x * 16;
+// Warms L2 with the 16 query-head vectors from v0 (thread t == 0 of a 256-thread group).
+__device__ __forceinline__ void prefetch_q16(const PrepArgs& a, long long v0, int t) {
+  if (t == 0 && v0 < a.n_vec) {
     const long long nv = a.n_vec - v0 < 16 ? a.n_vec - v0 : 16;
     prefetch_l2_bulk(a.q + v0 * kHeadDim, (uint32_t)(nv * kHeadDim * 2));
   }
-  pdl_wait();
-  const long long v = (long long)blockIdx.x * 16 + (tid >> 4);
+}
+
+// Query prep of the 16 vectors from v0 by a group of 256 threads (t = 0..255).
+__device__ __forceinline__ void prep_q16(const PrepArgs& a, long long v0, int t) {
+  const int tid = t;
+  const long long v = v0 + (tid >> 4);
   const int j = tid & 15;
   if (v >= a.n_vec) return;   // whole 16-lane groups leave together
   const int lane = tid & 31;
@@ -263,6 +273,43 @@ __global__ void __launch_bounds__(256) prep_q_kernel(PrepArgs a) {
     if ((j & 3) == 0) row[kCodeBytes + (j >> 2)] = (uint8_t)(e + 127);
   }
   if (j == 0) a.w_prime[v] = bf16_to_f32(a.w[v]) * a.w_scale;
+}
+
+__global__ void __launch_bounds__(256) prep_q_kernel(PrepArgs a) {
+  pdl_allow_next();
+  const long long v0 = (long long)blockIdx.x * 16;
+  prefetch_q16(a, v0, threadIdx.x);
+  pdl_wait();
+  prep_q16(a, v0, threadIdx.x);
+}
+
+// A decode step's key publish and query prep in one launch (the two are independent):
+// CTAs 0 .. n_keys-1 publish one key each (512 threads, four per output dimension), the
+// others prepare 32 query-head vectors each (two groups of 256 threads).
+__global__ void __launch_bounds__(4 * kHeadDim) publish_prep_kernel(PublishArgs pa, PrepArgs qa, int n_keys) {
+  pdl_allow_next();
+  const int cta = (int)blockIdx.x;
+  if (cta < n_keys) {
+    prefetch_wk(pa, cta);
+    pdl_wait();
+    publish_key<4>(pa, cta);
+  } else {
+    const long long v0 = (long long)(cta - n_keys) * 32 + 16 * (threadIdx.x >> 8);
+    prefetch_q16(qa, v0, threadIdx.x & 255);
+    pdl_wait();
+    prep_q16(qa, v0, threadIdx.x & 255);
+  }
+}
+
+cudaError_t launch_publish_prep(const PublishArgs& pa, const PrepArgs& qa, cudaStream_t stream) {
+  const long long keys = (long long)pa.B * pa.G;
+  if (keys >= 512 || qa.n_vec > 16384) {   // large: the separate kernels
+    cudaError_t e = launch_publish(pa, stream);
+    return e != cudaSuccess ? e : launch_prep_q(qa, stream);
+  }
+  const long long blocks = keys + (qa.n_vec + 31) / 32;
+  return launch_overlapped(publish_prep_kernel, dim3((unsigned)blocks), dim3(4 * kHeadDim), 0, stream, pa, qa,
+                           (int)keys);
 }
 
 // Many vectors (prefill): a CTA takes 64 vectors, brings their 16 KB of bf16 q into shared

@@ -99,6 +99,9 @@ struct PrepArgs {
   float w_scale;            // head_dim^-0.5 * H^-0.5
 };
 cudaError_t launch_prep_q(const PrepArgs& a, cudaStream_t stream);
+// A decode step's key publish and query prep in one launch (few keys and vectors), else
+// the two launches in order.
+cudaError_t launch_publish_prep(const PublishArgs& pa, const PrepArgs& qa, cudaStream_t stream);
 
 struct ScoreArgs {
   const uint8_t* q_rows;    // [rows][H][68]

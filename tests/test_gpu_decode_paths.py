@@ -138,3 +138,45 @@ def test_level_two_kept_blocks_only(X, B, start, cbk, cbs, topk):
                                        wl.topk, wl.offset, cand_in=cand, cand_block_size=cbs)
         C.compare_topk(top_kept.cpu().numpy().reshape(-1, wl.topk), ref_top.reshape(-1, wl.topk),
                        ref_sc.reshape(-1, wl.T), wl.offset)
+
+
+@pytest.mark.parametrize("name,B,H,start,fmt", [
+    ("fp_dec", 32, 64, 32767, 0),     # decode: publish and query prep in one launch
+    ("fp_h16", 5, 16, 4095, 0),
+    ("fp_fp8", 8, 64, 8191, 1),
+    ("fp_pf", 1, 64, 0, 0),           # prefill: the separate launches
+])
+def test_forward_publish_equals_separate_calls(X, name, B, H, start, fmt):
+    """indexer_forward_publish leaves the same cache, scores and indices as
+    indexer_publish_k followed by indexer_forward."""
+    base = WORKLOADS["decode"] if start > 0 else WORKLOADS["tiny_prefill"]
+    wl = dataclasses.replace(base, name=name, B=B, H=H, start_pos=start, key_format=fmt,
+                             topk=min(base.topk, 512))
+    d = C.dims_of(wl)
+    table = C.gpu_table(wl.max_pos)
+    if start > 0:
+        cache_a = X.new_key_cache(wl.B, wl.T_cap, key_format=fmt)
+        X.indexer_publish_k(d, wl.latent("cuda"), wl.wk("cuda"), wl.k_norm_w("cuda"), table, 0, cache_a)
+        lat = wl.decode_latent("cuda")
+    else:
+        cache_a = X.new_key_cache(wl.B, wl.T_cap, key_format=fmt)
+        lat = wl.latent("cuda")
+    cache_b = cache_a.clone()
+    q, w = wl.q("cuda"), wl.w("cuda")
+    outs = []
+    for cache, fused in ((cache_a, False), (cache_b, True)):
+        ws = torch.empty(X.indexer_workspace_size(d, wl.B, wl.S, wl.start_pos), dtype=torch.uint8, device="cuda")
+        X.indexer_workspace_init(ws)
+        top = torch.empty((wl.B, wl.S, wl.topk), dtype=torch.int32, device="cuda")
+        sc = torch.empty((wl.B, wl.S, wl.T), dtype=torch.float32, device="cuda")
+        if fused:
+            X.indexer_forward_publish(d, lat, wl.wk("cuda"), wl.k_norm_w("cuda"), q, w, wl.start_pos, table, cache,
+                                      top, ws, scores_out=sc)
+        else:
+            X.indexer_publish_k(d, lat, wl.wk("cuda"), wl.k_norm_w("cuda"), table, wl.start_pos, cache)
+            X.indexer_forward(d, q, w, wl.start_pos, table, cache, top, ws, scores_out=sc)
+        X.indexer_status(ws)
+        outs.append((top, sc))
+    assert torch.equal(cache_a, cache_b), "caches differ"
+    assert torch.equal(outs[0][1], outs[1][1]), "scores differ"
+    assert torch.equal(outs[0][0], outs[1][0]), "indices differ"
