@@ -388,6 +388,15 @@ def run_ours(args, dist: Dist):
                 "kernel_ms": score_ms,
                 "peak_source": f"{peaks['source']} bf16_tflops x {fm['ratio']:g} (nominal {fm['label']}/bf16)"}
 
+    # the HBM-bound helper kernels against the same peak: algorithmic bytes per launch
+    rb = fmt_of(wl)["row"]
+    nvec = wl.B * wl.S * wl.H
+    keys = wl.B * (1 if st.decode else wl.T)
+    helper_bytes = {"prep_q": nvec * (wl.D * 2 + 2 + rb + 4),
+                    "publish": keys * (wl.D * 2 + rb) + wl.D * wl.D * 2 + wl.D * 2}
+    helpers = {k: {"bytes": b, "GB/s": b / (kernel_ms[k] / 1e3) / 1e9,
+                   "frac": b / (kernel_ms[k] / 1e3) / 1e9 / peaks["hbm_gbs"]}
+               for k, b in helper_bytes.items() if kernel_ms.get(k)}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -401,6 +410,7 @@ def run_ours(args, dist: Dist):
         "key_scores_per_s": key_scores,
         "kernel_ms": kernel_ms,
         "roofline": roof,
+        "helper_rooflines": helpers,
         "e2e": e2e,
         "gpu_launches": st.launches_per_step() * args.steps,
         "clocks": clocks,

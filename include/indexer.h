@@ -243,7 +243,7 @@ int indexer_forward(const IndexerDims* dims, const indexer_bf16* q, const indexe
  * ([index-keys] Indexer.forward publishes the keys its tokens complete before scoring;
  * [attention.py] DeepseekV4Indexer.forward: _produce_k, then the query path). The step's
  * keys are written before any score is computed. The publish and the query prep are
- * independent, so for a decode step (fewer than 512 keys and 16384 query-head vectors)
+ * independent, so for a decode step (at most 160 keys and 16384 query-head vectors)
  * they run in one launch. Arguments: those of indexer_publish_k (latent [B][G][Din], wk,
  * k_norm_w, the start_pos rule for G) and of indexer_forward; k_cache is written.
  * ------------------------------------------------------------------------- */

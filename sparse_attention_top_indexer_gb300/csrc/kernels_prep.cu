@@ -38,10 +38,10 @@ cudaError_t launch_rope_table(const RopeFreqs& freqs, int half, int max_pos, flo
 }
 
 // ---------------------------------------------------------------------------- key publish
-// One CTA per key: 128 x TPO threads (TPO = 4 for a few keys, 1 for many).
+// One CTA per key: 128 x TPO threads (TPO = 8 for a few keys, 4 for a few hundred, 1 for many).
 //  1. k_pre[o] = bf16( sum_i wk[o][i] * latent[i] ): bf16*bf16 products are exact in f32,
 //     their sum is carried error-free (TwoSum) and rounded once to bf16 ("DeepSeek V4.1"
-//     index-keys page, Indexer: wk bf16 Linear). Output o's products are split over four
+//     index-keys page, Indexer: wk bf16 Linear). Output o's products are split over TPO
 //     consecutive threads (four accumulators each), whose parts are merged with TwoSum
 //     across the lanes; every global read is issued at entry. From step 2 on, thread
 //     o < 128 owns output dim o.
@@ -226,8 +226,9 @@ __global__ void __launch_bounds__(kHeadDim * TPO) publish_kernel(PublishArgs a) 
 
 cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream) {
   const long long keys = (long long)a.B * a.G;
-  // few keys (a decode step): four threads per output dimension for a shorter chain;
-  // many keys (prefill): one, for throughput
+  // few keys (a decode step, at most about one per SM): eight threads per output dimension
+  // for the shortest chain; a few hundred: four; many keys (prefill): one, for throughput
+  if (keys <= 160) return launch_overlapped(publish_kernel<8>, dim3((unsigned)keys), dim3(8 * kHeadDim), 0, stream, a);
   if (keys < 512) return launch_overlapped(publish_kernel<4>, dim3((unsigned)keys), dim3(4 * kHeadDim), 0, stream, a);
   return launch_overlapped(publish_kernel<1>, dim3((unsigned)keys), dim3(kHeadDim), 0, stream, a);
 }
@@ -284,17 +285,17 @@ __global__ void __launch_bounds__(256) prep_q_kernel(PrepArgs a) {
 }
 
 // A decode step's key publish and query prep in one launch (the two are independent):
-// CTAs 0 .. n_keys-1 publish one key each (512 threads, four per output dimension), the
-// others prepare 32 query-head vectors each (two groups of 256 threads).
-__global__ void __launch_bounds__(4 * kHeadDim) publish_prep_kernel(PublishArgs pa, PrepArgs qa, int n_keys) {
+// CTAs 0 .. n_keys-1 publish one key each (1024 threads, eight per output dimension), the
+// others prepare 64 query-head vectors each (four groups of 256 threads).
+__global__ void __launch_bounds__(8 * kHeadDim) publish_prep_kernel(PublishArgs pa, PrepArgs qa, int n_keys) {
   pdl_allow_next();
   const int cta = (int)blockIdx.x;
   if (cta < n_keys) {
     prefetch_wk(pa, cta);
     pdl_wait();
-    publish_key<4>(pa, cta);
+    publish_key<8>(pa, cta);
   } else {
-    const long long v0 = (long long)(cta - n_keys) * 32 + 16 * (threadIdx.x >> 8);
+    const long long v0 = (long long)(cta - n_keys) * 64 + 16 * (threadIdx.x >> 8);
     prefetch_q16(qa, v0, threadIdx.x & 255);
     pdl_wait();
     prep_q16(qa, v0, threadIdx.x & 255);
@@ -303,12 +304,12 @@ __global__ void __launch_bounds__(4 * kHeadDim) publish_prep_kernel(PublishArgs 
 
 cudaError_t launch_publish_prep(const PublishArgs& pa, const PrepArgs& qa, cudaStream_t stream) {
   const long long keys = (long long)pa.B * pa.G;
-  if (keys >= 512 || qa.n_vec > 16384) {   // large: the separate kernels
+  if (keys > 160 || qa.n_vec > 16384) {   // larger: the separate kernels
     cudaError_t e = launch_publish(pa, stream);
     return e != cudaSuccess ? e : launch_prep_q(qa, stream);
   }
-  const long long blocks = keys + (qa.n_vec + 31) / 32;
-  return launch_overlapped(publish_prep_kernel, dim3((unsigned)blocks), dim3(4 * kHeadDim), 0, stream, pa, qa,
+  const long long blocks = keys + (qa.n_vec + 63) / 64;
+  return launch_overlapped(publish_prep_kernel, dim3((unsigned)blocks), dim3(8 * kHeadDim), 0, stream, pa, qa,
                            (int)keys);
 }
 
