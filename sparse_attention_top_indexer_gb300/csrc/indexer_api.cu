@@ -396,8 +396,8 @@ int indexer_select_candidate_blocks(const IndexerDims* dims, const float* scores
   return ok();
 }
 
-static int topk_checked(const IndexerDims* dims, const float* scores, int B, int S, int start_pos, int T,
-                        const int32_t* cand, int32_t* out, cudaStream_t stream, bool sparse = false) {
+static TopkArgs make_topk_args(const IndexerDims* dims, const float* scores, int B, int S, int start_pos, int T,
+                               const int32_t* cand, int32_t* out, bool sparse) {
   TopkArgs a{};
   a.scores = scores;
   a.out = out;
@@ -413,9 +413,20 @@ static int topk_checked(const IndexerDims* dims, const float* scores, int B, int
   a.cbk = dims->cand_topk_blocks;
   a.cbs = dims->cand_block_size > 0 ? dims->cand_block_size : 1;
   a.sparse = sparse ? 1 : 0;
+  return a;
+}
+
+static int topk_checked(const IndexerDims* dims, const float* scores, int B, int S, int start_pos, int T,
+                        const int32_t* cand, int32_t* out, cudaStream_t stream, bool sparse = false) {
+  const TopkArgs a = make_topk_args(dims, scores, B, S, start_pos, T, cand, out, sparse);
   const cudaError_t e = launch_topk(a, stream);
   if (e != cudaSuccess) return cuda_fail(e, "topk launch");
   return INDEXER_OK;
+}
+
+// Level one with few rows and no filter of its own: candidate blocks and top-k in one launch.
+static bool fuse_cand_topk(int rows, int T, const int32_t* cand_in, const int32_t* cand_out) {
+  return cand_out != nullptr && cand_in == nullptr && rows < 4096 && T <= kTopkMaxT;
 }
 
 int indexer_topk(const IndexerDims* dims, const float* scores, int B, int S, int start_pos, int T, int32_t* out,
@@ -510,6 +521,12 @@ static int forward_impl(const IndexerDims* dims, const indexer_bf16* q, const in
       c.ratio = dims->ratio;
       c.cbk = dims->cand_topk_blocks;
       c.cbs = dims->cand_block_size;
+      if (fuse_cand_topk(B * S, T, cand_in, cand_out)) {
+        const TopkArgs ta = make_topk_args(dims, scores, B, S, start_pos, T, nullptr, topk_out, false);
+        const cudaError_t e2 = launch_cand_topk(c, ta, st);
+        if (e2 != cudaSuccess) return cuda_fail(e2, "candidate / topk launch");
+        return ok();
+      }
       const cudaError_t e2 = launch_candidates(c, st);
       if (e2 != cudaSuccess) return cuda_fail(e2, "candidate launch");
     }
@@ -677,8 +694,9 @@ int indexer_forward_paged(const IndexerDims* dims, const indexer_bf16* q, const 
     const cudaError_t e = launch_scores(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "scores launch");
   }
+  CandArgs cargs{};
   if (cand_out) {
-    CandArgs c{};
+    CandArgs& c = cargs;
     c.scores = scores;
     c.blocks = cand_out;
     c.rinfo = rows;
@@ -689,8 +707,10 @@ int indexer_forward_paged(const IndexerDims* dims, const indexer_bf16* q, const 
     c.ratio = dims->ratio;
     c.cbk = dims->cand_topk_blocks;
     c.cbs = dims->cand_block_size;
-    const cudaError_t e = launch_candidates(c, st);
-    if (e != cudaSuccess) return cuda_fail(e, "candidate launch");
+    if (!fuse_cand_topk(Q, T_max, cand_in, cand_out)) {
+      const cudaError_t e = launch_candidates(c, st);
+      if (e != cudaSuccess) return cuda_fail(e, "candidate launch");
+    }
   }
   {
     TopkArgs a{};
@@ -708,7 +728,8 @@ int indexer_forward_paged(const IndexerDims* dims, const indexer_bf16* q, const 
     a.cbk = dims->cand_topk_blocks;
     a.cbs = dims->cand_block_size > 0 ? dims->cand_block_size : 1;
     a.sparse = sparse2 ? 1 : 0;
-    const cudaError_t e = launch_topk(a, st);
+    const cudaError_t e = fuse_cand_topk(Q, T_max, cand_in, cand_out) ? launch_cand_topk(cargs, a, st)
+                                                                       : launch_topk(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "topk launch");
   }
   return ok();

@@ -240,7 +240,102 @@ __global__ void __launch_bounds__(kSelThreads, 1) cand_kernel(const CandArgs a) 
   select_top<kSelThreads, BPT>(key, min(a.cbk, nblk), a.blocks + (size_t)row * a.cbk, a.cbk, 0, sh.sel);
 }
 
+// Level one of the two-level top-k without a filter of its own (the candidate source
+// layer): the candidate blocks and the row's own top-k come from the same scores, so one
+// CTA per row loads them into registers once, forms the block keys (cand_kernel's rule),
+// keeps the cbk best blocks, then selects the k_eff best positions (topk_kernel's rule,
+// including the short-context fill) with the same primitive.
+union CandTopkShared {
+  uint32_t bkeys[kCandMaxBlocks];
+  SelectShared<kSelThreads> sel;   // reused once the block keys are in registers
+};
+
+template <int KPT, int BPT>
+__global__ void __launch_bounds__(kSelThreads, 1) cand_topk_kernel(const CandArgs c, const TopkArgs a) {
+  __shared__ CandTopkShared sh;
+  const int tid = threadIdx.x;
+  pdl_allow_next();
+  pdl_wait();
+  const int row = blockIdx.x;
+  const int2 ext = row_extent(a.rinfo, row, a.S, a.T, a.start_pos, a.ratio);
+  const int vis = ext.x;
+  const int k_eff = min(a.topk, ext.y);
+  const int nblk = (a.T + c.cbs - 1) / c.cbs;
+  for (int i = tid; i < nblk; i += kSelThreads) sh.bkeys[i] = 0u;
+  __syncthreads();
+  const int base = tid * KPT;
+  const float* src = a.scores + (size_t)row * a.ld;
+  uint32_t key[KPT];   // position keys: finite scores at t < vis, else 0
+  if ((a.ld & 3) == 0) {   // rows start 16-byte aligned: float4 loads
+#pragma unroll
+    for (int j = 0; j < KPT; j += 4) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (base + j < vis) v = *reinterpret_cast<const float4*>(src + base + j);
+      const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) key[j + u] = (base + j + u < vis && isfinite(f[u])) ? order_key(f[u]) : 0u;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      const float f = base + j < vis ? src[base + j] : 0.f;
+      key[j] = (base + j < vis && isfinite(f)) ? order_key(f) : 0u;
+    }
+  }
+  if (base < vis) {   // block maxima: positions advance by one, one block boundary at a time
+    int blk = base / c.cbs, bnd = (blk + 1) * c.cbs;
+    uint32_t run = 0u;
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) {
+      if (base + j >= bnd) {
+        if (run) atomicMax(&sh.bkeys[blk], run);
+        ++blk;
+        bnd += c.cbs;
+        run = 0u;
+      }
+      run = max(run, key[j]);
+    }
+    if (run) atomicMax(&sh.bkeys[blk], run);
+  }
+  __syncthreads();
+  uint32_t bk[BPT];
+#pragma unroll
+  for (int j = 0; j < BPT; ++j) {
+    const int bi = tid * BPT + j;
+    bk[j] = bi < nblk ? sh.bkeys[bi] : 0u;
+  }
+  __syncthreads();   // the block keys are in registers: the shared memory is reused below
+  select_top<kSelThreads, BPT>(bk, min(c.cbk, nblk), c.blocks + (size_t)row * c.cbk, c.cbk, 0, sh.sel);
+  __syncthreads();   // the selection's shared memory is reused for the top-k
+  int32_t* out = a.out + (size_t)row * a.topk;
+  if (vis <= k_eff) {   // short-context rule: every visible position, in order
+    for (int i = tid; i < a.topk; i += kSelThreads) out[i] = i < vis ? i + a.offset : -1;
+    return;
+  }
+  select_top<kSelThreads, KPT>(key, k_eff, out, a.topk, a.offset, sh.sel);
+}
+
+template <int KPT>
+cudaError_t launch_cand_topk_kpt(const CandArgs& c, const TopkArgs& a, int nblk, cudaStream_t stream) {
+  const dim3 grid(a.rows), block(kSelThreads);
+  if (nblk <= kSelThreads) return launch_overlapped(cand_topk_kernel<KPT, 1>, grid, block, 0, stream, c, a);
+  if (nblk <= 2 * kSelThreads) return launch_overlapped(cand_topk_kernel<KPT, 2>, grid, block, 0, stream, c, a);
+  if (nblk <= 4 * kSelThreads) return launch_overlapped(cand_topk_kernel<KPT, 4>, grid, block, 0, stream, c, a);
+  if (nblk <= 8 * kSelThreads) return launch_overlapped(cand_topk_kernel<KPT, 8>, grid, block, 0, stream, c, a);
+  return cudaErrorInvalidValue;
+}
+
 }  // namespace
+
+cudaError_t launch_cand_topk(const CandArgs& c, const TopkArgs& a, cudaStream_t stream) {
+  if (a.rows <= 0) return cudaSuccess;
+  if (a.cand != nullptr || a.sparse || c.rows != a.rows || c.ld != a.ld) return cudaErrorInvalidValue;
+  const int nblk = (a.T + c.cbs - 1) / c.cbs;
+  if (a.T <= kSelThreads * 8) return launch_cand_topk_kpt<8>(c, a, nblk, stream);
+  if (a.T <= kSelThreads * 16) return launch_cand_topk_kpt<16>(c, a, nblk, stream);
+  if (a.T <= kSelThreads * 32) return launch_cand_topk_kpt<32>(c, a, nblk, stream);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   if (a.rows <= 0) return cudaSuccess;

@@ -147,6 +147,9 @@ struct CandArgs {
   int rows, S, T, ld, start_pos, ratio, cbk, cbs;
 };
 cudaError_t launch_candidates(const CandArgs& a, cudaStream_t stream);
+// Candidate blocks and top-k of the same unfiltered rows in one launch (c and a describe the
+// same rows); for level one with few rows.
+cudaError_t launch_cand_topk(const CandArgs& c, const TopkArgs& a, cudaStream_t stream);
 
 // Sets the thread-local message returned by indexer_last_error(); returns code.
 int set_last_error(int code, const char* msg);
