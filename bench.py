@@ -264,10 +264,11 @@ class Setup:
                                       self.table, self.caches[i], self.top, self.ws)
 
     def launches_per_step(self) -> int:
-        # decode: publish + query prep in one launch, scores, top-k; prefill: separate
-        # publish and query prep launches
+        # decode: publish + query prep in one launch, scores, top-k (level one: candidate
+        # blocks and top-k in one launch); prefill: separate publish and query prep launches;
+        # a two-level step's consumer layer: query prep, scores, top-k
         small = self.decode and self.wl.B * self.wl.S * self.wl.H <= 16384
-        return (3 if small else 4) + (4 if self.wl.two_level else 0)
+        return (3 if small else 4) + (3 if self.wl.two_level else 0)
 
     def kernel_kinds(self):
         """One launch of each kernel of the step through its own entry point, on batch i."""

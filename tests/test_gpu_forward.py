@@ -193,3 +193,31 @@ def test_short_context_rows_exact(X):
         if vis[s] <= 128:
             want = [i + wl.offset for i in range(vis[s])] + [-1] * (128 - vis[s])
             assert list(top[s]) == want
+
+
+@pytest.mark.parametrize("ratio,S,start,H,fmt,topk", [
+    (1, 96, 0, 64, 0, 32),        # no compression
+    (2, 200, 0, 16, 0, 40),       # ratio 2 prefill
+    (4, 300, 1000, 64, 0, 128),   # chunked prefill: 300 rows at start_pos 1000
+    (1, 1, 511, 32, 0, 64),       # ratio 1 decode (every token completes a group)
+    (2, 64, 640, 128, 1, 100),    # FP8, ratio 2, 128 heads, a chunk at start_pos 640
+])
+def test_forward_ratios_and_chunks(X, ratio, S, start, H, fmt, topk):
+    """Compression ratios 1 and 2 and chunked prefill (start_pos > 0, S > 1) against the
+    oracle on every row."""
+    wl = dataclasses.replace(WORKLOADS["prefill"], name=f"r{ratio}_{S}_{start}_{fmt}", B=2, S=S, start_pos=start,
+                             ratio=ratio, H=H, topk=topk, key_format=fmt)
+    table = C.gpu_table(wl.max_pos)
+    cos, sin = C.oracle_table(wl.max_pos)
+    cache = C.gpu_cache(wl, table)
+    ref_cache = C.oracle_cache(wl, cos, sin)
+    assert np.array_equal(C.any_pages_to_rows(cache), ref_cache)
+    q, w = wl.q("cuda"), wl.w("cuda")
+    top, _, sc = _run_forward(X, wl, q, w, table, cache)
+    ref_top, _, ref_sc = O.forward(C.bits(q), C.bits(w), ref_cache, cos, sin, wl.start_pos, wl.ratio, wl.rope_dim,
+                                   wl.topk, wl.offset)
+    C.assert_scores_close(sc.cpu().numpy(), ref_sc)
+    swaps = C.compare_topk(top.cpu().numpy().reshape(-1, topk), ref_top.reshape(-1, topk), ref_sc.reshape(-1, wl.T),
+                           wl.offset)
+    _check_properties(top.cpu().numpy(), wl)
+    print(f"ratio {ratio} S{S} start {start}: boundary swaps {swaps}")
