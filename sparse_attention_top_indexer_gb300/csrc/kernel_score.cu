@@ -813,8 +813,9 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
       const uint32_t sfb = (uint32_t)(C::SFB_COL + qb * 2 * C::SB);
       for (int i = 0; i < d.nt; ++i, ++j) {
         const int st = (int)(j % C::NSTAGE), c = (int)(j % C::NACC);
-        bool ok = warp_wait(bar_ready(c), (j / C::NACC) & 1u);
-        if (ok) ok = warp_wait(bar_full(st), (j / C::NSTAGE) & 1u);
+        // the scale warps arrive on "ready" only after they have seen the tile's copy land
+        // (its full barrier), so the tile is in place once "ready" is seen
+        const bool ok = warp_wait(bar_ready(c), (j / C::NACC) & 1u);
         if (!ok) {
           failed = true;
           break;
