@@ -283,13 +283,10 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   }
   return true;
 }
-// Lane 0 of each warp waits (bounded) for the phase; the warp follows it. Warp-uniform.
+// The whole warp waits (bounded) for the phase, converged; warp-uniform result.
 __device__ __forceinline__ bool warp_wait_bounded(uint32_t bar, uint32_t parity) {
-  uint32_t ok = 1u;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity) ? 1u : 0u;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();
-  return ok != 0u;
+  const bool ok = mbar_wait(bar, parity);
+  return __all_sync(0xffffffffu, ok);
 }
 // Bulk (non-tensor TMA) copy global -> shared; dst, src and bytes multiples of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

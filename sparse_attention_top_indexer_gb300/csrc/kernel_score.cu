@@ -177,13 +177,12 @@ __device__ __forceinline__ void issue_tile_mma(uint32_t acc, uint32_t pa, uint32
   }
 }
 
-// Lane 0 waits (bounded) for the phase; the warp follows it. Warp-uniform result.
+// The whole warp waits (bounded) for the phase, converged: every lane polls, and the warp
+// agrees on the result (a single polling lane followed by a shuffle measured ~20 % slower in
+// the score kernels). Warp-uniform result.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
-  uint32_t ok = 1u;
-  if ((threadIdx.x & 31) == 0) ok = mbar_wait(bar, parity) ? 1u : 0u;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();
-  return ok != 0u;
+  const bool ok = mbar_wait(bar, parity);
+  return __all_sync(0xffffffffu, ok);
 }
 
 template <int H, int QG, int EPI, class F>
