@@ -385,19 +385,21 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
       // the page has landed, and accumulator c (with its scale set) has been drained
       bool ok = warp_wait(bar_full(st), (uint32_t)(i / C::NSTAGE) & 1u);
       if (ok && i >= C::NACC) ok = warp_wait(bar_empty(c), (uint32_t)((i - C::NACC) / C::NACC) & 1u);
+      if (ok) {
+        tc_fence_after();
+        if constexpr (!F::kFp8) {   // the tile's A scales
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(stg + st * F::kStage + page_scale_offset(key));
+          const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
+          tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * c), lo, lo, lo, lo, hi, hi, hi, hi);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+      }
+      // one barrier: the four warps' scales are stored, and they agree that every wait ended
       if (!named_bar_and(1, 128, ok)) {
         failed = true;
         break;
       }
-      tc_fence_after();
-      if constexpr (!F::kFp8) {   // the tile's A scales
-        const uint32_t w = *reinterpret_cast<const uint32_t*>(stg + st * F::kStage + page_scale_offset(key));
-        const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
-        tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * c), lo, lo, lo, lo, hi, hi, hi, hi);
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      named_bar_sync(1, 128);
       if (tid == 0) {
         tc_fence_after();
         const uint32_t pa = stg0 + (uint32_t)(st * F::kStage);
