@@ -38,49 +38,59 @@ cudaError_t launch_rope_table(const RopeFreqs& freqs, int half, int max_pos, flo
 }
 
 // ---------------------------------------------------------------------------- key publish
-// One CTA per key: 128 x TPO threads (TPO = 8 for a few keys, 4 for a few hundred, 1 for many).
+// Per key:
 //  1. k_pre[o] = bf16( sum_i wk[o][i] * latent[i] ): bf16*bf16 products are exact in f32,
 //     their sum is carried error-free (TwoSum) and rounded once to bf16 ("DeepSeek V4.1"
 //     index-keys page, Indexer: wk bf16 Linear). Output o's products are split over TPO
 //     consecutive threads (four accumulators each), whose parts are merged with TwoSum
-//     across the lanes; every global read is issued at entry. From step 2 on, thread
-//     o < 128 owns output dim o.
-//  2. RMSNorm in f64: y = bf16( (w[o] * k_pre[o]) * (1 / sqrt(sum(k_pre^2) / 128 + eps)) );
-//     the reciprocal square root is formed once per key.
+//     across the lanes; every global read is issued before the first is used.
+//  2. RMSNorm: y = bf16( (w[o] * k_pre[o]) * (1 / sqrt(sum(k_pre^2) / 128 + eps)) ) with the
+//     sum of squares taken exactly in 64-bit fixed point and the rest in f64; the
+//     reciprocal square root is formed once per key.
 //  3. RoPE on the last rope_dim dims at the group position: interleaved pair (2i, 2i+1)
 //     rotated by table entry i with the f32 sequence x0*c - x1*s, x0*s + x1*c, then bf16.
 //  4. e2m1/e8m0 quantisation per 32-block (warp w owns block w); the 64 code bytes and
 //     4 scale bytes go to the key's places in its 64-key page of the pool.
+// Many keys (prefill): one CTA per key. Few keys (a decode step): a cluster of kPubCl
+// CTAs per key, CTA r forming outputs [32r, 32r + 32) of step 1 and storing them into the
+// shared memory of CTA 0 of the cluster, which runs steps 2-4; step 1 is most of a key's
+// arithmetic, so a key takes four SMs' issue slots instead of one.
+constexpr int kPubCl = 4;
+constexpr int kPubClThreads = 256;   // 8 threads per output dim, kHeadDim / kPubCl dims per CTA
+
 // Warms L2 with wk (CTAs 0..3 of a launch, 32 rows each) while the kernels before run.
 __device__ __forceinline__ void prefetch_wk(const PublishArgs& a, int cta) {
   if (threadIdx.x == 0 && cta < 4) prefetch_l2_bulk(a.wk + (size_t)cta * 32 * a.Din, (uint32_t)(32 * a.Din * 2));
 }
 
-// The whole publish of key `key` by the CTA's kHeadDim * TPO threads.
-template <int TPO>
-__device__ __forceinline__ void publish_key(const PublishArgs& a, int key) {
-  constexpr int NT = kHeadDim * TPO;
-  __shared__ float lat[1024];
-  __shared__ float kx[kHeadDim];
-  __shared__ float kv[kHeadDim];
-  __shared__ double wsum[4];
-  __shared__ double rinv;
-  const int tid = threadIdx.x;
+// The key's latent row (Din * 2 bytes: a multiple of 16 at a 16-byte aligned address).
+__device__ __forceinline__ const uint16_t* key_latent(const PublishArgs& a, int key) {
+  return a.latent + (size_t)key * a.Din;   // [B][G][Din]: key = b * G + j
+}
+
+// The key's slot in the page pool and its RoPE position. False for a padding entry, and for
+// metadata outside the pool or the RoPE table (reported when `report`); the answer depends
+// on the key alone, so every CTA of a key's cluster takes the same branch.
+__device__ __forceinline__ bool key_target(const PublishArgs& a, int key, bool report, long long& slot, int& pos) {
   const int b = key / a.G, j = key % a.G;
-  // the key's slot in the page pool and its RoPE position
-  long long slot = (long long)b * a.T_cap + a.slot0 + j;
-  int pos = a.pos0 + j * a.pos_step;
-  if (a.slots != nullptr) {
-    slot = a.slots[key];
-    pos = a.positions[key];
-    if (slot < 0) return;   // a padding entry: nothing to publish
-    if (slot >= (long long)a.num_pages * kPageKeys || pos < 0 || pos >= a.max_pos) {
-      if (tid == 0) atomicOr(a.status, kStatusBadMeta);
-      return;
-    }
+  slot = (long long)b * a.T_cap + a.slot0 + j;
+  pos = a.pos0 + j * a.pos_step;
+  if (a.slots == nullptr) return true;
+  slot = a.slots[key];
+  pos = a.positions[key];
+  if (slot < 0) return false;   // a padding entry: nothing to publish
+  if (slot >= (long long)a.num_pages * kPageKeys || pos < 0 || pos >= a.max_pos) {
+    if (report && threadIdx.x == 0) atomicOr(a.status, kStatusBadMeta);
+    return false;
   }
-  const int o = tid / TPO, part = tid % TPO;
-  // every global read of the key is issued before the first is used
+  return true;
+}
+
+// Step 1 for output o by its part `part` of TPO threads (NT threads call it together: the
+// latent row is staged in `lat` by all of them). Returns k_pre[o] (in every part).
+template <int TPO, int NT>
+__device__ __forceinline__ float linear_out(const PublishArgs& a, const uint16_t* src, int o, int part, float* lat) {
+  const int tid = threadIdx.x;
   const int span = ((a.Din + 8 * TPO - 1) / (8 * TPO)) * 8;   // elements per part, a multiple of 8
   const int e_begin = part * span, e_end = min(a.Din, e_begin + span);
   const uint16_t* wrow = a.wk + (size_t)o * a.Din;
@@ -89,93 +99,159 @@ __device__ __forceinline__ void publish_key(const PublishArgs& a, int key) {
 #pragma unroll
   for (int u = 0; u < kPre; ++u)
     wpre[u] = (e_begin + 8 * u < e_end) ? *reinterpret_cast<const uint4*>(wrow + e_begin + 8 * u) : make_uint4(0, 0, 0, 0);
-  const uint32_t knorm_bits = tid < kHeadDim ? a.knorm[tid] : 0u;
-  const int rstart = kHeadDim - a.rope_dim;
-  float2 cs = make_float2(1.f, 0.f);
-  if (tid < kHeadDim && tid >= rstart)
-    cs = reinterpret_cast<const float2*>(a.rope_cs)[(size_t)pos * (a.rope_dim / 2) + ((tid - rstart) >> 1)];
-  const uint16_t* src = a.latent + ((size_t)b * a.G + j) * a.Din;
   for (int i = tid; i < a.Din; i += NT) lat[i] = bf16_to_f32(src[i]);
   __syncthreads();
 
-  // 1. exact dot product, rounded once: output o's products are split over TPO consecutive
-  //    threads, each carrying its part error-free in four (sum, error) pairs; the parts are
-  //    merged with TwoSum across the lanes
-  {
-    constexpr int kAcc = 4;
-    float s[kAcc], c[kAcc];
+  constexpr int kAcc = 4;
+  float s[kAcc], c[kAcc];
 #pragma unroll
-    for (int k = 0; k < kAcc; ++k) s[k] = c[k] = 0.f;
-    for (int e0 = e_begin; e0 < e_end; e0 += 8 * kPre) {
-      uint4 w8[kPre];
+  for (int k = 0; k < kAcc; ++k) s[k] = c[k] = 0.f;
+  for (int e0 = e_begin; e0 < e_end; e0 += 8 * kPre) {
+    uint4 w8[kPre];
 #pragma unroll
-      for (int u = 0; u < kPre; ++u)
-        w8[u] = e0 == e_begin ? wpre[u]
-                              : ((e0 + 8 * u < e_end) ? *reinterpret_cast<const uint4*>(wrow + e0 + 8 * u)
-                                                      : make_uint4(0, 0, 0, 0));
+    for (int u = 0; u < kPre; ++u)
+      w8[u] = e0 == e_begin ? wpre[u]
+                            : ((e0 + 8 * u < e_end) ? *reinterpret_cast<const uint4*>(wrow + e0 + 8 * u)
+                                                    : make_uint4(0, 0, 0, 0));
 #pragma unroll
-      for (int u = 0; u < kPre; ++u) {
-        const uint32_t ww[4] = {w8[u].x, w8[u].y, w8[u].z, w8[u].w};
-        const int eu = e0 + 8 * u;
-        if (eu < e_end) {
+    for (int u = 0; u < kPre; ++u) {
+      const uint32_t ww[4] = {w8[u].x, w8[u].y, w8[u].z, w8[u].w};
+      const int eu = e0 + 8 * u;
+      if (eu < e_end) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float p0 = __fmul_rn(bf16_to_f32(ww[k] & 0xFFFFu), lat[eu + 2 * k]);
-            const float p1 = __fmul_rn(bf16_to_f32(ww[k] >> 16), lat[eu + 2 * k + 1]);
-            float t, e;
-            two_sum(s[k], p0, t, e);
-            s[k] = t;
-            c[k] = __fadd_rn(c[k], e);
-            two_sum(s[k], p1, t, e);
-            s[k] = t;
-            c[k] = __fadd_rn(c[k], e);
-          }
+        for (int k = 0; k < 4; ++k) {
+          const float p0 = __fmul_rn(bf16_to_f32(ww[k] & 0xFFFFu), lat[eu + 2 * k]);
+          const float p1 = __fmul_rn(bf16_to_f32(ww[k] >> 16), lat[eu + 2 * k + 1]);
+          float t, e;
+          two_sum(s[k], p0, t, e);
+          s[k] = t;
+          c[k] = __fadd_rn(c[k], e);
+          two_sum(s[k], p1, t, e);
+          s[k] = t;
+          c[k] = __fadd_rn(c[k], e);
         }
       }
     }
-    float hi = s[0], lo = c[0];
-#pragma unroll
-    for (int k = 1; k < kAcc; ++k) {
-      float t, e;
-      two_sum(hi, s[k], t, e);
-      hi = t;
-      lo = __fadd_rn(__fadd_rn(lo, c[k]), e);
-    }
-#pragma unroll
-    for (int off = 1; off < TPO; off <<= 1) {
-      const float ohi = __shfl_xor_sync(0xffffffffu, hi, off), olo = __shfl_xor_sync(0xffffffffu, lo, off);
-      float t, e;
-      two_sum(hi, ohi, t, e);
-      hi = t;
-      lo = __fadd_rn(__fadd_rn(lo, olo), e);
-    }
-    {
-      float t, e;
-      two_sum(hi, lo, t, e);   // normalise: |e| <= ulp(t) / 2
-      hi = t;
-      lo = e;
-    }
-    if (part == 0) kx[o] = bf16_to_f32(f32pair_to_bf16_rne(hi, lo));
   }
-  __syncthreads();
-  if (tid >= kHeadDim) return;   // one thread per output dimension from here on
-  const int warp = tid >> 5, lane = tid & 31;
+  float hi = s[0], lo = c[0];
+#pragma unroll
+  for (int k = 1; k < kAcc; ++k) {
+    float t, e;
+    two_sum(hi, s[k], t, e);
+    hi = t;
+    lo = __fadd_rn(__fadd_rn(lo, c[k]), e);
+  }
+#pragma unroll
+  for (int off = 1; off < TPO; off <<= 1) {
+    const float ohi = __shfl_xor_sync(0xffffffffu, hi, off), olo = __shfl_xor_sync(0xffffffffu, lo, off);
+    float t, e;
+    two_sum(hi, ohi, t, e);
+    hi = t;
+    lo = __fadd_rn(__fadd_rn(lo, olo), e);
+  }
+  float t, e;
+  two_sum(hi, lo, t, e);   // normalise: |e| <= ulp(t) / 2
+  return bf16_to_f32(f32pair_to_bf16_rne(t, e));
+}
+
+// y = bf16( (w x) * (1 / sqrt(ms + eps)) ) evaluated in f64 as the RMSNorm reading states it,
+// ms = sum(k_pre^2) / 128 summed in f64 (exact when the values lie within 2^30 of each other
+// in magnitude). Slow on this part (f64 is a narrow unit): taken only where the f32 route
+// below cannot vouch for its rounding.
+__device__ __noinline__ float rmsnorm_f64(const float* kx, float wx, float eps) {
+  double ss = 0.0;
+  for (int i = 0; i < kHeadDim; ++i) ss += (double)kx[i] * (double)kx[i];
+  const double r = 1.0 / sqrt(ss / (double)kHeadDim + (double)eps);
+  return bf16_to_f32(f64_to_bf16_rne((double)wx * r));
+}
+
+// (hi, lo) <- (a_hi, a_lo) + (b_hi, b_lo), unnormalised: the high parts exactly, the low
+// parts with two roundings.
+__device__ __forceinline__ void pair_add(float& hi, float& lo, float bhi, float blo) {
+  float t, e;
+  two_sum(hi, bhi, t, e);
+  hi = t;
+  lo = __fadd_rn(__fadd_rn(lo, blo), e);
+}
+
+// Steps 2-4 by the key's 128 threads (tid = output dim; named barrier 1). kx: the key's
+// 128 k_pre values in shared memory.
+__device__ __forceinline__ void finish_key(const PublishArgs& a, long long slot, const float* kx,
+                                           uint32_t knorm_bits, float2 cs) {
+  __shared__ float wsum[2][4];
+  __shared__ int wfast[4];
+  __shared__ float kv[kHeadDim];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int rstart = kHeadDim - a.rope_dim;
   const float x = kx[tid];
 
-  // 2. RMSNorm in f64 (the squares of bf16 values are exact; the sum is exact for any
-  //    realistic dynamic range, so its order does not matter)
-  double ss = (double)x * (double)x;
+  // 2. RMSNorm. The result must be bf16 of the f64 evaluation (rmsnorm_f64). The f32 route
+  //    carries every quantity as an unevaluated pair hi + lo:
+  //    - x^2 is exact in f32 when every nonzero |x| lies in [2^-40, 2^56); the 128 squares
+  //      are summed with TwoSum (relative error below 2^-42),
+  //    - v = ms + eps; r = 1 / sqrt(v) from the f32 estimate r0 and one correction
+  //      r0 * (1 + d/2 + 3d^2/8), d = 1 - v r0^2 formed from exact products,
+  //    - P = (w x) * r with an exact product of the high part,
+  //    so P is within 2^-41 |P| of the exact value and the f64 evaluation within 2^-50 of it.
+  //    Where P lies more than 2^-38 |P| from the bf16 rounding midpoint next to it, both round
+  //    alike; otherwise (about 2^-29 of the values) and outside those ranges the f64 path runs.
+  const uint32_t xb = __float_as_uint(x) >> 16;   // x is a bf16 value
+  const uint32_t ef = (xb >> 7) & 0xFFu;
+  const bool in_range = (xb & 0x7FFFu) == 0 || (ef >= 127 - 40 && ef < 127 + 56);
+  float sh = __fmul_rn(x, x), sl = 0.f;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
-  if (lane == 0) wsum[warp] = ss;
-  named_bar_sync(1, kHeadDim);
-  if (tid == 0) {
-    const double ms = ((wsum[0] + wsum[1]) + (wsum[2] + wsum[3])) / (double)kHeadDim;
-    rinv = 1.0 / sqrt(ms + (double)a.eps);
+  for (int off = 16; off > 0; off >>= 1)
+    pair_add(sh, sl, __shfl_xor_sync(0xffffffffu, sh, off), __shfl_xor_sync(0xffffffffu, sl, off));
+  const bool warp_fast = __all_sync(0xffffffffu, in_range);
+  if (lane == 0) {
+    wsum[0][warp] = sh;
+    wsum[1][warp] = sl;
+    wfast[warp] = warp_fast;
   }
-  named_bar_sync(1, kHeadDim);
   const float wx = __fmul_rn(bf16_to_f32(knorm_bits), x);   // exact (bf16 * bf16)
-  float y = bf16_to_f32(f64_to_bf16_rne((double)wx * rinv));
+  named_bar_sync(1, kHeadDim);
+  bool slow = !(wfast[0] && wfast[1] && wfast[2] && wfast[3]);
+  float y = 0.f;
+  if (!slow) {
+    float mh = wsum[0][0], ml = wsum[1][0];
+    pair_add(mh, ml, wsum[0][1], wsum[1][1]);
+    float nh = wsum[0][2], nl = wsum[1][2];
+    pair_add(nh, nl, wsum[0][3], wsum[1][3]);
+    pair_add(mh, ml, nh, nl);
+    mh = __fmul_rn(mh, 1.f / kHeadDim);   // exact: a power of two, and ms >= 2^-87 or 0
+    ml = __fmul_rn(ml, 1.f / kHeadDim);
+    float vh, vl;
+    two_sum(mh, a.eps, vh, vl);
+    vl = __fadd_rn(vl, ml);
+    {
+      float t, e;
+      two_sum(vh, vl, t, e);
+      vh = t;
+      vl = e;
+    }
+    slow = !(vh >= 0x1p-100f && vh < 0x1p100f);
+    if (!slow && wx == 0.f) {
+      y = wx;   // (w x) * r of a signed zero, r finite
+    } else if (!slow) {
+      const float awx = fabsf(wx);
+      slow = !(awx >= 0x1p-80f && awx < 0x1p100f);
+      const float r0 = rsqrtf(vh);
+      const float p = __fmul_rn(r0, r0), pe = __fmaf_rn(r0, r0, -p);   // r0^2 = p + pe
+      const float q = __fmul_rn(vh, p), qe = __fmaf_rn(vh, p, -q);     // vh p = q + qe
+      const float d = __fsub_rn(__fsub_rn(1.f, q), __fadd_rn(qe, __fmaf_rn(vh, pe, __fmul_rn(vl, p))));
+      const float rl = __fmul_rn(r0, __fmaf_rn(0.375f, __fmul_rn(d, d), __fmul_rn(0.5f, d)));
+      const float ph = __fmul_rn(wx, r0);
+      const float pl = __fmaf_rn(wx, rl, __fmaf_rn(wx, r0, -ph));
+      float Ph, Pl;
+      two_sum(ph, pl, Ph, Pl);
+      const float aP = fabsf(Ph);
+      const float mid = __uint_as_float((__float_as_uint(Ph) & 0xFFFF0000u) | 0x8000u);
+      const float dist = __fadd_rn(__fsub_rn(Ph, mid), Pl);   // (Ph - mid is exact)
+      slow = slow || !(aP >= 0x1p-90f && aP < 0x1p120f) || fabsf(dist) <= __fmul_rn(aP, 0x1p-38f);
+      y = bf16_to_f32(f32pair_to_bf16_rne(Ph, Pl));
+    }
+  }
+  if (slow) y = rmsnorm_f64(kx, wx, a.eps);
 
   // 3. RoPE
   kv[tid] = y;
@@ -216,7 +292,58 @@ __device__ __forceinline__ void publish_key(const PublishArgs& a, int key) {
   if (lane == 0) page[page_scale_offset(m) + warp] = (uint8_t)(e + 127);
 }
 
-template <int TPO>   // threads per output dimension (1 or 4)
+// The RoPE table entry and norm weight of output dim tid (< kHeadDim) at position pos.
+__device__ __forceinline__ void key_tail_inputs(const PublishArgs& a, int pos, int tid, uint32_t& knorm_bits,
+                                                float2& cs) {
+  const int rstart = kHeadDim - a.rope_dim;
+  knorm_bits = a.knorm[tid];
+  cs = make_float2(1.f, 0.f);
+  if (tid >= rstart) cs = reinterpret_cast<const float2*>(a.rope_cs)[(size_t)pos * (a.rope_dim / 2) + ((tid - rstart) >> 1)];
+}
+
+// The whole publish of key `key` by one CTA of kHeadDim * TPO threads.
+template <int TPO>
+__device__ __forceinline__ void publish_key(const PublishArgs& a, int key) {
+  __shared__ float lat[1024];
+  __shared__ float kx[kHeadDim];
+  long long slot;
+  int pos;
+  if (!key_target(a, key, true, slot, pos)) return;
+  const int tid = threadIdx.x;
+  uint32_t knorm_bits = 0;
+  float2 cs = make_float2(1.f, 0.f);
+  if (tid < kHeadDim) key_tail_inputs(a, pos, tid, knorm_bits, cs);
+  const float v = linear_out<TPO, kHeadDim * TPO>(a, key_latent(a, key), tid / TPO, tid % TPO, lat);
+  if (tid % TPO == 0) kx[tid / TPO] = v;
+  __syncthreads();
+  if (tid >= kHeadDim) return;   // one thread per output dimension from here on
+  finish_key(a, slot, kx, knorm_bits, cs);
+}
+
+// The publish of key `key` by CTA `rank` of its cluster (kPubClThreads threads).
+__device__ __forceinline__ void publish_key_cluster(const PublishArgs& a, int key, int rank) {
+  __shared__ float lat[1024];
+  __shared__ float kx[kHeadDim];   // filled in CTA 0 by the whole cluster
+  long long slot;
+  int pos;
+  if (!key_target(a, key, rank == 0, slot, pos)) return;   // the whole cluster leaves together
+  cluster_arrive_relaxed();   // (CTA 0 must be running before its shared memory is written)
+  const int tid = threadIdx.x;
+  uint32_t knorm_bits = 0;
+  float2 cs = make_float2(1.f, 0.f);
+  if (rank == 0 && tid < kHeadDim) key_tail_inputs(a, pos, tid, knorm_bits, cs);
+  constexpr int TPO = kPubClThreads / (kHeadDim / kPubCl);
+  const int o = rank * (kHeadDim / kPubCl) + tid / TPO;
+  const float v = linear_out<TPO, kPubClThreads>(a, key_latent(a, key), o, tid % TPO, lat);
+  cluster_wait();
+  if (tid % TPO == 0) st_shared_cluster_f32(map_shared_rank(smem_u32(&kx[o]), 0), v);
+  cluster_arrive_release();
+  cluster_wait_acquire();   // CTA 0 now holds all 128 outputs
+  if (rank != 0 || tid >= kHeadDim) return;
+  finish_key(a, slot, kx, knorm_bits, cs);
+}
+
+template <int TPO>   // threads per output dimension
 __global__ void __launch_bounds__(kHeadDim * TPO) publish_kernel(PublishArgs a) {
   pdl_allow_next();
   prefetch_wk(a, blockIdx.x);
@@ -224,11 +351,21 @@ __global__ void __launch_bounds__(kHeadDim * TPO) publish_kernel(PublishArgs a) 
   publish_key<TPO>(a, blockIdx.x);
 }
 
+__global__ void __cluster_dims__(kPubCl, 1, 1) __launch_bounds__(kPubClThreads) publish_cluster_kernel(PublishArgs a) {
+  pdl_allow_next();
+  const int key = (int)blockIdx.x / kPubCl, rank = (int)blockIdx.x % kPubCl;   // 1-D clusters
+  prefetch_wk(a, blockIdx.x);
+  if (threadIdx.x == 0 && rank == 0) prefetch_l2_bulk(key_latent(a, key), (uint32_t)(a.Din * 2));
+  pdl_wait();
+  publish_key_cluster(a, key, rank);
+}
+
 cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream) {
   const long long keys = (long long)a.B * a.G;
-  // few keys (a decode step, at most about one per SM): eight threads per output dimension
-  // for the shortest chain; a few hundred: four; many keys (prefill): one, for throughput
-  if (keys <= 160) return launch_overlapped(publish_kernel<8>, dim3((unsigned)keys), dim3(8 * kHeadDim), 0, stream, a);
+  // few keys (a decode step): a cluster of four CTAs per key; a few hundred: four threads
+  // per output dimension; many keys (prefill): one, for throughput
+  if (keys <= 160)
+    return launch_overlapped(publish_cluster_kernel, dim3((unsigned)(keys * kPubCl)), dim3(kPubClThreads), 0, stream, a);
   if (keys < 512) return launch_overlapped(publish_kernel<4>, dim3((unsigned)keys), dim3(4 * kHeadDim), 0, stream, a);
   return launch_overlapped(publish_kernel<1>, dim3((unsigned)keys), dim3(kHeadDim), 0, stream, a);
 }
@@ -285,20 +422,24 @@ __global__ void __launch_bounds__(256) prep_q_kernel(PrepArgs a) {
 }
 
 // A decode step's key publish and query prep in one launch (the two are independent):
-// CTAs 0 .. n_keys-1 publish one key each (1024 threads, eight per output dimension), the
-// others prepare 64 query-head vectors each (four groups of 256 threads).
-__global__ void __launch_bounds__(8 * kHeadDim) publish_prep_kernel(PublishArgs pa, PrepArgs qa, int n_keys) {
+// CTAs 0 .. kPubCl * n_keys - 1 publish the keys (a cluster per key), the others prepare
+// 16 query-head vectors each (256 threads).
+__global__ void __cluster_dims__(kPubCl, 1, 1) __launch_bounds__(kPubClThreads)
+    publish_prep_kernel(PublishArgs pa, PrepArgs qa, int n_keys) {
+  static_assert(kPubClThreads == 256, "query prep takes 16 vectors per 256 threads");
   pdl_allow_next();
   const int cta = (int)blockIdx.x;
-  if (cta < n_keys) {
+  if (cta < n_keys * kPubCl) {   // whole clusters: n_keys * kPubCl is a multiple of the cluster size
+    const int key = cta / kPubCl, rank = cta % kPubCl;
     prefetch_wk(pa, cta);
+    if (threadIdx.x == 0 && rank == 0) prefetch_l2_bulk(key_latent(pa, key), (uint32_t)(pa.Din * 2));
     pdl_wait();
-    publish_key<8>(pa, cta);
+    publish_key_cluster(pa, key, rank);
   } else {
-    const long long v0 = (long long)(cta - n_keys) * 64 + 16 * (threadIdx.x >> 8);
-    prefetch_q16(qa, v0, threadIdx.x & 255);
+    const long long v0 = (long long)(cta - n_keys * kPubCl) * 16;
+    prefetch_q16(qa, v0, threadIdx.x);
     pdl_wait();
-    prep_q16(qa, v0, threadIdx.x & 255);
+    prep_q16(qa, v0, threadIdx.x);
   }
 }
 
@@ -308,8 +449,9 @@ cudaError_t launch_publish_prep(const PublishArgs& pa, const PrepArgs& qa, cudaS
     cudaError_t e = launch_publish(pa, stream);
     return e != cudaSuccess ? e : launch_prep_q(qa, stream);
   }
-  const long long blocks = keys + (qa.n_vec + 63) / 64;
-  return launch_overlapped(publish_prep_kernel, dim3((unsigned)blocks), dim3(8 * kHeadDim), 0, stream, pa, qa,
+  const long long prep_ctas = (qa.n_vec + 15) / 16;
+  const long long blocks = keys * kPubCl + (prep_ctas + kPubCl - 1) / kPubCl * kPubCl;   // whole clusters
+  return launch_overlapped(publish_prep_kernel, dim3((unsigned)blocks), dim3(kPubClThreads), 0, stream, pa, qa,
                            (int)keys);
 }
 
