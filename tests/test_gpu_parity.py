@@ -65,6 +65,33 @@ def test_publish_decode_slot(X):
     assert not got[:, :8191].any()
 
 
+# RMSNorm over the ranges of k_pre: keys far outside the f32 route's range (2^70 and 2^-60
+# latents take the f64 evaluation), all-zero keys, magnitudes 2^32 apart inside one key
+# (wk rows scaled 2^(o/4 - 16)), zero and negative norm weights; the cluster path (40
+# decode keys), four threads per output (200 keys) and one (600 keys).
+@pytest.mark.parametrize("B,G,start", [(40, 1, 32767), (1, 200, 0), (1, 600, 0)])
+@pytest.mark.parametrize("fmt", ["mxfp4", "fp8"])
+def test_publish_norm_ranges(X, B, G, start, fmt):
+    wl = dataclasses.replace(WORKLOADS["decode"], name="pubnorm", key_format=1 if fmt == "fp8" else 0)
+    D, n = wl.D, B * G
+    g = torch.Generator().manual_seed(4242 + G)
+    key_scale = torch.tensor([1.0, 2.0 ** 70, 2.0 ** -60, 0.0, 2.0 ** 20, 2.0 ** -30, 1e-3])[torch.arange(n) % 7]
+    lat = (torch.randn(n, D, generator=g) * key_scale[:, None]).to(torch.bfloat16).reshape(B, G, D)
+    row_scale = 2.0 ** (torch.arange(128, dtype=torch.float32) / 4.0 - 16.0)
+    wk = (torch.randn(128, D, generator=g) * row_scale[:, None]).to(torch.bfloat16)
+    knorm = torch.randn(128, generator=g).to(torch.bfloat16)
+    knorm[::7] = 0
+    T_cap = wl.T_cap if start else (G + 63) // 64 * 64
+    table = C.gpu_table(wl.max_pos)
+    cos, sin = C.oracle_table(wl.max_pos)
+    cache = X.new_key_cache(B, T_cap, key_format=wl.key_format)
+    X.indexer_publish_k(C.dims_of(wl), lat.cuda(), wk.cuda(), knorm.cuda(), table, start, cache)
+    slots, rows, _ = O.publish_keys(C.bits(lat), C.bits(wk), C.bits(knorm), cos, sin, start, wl.ratio, wl.rope_dim,
+                                    wl.norm_eps, fmt=fmt)
+    got = C.any_pages_to_rows(cache)[:, slots]
+    assert np.array_equal(got, rows), f"{np.sum(np.any(got != rows, axis=-1))} of {n} keys differ"
+
+
 # ----------------------------------------------------------------------------- query prep
 @pytest.mark.parametrize("name,B,S,H,start", [("qa", 2, 37, 64, 0), ("qb", 1, 256, 8, 0), ("qc", 32, 1, 64, 32767),
                                               ("qd", 3, 5, 16, 1000), ("qe", 2, 9, 128, 7)])
