@@ -64,6 +64,23 @@ __device__ __forceinline__ uint32_t f32_to_bf16_rne(float f) {
   return (b + 0x7FFFu + ((b >> 16) & 1u)) >> 16;
 }
 
+// Two f32 rounded to bf16 to nearest, ties to even, in one conversion: lo in bits 0-15,
+// hi in bits 16-31 (for finite inputs the same as f32_to_bf16_rne of each).
+__device__ __forceinline__ uint32_t bf16x2_rne(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// RoPE of one interleaved pair: (x0*c - x1*s, x0*s + x1*c) with f32 products and sums,
+// each rounded to bf16 (returned as f32 values).
+__device__ __forceinline__ void rope_pair_bf16(float& x0, float& x1, float2 cs) {
+  const uint32_t r = bf16x2_rne(__fsub_rn(__fmul_rn(x0, cs.x), __fmul_rn(x1, cs.y)),
+                                __fadd_rn(__fmul_rn(x0, cs.y), __fmul_rn(x1, cs.x)));
+  x0 = __uint_as_float(r << 16);
+  x1 = __uint_as_float(r & 0xFFFF0000u);
+}
+
 // Round an f64 to bf16 once (no intermediate f32), to nearest with ties to even.
 // bf16 keeps 7 explicit mantissa bits; below 2^-126 the spacing is fixed at 2^-133.
 __device__ __forceinline__ uint32_t f64_to_bf16_rne(double x) {
@@ -203,15 +220,12 @@ __device__ __forceinline__ uint32_t quant_q_slice(uint4 raw, int j, const float2
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int e0 = j * 8 + 2 * k;   // even element; rstart is even so pairs never straddle
-    if (e0 >= rstart) {
-      const float x0 = x[2 * k], x1 = x[2 * k + 1];
-      x[2 * k] = bf16_to_f32(f32_to_bf16_rne(__fsub_rn(__fmul_rn(x0, c[k].x), __fmul_rn(x1, c[k].y))));
-      x[2 * k + 1] = bf16_to_f32(f32_to_bf16_rne(__fadd_rn(__fmul_rn(x0, c[k].y), __fmul_rn(x1, c[k].x))));
-    }
+    if (e0 >= rstart) rope_pair_bf16(x[2 * k], x[2 * k + 1], c[k]);
   }
-  uint32_t amax = 0;
+  float am = 0.f;   // the largest |x| (bf16 values), as bf16 bits
 #pragma unroll
-  for (int k = 0; k < 8; ++k) amax = max(amax, (__float_as_uint(x[k]) >> 16) & 0x7FFFu);
+  for (int k = 0; k < 8; ++k) am = fmaxf(am, fabsf(x[k]));
+  uint32_t amax = __float_as_uint(am) >> 16;
   amax = max(amax, __shfl_xor_sync(gmask, amax, 1));
   amax = max(amax, __shfl_xor_sync(gmask, amax, 2));
   const int ex = e8m0_exponent(amax);
@@ -239,15 +253,12 @@ __device__ __forceinline__ uint2 quant_q_slice_fp8(uint4 raw, int j, const float
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int e0 = j * 8 + 2 * k;
-    if (e0 >= rstart) {
-      const float x0 = x[2 * k], x1 = x[2 * k + 1];
-      x[2 * k] = bf16_to_f32(f32_to_bf16_rne(__fsub_rn(__fmul_rn(x0, c[k].x), __fmul_rn(x1, c[k].y))));
-      x[2 * k + 1] = bf16_to_f32(f32_to_bf16_rne(__fadd_rn(__fmul_rn(x0, c[k].y), __fmul_rn(x1, c[k].x))));
-    }
+    if (e0 >= rstart) rope_pair_bf16(x[2 * k], x[2 * k + 1], c[k]);
   }
-  uint32_t amax = 0;
+  float am = 0.f;   // the largest |x| (bf16 values), as bf16 bits
 #pragma unroll
-  for (int k = 0; k < 8; ++k) amax = max(amax, (__float_as_uint(x[k]) >> 16) & 0x7FFFu);
+  for (int k = 0; k < 8; ++k) am = fmaxf(am, fabsf(x[k]));
+  uint32_t amax = __float_as_uint(am) >> 16;
 #pragma unroll
   for (int off = 1; off < 16; off <<= 1) amax = max(amax, __shfl_xor_sync(gmask, amax, off));
   const int ex = fp8_exponent(amax);

@@ -393,7 +393,7 @@ __device__ __forceinline__ void prep_q16(const PrepArgs& a, long long v0, int t)
   const int lane = tid & 31;
   const unsigned gmask = 0xFFFFu << (lane & 16);
   const int qrow = (int)(v >> a.h_shift);   // H is a power of two
-  const int pos = a.rows ? a.rows[qrow].pos : a.start_pos + qrow % a.S;
+  const int pos = a.rows ? a.rows[qrow].pos : a.start_pos + (a.S == 1 ? 0 : qrow % a.S);
   const uint4 raw = *reinterpret_cast<const uint4*>(a.q + v * kHeadDim + j * 8);
   float2 c[4];
   load_rope_slice(reinterpret_cast<const float2*>(a.rope_cs) + (size_t)pos * (a.rope_dim / 2), j, a.rope_dim, c);
@@ -495,13 +495,18 @@ __global__ void __launch_bounds__(256) prep_q_bulk_kernel(PrepArgs a) {
   const int g = tid >> 4, j = tid & 15;
   const int lane = tid & 31;
   const unsigned gmask = 0xFFFFu << (lane & 16);
+  // the batch's first query row and its index in its sequence (one division per CTA; the
+  // batch's rows follow it, wrapping at S)
+  const int qrow0 = (int)(v0 >> a.h_shift);   // H is a power of two
+  const int s0 = a.rows ? 0 : qrow0 % a.S;
 #pragma unroll
   for (int p = 0; p < NV / 16; ++p) {
     const int vi = 16 * p + g;
     if (vi < nv) {   // the 16 lanes of a group agree
       const long long v = v0 + vi;
-      const int qrow = (int)(v >> a.h_shift);   // H is a power of two
-      const int pos = a.rows ? a.rows[qrow].pos : a.start_pos + qrow % a.S;
+      const int qrow = (int)(v >> a.h_shift);
+      const int srow_ = s0 + (qrow - qrow0);
+      const int pos = a.rows ? a.rows[qrow].pos : a.start_pos + (srow_ < a.S ? srow_ : srow_ % a.S);
       float2 c[4];
       load_rope_slice(reinterpret_cast<const float2*>(a.rope_cs) + (size_t)pos * (a.rope_dim / 2), j, a.rope_dim, c);
       const uint4 raw = *reinterpret_cast<const uint4*>(sq + vi * kHeadDim + j * 8);

@@ -93,8 +93,10 @@ def test_publish_norm_ranges(X, B, G, start, fmt):
 
 
 # ----------------------------------------------------------------------------- query prep
+# qf: 80040 vectors, the bulk-copy kernel (above 16384 vectors; 64 vectors per CTA) with a
+# ragged last batch of 40
 @pytest.mark.parametrize("name,B,S,H,start", [("qa", 2, 37, 64, 0), ("qb", 1, 256, 8, 0), ("qc", 32, 1, 64, 32767),
-                                              ("qd", 3, 5, 16, 1000), ("qe", 2, 9, 128, 7)])
+                                              ("qd", 3, 5, 16, 1000), ("qe", 2, 9, 128, 7), ("qf", 5, 2001, 8, 3)])
 def test_prep_q_bit_exact(X, name, B, S, H, start):
     wl = dataclasses.replace(WORKLOADS["prefill"], name=name, B=B, S=S, H=H, start_pos=start)
     table = C.gpu_table(wl.max_pos)
