@@ -160,13 +160,12 @@ __device__ __forceinline__ uint32_t e4m3x2(float x0, float x1) {
 }
 
 // Two e2m1 codes in one byte: x0 -> low nibble, x1 -> high nibble; round to nearest
-// even on the e2m1 grid (hardware conversion); the sign bits are forced to the signs
-// of the inputs so that negative values rounding to zero keep their sign.
+// even on the e2m1 grid (hardware conversion). The conversion keeps the sign of a
+// negative value that rounds to zero (code 0x8; checked on the GPU for -0, -1e-30, -0.1
+// and the tie -0.25), as the quantiser's sign rule asks.
 __device__ __forceinline__ uint32_t e2m1x2(float x0, float x1) {
   uint32_t r;
   asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }" : "=r"(r) : "f"(x1), "f"(x0));
-  r |= (__float_as_uint(x0) >> 28) & 0x8u;
-  r |= (__float_as_uint(x1) >> 24) & 0x80u;
   return r;
 }
 

@@ -231,6 +231,32 @@ def test_paged_bad_metadata_is_reported(X):
     assert e.value.code == -4
 
 
+def test_paged_publish_few_keys_with_padding(X):
+    """A decode-sized slot mapping (40 entries, the cluster-per-key publish) with padding
+    entries (-1) interleaved: every real key lands at its slot bit-exact, and no other row of
+    the pool is written."""
+    m = MIXED["mixed_small"]
+    d = _dims(X, m)
+    table = C.gpu_table(m.max_pos)
+    cos, sin = C.oracle_table(m.max_pos)
+    n = 40
+    slots = torch.arange(n, dtype=torch.int32) * 3 + 130   # spread over pages 2 .. 3
+    slots[::5] = -1
+    pos = torch.arange(n, dtype=torch.int32) * m.ratio
+    pool = X.new_key_pool(m.num_pages)
+    ws = _status_ws(X)
+    X.indexer_publish_k_paged(d, m.latent(0)[:n].cuda(), m.wk("cuda"), m.k_norm_w("cuda"), table, pos.cuda(),
+                              slots.cuda(), pool, ws)
+    X.indexer_status(ws)
+    got = C.pages_to_rows(pool)
+    ref = _oracle_keys(m, 0, cos, sin)[:n]
+    real = slots >= 0
+    assert np.array_equal(got[slots[real].numpy()], ref[real.numpy()])
+    untouched = np.ones(got.shape[0], dtype=bool)
+    untouched[slots[real].numpy()] = False
+    assert not got[untouched].any()
+
+
 def test_paged_unowned_rows_are_empty(X):
     """Rows past q_start[n_seq] belong to no sequence: all -1, and the owned rows are
     unaffected."""
