@@ -172,6 +172,29 @@ int indexer_prep_q(const IndexerDims* dims, const indexer_bf16* q, const indexer
                    indexer_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * indexer_prep_q_proj -- the query projection fused with query prep ([index-keys]
+ * Indexer.forward: q = wq_b(qr) unflattened to [H][128], then the same RoPE and
+ * fp4_act_quant as indexer_prep_q; weights_proj output scaled as there). Reading: wq_b
+ * is a bf16 Linear (no bias); its output is the f32 tensor-core accumulation of the
+ * exact bf16 products, rounded once to bf16 (the order of the f32 sums is the
+ * hardware's, so a q value can differ from the exactly rounded sum by one bf16 unit where
+ * the sum lies within f32 rounding of a bf16 midpoint); the quantised rows are those of
+ * that q. The bf16 q never goes through global memory unless q_out is given.
+ *   qr:      bf16 [B][S][Kq] (Kq = q_lora_rank, a multiple of 64 in [64, 16384]), 16-byte
+ *            aligned
+ *   wq_b:    bf16 [H * 128][Kq] (row o produces feature o = head * 128 + dim), 16-byte aligned
+ *   w:       bf16 [B][S][H] (weights_proj output)
+ *   q_rows:  uint8 [B][S][H][68], 16-byte aligned; w_prime: float [B][S][H]
+ *   q_out:   bf16 [B][S][H][128] (the projection before RoPE, for checks) or NULL
+ *   ws/ws_bytes: status word (INDEXER_STATUS_BYTES), initialised by indexer_workspace_init
+ * MXFP4 query rows only (INDEXER_ERR_DIMS for key_format FP8); n_heads even.
+ * ------------------------------------------------------------------------- */
+int indexer_prep_q_proj(const IndexerDims* dims, const indexer_bf16* qr, int Kq, const indexer_bf16* wq_b,
+                        const indexer_bf16* w, int B, int S, int start_pos, const float* rope_cs, int max_pos,
+                        uint8_t* q_rows, float* w_prime, indexer_bf16* q_out, void* ws, size_t ws_bytes,
+                        indexer_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * indexer_scores -- index scores of prepared queries against the key cache
  * ([index-keys] Indexer.forward: einsum("bshd,btd->bsht"), relu, * weights,
  * sum over heads; causal mask t >= vis(s) -> -inf; level two: -inf outside the

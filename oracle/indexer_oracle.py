@@ -15,7 +15,7 @@ __all__ = [
     "FP4_BLOCK", "E2M1_GRID", "KEY_ROW_BYTES", "SCALE_FLOOR", "key_row_bytes", "f32_to_bf16",
     "bf16_to_f64", "f64_to_bf16", "yarn_freqs_cis", "linear_bf16", "rmsnorm_bf16",
     "rope_interleaved", "fp4_quant_e8m0", "pack_row68", "unpack_row68", "dequant_row68",
-    "key_slots", "publish_keys", "prep_queries", "visible_lens", "index_scores",
+    "key_slots", "publish_keys", "project_queries", "prep_queries", "visible_lens", "index_scores",
     "select_candidate_blocks", "candidate_mask", "topk_positions", "forward",
     "FP8_BLOCK", "E4M3_GRID", "FP8_SCALE_FLOOR", "FP8_ROW_BYTES", "fp8_quant_ue8m0", "pack_row132",
     "dequant_row132", "dequant_row", "quantise_rows",
@@ -325,6 +325,15 @@ def publish_keys(latent_bits, wk_bits, knorm_bits, cos, sin, start_pos: int, rat
     k = rmsnorm_bf16(k, knorm_bits, eps)
     k = rope_interleaved(k, cos, sin, positions[None, :], rope_dim)
     return slots, quantise_rows(k, fmt), k
+
+
+def project_queries(qr_bits: np.ndarray, wq_b_bits: np.ndarray, n_heads: int) -> np.ndarray:
+    """q = wq_b(qr) unflattened to [..., n_heads, 128] (index-keys page, Indexer.forward:
+    self.wq_b(qr).unflatten(-1, (n_local_heads, index_head_dim))). Reading: wq_b is a bf16
+    Linear with no bias, its sum taken exactly and rounded once to bf16 (linear_bf16).
+    qr_bits [..., Kq]; wq_b_bits [n_heads * 128, Kq]."""
+    q = linear_bf16(qr_bits, wq_b_bits)
+    return q.reshape(*q.shape[:-1], n_heads, q.shape[-1] // n_heads)
 
 
 def prep_queries(q_bits, w_bits, cos, sin, start_pos: int, rope_dim: int, n_heads: int,

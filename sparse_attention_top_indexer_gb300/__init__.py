@@ -19,7 +19,7 @@ __all__ = [
     "PAGE_BYTES", "KEY_MXFP4", "KEY_FP8", "ROW_BYTES_FP8", "PAGE_BYTES_FP8", "row_bytes", "page_bytes",
     "new_key_cache", "new_key_pool", "indexer_publish_k_paged", "indexer_forward_paged",
     "indexer_workspace_size_paged", "indexer_forward_publish",
-    "indexer_rope_table", "indexer_publish_k", "indexer_prep_q", "indexer_scores",
+    "indexer_rope_table", "indexer_publish_k", "indexer_prep_q", "indexer_prep_q_proj", "indexer_scores",
     "indexer_select_candidate_blocks", "indexer_topk", "indexer_forward", "indexer_workspace_size",
     "indexer_workspace_init", "indexer_status", "indexer_abi_version", "make_dims", "indexer_forward_noalloc",
     "NOALLOC_SCRATCH_BYTES",
@@ -67,6 +67,8 @@ _SIGS = {
     "indexer_rope_table": [ctypes.POINTER(IndexerYarn), _I, _I, _P, _P],
     "indexer_publish_k": [ctypes.POINTER(IndexerDims), _P, _I, _I, _I, _P, _P, _P, _I, _I, _P, _I, _P],
     "indexer_prep_q": [ctypes.POINTER(IndexerDims), _P, _P, _I, _I, _I, _P, _I, _P, _P, _P],
+    "indexer_prep_q_proj": [ctypes.POINTER(IndexerDims), _P, _I, _P, _P, _I, _I, _I, _P, _I, _P, _P, _P, _P,
+                            ctypes.c_size_t, _P],
     "indexer_scores": [ctypes.POINTER(IndexerDims), _P, _P, _I, _I, _I, _P, _I, _P, _P, _P, ctypes.c_size_t, _P],
     "indexer_select_candidate_blocks": [ctypes.POINTER(IndexerDims), _P, _I, _I, _I, _I, _P, _P],
     "indexer_topk": [ctypes.POINTER(IndexerDims), _P, _I, _I, _I, _I, _P, _P],
@@ -208,6 +210,20 @@ def indexer_prep_q(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor, start_po
         ctypes.byref(dims), _ptr(q, torch.bfloat16, "q"), _ptr(w, torch.bfloat16, "w"), B, S, start_pos,
         _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(q_rows, torch.uint8, "q_rows"),
         _ptr(w_prime, torch.float32, "w_prime"), _stream(stream)))
+
+
+def indexer_prep_q_proj(dims: IndexerDims, qr: torch.Tensor, wq_b: torch.Tensor, w: torch.Tensor, start_pos: int,
+                        rope_cs: torch.Tensor, q_rows: torch.Tensor, w_prime: torch.Tensor, ws: torch.Tensor,
+                        q_out: Optional[torch.Tensor] = None, stream=None):
+    """qr bf16 [B, S, Kq]; wq_b bf16 [H * 128, Kq]; w bf16 [B, S, H]; q_rows uint8 [B, S, H, 68];
+    w_prime f32 [B, S, H]; ws the status workspace; q_out bf16 [B, S, H, 128] or None."""
+    B, S, Kq = qr.shape
+    _check(load_library().indexer_prep_q_proj(
+        ctypes.byref(dims), _ptr(qr, torch.bfloat16, "qr"), Kq, _ptr(wq_b, torch.bfloat16, "wq_b"),
+        _ptr(w, torch.bfloat16, "w"), B, S, start_pos, _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0],
+        _ptr(q_rows, torch.uint8, "q_rows"), _ptr(w_prime, torch.float32, "w_prime"),
+        _ptr(q_out, torch.bfloat16, "q_out"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
+        _stream(stream)))
 
 
 def indexer_scores(dims: IndexerDims, q_rows: torch.Tensor, w_prime: torch.Tensor, start_pos: int,

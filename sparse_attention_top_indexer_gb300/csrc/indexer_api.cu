@@ -157,7 +157,7 @@ extern "C" {
 
 const char* indexer_last_error(void) { return g_last_error.c_str(); }
 
-int indexer_abi_version(void) { return 400; }
+int indexer_abi_version(void) { return 401; }
 
 // ---------------------------------------------------------------------------- RoPE table
 int indexer_rope_table(const IndexerYarn* y, int rope_dim, int max_pos, float* table, indexer_stream_t stream) {
@@ -318,6 +318,44 @@ int indexer_prep_q(const IndexerDims* dims, const indexer_bf16* q, const indexer
     return fail(INDEXER_ERR_ALIGN, "q_rows must be 16-byte aligned and w_prime 4-byte aligned");
   RETURN_IF(check_arch());
   RETURN_IF(prep_q_checked(dims, q, w, B, S, start_pos, rope_cs, q_rows, w_prime, (cudaStream_t)stream));
+  return ok();
+}
+
+// ---------------------------------------------------------------------------- fused query projection
+int indexer_prep_q_proj(const IndexerDims* dims, const indexer_bf16* qr, int Kq, const indexer_bf16* wq_b,
+                        const indexer_bf16* w, int B, int S, int start_pos, const float* rope_cs, int max_pos,
+                        uint8_t* q_rows, float* w_prime, indexer_bf16* q_out, void* ws, size_t ws_bytes,
+                        indexer_stream_t stream) {
+  RETURN_IF(check_prep_args(dims, qr, w, B, S, start_pos, rope_cs, max_pos));
+  if (is_fp8(dims)) return fail(INDEXER_ERR_DIMS, "the fused query projection writes MXFP4 query rows only");
+  if (Kq < 64 || Kq > 16384 || (Kq % 64))
+    return fail(INDEXER_ERR_DIMS, "Kq (q_lora_rank) must be a multiple of 64 in [64, 16384] (got %d)", Kq);
+  if (dims->n_heads % 2) return fail(INDEXER_ERR_DIMS, "the fused query projection takes an even n_heads");
+  if (!wq_b || !q_rows || !w_prime || !ws) return fail(INDEXER_ERR_NULL, "wq_b, q_rows, w_prime and ws must not be NULL");
+  if (!aligned(wq_b, 16) || !aligned(q_rows, 16) || !aligned(w_prime, 4) || !aligned(ws, 16) ||
+      (q_out && !aligned(q_out, 16)))
+    return fail(INDEXER_ERR_ALIGN, "qr, wq_b, q_rows, q_out and ws must be 16-byte aligned, w_prime 4-byte aligned");
+  if (ws_bytes < INDEXER_STATUS_BYTES) return fail(INDEXER_ERR_WORKSPACE, "ws needs %d bytes", INDEXER_STATUS_BYTES);
+  if ((long long)B * S > (1ll << 30)) return fail(INDEXER_ERR_DIMS, "B * S is too large");
+  RETURN_IF(check_arch());
+  QprojArgs a{};
+  a.qr = qr;
+  a.wq_b = wq_b;
+  a.w = w;
+  a.rope_cs = rope_cs;
+  a.q_rows = q_rows;
+  a.w_prime = w_prime;
+  a.q_out = q_out;
+  a.status = static_cast<uint32_t*>(ws);
+  a.R = B * S;
+  a.Kq = Kq;
+  a.H = dims->n_heads;
+  a.S = S;
+  a.start_pos = start_pos;
+  a.rope_dim = dims->rope_dim;
+  a.w_scale = make_prep_args(dims, qr, w, B, S, start_pos, rope_cs, q_rows, w_prime, nullptr).w_scale;
+  const cudaError_t e = launch_qproj(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "query projection launch");
   return ok();
 }
 

@@ -59,6 +59,22 @@ struct PublishArgs {
 };
 cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream);
 
+// The query projection q = bf16(qr wq_b^T) with RoPE and the MXFP4 quantiser in its epilogue
+// (the query prep of a uniform batch of R = B * S rows, row r at position start_pos + r % S).
+struct QprojArgs {
+  const uint16_t* qr;       // [R][Kq] bf16
+  const uint16_t* wq_b;     // [H * 128][Kq] bf16 (row o produces feature o = head * 128 + dim)
+  const uint16_t* w;        // [R][H] bf16
+  const float* rope_cs;     // [max_pos][rd/2][2]
+  uint8_t* q_rows;          // [R][H][68]
+  float* w_prime;           // [R][H]
+  uint16_t* q_out = nullptr;     // [R][H * 128] bf16 (the projection before RoPE), or nullptr
+  uint32_t* status = nullptr;
+  int R, Kq, H, S, start_pos, rope_dim;
+  float w_scale;
+};
+cudaError_t launch_qproj(const QprojArgs& a, cudaStream_t stream);
+
 // Per-row metadata of a batch of sequences with their own start positions and query-row
 // counts, built on the device by the plan kernel.
 struct alignas(16) RowInfo {

@@ -42,7 +42,7 @@ def test_struct_layouts_match_header(X):
 
 
 def test_abi_version(X):
-    assert X.indexer_abi_version() == 400   # key_format field: MXFP4 or FP8 rows
+    assert X.indexer_abi_version() == 401   # + indexer_prep_q_proj (the fused query projection)
 
 
 def test_workspace_size_host_only(X):

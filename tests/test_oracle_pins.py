@@ -275,6 +275,19 @@ def test_linear_is_correctly_rounded_exact_sum():
             assert _frac_of_bits(y[i, o]) == _round_frac_bf16(exact)
 
 
+def test_query_projection_unflattens_feature_h_times_128_plus_d():
+    """q = wq_b(qr) unflattened to [H][128]: feature o = h * 128 + d, each the correctly
+    rounded exact sum (checked by brute force with fractions on a tiny case)."""
+    qr = _rand_bf16((2, 3, 64))
+    wq = _rand_bf16((2 * 128, 64), scale=64 ** -0.5)
+    q = O.project_queries(qr, wq, 2)
+    assert q.shape == (2, 3, 2, 128)
+    for b, s, h, dd in [(0, 0, 0, 0), (0, 2, 1, 5), (1, 1, 0, 127), (1, 2, 1, 64), (0, 1, 1, 100)]:
+        o = h * 128 + dd
+        exact = sum(_frac_of_bits(qr[b, s, j]) * _frac_of_bits(wq[o, j]) for j in range(64))
+        assert _frac_of_bits(q[b, s, h, dd]) == _round_frac_bf16(exact)
+
+
 def test_rmsnorm_against_high_precision():
     from decimal import Decimal, getcontext
     getcontext().prec = 60

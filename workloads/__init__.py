@@ -158,6 +158,7 @@ class Workload:
     norm_eps: float = 1e-6
     seed: int = 0
     key_format: int = 0       # 0: MXFP4 rows (68 bytes), 1: FP8 rows (132 bytes)
+    q_lora_rank: int = 1280   # K of the query projection wq_b (qr -> H * 128)
 
     @property
     def end_pos(self) -> int:
@@ -196,6 +197,15 @@ class Workload:
         per = self.H * self.D
         return torch.stack([normal_bf16_flat(sid, r * per, per, device=device).view(self.H, self.D)
                             for r in rows])
+
+    def qr(self, device="cpu", tag: str = "qr") -> torch.Tensor:
+        """The query latent fed to wq_b, [B, S, q_lora_rank] (unit normal)."""
+        return normal_bf16(self.seed, f"{self.name}/{tag}", (self.B, self.S, self.q_lora_rank), device=device)
+
+    def wq_b(self, device="cpu") -> torch.Tensor:
+        """wq_b [H * 128, q_lora_rank], normal with std q_lora_rank^-0.5, so q has unit scale."""
+        return normal_bf16(self.seed, f"{self.name}/wq_b", (self.H * self.D, self.q_lora_rank),
+                           std=self.q_lora_rank ** -0.5, device=device)
 
     def w(self, device="cpu", tag: str = "w") -> torch.Tensor:
         w = normal_bf16(self.seed, f"{self.name}/{tag}", (self.B, self.S, self.H), device=device)
