@@ -5,23 +5,20 @@
 // through HBM.
 //
 // One persistent CTA per SM takes output tiles of 128 query rows x 256 features (two heads):
-//   * warps 0-3 (producers) copy the K-chunks of 64 of qr (A, 128 x 64) and wq_b (B,
-//     256 x 64) with 16-byte cp.async into the no-swizzle K-major core-matrix layout (8 rows
-//     x 16 bytes per core matrix, 128 B apart along K, 1024 B apart along M/N), four stages
-//     deep; before it waits for a stage to be released, each thread signals the "full"
-//     barrier of the chunk it issued two chunks earlier (its own copies of it have landed;
-//     then a proxy fence), so a chunk's MMAs never wait on the completion of the chunk
-//     before them;
-//   * warp 4 (MMA) issues four tcgen05.mma.kind::f16 (bf16 x bf16 -> f32, M 128, N 256,
-//     K 16) per stage into one of two accumulators (2 x 256 tensor-memory columns) and
-//     commits the stage back to the producers and, after the last chunk, the accumulator to
-//     the epilogue;
-//   * warps 5-8 (epilogue): thread m owns query row m0 + m (tensor-memory lane m) and takes
+//   * warp 0 (producer): one thread loads each K-chunk of 64 of qr (A, 128 x 64) and wq_b
+//     (B, 256 x 64) with two tensor-map copies (cp.async.bulk.tensor, 128-byte swizzle; rows
+//     past R are zero-filled by the copy) into a four-stage ring;
+//   * warp 1 (MMA): four tcgen05.mma.kind::f16 (bf16 x bf16 -> f32, M 128, N 256, K 16, both
+//     operands K-major with the 128-byte swizzle) per stage into one of two accumulators
+//     (2 x 256 tensor-memory columns); each stage is committed back to the producer and,
+//     after the last chunk, the accumulator to the epilogue;
+//   * warps 2-5 (epilogue): thread m owns query row m0 + m (tensor-memory lane m) and takes
 //     its two heads a 32-column block at a time: the accumulator rounded to bf16 (q as the
 //     Linear's bf16 output; optionally stored for parity checks), RoPE on the rope blocks
 //     with the same f32 rotation as the query-prep kernels, the block's e8m0 scale and
 //     e2m1 codes; then w' = w * head_dim^-0.5 * H^-0.5 for the row's two heads.
 // Every wait on an mbarrier is bounded; a role that gives up reports through the status word.
+#include <cuda.h>   // CUtensorMap and its enums (the encoder comes through the runtime)
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
@@ -33,36 +30,40 @@ namespace {
 
 constexpr int kQpM = 128;                 // query rows per tile
 constexpr int kQpN = 256;                 // output features per tile (two heads)
-constexpr int kQpK = 64;                  // K per stage
+constexpr int kQpK = 64;                  // K per stage: 128 bytes of bf16, one swizzle row
 constexpr int kQpStages = 4;
-constexpr int kQpLag = 2;                 // chunks between a chunk's copies and its "full" signal
 constexpr int kQpAStage = kQpM * kQpK * 2;            // 16 KB
 constexpr int kQpBStage = kQpN * kQpK * 2;            // 32 KB
 constexpr int kQpStage = kQpAStage + kQpBStage;
-constexpr int kQpPieces = (kQpM + kQpN) * kQpK * 2 / 16;   // 16-byte copies per stage
-constexpr int kQpProducers = 128;
-constexpr int kQpThreads = kQpProducers + 32 + 128;
-constexpr int kQpMmaWarp = 4;
+constexpr int kQpThreads = 32 + 32 + 128;
 constexpr int kQpNBar = 2 * kQpStages + 4;          // full, empty per stage; acc full, acc empty
 constexpr int kQpSmem = 1024 + kQpStages * kQpStage + kQpNBar * 8 + 16;
-static_assert(kQpPieces % kQpProducers == 0, "whole copies per producer thread");
-static_assert(kQpLag >= 1 && kQpLag < kQpStages, "a chunk is handed over before its stage comes round again");
+static_assert(kQpAStage % 1024 == 0 && kQpStage % 1024 == 0, "swizzled tiles start on 1024-byte boundaries");
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+struct QprojParams {
+  CUtensorMap map_a;   // qr: [R][Kq] bf16, boxes of 64 x 128, 128-byte swizzle
+  CUtensorMap map_b;   // wq_b: [H * 128][Kq] bf16, boxes of 64 x 256, 128-byte swizzle
+  QprojArgs a;
+};
 
-// Offset of the 16-byte piece (row r, K group g) of a K-major no-swizzle tile.
-__device__ __forceinline__ uint32_t core_offset(int r, int g) {
-  return (uint32_t)((r >> 3) * 1024 + g * 128 + (r & 7) * 16);
+// 2-D tensor-map copy of the box at (x, y) into shared memory, completing bytes on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
 }
 
-__global__ void __launch_bounds__(kQpThreads, 1) qproj_prep_kernel(const QprojArgs a) {
+// Shared-memory matrix descriptor, K-major with the 128-byte swizzle: rows of 128 bytes, 8-row
+// groups 1024 bytes apart (the layout a 128-byte-swizzled tensor-map copy writes at a
+// 1024-byte aligned address); bits 46-48 hold 0b001, layout type 2 in bits 61-63. The K
+// steps of 16 elements inside a row advance the start address by 32 bytes.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
+}
+
+__global__ void __launch_bounds__(kQpThreads, 1) qproj_prep_kernel(const __grid_constant__ QprojParams prm) {
+  const QprojArgs& a = prm.a;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -75,11 +76,8 @@ __global__ void __launch_bounds__(kQpThreads, 1) qproj_prep_kernel(const QprojAr
   auto bar_accfull = [&](int x) { return bar0 + 8u * (uint32_t)(2 * kQpStages + x); };
   auto bar_accempty = [&](int x) { return bar0 + 8u * (uint32_t)(2 * kQpStages + 2 + x); };
   if (warp == 0) {
-    if (lane < kQpNBar) {
-      // a stage is full once all producer threads' copies of it have landed; an accumulator
-      // is free once the 128 epilogue threads have read it
-      const bool by_threads = lane < kQpStages || lane >= 2 * kQpStages + 2;
-      mbar_init(bar0 + 8u * (uint32_t)lane, by_threads ? 128u : 1u);
+    if (lane < kQpNBar) {   // an accumulator is free once the 128 epilogue threads have read it
+      mbar_init(bar0 + 8u * (uint32_t)lane, lane >= 2 * kQpStages + 2 ? 128u : 1u);
     }
     fence_mbar_init();
   } else if (warp == 1) {
@@ -96,44 +94,33 @@ __global__ void __launch_bounds__(kQpThreads, 1) qproj_prep_kernel(const QprojAr
   bool failed = false;
   pdl_wait();   // qr, wq_b and w may come from the kernels before
 
-  if (warp < kQpMmaWarp) {
-    // ------------------------------------------------------------ producers
-    uint32_t g = 0;   // stages filled so far
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t g = 0;   // chunks issued
     for (int t = blockIdx.x; t < n_tiles && !failed; t += gridDim.x) {
       const int m0 = (t / tiles_n) * kQpM, n0 = (t % tiles_n) * kQpN;
       for (int c = 0; c < kchunks; ++c, ++g) {
         const int st = (int)(g % kQpStages);
-        if (g >= (uint32_t)kQpLag) {   // chunk g - kQpLag has landed: hand it to the MMA warp
-          cp_async_wait<kQpLag - 1>();
-          fence_proxy_async_smem();
-          mbar_arrive(bar_full((int)((g - kQpLag) % kQpStages)));
-        }
         // the stage's previous chunk has been read by its MMAs (whose commit completes it)
         if (g >= (uint32_t)kQpStages && !warp_wait_bounded(bar_empty(st), ((g / kQpStages) - 1) & 1u)) {
           failed = true;
           break;
         }
-        const uint32_t sa = stg0 + (uint32_t)(st * kQpStage), sb = sa + kQpAStage;
-#pragma unroll 4
-        for (int u = 0; u < kQpPieces / kQpProducers; ++u) {
-          const int p = tid + kQpProducers * u;
-          if (p < kQpM * 8) {   // qr rows m0.., rows past R read nothing (zero-filled)
-            const int r = p >> 3, gk = p & 7, row = m0 + r;
-            const bool live = row < a.R;
-            const uint16_t* src = a.qr + (size_t)(live ? row : 0) * a.Kq + c * kQpK + gk * 8;
-            cp_async16(sa + core_offset(r, gk), src, live ? 16u : 0u);
-          } else {              // wq_b rows n0 .. n0 + 255 (H * 128 is a multiple of 256)
-            const int q = p - kQpM * 8, r = q >> 3, gk = q & 7;
-            cp_async16(sb + core_offset(r, gk), a.wq_b + (size_t)(n0 + r) * a.Kq + c * kQpK + gk * 8, 16u);
-          }
+        if (lane == 0) {
+          const uint32_t sa = stg0 + (uint32_t)(st * kQpStage);
+          mbar_arrive_expect_tx(bar_full(st), (uint32_t)kQpStage);
+          tma_load_2d(sa, &prm.map_a, c * kQpK, m0, bar_full(st));
+          tma_load_2d(sa + kQpAStage, &prm.map_b, c * kQpK, n0, bar_full(st));
         }
-        cp_async_commit();
+        __syncwarp();
       }
     }
-    cp_async_wait<0>();   // no copy stays in flight past this point
-    fence_proxy_async_smem();
-    for (uint32_t d = g >= (uint32_t)kQpLag ? g - kQpLag : 0u; d < g; ++d) mbar_arrive(bar_full((int)(d % kQpStages)));
-  } else if (warp == kQpMmaWarp) {
+    // no copy stays in flight past the final barrier: wait (bounded) for the last stages
+    if (lane == 0)
+      for (uint32_t d = g > (uint32_t)kQpStages ? g - kQpStages : 0u; d < g; ++d)
+        mbar_wait(bar_full((int)(d % kQpStages)), (d / kQpStages) & 1u);
+    __syncwarp();
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA warp
     const uint32_t idesc = idesc_bf16(kQpM, kQpN);
     uint32_t g = 0;
@@ -155,9 +142,9 @@ __global__ void __launch_bounds__(kQpThreads, 1) qproj_prep_kernel(const QprojAr
           tc_fence_after();
           const uint32_t sa = stg0 + (uint32_t)(st * kQpStage), sb = sa + kQpAStage;
 #pragma unroll
-          for (int kk = 0; kk < kQpK / 16; ++kk)   // K 16 per MMA: two core matrices along K
-            mma_bf16(tmem + (uint32_t)(acc * kQpN), smem_desc(sa + 256 * kk, 128, 1024),
-                     smem_desc(sb + 256 * kk, 128, 1024), idesc, (c | kk) != 0 ? 1u : 0u);
+          for (int kk = 0; kk < kQpK / 16; ++kk)   // K 16 per MMA: 32 bytes along the swizzled row
+            mma_bf16(tmem + (uint32_t)(acc * kQpN), smem_desc_sw128(sa + 32 * kk), smem_desc_sw128(sb + 32 * kk),
+                     idesc, (c | kk) != 0 ? 1u : 0u);
           tc_commit(bar_empty(st));
           if (c == kchunks - 1) tc_commit(bar_accfull(acc));
         }
@@ -246,25 +233,55 @@ __global__ void __launch_bounds__(kQpThreads, 1) qproj_prep_kernel(const QprojAr
   }
   __syncwarp();
   if (failed && lane == 0 && a.status) atomicOr(a.status, kStatusLoadTimeout);
-  // a role that gave up may leave the MMA warp waiting (bounded) on it; every role has
-  // finished its own asynchronous work before this barrier
+  // a role that gave up may leave another waiting (bounded) on it; every role has finished
+  // its own asynchronous work before this barrier
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// cuTensorMapEncodeTiled, looked up once through the runtime (no link against the driver).
+typedef CUresult (*TensorMapEncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                         const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                         CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+cudaError_t encode_bf16_rows(CUtensorMap* map, const void* base, long long rows, int cols, int box_rows) {
+  static TensorMapEncodeTiled encode = nullptr;
+  if (encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
+    encode = reinterpret_cast<TensorMapEncodeTiled>(fn);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kQpK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace
 
 cudaError_t launch_qproj(const QprojArgs& a, cudaStream_t stream) {
   if (a.R <= 0) return cudaSuccess;
-  cudaError_t e = cudaFuncSetAttribute(qproj_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQpSmem);
+  QprojParams p{};
+  p.a = a;
+  cudaError_t e = encode_bf16_rows(&p.map_a, a.qr, a.R, a.Kq, kQpM);
+  if (e == cudaSuccess) e = encode_bf16_rows(&p.map_b, a.wq_b, (long long)a.H * kHeadDim, a.Kq, kQpN);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(qproj_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQpSmem);
   int dev = 0, sms = 0;
   if (e == cudaSuccess) e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) return e;
   const long long tiles = (long long)((a.R + kQpM - 1) / kQpM) * (a.H / 2);
   const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);
-  return launch_overlapped(qproj_prep_kernel, dim3(grid), dim3(kQpThreads), (size_t)kQpSmem, stream, a);
+  return launch_overlapped(qproj_prep_kernel, dim3(grid), dim3(kQpThreads), (size_t)kQpSmem, stream, p);
 }
 
 }  // namespace indexer
