@@ -232,6 +232,9 @@ class Setup:
                       for i in range(rotate)] for t in tags}
         self.w = {t: [normal_bf16(wl.seed, f"{wl.name}/w{t[1:]}/{i}", (wl.B, wl.S, wl.H), device=dev)
                       for i in range(rotate)] for t in tags}
+        if wl.fused_q:   # the query latent and wq_b in place of q
+            self.qr = [wl.qr(dev, tag=f"qr/{i}") for i in range(rotate)]
+            self.wq = wl.wq_b(dev)
         self.ws_bytes = X.indexer_workspace_size(self.dims, wl.B, wl.S, wl.start_pos)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
         X.indexer_workspace_init(self.ws)
@@ -254,6 +257,13 @@ class Setup:
         in one call (indexer_forward_publish); a two-level step's consumer layer follows."""
         X, wl = self.X, self.wl
         sp = wl.start_pos if self.decode else 0
+        if wl.fused_q:   # key publish, the fused query projection + prep, scores, top-k
+            X.indexer_publish_k(self.dims, self.lat[i], self.wk, self.knw, self.table, sp, self.caches[i])
+            X.indexer_prep_q_proj(self.dims, self.qr[i], self.wq, self.w["q"][i], wl.start_pos, self.table,
+                                  self.q_rows, self.w_prime, self.ws)
+            X.indexer_scores(self.dims, self.q_rows, self.w_prime, wl.start_pos, self.caches[i], self.scores, self.ws)
+            X.indexer_topk(self.dims, self.scores, wl.start_pos, self.top)
+            return
         if wl.two_level:
             X.indexer_forward_publish(self.dims, self.lat[i], self.wk, self.knw, self.q["q1"][i], self.w["q1"][i], sp,
                                       self.table, self.caches[i], self.top1, self.ws, cand_out=self.cand)
@@ -268,6 +278,8 @@ class Setup:
         # blocks and top-k in one launch); prefill: separate publish and query prep launches;
         # a two-level step's consumer layer: query prep, scores, top-k
         small = self.decode and self.wl.B * self.wl.S * self.wl.H <= 16384
+        if self.wl.fused_q:
+            return 4
         return (3 if small else 4) + (3 if self.wl.two_level else 0)
 
     def kernel_kinds(self):
@@ -285,6 +297,10 @@ class Setup:
         if wl.two_level:
             kinds["candidates"] = lambda i: X.indexer_select_candidate_blocks(self.dims, self.scores, wl.start_pos,
                                                                               self.cand)
+        if wl.fused_q:
+            kinds["prep_q_proj"] = lambda i: X.indexer_prep_q_proj(self.dims, self.qr[i], self.wq, self.w[tag][i],
+                                                                   wl.start_pos, self.table, self.q_rows,
+                                                                   self.w_prime, self.ws)
         return kinds
 
 
@@ -398,6 +414,11 @@ def run_ours(args, dist: Dist):
     helpers = {k: {"bytes": b, "GB/s": b / (kernel_ms[k] / 1e3) / 1e9,
                    "frac": b / (kernel_ms[k] / 1e3) / 1e9 / peaks["hbm_gbs"]}
                for k, b in helper_bytes.items() if kernel_ms.get(k)}
+    if kernel_ms.get("prep_q_proj"):   # the bf16 projection on the tensor cores
+        pf = 2.0 * wl.B * wl.S * wl.q_lora_rank * wl.H * wl.D
+        pa = pf / (kernel_ms["prep_q_proj"] / 1e3) / 1e12
+        helpers["prep_q_proj"] = {"flops": pf, "TFLOP/s": pa, "frac": pa / peaks["bf16_tflops"],
+                                  "peak_source": f"{peaks['source']} bf16_tflops"}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -590,7 +611,7 @@ def breakdown(st: Setup, rotate: int, reps: int = 20):
     between CUDA events on the launching stream."""
     out = {}
     kinds = st.kernel_kinds()
-    for name in ["publish", "prep_q", "scores", "candidates", "topk"]:
+    for name in ["publish", "prep_q", "prep_q_proj", "scores", "candidates", "topk"]:
         if name not in kinds:
             continue
         g = capture(kinds[name], rotate)
@@ -620,13 +641,22 @@ def run_e2e(st: Setup, args, dist: Dist):
     q1 = st.q.get("q1")
     steps = args.steps if wl.S == 1 else min(args.steps, 64)
 
+    if wl.fused_q:   # the query latent crosses the bus instead of q
+        qh = [t.cpu().pin_memory() for t in st.qr]
+        qd = torch.empty_like(st.qr[0])
+
     def one(i):
         j = i % R
         qd.copy_(qh[j], non_blocking=True)
         wd.copy_(wh[j], non_blocking=True)
         ld.copy_(lh[j], non_blocking=True)
         sp = wl.start_pos if st.decode else 0
-        if wl.two_level:
+        if wl.fused_q:
+            X.indexer_publish_k(st.dims, ld, st.wk, st.knw, st.table, sp, st.caches[j])
+            X.indexer_prep_q_proj(st.dims, qd, st.wq, wd, wl.start_pos, st.table, st.q_rows, st.w_prime, st.ws)
+            X.indexer_scores(st.dims, st.q_rows, st.w_prime, wl.start_pos, st.caches[j], st.scores, st.ws)
+            X.indexer_topk(st.dims, st.scores, wl.start_pos, st.top)
+        elif wl.two_level:
             X.indexer_forward_publish(st.dims, ld, st.wk, st.knw, q1[j], st.w["q1"][j], sp, st.table, st.caches[j],
                                       st.top1, st.ws, cand_out=st.cand)
             X.indexer_forward(st.dims, qd, wd, wl.start_pos, st.table, st.caches[j], st.top, st.ws, cand_in=st.cand)
@@ -649,12 +679,15 @@ def run_e2e(st: Setup, args, dist: Dist):
     d2h = outh[0].numel() * 4
     return {"value": dist.world * wl.B * wl.S * steps / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
-            "api": "indexer_forward_publish (eager Python/ctypes calls, pinned host buffers)"}
+            "api": ("indexer_publish_k, indexer_prep_q_proj, indexer_scores, indexer_topk" if wl.fused_q
+                    else "indexer_forward_publish") + " (eager Python/ctypes calls, pinned host buffers)"}
 
 
 def describe(wl: Workload) -> str:
     kind = "decode" if wl.S == 1 else "prefill"
     extra = f", two-level {wl.cand_topk_blocks}x{wl.cand_block_size} candidate blocks" if wl.two_level else ""
+    if wl.fused_q:
+        extra += f", queries from qr through wq_b (q_lora_rank {wl.q_lora_rank}) fused into the query prep"
     return (f"{wl.name}: {kind} B{wl.B} S{wl.S} start_pos {wl.start_pos}, ratio {wl.ratio} -> {wl.T} compressed "
             f"positions, H{wl.H} {fmt_of(wl)['label']} heads, top-{wl.topk}, offset {wl.offset}{extra}")
 
@@ -681,6 +714,8 @@ class OracleSample:
             self.cache.append(c)
         self.q = C.bits(wl.q()[: self.n_seq])
         self.w = C.bits(wl.w()[: self.n_seq])
+        if wl.fused_q:   # queries from the query latent through wq_b, inside the timed step
+            self.qr, self.wq = C.bits(wl.qr()[: self.n_seq]), C.bits(wl.wq_b())
         self.dl = C.bits(wl.decode_latent()[: self.n_seq]) if wl.S == 1 else None
 
     def query(self, b: int, key_frac: float = 1.0):
@@ -691,7 +726,8 @@ class OracleSample:
                                             wl.ratio, wl.rope_dim, wl.norm_eps, fmt=fmt_of(wl)["name"])
             self.cache[b][0, slots] = rows[0]
         T = max(1, int(math.ceil(wl.T * key_frac)))
-        rows_q, wprime, _ = O.prep_queries(self.q[b:b + 1], self.w[b:b + 1], self.cos, self.sin, wl.start_pos,
+        q = O.project_queries(self.qr[b:b + 1], self.wq, wl.H) if wl.fused_q else self.q[b:b + 1]
+        rows_q, wprime, _ = O.prep_queries(q, self.w[b:b + 1], self.cos, self.sin, wl.start_pos,
                                            wl.rope_dim, wl.H, fmt=fmt_of(wl)["name"])
         vis = np.minimum(O.visible_lens(wl.start_pos, wl.S, wl.ratio), T)
         sc = O.index_scores(rows_q, wprime, self.cache[b], T, vis)

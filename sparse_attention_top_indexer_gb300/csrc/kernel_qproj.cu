@@ -166,13 +166,22 @@ __global__ void __launch_bounds__(kQpThreads, 1) qproj_prep_kernel(const __grid_
       const int m0 = (t / tiles_n) * kQpM, h0 = (t % tiles_n) * 2;
       const int row = m0 + m;
       const bool live = row < a.R;
+      // what does not come from the accumulator is fetched before waiting for it: the row's
+      // two head weights, and its RoPE table row (rope_dim * 4 bytes) into L1
+      const int pos = a.start_pos + (live ? row % a.S : 0);
+      const float2* cs_row = reinterpret_cast<const float2*>(a.rope_cs) + (size_t)pos * (a.rope_dim / 2);
+      uint32_t wbits0 = 0u, wbits1 = 0u;
+      if (live) {
+        wbits0 = a.w[(size_t)row * a.H + h0];
+        wbits1 = a.w[(size_t)row * a.H + h0 + 1];
+        for (int o = 0; o < a.rope_dim * 4; o += 128)
+          asm volatile("prefetch.global.L1 [%0];" ::"l"(reinterpret_cast<const char*>(cs_row) + o));
+      }
       if (!warp_wait_bounded(bar_accfull(acc), (uint32_t)(ti >> 1) & 1u)) {
         failed = true;
         break;
       }
       tc_fence_after();
-      const int pos = a.start_pos + (live ? row % a.S : 0);
-      const float2* cs_row = reinterpret_cast<const float2*>(a.rope_cs) + (size_t)pos * (a.rope_dim / 2);
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         const int h = h0 + hh;
@@ -227,7 +236,7 @@ __global__ void __launch_bounds__(kQpThreads, 1) qproj_prep_kernel(const __grid_
             qrow[kCodeBytes + b] = (uint8_t)(e + 127);
           }
         }
-        if (live) a.w_prime[(size_t)row * a.H + h] = bf16_to_f32(a.w[(size_t)row * a.H + h]) * a.w_scale;
+        if (live) a.w_prime[(size_t)row * a.H + h] = bf16_to_f32(hh == 0 ? wbits0 : wbits1) * a.w_scale;
       }
     }
   }

@@ -159,6 +159,7 @@ class Workload:
     seed: int = 0
     key_format: int = 0       # 0: MXFP4 rows (68 bytes), 1: FP8 rows (132 bytes)
     q_lora_rank: int = 1280   # K of the query projection wq_b (qr -> H * 128)
+    fused_q: bool = False     # queries enter as qr: the projection wq_b runs inside the step
 
     @property
     def end_pos(self) -> int:
@@ -244,6 +245,8 @@ WORKLOADS = {
         # the FP8 key format (132-byte rows) on the decode and prefill shapes
         Workload("decode_fp8", B=32, S=1, start_pos=32767, ratio=4, H=64, topk=2048, key_format=1),
         Workload("prefill_fp8", B=1, S=8192, start_pos=0, ratio=4, H=64, topk=512, key_format=1),
+        # the prefill shape with the query projection (qr -> wq_b -> q) fused into the query prep
+        Workload("prefill_qproj", B=1, S=8192, start_pos=0, ratio=4, H=64, topk=512, fused_q=True),
     ]
 }
 
