@@ -644,9 +644,19 @@ def run_e2e(st: Setup, args, dist: Dist):
     if wl.fused_q:   # the query latent crosses the bus instead of q
         qh = [t.cpu().pin_memory() for t in st.qr]
         qd = torch.empty_like(st.qr[0])
+    host_call = not wl.fused_q and not wl.two_level   # one C call takes the host buffers itself
+    if host_call:
+        ws_h = torch.empty(X.indexer_workspace_size_host(st.dims, wl.B, wl.S, wl.start_pos, lh[0].shape[1],
+                                                         lh[0].shape[2]), dtype=torch.uint8, device=st.dev)
+        X.indexer_workspace_init(ws_h)
 
     def one(i):
         j = i % R
+        if host_call:
+            sp = wl.start_pos if st.decode else 0
+            X.indexer_forward_publish_host(st.dims, lh[j], st.wk, st.knw, qh[j], wh[j], sp, st.table, st.caches[j],
+                                           outh[j], ws_h)
+            return
         qd.copy_(qh[j], non_blocking=True)
         wd.copy_(wh[j], non_blocking=True)
         ld.copy_(lh[j], non_blocking=True)
@@ -675,12 +685,15 @@ def run_e2e(st: Setup, args, dist: Dist):
     e1.record()
     torch.cuda.synchronize()
     ms = dist.max(e0.elapsed_time(e1))
+    if host_call:
+        X.indexer_status(ws_h)
     h2d = qh[0].numel() * 2 + wh[0].numel() * 2 + lh[0].numel() * 2
     d2h = outh[0].numel() * 4
     return {"value": dist.world * wl.B * wl.S * steps / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
             "api": ("indexer_publish_k, indexer_prep_q_proj, indexer_scores, indexer_topk" if wl.fused_q
-                    else "indexer_forward_publish") + " (eager Python/ctypes calls, pinned host buffers)"}
+                    else "indexer_forward_publish_host" if host_call else "indexer_forward_publish")
+                   + " (eager Python/ctypes calls, pinned host buffers)"}
 
 
 def describe(wl: Workload) -> str:

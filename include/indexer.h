@@ -278,6 +278,25 @@ int indexer_forward_publish(const IndexerDims* dims, const indexer_bf16* latent,
                             indexer_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * indexer_forward_publish_host -- indexer_forward_publish with the step's inputs and
+ * its top-k in HOST memory: the call copies latent, q and w to device staging inside the
+ * workspace, runs the step and copies the indices back, all on `stream` (pinned host
+ * buffers let the copies run asynchronously; topk_out_h is valid once the stream has
+ * reached the call's end). Arguments as indexer_forward_publish, with:
+ *   latent_h: bf16 [B][G][Din], q_h: bf16 [B][S][H][128], w_h: bf16 [B][S][H] (host)
+ *   topk_out_h: int32 [B][S][index_topk] (host)
+ *   ws/ws_bytes: at least indexer_workspace_size_host() bytes, 256-byte aligned,
+ *                initialised once by indexer_workspace_init
+ * No candidate filter and no score output (use indexer_forward_publish for those).
+ * ------------------------------------------------------------------------- */
+size_t indexer_workspace_size_host(const IndexerDims* dims, int B, int S, int start_pos, int G, int Din);
+int indexer_forward_publish_host(const IndexerDims* dims, const indexer_bf16* latent_h, int G, int Din,
+                                 const indexer_bf16* wk, const indexer_bf16* k_norm_w, const indexer_bf16* q_h,
+                                 const indexer_bf16* w_h, int B, int S, int start_pos, const float* rope_cs,
+                                 int max_pos, uint8_t* k_cache, int T_cap, int32_t* topk_out_h, void* ws,
+                                 size_t ws_bytes, indexer_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * indexer_forward_noalloc -- indexer_forward for callers that cannot allocate
  * device memory at call time. The pages have no counterpart: this is a deployment
  * convenience of the library. Some hosts own all of the device's memory -- a

@@ -21,7 +21,8 @@ __all__ = [
     "indexer_workspace_size_paged", "indexer_forward_publish",
     "indexer_rope_table", "indexer_publish_k", "indexer_prep_q", "indexer_prep_q_proj", "indexer_scores",
     "indexer_select_candidate_blocks", "indexer_topk", "indexer_forward", "indexer_workspace_size",
-    "indexer_workspace_init", "indexer_status", "indexer_abi_version", "make_dims", "indexer_forward_noalloc",
+    "indexer_workspace_init", "indexer_status", "indexer_abi_version", "indexer_forward_publish_host",
+    "indexer_workspace_size_host", "make_dims", "indexer_forward_noalloc",
     "NOALLOC_SCRATCH_BYTES",
 ]
 
@@ -78,6 +79,8 @@ _SIGS = {
                                 _P],
     "indexer_forward_publish": [ctypes.POINTER(IndexerDims), _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _P, _I, _P, _I,
                                 _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+    "indexer_forward_publish_host": [ctypes.POINTER(IndexerDims), _P, _I, _I, _P, _P, _P, _P, _I, _I, _I, _P, _I,
+                                     _P, _I, _P, _P, ctypes.c_size_t, _P],
     "indexer_workspace_init": [_P, ctypes.c_size_t, _P],
     "indexer_publish_k_paged": [ctypes.POINTER(IndexerDims), _P, _I, _I, _P, _P, _P, _I, _P, _P, _P, _I, _P,
                                 ctypes.c_size_t, _P],
@@ -102,6 +105,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.indexer_workspace_size.argtypes = [ctypes.POINTER(IndexerDims), _I, _I, _I]
     lib.indexer_workspace_size.restype = ctypes.c_size_t
     lib.indexer_workspace_size_paged.argtypes = [ctypes.POINTER(IndexerDims), _I, _I, _I]
+    lib.indexer_workspace_size_host.argtypes = [ctypes.POINTER(IndexerDims), _I, _I, _I, _I, _I]
+    lib.indexer_workspace_size_host.restype = ctypes.c_size_t
     lib.indexer_workspace_size_paged.restype = ctypes.c_size_t
     lib.indexer_last_error.argtypes = []
     lib.indexer_last_error.restype = ctypes.c_char_p
@@ -173,6 +178,18 @@ def _ptr(t: Optional[torch.Tensor], dtype=None, name: str = "tensor") -> Optiona
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _hptr(t: torch.Tensor, dtype, name: str) -> int:
+    """Address of a contiguous host tensor (pinned memory lets the library's copies run
+    asynchronously)."""
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     return t.data_ptr()
 
@@ -341,6 +358,28 @@ def indexer_forward_paged(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor, s
         _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
         _ptr(topk_out, torch.int32, "topk_out"), _ptr(scores_out, torch.float32, "scores_out"),
         _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def indexer_workspace_size_host(dims: IndexerDims, B: int, S: int, start_pos: int, G: int, Din: int) -> int:
+    return int(load_library().indexer_workspace_size_host(ctypes.byref(dims), B, S, start_pos, G, Din))
+
+
+def indexer_forward_publish_host(dims: IndexerDims, latent_h: torch.Tensor, wk: torch.Tensor, k_norm_w: torch.Tensor,
+                                 q_h: torch.Tensor, w_h: torch.Tensor, start_pos: int, rope_cs: torch.Tensor,
+                                 k_cache: torch.Tensor, topk_out_h: torch.Tensor, ws: torch.Tensor, stream=None):
+    """indexer_forward_publish with latent_h [B, G, Din], q_h [B, S, H, 128], w_h [B, S, H] and
+    topk_out_h [B, S, index_topk] in host memory; ws of indexer_workspace_size_host bytes. The
+    indices are in topk_out_h once the stream has passed the call."""
+    B, G, Din = latent_h.shape
+    S = q_h.shape[1]
+    if q_h.shape[0] != B or k_cache.shape[0] != B:
+        raise ValueError("latent_h, q_h and k_cache must share the batch")
+    _check(load_library().indexer_forward_publish_host(
+        ctypes.byref(dims), _hptr(latent_h, torch.bfloat16, "latent_h"), G, Din, _ptr(wk, torch.bfloat16, "wk"),
+        _ptr(k_norm_w, torch.bfloat16, "k_norm_w"), _hptr(q_h, torch.bfloat16, "q_h"), _hptr(w_h, torch.bfloat16, "w_h"),
+        B, S, start_pos, _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(k_cache, torch.uint8, "k_cache"),
+        _cache_tcap(k_cache, dims), _hptr(topk_out_h, torch.int32, "topk_out_h"), _ptr(ws, None, "ws"),
+        ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def indexer_forward_publish(dims: IndexerDims, latent: torch.Tensor, wk: torch.Tensor, k_norm_w: torch.Tensor,

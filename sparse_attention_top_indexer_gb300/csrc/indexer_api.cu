@@ -157,7 +157,7 @@ extern "C" {
 
 const char* indexer_last_error(void) { return g_last_error.c_str(); }
 
-int indexer_abi_version(void) { return 401; }
+int indexer_abi_version(void) { return 402; }
 
 // ---------------------------------------------------------------------------- RoPE table
 int indexer_rope_table(const IndexerYarn* y, int rope_dim, int max_pos, float* table, indexer_stream_t stream) {
@@ -791,6 +791,60 @@ int indexer_forward_publish(const IndexerDims* dims, const indexer_bf16* latent,
   RETURN_IF(build_publish(dims, latent, B, G, Din, wk, k_norm_w, rope_cs, max_pos, start_pos, k_cache, T_cap, &pa));
   return forward_impl(dims, q, w, B, S, start_pos, rope_cs, max_pos, k_cache, T_cap, cand_in, cand_out, topk_out,
                       scores_out, ws, ws_bytes, stream, &pa);
+}
+
+// ---------------------------------------------------------------------------- host-buffer step
+// Device staging for a step's host inputs and output, after the forward's own workspace.
+struct HostStaging {
+  size_t base, latent, q, w, top, total;
+};
+static size_t round256(size_t n) { return (n + 255) / 256 * 256; }
+static HostStaging host_staging(const IndexerDims* dims, int B, int S, int start_pos, int G, int Din) {
+  HostStaging h{};
+  h.base = round256(indexer_workspace_size(dims, B, S, start_pos));
+  h.latent = h.base;
+  h.q = h.latent + round256((size_t)B * G * Din * 2);
+  h.w = h.q + round256((size_t)B * S * dims->n_heads * dims->head_dim * 2);
+  h.top = h.w + round256((size_t)B * S * dims->n_heads * 2);
+  h.total = h.top + round256((size_t)B * S * dims->index_topk * 4);
+  return h;
+}
+
+size_t indexer_workspace_size_host(const IndexerDims* dims, int B, int S, int start_pos, int G, int Din) {
+  if (check_dims(dims) != INDEXER_OK || B <= 0 || S <= 0 || G < 0 || Din <= 0) return 0;
+  return host_staging(dims, B, S, start_pos, G, Din).total;
+}
+
+int indexer_forward_publish_host(const IndexerDims* dims, const indexer_bf16* latent_h, int G, int Din,
+                                 const indexer_bf16* wk, const indexer_bf16* k_norm_w, const indexer_bf16* q_h,
+                                 const indexer_bf16* w_h, int B, int S, int start_pos, const float* rope_cs,
+                                 int max_pos, uint8_t* k_cache, int T_cap, int32_t* topk_out_h, void* ws,
+                                 size_t ws_bytes, indexer_stream_t stream) {
+  RETURN_IF(check_dims(dims));
+  RETURN_IF(check_rows(B, S, start_pos));
+  if (!latent_h || !q_h || !w_h || !topk_out_h || !ws) return fail(INDEXER_ERR_NULL, "a required pointer is NULL");
+  if (G < 0 || Din <= 0) return fail(INDEXER_ERR_DIMS, "G must be >= 0 and Din > 0");
+  const HostStaging h = host_staging(dims, B, S, start_pos, G, Din);
+  if (ws_bytes < h.total)
+    return fail(INDEXER_ERR_WORKSPACE, "ws has %zu bytes, indexer_workspace_size_host needs %zu", ws_bytes, h.total);
+  if (!aligned(ws, 256)) return fail(INDEXER_ERR_ALIGN, "ws must be 256-byte aligned");
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  auto* lat_d = reinterpret_cast<indexer_bf16*>(base + h.latent);
+  auto* q_d = reinterpret_cast<indexer_bf16*>(base + h.q);
+  auto* w_d = reinterpret_cast<indexer_bf16*>(base + h.w);
+  auto* top_d = reinterpret_cast<int32_t*>(base + h.top);
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t qb = (size_t)B * S * dims->n_heads * dims->head_dim * 2, wb = (size_t)B * S * dims->n_heads * 2;
+  const size_t lb = (size_t)B * G * Din * 2, tb = (size_t)B * S * dims->index_topk * 4;
+  cudaError_t e = lb ? cudaMemcpyAsync(lat_d, latent_h, lb, cudaMemcpyHostToDevice, st) : cudaSuccess;
+  if (e == cudaSuccess) e = cudaMemcpyAsync(q_d, q_h, qb, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(w_d, w_h, wb, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "input copies");
+  RETURN_IF(indexer_forward_publish(dims, lat_d, G, Din, wk, k_norm_w, q_d, w_d, B, S, start_pos, rope_cs, max_pos,
+                                    k_cache, T_cap, nullptr, nullptr, top_d, nullptr, ws, h.base, stream));
+  e = cudaMemcpyAsync(topk_out_h, top_d, tb, cudaMemcpyDeviceToHost, st);
+  if (e != cudaSuccess) return cuda_fail(e, "output copy");
+  return ok();
 }
 
 int indexer_workspace_init(void* ws, size_t ws_bytes, indexer_stream_t stream) {

@@ -42,7 +42,7 @@ def test_struct_layouts_match_header(X):
 
 
 def test_abi_version(X):
-    assert X.indexer_abi_version() == 401   # + indexer_prep_q_proj (the fused query projection)
+    assert X.indexer_abi_version() == 402   # + indexer_forward_publish_host (host-buffer step)
 
 
 def test_workspace_size_host_only(X):

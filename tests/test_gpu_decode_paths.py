@@ -180,3 +180,42 @@ def test_forward_publish_equals_separate_calls(X, name, B, H, start, fmt):
     assert torch.equal(cache_a, cache_b), "caches differ"
     assert torch.equal(outs[0][1], outs[1][1]), "scores differ"
     assert torch.equal(outs[0][0], outs[1][0]), "indices differ"
+
+
+@pytest.mark.parametrize("start", [32767, 0])
+def test_forward_publish_host_equals_device(X, start):
+    """indexer_forward_publish_host (inputs and indices in pinned host memory, copied by the
+    call on its stream) leaves the same cache and indices as indexer_forward_publish."""
+    base = WORKLOADS["decode"] if start > 0 else WORKLOADS["tiny_prefill"]
+    wl = dataclasses.replace(base, name=f"fph{start}", B=6 if start > 0 else 2, topk=min(base.topk, 512))
+    d = C.dims_of(wl)
+    table = C.gpu_table(wl.max_pos)
+    cache_a = X.new_key_cache(wl.B, wl.T_cap)
+    if start > 0:
+        X.indexer_publish_k(d, wl.latent("cuda"), wl.wk("cuda"), wl.k_norm_w("cuda"), table, 0, cache_a)
+        lat = wl.decode_latent("cuda")
+    else:
+        lat = wl.latent("cuda")
+    cache_b = cache_a.clone()
+    q, w = wl.q("cuda"), wl.w("cuda")
+    ws = torch.empty(X.indexer_workspace_size(d, wl.B, wl.S, wl.start_pos), dtype=torch.uint8, device="cuda")
+    X.indexer_workspace_init(ws)
+    top = torch.empty((wl.B, wl.S, wl.topk), dtype=torch.int32, device="cuda")
+    X.indexer_forward_publish(d, lat, wl.wk("cuda"), wl.k_norm_w("cuda"), q, w, wl.start_pos, table, cache_a, top, ws)
+    X.indexer_status(ws)
+    n = X.indexer_workspace_size_host(d, wl.B, wl.S, wl.start_pos, lat.shape[1], lat.shape[2])
+    assert n > ws.numel()
+    ws_h = torch.empty(n, dtype=torch.uint8, device="cuda")
+    X.indexer_workspace_init(ws_h)
+    top_h = torch.full((wl.B, wl.S, wl.topk), -7, dtype=torch.int32).pin_memory()
+    X.indexer_forward_publish_host(d, lat.cpu().pin_memory(), wl.wk("cuda"), wl.k_norm_w("cuda"), q.cpu().pin_memory(),
+                                   w.cpu().pin_memory(), wl.start_pos, table, cache_b, top_h, ws_h)
+    torch.cuda.synchronize()
+    X.indexer_status(ws_h)
+    assert torch.equal(cache_a, cache_b), "caches differ"
+    assert torch.equal(top.cpu(), top_h), "indices differ"
+    with pytest.raises(X.IndexerError) as e:   # the workspace must hold the staging too
+        X.indexer_forward_publish_host(d, lat.cpu().pin_memory(), wl.wk("cuda"), wl.k_norm_w("cuda"),
+                                       q.cpu().pin_memory(), w.cpu().pin_memory(), wl.start_pos, table, cache_b, top_h,
+                                       ws)
+    assert e.value.code == -5
