@@ -6,10 +6,11 @@
 // masked to -inf and, for a level-two layer, -inf outside the candidate blocks.
 //
 // One CTA (256 threads) takes a group of QG query rows of one sequence and a run of
-// 128-key pages of the paged key cache. A page already holds its codes in the tensor
-// cores' K-major core-matrix order, so the MMA reads the A operand straight from the
-// stage buffer the page was bulk-copied into (cp.async.bulk, one copy per page, into a
-// ring of NSTAGE stages):
+// 128-key tiles (two 64-key pages each) of the paged key cache. A page already holds its
+// codes in the tensor cores' K-major core-matrix order, so the MMA reads the A operand
+// straight from the stage buffer the tile was bulk-copied into (cp.async.bulk: one copy
+// when the tile's two pages are adjacent in the pool, else one per page; a ring of NSTAGE
+// stages):
 //   * MMA warpgroup (warps 0-3): rewrites the group's quantised query rows into the same
 //     core-matrix order once (the B operand, N = QG * H padded to 16) and stores their
 //     scale factors in tensor memory; then, per page, each warp stores the A scale factors
@@ -20,7 +21,8 @@
 //     N head dot products with tcgen05.ld, releases the accumulator, and forms
 //     sum_h w' * max(dot, 0) per query row in f32 -- no shuffles, because keys, not heads,
 //     sit on the lanes. Once a page's MMA has completed, its stage is refilled from here.
-// Only lane 0 of a warp polls an mbarrier; the warp follows through __syncwarp.
+// Every lane of a waiting warp polls the mbarrier (bounded) and the warp agrees on the
+// outcome with __all_sync. Several query rows per group run in score_rows_kernel below.
 //
 // Tensor-memory scale layout: the MMA reads the scale factors of A row m from lane m,
 // column m / 32 of the scale set, and those of B row n = 32 j + i from column j, lane i of
