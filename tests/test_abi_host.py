@@ -129,6 +129,36 @@ def test_paged_validation_rejects_without_launch(X):
                                        0x6000, 0x7008, 8, 0x8000, 256, None) == -2
 
 
+def test_qproj_and_host_step_validation_without_launch(X):
+    lib = X.load_library()
+    d = X.make_dims(n_heads=64, ratio=4, index_topk=16)
+    d8 = X.make_dims(n_heads=64, ratio=4, index_topk=16, key_format=1)
+
+    def qp(dd, Kq=1280, qr=0x1000, wq=0x2000, q_out=None, ws=0x9000, wsb=256):
+        return lib.indexer_prep_q_proj(ctypes.byref(dd), qr, Kq, wq, 0x3000, 1, 8, 0, 0x4000, 64, 0x5000, 0x6000,
+                                       q_out, ws, wsb, None)
+    assert qp(d8) == -3                      # the fused projection writes MXFP4 rows only
+    assert qp(d, Kq=96) == -3                # q_lora_rank not a multiple of 64
+    assert qp(d, wq=None) == -1
+    assert qp(d, wq=0x2008) == -2            # wq_b not 16-byte aligned
+    assert qp(d, qr=0x1008) == -2
+    assert qp(d, q_out=0x7008) == -2
+    assert qp(d, wsb=16) == -5               # no room for the status word
+
+    # the host-buffer step: staging for latent, q, w and the indices after the forward's workspace
+    r = lambda x: (x + 255) // 256 * 256
+    n = X.indexer_workspace_size_host(d, 32, 1, 32767, 1, 128)
+    assert n == (r(X.indexer_workspace_size(d, 32, 1, 32767)) + r(32 * 128 * 2) + r(32 * 64 * 128 * 2) + r(32 * 64 * 2)
+                 + r(32 * 16 * 4))
+
+    def fh(topk_h=0x8000, ws=0x10000, ws_bytes=n):
+        return lib.indexer_forward_publish_host(ctypes.byref(d), 0x1000, 1, 128, 0x2000, 0x3000, 0x4000, 0x5000, 32, 1,
+                                                32767, 0x6000, 32768, 0x7000, 8192, topk_h, ws, ws_bytes, None)
+    assert fh(topk_h=None) == -1
+    assert fh(ws_bytes=n - 1) == -5
+    assert fh(ws=0x10010) == -2              # the staging is carved at 256-byte offsets
+
+
 def test_missing_library_fails_loudly(tmp_path):
     import sparse_attention_top_indexer_gb300 as X
     saved = X._lib
