@@ -1,4 +1,5 @@
 """The seeded input generator: splitmix64 bits, slice consistency, shapes."""
+import dataclasses
 import math
 
 import numpy as np
@@ -61,3 +62,18 @@ def test_heavy_rows_fraction():
     u = W.uniform_f64(p.seed, f"{p.name}/w/heavy", (p.B, p.S))
     frac = (u < p.heavy_frac).double().mean().item()
     assert abs(frac - 0.05) < 0.005
+
+
+def test_query_latent_and_projection_generators():
+    """qr [B, S, q_lora_rank] is unit normal, wq_b [H * 128, q_lora_rank] has std
+    q_lora_rank^-0.5 (so q = wq_b(qr) has unit scale), both deterministic and distinct."""
+    wl = dataclasses.replace(W.WORKLOADS["prefill"], name="gen_qp", B=2, S=48, H=8, q_lora_rank=256)
+    qr, wq = wl.qr(), wl.wq_b()
+    assert qr.shape == (2, 48, 256) and wq.shape == (8 * 128, 256)
+    assert qr.dtype == torch.bfloat16 and wq.dtype == torch.bfloat16
+    assert torch.equal(qr, wl.qr()) and torch.equal(wq, wl.wq_b())
+    assert abs(qr.float().std().item() - 1.0) < 0.05
+    assert abs(wq.float().std().item() * 256 ** 0.5 - 1.0) < 0.05
+    q = qr.float().reshape(-1, 256) @ wq.float().T
+    assert 0.8 < q.std().item() < 1.2
+    assert not torch.equal(qr, dataclasses.replace(wl, name="gen_qp2").qr())
