@@ -283,7 +283,9 @@ int indexer_forward_publish(const IndexerDims* dims, const indexer_bf16* latent,
  * workspace, runs the step and copies the indices back, all on `stream` (pinned host
  * buffers let the copies run asynchronously; topk_out_h is valid once the stream has
  * reached the call's end). Arguments as indexer_forward_publish, with:
- *   latent_h: bf16 [B][G][Din], q_h: bf16 [B][S][H][128], w_h: bf16 [B][S][H] (host)
+ *   latent_h: bf16 [B][G][Din], q_h: bf16 [B][S][H][128], w_h: bf16 [B][S][H] (host);
+ *             G == 0 (a decode token that completes no group): no key is published, the
+ *             step is indexer_forward, and latent_h may be NULL
  *   topk_out_h: int32 [B][S][index_topk] (host)
  *   ws/ws_bytes: at least indexer_workspace_size_host() bytes, 256-byte aligned,
  *                initialised once by indexer_workspace_init

@@ -374,8 +374,9 @@ def indexer_forward_publish_host(dims: IndexerDims, latent_h: torch.Tensor, wk: 
     S = q_h.shape[1]
     if q_h.shape[0] != B or k_cache.shape[0] != B:
         raise ValueError("latent_h, q_h and k_cache must share the batch")
+    lat = _hptr(latent_h, torch.bfloat16, "latent_h") if G > 0 else None   # G == 0: no key this step
     _check(load_library().indexer_forward_publish_host(
-        ctypes.byref(dims), _hptr(latent_h, torch.bfloat16, "latent_h"), G, Din, _ptr(wk, torch.bfloat16, "wk"),
+        ctypes.byref(dims), lat, G, Din, _ptr(wk, torch.bfloat16, "wk"),
         _ptr(k_norm_w, torch.bfloat16, "k_norm_w"), _hptr(q_h, torch.bfloat16, "q_h"), _hptr(w_h, torch.bfloat16, "w_h"),
         B, S, start_pos, _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(k_cache, torch.uint8, "k_cache"),
         _cache_tcap(k_cache, dims), _hptr(topk_out_h, torch.int32, "topk_out_h"), _ptr(ws, None, "ws"),

@@ -822,7 +822,8 @@ int indexer_forward_publish_host(const IndexerDims* dims, const indexer_bf16* la
                                  size_t ws_bytes, indexer_stream_t stream) {
   RETURN_IF(check_dims(dims));
   RETURN_IF(check_rows(B, S, start_pos));
-  if (!latent_h || !q_h || !w_h || !topk_out_h || !ws) return fail(INDEXER_ERR_NULL, "a required pointer is NULL");
+  if ((G > 0 && !latent_h) || !q_h || !w_h || !topk_out_h || !ws)
+    return fail(INDEXER_ERR_NULL, "a required pointer is NULL");
   if (G < 0 || Din <= 0) return fail(INDEXER_ERR_DIMS, "G must be >= 0 and Din > 0");
   const HostStaging h = host_staging(dims, B, S, start_pos, G, Din);
   if (ws_bytes < h.total)
@@ -840,8 +841,12 @@ int indexer_forward_publish_host(const IndexerDims* dims, const indexer_bf16* la
   if (e == cudaSuccess) e = cudaMemcpyAsync(q_d, q_h, qb, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(w_d, w_h, wb, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return cuda_fail(e, "input copies");
-  RETURN_IF(indexer_forward_publish(dims, lat_d, G, Din, wk, k_norm_w, q_d, w_d, B, S, start_pos, rope_cs, max_pos,
-                                    k_cache, T_cap, nullptr, nullptr, top_d, nullptr, ws, h.base, stream));
+  if (G > 0)
+    RETURN_IF(indexer_forward_publish(dims, lat_d, G, Din, wk, k_norm_w, q_d, w_d, B, S, start_pos, rope_cs, max_pos,
+                                      k_cache, T_cap, nullptr, nullptr, top_d, nullptr, ws, h.base, stream));
+  else   // no key completes this step: the forward alone
+    RETURN_IF(indexer_forward(dims, q_d, w_d, B, S, start_pos, rope_cs, max_pos, k_cache, T_cap, nullptr, nullptr,
+                              top_d, nullptr, ws, h.base, stream));
   e = cudaMemcpyAsync(topk_out_h, top_d, tb, cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return cuda_fail(e, "output copy");
   return ok();

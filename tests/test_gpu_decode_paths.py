@@ -214,6 +214,27 @@ def test_forward_publish_host_equals_device(X, start):
     X.indexer_status(ws_h)
     assert torch.equal(cache_a, cache_b), "caches differ"
     assert torch.equal(top.cpu(), top_h), "indices differ"
+    # a token that completes no group (G == 0): the forward alone, on the published cache
+    wl0 = dataclasses.replace(wl, start_pos=wl.start_pos + 1) if start > 0 else None
+    if wl0 is not None:
+        d0 = C.dims_of(wl0)
+        table0 = C.gpu_table(wl0.max_pos)   # one more position than the publishing step's
+        ws0 = torch.empty(X.indexer_workspace_size(d0, wl0.B, wl0.S, wl0.start_pos), dtype=torch.uint8,
+                          device="cuda")
+        X.indexer_workspace_init(ws0)
+        top0 = torch.empty_like(top)
+        X.indexer_forward(d0, q, w, wl0.start_pos, table0, cache_a, top0, ws0)
+        X.indexer_status(ws0)
+        n0 = X.indexer_workspace_size_host(d0, wl0.B, wl0.S, wl0.start_pos, 0, lat.shape[2])
+        ws0h = torch.empty(n0, dtype=torch.uint8, device="cuda")
+        X.indexer_workspace_init(ws0h)
+        top0h = torch.full_like(top_h, -7).pin_memory()
+        X.indexer_forward_publish_host(d0, torch.empty((wl.B, 0, lat.shape[2]), dtype=torch.bfloat16),
+                                       wl.wk("cuda"), wl.k_norm_w("cuda"), q.cpu().pin_memory(), w.cpu().pin_memory(),
+                                       wl0.start_pos, table0, cache_b, top0h, ws0h)
+        torch.cuda.synchronize()
+        X.indexer_status(ws0h)
+        assert torch.equal(top0.cpu(), top0h), "indices differ without a key to publish"
     with pytest.raises(X.IndexerError) as e:   # the workspace must hold the staging too
         X.indexer_forward_publish_host(d, lat.cpu().pin_memory(), wl.wk("cuda"), wl.k_norm_w("cuda"),
                                        q.cpu().pin_memory(), w.cpu().pin_memory(), wl.start_pos, table, cache_b, top_h,
