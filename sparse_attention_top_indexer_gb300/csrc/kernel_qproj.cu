@@ -254,16 +254,16 @@ typedef CUresult (*TensorMapEncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuui
                                          const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                          CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+TensorMapEncodeTiled lookup_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  return e == cudaSuccess && q == cudaDriverEntryPointSuccess ? reinterpret_cast<TensorMapEncodeTiled>(fn) : nullptr;
+}
+
 cudaError_t encode_bf16_rows(CUtensorMap* map, const void* base, long long rows, int cols, int box_rows) {
-  static TensorMapEncodeTiled encode = nullptr;
-  if (encode == nullptr) {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess) return e;
-    if (q != cudaDriverEntryPointSuccess || fn == nullptr) return cudaErrorNotSupported;
-    encode = reinterpret_cast<TensorMapEncodeTiled>(fn);
-  }
+  static const TensorMapEncodeTiled encode = lookup_encode();   // looked up once, thread-safely
+  if (encode == nullptr) return cudaErrorNotSupported;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
   const cuuint32_t box[2] = {(cuuint32_t)kQpK, (cuuint32_t)box_rows};
