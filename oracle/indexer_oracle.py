@@ -348,7 +348,9 @@ def prep_queries(q_bits, w_bits, cos, sin, start_pos: int, rope_dim: int, n_head
     B, S, H, D = q_bits.shape
     pos = (start_pos + np.arange(S)) if row_positions is None else np.asarray(row_positions)
     qr = rope_interleaved(q_bits, cos, sin, np.broadcast_to(pos[None, :, None], (B, S, H)), rope_dim)
-    wprime = bf16_to_f64(w_bits) * (D ** -0.5 * n_heads ** -0.5)
+    # softmax_scale * n_heads**-0.5 = (D * H)**-0.5, evaluated with one rounding (exact
+    # whenever D * H is a power of four)
+    wprime = bf16_to_f64(w_bits) * (float(D * n_heads) ** -0.5)
     return quantise_rows(qr, fmt), wprime, qr
 
 

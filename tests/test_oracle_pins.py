@@ -264,6 +264,78 @@ def test_rope_preserves_pair_norm():
     assert np.all(np.abs(na - nb) <= 2 ** -7 * na + 1e-30)
 
 
+# A rotation whose result depends on the f32 operation order. x0 = x1 = 1 + 2^-7 (bf16
+# 0x3F81), c = 1 - 2^-24 (f32 0x3F7FFFFF), s = 1 - 2^-23 (f32 0x3F7FFFFE). By hand:
+#   x0*c = 1 + 2^-7 - 2^-24 - 2^-31 lies 2^-24 - 2^-31 above L = 1 + 2^-7 - 2^-23 and
+#          2^-24 + 2^-31 below 1 + 2^-7, so it rounds to L in f32;
+#   x1*s = 1 + 2^-7 - 2^-23 - 2^-30 lies 2^-30 below L, so it also rounds to L;
+#   y0 = f32(L - L) = +0  (bf16 0x0000).
+# With a fused multiply-add (f32(x0*c - f32(x1*s))) y0 would be 2^-24 - 2^-31, and exact
+# arithmetic would give 2^-24 + 2^-31: both nonzero. y1 = f32(L + L) = 2 + 2^-6 - 2^-22,
+# which rounds to bf16 2 + 2^-6 (0x4001).
+_ROPE_ORDER_X = 0x3F81
+_ROPE_ORDER_C = np.array([0x3F7FFFFF], np.uint32).view(np.float32)[0]
+_ROPE_ORDER_S = np.array([0x3F7FFFFE], np.uint32).view(np.float32)[0]
+
+
+def test_rope_f32_rounds_each_product_then_the_sum():
+    """The RoPE reading (products rounded to f32, then their difference / sum rounded to
+    f32, no fused multiply-add) on a hand-derived case where the order decides the result."""
+    x = np.zeros((1, 128), np.uint16)
+    x[0, 64] = x[0, 65] = _ROPE_ORDER_X
+    cos = np.ones((1, 32), np.float32)
+    sin = np.zeros((1, 32), np.float32)
+    cos[0, 0], sin[0, 0] = _ROPE_ORDER_C, _ROPE_ORDER_S
+    y = O.rope_interleaved(x, cos, sin, np.zeros(1, int), 64)
+    assert y[0, 64] == 0x0000
+    assert y[0, 65] == 0x4001
+
+
+# --------------------------------------------------------------------- query prep
+def test_query_head_weight_factor_matches_the_pages_constants():
+    """w' = weights * softmax_scale * n_heads^-0.5 with softmax_scale = index_head_dim^-0.5
+    (index-keys page, Indexer.__init__ softmax_scale, Indexer.forward weights line). For
+    index_head_dim 128: H 8 -> 1/32, H 32 -> 1/64, H 128 -> 1/128 exactly; H 64 ->
+    0.011048543456..., H 16 -> 0.022097086912... (decimal constants, not recomputed)."""
+    table_c = np.ones((4, 32), np.float32)
+    table_s = np.zeros((4, 32), np.float32)
+    exact = {8: 0.03125, 32: 0.015625, 128: 0.0078125}
+    approx = {64: 0.011048543456039806, 16: 0.022097086912079612}
+    for H in (8, 16, 32, 64, 128):
+        q = _rand_bf16((1, 2, H, 128))
+        w = _rand_bf16((1, 2, H), scale=3.0)
+        _, wprime, _ = O.prep_queries(q, w, table_c, table_s, 0, 64, H)
+        ratio = wprime / O.bf16_to_f64(w)
+        ok = np.isfinite(ratio)
+        if H in exact:
+            assert np.array_equal(wprime, O.bf16_to_f64(w) * exact[H])
+        else:
+            assert np.all(np.abs(ratio[ok] - approx[H]) <= 1e-15)
+    # a unit weight gives the factor itself
+    one = np.full((1, 1, 64), 0x3F80, np.uint16)
+    _, wp, _ = O.prep_queries(_rand_bf16((1, 1, 64, 128)), one, table_c, table_s, 0, 64, 64)
+    assert np.all(np.abs(wp - 0.011048543456039806) < 1e-16)
+
+
+def test_query_rope_position_is_start_pos_plus_row():
+    """Row s of a chunk starting at start_pos is rotated at position start_pos + s (index-keys
+    page, Indexer.forward: freqs_cis[start_pos:end_pos] applied to q). A table whose pair-0
+    cosine encodes the position ((p + 1) / 4096, exact in bf16 for p < 255) and whose sines
+    are zero turns the query value 1.0 at the pair's first element into that position."""
+    max_pos = 200
+    cos = np.ones((max_pos, 32), np.float32)
+    sin = np.zeros((max_pos, 32), np.float32)
+    cos[:, 0] = (np.arange(max_pos) + 1) / 4096.0
+    for start, S in ((0, 3), (100, 5), (190, 10)):
+        q = np.zeros((2, S, 4, 128), np.uint16)
+        q[..., 64] = 0x3F80                                   # 1.0 at the first rotated dim
+        w = np.full((2, S, 4), 0x3F80, np.uint16)
+        _, _, qrot = O.prep_queries(q, w, cos, sin, start, 64, 4)
+        got = O.bf16_to_f64(qrot[..., 64]) * 4096.0 - 1.0
+        want = np.broadcast_to((start + np.arange(S))[None, :, None], got.shape)
+        assert np.array_equal(got, want)
+
+
 # ----------------------------------------------------------------------- wk / RMSNorm
 def test_linear_is_correctly_rounded_exact_sum():
     x = _rand_bf16((6, 128))
