@@ -316,13 +316,25 @@ int indexer_forward_publish_host(const IndexerDims* dims, const indexer_bf16* la
  *   - all calls share the one array: calls that may run at the same time on the GPU
  *     (different streams or host threads without ordering) race on it and must not
  *     be issued; each call clears the status word it starts from;
- *   - device-wait timeouts are not reported (the status word lives in the array).
+ *   - arguments are checked before anything is enqueued: a rejected call does not
+ *     touch the array;
+ *   - the array's address stays valid for the life of the process; after a
+ *     cudaDeviceReset the module holding it is gone, so do not call this entry point
+ *     on that device again;
+ *   - device-wait timeouts set the status word at the start of the array; read it
+ *     with indexer_noalloc_status.
  * ------------------------------------------------------------------------- */
 #define INDEXER_NOALLOC_SCRATCH_BYTES (8 * 1024 * 1024)
 int indexer_forward_noalloc(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
                             int start_pos, const float* rope_cs, int max_pos, const uint8_t* k_cache, int T_cap,
                             const int32_t* cand_in, int32_t* cand_out, int32_t* topk_out, float* scores_out,
                             indexer_stream_t stream);
+
+/* indexer_noalloc_status -- the status word of indexer_forward_noalloc's static array on
+ * the current device (no counterpart on the pages): synchronises `stream`, reads and clears
+ * the word, and returns INDEXER_OK, INDEXER_ERR_DEVICE_TIMEOUT or INDEXER_ERR_RANGE as
+ * indexer_status does for a workspace. Allocates nothing. */
+int indexer_noalloc_status(indexer_stream_t stream);
 
 /* ---------------------------------------------------------------------------
  * Page pool and mixed batches: a server's form of the same path ([attention.py]
@@ -375,6 +387,26 @@ int indexer_forward_paged(const IndexerDims* dims, const indexer_bf16* q, const 
  * groups. */
 size_t indexer_workspace_size_paged(const IndexerDims* dims, int Q, int n_seq, int T_max);
 
+/* ---------------------------------------------------------------------------
+ * Row-major caches. The pages hold the indexer cache one row per compressed position:
+ * [index-keys] Indexer.__init__ registers k_cache [max_batch_size][max_seq_len / ratio]
+ * [index_head_dim]; [attention.py] DeepseekV4IndexerCache binds a [num_blocks]
+ * [block_size][68] (MXFP4) or [..][132] (FP8) tensor, _indexer_k_cache_head_dim giving
+ * the row width. These two calls move keys between that row-major form and this
+ * library's 64-key pages (a pure byte permutation, bit-exact both ways), so a caller
+ * holding such a cache can use every other entry point:
+ *   rows:    uint8 [n_seq][ld_rows][row bytes] (68 or 132 by dims->key_format), 4-byte
+ *            aligned; key t of sequence b is row b * ld_rows + t
+ *   k_cache: uint8 [n_seq][T_cap / 64][page bytes], 16-byte aligned (a page pool
+ *            [num_pages][page bytes] is n_seq = num_pages, T_cap = ld_rows = 64)
+ *   n_keys:  keys 0 .. n_keys-1 of every sequence are moved (n_keys <= T_cap, <= ld_rows);
+ *            the other keys of the destination are left as they are.
+ * ------------------------------------------------------------------------- */
+int indexer_cache_from_rows(const IndexerDims* dims, const uint8_t* rows, int n_seq, int n_keys, int ld_rows,
+                            uint8_t* k_cache, int T_cap, indexer_stream_t stream);
+int indexer_cache_to_rows(const IndexerDims* dims, const uint8_t* k_cache, int T_cap, int n_seq, int n_keys,
+                          uint8_t* rows, int ld_rows, indexer_stream_t stream);
+
 /* Bytes of workspace indexer_forward needs for these sizes (0 on invalid dims).
  * Layout: status header, quantised query rows, head weights, f32 scores. */
 size_t indexer_workspace_size(const IndexerDims* dims, int B, int S, int start_pos);
@@ -387,6 +419,17 @@ int indexer_workspace_init(void* ws, size_t ws_bytes, indexer_stream_t stream);
 /* Synchronises `stream`, reads and clears the status word of `ws` and returns
  * INDEXER_OK or INDEXER_ERR_DEVICE_TIMEOUT. For tests and diagnostics. */
 int indexer_status(void* ws, indexer_stream_t stream);
+
+/* indexer_scores_hold_test -- for tests of the bounded device waits only (no counterpart
+ * on the pages). Launches the several-row score kernel of indexer_scores (S >= 2, no
+ * candidate filter) with its producer role held back: no query row, key tile or MMA is
+ * ever requested, so every other role's wait runs out after wait_ns nanoseconds (1e3 ..
+ * 1e9). The kernel records the timeout in the status word of `ws` (indexer_status then
+ * returns INDEXER_ERR_DEVICE_TIMEOUT), frees its tensor memory and returns with nothing in
+ * flight; `scores` is not written. Arguments otherwise as indexer_scores. */
+int indexer_scores_hold_test(const IndexerDims* dims, const uint8_t* q_rows, const float* w_prime, int B, int S,
+                             int start_pos, const uint8_t* k_cache, int T_cap, float* scores, void* ws,
+                             size_t ws_bytes, uint64_t wait_ns, indexer_stream_t stream);
 
 /* Message of the last failure on this thread ("" if none). */
 const char* indexer_last_error(void);

@@ -23,7 +23,8 @@ __all__ = [
     "indexer_select_candidate_blocks", "indexer_topk", "indexer_forward", "indexer_workspace_size",
     "indexer_workspace_init", "indexer_status", "indexer_abi_version", "indexer_forward_publish_host",
     "indexer_workspace_size_host", "make_dims", "indexer_forward_noalloc",
-    "NOALLOC_SCRATCH_BYTES",
+    "NOALLOC_SCRATCH_BYTES", "indexer_noalloc_status", "indexer_cache_from_rows", "indexer_cache_to_rows",
+    "indexer_scores_hold_test",
 ]
 
 KEY_ROW_BYTES = 68
@@ -87,6 +88,11 @@ _SIGS = {
     "indexer_forward_paged": [ctypes.POINTER(IndexerDims), _P, _P, _I, _I, _P, _P, _I, _P, _I, _P, _I, _P, _I,
                               _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "indexer_status": [_P, _P],
+    "indexer_noalloc_status": [_P],
+    "indexer_scores_hold_test": [ctypes.POINTER(IndexerDims), _P, _P, _I, _I, _I, _P, _I, _P, _P, ctypes.c_size_t,
+                                 ctypes.c_uint64, _P],
+    "indexer_cache_from_rows": [ctypes.POINTER(IndexerDims), _P, _I, _I, _I, _P, _I, _P],
+    "indexer_cache_to_rows": [ctypes.POINTER(IndexerDims), _P, _I, _I, _I, _P, _I, _P],
 }
 
 
@@ -255,6 +261,19 @@ def indexer_scores(dims: IndexerDims, q_rows: torch.Tensor, w_prime: torch.Tenso
         _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), _stream(stream)))
 
 
+def indexer_scores_hold_test(dims: IndexerDims, q_rows: torch.Tensor, w_prime: torch.Tensor, start_pos: int,
+                             k_cache: torch.Tensor, scores: torch.Tensor, ws: torch.Tensor, wait_ns: int, stream=None):
+    """Test of the bounded device waits: the several-row score kernel with its producer held
+    back, so its other roles' waits run out after wait_ns; indexer_status(ws) then raises
+    INDEXER_ERR_DEVICE_TIMEOUT. See include/indexer.h."""
+    B, S = q_rows.shape[:2]
+    _check(load_library().indexer_scores_hold_test(
+        ctypes.byref(dims), _ptr(q_rows, torch.uint8, "q_rows"), _ptr(w_prime, torch.float32, "w_prime"), B, S,
+        start_pos, _ptr(k_cache, torch.uint8, "k_cache"), _cache_tcap(k_cache, dims),
+        _ptr(scores, torch.float32, "scores"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(), int(wait_ns),
+        _stream(stream)))
+
+
 def indexer_select_candidate_blocks(dims: IndexerDims, scores: torch.Tensor, start_pos: int,
                                     blocks_out: torch.Tensor, stream=None):
     """scores f32 [B, S, T]; blocks_out int32 [B, S, cand_topk_blocks]."""
@@ -314,6 +333,41 @@ def indexer_forward_noalloc(dims: IndexerDims, q: torch.Tensor, w: torch.Tensor,
         _ptr(rope_cs, torch.float32, "rope_cs"), rope_cs.shape[0], _ptr(k_cache, torch.uint8, "k_cache"),
         _cache_tcap(k_cache, dims), _ptr(cand_in, torch.int32, "cand_in"), _ptr(cand_out, torch.int32, "cand_out"),
         _ptr(topk_out, torch.int32, "topk_out"), _ptr(scores_out, torch.float32, "scores_out"), _stream(stream)))
+
+
+def indexer_noalloc_status(stream=None):
+    """Synchronises the stream, reads and clears the status word of the no-alloc entry
+    point's static scratch on the current device; raises IndexerError if a device wait of
+    the last indexer_forward_noalloc call ran out."""
+    _check(load_library().indexer_noalloc_status(_stream(stream)))
+
+
+def indexer_cache_from_rows(dims: IndexerDims, rows: torch.Tensor, k_cache: torch.Tensor, n_keys: Optional[int] = None,
+                            stream=None):
+    """Keys given as row-major rows uint8 [n_seq, ld_rows, row bytes] (the pages' indexer-cache
+    layout) into pages k_cache uint8 [n_seq, T_cap / 64, page bytes]; keys 0 .. n_keys-1 of every
+    sequence (default: all rows that fit)."""
+    n_seq, ld_rows, rb = rows.shape
+    T_cap = _cache_tcap(k_cache, dims)
+    if rb != row_bytes(dims.key_format) or k_cache.shape[0] != n_seq:
+        raise ValueError("rows must be [n_seq, ld_rows, row bytes of the dims' format] and match k_cache's batch")
+    n = min(ld_rows, T_cap) if n_keys is None else n_keys
+    _check(load_library().indexer_cache_from_rows(ctypes.byref(dims), _ptr(rows, torch.uint8, "rows"), n_seq, n,
+                                                  ld_rows, _ptr(k_cache, torch.uint8, "k_cache"), T_cap,
+                                                  _stream(stream)))
+
+
+def indexer_cache_to_rows(dims: IndexerDims, k_cache: torch.Tensor, rows: torch.Tensor, n_keys: Optional[int] = None,
+                          stream=None):
+    """Pages k_cache uint8 [n_seq, T_cap / 64, page bytes] into row-major rows uint8
+    [n_seq, ld_rows, row bytes]; keys 0 .. n_keys-1 of every sequence (default: all that fit)."""
+    n_seq, ld_rows, rb = rows.shape
+    T_cap = _cache_tcap(k_cache, dims)
+    if rb != row_bytes(dims.key_format) or k_cache.shape[0] != n_seq:
+        raise ValueError("rows must be [n_seq, ld_rows, row bytes of the dims' format] and match k_cache's batch")
+    n = min(ld_rows, T_cap) if n_keys is None else n_keys
+    _check(load_library().indexer_cache_to_rows(ctypes.byref(dims), _ptr(k_cache, torch.uint8, "k_cache"), T_cap,
+                                                n_seq, n, _ptr(rows, torch.uint8, "rows"), ld_rows, _stream(stream)))
 
 
 def indexer_publish_k_paged(dims: IndexerDims, latent: torch.Tensor, wk: torch.Tensor, k_norm_w: torch.Tensor,

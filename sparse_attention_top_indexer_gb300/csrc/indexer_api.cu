@@ -157,7 +157,7 @@ extern "C" {
 
 const char* indexer_last_error(void) { return g_last_error.c_str(); }
 
-int indexer_abi_version(void) { return 402; }
+int indexer_abi_version(void) { return 403; }
 
 // ---------------------------------------------------------------------------- RoPE table
 int indexer_rope_table(const IndexerYarn* y, int rope_dim, int max_pos, float* table, indexer_stream_t stream) {
@@ -407,6 +407,46 @@ int indexer_scores(const IndexerDims* dims, const uint8_t* q_rows, const float* 
   return ok();
 }
 
+int indexer_scores_hold_test(const IndexerDims* dims, const uint8_t* q_rows, const float* w_prime, int B, int S,
+                             int start_pos, const uint8_t* k_cache, int T_cap, float* scores, void* ws,
+                             size_t ws_bytes, uint64_t wait_ns, indexer_stream_t stream) {
+  RETURN_IF(check_dims(dims));
+  RETURN_IF(check_rows(B, S, start_pos));
+  if (S < 2) return fail(INDEXER_ERR_DIMS, "the hold test runs the several-row kernel: S must be >= 2");
+  if (wait_ns < 1000ull || wait_ns > 1000000000ull) return fail(INDEXER_ERR_RANGE, "wait_ns must be in [1e3, 1e9]");
+  const int T = (start_pos + S) / dims->ratio;
+  if (T < 1) return fail(INDEXER_ERR_RANGE, "no key is visible");
+  RETURN_IF(check_cache(k_cache, T_cap, T));
+  if (!q_rows || !w_prime || !scores || !ws) return fail(INDEXER_ERR_NULL, "a required pointer is NULL");
+  if (!aligned(q_rows, 16) || !aligned(w_prime, 16) || !aligned(scores, 4) || !aligned(ws, 16))
+    return fail(INDEXER_ERR_ALIGN, "q_rows, w_prime and ws must be 16-byte aligned, scores 4-byte aligned");
+  if (ws_bytes < INDEXER_STATUS_BYTES) return fail(INDEXER_ERR_WORKSPACE, "workspace smaller than %d bytes", INDEXER_STATUS_BYTES);
+  RETURN_IF(check_arch());
+  ScoreArgs a{};
+  a.q_rows = q_rows;
+  a.w_prime = w_prime;
+  a.k_pool = k_cache;
+  a.pages_per_seq = T_cap / INDEXER_PAGE_KEYS;
+  a.scores = scores;
+  a.ld = T;
+  a.status = static_cast<uint32_t*>(ws);
+  a.sched = static_cast<uint32_t*>(ws) + kSchedWord;
+  a.B = B;
+  a.S = S;
+  a.H = dims->n_heads;
+  a.T = T;
+  a.start_pos = start_pos;
+  a.ratio = dims->ratio;
+  a.cbk = dims->cand_topk_blocks;
+  a.cbs = 1;
+  a.fp8 = is_fp8(dims) ? 1 : 0;
+  a.wait_ns = wait_ns;
+  a.hold_producer = 1;
+  const cudaError_t e = launch_scores(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "scores launch");
+  return ok();
+}
+
 // ---------------------------------------------------------------------------- selection
 int indexer_select_candidate_blocks(const IndexerDims* dims, const float* scores, int B, int S, int start_pos, int T,
                                     int32_t* blocks_out, indexer_stream_t stream) {
@@ -487,12 +527,11 @@ size_t indexer_workspace_size(const IndexerDims* dims, int B, int S, int start_p
   return ws_layout(dims, B, S, start_pos).total;
 }
 
-// The forward of indexer_forward; with `pub`, the step's key publish runs first (in the same
-// launch as the query prep when both are small).
-static int forward_impl(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
-                        int start_pos, const float* rope_cs, int max_pos, const uint8_t* k_cache, int T_cap,
-                        const int32_t* cand_in, int32_t* cand_out, int32_t* topk_out, float* scores_out, void* ws,
-                        size_t ws_bytes, indexer_stream_t stream, const PublishArgs* pub) {
+// Every check of indexer_forward's arguments (no launch, nothing enqueued).
+static int check_forward(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
+                         int start_pos, const float* rope_cs, int max_pos, const uint8_t* k_cache, int T_cap,
+                         const int32_t* cand_in, const int32_t* cand_out, const int32_t* topk_out,
+                         const float* scores_out, const void* ws, size_t ws_bytes) {
   RETURN_IF(check_prep_args(dims, q, w, B, S, start_pos, rope_cs, max_pos));
   const int T = (start_pos + S) / dims->ratio;
   RETURN_IF(check_cache(k_cache, T_cap, T));
@@ -503,7 +542,19 @@ static int forward_impl(const IndexerDims* dims, const indexer_bf16* q, const in
   if (cand_in || cand_out) RETURN_IF(check_cand_dims(dims, T));
   const WsLayout l = ws_layout(dims, B, S, start_pos);
   if (ws_bytes < l.total) return fail(INDEXER_ERR_WORKSPACE, "workspace of %zu bytes < %zu needed", ws_bytes, l.total);
-  RETURN_IF(check_arch());
+  return check_arch();
+}
+
+// The forward of indexer_forward; with `pub`, the step's key publish runs first (in the same
+// launch as the query prep when both are small).
+static int forward_impl(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
+                        int start_pos, const float* rope_cs, int max_pos, const uint8_t* k_cache, int T_cap,
+                        const int32_t* cand_in, int32_t* cand_out, int32_t* topk_out, float* scores_out, void* ws,
+                        size_t ws_bytes, indexer_stream_t stream, const PublishArgs* pub) {
+  RETURN_IF(check_forward(dims, q, w, B, S, start_pos, rope_cs, max_pos, k_cache, T_cap, cand_in, cand_out, topk_out,
+                          scores_out, ws, ws_bytes));
+  const int T = (start_pos + S) / dims->ratio;
+  const WsLayout l = ws_layout(dims, B, S, start_pos);
   cudaStream_t st = (cudaStream_t)stream;
   uint8_t* base = static_cast<uint8_t*>(ws);
   uint8_t* q_rows = base + l.q_rows;
@@ -811,8 +862,8 @@ static HostStaging host_staging(const IndexerDims* dims, int B, int S, int start
 }
 
 size_t indexer_workspace_size_host(const IndexerDims* dims, int B, int S, int start_pos, int G, int Din) {
-  if (check_dims(dims) != INDEXER_OK || B <= 0 || S <= 0 || G < 0 || Din <= 0) return 0;
-  return host_staging(dims, B, S, start_pos, G, Din).total;
+  if (check_dims(dims) != INDEXER_OK || B <= 0 || S <= 0 || G < 0 || (G > 0 && Din <= 0)) return 0;
+  return host_staging(dims, B, S, start_pos, G, G > 0 ? Din : 0).total;
 }
 
 int indexer_forward_publish_host(const IndexerDims* dims, const indexer_bf16* latent_h, int G, int Din,
@@ -824,7 +875,8 @@ int indexer_forward_publish_host(const IndexerDims* dims, const indexer_bf16* la
   RETURN_IF(check_rows(B, S, start_pos));
   if ((G > 0 && !latent_h) || !q_h || !w_h || !topk_out_h || !ws)
     return fail(INDEXER_ERR_NULL, "a required pointer is NULL");
-  if (G < 0 || Din <= 0) return fail(INDEXER_ERR_DIMS, "G must be >= 0 and Din > 0");
+  if (G < 0 || (G > 0 && Din <= 0)) return fail(INDEXER_ERR_DIMS, "G must be >= 0, and Din > 0 when G > 0");
+  if (G == 0) Din = 0;   // no key is published: the latent is not read
   const HostStaging h = host_staging(dims, B, S, start_pos, G, Din);
   if (ws_bytes < h.total)
     return fail(INDEXER_ERR_WORKSPACE, "ws has %zu bytes, indexer_workspace_size_host needs %zu", ws_bytes, h.total);
@@ -834,6 +886,13 @@ int indexer_forward_publish_host(const IndexerDims* dims, const indexer_bf16* la
   auto* q_d = reinterpret_cast<indexer_bf16*>(base + h.q);
   auto* w_d = reinterpret_cast<indexer_bf16*>(base + h.w);
   auto* top_d = reinterpret_cast<int32_t*>(base + h.top);
+  // every check of the step (publish and forward, on the staging pointers) before any copy
+  if (G > 0) {
+    PublishArgs pa{};
+    RETURN_IF(build_publish(dims, lat_d, B, G, Din, wk, k_norm_w, rope_cs, max_pos, start_pos, k_cache, T_cap, &pa));
+  }
+  RETURN_IF(check_forward(dims, q_d, w_d, B, S, start_pos, rope_cs, max_pos, k_cache, T_cap, nullptr, nullptr, top_d,
+                          nullptr, ws, h.base));
   cudaStream_t st = (cudaStream_t)stream;
   const size_t qb = (size_t)B * S * dims->n_heads * dims->head_dim * 2, wb = (size_t)B * S * dims->n_heads * 2;
   const size_t lb = (size_t)B * G * Din * 2, tb = (size_t)B * S * dims->index_topk * 4;
@@ -850,6 +909,48 @@ int indexer_forward_publish_host(const IndexerDims* dims, const indexer_bf16* la
   e = cudaMemcpyAsync(topk_out_h, top_d, tb, cudaMemcpyDeviceToHost, st);
   if (e != cudaSuccess) return cuda_fail(e, "output copy");
   return ok();
+}
+
+// ---------------------------------------------------------------------------- row-major caches
+static int layout_call(const IndexerDims* dims, const uint8_t* rows_in, uint8_t* rows_out, int n_seq, int n_keys,
+                       int ld_rows, const uint8_t* pages_in, uint8_t* pages_out, int T_cap, indexer_stream_t stream) {
+  RETURN_IF(check_dims(dims));
+  const bool to_pages = rows_in != nullptr;
+  if ((to_pages ? (const void*)pages_out : (const void*)rows_out) == nullptr ||
+      (to_pages ? (const void*)rows_in : (const void*)pages_in) == nullptr)
+    return fail(INDEXER_ERR_NULL, "rows and k_cache must not be NULL");
+  if (n_seq < 1 || n_keys < 0) return fail(INDEXER_ERR_DIMS, "n_seq must be >= 1 and n_keys >= 0");
+  if (T_cap < INDEXER_PAGE_KEYS || (T_cap % INDEXER_PAGE_KEYS))
+    return fail(INDEXER_ERR_ALIGN, "T_cap must be a positive multiple of %d (got %d)", INDEXER_PAGE_KEYS, T_cap);
+  if (n_keys > T_cap || n_keys > ld_rows)
+    return fail(INDEXER_ERR_RANGE, "n_keys %d exceeds T_cap %d or ld_rows %d", n_keys, T_cap, ld_rows);
+  const void* rp = to_pages ? (const void*)rows_in : (const void*)rows_out;
+  const void* pp = to_pages ? (const void*)pages_out : (const void*)pages_in;
+  if (!aligned(rp, 4) || !aligned(pp, 16)) return fail(INDEXER_ERR_ALIGN, "rows must be 4-byte and k_cache 16-byte aligned");
+  RETURN_IF(check_arch());
+  LayoutArgs a{};
+  a.rows_in = rows_in;
+  a.pages = pages_out;
+  a.pages_in = pages_in;
+  a.rows_out = rows_out;
+  a.n_seq = n_seq;
+  a.n_keys = n_keys;
+  a.ld_rows = ld_rows;
+  a.T_cap = T_cap;
+  a.fp8 = is_fp8(dims) ? 1 : 0;
+  const cudaError_t e = launch_layout(a, to_pages, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "layout launch");
+  return ok();
+}
+
+int indexer_cache_from_rows(const IndexerDims* dims, const uint8_t* rows, int n_seq, int n_keys, int ld_rows,
+                            uint8_t* k_cache, int T_cap, indexer_stream_t stream) {
+  return layout_call(dims, rows, nullptr, n_seq, n_keys, ld_rows, nullptr, k_cache, T_cap, stream);
+}
+
+int indexer_cache_to_rows(const IndexerDims* dims, const uint8_t* k_cache, int T_cap, int n_seq, int n_keys,
+                          uint8_t* rows, int ld_rows, indexer_stream_t stream) {
+  return layout_call(dims, nullptr, rows, n_seq, n_keys, ld_rows, k_cache, nullptr, T_cap, stream);
 }
 
 int indexer_workspace_init(void* ws, size_t ws_bytes, indexer_stream_t stream) {
@@ -880,3 +981,13 @@ int indexer_status(void* ws, indexer_stream_t stream) {
 }
 
 }  // extern "C"
+
+namespace indexer {
+int check_forward_args(const IndexerDims* dims, const uint16_t* q, const uint16_t* w, int B, int S, int start_pos,
+                       const float* rope_cs, int max_pos, const uint8_t* k_cache, int T_cap, const int32_t* cand_in,
+                       const int32_t* cand_out, const int32_t* topk_out, const float* scores_out, const void* ws,
+                       size_t ws_bytes) {
+  return check_forward(dims, q, w, B, S, start_pos, rope_cs, max_pos, k_cache, T_cap, cand_in, cand_out, topk_out,
+                       scores_out, ws, ws_bytes);
+}
+}  // namespace indexer

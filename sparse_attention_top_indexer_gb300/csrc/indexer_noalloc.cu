@@ -11,11 +11,14 @@
 // The scratch is a file-scope __device__ array of INDEXER_NOALLOC_SCRATCH_BYTES. Every
 // GPU that loads this library holds that much memory until the process exits. Its
 // device address is looked up once per device, on the first call made while that
-// device is current. All calls share the one array, so calls that overlap on the GPU
-// (different streams, or different host threads, without ordering between them) race
-// on it and must not be issued. The array keeps what the last call left in it; each
-// call clears the status word at its start, and every other byte it reads was written
-// earlier in the same call.
+// device is current, and kept for the life of the process (a cudaDeviceReset unloads the
+// module that holds the array, so this entry point must not be used on a device after a
+// reset). All calls share the one array, so calls that overlap on the GPU (different
+// streams, or different host threads, without ordering between them) race on it and
+// must not be issued. The array keeps what the last call left in it; each call that
+// passes its argument checks clears the status word at its start, and every other byte
+// it reads was written earlier in the same call. indexer_noalloc_status reads and clears
+// that status word, so a caller can learn that a bounded device wait ran out.
 #include <cstdio>
 #include <mutex>
 
@@ -74,14 +77,27 @@ extern "C" int indexer_forward_noalloc(const IndexerDims* dims, const indexer_bf
     return indexer::set_last_error(INDEXER_ERR_WORKSPACE, msg);
   }
   void* scratch = nullptr;
-  const int rc = scratch_for_current_device(&scratch);
+  int rc = scratch_for_current_device(&scratch);
+  if (rc != INDEXER_OK) return rc;
+  // every argument check of the forward (including dims for which need == 0) runs before
+  // anything is enqueued, so a rejected call leaves the shared array untouched
+  rc = indexer::check_forward_args(dims, q, w, B, S, start_pos, rope_cs, max_pos, k_cache, T_cap, cand_in, cand_out,
+                                   topk_out, scores_out, scratch, (size_t)INDEXER_NOALLOC_SCRATCH_BYTES);
   if (rc != INDEXER_OK) return rc;
   // the status word must start at zero; kernels only OR bits into it
   const cudaError_t e = cudaMemsetAsync(scratch, 0, INDEXER_STATUS_BYTES, (cudaStream_t)stream);
   if (e != cudaSuccess)
     return report(INDEXER_ERR_CUDA, "clearing the static scratch status word: %s", cudaGetErrorString(e));
-  // invalid arguments (including dims for which need == 0) are rejected by indexer_forward's
-  // own validation before anything is launched
   return indexer_forward(dims, q, w, B, S, start_pos, rope_cs, max_pos, k_cache, T_cap, cand_in, cand_out,
                          topk_out, scores_out, scratch, (size_t)INDEXER_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+// The status word of the last indexer_forward_noalloc call on the current device: waits for
+// `stream`, reads the word from the static array, clears it and returns INDEXER_OK, or the
+// error indexer_status would give for the same bits. Allocates nothing.
+extern "C" int indexer_noalloc_status(indexer_stream_t stream) {
+  void* scratch = nullptr;
+  const int rc = scratch_for_current_device(&scratch);
+  if (rc != INDEXER_OK) return rc;
+  return indexer_status(scratch, stream);
 }

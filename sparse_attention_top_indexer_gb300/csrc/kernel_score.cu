@@ -182,8 +182,8 @@ __device__ __forceinline__ void issue_tile_mma(uint32_t acc, uint32_t pa, uint32
 // The whole warp waits (bounded) for the phase, converged: every lane polls, and the warp
 // agrees on the result (a single polling lane followed by a shuffle measured ~20 % slower in
 // the score kernels). Warp-uniform result.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
-  const bool ok = mbar_wait(bar, parity);
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
+  const bool ok = mbar_wait(bar, parity, limit_ns);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -651,16 +651,20 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
   tc_fence_after();
   const uint32_t tmem = info[0];
   bool failed = false;
+  const uint64_t wait_ns = a.wait_ns ? a.wait_ns : kWaitLimitNs;
 
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ producer warp
+    // (a test of the bounded waits holds this role back: no group, copy or MMA is ever
+    // issued and every other role's first wait runs out)
+    if (!a.hold_producer) {
     pdl_wait();   // query rows, w', pages and the group list of the kernels before are complete
     const int gps = (a.S + QG - 1) / QG;                       // uniform batch: groups per sequence
     const long long total = a.groups ? (long long)a.n_groups : (long long)gps * a.B;
     uint32_t j = 0;                                            // tiles issued
     for (int k = 0;; ++k) {
       const int qb = k & 1;
-      if (k >= 2 && !warp_wait(bar_qfree(qb), (uint32_t)((k - 2) >> 1) & 1u)) {
+      if (k >= 2 && !warp_wait(bar_qfree(qb), (uint32_t)((k - 2) >> 1) & 1u, wait_ns)) {
         failed = true;
         break;
       }
@@ -727,7 +731,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
           const int st = (int)(j % C::NSTAGE);
           // the stage's previous tile: its MMA has completed (FP8: and its key scales were read)
           if (j >= (uint32_t)C::NSTAGE &&
-              !warp_wait(F::kFp8 ? bar_sread(st) : bar_free(st), ((j / C::NSTAGE) - 1) & 1u)) {
+              !warp_wait(F::kFp8 ? bar_sread(st) : bar_free(st), ((j / C::NSTAGE) - 1) & 1u, wait_ns)) {
             failed = true;
             break;
           }
@@ -741,6 +745,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
       }
       if (failed) break;
     }
+    }
   } else if (warp < 4) {
     // ------------------------------------------------------------ scale warpgroup
     const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);   // this warp's lane quadrant
@@ -750,7 +755,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
       const int qb = k & 1;
       // the four warps agree at every group start (a warp that gave up inside the previous
       // group has skipped its remaining waits and arrives here with failed set)
-      if (!named_bar_and(1, 128, !failed && warp_wait(bar_qfull(qb), (uint32_t)(k >> 1) & 1u))) {
+      if (!named_bar_and(1, 128, !failed && warp_wait(bar_qfull(qb), (uint32_t)(k >> 1) & 1u, wait_ns))) {
         failed = true;
         break;
       }
@@ -783,8 +788,8 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
         const int st = (int)(j % C::NSTAGE), c = (int)(j % C::NACC);
         // the tile has landed, and accumulator c (with its scale set) has been drained; each
         // warp goes on by itself and arrives on the accumulator's "ready" barrier
-        bool ok = warp_wait(bar_full(st), (j / C::NSTAGE) & 1u);
-        if (ok && j >= (uint32_t)C::NACC) ok = warp_wait(bar_empty(c), ((j - C::NACC) / C::NACC) & 1u);
+        bool ok = warp_wait(bar_full(st), (j / C::NSTAGE) & 1u, wait_ns);
+        if (ok && j >= (uint32_t)C::NACC) ok = warp_wait(bar_empty(c), ((j - C::NACC) / C::NACC) & 1u, wait_ns);
         if (!ok) {
           failed = true;
           continue;
@@ -805,7 +810,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
     uint32_t j = 0;
     for (int k = 0; !failed; ++k) {
       const int qb = k & 1;
-      if (!warp_wait(bar_qfull(qb), (uint32_t)(k >> 1) & 1u)) {
+      if (!warp_wait(bar_qfull(qb), (uint32_t)(k >> 1) & 1u, wait_ns)) {
         failed = true;
         break;
       }
@@ -818,7 +823,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
         const int st = (int)(j % C::NSTAGE), c = (int)(j % C::NACC);
         // the scale warps arrive on "ready" only after they have seen the tile's copy land
         // (its full barrier), so the tile is in place once "ready" is seen
-        const bool ok = warp_wait(bar_ready(c), (j / C::NACC) & 1u);
+        const bool ok = warp_wait(bar_ready(c), (j / C::NACC) & 1u, wait_ns);
         if (!ok) {
           failed = true;
           break;
@@ -846,7 +851,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
     uint32_t j = 0;
     for (int k = 0; !failed; ++k) {
       const int qb = k & 1;
-      if (!warp_wait(bar_qfull(qb), (uint32_t)(k >> 1) & 1u)) {
+      if (!warp_wait(bar_qfull(qb), (uint32_t)(k >> 1) & 1u, wait_ns)) {
         failed = true;
         break;
       }
@@ -861,7 +866,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
         for (int n = ge; n < C::N; n += EPI * kEpiThreads)
           ws[n] = n < d.nq * H ? wq[n] * *reinterpret_cast<const float*>(qstg + n * F::kRow + F::kCode) : 0.f;
         mbar_arrive(bar_wsready(qb));
-        if (!warp_wait(bar_wsready(qb), (uint32_t)(k >> 1) & 1u)) {
+        if (!warp_wait(bar_wsready(qb), (uint32_t)(k >> 1) & 1u, wait_ns)) {
           failed = true;
           break;
         }
@@ -884,7 +889,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
         // tile j's MMA has completed (its stage's barrier; the stage cannot be refilled and
         // complete again before this accumulator is released, as NSTAGE > NACC)
         const int st = (int)(j % C::NSTAGE);
-        if (!warp_wait(bar_free(st), (j / C::NSTAGE) & 1u)) {
+        if (!warp_wait(bar_free(st), (j / C::NSTAGE) & 1u, wait_ns)) {
           failed = true;
           break;
         }
@@ -948,13 +953,13 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
     const int issued = (int)info[1], mmas = (int)info[2], qph = (int)info[3];
     for (int st = 0; st < C::NSTAGE && st < issued; ++st) {
       const int last = st + ((issued - 1 - st) / C::NSTAGE) * C::NSTAGE;
-      mbar_wait(bar_full(st), (uint32_t)(last / C::NSTAGE) & 1u);
+      mbar_wait(bar_full(st), (uint32_t)(last / C::NSTAGE) & 1u, wait_ns);
     }
     for (int q = 0; q < 2 && q < qph; ++q) {
       const int last = q + ((qph - 1 - q) / 2) * 2;
-      mbar_wait(bar_qfull(q), (uint32_t)(last >> 1) & 1u);
+      mbar_wait(bar_qfull(q), (uint32_t)(last >> 1) & 1u, wait_ns);
     }
-    if (mmas > 0) mbar_wait(bar_free((mmas - 1) % C::NSTAGE), (uint32_t)((mmas - 1) / C::NSTAGE) & 1u);
+    if (mmas > 0) mbar_wait(bar_free((mmas - 1) % C::NSTAGE), (uint32_t)((mmas - 1) / C::NSTAGE) & 1u, wait_ns);
   }
   __syncthreads();
   if (tid == 0) {   // the last CTA to finish rewinds the group counter for the next launch

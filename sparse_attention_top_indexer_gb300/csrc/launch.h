@@ -7,6 +7,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+struct IndexerDims;   // include/indexer.h
+
 namespace indexer {
 
 // Launches `kernel` with programmatic stream serialisation (the kernel calls pdl_wait()
@@ -141,6 +143,10 @@ struct ScoreArgs {
                             // blocks (cand); keys outside them are not written
   int tiles_per_cta;        // set by the launcher
   int fp8;                  // FP8 key and query rows (132 bytes, 8448-byte pages) instead of MXFP4
+  // tests of the bounded waits (several-row kernel only): the waits' limit in ns (0: one
+  // second), and a producer role that is held back so that every other role's wait runs out
+  unsigned long long wait_ns = 0;
+  int hold_producer = 0;
 };
 cudaError_t launch_scores(const ScoreArgs& a, cudaStream_t stream);
 // Query rows per score CTA (QG) for n_heads H: 1 for single rows (decode), else 128 / H.
@@ -167,8 +173,26 @@ cudaError_t launch_candidates(const CandArgs& a, cudaStream_t stream);
 // same rows); for level one with few rows.
 cudaError_t launch_cand_topk(const CandArgs& c, const TopkArgs& a, cudaStream_t stream);
 
+// Row-major key rows <-> 64-key pages (both directions use the same sizes).
+struct LayoutArgs {
+  const uint8_t* rows_in = nullptr;    // [n_seq][ld_rows][row bytes] (to pages)
+  uint8_t* pages = nullptr;            // [n_seq][T_cap / 64][page bytes] (to pages)
+  const uint8_t* pages_in = nullptr;   // (to rows)
+  uint8_t* rows_out = nullptr;         // (to rows)
+  int n_seq, n_keys, ld_rows, T_cap;
+  int fp8;
+};
+cudaError_t launch_layout(const LayoutArgs& a, bool to_pages, cudaStream_t stream);
+
 // Sets the thread-local message returned by indexer_last_error(); returns code.
 int set_last_error(int code, const char* msg);
+
+// Every argument check of indexer_forward (sets the error message and returns its code, or
+// INDEXER_OK); enqueues nothing. dims is an IndexerDims of include/indexer.h.
+int check_forward_args(const ::IndexerDims* dims, const uint16_t* q, const uint16_t* w, int B, int S,
+                       int start_pos, const float* rope_cs, int max_pos, const uint8_t* k_cache, int T_cap,
+                       const int32_t* cand_in, const int32_t* cand_out, const int32_t* topk_out,
+                       const float* scores_out, const void* ws, size_t ws_bytes);
 
 // Largest T the top-k kernel accepts (keys held in shared memory).
 constexpr int kTopkMaxT = 32768;

@@ -18,6 +18,21 @@ from workloads import ROPE, WORKLOADS, Workload
 SCORE_ATOL = 1e-3
 SCORE_RTOL = 1e-2
 
+# Boundary swaps per compared case, reported at the end of the session (conftest.py) and
+# written to a JSON file: {case: {"swaps": n, "rows": r, "selected": k}}.
+SWAPS: dict = {}
+# At most this fraction of the selected entries may be boundary swaps.
+MAX_SWAP_FRACTION = 1e-3
+
+
+def record_swaps(case: str, swaps: int, rows: int, selected: int):
+    """Records a case's boundary-swap count and asserts it stays a small fraction of the
+    entries selected."""
+    prev = SWAPS.get(case, {"swaps": 0, "rows": 0, "selected": 0})
+    SWAPS[case] = {"swaps": prev["swaps"] + int(swaps), "rows": prev["rows"] + int(rows),
+                   "selected": prev["selected"] + int(selected)}
+    assert swaps <= max(2, MAX_SWAP_FRACTION * selected), f"{case}: {swaps} boundary swaps in {selected} entries"
+
 
 def bits(t: torch.Tensor) -> np.ndarray:
     """bf16 tensor -> numpy uint16 bit patterns (on the CPU)."""

@@ -42,7 +42,7 @@ def test_struct_layouts_match_header(X):
 
 
 def test_abi_version(X):
-    assert X.indexer_abi_version() == 402   # + indexer_forward_publish_host (host-buffer step)
+    assert X.indexer_abi_version() == 403   # + row-major cache conversions, no-alloc status reader
 
 
 def test_workspace_size_host_only(X):
@@ -157,6 +157,36 @@ def test_qproj_and_host_step_validation_without_launch(X):
     assert fh(topk_h=None) == -1
     assert fh(ws_bytes=n - 1) == -5
     assert fh(ws=0x10010) == -2              # the staging is carved at 256-byte offsets
+
+    # the step's own checks (cache alignment, T_cap, positions) run before any copy is enqueued
+    def fh2(G=1, Din=128, lat=0x1000, cache=0x7000, T_cap=8192, max_pos=32768, ws_bytes=None):
+        nb = X.indexer_workspace_size_host(d, 32, 1, 32767, G, Din)
+        return lib.indexer_forward_publish_host(ctypes.byref(d), lat, G, Din, 0x2000, 0x3000, 0x4000, 0x5000, 32, 1,
+                                                32767, 0x6000, max_pos, cache, T_cap, 0x8000, 0x10000,
+                                                nb if ws_bytes is None else ws_bytes, None)
+    assert fh2(cache=0x7008) == -2
+    assert fh2(T_cap=8128) == -4             # 8192 keys do not fit
+    assert fh2(max_pos=32000) == -4          # query position beyond the table
+    # no key completes this step: no latent, and Din is not read
+    assert X.indexer_workspace_size_host(d, 32, 1, 32767, 0, 0) > 0
+    assert fh2(G=0, Din=0, lat=None) not in (-1, -2, -3, -4, -5)   # passes every argument check
+
+
+def test_row_layout_validation_without_launch(X):
+    lib = X.load_library()
+    d = X.make_dims(n_heads=64, ratio=4, index_topk=16)
+    to_pages = lambda rows=0x1000, n_seq=2, n_keys=100, ld=128, cache=0x2000, T_cap=128: \
+        lib.indexer_cache_from_rows(ctypes.byref(d), rows, n_seq, n_keys, ld, cache, T_cap, None)
+    to_rows = lambda cache=0x2000, T_cap=128, n_seq=2, n_keys=100, rows=0x1000, ld=128: \
+        lib.indexer_cache_to_rows(ctypes.byref(d), cache, T_cap, n_seq, n_keys, rows, ld, None)
+    assert to_pages(rows=None) == -1 and to_rows(rows=None) == -1
+    assert to_pages(cache=None) == -1 and to_rows(cache=None) == -1
+    assert to_pages(T_cap=96) == -2                 # not a whole number of pages
+    assert to_pages(n_keys=200) == -4               # beyond T_cap
+    assert to_rows(n_keys=129, T_cap=192) == -4     # beyond ld_rows
+    assert to_pages(rows=0x1002) == -2              # rows are moved as 4-byte words
+    assert to_rows(cache=0x2008) == -2
+    assert to_pages(n_seq=0) == -3
 
 
 def test_missing_library_fails_loudly(tmp_path):

@@ -65,7 +65,7 @@ def test_forward_full_compare(X, name):
     swaps = C.compare_topk(top.cpu().numpy().reshape(-1, wl.topk), ref_top.reshape(-1, wl.topk),
                            ref_sc.reshape(-1, wl.T), wl.offset)
     _check_properties(top.cpu().numpy(), wl)
-    print(f"{name}: boundary swaps {swaps}")
+    C.record_swaps(f"forward/{name}", swaps, wl.B * wl.S, int((top >= 0).sum()))
 
 
 def test_forward_two_level_decode(X):
@@ -108,7 +108,7 @@ def test_forward_two_level_decode(X):
     for r in range(wl.B):
         v = t2[r][t2[r] >= 0]
         assert len(v) == wl.topk and np.all(keep[r, v])
-    print(f"two-level: level-two boundary swaps {swaps}")
+    C.record_swaps("forward/two_level_decode level two", swaps, wl.B * wl.S, int((top2 >= 0).sum()))
 
 
 def _sample_rows(wl: Workload, n_rand: int, seed: int):
@@ -133,7 +133,7 @@ def test_forward_prefill_sampled(X, name, n_rand):
     ref_cache = C.oracle_cache(wl, cos, sin)
     assert np.array_equal(C.pages_to_rows(cache), ref_cache)
     q, w = wl.q("cuda"), wl.w("cuda")
-    top, _, sc = _run_forward(X, wl, q, w, table, cache, want_scores=(name != "large_prefill"))
+    top, _, sc = _run_forward(X, wl, q, w, table, cache)
     top_np = top.cpu().numpy()
     _check_properties(top_np, wl)
     w_cpu = w.cpu()
@@ -152,7 +152,8 @@ def test_forward_prefill_sampled(X, name, n_rand):
         if sc is not None:
             C.assert_scores_close(sc[b, rows].cpu().numpy(), ref_sc)
         total_swaps += C.compare_topk(top_np[b, rows], ref_top, ref_sc, wl.offset)
-    print(f"{name}: boundary swaps on sampled rows {total_swaps}")
+    C.record_swaps(f"forward/{name} sampled rows", total_swaps, wl.B * len(rows),
+                   int((top_np[:, rows] >= 0).sum()))
 
 
 # ----------------------------------------------------------------------------- edge cases
@@ -220,4 +221,4 @@ def test_forward_ratios_and_chunks(X, ratio, S, start, H, fmt, topk):
     swaps = C.compare_topk(top.cpu().numpy().reshape(-1, topk), ref_top.reshape(-1, topk), ref_sc.reshape(-1, wl.T),
                            wl.offset)
     _check_properties(top.cpu().numpy(), wl)
-    print(f"ratio {ratio} S{S} start {start}: boundary swaps {swaps}")
+    C.record_swaps(f"forward/ratio {ratio} S{S} start {start} fmt {fmt}", swaps, wl.B * wl.S, int((top >= 0).sum()))

@@ -95,7 +95,7 @@ def test_fp8_decode_forward_and_split(X, B, H, start, topk):
     X.indexer_topk(d, sc2, wl.start_pos, top2)
     X.indexer_status(ws)
     assert torch.equal(sc2, sc) and torch.equal(top2, top)
-    print(f"fp8 decode B{B} H{H}: boundary swaps {swaps}")
+    C.record_swaps(f"fp8/decode B{B} H{H}", swaps, wl.B, int((top >= 0).sum()))
 
 
 @pytest.mark.parametrize("S,H,topk", [(256, 8, 16), (2048, 64, 128), (1024, 128, 64)])
@@ -113,7 +113,7 @@ def test_fp8_prefill_forward(X, S, H, topk):
     C.assert_scores_close(sc.cpu().numpy(), ref_sc)
     swaps = C.compare_topk(top.cpu().numpy().reshape(-1, wl.topk), ref_top.reshape(-1, wl.topk),
                            ref_sc.reshape(-1, wl.T), wl.offset)
-    print(f"fp8 prefill S{S} H{H}: boundary swaps {swaps}")
+    C.record_swaps(f"fp8/prefill S{S} H{H}", swaps, wl.B * wl.S, int((top >= 0).sum()))
 
 
 def test_fp8_two_level_decode(X):
@@ -144,7 +144,7 @@ def test_fp8_two_level_decode(X):
                                      cand_block_size=wl.cand_block_size)
     swaps = C.compare_topk(top2.cpu().numpy().reshape(-1, wl.topk), ref_top2.reshape(-1, wl.topk),
                            ref_sc2.reshape(-1, wl.T), wl.offset)
-    print(f"fp8 two-level: level-two boundary swaps {swaps}")
+    C.record_swaps("fp8/two-level level two", swaps, wl.B, int((top2 >= 0).sum()))
 
 
 def test_fp8_mixed_batch_page_pool(X):

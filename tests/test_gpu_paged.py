@@ -122,7 +122,7 @@ def test_forward_paged_mixed_against_oracle(X, name):
                                        m.rope_dim, m.topk, m.offset)
         C.assert_scores_close(sc[r0:r0 + S, :T], ref_sc[0, :, :T])
         swaps += C.compare_topk(top[r0:r0 + S], ref_top[0], ref_sc[0, :, :T].reshape(S, T), m.offset)
-    print(f"{name}: boundary swaps {swaps}")
+    C.record_swaps(f"paged/{name}", swaps, int(top.shape[0]), int((top >= 0).sum()))
 
 
 @pytest.mark.parametrize("name", ["decode", "tiny_prefill"])
@@ -192,7 +192,7 @@ def test_forward_paged_two_level(X):
                                m.rope_dim, m.topk, m.offset, cand_in=ref_cand[None, b:b + 1],
                                cand_block_size=64)
         swaps += C.compare_topk(top2[b:b + 1], rt[0], rsc[0].reshape(1, -1), m.offset)
-    print(f"two-level paged: level-two boundary swaps {swaps}")
+    C.record_swaps("paged/two-level level two", swaps, int(top2.shape[0]), int((top2 >= 0).sum()))
 
 
 def test_paged_bad_metadata_is_reported(X):

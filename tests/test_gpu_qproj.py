@@ -49,18 +49,31 @@ def test_qproj_parity(X, name, B, S, H, Kq, start):
     ref_q = O.project_queries(C.bits(qr), C.bits(wq), H)
     got_q = C.bits(qo)
     diff = got_q != ref_q
-    assert diff.mean() < 1e-2, f"{diff.mean():.2e} of q differ"
+    assert diff.mean() < 1e-3, f"{diff.mean():.2e} of q differ"
     a64, b64 = O.bf16_to_f64(C.bits(qr)).reshape(-1, Kq), O.bf16_to_f64(C.bits(wq))
     exact = (a64 @ b64.T).reshape(got_q.shape)
     mag = (np.abs(a64) @ np.abs(b64).T).reshape(got_q.shape)
-    err = np.abs(O.bf16_to_f64(got_q) - exact)
-    assert np.all(err <= 2.0 ** -8 * np.abs(exact) + Kq * 2.0 ** -24 * mag + 2.0 ** -133)
+    acc_bound = Kq * 2.0 ** -24 * mag
+    g64, r64 = O.bf16_to_f64(got_q), O.bf16_to_f64(ref_q)
+    err = np.abs(g64 - exact)
+    assert np.all(err <= 2.0 ** -8 * np.abs(exact) + acc_bound + 2.0 ** -133)
+    # a value differs only where the exact sum lies within the accumulation bound of the bf16
+    # rounding midpoint between the two results (or, where the sum cancels, of either result)
+    mid = 0.5 * (g64 + r64)
+    near_mid = np.abs(exact - mid) <= acc_bound + 2.0 ** -133
+    assert np.all(near_mid[diff] | (err[diff] <= acc_bound[diff] + 2.0 ** -133))
     # rows and w': the oracle's query prep of the GPU's own q (the quantiser decides in the
     # kernel's precision), bit-exact
     ref_rows, ref_w, _ = O.prep_queries(got_q, C.bits(w), cos, sin, start, wl.rope_dim, H)
     got = rows.cpu().numpy()
     assert np.array_equal(got, ref_rows), f"{np.sum(np.any(got != ref_rows, axis=-1))} query rows differ"
     assert np.allclose(wp.cpu().numpy(), ref_w, rtol=2e-7, atol=0)
+    # end to end from qr: the oracle's rows of its own (exactly rounded) q differ from the
+    # kernel's only in head vectors that hold one of the q values counted above
+    ref_rows_e2e, _, _ = O.prep_queries(ref_q, C.bits(w), cos, sin, start, wl.rope_dim, H)
+    row_diff = np.any(got != ref_rows_e2e, axis=-1)
+    assert np.all(np.any(diff, axis=-1)[row_diff]), "a query row differs without a differing q value"
+    assert row_diff.mean() <= np.any(diff, axis=-1).mean()
     # without q_out: the same rows
     rows2 = torch.zeros_like(rows)
     X.indexer_prep_q_proj(d, qr, wq, w, start, table, rows2, wp, ws)

@@ -291,6 +291,33 @@ def test_rope_f32_rounds_each_product_then_the_sum():
     assert y[0, 65] == 0x4001
 
 
+# A case where the rotation order still shows after the fp4 quantiser. x0 = -0.75 (bf16
+# 0xBF40), x1 = 1 + 2^-7 (0x3F81), c = f32 0x3F2EE23C, s = 0.5; a second pair holds 1.5
+# (unrotated), which fixes block 2's scale at 2^-2 (amax 1.5 -> e = -2, byte 125). By hand:
+#   x0*s = -0.375 exactly; x1*c = 0.6884765625 + 2.79e-8 rounds in f32 to 0.6884765625;
+#   y1 = f32(-0.375 + 0.6884765625) = 0.3134765625 = 0.3125 + 2^-10, the midpoint between
+#   bf16 0.3125 and 0.314453125, so it rounds to even: 0.3125. At scale 2^-2 that is 1.25,
+#   the e2m1 tie between 1.0 (code 2) and 1.5 (code 3): code 2.
+# A fused multiply-add would keep the 2.79e-8, round y1 up to bf16 0.314453125 and give
+# code 3. This is the case the GPU parity test drives through the query prep.
+ROPE_TIE_Q = (0xBF40, 0x3F81)
+ROPE_TIE_CS = (np.array([0x3F2EE23C], np.uint32).view(np.float32)[0], np.float32(0.5))
+
+
+def test_rope_order_shows_after_quantisation():
+    x = np.zeros((1, 1, 1, 128), np.uint16)
+    x[..., 64], x[..., 65] = ROPE_TIE_Q
+    x[..., 66] = 0x3FC0                                   # 1.5, rotated by the identity pair
+    cos = np.ones((1, 32), np.float32)
+    sin = np.zeros((1, 32), np.float32)
+    cos[0, 0], sin[0, 0] = ROPE_TIE_CS
+    rows, _, qrot = O.prep_queries(x, np.full((1, 1, 1), 0x3F80, np.uint16), cos, sin, 0, 64, 1)
+    assert qrot[0, 0, 0, 65] == 0x3EA0                    # bf16 0.3125
+    codes, scales = O.unpack_row68(rows[0, 0, 0])
+    assert scales[2] == 125
+    assert codes[65] == 2
+
+
 # --------------------------------------------------------------------- query prep
 def test_query_head_weight_factor_matches_the_pages_constants():
     """w' = weights * softmax_scale * n_heads^-0.5 with softmax_scale = index_head_dim^-0.5
