@@ -1,28 +1,32 @@
 #!/usr/bin/env python3
 """Indexer hot-path benchmark (one JSON line on rank 0).
 
-Default workload: decode -- 32 sequences, one query each at start_pos 32767
-(8192 compressed positions at ratio 4), 64 fp4 index heads, top-2048. One step
-is the whole hot path for that batch: publish the key of the group the token
-completes, then query prep + scores + causal mask + top-k (indexer_forward).
+Default workload: the large prefill -- 2 sequences of 32768 query rows from start_pos 0
+(8192 compressed positions each at ratio 4), 64 fp4 index heads, top-2048, offset 8192,
+5 % of the rows with head weights x8. One step is the whole hot path for that batch:
+publish the keys of the step's groups, then query prep + scores + causal mask + top-k
+(indexer_forward_publish). The decode, prefill, two-level decode and tiny prefill
+workloads are measured in the same run and reported under "per_config".
 
   value        queries/s over all ranks, inputs resident in HBM, CUDA-graph
                replay of the steps, CUDA events on the launching stream.
-               16 rotating key-cache copies (285 MB) keep the caches out of L2.
-  e2e          the same metric through the public C-ABI calls with pinned HOST
-               buffers: per step q/w/latent host->device, the calls, top-k
+               Inputs larger than L2 (1.07 GB of q per step) or rotating copies.
+  e2e          the same metric through the public C-ABI call with pinned HOST
+               buffers: per step the inputs host->device, the call, the top-k
                device->host, all inside the timed region.
-  roofline     the dominant kernel (scores): algorithmic bytes (or flops) per
+  roofline     the dominant kernel (scores): algorithmic flops (or bytes) per
                launch / its average duration, from CUDA events around a graph
                of back-to-back launches of that kernel alone (its own entry
-               point, rotating inputs), against the measured peak in
-               MEASURED_PEAKS.json.
+               point), against the measured peak in MEASURED_PEAKS.json.
+  step_roofline the whole step against the same peak (the step's algorithmic
+               work / the step's time).
   cpu_baseline the CPU oracle, as it stands, on a bounded sample of the same
-               workload (rank 0, N=1).
+               workload, one process per host core (rank 0, N=1).
 
 --impl reference times that oracle as the reference arm.
-Multi-GPU (torchrun): every rank runs its own replica of the workload (decode
-shards by sequence, no data-path collective); the time is the max over ranks.
+Multi-GPU (torchrun): every rank runs its own replica of the workload (the path
+shards by sequence and query row, no data-path collective); the time is the max
+over ranks.
 """
 from __future__ import annotations
 
@@ -60,16 +64,30 @@ def fmt_of(wl) -> dict:
 ROTATE = 16
 
 
+HEADLINE = "large_prefill"
+# timed steps of each workload when --steps is not given (each run a fraction of a second)
+DEFAULT_STEPS = {"large_prefill": 40, "prefill": 400, "prefill_fp8": 400, "prefill_qproj": 200, "decode": 5000,
+                 "decode_fp8": 5000, "two_level_decode": 2000, "tiny_prefill": 5000}
+# the other configurations, measured in the same run as the headline and reported under per_config
+PER_CONFIG = ("tiny_prefill", "decode", "prefill", "two_level_decode")
+
+
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20000)
-    p.add_argument("--warmup", type=int, default=2000)
+    p.add_argument("--steps", type=int, default=None)
+    p.add_argument("--warmup", type=int, default=None)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="decode", choices=sorted(WORKLOADS) + sorted(MIXED))
+    p.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS) + sorted(MIXED))
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
-    return p.parse_args()
+    p.add_argument("--no-per-config", action="store_true", help="skip the other configurations' sub-records")
+    a = p.parse_args()
+    if a.steps is None:
+        a.steps = DEFAULT_STEPS.get(a.workload, 1000)
+    if a.warmup is None:
+        a.warmup = max(3, a.steps // 10)
+    return a
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -329,8 +347,22 @@ def capture(fn, n: int):
     return g
 
 
-def run_ours(args, dist: Dist):
-    wl = WORKLOADS[args.workload]
+def step_units(wl: Workload):
+    """Algorithmic work of one whole step (key publish, query prep, scores, top-k): HBM bytes
+    (keys read once, bf16 q and w in, the step's latents in, indices out) and tensor flops."""
+    u = score_units(wl)
+    rb = fmt_of(wl)["row"]
+    keys_pub = wl.B * (1 if (wl.S == 1 and wl.start_pos > 0) else wl.T)
+    nvec = wl.B * wl.S * wl.H
+    by = (wl.B * wl.T * rb + keys_pub * (wl.D * 2 + rb) + nvec * (wl.D * 2 + 2) + wl.B * wl.S * wl.topk * 4)
+    return {"bytes": by, "flops": u["flops"], "pairs": u["pairs"]}
+
+
+def run_ours(args, dist: Dist, name=None, steps=None, warmup=None, with_e2e=True):
+    name = name or args.workload
+    steps = steps or args.steps
+    warmup = args.warmup if warmup is None else warmup
+    wl = WORKLOADS[name]
     dev = torch.device("cuda", dist.local)
     torch.cuda.set_device(dev)
     big_inputs = wl.B * wl.S * wl.H * wl.D * 2 > 256 * 1024 * 1024
@@ -344,10 +376,10 @@ def run_ours(args, dist: Dist):
 
     # graphs of `rotate` steps (+ remainders) replayed for the warm-up and the timed region
     g_full = capture(st.step, rotate)
-    rem = args.steps % rotate
+    rem = steps % rotate
     g_rem = capture(st.step, rem) if rem else None
-    n_full = args.steps // rotate
-    for _ in range(max(1, math.ceil(args.warmup / rotate))):
+    n_full = steps // rotate
+    for _ in range(max(1, math.ceil(warmup / rotate))):
         g_full.replay()
     torch.cuda.synchronize()
 
@@ -372,31 +404,41 @@ def run_ours(args, dist: Dist):
     ms = e0.elapsed_time(e1)
     ms_max = dist.max(ms)
     X.indexer_status(st.ws)
+    del g_full, g_rem
 
-    queries = dist.world * wl.B * wl.S * args.steps
+    queries = dist.world * wl.B * wl.S * steps
     value = queries / (ms_max / 1e3)
     units = score_units(wl)
-    key_scores = dist.world * units["pairs"] * args.steps / (ms_max / 1e3)
+    key_scores = dist.world * units["pairs"] * steps / (ms_max / 1e3)
 
     # per-kernel breakdown (split entry points, events between kernels, graph replay)
     kernel_ms = breakdown(st, rotate)
 
     # end to end through the public API with pinned host buffers
-    e2e = run_e2e(st, args, dist)
+    e2e = run_e2e(st, steps, dist) if with_e2e else None
 
     peaks = measured_peaks()
     score_ms = kernel_ms.get("scores")
+    fm = fmt_of(wl)
+    step_ms = ms_max / steps
+    su = step_units(wl)
     if wl.S == 1:
         achieved = units["bytes"] / (score_ms / 1e3) / 1e9 if score_ms else None
         peak = peaks["hbm_gbs"]
         roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak if achieved else None,
                 "traffic": profile_traffic(f"scores_{wl.name}"),
-                "algorithmic_bytes_per_launch": units["bytes"], "kernel": f"score_kernel<{wl.H},1,1,{fmt_of(wl)['name']}>",
+                "algorithmic_bytes_per_launch": units["bytes"], "kernel": f"score_kernel<{wl.H},1,1,{fm['name']}>",
                 "kernel_ms": score_ms, "peak_source": f"{peaks['source']} hbm_gbs"}
+        sa = su["bytes"] / (step_ms / 1e3) / 1e9
+        step_roof = {"bound": "hbm", "achieved": sa, "peak": peak, "unit": "GB/s", "frac": sa / peak,
+                     "algorithmic_bytes_per_step": su["bytes"], "step_ms": step_ms}
+        st_ms = (kernel_ms.get("scores") or 0) + (kernel_ms.get("topk") or 0)
+        if st_ms:   # scoring + top-k, the two kernels the decode target names
+            step_roof["scores_topk"] = {"ms": st_ms, "achieved": units["bytes"] / (st_ms / 1e3) / 1e9,
+                                        "frac": units["bytes"] / (st_ms / 1e3) / 1e9 / peak}
     else:
         achieved = units["flops"] / (score_ms / 1e3) / 1e12 if score_ms else None
-        fm = fmt_of(wl)
         peak = peaks["bf16_tflops"] * fm["ratio"]
         roof = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": achieved / peak if achieved else None,
@@ -404,13 +446,17 @@ def run_ours(args, dist: Dist):
                 "algorithmic_flops_per_launch": units["flops"], "kernel": "score_rows_kernel",
                 "kernel_ms": score_ms,
                 "peak_source": f"{peaks['source']} bf16_tflops x {fm['ratio']:g} (nominal {fm['label']}/bf16)"}
+        sa = su["flops"] / (step_ms / 1e3) / 1e12
+        step_roof = {"bound": "tensor", "achieved": sa, "peak": peak, "unit": "TFLOP/s", "frac": sa / peak,
+                     "algorithmic_flops_per_step": su["flops"], "step_ms": step_ms}
 
     # the HBM-bound helper kernels against the same peak: algorithmic bytes per launch
-    rb = fmt_of(wl)["row"]
+    rb = fm["row"]
     nvec = wl.B * wl.S * wl.H
     keys = wl.B * (1 if st.decode else wl.T)
     helper_bytes = {"prep_q": nvec * (wl.D * 2 + 2 + rb + 4),
-                    "publish": keys * (wl.D * 2 + rb) + wl.D * wl.D * 2 + wl.D * 2}
+                    "publish": keys * (wl.D * 2 + rb) + wl.D * wl.D * 2 + wl.D * 2,
+                    "topk": units["pairs"] * 4 + wl.B * wl.S * wl.topk * 4}
     helpers = {k: {"bytes": b, "GB/s": b / (kernel_ms[k] / 1e3) / 1e9,
                    "frac": b / (kernel_ms[k] / 1e3) / 1e9 / peaks["hbm_gbs"]}
                for k, b in helper_bytes.items() if kernel_ms.get(k)}
@@ -420,24 +466,45 @@ def run_ours(args, dist: Dist):
         helpers["prep_q_proj"] = {"flops": pf, "TFLOP/s": pa, "frac": pa / peaks["bf16_tflops"],
                                   "peak_source": f"{peaks['source']} bf16_tflops"}
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": fmt_of(wl)["dtype"], "data": "synthetic",
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": steps,
+        "warmup": warmup, "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": fm["dtype"], "data": "synthetic",
         "config": {"workload": describe(wl), "B": wl.B, "S": wl.S, "start_pos": wl.start_pos, "T": wl.T,
                    "H": wl.H, "topk": wl.topk, "ratio": wl.ratio,
                    "l2": (f"{rotate} rotating key caches / inputs "
-                          f"({rotate * wl.B * wl.T_cap * (132 if wl.key_format == 1 else 68) / 1e6:.0f} MB)"
-                          if rotate > 1 else "inputs larger than L2"),
+                          f"({rotate * wl.B * wl.T_cap * rb / 1e6:.0f} MB of keys)"
+                          if rotate > 1 else
+                          f"inputs larger than L2 ({wl.B * wl.S * wl.H * wl.D * 2 / 1e9:.2f} GB of q per step)"),
                    "timing": "CUDA-graph replay, CUDA events on the launching stream"},
         "key_scores_per_s": key_scores,
         "kernel_ms": kernel_ms,
         "roofline": roof,
+        "step_roofline": step_roof,
         "helper_rooflines": helpers,
         "e2e": e2e,
-        "gpu_launches": st.launches_per_step() * args.steps,
+        "gpu_launches": st.launches_per_step() * steps,
         "clocks": clocks,
     }
+    del st
+    torch.cuda.empty_cache()
     return line, wl
+
+
+def per_config_records(args, dist: Dist) -> dict:
+    """The other configurations, measured in the same run: value, step time, kernel times,
+    the dominant kernel's roofline and the whole step's, and e2e through the host-buffer call."""
+    out = {}
+    for name in PER_CONFIG:
+        if name == args.workload:
+            continue
+        steps = DEFAULT_STEPS[name]
+        line, _ = run_ours(args, dist, name=name, steps=steps, warmup=max(3, steps // 10))
+        out[name] = {k: line[k] for k in ("value", "unit", "ms_per_step", "steps", "warmup", "key_scores_per_s",
+                                          "kernel_ms", "roofline", "step_roofline", "e2e", "gpu_launches",
+                                          "clocks")}
+        out[name]["workload"] = line["config"]["workload"]
+        out[name]["l2"] = line["config"]["l2"]
+    return out
 
 
 # ----------------------------------------------------------------------------- mixed batches
@@ -629,7 +696,7 @@ def breakdown(st: Setup, rotate: int, reps: int = 20):
     return out
 
 
-def run_e2e(st: Setup, args, dist: Dist):
+def run_e2e(st: Setup, n_steps: int, dist: Dist):
     wl, X = st.wl, st.X
     R = st.rotate
     tag = "q2" if wl.two_level else "q"
@@ -639,7 +706,7 @@ def run_e2e(st: Setup, args, dist: Dist):
     outh = [torch.empty(st.top.shape, dtype=torch.int32).pin_memory() for _ in range(R)]
     qd, wd, ld = torch.empty_like(st.q[tag][0]), torch.empty_like(st.w[tag][0]), torch.empty_like(st.lat[0])
     q1 = st.q.get("q1")
-    steps = args.steps if wl.S == 1 else min(args.steps, 64)
+    steps = n_steps if wl.S == 1 else min(n_steps, 64)
 
     if wl.fused_q:   # the query latent crosses the bus instead of q
         qh = [t.cpu().pin_memory() for t in st.qr]
@@ -707,71 +774,109 @@ def describe(wl: Workload) -> str:
 
 # ----------------------------------------------------------------------------- oracle arm / baseline
 class OracleSample:
-    """The CPU oracle on sequences of the workload (keys published once, untimed)."""
+    """The CPU oracle on one sequence of the workload (its keys published once, untimed).
+    A decode step is the sequence's query row with the publish of the key its token
+    completes; a prefill step is a set of query rows sampled across the sequence (rows are
+    independent given the keys), each generated on its own from the seeded streams."""
 
-    def __init__(self, wl: Workload, n_seq: int):
+    def __init__(self, wl: Workload, b: int = 0):
         import oracle as O
-        self.O, self.wl = O, wl
+        self.O, self.wl, self.b = O, wl, b
         from tests import cases as C
         self.C = C
         self.cos, self.sin = C.oracle_table(wl.max_pos, wl.rope_dim)
         self.wk, self.knw = C.bits(wl.wk()), C.bits(wl.k_norm_w())
-        self.n_seq = min(n_seq, wl.B)
-        lat = wl.latent()
-        self.cache = []
-        for b in range(self.n_seq):
-            slots, rows, _ = O.publish_keys(C.bits(lat[b:b + 1]), self.wk, self.knw, self.cos, self.sin, 0, wl.ratio,
-                                            wl.rope_dim, wl.norm_eps, fmt=fmt_of(wl)["name"])
-            c = np.zeros((1, wl.T_cap, fmt_of(wl)["row"]), np.uint8)
-            c[0, slots] = rows[0]
-            self.cache.append(c)
-        self.q = C.bits(wl.q()[: self.n_seq])
-        self.w = C.bits(wl.w()[: self.n_seq])
+        self.fmt = fmt_of(wl)
+        lat = C.bits(wl.latent()[b:b + 1])
+        slots, rows, _ = O.publish_keys(lat, self.wk, self.knw, self.cos, self.sin, 0, wl.ratio, wl.rope_dim,
+                                        wl.norm_eps, fmt=self.fmt["name"])
+        self.cache = np.zeros((1, wl.T_cap, self.fmt["row"]), np.uint8)
+        self.cache[0, slots] = rows[0]
+        self.w = C.bits(wl.w()[b])                                   # [S, H], heavy rows included
         if wl.fused_q:   # queries from the query latent through wq_b, inside the timed step
-            self.qr, self.wq = C.bits(wl.qr()[: self.n_seq]), C.bits(wl.wq_b())
-        self.dl = C.bits(wl.decode_latent()[: self.n_seq]) if wl.S == 1 else None
+            self.qr, self.wq = C.bits(wl.qr()[b]), C.bits(wl.wq_b())
+        self.dl = C.bits(wl.decode_latent()[b:b + 1]) if wl.S == 1 and wl.start_pos > 0 else None
 
-    def query(self, b: int, key_frac: float = 1.0):
-        """Oracle step for sequence b's query row(s): step-key publish (decode), prep, scores, top-k."""
-        O, wl = self.O, self.wl
+    def run(self, rows) -> int:
+        """One oracle step over the given query rows of the sequence (publish of the step's key
+        for decode, query prep, scores, causal mask, top-k); returns the rows done."""
+        O, wl, C = self.O, self.wl, self.C
+        rows = np.asarray(rows)
         if self.dl is not None:
-            slots, rows, _ = O.publish_keys(self.dl[b:b + 1], self.wk, self.knw, self.cos, self.sin, wl.start_pos,
-                                            wl.ratio, wl.rope_dim, wl.norm_eps, fmt=fmt_of(wl)["name"])
-            self.cache[b][0, slots] = rows[0]
-        T = max(1, int(math.ceil(wl.T * key_frac)))
-        q = O.project_queries(self.qr[b:b + 1], self.wq, wl.H) if wl.fused_q else self.q[b:b + 1]
-        rows_q, wprime, _ = O.prep_queries(q, self.w[b:b + 1], self.cos, self.sin, wl.start_pos,
-                                           wl.rope_dim, wl.H, fmt=fmt_of(wl)["name"])
-        vis = np.minimum(O.visible_lens(wl.start_pos, wl.S, wl.ratio), T)
-        sc = O.index_scores(rows_q, wprime, self.cache[b], T, vis)
-        O.topk_positions(sc[0], vis, max(1, int(math.ceil(wl.topk * key_frac))), wl.offset, T)
+            slots, krows, _ = O.publish_keys(self.dl, self.wk, self.knw, self.cos, self.sin, wl.start_pos,
+                                             wl.ratio, wl.rope_dim, wl.norm_eps, fmt=self.fmt["name"])
+            self.cache[0, slots] = krows[0]
+        flat = [self.b * wl.S + int(r) for r in rows]
+        if wl.fused_q:
+            q = O.project_queries(self.qr[rows][None], self.wq, wl.H)
+        else:
+            q = C.bits(wl.q_rows(flat))[None]                       # [1, R, H, D]
+        pos = wl.start_pos + rows
+        q_rows, wprime, _ = O.prep_queries(q, self.w[rows][None], self.cos, self.sin, wl.start_pos, wl.rope_dim,
+                                           wl.H, row_positions=pos, fmt=self.fmt["name"])
+        vis = O.visible_lens(wl.start_pos, len(rows), wl.ratio, row_positions=pos)
+        sc = O.index_scores(q_rows, wprime, self.cache, wl.T, vis)
+        O.topk_positions(sc[0], vis, wl.topk, wl.offset, wl.T)
+        return len(rows)
+
+
+def _oracle_worker(job):
+    """One host process of the oracle baseline: an OracleSample of one sequence, then steps of
+    `rows_per_step` sampled rows until `seconds` have passed (or exactly `n_steps` steps).
+    Returns (rows done, wall seconds, CPU seconds)."""
+    name, worker, seconds, n_steps, n_warm, rows_per_step = job
+    wl = WORKLOADS[name]
+    samp = OracleSample(wl, b=worker % wl.B)
+    rng = np.random.default_rng(1000 + worker)
+    pick = lambda: np.sort(rng.choice(wl.S, size=min(rows_per_step, wl.S), replace=False))
+    for _ in range(n_warm):
+        samp.run(pick())
+    n = 0
+    c0, t0 = time.process_time(), time.perf_counter()
+    k = 0
+    while True:
+        n += samp.run(pick())
+        k += 1
+        if (n_steps and k >= n_steps) or (not n_steps and time.perf_counter() - t0 >= seconds):
+            break
+    return n, time.perf_counter() - t0, time.process_time() - c0
+
+
+def _oracle_pool_run(name: str, seconds: float, n_steps: int, n_warm: int, rows_per_step: int):
+    """Runs _oracle_worker in one spawned process per host core (single-threaded numpy each)."""
+    import multiprocessing as mp
+    n = max(1, os.cpu_count() or 1)
+    saved = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in saved:
+        os.environ[k] = "1"
+    try:
+        with mp.get_context("spawn").Pool(n) as pool:
+            res = pool.map(_oracle_worker, [(name, i, seconds, n_steps, n_warm, rows_per_step) for i in range(n)])
+    finally:
+        for k, v in saved.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    rows = sum(r[0] for r in res)
+    wall = max(r[1] for r in res)
+    cpu = sum(r[2] for r in res)
+    return rows, wall, cpu, n
+
+
+def _rows_per_step(wl: Workload) -> int:
+    return 1 if wl.S == 1 else 2
 
 
 def cpu_baseline(wl: Workload, seconds: float):
-    if wl.S != 1:
-        # prefill: one query row group of the workload per sample step (rows are independent)
-        wl_s = dataclasses_replace(wl, S=min(wl.S, 64), B=1)
-    else:
-        wl_s = wl
-    samp = OracleSample(wl_s, n_seq=4)
-    n = 0
-    c0, t0 = time.process_time(), time.perf_counter()
-    while True:
-        samp.query(n % samp.n_seq)
-        n += 1
-        if time.perf_counter() - t0 >= seconds:
-            break
-    wall = time.perf_counter() - t0
-    cpu = time.process_time() - c0
-    queries = n * wl_s.S
-    return {"value": queries / wall, "unit": UNIT, "cores": max(1, round(cpu / wall)), "kind": "oracle",
-            "sample": f"{n} oracle steps of {wl_s.S} query row(s) each ({describe(wl_s)}), {wall:.1f} s wall, "
-                      f"keys published untimed; numpy f64 on {os.cpu_count()} host cores"}
-
-
-def dataclasses_replace(wl, **kw):
-    import dataclasses
-    return dataclasses.replace(wl, **kw)
+    rps = _rows_per_step(wl)
+    rows, wall, cpu, n = _oracle_pool_run(wl.name, seconds, 0, 1, rps)
+    return {"value": rows / wall, "unit": UNIT, "cores": n, "nproc": os.cpu_count(), "kind": "oracle",
+            "cpu_seconds_per_wall_second": cpu / wall,
+            "sample": (f"{n} processes (one per host core, single-threaded numpy f64), each on one sequence of "
+                       f"{describe(wl)}: steps of {rps} query row(s) drawn uniformly over the sequence's rows "
+                       f"(decode: the step's key publish too), {rows} rows in {wall:.1f} s wall; keys published "
+                       f"untimed")}
 
 
 def run_reference(args, dist: Dist):
@@ -782,30 +887,19 @@ def run_reference(args, dist: Dist):
     wl = WORKLOADS[args.workload]
     if dist.rank != 0:
         return None, wl
-    wl_s = wl if wl.S == 1 else dataclasses_replace(wl, S=min(wl.S, 64), B=1)
-    samp = OracleSample(wl_s, n_seq=2)
-    t = time.perf_counter()
-    samp.query(0)
-    t_q = time.perf_counter() - t
-    budget = 150.0 / max(1, args.steps + args.warmup)        # seconds per step so the run ends in minutes
-    frac = min(1.0, budget / max(t_q, 1e-6))
-    for i in range(args.warmup):
-        samp.query(i % samp.n_seq, frac)
-    c0, t0 = time.process_time(), time.perf_counter()
-    for i in range(args.steps):
-        samp.query(i % samp.n_seq, frac)
-    wall = time.perf_counter() - t0
-    cpu = time.process_time() - c0
-    value = args.steps * frac * wl_s.S / wall
-    sample = (f"each step: one sequence's {wl_s.S} query row(s) of {describe(wl_s)}, scored against "
-              f"{frac:.4f} of its keys (value scaled by that fraction); keys published untimed")
+    rps = _rows_per_step(wl)
+    rows, wall, cpu, n = _oracle_pool_run(wl.name, 0.0, args.steps, args.warmup, rps)
+    value = rows / wall
+    sample = (f"each step: every one of {n} processes (one per host core, single-threaded numpy f64) runs {rps} "
+              f"query row(s) of one sequence of {describe(wl)}, drawn uniformly over its rows (decode: with the "
+              f"step's key publish); keys published untimed")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": wall * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
         "config": {"workload": describe(wl), "B": wl.B, "S": wl.S, "start_pos": wl.start_pos, "T": wl.T, "H": wl.H,
                    "topk": wl.topk, "ratio": wl.ratio},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": max(1, round(cpu / wall)), "kind": "oracle",
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": n, "nproc": os.cpu_count(), "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -822,6 +916,8 @@ def main():
             line = run_mixed(args, dist)
         else:
             line, wl = run_ours(args, dist)
+            if args.workload == HEADLINE and not args.no_per_config:
+                line["per_config"] = per_config_records(args, dist)
             if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
                 line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
         if dist.rank == 0 and line is not None:
