@@ -110,6 +110,11 @@ typedef struct IndexerDims {
     float norm_eps;            /* k_norm RMSNorm epsilon */
     int32_t key_format;        /* INDEXER_KEY_MXFP4 (0) or INDEXER_KEY_FP8 (1): the row format of
                                   keys and quantised queries, see below */
+    int32_t n_heads_total;     /* 0, or the model's index_n_heads when this call holds only a shard
+                                  of n_heads of them (head-parallel scoring: [index-keys]
+                                  Indexer.__init__ n_local_heads = index_n_heads // world_size, the
+                                  head weights still scaled by index_n_heads^-0.5, and
+                                  Indexer.forward all-reduces the partial scores); >= n_heads */
 } IndexerDims;
 
 /* YaRN parameters of the compressed layers ([compress] yarn_freqs_cis). */
@@ -166,6 +171,10 @@ int indexer_publish_k(const IndexerDims* dims, const indexer_bf16* latent, int B
  *   q_rows:  uint8 [B][S][H][68] quantised query rows (same row format as keys), 16-byte
  *            aligned
  *   w_prime: float [B][S][H] = w * 128^-0.5 * H^-0.5 (f32)
+ * Head-parallel: with dims->n_heads_total set, q and w hold this call's n_heads heads and
+ *   w' = w * 128^-0.5 * n_heads_total^-0.5, so the scores of indexer_scores are this
+ *   shard's part of the head sum; the shards' scores add up (an all-reduce) to the full
+ *   score, masked entries staying -inf, before indexer_topk.
  * ------------------------------------------------------------------------- */
 int indexer_prep_q(const IndexerDims* dims, const indexer_bf16* q, const indexer_bf16* w, int B, int S,
                    int start_pos, const float* rope_cs, int max_pos, uint8_t* q_rows, float* w_prime,

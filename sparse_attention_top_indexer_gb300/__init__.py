@@ -44,7 +44,7 @@ class IndexerDims(ctypes.Structure):
         ("n_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("rope_dim", ctypes.c_int32),
         ("ratio", ctypes.c_int32), ("index_topk", ctypes.c_int32), ("offset", ctypes.c_int32),
         ("cand_topk_blocks", ctypes.c_int32), ("cand_block_size", ctypes.c_int32), ("norm_eps", ctypes.c_float),
-        ("key_format", ctypes.c_int32),
+        ("key_format", ctypes.c_int32), ("n_heads_total", ctypes.c_int32),
     ]
 
 
@@ -124,9 +124,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
 
 def make_dims(n_heads: int, ratio: int, index_topk: int, offset: int = 0, rope_dim: int = 64,
               head_dim: int = 128, cand_topk_blocks: int = 0, cand_block_size: int = 0,
-              norm_eps: float = 1e-6, key_format: int = KEY_MXFP4) -> IndexerDims:
+              norm_eps: float = 1e-6, key_format: int = KEY_MXFP4, n_heads_total: int = 0) -> IndexerDims:
+    """n_heads_total: 0, or the model's index head count when this call holds a shard of
+    n_heads of them (head-parallel scoring)."""
     return IndexerDims(n_heads, head_dim, rope_dim, ratio, index_topk, offset, cand_topk_blocks, cand_block_size,
-                       norm_eps, key_format)
+                       norm_eps, key_format, n_heads_total)
 
 
 def row_bytes(key_format: int = KEY_MXFP4) -> int:

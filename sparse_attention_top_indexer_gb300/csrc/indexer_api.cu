@@ -75,7 +75,17 @@ int check_dims(const IndexerDims* d) {
     return fail(INDEXER_ERR_DIMS, "norm_eps must be finite and >= 0");
   if (d->key_format != INDEXER_KEY_MXFP4 && d->key_format != INDEXER_KEY_FP8)
     return fail(INDEXER_ERR_DIMS, "key_format must be INDEXER_KEY_MXFP4 or INDEXER_KEY_FP8 (got %d)", d->key_format);
+  if (d->n_heads_total != 0 && (d->n_heads_total < h || d->n_heads_total > (1 << 16)))
+    return fail(INDEXER_ERR_DIMS, "n_heads_total must be 0 or in [n_heads, 65536] (got %d)", d->n_heads_total);
   return INDEXER_OK;
+}
+
+// softmax_scale * index_n_heads^-0.5 with softmax_scale = index_head_dim^-0.5 ("DeepSeek V4.1"
+// index-keys page, Indexer.__init__ and the weights line of Indexer.forward); a head shard
+// keeps the model's head count.
+float head_weight_scale(const IndexerDims* d) {
+  const int h = d->n_heads_total ? d->n_heads_total : d->n_heads;
+  return (float)(1.0 / std::sqrt((double)d->head_dim * (double)h));
 }
 
 // Bytes of one quantised row / one 64-key page in the dims' key format.
@@ -157,7 +167,7 @@ extern "C" {
 
 const char* indexer_last_error(void) { return g_last_error.c_str(); }
 
-int indexer_abi_version(void) { return 403; }
+int indexer_abi_version(void) { return 404; }
 
 // ---------------------------------------------------------------------------- RoPE table
 int indexer_rope_table(const IndexerYarn* y, int rope_dim, int max_pos, float* table, indexer_stream_t stream) {
@@ -284,7 +294,7 @@ static PrepArgs make_prep_args(const IndexerDims* dims, const indexer_bf16* q, c
   a.fp8 = is_fp8(dims) ? 1 : 0;
   a.rope_dim = dims->rope_dim;
   a.start_pos = start_pos;
-  a.w_scale = (float)(1.0 / std::sqrt((double)dims->head_dim) / std::sqrt((double)dims->n_heads));
+  a.w_scale = head_weight_scale(dims);
   return a;
 }
 
@@ -748,7 +758,7 @@ int indexer_forward_paged(const IndexerDims* dims, const indexer_bf16* q, const 
     a.h_shift = __builtin_ctz((unsigned)dims->n_heads);
     a.fp8 = is_fp8(dims) ? 1 : 0;
     a.rope_dim = dims->rope_dim;
-    a.w_scale = (float)(1.0 / std::sqrt((double)dims->head_dim) / std::sqrt((double)dims->n_heads));
+    a.w_scale = head_weight_scale(dims);
     const cudaError_t e = launch_prep_q(a, st);
     if (e != cudaSuccess) return cuda_fail(e, "prep_q launch");
   }

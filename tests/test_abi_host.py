@@ -37,12 +37,12 @@ def test_every_declared_symbol_is_exported(X):
 
 
 def test_struct_layouts_match_header(X):
-    assert ctypes.sizeof(X.IndexerDims) == 40
+    assert ctypes.sizeof(X.IndexerDims) == 44
     assert X.IndexerYarn.beta_slow.offset == 32
 
 
 def test_abi_version(X):
-    assert X.indexer_abi_version() == 403   # + row-major cache conversions, no-alloc status reader
+    assert X.indexer_abi_version() == 404   # + IndexerDims.n_heads_total (head-parallel scoring)
 
 
 def test_workspace_size_host_only(X):
