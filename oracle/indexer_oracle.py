@@ -19,6 +19,7 @@ __all__ = [
     "select_candidate_blocks", "candidate_mask", "topk_positions", "forward",
     "FP8_BLOCK", "E4M3_GRID", "FP8_SCALE_FLOOR", "FP8_ROW_BYTES", "fp8_quant_ue8m0", "pack_row132",
     "dequant_row132", "dequant_row", "quantise_rows",
+    "LATENT_BLOCK", "LATENT_SCALE_FLOOR", "e4m3_round", "fp4_quant_e4m3", "weights_proj", "compress_latent",
 ]
 
 # fp4_block_size (compress module page, constant FP4_BLOCK).
@@ -477,3 +478,94 @@ def forward(q_bits, w_bits, k_rows, cos, sin, start_pos: int, ratio: int, rope_d
         sc = flat.reshape(B, S, T)
     top = topk_positions(flat, vis_flat, index_topk, offset, T).reshape(B, S, index_topk)
     return top, cand_out, sc
+
+
+# ----------------------------------------------------------------------------- upstream producers
+# The inputs of the key publish and the query prep come from three producers on the pages:
+# the Compressor's latent (compress module page, compressor / Compressor.forward; attention.py
+# patch page, compressor_kv_score and fused_wkv_wgate), the head weights (index-keys page,
+# Indexer.__init__ weights_proj, Indexer.forward weights line), and the fp4 quantiser with
+# e4m3 scales that the compressed latent goes through (compress module page,
+# fp4_quant_e4m3_inplace, LATENT_BLOCK, precision policy).
+
+# Block size of the compressed latent's quantiser (compress module page, LATENT_BLOCK:
+# fp4_act_quant(latent, 16, ...)) and its amax floor (fp4_quant_e4m3_inplace: 6 * 2^-9).
+LATENT_BLOCK = 16
+LATENT_SCALE_FLOOR = 6.0 * 2.0 ** -9
+
+
+def e4m3_round(y: np.ndarray) -> np.ndarray:
+    """Non-negative f64 values rounded to the nearest e4m3 ("fn" variant, largest 448)
+    magnitude, ties to the even code, saturating at 448. Returns the 7-bit magnitude codes."""
+    y = np.minimum(np.asarray(y, dtype=np.float64), E4M3_GRID[-1])
+    hi = np.clip(np.searchsorted(E4M3_GRID, y, side="left"), 0, len(E4M3_GRID) - 1)
+    lo = np.maximum(hi - 1, 0)
+    d_hi, d_lo = E4M3_GRID[hi] - y, y - E4M3_GRID[lo]
+    take_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (lo % 2 == 0))
+    return np.where(take_lo, lo, hi).astype(np.uint8)
+
+
+def fp4_quant_e4m3(x_bits: np.ndarray, block: int = LATENT_BLOCK):
+    """fp4_quant_e4m3_inplace (compress module page): per block of 16 values, amax floored at
+    6 * 2^-9, scale = amax / 6 rounded through e4m3, values x / scale rounded onto the e2m1
+    grid (to nearest, ties to the even code, keeping the sign; beyond 6 the nearest grid
+    point is 6), dequantised back to bf16 (sign * grid * scale has at most 6 significant
+    bits, so it is exact in bf16 down to the subnormal range). Readings: amax / 6 and
+    x / scale are the exact quotients (f64 here; a quotient that sits on a tie is exactly
+    representable, so f64 decides ties like exact arithmetic).
+    Returns (codes uint8 [..., n] with sign in bit 3, scale magnitude codes uint8
+    [..., n / 16] (e4m3, positive), dequantised bf16 bits [..., n])."""
+    x_bits = np.asarray(x_bits, dtype=np.uint16)
+    shp = x_bits.shape
+    nb = shp[-1] // block
+    x = bf16_to_f64(x_bits).reshape(*shp[:-1], nb, block)
+    neg = ((x_bits >> 15) & 1).reshape(*shp[:-1], nb, block).astype(np.uint8)
+    amax = np.maximum(np.max(np.abs(x), axis=-1), LATENT_SCALE_FLOOR)
+    sc_code = e4m3_round(amax / 6.0)
+    sc = E4M3_GRID[sc_code]
+    y = np.abs(x) / sc[..., None]
+    dist = np.abs(y[..., None] - E2M1_GRID)
+    best = dist.min(axis=-1, keepdims=True)
+    is_best = dist == best
+    even = (np.arange(8) % 2 == 0)
+    choose_even = is_best & even
+    mag = np.where(choose_even.any(axis=-1), np.argmax(choose_even, axis=-1), np.argmax(is_best, axis=-1))
+    codes = (mag.astype(np.uint8) | (neg << 3)).reshape(shp)
+    deq = np.where(neg == 1, -1.0, 1.0) * E2M1_GRID[mag] * sc[..., None]
+    return codes, sc_code, f64_to_bf16(deq.reshape(shp))
+
+
+def weights_proj(x_bits: np.ndarray, wp_bits: np.ndarray) -> np.ndarray:
+    """w = weights_proj(x) (index-keys page, Indexer.__init__: weights_proj is a bf16 Linear
+    dim -> n_heads; Indexer.forward: weights = weights_proj(x) * ...). Reading: no bias, the
+    exact sum rounded once to bf16, as linear_bf16. x_bits [..., dim]; wp_bits [n_heads, dim]."""
+    return linear_bf16(x_bits, wp_bits)
+
+
+def compress_latent(x_bits: np.ndarray, wkv_bits: np.ndarray, wgate_bits: np.ndarray, norm_bits: np.ndarray,
+                    ratio: int, eps: float) -> np.ndarray:
+    """Compressor.forward (compress module page: softmax pooling of ratio tokens into one
+    latent, a plain projection at ratio 1; the compressor is f32 until its RMSNorm casts to
+    bf16; attention.py patch page: kv_score = hidden_states @ fused_wkv_wgate.weight^T with
+    an f32 result). Readings, where the pages give no body:
+      kv[t] = x[t] Wkv^T and score[t] = x[t] Wgate^T (the two halves of fused_wkv_wgate),
+        as exact sums (the GPU accumulates in f32);
+      group g holds tokens g*ratio .. g*ratio + ratio - 1 of the sequence; per latent dim d,
+        the weights are the softmax over those tokens of score[., d], and the pooled value is
+        sum_t softmax_t * kv[t, d] (at ratio 1 the softmax is 1: the plain projection);
+      RMSNorm of the pooled vector as rmsnorm_bf16 reads it (bf16((w * p) / sqrt(mean(p^2) +
+        eps))), on the unrounded pooled values.
+    x_bits [B, S, dim] bf16 with S a multiple of ratio; wkv_bits, wgate_bits [hd, dim];
+    norm_bits [hd]. Returns the latent bf16 bits [B, S / ratio, hd]."""
+    x = bf16_to_f64(x_bits)
+    kv = x @ bf16_to_f64(wkv_bits).T
+    sc = x @ bf16_to_f64(wgate_bits).T
+    B, S, hd = kv.shape
+    G = S // ratio
+    kv = kv[:, :G * ratio].reshape(B, G, ratio, hd)
+    sc = sc[:, :G * ratio].reshape(B, G, ratio, hd)
+    e = np.exp(sc - sc.max(axis=2, keepdims=True))
+    pooled = (e * kv).sum(axis=2) / e.sum(axis=2)
+    ms = np.sum(pooled * pooled, axis=-1, keepdims=True) / hd
+    r = 1.0 / np.sqrt(ms + float(np.float32(eps)))
+    return f64_to_bf16((bf16_to_f64(norm_bits) * pooled) * r)
