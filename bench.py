@@ -490,6 +490,51 @@ def run_ours(args, dist: Dist, name=None, steps=None, warmup=None, with_e2e=True
     return line, wl
 
 
+def measure_producers(wl: Workload, dev, reps: int = 3) -> dict:
+    """The upstream producers on the workload's tokens (indexer_compress_weights: the
+    Compressor's latent and its fp4/e4m3 copy, and weights_proj, from hidden states of size
+    wl.dim): CUDA-event time of a graph of back-to-back launches, against the larger of the
+    HBM time of its algorithmic bytes and the bf16 tensor time of its flops."""
+    import sparse_attention_top_indexer_gb300 as X
+    d = X.make_dims(n_heads=wl.H, ratio=wl.ratio, index_topk=wl.topk, norm_eps=wl.norm_eps)
+    x = wl.x(dev)
+    wkv, wg, nw, wp = wl.wkv(dev), wl.wgate(dev), wl.c_norm_w(dev), wl.wproj(dev)
+    G = wl.S // wl.ratio
+    lat = torch.empty((wl.B, G, wl.D), dtype=torch.bfloat16, device=dev)
+    latq = torch.empty_like(lat)
+    w = torch.empty((wl.B, wl.S, wl.H), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(X.STATUS_BYTES, dtype=torch.uint8, device=dev)
+    X.indexer_workspace_init(ws)
+    fn = lambda i: X.indexer_compress_weights(d, x, wkv, wg, nw, wp, lat, w, ws, latent_q=latq)
+    fn(0)
+    torch.cuda.synchronize()
+    g = capture(fn, reps)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    X.indexer_status(ws)
+    ms = e0.elapsed_time(e1) / (reps * reps)
+    R = wl.B * wl.S
+    n_out = 2 * wl.D + wl.H
+    flops = 2.0 * R * wl.dim * n_out
+    byts = R * wl.dim * 2 + n_out * wl.dim * 2 + 2 * R // wl.ratio * wl.D * 2 + R * wl.H * 2
+    peaks = measured_peaks()
+    t_hbm = byts / (peaks["hbm_gbs"] * 1e9) * 1e3
+    t_mma = flops / (peaks["bf16_tflops"] * 1e12) * 1e3
+    del x, g
+    torch.cuda.empty_cache()
+    return {"kernel": "compress_kernel (indexer_compress_weights)", "ms": ms, "rows": R, "dim": wl.dim,
+            "outputs_per_row": n_out, "flops": flops, "bytes": byts, "TFLOP/s": flops / (ms / 1e3) / 1e12,
+            "GB/s": byts / (ms / 1e3) / 1e9, "bound": "hbm" if t_hbm >= t_mma else "tensor",
+            "frac": max(t_hbm, t_mma) / ms,
+            "peak_source": f"{peaks['source']} hbm_gbs and bf16_tflops (the larger of the two times)"}
+
+
 def per_config_records(args, dist: Dist) -> dict:
     """The other configurations, measured in the same run: value, step time, kernel times,
     the dominant kernel's roofline and the whole step's, and e2e through the host-buffer call."""
@@ -918,6 +963,7 @@ def main():
             line, wl = run_ours(args, dist)
             if args.workload == HEADLINE and not args.no_per_config:
                 line["per_config"] = per_config_records(args, dist)
+                line["upstream_producers"] = measure_producers(wl, torch.device("cuda", dist.local))
             if dist.rank == 0 and dist.world == 1 and not args.no_cpu_baseline:
                 line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
         if dist.rank == 0 and line is not None:

@@ -204,6 +204,34 @@ int indexer_prep_q_proj(const IndexerDims* dims, const indexer_bf16* qr, int Kq,
                         indexer_stream_t stream);
 
 /* ---------------------------------------------------------------------------
+ * indexer_compress_weights -- the producers upstream of the key publish and the query prep,
+ * from one pass over the hidden states x (B sequences of S tokens, S a multiple of ratio):
+ *   latent   = Compressor(x): kv = x Wkv^T and score = x Wgate^T per token (f32 tensor-core
+ *              sums of bf16 products; [attention.py] compressor_kv_score, fused_wkv_wgate),
+ *              per latent dim the softmax over each group's ratio tokens of score weighting kv
+ *              ([compress] compressor: softmax pooling of ratio tokens, a plain projection at
+ *              ratio 1), then RMSNorm(norm_w, dims->norm_eps) rounded to bf16 (the
+ *              compressor is f32 until its RMSNorm casts to bf16); the pre-RoPE latent that
+ *              indexer_publish_k takes;
+ *   latent_q = the latent through [compress] fp4_quant_e4m3_inplace (LATENT_BLOCK 16, amax
+ *              floored at 6 * 2^-9, scale amax / 6 rounded through e4m3, e2m1 values),
+ *              dequantised back to bf16 (the compressed KV the attention layer keeps);
+ *   w_out    = weights_proj(x) ([index-keys] Indexer.__init__, a bf16 Linear dim -> n_heads),
+ *              the f32 accumulation rounded once to bf16; indexer_prep_q's w.
+ *   x:        bf16 [B][S][dim], dim a multiple of 64 in [64, 65536], 16-byte aligned
+ *   wkv, wgate: bf16 [128][dim] (the two halves of fused_wkv_wgate); norm_w: bf16 [128]
+ *   wproj:    bf16 [n_heads][dim]
+ *   latent, latent_q: bf16 [B][S / ratio][128] (latent_q may be NULL)
+ *   w_out:    bf16 [B][S][n_heads]
+ *   ws/ws_bytes: status word (INDEXER_STATUS_BYTES), initialised by indexer_workspace_init
+ * ratio must be 1, 2, 4, 8, 16 or 32 (a group's tokens share one warp).
+ * ------------------------------------------------------------------------- */
+int indexer_compress_weights(const IndexerDims* dims, const indexer_bf16* x, int B, int S, int dim,
+                             const indexer_bf16* wkv, const indexer_bf16* wgate, const indexer_bf16* norm_w,
+                             const indexer_bf16* wproj, indexer_bf16* latent, indexer_bf16* latent_q,
+                             indexer_bf16* w_out, void* ws, size_t ws_bytes, indexer_stream_t stream);
+
+/* ---------------------------------------------------------------------------
  * indexer_scores -- index scores of prepared queries against the key cache
  * ([index-keys] Indexer.forward: einsum("bshd,btd->bsht"), relu, * weights,
  * sum over heads; causal mask t >= vis(s) -> -inf; level two: -inf outside the

@@ -24,7 +24,7 @@ __all__ = [
     "indexer_workspace_init", "indexer_status", "indexer_abi_version", "indexer_forward_publish_host",
     "indexer_workspace_size_host", "make_dims", "indexer_forward_noalloc",
     "NOALLOC_SCRATCH_BYTES", "indexer_noalloc_status", "indexer_cache_from_rows", "indexer_cache_to_rows",
-    "indexer_scores_hold_test",
+    "indexer_scores_hold_test", "indexer_compress_weights",
 ]
 
 KEY_ROW_BYTES = 68
@@ -89,6 +89,8 @@ _SIGS = {
                               _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
     "indexer_status": [_P, _P],
     "indexer_noalloc_status": [_P],
+    "indexer_compress_weights": [ctypes.POINTER(IndexerDims), _P, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P,
+                                 ctypes.c_size_t, _P],
     "indexer_scores_hold_test": [ctypes.POINTER(IndexerDims), _P, _P, _I, _I, _I, _P, _I, _P, _P, ctypes.c_size_t,
                                  ctypes.c_uint64, _P],
     "indexer_cache_from_rows": [ctypes.POINTER(IndexerDims), _P, _I, _I, _I, _P, _I, _P],
@@ -249,6 +251,21 @@ def indexer_prep_q_proj(dims: IndexerDims, qr: torch.Tensor, wq_b: torch.Tensor,
         _ptr(q_rows, torch.uint8, "q_rows"), _ptr(w_prime, torch.float32, "w_prime"),
         _ptr(q_out, torch.bfloat16, "q_out"), _ptr(ws, None, "ws"), ws.numel() * ws.element_size(),
         _stream(stream)))
+
+
+def indexer_compress_weights(dims: IndexerDims, x: torch.Tensor, wkv: torch.Tensor, wgate: torch.Tensor,
+                             norm_w: torch.Tensor, wproj: torch.Tensor, latent: torch.Tensor, w_out: torch.Tensor,
+                             ws: torch.Tensor, latent_q: Optional[torch.Tensor] = None, stream=None):
+    """x bf16 [B, S, dim]; wkv, wgate bf16 [128, dim]; norm_w bf16 [128]; wproj bf16 [H, dim];
+    latent (and latent_q) bf16 [B, S / ratio, 128]; w_out bf16 [B, S, H]; ws the status workspace.
+    The Compressor's latent, its fp4/e4m3 quantised copy and weights_proj(x); see include/indexer.h."""
+    B, S, dim = x.shape
+    _check(load_library().indexer_compress_weights(
+        ctypes.byref(dims), _ptr(x, torch.bfloat16, "x"), B, S, dim, _ptr(wkv, torch.bfloat16, "wkv"),
+        _ptr(wgate, torch.bfloat16, "wgate"), _ptr(norm_w, torch.bfloat16, "norm_w"),
+        _ptr(wproj, torch.bfloat16, "wproj"), _ptr(latent, torch.bfloat16, "latent"),
+        _ptr(latent_q, torch.bfloat16, "latent_q"), _ptr(w_out, torch.bfloat16, "w_out"), _ptr(ws, None, "ws"),
+        ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def indexer_scores(dims: IndexerDims, q_rows: torch.Tensor, w_prime: torch.Tensor, start_pos: int,

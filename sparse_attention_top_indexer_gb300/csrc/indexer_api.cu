@@ -167,7 +167,7 @@ extern "C" {
 
 const char* indexer_last_error(void) { return g_last_error.c_str(); }
 
-int indexer_abi_version(void) { return 404; }
+int indexer_abi_version(void) { return 405; }
 
 // ---------------------------------------------------------------------------- RoPE table
 int indexer_rope_table(const IndexerYarn* y, int rope_dim, int max_pos, float* table, indexer_stream_t stream) {
@@ -366,6 +366,46 @@ int indexer_prep_q_proj(const IndexerDims* dims, const indexer_bf16* qr, int Kq,
   a.w_scale = make_prep_args(dims, qr, w, B, S, start_pos, rope_cs, q_rows, w_prime, nullptr).w_scale;
   const cudaError_t e = launch_qproj(a, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "query projection launch");
+  return ok();
+}
+
+// ---------------------------------------------------------------------------- upstream producers
+int indexer_compress_weights(const IndexerDims* dims, const indexer_bf16* x, int B, int S, int dim,
+                             const indexer_bf16* wkv, const indexer_bf16* wgate, const indexer_bf16* norm_w,
+                             const indexer_bf16* wproj, indexer_bf16* latent, indexer_bf16* latent_q,
+                             indexer_bf16* w_out, void* ws, size_t ws_bytes, indexer_stream_t stream) {
+  RETURN_IF(check_dims(dims));
+  if (!x || !wkv || !wgate || !norm_w || !wproj || !latent || !w_out || !ws)
+    return fail(INDEXER_ERR_NULL, "a required pointer is NULL");
+  if (B < 1 || S < 1) return fail(INDEXER_ERR_DIMS, "B and S must be >= 1 (got %d, %d)", B, S);
+  const int r = dims->ratio;
+  if (r != 1 && r != 2 && r != 4 && r != 8 && r != 16 && r != 32)
+    return fail(INDEXER_ERR_DIMS, "the fused compressor takes ratio 1, 2, 4, 8, 16 or 32 (got %d)", r);
+  if (S % r) return fail(INDEXER_ERR_DIMS, "S = %d is not a whole number of groups of %d tokens", S, r);
+  if (dim < 64 || dim > 65536 || (dim % 64)) return fail(INDEXER_ERR_DIMS, "dim must be a multiple of 64 in [64, 65536]");
+  if ((long long)B * S > (1ll << 30)) return fail(INDEXER_ERR_DIMS, "B * S is too large");
+  if (!aligned(x, 16) || !aligned(wkv, 16) || !aligned(wgate, 16) || !aligned(wproj, 16) || !aligned(latent, 16) ||
+      (latent_q && !aligned(latent_q, 16)) || !aligned(w_out, 4) || !aligned(ws, 16))
+    return fail(INDEXER_ERR_ALIGN, "x, the weights, latent, latent_q and ws must be 16-byte aligned, w_out 4-byte");
+  if (ws_bytes < INDEXER_STATUS_BYTES) return fail(INDEXER_ERR_WORKSPACE, "ws needs %d bytes", INDEXER_STATUS_BYTES);
+  RETURN_IF(check_arch());
+  CompressArgs a{};
+  a.x = x;
+  a.wkv = wkv;
+  a.wgate = wgate;
+  a.norm_w = norm_w;
+  a.wproj = wproj;
+  a.latent = latent;
+  a.latent_q = latent_q;
+  a.w_out = w_out;
+  a.status = static_cast<uint32_t*>(ws);
+  a.R = B * S;
+  a.dim = dim;
+  a.H = dims->n_heads;
+  a.ratio = r;
+  a.eps = dims->norm_eps;
+  const cudaError_t e = launch_compress(a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "compress launch");
   return ok();
 }
 

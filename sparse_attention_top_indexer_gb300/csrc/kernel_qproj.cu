@@ -18,11 +18,11 @@
 //     with the same f32 rotation as the query-prep kernels, the block's e8m0 scale and
 //     e2m1 codes; then w' = w * head_dim^-0.5 * H^-0.5 for the row's two heads.
 // Every wait on an mbarrier is bounded; a role that gives up reports through the status word.
-#include <cuda.h>   // CUtensorMap and its enums (the encoder comes through the runtime)
 #include <cuda_runtime.h>
 
 #include "device_common.cuh"
 #include "launch.h"
+#include "tma_common.cuh"
 
 namespace indexer {
 
@@ -45,22 +45,6 @@ struct QprojParams {
   CUtensorMap map_b;   // wq_b: [H * 128][Kq] bf16, boxes of 64 x 256, 128-byte swizzle
   QprojArgs a;
 };
-
-// 2-D tensor-map copy of the box at (x, y) into shared memory, completing bytes on `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
-}
-
-// Shared-memory matrix descriptor, K-major with the 128-byte swizzle: rows of 128 bytes, 8-row
-// groups 1024 bytes apart (the layout a 128-byte-swizzled tensor-map copy writes at a
-// 1024-byte aligned address); bits 46-48 hold 0b001, layout type 2 in bits 61-63. The K
-// steps of 16 elements inside a row advance the start address by 32 bytes.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
-         (2ull << 61);
-}
 
 __global__ void __launch_bounds__(kQpThreads, 1) qproj_prep_kernel(const __grid_constant__ QprojParams prm) {
   const QprojArgs& a = prm.a;
@@ -247,31 +231,6 @@ __global__ void __launch_bounds__(kQpThreads, 1) qproj_prep_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem, 512);
-}
-
-// cuTensorMapEncodeTiled, looked up once through the runtime (no link against the driver).
-typedef CUresult (*TensorMapEncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                         const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                         CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-TensorMapEncodeTiled lookup_encode() {
-  void* fn = nullptr;
-  cudaDriverEntryPointQueryResult q;
-  const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-  return e == cudaSuccess && q == cudaDriverEntryPointSuccess ? reinterpret_cast<TensorMapEncodeTiled>(fn) : nullptr;
-}
-
-cudaError_t encode_bf16_rows(CUtensorMap* map, const void* base, long long rows, int cols, int box_rows) {
-  static const TensorMapEncodeTiled encode = lookup_encode();   // looked up once, thread-safely
-  if (encode == nullptr) return cudaErrorNotSupported;
-  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  const cuuint32_t box[2] = {(cuuint32_t)kQpK, (cuuint32_t)box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace

@@ -52,6 +52,13 @@ struct FmtFp8 {
   static constexpr int kStage = 17408;   // two pages (16896 B) padded to a 1 KB multiple
 };
 constexpr int kEpiThreads = 128;                     // one epilogue warpgroup
+constexpr int kEpiWarps = 4;
+// The lanes of a converged warp are done (their earlier shared-memory and tensor-memory
+// accesses ordered by the warp synchronisation); one lane arrives for the warp.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
 constexpr int kMaxPages = 32768 / kPageKeys;         // pages of the longest row a sparse launch takes
 constexpr int kMaxTilesCta = 256;                    // tiles one CTA takes at most
 
@@ -554,12 +561,13 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
 //     the accumulator in 64-column halves, release it, form sum_h w' * max(dot, 0) per row
 //     and store; after its last tile of a group every epilogue thread releases the query
 //     buffer of that group.
-template <int H, int QG, int EPI, class F>
+template <int H, int QG, int EPI, int NMMA, class F>
 struct RowsCfg {
-  static constexpr int THREADS = 128 * (1 + EPI) + 64;
-  static constexpr int MMA_WARP = 4 * (1 + EPI);
-  static constexpr int PRODUCER_WARP = MMA_WARP + 1;
-  static constexpr int QFREE_COUNT = 128 * (1 + EPI) + 32;   // scale warpgroup, epilogue, MMA warp
+  static constexpr int THREADS = 128 * (1 + EPI) + 32 * NMMA + 32;
+  static constexpr int MMA_WARP = 4 * (1 + EPI);              // the first of NMMA MMA warps
+  static constexpr int PRODUCER_WARP = MMA_WARP + NMMA;
+  static constexpr int QFREE_COUNT = 4 * (1 + EPI) + NMMA;    // warps: scale warpgroup, epilogue, MMA
+  static constexpr int CHUNK = EPI >= 3 ? 32 : 64;            // accumulator columns an epilogue load takes
   static constexpr int N = QG * H;
   static constexpr int NP = round_up(N, 16);
   static constexpr int NCB = (NP + 31) / 32;
@@ -586,9 +594,10 @@ struct RowsCfg {
   // full, free, done, empty, qfull, qfree, ready; FP8: scales read (per stage), scaled w' ready
   static constexpr int NBAR = 2 * NSTAGE + 3 * NACC + 4 + (F::kFp8 ? NSTAGE + 2 : 0);
   static constexpr int OFF_BAR = OFF_GD + 2 * 32;
-  static constexpr int OFF_INFO = OFF_BAR + NBAR * 8;                     // tmem, tiles, mmas, q phases
-  static constexpr int SMEM = OFF_INFO + 16;
+  static constexpr int OFF_INFO = OFF_BAR + NBAR * 8;   // tmem, tiles issued, q phases, each MMA warp's tiles
+  static constexpr int SMEM = OFF_INFO + 4 * (3 + NMMA);
   static_assert(N <= 256 && NCB * 32 % 64 == 0, "epilogue reads 64-column halves");
+  static_assert(NMMA >= 1 && 3 + NMMA <= 8, "MMA warps");
   static_assert(TMEM_NEED <= (int)TMEM_COLS && TMEM_COLS <= 512u, "tensor memory budget");
   static_assert(SFA_COL % 4 == 0 && SFB_COL % 4 == 0 && SB % 4 == 0, "scale sets must be 4-column aligned");
   static_assert(NBAR <= 64, "barriers are initialised by the lanes of two passes of one warp");
@@ -602,15 +611,16 @@ struct GroupDesc {   // one query group, as the producer hands it to the other r
   int Tb, nt, ntiles, live;   // keys of the sequence, tiles to score, tiles of the sequence, 0 = no more groups
 };
 
-template <int H, int QG, int EPI, class F>
-__global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows_kernel(const ScoreArgs a) {
-  using C = RowsCfg<H, QG, EPI, F>;
+template <int H, int QG, int EPI, int NMMA, class F>
+__global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) score_rows_kernel(const ScoreArgs a) {
+  using C = RowsCfg<H, QG, EPI, NMMA, F>;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   pdl_allow_next();
   GroupDesc* gdesc = reinterpret_cast<GroupDesc*>(smem + C::OFF_GD);
-  uint32_t* info = reinterpret_cast<uint32_t*>(smem + C::OFF_INFO);   // [0] tmem, [1] tiles issued, [2] mmas, [3] q phases
+  // [0] tmem, [1] tiles issued, [2] q phases, [3 + m] tiles MMA warp m has issued (last + 1)
+  uint32_t* info = reinterpret_cast<uint32_t*>(smem + C::OFF_INFO);
   const uint8_t* stg = smem + C::OFF_STG;
   const uint32_t stg0 = smem_u32(stg);
   uint32_t* sfw = reinterpret_cast<uint32_t*>(smem + C::OFF_SFW);
@@ -636,12 +646,12 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
       // read); an accumulator's scales are ready once the four scale warps have stored them;
       // FP8: a stage's key scales have been read by the epilogue warpgroup of its tile, and
       // a query buffer's scaled head weights have been written by all epilogue threads
-      mbar_init(bar0 + 8u * (uint32_t)i, empty_bar || ready_bar || sread_bar ? (uint32_t)kEpiThreads
+      mbar_init(bar0 + 8u * (uint32_t)i, empty_bar || ready_bar || sread_bar ? (uint32_t)kEpiWarps
                                          : qfree_bar ? (uint32_t)C::QFREE_COUNT
-                                         : ws_bar ? (uint32_t)(EPI * kEpiThreads) : 1u);
+                                         : ws_bar ? (uint32_t)(EPI * kEpiWarps) : 1u);
     }
     fence_mbar_init();
-    if (lane == 0) info[1] = info[2] = info[3] = 0u;
+    if (lane < 3 + NMMA) info[lane] = 0u;
   } else if (warp == 1) {
     tmem_alloc(smem_u32(&info[0]), C::TMEM_COLS);
     tmem_relinquish();
@@ -713,7 +723,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
         } else {
           mbar_arrive(bar_qfull(qb));   // no more groups: the other roles stop here
         }
-        info[3] = (uint32_t)(k + 1);
+        info[2] = (uint32_t)(k + 1);
       }
       __syncwarp();
       if (!d.live) break;
@@ -762,7 +772,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
       const GroupDesc d = gdesc[qb];
       if (!d.live) break;
       if (d.nt == 0) {
-        mbar_arrive(bar_qfree(qb));
+        warp_arrive(bar_qfree(qb));
         continue;
       }
       // query rows -> B operand buffer qb (core-matrix order) and B scale set qb
@@ -773,7 +783,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
       named_bar_sync(1, 128);
       // done with the buffer's descriptor and raw rows (the B operand itself stays in use
       // until the group's MMAs complete, which the epilogue's release covers)
-      mbar_arrive(bar_qfree(qb));
+      warp_arrive(bar_qfree(qb));
       const uint32_t sfb = (uint32_t)(C::SFB_COL + qb * 2 * C::SB);
       if constexpr (!F::kFp8) {
 #pragma unroll
@@ -802,11 +812,12 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
         }
         tmem_wait_st();   // (also the group's B scales, for its first tile)
         tc_fence_before();
-        mbar_arrive(bar_ready(c));
+        warp_arrive(bar_ready(c));
       }
     }
-  } else if (warp == C::MMA_WARP) {
-    // ------------------------------------------------------------ MMA warp
+  } else if (warp >= C::MMA_WARP && warp < C::PRODUCER_WARP) {
+    // ------------------------------------------------------------ MMA warps (tile j is warp j % NMMA's)
+    const int mid = warp - C::MMA_WARP;
     uint32_t j = 0;
     for (int k = 0; !failed; ++k) {
       const int qb = k & 1;
@@ -816,10 +827,11 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
       }
       const GroupDesc d = gdesc[qb];
       if (!d.live) break;
-      mbar_arrive(bar_qfree(qb));   // the descriptor is in registers
+      warp_arrive(bar_qfree(qb));   // the descriptor is in registers
       const uint32_t qbaddr = smem_u32(smem + C::OFF_QB + qb * C::QB_STRIDE);
       const uint32_t sfb = (uint32_t)(C::SFB_COL + qb * 2 * C::SB);
       for (int i = 0; i < d.nt; ++i, ++j) {
+        if ((int)(j % NMMA) != mid) continue;
         const int st = (int)(j % C::NSTAGE), c = (int)(j % C::NACC);
         // the scale warps arrive on "ready" only after they have seen the tile's copy land
         // (its full barrier), so the tile is in place once "ready" is seen
@@ -835,12 +847,12 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
           const uint32_t sfa = tmem + (uint32_t)(C::SFA_COL + 8 * c);
           issue_tile_mma<F, C::NP>(acc, pa, qbaddr, sfa, tmem + sfb, C::SB);
           tc_commit(bar_free(st));   // the stage may be refilled and the accumulator read
-          info[2] = j + 1;
+          info[3 + mid] = j + 1;
         }
         __syncwarp();
       }
     }
-  } else if (warp < C::PRODUCER_WARP) {
+  } else if (warp >= 4 && warp < C::MMA_WARP) {
     // ------------------------------------------------------------ epilogue warpgroups
     constexpr int P = H >= 32 ? 4 : 2;   // independent partial sums per row (pairs of heads)
     const int grp = (warp - 4) >> 2;
@@ -865,7 +877,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
         const uint8_t* qstg = smem + C::OFF_QSTG + qb * C::QSTG_STRIDE;
         for (int n = ge; n < C::N; n += EPI * kEpiThreads)
           ws[n] = n < d.nq * H ? wq[n] * *reinterpret_cast<const float*>(qstg + n * F::kRow + F::kCode) : 0.f;
-        mbar_arrive(bar_wsready(qb));
+        warp_arrive(bar_wsready(qb));
         if (!warp_wait(bar_wsready(qb), (uint32_t)(k >> 1) & 1u, wait_ns)) {
           failed = true;
           break;
@@ -896,7 +908,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
         float sk = 1.f;   // FP8: this key's scale; the stage may be refilled once all are read
         if constexpr (F::kFp8) {
           sk = *reinterpret_cast<const float*>(stg + st * F::kStage + page_scale_offset_fp8(et));
-          mbar_arrive(bar_sread(st));
+          warp_arrive(bar_sread(st));
         }
         tc_fence_after();
         float part[QG][P];
@@ -904,17 +916,21 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
         for (int qi = 0; qi < QG; ++qi)
 #pragma unroll
           for (int p = 0; p < P; ++p) part[qi][p] = 0.f;
+        constexpr int CH = C::CHUNK;
 #pragma unroll
-        for (int h = 0; h < C::NCB * 32 / 64; ++h) {   // 64-column halves of the accumulator
-          float v[64];
-          tmem_ld64(tq + (uint32_t)(c * C::NP + 64 * h), v);
-          if (h == C::NCB * 32 / 64 - 1) {
+        for (int h = 0; h < C::NCB * 32 / CH; ++h) {   // CH-column pieces of the accumulator
+          float v[CH];
+          if constexpr (CH == 64)
+            tmem_ld64(tq + (uint32_t)(c * C::NP + CH * h), v);
+          else
+            tmem_ld32(tq + (uint32_t)(c * C::NP + CH * h), v);
+          if (h == C::NCB * 32 / CH - 1) {
             tc_fence_before();
-            mbar_arrive(bar_empty(c));   // accumulator c and its scale set may be reused
+            warp_arrive(bar_empty(c));   // accumulator c and its scale set may be reused
           }
 #pragma unroll
-          for (int u = 0; u < 64; u += 4) {
-            const int n = 64 * h + u;
+          for (int u = 0; u < CH; u += 4) {
+            const int n = CH * h + u;
             if (n < C::N) {
               const float4 w4 = *reinterpret_cast<const float4*>(wq + n);
               const int qi = n / H, p0 = (n % P), p1 = ((n + 2) % P);
@@ -940,17 +956,17 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
         __syncwarp();
       }
       if (failed) break;
-      mbar_arrive(bar_qfree(qb));   // this thread is done with the group's query buffer
+      warp_arrive(bar_qfree(qb));   // this warp is done with the group's query buffer
     }
   }
   __syncwarp();
   if (failed && lane == 0)
-    atomicOr(a.status, warp < 4 || warp >= C::MMA_WARP ? kStatusLoadTimeout : kStatusMmaTimeout);
+    atomicOr(a.status, warp >= 4 && warp < C::MMA_WARP ? kStatusMmaTimeout : kStatusLoadTimeout);
   // on failure, bounded waits for whatever may still be in flight before shared and tensor
   // memory go
   const bool any_failed = __syncthreads_or(failed);
   if (any_failed && tid == 0) {
-    const int issued = (int)info[1], mmas = (int)info[2], qph = (int)info[3];
+    const int issued = (int)info[1], qph = (int)info[2];
     for (int st = 0; st < C::NSTAGE && st < issued; ++st) {
       const int last = st + ((issued - 1 - st) / C::NSTAGE) * C::NSTAGE;
       mbar_wait(bar_full(st), (uint32_t)(last / C::NSTAGE) & 1u, wait_ns);
@@ -959,7 +975,10 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, F>::THREADS, 1) score_rows
       const int last = q + ((qph - 1 - q) / 2) * 2;
       mbar_wait(bar_qfull(q), (uint32_t)(last >> 1) & 1u, wait_ns);
     }
-    if (mmas > 0) mbar_wait(bar_free((mmas - 1) % C::NSTAGE), (uint32_t)((mmas - 1) / C::NSTAGE) & 1u, wait_ns);
+    for (int m = 0; m < NMMA; ++m) {   // each MMA warp's last tile (its commit tracks all its MMAs)
+      const int mmas = (int)info[3 + m];
+      if (mmas > 0) mbar_wait(bar_free((mmas - 1) % C::NSTAGE), (uint32_t)((mmas - 1) / C::NSTAGE) & 1u, wait_ns);
+    }
   }
   __syncthreads();
   if (tid == 0) {   // the last CTA to finish rewinds the group counter for the next launch
@@ -1039,19 +1058,19 @@ cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
   return launch_overlapped(score_kernel<H, QG, EPI, F>, grid, dim3(C::THREADS), smem, stream, a);
 }
 
-template <int H, int QG, int EPI, class F>
+template <int H, int QG, int EPI, int NMMA, class F>
 cudaError_t launch_rows(ScoreArgs a, cudaStream_t stream) {
-  using C = RowsCfg<H, QG, EPI, F>;
+  using C = RowsCfg<H, QG, EPI, NMMA, F>;
   const size_t smem = (size_t)C::SMEM + 1024;   // + base alignment slack
   static int set_bytes[64] = {0};
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64 || set_bytes[dev] < (int)smem) {
-    err = cudaFuncSetAttribute(score_rows_kernel<H, QG, EPI, F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    err = cudaFuncSetAttribute(score_rows_kernel<H, QG, EPI, NMMA, F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                (int)smem);
     if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(score_rows_kernel<H, QG, EPI, F>, cudaFuncAttributePreferredSharedMemoryCarveout,
+      err = cudaFuncSetAttribute(score_rows_kernel<H, QG, EPI, NMMA, F>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  (int)cudaSharedmemCarveoutMaxShared);
     if (err != cudaSuccess) return err;
     if (dev >= 0 && dev < 64) set_bytes[dev] = (int)smem;
@@ -1059,9 +1078,16 @@ cudaError_t launch_rows(ScoreArgs a, cudaStream_t stream) {
   const long long groups = a.groups ? (long long)a.n_groups : (long long)((a.S + QG - 1) / QG) * a.B;
   if (groups <= 0) return cudaSuccess;
   const long long ctas = groups < sm_count() ? groups : sm_count();   // one persistent CTA per SM
-  return launch_overlapped(score_rows_kernel<H, QG, EPI, F>, dim3((unsigned)ctas), dim3(C::THREADS), smem, stream,
+  return launch_overlapped(score_rows_kernel<H, QG, EPI, NMMA, F>, dim3((unsigned)ctas), dim3(C::THREADS), smem, stream,
                            a);
 }
+
+#ifndef ROWS_EPI
+#define ROWS_EPI 2
+#endif
+#ifndef ROWS_NMMA
+#define ROWS_NMMA 2
+#endif
 
 template <class F>
 cudaError_t launch_scores_fmt(const ScoreArgs& a, cudaStream_t stream) {
@@ -1069,13 +1095,14 @@ cudaError_t launch_scores_fmt(const ScoreArgs& a, cudaStream_t stream) {
   // with score_group_rows(H, true))
   const bool single = a.S == 1;
   if (!single && a.cand == nullptr && a.sched != nullptr) {
-    // several rows per group: the persistent kernel (N = 128, two epilogue warpgroups)
+    // several rows per group: the persistent kernel (N = 128, ROWS_EPI epilogue warpgroups,
+    // ROWS_NMMA MMA warps taking alternate tiles)
     switch (a.H) {
-      case 8: return launch_rows<8, 16, 2, F>(a, stream);
-      case 16: return launch_rows<16, 8, 2, F>(a, stream);
-      case 32: return launch_rows<32, 4, 2, F>(a, stream);
-      case 64: return launch_rows<64, 2, 2, F>(a, stream);
-      case 128: return launch_rows<128, 1, 2, F>(a, stream);
+      case 8: return launch_rows<8, 16, ROWS_EPI, ROWS_NMMA, F>(a, stream);
+      case 16: return launch_rows<16, 8, ROWS_EPI, ROWS_NMMA, F>(a, stream);
+      case 32: return launch_rows<32, 4, ROWS_EPI, ROWS_NMMA, F>(a, stream);
+      case 64: return launch_rows<64, 2, ROWS_EPI, ROWS_NMMA, F>(a, stream);
+      case 128: return launch_rows<128, 1, ROWS_EPI, ROWS_NMMA, F>(a, stream);
       default: return cudaErrorInvalidValue;
     }
   }

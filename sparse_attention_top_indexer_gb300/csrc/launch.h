@@ -77,6 +77,25 @@ struct QprojArgs {
 };
 cudaError_t launch_qproj(const QprojArgs& a, cudaStream_t stream);
 
+// The producers upstream of the key publish and the query prep, from one pass over the
+// hidden states x: the Compressor's latent (kv and gate projections, softmax pooling of
+// `ratio` tokens per dim, RMSNorm to bf16), the latent through the fp4 quantiser with e4m3
+// block-16 scales (dequantised to bf16), and the head weights w = weights_proj(x) (bf16).
+struct CompressArgs {
+  const uint16_t* x;        // [R][dim] bf16, R = B * S rows, S a multiple of ratio
+  const uint16_t* wkv;      // [128][dim] bf16
+  const uint16_t* wgate;    // [128][dim] bf16
+  const uint16_t* norm_w;   // [128] bf16
+  const uint16_t* wproj;    // [H][dim] bf16
+  uint16_t* latent;         // [R / ratio][128] bf16
+  uint16_t* latent_q = nullptr;   // [R / ratio][128] bf16 or nullptr
+  uint16_t* w_out;          // [R][H] bf16
+  uint32_t* status = nullptr;
+  int R, dim, H, ratio;
+  float eps;
+};
+cudaError_t launch_compress(const CompressArgs& a, cudaStream_t stream);
+
 // Per-row metadata of a batch of sequences with their own start positions and query-row
 // counts, built on the device by the plan kernel.
 struct alignas(16) RowInfo {

@@ -42,7 +42,7 @@ def test_struct_layouts_match_header(X):
 
 
 def test_abi_version(X):
-    assert X.indexer_abi_version() == 404   # + IndexerDims.n_heads_total (head-parallel scoring)
+    assert X.indexer_abi_version() == 405   # + indexer_compress_weights (upstream producers)
 
 
 def test_workspace_size_host_only(X):

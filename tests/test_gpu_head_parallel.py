@@ -72,7 +72,9 @@ def test_shards_sum_to_the_full_scores(X, name, over, world):
     a, b = total.cpu().numpy(), full.cpu().numpy()
     assert np.array_equal(np.isneginf(a), np.isneginf(b))
     fin = np.isfinite(b)
-    assert np.all(np.abs(a[fin] - b[fin]) <= 1e-5 * (np.abs(b[fin]) + 1e-2))
+    # f32 sums in another order: the shards' partials are O(1) and may cancel, so the bound is
+    # on the size of the terms, not of the total
+    assert np.all(np.abs(a[fin] - b[fin]) <= 4e-6 + 1e-5 * np.abs(b[fin]))
     # the oracle
     ref_top, _, ref_sc = O.forward(C.bits(q), C.bits(w), ref_cache, cos, sin, wl.start_pos, wl.ratio, wl.rope_dim,
                                    wl.topk, wl.offset, cand_in=None if cand is None else ref_cand,

@@ -160,6 +160,7 @@ class Workload:
     key_format: int = 0       # 0: MXFP4 rows (68 bytes), 1: FP8 rows (132 bytes)
     q_lora_rank: int = 1280   # K of the query projection wq_b (qr -> H * 128)
     fused_q: bool = False     # queries enter as qr: the projection wq_b runs inside the step
+    dim: int = 4096           # hidden size of x for the upstream producers (not given on the pages)
 
     @property
     def end_pos(self) -> int:
@@ -230,6 +231,28 @@ class Workload:
     def k_norm_w(self, device="cpu") -> torch.Tensor:
         return normal_bf16(self.seed, f"{self.name}/k_norm_w", (self.D,), std=math.sqrt(0.1), mean=1.0,
                            device=device)
+
+    # ------------------------------------------------------------ upstream producers
+    def x(self, device="cpu") -> torch.Tensor:
+        """Hidden states [B, S, dim] (unit normal) for the Compressor and weights_proj."""
+        return normal_bf16(self.seed, f"{self.name}/x", (self.B, self.S, self.dim), device=device)
+
+    def wkv(self, device="cpu") -> torch.Tensor:
+        """Compressor kv projection [128, dim], std dim^-0.5 (kv of unit scale)."""
+        return normal_bf16(self.seed, f"{self.name}/wkv", (self.D, self.dim), std=self.dim ** -0.5, device=device)
+
+    def wgate(self, device="cpu") -> torch.Tensor:
+        """Compressor gate projection [128, dim], std dim^-0.5."""
+        return normal_bf16(self.seed, f"{self.name}/wgate", (self.D, self.dim), std=self.dim ** -0.5, device=device)
+
+    def c_norm_w(self, device="cpu") -> torch.Tensor:
+        """The Compressor's RMSNorm weight [128], 1 + N(0, 0.1) like k_norm."""
+        return normal_bf16(self.seed, f"{self.name}/c_norm_w", (self.D,), std=math.sqrt(0.1), mean=1.0,
+                           device=device)
+
+    def wproj(self, device="cpu") -> torch.Tensor:
+        """weights_proj [H, dim], std dim^-0.5 (head weights of unit scale)."""
+        return normal_bf16(self.seed, f"{self.name}/wproj", (self.H, self.dim), std=self.dim ** -0.5, device=device)
 
 
 WORKLOADS = {
