@@ -475,11 +475,12 @@ __device__ __forceinline__ void tmem_ld128(uint32_t taddr, float (&v)[128]) {
   for (int i = 0; i < 128; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Two f32 FMAs in one instruction (round to nearest each): (d0, d1) = (a0*b0 + c0, a1*b1 + c1).
+// Two f32 FMAs in one instruction (round to nearest each): (d0, d1) = (a0*b0 + c0, a1*b1 + c1),
+// through the compiler's float2 builtin, so the register pairs are the allocator's choice.
 __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
-  asm("{ .reg .b64 ra, rb, rc; mov.b64 ra, {%2, %3}; mov.b64 rb, {%4, %5}; mov.b64 rc, {%0, %1};\n\t"
-      "fma.rn.f32x2 rc, ra, rb, rc; mov.b64 {%0, %1}, rc; }"
-      : "+f"(d0), "+f"(d1) : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+  const float2 r = __ffma2_rn(make_float2(a0, a1), make_float2(b0, b1), make_float2(d0, d1));
+  d0 = r.x;
+  d1 = r.y;
 }
 
 }  // namespace indexer

@@ -194,6 +194,24 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint64_
   return __all_sync(0xffffffffu, ok);
 }
 
+// The whole warp waits (bounded) for two phases (the second only when `need2`): both polls
+// are issued before the warp branches on them, so a wait whose phases have completed costs one
+// poll's latency, not two. Warp-uniform result.
+__device__ __forceinline__ bool warp_wait2(uint32_t bar1, uint32_t par1, uint32_t bar2, uint32_t par2, bool need2,
+                                           uint64_t limit_ns) {
+  bool ok1 = mbar_try_wait(bar1, par1);
+  bool ok2 = !need2 || mbar_try_wait(bar2, par2);
+  if (!(ok1 && ok2)) {
+    const uint64_t t0 = global_ns();
+    while (!(ok1 && ok2)) {
+      if (!ok1) ok1 = mbar_try_wait(bar1, par1);
+      if (!ok2) ok2 = mbar_try_wait(bar2, par2);
+      if (!(ok1 && ok2) && global_ns() - t0 > limit_ns) break;
+    }
+  }
+  return __all_sync(0xffffffffu, ok1 && ok2);
+}
+
 template <int H, int QG, int EPI, class F>
 __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
                                   ScoreCfg<H, QG, EPI, F>::TMEM_COLS <= 256 && ScoreCfg<H, QG, EPI, F>::THREADS <= 256
@@ -550,16 +568,21 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
 //     of NSTAGE stages, each stage refilled once the MMA that read it has completed;
 //   * scale warpgroup (warps 0-3): per group, rewrites the query rows into the B operand
 //     (core-matrix order, one of two buffers) and stores their scales in tensor memory (one
-//     of two sets); per tile, once the accumulator's previous use has been drained, the
-//     four warps store the tile's A scales (each warp its own lane quadrant) and signal the
-//     MMA warp through the accumulator's "scales ready" mbarrier;
-//   * MMA warp: per tile, one thread issues the two block-scaled MMAs into one of NACC
-//     accumulators and commits to the stage's mbarrier (which frees the stage for the
-//     producer and hands the accumulator to the epilogue), so the scale stores of the next
-//     tiles overlap the issue of this one;
+//     of two sets); per tile, once the tile has landed and the MMA that last read the scale
+//     set j % NSC has completed, the four warps store the tile's A scales there (each warp its
+//     own lane quadrant) and signal the set's "ready" mbarrier. The sets form a ring of their
+//     own, so the scale warps run ahead of the accumulators instead of waiting for an
+//     epilogue to drain one;
+//   * NMMA MMA warps taking alternate tiles: once the tile's scale set is ready and its
+//     accumulator (j % NACC) has been drained, one thread issues the two block-scaled MMAs and
+//     commits to the stage's mbarrier, which frees the stage for the producer and the scale
+//     set for the scale warps and hands the accumulator to the epilogue (NSTAGE > NACC). The
+//     two waits are polled together: a wait on a completed mbarrier costs the poll's latency
+//     (~150 cycles when the warp branches on it), so each hand-off on an accumulator's round
+//     trip (MMA -> epilogue -> MMA) sets the tile rate;
 //   * EPI epilogue warpgroups take alternate tiles (over the whole sequence of groups): read
-//     the accumulator in 64-column halves, release it, form sum_h w' * max(dot, 0) per row
-//     and store; after its last tile of a group every epilogue thread releases the query
+//     the accumulator in CHUNK-column pieces, release it, form sum_h w' * max(dot, 0) per row
+//     and store; after its last tile of a group every epilogue warp releases the query
 //     buffer of that group.
 template <int H, int QG, int EPI, int NMMA, class F>
 struct RowsCfg {
@@ -573,12 +596,16 @@ struct RowsCfg {
   static constexpr int NCB = (NP + 31) / 32;
   static constexpr int SB = round_up(NCB, 4);
   static constexpr int NSTAGE = F::kFp8 ? 8 : 12;
-  // NACC accumulators (MXFP4: with their A scale sets, and two B scale sets, one per
-  // query buffer; FP8: no scale sets)
+  // NSC key-scale sets (8 columns each) in a ring of their own: a tile's A scales go into set
+  // j % NSC once the MMA that last read the set has completed, so the scale warps run ahead of
+  // the accumulators (NSC < NSTAGE keeps the stage barriers unambiguous for that wait)
+  static constexpr int NSC = 6;
+  // NACC accumulators (MXFP4: then the NSC A scale sets and two B scale sets, one per query
+  // buffer; FP8: no scale sets)
   static constexpr int NACC = F::kFp8 ? (512 / NP < 4 ? 512 / NP : 4)
-                            : 3 * (NP + 8) + 4 * SB <= 512 ? 3 : 2 * (NP + 8) + 4 * SB <= 512 ? 2 : 1;
+                            : 3 * NP + 8 * NSC + 4 * SB <= 512 ? 3 : 2 * NP + 8 * NSC + 4 * SB <= 512 ? 2 : 1;
   static constexpr int SFA_COL = NACC * NP;
-  static constexpr int SFB_COL = SFA_COL + 8 * NACC;   // set q: columns SFB_COL + 2*SB*q ..
+  static constexpr int SFB_COL = SFA_COL + 8 * NSC;   // set q: columns SFB_COL + 2*SB*q ..
   static constexpr int TMEM_NEED = F::kFp8 ? NACC * NP : SFB_COL + 4 * SB;
   static constexpr uint32_t TMEM_COLS = pow2_cols(TMEM_NEED);
   static constexpr int QB_STRIDE = round_up(NP * F::kCode, 1024);
@@ -591,8 +618,12 @@ struct RowsCfg {
   static constexpr int OFF_WS = OFF_W + 2 * W_STRIDE;                    // FP8: w' times the row's scale
   static constexpr int OFF_SFW = OFF_WS + (F::kFp8 ? 2 * W_STRIDE : 0);
   static constexpr int OFF_GD = round_up(OFF_SFW + NCB * 32 * 4, 16);   // two group descriptors
-  // full, free, done, empty, qfull, qfree, ready; FP8: scales read (per stage), scaled w' ready
-  static constexpr int NBAR = 2 * NSTAGE + 3 * NACC + 4 + (F::kFp8 ? NSTAGE + 2 : 0);
+  // barriers: full and free per stage, empty per accumulator, qfull and qfree per query
+  // buffer, ready per scale set; FP8: scales read (per stage), scaled w' ready
+  static constexpr int B_FULL = 0, B_FREE = NSTAGE, B_EMPTY = 2 * NSTAGE, B_QFULL = B_EMPTY + NACC;
+  static constexpr int B_QFREE = B_QFULL + 2, B_READY = B_QFREE + 2, B_SREAD = B_READY + NSC;
+  static constexpr int B_WS = B_SREAD + (F::kFp8 ? NSTAGE : 0);
+  static constexpr int NBAR = B_WS + (F::kFp8 ? 2 : 0);
   static constexpr int OFF_BAR = OFF_GD + 2 * 32;
   static constexpr int OFF_INFO = OFF_BAR + NBAR * 8;   // tmem, tiles issued, q phases, each MMA warp's tiles
   static constexpr int SMEM = OFF_INFO + 4 * (3 + NMMA);
@@ -603,6 +634,7 @@ struct RowsCfg {
   static_assert(NBAR <= 64, "barriers are initialised by the lanes of two passes of one warp");
   static_assert(QFREE_COUNT < (1 << 20), "mbarrier arrival count");
   static_assert(NSTAGE > NACC, "the epilogue waits on a stage's barrier for its accumulator");
+  static_assert(NSTAGE > NSC, "the scale warps wait on a stage's barrier for a scale set");
   static_assert(OFF_GD + 64 + NBAR * 8 + 16 + 1024 <= 227 * 1024, "shared memory budget");
 };
 
@@ -625,22 +657,21 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
   const uint32_t stg0 = smem_u32(stg);
   uint32_t* sfw = reinterpret_cast<uint32_t*>(smem + C::OFF_SFW);
   const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
-  auto bar_full = [&](int st) { return bar0 + 8u * (uint32_t)st; };
-  auto bar_free = [&](int st) { return bar0 + 8u * (uint32_t)(C::NSTAGE + st); };
-  auto bar_done = [&](int c) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + c); };
-  auto bar_empty = [&](int c) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + C::NACC + c); };
-  auto bar_qfull = [&](int q) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + 2 * C::NACC + q); };
-  auto bar_qfree = [&](int q) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + 2 * C::NACC + 2 + q); };
-  auto bar_ready = [&](int c) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + 2 * C::NACC + 4 + c); };
-  auto bar_sread = [&](int st) { return bar0 + 8u * (uint32_t)(2 * C::NSTAGE + 3 * C::NACC + 4 + st); };
-  auto bar_wsready = [&](int q) { return bar0 + 8u * (uint32_t)(3 * C::NSTAGE + 3 * C::NACC + 4 + q); };
+  auto bar_full = [&](int st) { return bar0 + 8u * (uint32_t)(C::B_FULL + st); };
+  auto bar_free = [&](int st) { return bar0 + 8u * (uint32_t)(C::B_FREE + st); };
+  auto bar_empty = [&](int c) { return bar0 + 8u * (uint32_t)(C::B_EMPTY + c); };
+  auto bar_qfull = [&](int q) { return bar0 + 8u * (uint32_t)(C::B_QFULL + q); };
+  auto bar_qfree = [&](int q) { return bar0 + 8u * (uint32_t)(C::B_QFREE + q); };
+  auto bar_ready = [&](int sc) { return bar0 + 8u * (uint32_t)(C::B_READY + sc); };
+  auto bar_sread = [&](int st) { return bar0 + 8u * (uint32_t)(C::B_SREAD + st); };
+  auto bar_wsready = [&](int q) { return bar0 + 8u * (uint32_t)(C::B_WS + q); };
   if (warp == 0) {
     for (int i = lane; i < C::NBAR; i += 32) {
-      const bool empty_bar = i >= 2 * C::NSTAGE + C::NACC && i < 2 * C::NSTAGE + 2 * C::NACC;
-      const bool qfree_bar = i >= 2 * C::NSTAGE + 2 * C::NACC + 2 && i < 2 * C::NSTAGE + 2 * C::NACC + 4;
-      const bool ready_bar = i >= 2 * C::NSTAGE + 2 * C::NACC + 4 && i < 2 * C::NSTAGE + 3 * C::NACC + 4;
-      const bool sread_bar = i >= 2 * C::NSTAGE + 3 * C::NACC + 4 && i < 3 * C::NSTAGE + 3 * C::NACC + 4;
-      const bool ws_bar = i >= 3 * C::NSTAGE + 3 * C::NACC + 4;
+      const bool empty_bar = i >= C::B_EMPTY && i < C::B_EMPTY + C::NACC;
+      const bool qfree_bar = i >= C::B_QFREE && i < C::B_QFREE + 2;
+      const bool ready_bar = i >= C::B_READY && i < C::B_READY + C::NSC;
+      const bool sread_bar = F::kFp8 && i >= C::B_SREAD && i < C::B_SREAD + C::NSTAGE;
+      const bool ws_bar = F::kFp8 && i >= C::B_WS;
       // a query buffer is released by the scale warpgroup and the MMA warp (once they have
       // read it) and by every epilogue thread (once the group's last accumulator has been
       // read); an accumulator's scales are ready once the four scale warps have stored them;
@@ -795,11 +826,12 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
       }
       for (int i = 0; i < d.nt; ++i, ++j) {
         if (failed) continue;   // no more waits; the next group start reports it
-        const int st = (int)(j % C::NSTAGE), c = (int)(j % C::NACC);
-        // the tile has landed, and accumulator c (with its scale set) has been drained; each
-        // warp goes on by itself and arrives on the accumulator's "ready" barrier
-        bool ok = warp_wait(bar_full(st), (j / C::NSTAGE) & 1u, wait_ns);
-        if (ok && j >= (uint32_t)C::NACC) ok = warp_wait(bar_empty(c), ((j - C::NACC) / C::NACC) & 1u, wait_ns);
+        const int st = (int)(j % C::NSTAGE), sc = (int)(j % C::NSC);
+        // the tile has landed, and the MMA that last read scale set sc (tile j - NSC) has
+        // completed; each warp goes on by itself and arrives on the set's "ready" barrier
+        const uint32_t prev = j - (uint32_t)C::NSC;
+        const bool ok = warp_wait2(bar_full(st), (j / C::NSTAGE) & 1u, bar_free((int)(prev % C::NSTAGE)),
+                                   (prev / C::NSTAGE) & 1u, j >= (uint32_t)C::NSC, wait_ns);
         if (!ok) {
           failed = true;
           continue;
@@ -808,11 +840,11 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
         if constexpr (!F::kFp8) {   // the tile's A scales
           const uint32_t w = *reinterpret_cast<const uint32_t*>(stg + st * F::kStage + page_scale_offset(key));
           const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
-          tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * c), lo, lo, lo, lo, hi, hi, hi, hi);
+          tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * sc), lo, lo, lo, lo, hi, hi, hi, hi);
         }
         tmem_wait_st();   // (also the group's B scales, for its first tile)
         tc_fence_before();
-        warp_arrive(bar_ready(c));
+        warp_arrive(bar_ready(sc));
       }
     }
   } else if (warp >= C::MMA_WARP && warp < C::PRODUCER_WARP) {
@@ -832,10 +864,12 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
       const uint32_t sfb = (uint32_t)(C::SFB_COL + qb * 2 * C::SB);
       for (int i = 0; i < d.nt; ++i, ++j) {
         if ((int)(j % NMMA) != mid) continue;
-        const int st = (int)(j % C::NSTAGE), c = (int)(j % C::NACC);
-        // the scale warps arrive on "ready" only after they have seen the tile's copy land
-        // (its full barrier), so the tile is in place once "ready" is seen
-        const bool ok = warp_wait(bar_ready(c), (j / C::NACC) & 1u, wait_ns);
+        const int st = (int)(j % C::NSTAGE), c = (int)(j % C::NACC), sc = (int)(j % C::NSC);
+        // the tile's scale set is ready (the scale warps arrive only after they have seen the
+        // tile's copy land, so the tile is in place too) and accumulator c has been drained by
+        // the epilogue of tile j - NACC
+        const bool ok = warp_wait2(bar_ready(sc), (j / C::NSC) & 1u, bar_empty(c), ((j - C::NACC) / C::NACC) & 1u,
+                                   j >= (uint32_t)C::NACC, wait_ns);
         if (!ok) {
           failed = true;
           break;
@@ -844,7 +878,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
           tc_fence_after();
           const uint32_t pa = stg0 + (uint32_t)(st * F::kStage);
           const uint32_t acc = tmem + (uint32_t)(c * C::NP);
-          const uint32_t sfa = tmem + (uint32_t)(C::SFA_COL + 8 * c);
+          const uint32_t sfa = tmem + (uint32_t)(C::SFA_COL + 8 * sc);
           issue_tile_mma<F, C::NP>(acc, pa, qbaddr, sfa, tmem + sfb, C::SB);
           tc_commit(bar_free(st));   // the stage may be refilled and the accumulator read
           info[3 + mid] = j + 1;
@@ -926,7 +960,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
             tmem_ld32(tq + (uint32_t)(c * C::NP + CH * h), v);
           if (h == C::NCB * 32 / CH - 1) {
             tc_fence_before();
-            warp_arrive(bar_empty(c));   // accumulator c and its scale set may be reused
+            warp_arrive(bar_empty(c));   // accumulator c may take tile j + NACC
           }
 #pragma unroll
           for (int u = 0; u < CH; u += 4) {
@@ -1005,6 +1039,7 @@ int sm_count() {
   return cached[dev];
 }
 
+
 template <int H, int QG, int EPI, class F>
 cudaError_t launch_cfg(ScoreArgs a, cudaStream_t stream) {
   using C = ScoreCfg<H, QG, EPI, F>;
@@ -1082,12 +1117,10 @@ cudaError_t launch_rows(ScoreArgs a, cudaStream_t stream) {
                            a);
 }
 
-#ifndef ROWS_EPI
-#define ROWS_EPI 2
-#endif
-#ifndef ROWS_NMMA
-#define ROWS_NMMA 2
-#endif
+// The several-row kernel's epilogue warpgroups and MMA warps. Long sequences (>= 4096 keys)
+// with the model's 64 heads take a third epilogue warpgroup (32-column accumulator loads):
+// large prefill scores 2.665 against 2.747 ms, while 2048-key rows lose 4 % with it.
+constexpr int kRowsEpi = 2, kRowsEpiLong = 3, kRowsMma = 2, kRowsLongT = 4096;
 
 template <class F>
 cudaError_t launch_scores_fmt(const ScoreArgs& a, cudaStream_t stream) {
@@ -1095,14 +1128,16 @@ cudaError_t launch_scores_fmt(const ScoreArgs& a, cudaStream_t stream) {
   // with score_group_rows(H, true))
   const bool single = a.S == 1;
   if (!single && a.cand == nullptr && a.sched != nullptr) {
-    // several rows per group: the persistent kernel (N = 128, ROWS_EPI epilogue warpgroups,
-    // ROWS_NMMA MMA warps taking alternate tiles)
+    // several rows per group: the persistent kernel (N = 128, kRowsEpi epilogue warpgroups,
+    // kRowsMma MMA warps taking alternate tiles)
     switch (a.H) {
-      case 8: return launch_rows<8, 16, ROWS_EPI, ROWS_NMMA, F>(a, stream);
-      case 16: return launch_rows<16, 8, ROWS_EPI, ROWS_NMMA, F>(a, stream);
-      case 32: return launch_rows<32, 4, ROWS_EPI, ROWS_NMMA, F>(a, stream);
-      case 64: return launch_rows<64, 2, ROWS_EPI, ROWS_NMMA, F>(a, stream);
-      case 128: return launch_rows<128, 1, ROWS_EPI, ROWS_NMMA, F>(a, stream);
+      case 8: return launch_rows<8, 16, kRowsEpi, kRowsMma, F>(a, stream);
+      case 16: return launch_rows<16, 8, kRowsEpi, kRowsMma, F>(a, stream);
+      case 32: return launch_rows<32, 4, kRowsEpi, kRowsMma, F>(a, stream);
+      case 64:
+        return a.T >= kRowsLongT ? launch_rows<64, 2, kRowsEpiLong, kRowsMma, F>(a, stream)
+                                 : launch_rows<64, 2, kRowsEpi, kRowsMma, F>(a, stream);
+      case 128: return launch_rows<128, 1, kRowsEpi, kRowsMma, F>(a, stream);
       default: return cudaErrorInvalidValue;
     }
   }

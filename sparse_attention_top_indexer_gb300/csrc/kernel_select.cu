@@ -42,8 +42,14 @@ struct TopkKept {
 // in position order (select_top). Rows with no candidate filter and vis <= k_eff take the
 // short-context fill [0 .. vis).
 
+// Many rows per SM: the 256-thread builds are register-capped so that more rows share an SM
+// and hide more of each row's latency chain: 32 keys a thread at 64 registers (four CTAs;
+// large prefill 0.92 against 1.06 ms with three), 8 keys at 40 (six CTAs; the 2048-key
+// prefill 41.0 against 44.7 us with five).
+constexpr int topk_min_ctas(int NT, int KPT) { return NT != 256 ? 1 : KPT == 32 ? 4 : KPT == 8 ? 6 : 1; }
+
 template <int NT, int KPT>
-__global__ void __launch_bounds__(NT, 1) topk_kernel(const TopkArgs a) {
+__global__ void __launch_bounds__(NT, topk_min_ctas(NT, KPT)) topk_kernel(const TopkArgs a) {
   __shared__ SelectShared<NT> sh;
   __shared__ TopkKept kb;
   const int tid = threadIdx.x;
@@ -71,31 +77,37 @@ __global__ void __launch_bounds__(NT, 1) topk_kernel(const TopkArgs a) {
 
   const int base = tid * KPT;
   const float* src = a.scores + (size_t)row * a.ld;
-  auto make_key = [&](float f, int t) -> uint32_t {
-    bool ok = t < vis && isfinite(f);
-    if (ok && a.cand) {
-      const int blk = t / a.cbs;
-      ok = (kb.kept[blk >> 5] >> (blk & 31)) & 1u;
-    }
-    return ok ? order_key(f) : 0u;
-  };
+  auto make_key = [&](float f, int t) -> uint32_t { return t < vis && isfinite(f) ? order_key(f) : 0u; };
   uint32_t key[KPT];
-  if ((a.ld & 3) == 0) {   // rows start 16-byte aligned: float4 loads
 #pragma unroll
-    for (int j = 0; j < KPT; j += 4) {
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (base + j < vis) v = *reinterpret_cast<const float4*>(src + base + j);
-      key[j] = make_key(v.x, base + j);
-      key[j + 1] = make_key(v.y, base + j + 1);
-      key[j + 2] = make_key(v.z, base + j + 2);
-      key[j + 3] = make_key(v.w, base + j + 3);
+  for (int j = 0; j < KPT; ++j) key[j] = 0u;
+  if (base < vis) {   // threads past the visible positions hold no key
+    if ((a.ld & 3) == 0) {   // rows start 16-byte aligned: float4 loads
+#pragma unroll
+      for (int j = 0; j < KPT; j += 4) {
+        if (base + j < vis) {
+          const float4 v = *reinterpret_cast<const float4*>(src + base + j);
+          key[j] = make_key(v.x, base + j);
+          key[j + 1] = make_key(v.y, base + j + 1);
+          key[j + 2] = make_key(v.z, base + j + 2);
+          key[j + 3] = make_key(v.w, base + j + 3);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < KPT; ++j)
+        if (base + j < vis) key[j] = make_key(src[base + j], base + j);
     }
-  } else {
+    if (a.cand) {   // the candidate filter: positions outside the kept blocks hold no key
 #pragma unroll
-    for (int j = 0; j < KPT; ++j) key[j] = base + j < vis ? make_key(src[base + j], base + j) : 0u;
+      for (int j = 0; j < KPT; ++j) {
+        const int blk = (base + j) / a.cbs;   // < the row's blocks where key[j] != 0 (t < vis <= T)
+        if (key[j] != 0u && !((kb.kept[blk >> 5] >> (blk & 31)) & 1u)) key[j] = 0u;
+      }
+    }
   }
 
-  select_top<NT, KPT>(key, k_eff, out, a.topk, a.offset, sh);
+  select_top<NT, KPT>(key, k_eff, out, a.topk, a.offset, sh, vis);
 }
 
 // Level two with one query row: the top-k over the kept candidate blocks only. The row's
@@ -165,7 +177,7 @@ __global__ void __launch_bounds__(NT, 1) topk_sparse_kernel(const TopkArgs a) {
       }
     }
   }
-  select_top<NT, KPT>(key, k_eff, out, a.topk, 0, sh.sel);
+  select_top<NT, KPT>(key, k_eff, out, a.topk, 0, sh.sel, E);
   __syncthreads();   // every list index is written
   for (int i = tid; i < a.topk; i += NT) {
     const int g = out[i];
@@ -312,7 +324,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) cand_topk_kernel(const CandArg
     for (int i = tid; i < a.topk; i += kSelThreads) out[i] = i < vis ? i + a.offset : -1;
     return;
   }
-  select_top<kSelThreads, KPT>(key, k_eff, out, a.topk, a.offset, sh.sel);
+  select_top<kSelThreads, KPT>(key, k_eff, out, a.topk, a.offset, sh.sel, vis);
 }
 
 template <int KPT>

@@ -1,5 +1,6 @@
 // CTA-wide top-k selection over order-preserving uint32 keys held in registers, shared by
-// the stand-alone top-k kernel and the fused decode kernel.
+// the top-k kernels (all positions, the kept candidate positions, the fused candidate
+// blocks + top-k) and the candidate-block selection.
 //
 // Thread t holds the keys of positions [t*KPT, (t+1)*KPT); key 0 marks a position that
 // cannot be selected. The k_eff largest keys are kept, ties to the lower position, and
@@ -9,7 +10,8 @@
 // early once its bin holds exactly the keys still needed. With many rows per SM one warp
 // searches each histogram (fewer instructions); with one row per SM all threads do (a
 // shorter chain). One CTA-wide scan of packed (equal, greater) counts then gives every
-// thread its output slot, so no sort is needed.
+// thread its output slot, and each thread writes its selected positions from a bit mask,
+// so no sort is needed.
 #pragma once
 
 #include <cstdint>
@@ -27,10 +29,8 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 constexpr int kHistBins = 2048;
 
 // Radix digits of the selection, most significant first: 11 + 11 + 10 bits. The first
-// digit spreads typical score rows over ~100 bins, so plain shared-memory atomics see
-// little contention.
-__device__ __forceinline__ int digit_shift(int p) { return p == 0 ? 21 : (p == 1 ? 10 : 0); }
-__device__ __forceinline__ uint32_t digit_mask(int p) { return p == 2 ? 0x3FFu : 0x7FFu; }
+// digit spreads typical score rows over ~100 bins; shared-memory atomics see little
+// contention even when it does not (uniform scores in [1, 2), four bins: +8 % time).
 
 template <int NT>
 struct SelectShared {
@@ -71,12 +71,20 @@ __device__ __forceinline__ uint32_t cta_scan(uint32_t v, uint32_t& total, Select
 // below 2047 - 64 l, visiting them in an order rotated by l so that the lanes read 32
 // different banks; a scan of those sums from the top picks the lane holding the key, and
 // the warp then scans that lane's 64 bins two per lane.
+// BATCH loads are in flight at a time (64: all of them, for builds whose registers are capped
+// anyway; 8 otherwise, since a full unroll takes ~80 more registers).
+template <int BATCH>
 __device__ __forceinline__ void warp_search(const uint32_t* h, uint32_t need, uint32_t* bc) {
+  static_assert(BATCH % 8 == 0 && 64 % BATCH == 0, "whole batches of the eight partial sums");
   const int lane = threadIdx.x & 31;
   const int top = kHistBins - 1 - 64 * lane;
-  uint32_t own = 0u;
-#pragma unroll 16
-  for (int i = 0; i < 64; ++i) own += h[top - ((i + lane) & 63)];
+  uint32_t part[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};   // eight independent sums: a short add chain
+#pragma unroll 1
+  for (int i0 = 0; i0 < 64; i0 += BATCH) {
+#pragma unroll
+    for (int i = 0; i < BATCH; ++i) part[i & 7] += h[top - ((i0 + i + lane) & 63)];
+  }
+  const uint32_t own = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
   uint32_t incl = own;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -144,82 +152,96 @@ __device__ __forceinline__ void cta_search(const uint32_t* h, uint32_t need, Sel
 
 // All NT threads must call it; it ends with every output written by its thread (no
 // trailing barrier). WARP_SEARCH: one warp searches the histograms (many rows per SM);
-// otherwise all threads do (one row per SM, where the search's latency counts).
+// otherwise all threads do (one row per SM, where the search's latency counts). Only
+// threads with base < span may hold a nonzero key: the others skip the per-key loops.
+//
+// Instruction count is what bounds many rows per SM, so each step is lean: a valid key is
+// >= 0x00800000, so the first digit of a valid key is >= 4 and the first pass needs no
+// prefix test, and every later prefix is nonzero (a zero key never matches it); the
+// compaction builds a bit mask of the thread's selected keys and visits only those.
 template <int NT, int KPT, bool WARP_SEARCH = (NT <= 256)>
 __device__ void select_top(const uint32_t (&key)[KPT], int k_eff, int32_t* out, int width, int offset,
-                           SelectShared<NT>& sh) {
+                           SelectShared<NT>& sh, int span = NT * KPT) {
   static_assert(NT % 32 == 0 && NT >= 32, "whole warps");
+  static_assert(KPT <= 32, "one bit per key in a 32-bit mask");
   const int tid = threadIdx.x;
   const int base = tid * KPT;
+  const bool live = base < span;
   for (int i = tid; i < 2 * kHistBins; i += NT) (&sh.hist[0][0])[i] = 0u;
   __syncthreads();
 
-  uint32_t prefix = 0u, mask = 0u, need = (uint32_t)k_eff, kstar = 0u;
-  bool select_all = false, settled = false;
-#pragma unroll 1
-  for (int p = 0; p < 3; ++p) {
-    const int shift = digit_shift(p);
-    const uint32_t dm = digit_mask(p);
-    uint32_t* h = sh.hist[p & 1];
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) {
-      const uint32_t k = key[j];
-      if (k != 0u && (k & mask) == prefix) atomicAdd(&h[(k >> shift) & dm], 1u);
-    }
-    __syncthreads();
+  auto search = [&](const uint32_t* h, uint32_t need) {
     if constexpr (WARP_SEARCH) {
-      if (tid < 32) warp_search(h, need, sh.bc);
+      if (tid < 32) warp_search<KPT >= 32 ? 64 : 8>(h, need, sh.bc);
     } else {
       cta_search<NT>(h, need, sh);
     }
     __syncthreads();
-    if (p == 0 && sh.bc[3] <= need) {   // no more valid keys than k_eff: take them all
-      select_all = true;
-      break;
-    }
-    const uint32_t bin = sh.bc[0];
-    need -= sh.bc[1];
-    prefix |= bin << shift;
-    mask |= dm << shift;
-    if (sh.bc[2] == need) {   // the whole bin is taken: every key >= prefix
-      kstar = (prefix > 0u ? prefix : 1u) - 1u;
-      need = 0u;
-      settled = true;
-      break;
-    }
-    // zero this histogram for the pass after next (its atomics follow the next barrier)
-    for (int i = tid; i < kHistBins; i += NT) h[i] = 0u;
+  };
+
+  uint32_t need = (uint32_t)k_eff, kstar = 0u;
+  // pass 0: the top 11 bits
+  if (live) {
+#pragma unroll
+    for (int j = 0; j < KPT; ++j)
+      if (key[j] != 0u) atomicAdd(&sh.hist[0][key[j] >> 21], 1u);
   }
-  if (select_all) {
-    kstar = 0u;
+  __syncthreads();
+  search(sh.hist[0], need);
+  if (sh.bc[3] <= need) {   // no more valid keys than k_eff: take them all
     need = 0u;
-  } else if (!settled) {
-    kstar = prefix;          // all 32 bits fixed; `need` keys equal to it are still taken
+  } else {
+    uint32_t prefix = sh.bc[0] << 21, mask = 0xFFE00000u;
+    need -= sh.bc[1];
+    bool settled = sh.bc[2] == need;   // the whole bin is taken: every key >= prefix
+#pragma unroll 1
+    for (int p = 1; p < 3 && !settled; ++p) {
+      const int shift = p == 1 ? 10 : 0;
+      const uint32_t dm = p == 1 ? 0x7FFu : 0x3FFu;
+      uint32_t* h = sh.hist[p & 1];
+      if (p == 2) {   // pass 0's histogram, read by its search before the last barrier
+        for (int i = tid; i < kHistBins; i += NT) h[i] = 0u;
+        __syncthreads();
+      }
+      if (live) {
+#pragma unroll
+        for (int j = 0; j < KPT; ++j)
+          if ((key[j] & mask) == prefix) atomicAdd(&h[(key[j] >> shift) & dm], 1u);
+      }
+      __syncthreads();
+      search(h, need);
+      need -= sh.bc[1];
+      prefix |= sh.bc[0] << shift;
+      mask |= dm << shift;
+      settled = sh.bc[2] == need;
+    }
+    if (settled) {
+      kstar = prefix - 1u;   // prefix > 0 (see above)
+      need = 0u;
+    } else {
+      kstar = prefix;        // all 32 bits fixed; `need` keys equal to it are still taken
+    }
   }
 
-  // ordered compaction: one scan of (equal << 16 | greater) per thread
-  uint32_t gt = 0u, eq = 0u;
+  // ordered compaction: the keys above kstar, then the first `need` equal to it
+  uint32_t gtm = 0u, eqm = 0u;
+  if (live) {
 #pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    gt += key[j] > kstar;
-    eq += (need != 0u && key[j] == kstar);
+    for (int j = 0; j < KPT; ++j) {
+      gtm |= (key[j] > kstar ? 1u : 0u) << j;
+      if (need != 0u) eqm |= (key[j] == kstar ? 1u : 0u) << j;
+    }
   }
-  const uint32_t packed = (eq << 16) | gt;
+  const uint32_t packed = ((uint32_t)__popc(eqm) << 16) | (uint32_t)__popc(gtm);
   uint32_t total;
   const uint32_t before = cta_scan<NT>(packed, total, sh);   // (the passes read warp_tot before their last barrier)
   const uint32_t eq_before = before >> 16;
+  // equal keys are taken in position order: this thread's first (need - eq_before) of them
+  uint32_t take = need > eq_before ? need - eq_before : 0u;
+  uint32_t sel = gtm;
+  for (uint32_t m = eqm; m != 0u && take != 0u; m &= m - 1u, --take) sel |= m & (0u - m);
   uint32_t slot = (before & 0xFFFFu) + min(eq_before, need);
-  uint32_t eq_seen = eq_before;
-#pragma unroll
-  for (int j = 0; j < KPT; ++j) {
-    const uint32_t k = key[j];
-    if (k > kstar) {
-      out[slot++] = base + j + offset;
-    } else if (need != 0u && k == kstar) {
-      if (eq_seen < need) out[slot++] = base + j + offset;
-      ++eq_seen;
-    }
-  }
+  for (; sel != 0u; sel &= sel - 1u) out[slot++] = base + (__ffs(sel) - 1) + offset;
   const int sel_total = (int)((total & 0xFFFFu) + min(total >> 16, need));
   for (int i = sel_total + tid; i < width; i += NT) out[i] = -1;
 }
