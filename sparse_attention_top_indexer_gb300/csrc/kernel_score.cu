@@ -581,7 +581,8 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
 //     (~150 cycles when the warp branches on it), so each hand-off on an accumulator's round
 //     trip (MMA -> epilogue -> MMA) sets the tile rate;
 //   * EPI epilogue warpgroups take alternate tiles (over the whole sequence of groups): read
-//     the accumulator in CHUNK-column pieces, release it, form sum_h w' * max(dot, 0) per row
+//     the accumulator in 32-column pieces (each read in flight during the previous piece's
+//     arithmetic), release it, form sum_h w' * max(dot, 0) per row
 //     and store; after its last tile of a group every epilogue warp releases the query
 //     buffer of that group.
 template <int H, int QG, int EPI, int NMMA, class F>
@@ -590,7 +591,6 @@ struct RowsCfg {
   static constexpr int MMA_WARP = 4 * (1 + EPI);              // the first of NMMA MMA warps
   static constexpr int PRODUCER_WARP = MMA_WARP + NMMA;
   static constexpr int QFREE_COUNT = 4 * (1 + EPI) + NMMA;    // warps: scale warpgroup, epilogue, MMA
-  static constexpr int CHUNK = EPI >= 3 ? 32 : 64;            // accumulator columns an epilogue load takes
   static constexpr int N = QG * H;
   static constexpr int NP = round_up(N, 16);
   static constexpr int NCB = (NP + 31) / 32;
@@ -627,7 +627,7 @@ struct RowsCfg {
   static constexpr int OFF_BAR = OFF_GD + 2 * 32;
   static constexpr int OFF_INFO = OFF_BAR + NBAR * 8;   // tmem, tiles issued, q phases, each MMA warp's tiles
   static constexpr int SMEM = OFF_INFO + 4 * (3 + NMMA);
-  static_assert(N <= 256 && NCB * 32 % 64 == 0, "epilogue reads 64-column halves");
+  static_assert(N <= 256, "MMA N is at most 256");
   static_assert(NMMA >= 1 && 3 + NMMA <= 8, "MMA warps");
   static_assert(TMEM_NEED <= (int)TMEM_COLS && TMEM_COLS <= 512u, "tensor memory budget");
   static_assert(SFA_COL % 4 == 0 && SFB_COL % 4 == 0 && SB % 4 == 0, "scale sets must be 4-column aligned");
@@ -950,29 +950,37 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
         for (int qi = 0; qi < QG; ++qi)
 #pragma unroll
           for (int p = 0; p < P; ++p) part[qi][p] = 0.f;
-        constexpr int CH = C::CHUNK;
+        // 32-column pieces of the accumulator, each read issued before the previous piece's
+        // arithmetic so that the read's latency overlaps it; the accumulator is released once
+        // the last piece is in registers
+        constexpr int NH = C::NCB;
+        const uint32_t acc_addr = tq + (uint32_t)(c * C::NP);
+        uint32_t ra[32], rb[32];
+        tmem_ld32_issue(acc_addr, ra);
+        tmem_ld32_wait(ra);
 #pragma unroll
-        for (int h = 0; h < C::NCB * 32 / CH; ++h) {   // CH-column pieces of the accumulator
-          float v[CH];
-          if constexpr (CH == 64)
-            tmem_ld64(tq + (uint32_t)(c * C::NP + CH * h), v);
-          else
-            tmem_ld32(tq + (uint32_t)(c * C::NP + CH * h), v);
-          if (h == C::NCB * 32 / CH - 1) {
+        for (int h = 0; h < NH; ++h) {
+          uint32_t(&cur)[32] = (h & 1) ? rb : ra;
+          uint32_t(&nxt)[32] = (h & 1) ? ra : rb;
+          if (h + 1 < NH) {
+            tmem_ld32_issue(acc_addr + (uint32_t)(32 * (h + 1)), nxt);
+          } else {
             tc_fence_before();
             warp_arrive(bar_empty(c));   // accumulator c may take tile j + NACC
           }
 #pragma unroll
-          for (int u = 0; u < CH; u += 4) {
-            const int n = CH * h + u;
+          for (int u = 0; u < 32; u += 4) {
+            const int n = 32 * h + u;
             if (n < C::N) {
               const float4 w4 = *reinterpret_cast<const float4*>(wq + n);
               const int qi = n / H, p0 = (n % P), p1 = ((n + 2) % P);
-              ffma2(part[qi][p0], part[qi][p0 + 1], w4.x, w4.y, fmaxf(v[u], 0.f), fmaxf(v[u + 1], 0.f));
-              ffma2(part[(n + 2) / H][p1], part[(n + 2) / H][p1 + 1], w4.z, w4.w, fmaxf(v[u + 2], 0.f),
-                    fmaxf(v[u + 3], 0.f));
+              ffma2(part[qi][p0], part[qi][p0 + 1], w4.x, w4.y, fmaxf(__uint_as_float(cur[u]), 0.f),
+                    fmaxf(__uint_as_float(cur[u + 1]), 0.f));
+              ffma2(part[(n + 2) / H][p1], part[(n + 2) / H][p1 + 1], w4.z, w4.w,
+                    fmaxf(__uint_as_float(cur[u + 2]), 0.f), fmaxf(__uint_as_float(cur[u + 3]), 0.f));
             }
           }
+          if (h + 1 < NH) tmem_ld32_wait(nxt);
         }
         const int t = i * kTileKeys + et;
         if (t < d.Tb) {
