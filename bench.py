@@ -32,6 +32,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import dataclasses
 import json
 import math
 import os
@@ -82,6 +83,11 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget for cpu_baseline")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-per-config", action="store_true", help="skip the other configurations' sub-records")
+    p.add_argument("--profile-kernel", default=None, choices=["publish", "prep_q", "scores", "topk", "candidates"],
+                   help="run the workload's kernels once through the split entry points, then this kernel three "
+                        "times, and exit (a short, small-footprint command for ncu captures)")
+    p.add_argument("--batch", type=int, default=None,
+                   help="override the workload's batch (a smaller case of the same kernels, for ncu captures)")
     a = p.parse_args()
     if a.steps is None:
         a.steps = DEFAULT_STEPS.get(a.workload, 1000)
@@ -363,6 +369,8 @@ def run_ours(args, dist: Dist, name=None, steps=None, warmup=None, with_e2e=True
     steps = steps or args.steps
     warmup = args.warmup if warmup is None else warmup
     wl = WORKLOADS[name]
+    if args.batch and name == args.workload:
+        wl = dataclasses.replace(wl, B=args.batch)
     dev = torch.device("cuda", dist.local)
     torch.cuda.set_device(dev)
     big_inputs = wl.B * wl.S * wl.H * wl.D * 2 > 256 * 1024 * 1024
@@ -951,8 +959,32 @@ def run_reference(args, dist: Dist):
     return line, wl
 
 
+def profile_kernel(args):
+    """The workload's kernels once each through the split entry points (so every input of the
+    named kernel is real), then the named kernel three more times; prints one short line."""
+    wl = WORKLOADS[args.workload]
+    if args.batch:
+        wl = dataclasses.replace(wl, B=args.batch)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    st = Setup(wl, dev, 1)
+    kinds = st.kernel_kinds()
+    order = ["publish", "prep_q", "scores"] + (["candidates"] if wl.two_level else []) + ["topk"]
+    for k in order:
+        kinds[k](0)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        kinds[args.profile_kernel](0)
+    torch.cuda.synchronize()
+    st.X.indexer_status(st.ws)
+    print(json.dumps({"profile_kernel": args.profile_kernel, "workload": describe(wl)}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.profile_kernel:
+        profile_kernel(args)
+        return
     dist = Dist()
     try:
         if args.impl == "reference":

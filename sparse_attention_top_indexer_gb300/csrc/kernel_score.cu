@@ -693,13 +693,17 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
   const uint32_t tmem = info[0];
   bool failed = false;
   const uint64_t wait_ns = a.wait_ns ? a.wait_ns : kWaitLimitNs;
+  // every role waits for the kernels before (query rows, w', pages, the group list; the
+  // scores they read) before its first bounded wait, so that no wait's clock starts while
+  // the dependency is still running (a kernel before that runs longer than the limit would
+  // otherwise make these waits run out)
+  pdl_wait();
 
   if (warp == C::PRODUCER_WARP) {
     // ------------------------------------------------------------ producer warp
     // (a test of the bounded waits holds this role back: no group, copy or MMA is ever
     // issued and every other role's first wait runs out)
     if (!a.hold_producer) {
-    pdl_wait();   // query rows, w', pages and the group list of the kernels before are complete
     const int gps = (a.S + QG - 1) / QG;                       // uniform batch: groups per sequence
     const long long total = a.groups ? (long long)a.n_groups : (long long)gps * a.B;
     uint32_t j = 0;                                            // tiles issued
@@ -893,7 +897,6 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
     const int et = (tid - 128) & (kEpiThreads - 1);   // key within the tile == TMEM lane
     const int ge = tid - 128;
     const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    pdl_wait();   // the scores of the kernels before have been read
     uint32_t j = 0;
     for (int k = 0; !failed; ++k) {
       const int qb = k & 1;
