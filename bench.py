@@ -766,16 +766,27 @@ def run_e2e(st: Setup, n_steps: int, dist: Dist):
         qd = torch.empty_like(st.qr[0])
     host_call = not wl.fused_q and not wl.two_level   # one C call takes the host buffers itself
     if host_call:
-        ws_h = torch.empty(X.indexer_workspace_size_host(st.dims, wl.B, wl.S, wl.start_pos, lh[0].shape[1],
-                                                         lh[0].shape[2]), dtype=torch.uint8, device=st.dev)
-        X.indexer_workspace_init(ws_h)
+        # consecutive steps alternate between two streams, each with its own workspace, output
+        # buffer and key cache (where the workload rotates fewer than two), so that one step's
+        # host copies overlap the kernels of the step before, as a serving loop would run them
+        streams = [torch.cuda.Stream(device=st.dev) for _ in range(2)]
+        ws_h = []
+        for _ in range(2):
+            w_ = torch.empty(X.indexer_workspace_size_host(st.dims, wl.B, wl.S, wl.start_pos, lh[0].shape[1],
+                                                           lh[0].shape[2]), dtype=torch.uint8, device=st.dev)
+            X.indexer_workspace_init(w_)
+            ws_h.append(w_)
+        caches = st.caches if R >= 2 else [st.caches[0], st.caches[0].clone()]
+        outs = outh if R >= 2 else [outh[0], torch.empty_like(outh[0]).pin_memory()]
 
     def one(i):
         j = i % R
         if host_call:
             sp = wl.start_pos if st.decode else 0
-            X.indexer_forward_publish_host(st.dims, lh[j], st.wk, st.knw, qh[j], wh[j], sp, st.table, st.caches[j],
-                                           outh[j], ws_h)
+            k = i % 2
+            c = j if R >= 2 else k
+            X.indexer_forward_publish_host(st.dims, lh[j], st.wk, st.knw, qh[j], wh[j], sp, st.table, caches[c],
+                                           outs[c], ws_h[k], stream=streams[k])
             return
         qd.copy_(qh[j], non_blocking=True)
         wd.copy_(wh[j], non_blocking=True)
@@ -800,20 +811,29 @@ def run_e2e(st: Setup, n_steps: int, dist: Dist):
     dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
+    if host_call:
+        for s_ in streams:
+            s_.wait_event(e0)
     for i in range(steps):
         one(i)
+    if host_call:
+        for s_ in streams:
+            torch.cuda.current_stream().wait_stream(s_)
     e1.record()
     torch.cuda.synchronize()
     ms = dist.max(e0.elapsed_time(e1))
     if host_call:
-        X.indexer_status(ws_h)
+        for w_ in ws_h:
+            X.indexer_status(w_)
     h2d = qh[0].numel() * 2 + wh[0].numel() * 2 + lh[0].numel() * 2
     d2h = outh[0].numel() * 4
     return {"value": dist.world * wl.B * wl.S * steps / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": ms / steps,
             "api": ("indexer_publish_k, indexer_prep_q_proj, indexer_scores, indexer_topk" if wl.fused_q
                     else "indexer_forward_publish_host" if host_call else "indexer_forward_publish")
-                   + " (eager Python/ctypes calls, pinned host buffers)"}
+                   + " (eager Python/ctypes calls, pinned host buffers"
+                   + ("; consecutive steps on two streams, each step's copies overlapping the step before)"
+                      if host_call else ")")}
 
 
 def describe(wl: Workload) -> str:

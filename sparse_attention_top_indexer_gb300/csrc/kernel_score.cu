@@ -596,6 +596,7 @@ struct RowsCfg {
   static constexpr int NCB = (NP + 31) / 32;
   static constexpr int SB = round_up(NCB, 4);
   static constexpr int NSTAGE = F::kFp8 ? 8 : 12;
+  static constexpr int PBATCH = 4;   // tiles the producer requests per poll of the stage barriers
   // NSC key-scale sets (8 columns each) in a ring of their own: a tile's A scales go into set
   // j % NSC once the MMA that last read the set has completed, so the scale warps run ahead of
   // the accumulators (NSC < NSTAGE keeps the stage barriers unambiguous for that wait)
@@ -635,6 +636,7 @@ struct RowsCfg {
   static_assert(QFREE_COUNT < (1 << 20), "mbarrier arrival count");
   static_assert(NSTAGE > NACC, "the epilogue waits on a stage's barrier for its accumulator");
   static_assert(NSTAGE > NSC, "the scale warps wait on a stage's barrier for a scale set");
+  static_assert(PBATCH <= 32 && PBATCH < NSTAGE, "a batch of stages, one lane each");
   static_assert(OFF_GD + 64 + NBAR * 8 + 16 + 1024 <= 227 * 1024, "shared memory budget");
 };
 
@@ -682,7 +684,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
                                          : ws_bar ? (uint32_t)(EPI * kEpiWarps) : 1u);
     }
     fence_mbar_init();
-    if (lane < 3 + NMMA) info[lane] = 0u;
+    if (lane >= 1 && lane < 3 + NMMA) info[lane] = 0u;   // info[0] is the allocation's, written by warp 1
   } else if (warp == 1) {
     tmem_alloc(smem_u32(&info[0]), C::TMEM_COLS);
     tmem_relinquish();
@@ -772,19 +774,25 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
           if (p0 == -2 || p1 == -2) atomicOr(a.status, kStatusBadMeta);
         }
         const int n = min(32, d.nt - i0);
-        for (int u = 0; u < n; ++u, ++j) {
-          const int st = (int)(j % C::NSTAGE);
+        // C::PBATCH tiles at a time, each requested by the lane that looked up its pages: the
+        // lanes poll their stages' barriers together, so a batch pays one poll's latency (a
+        // completed barrier still costs ~150 cycles to branch on) instead of one per tile
+        for (int u0 = 0; u0 < n; u0 += C::PBATCH) {
+          const int nb = min(C::PBATCH, n - u0);
+          const bool mine = lane >= u0 && lane < u0 + nb;
+          const uint32_t jj = j + (uint32_t)(lane - u0);   // this lane's tile (when mine)
+          const int st = (int)(jj % C::NSTAGE);
           // the stage's previous tile: its MMA has completed (FP8: and its key scales were read)
-          if (j >= (uint32_t)C::NSTAGE &&
-              !warp_wait(F::kFp8 ? bar_sread(st) : bar_free(st), ((j / C::NSTAGE) - 1) & 1u, wait_ns)) {
+          bool ok = true;
+          if (mine && jj >= (uint32_t)C::NSTAGE)
+            ok = mbar_wait(F::kFp8 ? bar_sread(st) : bar_free(st), ((jj / C::NSTAGE) - 1) & 1u, wait_ns);
+          if (!__all_sync(0xffffffffu, ok)) {
             failed = true;
             break;
           }
-          const int q0 = __shfl_sync(0xffffffffu, p0, u), q1 = __shfl_sync(0xffffffffu, p1, u);
-          if (lane == 0) {
-            issue_tile_load<F>(a, max(q0, -1), max(q1, -1), stg0 + st * F::kStage, bar_full(st));
-            info[1] = j + 1;
-          }
+          if (mine) issue_tile_load<F>(a, max(p0, -1), max(p1, -1), stg0 + st * F::kStage, bar_full(st));
+          j += (uint32_t)nb;
+          if (lane == 0) info[1] = j;
           __syncwarp();
         }
       }
