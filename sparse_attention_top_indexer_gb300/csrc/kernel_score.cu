@@ -836,27 +836,40 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
           tmem_st_x1(tq + sfb + C::SB + jj, wd >> 16);
         }
       }
+      // ring positions kept as counters: tile j's stage st, its phase ph and scale set sc;
+      // tile j - NSC's stage pst and phase pph (the MMA that last read set sc)
+      int st = (int)(j % C::NSTAGE), sc = (int)(j % C::NSC);
+      uint32_t ph = (j / C::NSTAGE) & 1u;
+      const uint32_t prev0 = j + (uint32_t)(C::NSTAGE - C::NSC);   // tile j - NSC, one ring later
+      int pst = (int)(prev0 % C::NSTAGE);
+      uint32_t pph = ((prev0 / C::NSTAGE) & 1u) ^ 1u;
       for (int i = 0; i < d.nt; ++i, ++j) {
-        if (failed) continue;   // no more waits; the next group start reports it
-        const int st = (int)(j % C::NSTAGE), sc = (int)(j % C::NSC);
-        // the tile has landed, and the MMA that last read scale set sc (tile j - NSC) has
-        // completed; each warp goes on by itself and arrives on the set's "ready" barrier
-        const uint32_t prev = j - (uint32_t)C::NSC;
-        const bool ok = warp_wait2(bar_full(st), (j / C::NSTAGE) & 1u, bar_free((int)(prev % C::NSTAGE)),
-                                   (prev / C::NSTAGE) & 1u, j >= (uint32_t)C::NSC, wait_ns);
-        if (!ok) {
-          failed = true;
-          continue;
+        if (!failed) {   // after a failure no more waits; the next group start reports it
+          // the tile has landed, and the MMA that last read scale set sc has completed; each
+          // warp goes on by itself and arrives on the set's "ready" barrier
+          if (!warp_wait2(bar_full(st), ph, bar_free(pst), pph, j >= (uint32_t)C::NSC, wait_ns)) {
+            failed = true;
+          } else {
+            tc_fence_after();
+            if constexpr (!F::kFp8) {   // the tile's A scales
+              const uint32_t w = *reinterpret_cast<const uint32_t*>(stg + st * F::kStage + page_scale_offset(key));
+              const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
+              tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * sc), lo, lo, lo, lo, hi, hi, hi, hi);
+            }
+            tmem_wait_st();   // (also the group's B scales, for its first tile)
+            tc_fence_before();
+            warp_arrive(bar_ready(sc));
+          }
         }
-        tc_fence_after();
-        if constexpr (!F::kFp8) {   // the tile's A scales
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(stg + st * F::kStage + page_scale_offset(key));
-          const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
-          tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * sc), lo, lo, lo, lo, hi, hi, hi, hi);
+        if (++st == C::NSTAGE) {
+          st = 0;
+          ph ^= 1u;
         }
-        tmem_wait_st();   // (also the group's B scales, for its first tile)
-        tc_fence_before();
-        warp_arrive(bar_ready(sc));
+        if (++sc == C::NSC) sc = 0;
+        if (++pst == C::NSTAGE) {
+          pst = 0;
+          pph ^= 1u;
+        }
       }
     }
   } else if (warp >= C::MMA_WARP && warp < C::PRODUCER_WARP) {
@@ -874,14 +887,15 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
       warp_arrive(bar_qfree(qb));   // the descriptor is in registers
       const uint32_t qbaddr = smem_u32(smem + C::OFF_QB + qb * C::QB_STRIDE);
       const uint32_t sfb = (uint32_t)(C::SFB_COL + qb * 2 * C::SB);
-      for (int i = 0; i < d.nt; ++i, ++j) {
-        if ((int)(j % NMMA) != mid) continue;
-        const int st = (int)(j % C::NSTAGE), c = (int)(j % C::NACC), sc = (int)(j % C::NSC);
+      // this warp's tiles of the group only (global tile numbers jt = mid mod NMMA)
+      const uint32_t jend = j + (uint32_t)d.nt;
+      for (uint32_t jt = j + (uint32_t)((mid - (int)(j % NMMA) + NMMA) % NMMA); jt < jend; jt += NMMA) {
+        const int st = (int)(jt % C::NSTAGE), c = (int)(jt % C::NACC), sc = (int)(jt % C::NSC);
         // the tile's scale set is ready (the scale warps arrive only after they have seen the
         // tile's copy land, so the tile is in place too) and accumulator c has been drained by
-        // the epilogue of tile j - NACC
-        const bool ok = warp_wait2(bar_ready(sc), (j / C::NSC) & 1u, bar_empty(c), ((j - C::NACC) / C::NACC) & 1u,
-                                   j >= (uint32_t)C::NACC, wait_ns);
+        // the epilogue of tile jt - NACC
+        const bool ok = warp_wait2(bar_ready(sc), (jt / C::NSC) & 1u, bar_empty(c), ((jt - C::NACC) / C::NACC) & 1u,
+                                   jt >= (uint32_t)C::NACC, wait_ns);
         if (!ok) {
           failed = true;
           break;
@@ -893,10 +907,11 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
           const uint32_t sfa = tmem + (uint32_t)(C::SFA_COL + 8 * sc);
           issue_tile_mma<F, C::NP>(acc, pa, qbaddr, sfa, tmem + sfb, C::SB);
           tc_commit(bar_free(st));   // the stage may be refilled and the accumulator read
-          info[3 + mid] = j + 1;
+          info[3 + mid] = jt + 1;
         }
         __syncwarp();
       }
+      j = jend;
     }
   } else if (warp >= 4 && warp < C::MMA_WARP) {
     // ------------------------------------------------------------ epilogue warpgroups
@@ -940,13 +955,15 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
       int visq[QG];
 #pragma unroll
       for (int qi = 0; qi < QG; ++qi) visq[qi] = min(d.Tb, (d.pos0 + qi + 1) / a.ratio);
-      for (int i = 0; i < d.nt && !failed; ++i, ++j) {
-        if ((int)(j % EPI) != grp) continue;
-        const int c = (int)(j % C::NACC);
-        // tile j's MMA has completed (its stage's barrier; the stage cannot be refilled and
+      // this warpgroup's tiles of the group only (global tile numbers jt = grp mod EPI)
+      const uint32_t jend = j + (uint32_t)d.nt;
+      for (uint32_t jt = j + (uint32_t)((grp - (int)(j % EPI) + EPI) % EPI); jt < jend && !failed; jt += EPI) {
+        const int i = (int)(jt - j);   // the tile within the group
+        const int c = (int)(jt % C::NACC);
+        // tile jt's MMA has completed (its stage's barrier; the stage cannot be refilled and
         // complete again before this accumulator is released, as NSTAGE > NACC)
-        const int st = (int)(j % C::NSTAGE);
-        if (!warp_wait(bar_free(st), (j / C::NSTAGE) & 1u, wait_ns)) {
+        const int st = (int)(jt % C::NSTAGE);
+        if (!warp_wait(bar_free(st), (jt / C::NSTAGE) & 1u, wait_ns)) {
           failed = true;
           break;
         }
@@ -977,7 +994,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
             tmem_ld32_issue(acc_addr + (uint32_t)(32 * (h + 1)), nxt);
           } else {
             tc_fence_before();
-            warp_arrive(bar_empty(c));   // accumulator c may take tile j + NACC
+            warp_arrive(bar_empty(c));   // accumulator c may take tile jt + NACC
           }
 #pragma unroll
           for (int u = 0; u < 32; u += 4) {
@@ -1008,6 +1025,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
         }
         __syncwarp();
       }
+      j = jend;
       if (failed) break;
       warp_arrive(bar_qfree(qb));   // this warp is done with the group's query buffer
     }
