@@ -585,6 +585,24 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
 //     arithmetic), release it, form sum_h w' * max(dot, 0) per row
 //     and store; after its last tile of a group every epilogue warp releases the query
 //     buffer of that group.
+// Position of a tile in a ring of M slots: the slot (tile number mod M) and the parity of the
+// ring's round (tile number / M), advanced by a stride of at most M without dividing.
+template <int M>
+struct RingPos {
+  int slot;
+  uint32_t phase;
+  __device__ __forceinline__ explicit RingPos(uint32_t t) : slot((int)(t % M)), phase((t / M) & 1u) {}
+  template <int K>
+  __device__ __forceinline__ void advance() {
+    static_assert(K >= 1 && K <= M, "one wrap at most");
+    slot += K;
+    if (slot >= M) {
+      slot -= M;
+      phase ^= 1u;
+    }
+  }
+};
+
 template <int H, int QG, int EPI, int NMMA, class F>
 struct RowsCfg {
   static constexpr int THREADS = 128 * (1 + EPI) + 32 * NMMA + 32;
@@ -876,6 +894,11 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
     // ------------------------------------------------------------ MMA warps (tile j is warp j % NMMA's)
     const int mid = warp - C::MMA_WARP;
     uint32_t j = 0;
+    // this warp's tiles: global numbers mid, mid + NMMA, ... across all groups
+    uint32_t jt = (uint32_t)mid;
+    RingPos<C::NSTAGE> rst(jt);
+    RingPos<C::NACC> rc(jt);
+    RingPos<C::NSC> rsc(jt);
     for (int k = 0; !failed; ++k) {
       const int qb = k & 1;
       if (!warp_wait(bar_qfull(qb), (uint32_t)(k >> 1) & 1u, wait_ns)) {
@@ -887,15 +910,15 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
       warp_arrive(bar_qfree(qb));   // the descriptor is in registers
       const uint32_t qbaddr = smem_u32(smem + C::OFF_QB + qb * C::QB_STRIDE);
       const uint32_t sfb = (uint32_t)(C::SFB_COL + qb * 2 * C::SB);
-      // this warp's tiles of the group only (global tile numbers jt = mid mod NMMA)
+      // this warp's tiles of the group
       const uint32_t jend = j + (uint32_t)d.nt;
-      for (uint32_t jt = j + (uint32_t)((mid - (int)(j % NMMA) + NMMA) % NMMA); jt < jend; jt += NMMA) {
-        const int st = (int)(jt % C::NSTAGE), c = (int)(jt % C::NACC), sc = (int)(jt % C::NSC);
+      for (; jt < jend; jt += NMMA, rst.template advance<NMMA>(), rc.template advance<NMMA>(), rsc.template advance<NMMA>()) {
+        const int st = rst.slot, c = rc.slot, sc = rsc.slot;
         // the tile's scale set is ready (the scale warps arrive only after they have seen the
         // tile's copy land, so the tile is in place too) and accumulator c has been drained by
-        // the epilogue of tile jt - NACC
-        const bool ok = warp_wait2(bar_ready(sc), (jt / C::NSC) & 1u, bar_empty(c), ((jt - C::NACC) / C::NACC) & 1u,
-                                   jt >= (uint32_t)C::NACC, wait_ns);
+        // the epilogue of tile jt - NACC (the accumulator's previous round)
+        const bool ok = warp_wait2(bar_ready(sc), rsc.phase, bar_empty(c), rc.phase ^ 1u, jt >= (uint32_t)C::NACC,
+                                   wait_ns);
         if (!ok) {
           failed = true;
           break;
@@ -921,6 +944,10 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
     const int ge = tid - 128;
     const uint32_t tq = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     uint32_t j = 0;
+    // this warpgroup's tiles: global numbers grp, grp + EPI, ... across all groups
+    uint32_t jt = (uint32_t)grp;
+    RingPos<C::NSTAGE> rst(jt);
+    RingPos<C::NACC> rc(jt);
     for (int k = 0; !failed; ++k) {
       const int qb = k & 1;
       if (!warp_wait(bar_qfull(qb), (uint32_t)(k >> 1) & 1u, wait_ns)) {
@@ -955,15 +982,14 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
       int visq[QG];
 #pragma unroll
       for (int qi = 0; qi < QG; ++qi) visq[qi] = min(d.Tb, (d.pos0 + qi + 1) / a.ratio);
-      // this warpgroup's tiles of the group only (global tile numbers jt = grp mod EPI)
+      // this warpgroup's tiles of the group
       const uint32_t jend = j + (uint32_t)d.nt;
-      for (uint32_t jt = j + (uint32_t)((grp - (int)(j % EPI) + EPI) % EPI); jt < jend && !failed; jt += EPI) {
+      for (; jt < jend && !failed; jt += EPI, rst.template advance<EPI>(), rc.template advance<EPI>()) {
         const int i = (int)(jt - j);   // the tile within the group
-        const int c = (int)(jt % C::NACC);
+        const int c = rc.slot, st = rst.slot;
         // tile jt's MMA has completed (its stage's barrier; the stage cannot be refilled and
         // complete again before this accumulator is released, as NSTAGE > NACC)
-        const int st = (int)(jt % C::NSTAGE);
-        if (!warp_wait(bar_free(st), (jt / C::NSTAGE) & 1u, wait_ns)) {
+        if (!warp_wait(bar_free(st), rst.phase, wait_ns)) {
           failed = true;
           break;
         }
