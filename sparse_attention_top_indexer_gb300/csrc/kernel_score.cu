@@ -1180,10 +1180,10 @@ cudaError_t launch_rows(ScoreArgs a, cudaStream_t stream) {
                            a);
 }
 
-// The several-row kernel's epilogue warpgroups and MMA warps. Long sequences (>= 4096 keys)
-// with the model's 64 heads take a third epilogue warpgroup (32-column accumulator loads):
-// large prefill scores 2.665 against 2.747 ms, while 2048-key rows lose 4 % with it.
-constexpr int kRowsEpi = 2, kRowsEpiLong = 3, kRowsMma = 2, kRowsLongT = 4096;
+// The several-row kernel's epilogue warpgroups and MMA warps. The model's 64 heads (two query
+// rows per group) take a third epilogue warpgroup: 2048-key prefill scores 92.5 against
+// 96.7 us, 8192-key rows 2.293 against 2.493 ms.
+constexpr int kRowsEpi = 2, kRowsEpi64 = 3, kRowsMma = 2;
 
 template <class F>
 cudaError_t launch_scores_fmt(const ScoreArgs& a, cudaStream_t stream) {
@@ -1197,9 +1197,7 @@ cudaError_t launch_scores_fmt(const ScoreArgs& a, cudaStream_t stream) {
       case 8: return launch_rows<8, 16, kRowsEpi, kRowsMma, F>(a, stream);
       case 16: return launch_rows<16, 8, kRowsEpi, kRowsMma, F>(a, stream);
       case 32: return launch_rows<32, 4, kRowsEpi, kRowsMma, F>(a, stream);
-      case 64:
-        return a.T >= kRowsLongT ? launch_rows<64, 2, kRowsEpiLong, kRowsMma, F>(a, stream)
-                                 : launch_rows<64, 2, kRowsEpi, kRowsMma, F>(a, stream);
+      case 64: return launch_rows<64, 2, kRowsEpi64, kRowsMma, F>(a, stream);
       case 128: return launch_rows<128, 1, kRowsEpi, kRowsMma, F>(a, stream);
       default: return cudaErrorInvalidValue;
     }
