@@ -561,30 +561,30 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
 // first pages' latency) is paid once per SM instead of once per group. Groups are fetched
 // from a counter in the workspace (a uniform batch hands out the groups with the most
 // visible keys first), which balances the causal triangle across SMs.
+// Tiles are numbered across all of a CTA's groups; a role that takes every k-th tile keeps
+// its ring positions (stage, accumulator, scale set and their phases) as counters. The SM's
+// issue slots are the limit, so every role does as little per tile as it can:
 //   * producer warp (the last warp): fetches the next group, writes its descriptor and
-//     requests its query rows and w' into one of two query buffers (once the MMA warpgroup
-//     and the epilogue have released the buffer's previous group), then streams the group's
-//     tiles through a ring
-//     of NSTAGE stages, each stage refilled once the MMA that read it has completed;
+//     requests its query rows and w' into one of two query buffers (once the other roles
+//     have released the buffer's previous group), then streams the group's tiles through a
+//     ring of NSTAGE stages, PBATCH tiles at a time: the lane that looked up a tile's pages
+//     polls that stage's barrier (the MMA that last read it has completed) and issues its copy;
 //   * scale warpgroup (warps 0-3): per group, rewrites the query rows into the B operand
 //     (core-matrix order, one of two buffers) and stores their scales in tensor memory (one
 //     of two sets); per tile, once the tile has landed and the MMA that last read the scale
 //     set j % NSC has completed, the four warps store the tile's A scales there (each warp its
 //     own lane quadrant) and signal the set's "ready" mbarrier. The sets form a ring of their
-//     own, so the scale warps run ahead of the accumulators instead of waiting for an
-//     epilogue to drain one;
-//   * NMMA MMA warps taking alternate tiles: once the tile's scale set is ready and its
-//     accumulator (j % NACC) has been drained, one thread issues the two block-scaled MMAs and
-//     commits to the stage's mbarrier, which frees the stage for the producer and the scale
-//     set for the scale warps and hands the accumulator to the epilogue (NSTAGE > NACC). The
-//     two waits are polled together: a wait on a completed mbarrier costs the poll's latency
-//     (~150 cycles when the warp branches on it), so each hand-off on an accumulator's round
-//     trip (MMA -> epilogue -> MMA) sets the tile rate;
-//   * EPI epilogue warpgroups take alternate tiles (over the whole sequence of groups): read
-//     the accumulator in 32-column pieces (each read in flight during the previous piece's
-//     arithmetic), release it, form sum_h w' * max(dot, 0) per row
-//     and store; after its last tile of a group every epilogue warp releases the query
-//     buffer of that group.
+//     own, so the scale warps run ahead of the accumulators;
+//   * NMMA MMA warps, warp m taking tiles m, m + NMMA, ...: once the tile's scale set is
+//     ready and its accumulator (j % NACC) has been drained, one thread issues the two
+//     block-scaled MMAs and commits to the stage's mbarrier, which frees the stage for the
+//     producer and the scale set for the scale warps and hands the accumulator to the epilogue
+//     (NSTAGE > NACC). The two waits are polled together: a wait on a completed mbarrier still
+//     costs the poll's latency (~150 cycles when the warp branches on it);
+//   * EPI epilogue warpgroups, warpgroup g taking tiles g, g + EPI, ...: read the accumulator
+//     in 32-column pieces (each read in flight during the previous piece's arithmetic),
+//     release it, form sum_h w' * max(dot, 0) per row and store; after its last tile of a
+//     group every epilogue warp releases the query buffer of that group.
 // Position of a tile in a ring of M slots: the slot (tile number mod M) and the parity of the
 // ring's round (tile number / M), advanced by a stride of at most M without dividing.
 template <int M>
