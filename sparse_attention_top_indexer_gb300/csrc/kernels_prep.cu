@@ -360,6 +360,78 @@ __global__ void __cluster_dims__(kPubCl, 1, 1) __launch_bounds__(kPubClThreads) 
   publish_key_cluster(a, key, rank);
 }
 
+// Many keys of a latent of at most 128 elements (prefill): a CTA of 128 threads publishes KPC
+// keys. Thread o keeps row o of wk in registers for all of them (one CTA per key would read
+// the whole 32 KB of wk from L2 for every key) and the CTA stages the keys' latents with one
+// load; each key's arithmetic is publish_key<1>'s, in the same order.
+template <int KPC>
+__global__ void __launch_bounds__(kHeadDim) publish_multi_kernel(PublishArgs a, int n_keys) {
+  constexpr int kKeysPerCta = KPC;
+  __shared__ float lat[kKeysPerCta][128];
+  __shared__ float kx[kHeadDim];
+  pdl_allow_next();
+  prefetch_wk(a, blockIdx.x);
+  pdl_wait();
+  const int tid = threadIdx.x;
+  const int key0 = (int)blockIdx.x * kKeysPerCta;
+  const int nk = min(kKeysPerCta, n_keys - key0);
+  uint4 w8[16];   // row tid of wk: elements 8u .. 8u + 7 (zero past Din)
+  const uint16_t* wrow = a.wk + (size_t)tid * a.Din;
+#pragma unroll
+  for (int u = 0; u < 16; ++u)
+    w8[u] = 8 * u < a.Din ? *reinterpret_cast<const uint4*>(wrow + 8 * u) : make_uint4(0, 0, 0, 0);
+  for (int i = tid; i < nk * 128; i += kHeadDim) {
+    const int kk = i >> 7, e = i & 127;
+    if (e < a.Din) lat[kk][e] = bf16_to_f32(key_latent(a, key0 + kk)[e]);
+  }
+  __syncthreads();
+  for (int kk = 0; kk < nk; ++kk) {
+    long long slot;
+    int pos;
+    if (!key_target(a, key0 + kk, true, slot, pos)) continue;   // the same for every thread
+    uint32_t knorm_bits = 0;
+    float2 cs = make_float2(1.f, 0.f);
+    key_tail_inputs(a, pos, tid, knorm_bits, cs);
+    // k_pre[tid] = sum_e wk[tid][e] * latent[e]: four TwoSum-carried partial sums over the
+    // element pairs of each 8-element chunk, combined in order (linear_out<1, 128>'s order)
+    float sacc[4], cacc[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sacc[k] = cacc[k] = 0.f;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      if (8 * u < a.Din) {
+        const uint32_t ww[4] = {w8[u].x, w8[u].y, w8[u].z, w8[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float p0 = __fmul_rn(bf16_to_f32(ww[k] & 0xFFFFu), lat[kk][8 * u + 2 * k]);
+          const float p1 = __fmul_rn(bf16_to_f32(ww[k] >> 16), lat[kk][8 * u + 2 * k + 1]);
+          float t, e;
+          two_sum(sacc[k], p0, t, e);
+          sacc[k] = t;
+          cacc[k] = __fadd_rn(cacc[k], e);
+          two_sum(sacc[k], p1, t, e);
+          sacc[k] = t;
+          cacc[k] = __fadd_rn(cacc[k], e);
+        }
+      }
+    }
+    float hi = sacc[0], lo = cacc[0];
+#pragma unroll
+    for (int k = 1; k < 4; ++k) {
+      float t, e;
+      two_sum(hi, sacc[k], t, e);
+      hi = t;
+      lo = __fadd_rn(__fadd_rn(lo, cacc[k]), e);
+    }
+    float t, e;
+    two_sum(hi, lo, t, e);
+    __syncthreads();   // the previous key's outputs have been read
+    kx[tid] = bf16_to_f32(f32pair_to_bf16_rne(t, e));
+    __syncthreads();
+    finish_key(a, slot, kx, knorm_bits, cs);
+  }
+}
+
 cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream) {
   const long long keys = (long long)a.B * a.G;
   // few keys (a decode step): a cluster of four CTAs per key; a few hundred: four threads
@@ -367,6 +439,16 @@ cudaError_t launch_publish(const PublishArgs& a, cudaStream_t stream) {
   if (keys <= 160)
     return launch_overlapped(publish_cluster_kernel, dim3((unsigned)(keys * kPubCl)), dim3(kPubClThreads), 0, stream, a);
   if (keys < 512) return launch_overlapped(publish_kernel<4>, dim3((unsigned)keys), dim3(4 * kHeadDim), 0, stream, a);
+  if (a.Din <= 128) {   // wk in registers, several keys per CTA (more for more keys)
+    if (keys >= 8192)
+      return launch_overlapped(publish_multi_kernel<8>, dim3((unsigned)((keys + 7) / 8)), dim3(kHeadDim), 0, stream,
+                               a, (int)keys);
+    if (keys >= 4096)
+      return launch_overlapped(publish_multi_kernel<4>, dim3((unsigned)((keys + 3) / 4)), dim3(kHeadDim), 0, stream,
+                               a, (int)keys);
+    return launch_overlapped(publish_multi_kernel<2>, dim3((unsigned)((keys + 1) / 2)), dim3(kHeadDim), 0, stream, a,
+                             (int)keys);
+  }
   return launch_overlapped(publish_kernel<1>, dim3((unsigned)keys), dim3(kHeadDim), 0, stream, a);
 }
 
