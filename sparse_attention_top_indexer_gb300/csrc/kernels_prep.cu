@@ -581,6 +581,10 @@ __global__ void __launch_bounds__(256) prep_q_bulk_kernel(PrepArgs a) {
   // batch's rows follow it, wrapping at S)
   const int qrow0 = (int)(v0 >> a.h_shift);   // H is a power of two
   const int s0 = a.rows ? 0 : qrow0 % a.S;
+  // the slice's RoPE entries, reloaded only when the position changes (the vectors of a
+  // thread are heads of one query row whenever H >= 64)
+  int cpos = -1;
+  float2 c[4];
 #pragma unroll
   for (int p = 0; p < NV / 16; ++p) {
     const int vi = 16 * p + g;
@@ -589,8 +593,11 @@ __global__ void __launch_bounds__(256) prep_q_bulk_kernel(PrepArgs a) {
       const int qrow = (int)(v >> a.h_shift);
       const int srow_ = s0 + (qrow - qrow0);
       const int pos = a.rows ? a.rows[qrow].pos : a.start_pos + (srow_ < a.S ? srow_ : srow_ % a.S);
-      float2 c[4];
-      load_rope_slice(reinterpret_cast<const float2*>(a.rope_cs) + (size_t)pos * (a.rope_dim / 2), j, a.rope_dim, c);
+      if (pos != cpos) {
+        load_rope_slice(reinterpret_cast<const float2*>(a.rope_cs) + (size_t)pos * (a.rope_dim / 2), j, a.rope_dim,
+                        c);
+        cpos = pos;
+      }
       const uint4 raw = *reinterpret_cast<const uint4*>(sq + vi * kHeadDim + j * 8);
       int e;
       if (a.fp8) {
