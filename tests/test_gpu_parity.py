@@ -202,6 +202,30 @@ def test_topk_kernel_bit_exact(X, S, start, T_over, topk, offset, ties):
     assert np.array_equal(out.cpu().numpy().reshape(B * S, topk), ref)
 
 
+# Many rows (prefill): the register-capped 256-thread builds with 8, 16 and 32 keys a thread
+# (rows of 2048, 2524 / 3025 and 8192 keys; 3025 is not a multiple of four floats, so its rows
+# take the scalar loads), short-context and selected rows mixed, ties.
+@pytest.mark.parametrize("B,S,start,topk,offset,ties", [
+    (2, 2560, 30208, 2048, 8192, False),   # T 8192, every row selected
+    (2, 4096, 6000, 2048, 0, True),        # T 2524: about half the rows take the short fill
+    (1, 8192, 0, 512, 0, False),           # T 2048, the 2048-key prefill's shape
+    (1, 4100, 8000, 1000, 3, True),        # T 3025: rows not 16-byte aligned
+])
+def test_topk_many_rows_bit_exact(X, B, S, start, topk, offset, ties):
+    ratio = 4
+    T = (start + S) // ratio
+    sc = _synthetic_scores(S + start + B, B * S, T, ties).view(B, S, T)
+    vis = O.visible_lens(start, S, ratio)
+    for s in range(S):
+        sc[:, s, vis[s]:] = float("-inf")
+    d = X.make_dims(n_heads=64, ratio=ratio, index_topk=topk, offset=offset)
+    out = torch.empty((B, S, topk), dtype=torch.int32, device="cuda")
+    X.indexer_topk(d, sc.cuda(), start, out)
+    ref = O.topk_positions(sc.double().numpy().reshape(B * S, T), np.tile(vis, B), topk, offset, T)
+    got = out.cpu().numpy().reshape(B * S, topk)
+    assert np.array_equal(got, ref), f"{np.sum(np.any(got != ref, axis=-1))} of {B * S} rows differ"
+
+
 @pytest.mark.parametrize("T,cbs,cbk,ties", [(32768, 64, 64, False), (1000, 64, 8, True), (100, 7, 40, True)])
 def test_candidate_kernel_bit_exact(X, T, cbs, cbk, ties):
     B, S, ratio = 3, 1, 4
