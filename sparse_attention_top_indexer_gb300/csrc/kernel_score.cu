@@ -212,6 +212,27 @@ __device__ __forceinline__ bool warp_wait2(uint32_t bar1, uint32_t par1, uint32_
   return __all_sync(0xffffffffu, ok1 && ok2);
 }
 
+// The same for up to four phases (phase k only when needk).
+__device__ __forceinline__ bool warp_wait4(uint32_t b0, uint32_t p0, bool n0, uint32_t b1, uint32_t p1, bool n1,
+                                           uint32_t b2, uint32_t p2, bool n2, uint32_t b3, uint32_t p3, bool n3,
+                                           uint64_t limit_ns) {
+  bool ok0 = !n0 || mbar_try_wait(b0, p0);
+  bool ok1 = !n1 || mbar_try_wait(b1, p1);
+  bool ok2 = !n2 || mbar_try_wait(b2, p2);
+  bool ok3 = !n3 || mbar_try_wait(b3, p3);
+  if (!(ok0 && ok1 && ok2 && ok3)) {
+    const uint64_t t0 = global_ns();
+    while (!(ok0 && ok1 && ok2 && ok3)) {
+      if (!ok0) ok0 = mbar_try_wait(b0, p0);
+      if (!ok1) ok1 = mbar_try_wait(b1, p1);
+      if (!ok2) ok2 = mbar_try_wait(b2, p2);
+      if (!ok3) ok3 = mbar_try_wait(b3, p3);
+      if (!(ok0 && ok1 && ok2 && ok3) && global_ns() - t0 > limit_ns) break;
+    }
+  }
+  return __all_sync(0xffffffffu, ok0 && ok1 && ok2 && ok3);
+}
+
 template <int H, int QG, int EPI, class F>
 __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
                                   ScoreCfg<H, QG, EPI, F>::TMEM_COLS <= 256 && ScoreCfg<H, QG, EPI, F>::THREADS <= 256
@@ -573,8 +594,8 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
 //     (core-matrix order, one of two buffers) and stores their scales in tensor memory (one
 //     of two sets); per tile, once the tile has landed and the MMA that last read the scale
 //     set j % NSC has completed, the four warps store the tile's A scales there (each warp its
-//     own lane quadrant) and signal the set's "ready" mbarrier. The sets form a ring of their
-//     own, so the scale warps run ahead of the accumulators;
+//     own lane quadrant) and signal the set's "ready" mbarrier, two tiles per poll. The sets
+//     form a ring of their own, so the scale warps run ahead of the accumulators;
 //   * NMMA MMA warps, warp m taking tiles m, m + NMMA, ...: once the tile's scale set is
 //     ready and its accumulator (j % NACC) has been drained, one thread issues the two
 //     block-scaled MMAs and commits to the stage's mbarrier, which frees the stage for the
@@ -854,39 +875,57 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
           tmem_st_x1(tq + sfb + C::SB + jj, wd >> 16);
         }
       }
-      // ring positions kept as counters: tile j's stage st, its phase ph and scale set sc;
-      // tile j - NSC's stage pst and phase pph (the MMA that last read set sc)
-      int st = (int)(j % C::NSTAGE), sc = (int)(j % C::NSC);
-      uint32_t ph = (j / C::NSTAGE) & 1u;
-      const uint32_t prev0 = j + (uint32_t)(C::NSTAGE - C::NSC);   // tile j - NSC, one ring later
-      int pst = (int)(prev0 % C::NSTAGE);
-      uint32_t pph = ((prev0 / C::NSTAGE) & 1u) ^ 1u;
-      for (int i = 0; i < d.nt; ++i, ++j) {
+      // ring positions kept as counters: tile j's stage rs and scale set rsc; tile j - NSC's
+      // stage rp (the MMA that last read set rsc, one round of the stage ring earlier). Two
+      // tiles per poll: the warps pay one poll's latency (a wait on completed barriers still
+      // costs ~180 cycles) and one loop's bookkeeping for both
+      RingPos<C::NSTAGE> rs(j), rp(j + (uint32_t)(C::NSTAGE - C::NSC));
+      RingPos<C::NSC> rsc(j);
+      for (int i = 0; i < d.nt;) {
+        const bool two = i + 1 < d.nt;   // (warp-uniform)
+        RingPos<C::NSTAGE> rs1 = rs, rp1 = rp;
+        RingPos<C::NSC> rsc1 = rsc;
+        rs1.template advance<1>();
+        rp1.template advance<1>();
+        rsc1.template advance<1>();
         if (!failed) {   // after a failure no more waits; the next group start reports it
-          // the tile has landed, and the MMA that last read scale set sc has completed; each
-          // warp goes on by itself and arrives on the set's "ready" barrier
-          if (!warp_wait2(bar_full(st), ph, bar_free(pst), pph, j >= (uint32_t)C::NSC, wait_ns)) {
+          // the tiles have landed, and the MMAs that last read their scale sets have
+          // completed; each warp goes on by itself and arrives on the sets' "ready" barriers
+          if (!warp_wait4(bar_full(rs.slot), rs.phase, true, bar_free(rp.slot), rp.phase ^ 1u,
+                          j >= (uint32_t)C::NSC, bar_full(rs1.slot), rs1.phase, two, bar_free(rp1.slot),
+                          rp1.phase ^ 1u, two && j + 1 >= (uint32_t)C::NSC, wait_ns)) {
             failed = true;
           } else {
             tc_fence_after();
-            if constexpr (!F::kFp8) {   // the tile's A scales
-              const uint32_t w = *reinterpret_cast<const uint32_t*>(stg + st * F::kStage + page_scale_offset(key));
+            if constexpr (!F::kFp8) {   // the tiles' A scales
+              const uint32_t w = *reinterpret_cast<const uint32_t*>(stg + rs.slot * F::kStage + page_scale_offset(key));
               const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
-              tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * sc), lo, lo, lo, lo, hi, hi, hi, hi);
+              tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * rsc.slot), lo, lo, lo, lo, hi, hi, hi, hi);
+              if (two) {
+                const uint32_t w1 =
+                    *reinterpret_cast<const uint32_t*>(stg + rs1.slot * F::kStage + page_scale_offset(key));
+                const uint32_t lo1 = w1 & 0xFFFFu, hi1 = w1 >> 16;
+                tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * rsc1.slot), lo1, lo1, lo1, lo1, hi1, hi1, hi1, hi1);
+              }
             }
             tmem_wait_st();   // (also the group's B scales, for its first tile)
             tc_fence_before();
-            warp_arrive(bar_ready(sc));
+            warp_arrive(bar_ready(rsc.slot));
+            if (two) warp_arrive(bar_ready(rsc1.slot));
           }
         }
-        if (++st == C::NSTAGE) {
-          st = 0;
-          ph ^= 1u;
-        }
-        if (++sc == C::NSC) sc = 0;
-        if (++pst == C::NSTAGE) {
-          pst = 0;
-          pph ^= 1u;
+        if (two) {
+          i += 2;
+          j += 2;
+          rs.template advance<2>();
+          rp.template advance<2>();
+          rsc.template advance<2>();
+        } else {
+          i += 1;
+          j += 1;
+          rs = rs1;
+          rp = rp1;
+          rsc = rsc1;
         }
       }
     }
