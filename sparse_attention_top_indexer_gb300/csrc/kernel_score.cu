@@ -603,9 +603,8 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
 //     (NSTAGE > NACC). The two waits are polled together: a wait on a completed mbarrier still
 //     costs the poll's latency (~150 cycles when the warp branches on it);
 //   * EPI epilogue warpgroups, warpgroup g taking tiles g, g + EPI, ...: read the accumulator
-//     in 32-column pieces (each read in flight during the previous piece's arithmetic),
-//     release it, form sum_h w' * max(dot, 0) per row and store; after its last tile of a
-//     group every epilogue warp releases the query buffer of that group.
+//     in 32-column pieces, release it, form sum_h w' * max(dot, 0) per row and store; after
+//     its last tile of a group every epilogue warp releases the query buffer of that group.
 // Position of a tile in a ring of M slots: the slot (tile number mod M) and the parity of the
 // ring's round (tile number / M), advanced by a stride of at most M without dividing.
 template <int M>
@@ -1043,21 +1042,17 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
         for (int qi = 0; qi < QG; ++qi)
 #pragma unroll
           for (int p = 0; p < P; ++p) part[qi][p] = 0.f;
-        // 32-column pieces of the accumulator, each read issued before the previous piece's
-        // arithmetic so that the read's latency overlaps it; the accumulator is released once
-        // the last piece is in registers
+        // 32-column pieces of the accumulator, read one at a time (reading each piece ahead of
+        // the previous piece's arithmetic took more instructions and time); the accumulator is
+        // released once the last piece is in registers
         constexpr int NH = C::NCB;
         const uint32_t acc_addr = tq + (uint32_t)(c * C::NP);
-        uint32_t ra[32], rb[32];
-        tmem_ld32_issue(acc_addr, ra);
-        tmem_ld32_wait(ra);
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
-          uint32_t(&cur)[32] = (h & 1) ? rb : ra;
-          uint32_t(&nxt)[32] = (h & 1) ? ra : rb;
-          if (h + 1 < NH) {
-            tmem_ld32_issue(acc_addr + (uint32_t)(32 * (h + 1)), nxt);
-          } else {
+          uint32_t cur[32];
+          tmem_ld32_issue(acc_addr + (uint32_t)(32 * h), cur);
+          tmem_ld32_wait(cur);
+          if (h + 1 == NH) {
             tc_fence_before();
             warp_arrive(bar_empty(c));   // accumulator c may take tile jt + NACC
           }
@@ -1073,7 +1068,6 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
                     fmaxf(__uint_as_float(cur[u + 2]), 0.f), fmaxf(__uint_as_float(cur[u + 3]), 0.f));
             }
           }
-          if (h + 1 < NH) tmem_ld32_wait(nxt);
         }
         const int t = i * kTileKeys + et;
         if (t < d.Tb) {
