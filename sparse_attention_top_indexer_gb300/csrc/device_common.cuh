@@ -169,6 +169,30 @@ __device__ __forceinline__ uint32_t e2m1x2(float x0, float x1) {
   return r;
 }
 
+// Eight e2m1 codes in one word: byte k holds the codes of x[2k] (low nibble) and x[2k+1],
+// each converted as e2m1x2 does; the four bytes are packed by the conversion's register moves.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&x)[8]) {
+  uint32_t r;
+  asm("{ .reg .b8 t0, t1, t2, t3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 t3, %8, %7;\n\t"
+      "mov.b32 %0, {t0, t1, t2, t3}; }"
+      : "=r"(r)
+      : "f"(x[0]), "f"(x[1]), "f"(x[2]), "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7]));
+  return r;
+}
+
+// max |x[k]| over eight values with three-input maxima (finite inputs; -0 counts as +0).
+__device__ __forceinline__ float amax_abs8(const float (&x)[8]) {
+  float a, b, c;
+  asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(a) : "f"(x[0]), "f"(x[1]), "f"(x[2]));
+  asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(b) : "f"(x[3]), "f"(x[4]), "f"(x[5]));
+  asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(c) : "f"(x[6]), "f"(x[7]), "f"(a));
+  return fmaxf(b, c);
+}
+
 // ----------------------------------------------------------------------------- PTX: mbarrier / bulk copy
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -221,19 +245,21 @@ __device__ __forceinline__ uint32_t quant_q_slice(uint4 raw, int j, const float2
     const int e0 = j * 8 + 2 * k;   // even element; rstart is even so pairs never straddle
     if (e0 >= rstart) rope_pair_bf16(x[2 * k], x[2 * k + 1], c[k]);
   }
-  float am = 0.f;   // the largest |x| (bf16 values), as bf16 bits
-#pragma unroll
-  for (int k = 0; k < 8; ++k) am = fmaxf(am, fabsf(x[k]));
-  uint32_t amax = __float_as_uint(am) >> 16;
+  // the largest |x| (bf16 values), as bf16 bits
+  uint32_t amax = __float_as_uint(amax_abs8(x)) >> 16;
   amax = max(amax, __shfl_xor_sync(gmask, amax, 1));
   amax = max(amax, __shfl_xor_sync(gmask, amax, 2));
   const int ex = e8m0_exponent(amax);
   const float sc = pow2_neg(ex);
-  uint32_t word = 0;
+  float y[8];   // x * 2^-ex, exact (a power of two), two at a time
 #pragma unroll
-  for (int k = 0; k < 4; ++k) word |= e2m1x2(__fmul_rn(x[2 * k], sc), __fmul_rn(x[2 * k + 1], sc)) << (8 * k);
+  for (int k = 0; k < 4; ++k) {
+    const float2 r = __fmul2_rn(make_float2(x[2 * k], x[2 * k + 1]), make_float2(sc, sc));
+    y[2 * k] = r.x;
+    y[2 * k + 1] = r.y;
+  }
   *e = ex;
-  return word;
+  return e2m1x8(y);
 }
 
 // FP8 query slice: the same RoPE as quant_q_slice, then the row's 128-value amax over the

@@ -574,9 +574,14 @@ __global__ void __launch_bounds__(256) prep_q_bulk_kernel(PrepArgs a) {
     }
     return;
   }
-  const int g = tid >> 4, j = tid & 15;
-  const int lane = tid & 31;
-  const unsigned gmask = 0xFFFFu << (lane & 16);
+  // MXFP4 lanes: 8 per vector (4 vectors a warp), the 4 lanes of a 32-block adjacent; a warp
+  // takes one half of its vectors' slices (j < 8 or j >= 8), so that with the model's
+  // 64-element RoPE tail a warp either rotates all its slices or none (no divergent
+  // rotation). FP8 lanes: the 16 of a half-warp per vector (its scale spans the vector).
+  const int lane = tid & 31, warp = tid >> 5;
+  const int j = a.fp8 ? (tid & 15) : 8 * (warp & 1) + (lane & 7);
+  const int g = a.fp8 ? (tid >> 4) : 4 * (warp >> 1) + (lane >> 3);   // vector within each round of 16
+  const unsigned gmask = a.fp8 ? 0xFFFFu << (lane & 16) : 0xFFu << (lane & 24);
   // the batch's first query row and its index in its sequence (one division per CTA; the
   // batch's rows follow it, wrapping at S)
   const int qrow0 = (int)(v0 >> a.h_shift);   // H is a power of two
@@ -588,7 +593,7 @@ __global__ void __launch_bounds__(256) prep_q_bulk_kernel(PrepArgs a) {
 #pragma unroll
   for (int p = 0; p < NV / 16; ++p) {
     const int vi = 16 * p + g;
-    if (vi < nv) {   // the 16 lanes of a group agree
+    if (vi < nv) {   // the lanes of a vector agree
       const long long v = v0 + vi;
       const int qrow = (int)(v >> a.h_shift);
       const int srow_ = s0 + (qrow - qrow0);
