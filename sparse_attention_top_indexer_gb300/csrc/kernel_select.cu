@@ -75,39 +75,41 @@ __global__ void __launch_bounds__(NT, topk_min_ctas(NT, KPT)) topk_kernel(const 
   }
   __syncthreads();
 
-  const int base = tid * KPT;
+  // keys a thread holds: the row's visible positions spread over all threads, four at a time
+  // (a row that sees fewer than NT * KPT positions then takes fewer instructions per thread
+  // in every per-key loop, instead of leaving the threads past it idle)
+  const int kpt = min(KPT, max(4, (((vis + NT - 1) / NT) + 3) & ~3));
+  const int base = tid * kpt;
   const float* src = a.scores + (size_t)row * a.ld;
   auto make_key = [&](float f, int t) -> uint32_t { return t < vis && isfinite(f) ? order_key(f) : 0u; };
   uint32_t key[KPT];
 #pragma unroll
   for (int j = 0; j < KPT; ++j) key[j] = 0u;
   if (base < vis) {   // threads past the visible positions hold no key
-    if ((a.ld & 3) == 0) {   // rows start 16-byte aligned: float4 loads
-#pragma unroll
-      for (int j = 0; j < KPT; j += 4) {
-        if (base + j < vis) {
+    if ((a.ld & 3) == 0) {   // rows start 16-byte aligned (base is a multiple of 4): float4 loads
+      for_keys<KPT>(kpt, [&](int j) {
+        if ((j & 3) == 0 && base + j < vis) {
           const float4 v = *reinterpret_cast<const float4*>(src + base + j);
           key[j] = make_key(v.x, base + j);
           key[j + 1] = make_key(v.y, base + j + 1);
           key[j + 2] = make_key(v.z, base + j + 2);
           key[j + 3] = make_key(v.w, base + j + 3);
         }
-      }
+      });
     } else {
-#pragma unroll
-      for (int j = 0; j < KPT; ++j)
+      for_keys<KPT>(kpt, [&](int j) {
         if (base + j < vis) key[j] = make_key(src[base + j], base + j);
+      });
     }
     if (a.cand) {   // the candidate filter: positions outside the kept blocks hold no key
-#pragma unroll
-      for (int j = 0; j < KPT; ++j) {
+      for_keys<KPT>(kpt, [&](int j) {
         const int blk = (base + j) / a.cbs;   // < the row's blocks where key[j] != 0 (t < vis <= T)
         if (key[j] != 0u && !((kb.kept[blk >> 5] >> (blk & 31)) & 1u)) key[j] = 0u;
-      }
+      });
     }
   }
 
-  select_top<NT, KPT>(key, k_eff, out, a.topk, a.offset, sh, vis);
+  select_top<NT, KPT>(key, k_eff, out, a.topk, a.offset, sh, vis, kpt);
 }
 
 // Level two with one query row: the top-k over the kept candidate blocks only. The row's

@@ -2,8 +2,9 @@
 // the top-k kernels (all positions, the kept candidate positions, the fused candidate
 // blocks + top-k) and the candidate-block selection.
 //
-// Thread t holds the keys of positions [t*KPT, (t+1)*KPT); key 0 marks a position that
-// cannot be selected. The k_eff largest keys are kept, ties to the lower position, and
+// Thread t holds the keys of positions [t*kpt, (t+1)*kpt) (kpt <= KPT, chosen per row);
+// key 0 marks a position that cannot be selected. The k_eff largest keys are kept, ties to
+// the lower position, and
 // their positions (+offset) are written in ascending order, then -1 up to `width`.
 // Up to three most-significant-digit radix passes (11 + 11 + 10 bits, 2048-bin
 // shared-memory histograms) pin the k_eff-th largest key K*; a pass stops the search
@@ -150,6 +151,24 @@ __device__ __forceinline__ void cta_search(const uint32_t* h, uint32_t need, Sel
   }
 }
 
+// Calls fn(j) for the keys j < kpt of a thread, kpt a multiple of four (when KPT is): four at
+// a time, with a jump past the chunks at or beyond kpt (kpt is the same in all threads of the
+// CTA, so the jump is uniform and the skipped keys cost no issue slots).
+template <int KPT, class Fn>
+__device__ __forceinline__ void for_keys(int kpt, Fn&& fn) {
+  if constexpr (KPT % 4 != 0) {
+#pragma unroll
+    for (int j = 0; j < KPT; ++j) fn(j);
+  } else {
+#pragma unroll
+    for (int c = 0; c < KPT / 4; ++c) {
+      if (4 * c >= kpt) break;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) fn(4 * c + u);
+    }
+  }
+}
+
 // All NT threads must call it; it ends with every output written by its thread (no
 // trailing barrier). WARP_SEARCH: one warp searches the histograms (many rows per SM);
 // otherwise all threads do (one row per SM, where the search's latency counts). Only
@@ -159,13 +178,16 @@ __device__ __forceinline__ void cta_search(const uint32_t* h, uint32_t need, Sel
 // >= 0x00800000, so the first digit of a valid key is >= 4 and the first pass needs no
 // prefix test, and every later prefix is nonzero (a zero key never matches it); the
 // compaction builds a bit mask of the thread's selected keys and visits only those.
+// kpt: the keys a thread holds, positions [t*kpt, (t+1)*kpt) (a multiple of four, at most
+// KPT, the same in all threads; KPT itself when KPT is not a multiple of four); the keys
+// key[j] for j >= kpt are not read.
 template <int NT, int KPT, bool WARP_SEARCH = (NT <= 256)>
 __device__ void select_top(const uint32_t (&key)[KPT], int k_eff, int32_t* out, int width, int offset,
-                           SelectShared<NT>& sh, int span = NT * KPT) {
+                           SelectShared<NT>& sh, int span = NT * KPT, int kpt = KPT) {
   static_assert(NT % 32 == 0 && NT >= 32, "whole warps");
   static_assert(KPT <= 32, "one bit per key in a 32-bit mask");
   const int tid = threadIdx.x;
-  const int base = tid * KPT;
+  const int base = tid * kpt;
   const bool live = base < span;
   for (int i = tid; i < 2 * kHistBins; i += NT) (&sh.hist[0][0])[i] = 0u;
   __syncthreads();
@@ -182,9 +204,9 @@ __device__ void select_top(const uint32_t (&key)[KPT], int k_eff, int32_t* out, 
   uint32_t need = (uint32_t)k_eff, kstar = 0u;
   // pass 0: the top 11 bits
   if (live) {
-#pragma unroll
-    for (int j = 0; j < KPT; ++j)
+    for_keys<KPT>(kpt, [&](int j) {
       if (key[j] != 0u) atomicAdd(&sh.hist[0][key[j] >> 21], 1u);
+    });
   }
   __syncthreads();
   search(sh.hist[0], need);
@@ -204,9 +226,9 @@ __device__ void select_top(const uint32_t (&key)[KPT], int k_eff, int32_t* out, 
         __syncthreads();
       }
       if (live) {
-#pragma unroll
-        for (int j = 0; j < KPT; ++j)
+        for_keys<KPT>(kpt, [&](int j) {
           if ((key[j] & mask) == prefix) atomicAdd(&h[(key[j] >> shift) & dm], 1u);
+        });
       }
       __syncthreads();
       search(h, need);
@@ -226,11 +248,10 @@ __device__ void select_top(const uint32_t (&key)[KPT], int k_eff, int32_t* out, 
   // ordered compaction: the keys above kstar, then the first `need` equal to it
   uint32_t gtm = 0u, eqm = 0u;
   if (live) {
-#pragma unroll
-    for (int j = 0; j < KPT; ++j) {
+    for_keys<KPT>(kpt, [&](int j) {
       gtm |= (key[j] > kstar ? 1u : 0u) << j;
       if (need != 0u) eqm |= (key[j] == kstar ? 1u : 0u) << j;
-    }
+    });
   }
   const uint32_t packed = ((uint32_t)__popc(eqm) << 16) | (uint32_t)__popc(gtm);
   uint32_t total;
