@@ -586,22 +586,31 @@ __global__ void __launch_bounds__(256) prep_q_bulk_kernel(PrepArgs a) {
   // batch's rows follow it, wrapping at S)
   const int qrow0 = (int)(v0 >> a.h_shift);   // H is a power of two
   const int s0 = a.rows ? 0 : qrow0 % a.S;
-  // the slice's RoPE entries, reloaded only when the position changes (the vectors of a
-  // thread are heads of one query row whenever H >= 64)
+  // the slice's RoPE entries, reloaded only when the position changes; with H >= NV the
+  // CTA's vectors are all heads of row qrow0 (v0 is a multiple of NV and NV divides H), so
+  // the position and the slice are taken once, ahead of the loop
+  auto row_pos = [&](int qrow) {
+    const int srow_ = s0 + (qrow - qrow0);
+    return a.rows ? a.rows[qrow].pos : a.start_pos + (srow_ < a.S ? srow_ : srow_ % a.S);
+  };
+  const bool one_row = (1 << a.h_shift) >= NV;
   int cpos = -1;
   float2 c[4];
+  if (one_row) {
+    cpos = row_pos(qrow0);
+    load_rope_slice(reinterpret_cast<const float2*>(a.rope_cs) + (size_t)cpos * (a.rope_dim / 2), j, a.rope_dim, c);
+  }
 #pragma unroll
   for (int p = 0; p < NV / 16; ++p) {
     const int vi = 16 * p + g;
     if (vi < nv) {   // the lanes of a vector agree
-      const long long v = v0 + vi;
-      const int qrow = (int)(v >> a.h_shift);
-      const int srow_ = s0 + (qrow - qrow0);
-      const int pos = a.rows ? a.rows[qrow].pos : a.start_pos + (srow_ < a.S ? srow_ : srow_ % a.S);
-      if (pos != cpos) {
-        load_rope_slice(reinterpret_cast<const float2*>(a.rope_cs) + (size_t)pos * (a.rope_dim / 2), j, a.rope_dim,
-                        c);
-        cpos = pos;
+      if (!one_row) {
+        const int pos = row_pos((int)((v0 + vi) >> a.h_shift));
+        if (pos != cpos) {
+          load_rope_slice(reinterpret_cast<const float2*>(a.rope_cs) + (size_t)pos * (a.rope_dim / 2), j,
+                          a.rope_dim, c);
+          cpos = pos;
+        }
       }
       const uint4 raw = *reinterpret_cast<const uint4*>(sq + vi * kHeadDim + j * 8);
       int e;
