@@ -34,8 +34,8 @@ constexpr int kHistBins = 2048;
 // contention even when it does not (uniform scores in [1, 2), four bins: +8 % time).
 
 template <int NT>
-struct SelectShared {
-  uint32_t hist[2][kHistBins];
+struct alignas(16) SelectShared {
+  uint32_t hist[2][kHistBins];   // 16-byte aligned: the bin search reads four bins at a time
   uint32_t warp_tot[NT / 32];
   uint32_t bc[4];            // bin, count above the bin, count in the bin, count in all bins
 };
@@ -69,23 +69,27 @@ __device__ __forceinline__ uint32_t cta_scan(uint32_t v, uint32_t& total, Select
 // Warp 0 of the CTA: in histogram h (larger digit = larger keys) find the bin holding the
 // need-th largest key (need >= 1) and set bc = {bin, keys in the bins above it, keys in it,
 // keys in all bins}; with fewer than need keys in all, only bc[3]. Lane l sums the 64 bins
-// below 2047 - 64 l, visiting them in an order rotated by l so that the lanes read 32
-// different banks; a scan of those sums from the top picks the lane holding the key, and
-// the warp then scans that lane's 64 bins two per lane.
-// BATCH loads are in flight at a time (64: all of them, for builds whose registers are capped
-// anyway; 8 otherwise, since a full unroll takes ~80 more registers).
+// below 2047 - 64 l as 16 four-bin chunks (16-byte loads), visiting them in an order rotated
+// by l so that the eight lanes of each 128-byte phase read distinct banks; a scan of those
+// sums from the top picks the lane holding the key, and the warp then scans that lane's 64
+// bins two per lane. BATCH chunks are in flight at a time (four keep the register-capped
+// builds from spilling more).
 template <int BATCH>
 __device__ __forceinline__ void warp_search(const uint32_t* h, uint32_t need, uint32_t* bc) {
-  static_assert(BATCH % 8 == 0 && 64 % BATCH == 0, "whole batches of the eight partial sums");
+  static_assert(BATCH % 4 == 0 && 16 % BATCH == 0, "whole batches of the four partial sums");
   const int lane = threadIdx.x & 31;
   const int top = kHistBins - 1 - 64 * lane;
-  uint32_t part[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};   // eight independent sums: a short add chain
+  const uint4* hv = reinterpret_cast<const uint4*>(h + (top - 63));   // 16-byte aligned: top - 63 = 64 (31 - lane)
+  uint32_t part[4] = {0u, 0u, 0u, 0u};   // four independent sums: a short add chain
 #pragma unroll 1
-  for (int i0 = 0; i0 < 64; i0 += BATCH) {
+  for (int m0 = 0; m0 < 16; m0 += BATCH) {
 #pragma unroll
-    for (int i = 0; i < BATCH; ++i) part[i & 7] += h[top - ((i0 + i + lane) & 63)];
+    for (int m = 0; m < BATCH; ++m) {
+      const uint4 v = hv[(m0 + m + lane) & 15];
+      part[m & 3] += (v.x + v.y) + (v.z + v.w);
+    }
   }
-  const uint32_t own = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+  const uint32_t own = (part[0] + part[1]) + (part[2] + part[3]);
   uint32_t incl = own;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
@@ -194,7 +198,7 @@ __device__ void select_top(const uint32_t (&key)[KPT], int k_eff, int32_t* out, 
 
   auto search = [&](const uint32_t* h, uint32_t need) {
     if constexpr (WARP_SEARCH) {
-      if (tid < 32) warp_search<KPT >= 32 ? 64 : 8>(h, need, sh.bc);
+      if (tid < 32) warp_search<4>(h, need, sh.bc);
     } else {
       cta_search<NT>(h, need, sh);
     }
