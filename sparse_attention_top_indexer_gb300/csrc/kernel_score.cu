@@ -168,6 +168,12 @@ __device__ __forceinline__ void build_b_operand(const uint8_t* qstg, uint8_t* qB
   }
 }
 
+// {x0 + |x0|, x1 + |x1|} = 2 max(x, 0) of two values with one packed add (exact: x + x = 2x,
+// x + |x| = +0 for x <= 0).
+__device__ __forceinline__ float2 twice_relu2(float x0, float x1) {
+  return __fadd2_rn(make_float2(x0, x1), make_float2(fabsf(x0), fabsf(x1)));
+}
+
 // One tile's MMAs: MXFP4 -- two block-scaled MMAs of K = 64; FP8 -- four e4m3 MMAs of K = 32.
 template <class F, int NP>
 __device__ __forceinline__ void issue_tile_mma(uint32_t acc, uint32_t pa, uint32_t qb, uint32_t sfa, uint32_t sfb,
@@ -518,9 +524,10 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
       for (int n = 0; n < C::N; n += 4) {
         const float4 w4 = *reinterpret_cast<const float4*>(wq + n);
         const int qi = n / H, p0 = (n % P), p1 = ((n + 2) % P);
-        ffma2(part[qi][p0], part[qi][p0 + 1], w4.x, w4.y, fmaxf(v[n], 0.f), fmaxf(v[n + 1], 0.f));
-        ffma2(part[(n + 2) / H][p1], part[(n + 2) / H][p1 + 1], w4.z, w4.w, fmaxf(v[n + 2], 0.f),
-              fmaxf(v[n + 3], 0.f));
+        const float2 r01 = twice_relu2(v[n], v[n + 1]);   // 2 max(dot, 0), halved at the row's sum
+        const float2 r23 = twice_relu2(v[n + 2], v[n + 3]);
+        ffma2(part[qi][p0], part[qi][p0 + 1], w4.x, w4.y, r01.x, r01.y);
+        ffma2(part[(n + 2) / H][p1], part[(n + 2) / H][p1 + 1], w4.z, w4.w, r23.x, r23.y);
       }
       if (et == 0 && i + C::NSTAGE < nt) {
         // the MMA that read this page's stage has completed: refill it
@@ -541,6 +548,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
             float acc = part[qi][0];
 #pragma unroll
             for (int p = 1; p < P; ++p) acc += part[qi][p];
+            acc *= 0.5f;   // the partial sums hold twice the head sum
             const int vis = min(Tb, (pos0 + qi + 1) / a.ratio);
             bool keep = present && t < vis;
             if (a.cand) {
@@ -1062,10 +1070,12 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
             if (n < C::N) {
               const float4 w4 = *reinterpret_cast<const float4*>(wq + n);
               const int qi = n / H, p0 = (n % P), p1 = ((n + 2) % P);
-              ffma2(part[qi][p0], part[qi][p0 + 1], w4.x, w4.y, fmaxf(__uint_as_float(cur[u]), 0.f),
-                    fmaxf(__uint_as_float(cur[u + 1]), 0.f));
-              ffma2(part[(n + 2) / H][p1], part[(n + 2) / H][p1 + 1], w4.z, w4.w,
-                    fmaxf(__uint_as_float(cur[u + 2]), 0.f), fmaxf(__uint_as_float(cur[u + 3]), 0.f));
+              // 2 max(dot, 0) = dot + |dot| for two elements at once (the halving is applied to
+              // the row's sum: exact, a power of two)
+              const float2 r01 = twice_relu2(__uint_as_float(cur[u]), __uint_as_float(cur[u + 1]));
+              const float2 r23 = twice_relu2(__uint_as_float(cur[u + 2]), __uint_as_float(cur[u + 3]));
+              ffma2(part[qi][p0], part[qi][p0 + 1], w4.x, w4.y, r01.x, r01.y);
+              ffma2(part[(n + 2) / H][p1], part[(n + 2) / H][p1 + 1], w4.z, w4.w, r23.x, r23.y);
             }
           }
         }
@@ -1077,6 +1087,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
               float acc = part[qi][0];
 #pragma unroll
               for (int p = 1; p < P; ++p) acc += part[qi][p];
+              acc *= 0.5f;   // the partial sums hold twice the head sum
               if constexpr (F::kFp8) acc *= sk;
               a.scores[(size_t)(d.row0 + qi) * a.ld + t] = t < visq[qi] ? acc : -__int_as_float(0x7f800000);
             }
