@@ -76,6 +76,8 @@ __host__ __device__ constexpr int max_acc(int NP, int SB, int budget) {
 
 // FP8 accumulators: at most 4; N <= 64 keeps them within 256 columns (two CTAs per SM),
 // larger N takes the 512 columns of one CTA per SM (its epilogue reads 128 columns at once)
+constexpr int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
+
 __host__ __device__ constexpr int acc_f8(int NP) {
   return NP <= 64 ? (256 / NP < 4 ? 256 / NP : 4) : (512 / NP < 4 ? 512 / NP : 4);
 }
@@ -103,7 +105,13 @@ struct ScoreCfg {
   static constexpr int OFF_QSTG = OFF_STG + NSTAGE * F::kStage;             // raw query rows
   static constexpr int OFF_W = OFF_QSTG + round_up(N * F::kRow, 16);
   static constexpr int OFF_SFW = OFF_W + round_up(N * 4, 16);
-  static constexpr int NBAR = NSTAGE + 2 * NACC + 1;                          // full, done, empty, q
+  // barriers: full per stage; done per accumulator and epilogue warpgroup (the MMA of tile i
+  // commits to the barrier of the warpgroup that reads it, so each done barrier's phases are
+  // consumed in order by one warpgroup: with one per accumulator, a warpgroup taking every
+  // other tile would skip phases and a parity wait could pass on a phase two rounds old);
+  // empty per accumulator; the query rows
+  static constexpr int LDONE = NACC / gcd_int(NACC, EPI) * EPI;   // tiles per round of (accumulator, warpgroup) pairs
+  static constexpr int NBAR = NSTAGE + NACC * EPI + NACC + 1;
   static constexpr int OFF_BAR = round_up(OFF_SFW + NCB * 32 * 4, 8);
   static constexpr int OFF_INFO = OFF_BAR + NBAR * 8;                         // tmem base, counters
   static constexpr int OFF_PTAB = round_up(OFF_INFO + 16, 16);   // pool page of each half of this CTA's tiles
@@ -359,9 +367,10 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
   uint32_t* cand_bits = reinterpret_cast<uint32_t*>(smem + C::OFF_CAND);
   const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
   auto bar_full = [&](int st) { return bar0 + 8u * (uint32_t)st; };
-  auto bar_done = [&](int c) { return bar0 + 8u * (uint32_t)(C::NSTAGE + c); };
-  auto bar_empty = [&](int c) { return bar0 + 8u * (uint32_t)(C::NSTAGE + C::NACC + c); };
-  const uint32_t bar_q = bar0 + 8u * (uint32_t)(C::NSTAGE + 2 * C::NACC);
+  // tile i's accumulator i % NACC, read by epilogue warpgroup i % EPI
+  auto bar_done = [&](int i) { return bar0 + 8u * (uint32_t)(C::NSTAGE + (i % C::NACC) * EPI + i % EPI); };
+  auto bar_empty = [&](int c) { return bar0 + 8u * (uint32_t)(C::NSTAGE + C::NACC * EPI + c); };
+  const uint32_t bar_q = bar0 + 8u * (uint32_t)(C::NBAR - 1);
   const uint32_t stg0 = smem_u32(stg);
   // pool pages of tile i's halves into ptab (an entry outside the pool is reported and its
   // keys score -inf)
@@ -383,7 +392,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
   const int first = min(nt, C::NSTAGE);
   if (warp == 0) {
     if (lane < C::NBAR) {
-      const bool empty_bar = lane >= C::NSTAGE + C::NACC && lane < C::NSTAGE + 2 * C::NACC;
+      const bool empty_bar = lane >= C::NSTAGE + C::NACC * EPI && lane < C::NSTAGE + C::NACC * EPI + C::NACC;
       mbar_init(bar0 + 8u * (uint32_t)lane, empty_bar ? (uint32_t)kEpiThreads : 1u);
       fence_mbar_init();
     }
@@ -460,7 +469,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
         const uint32_t acc = tmem + (uint32_t)(c * C::NP);
         const uint32_t sfa = tmem + (uint32_t)(C::SFA_COL + 8 * c);
         issue_tile_mma<F, C::NP>(acc, pa, qb, sfa, tmem + C::SFB_COL, C::SB);
-        tc_commit(bar_done(c));
+        tc_commit(bar_done(i));
         info[2] = (uint32_t)(i + 1);
       }
       __syncwarp();
@@ -495,7 +504,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
     if (a.fill_masked) fill_masked(ge, EPI * kEpiThreads);
     for (int i = grp; i < nt && !failed; i += EPI) {   // this group's pages
       const int c = i % C::NACC;
-      bool ok = warp_wait(bar_done(c), (uint32_t)(i / C::NACC) & 1u);
+      bool ok = warp_wait(bar_done(i), (uint32_t)(i / C::LDONE) & 1u);
       float sk = 1.f;   // FP8: this key's scale, read before the stage is refilled
       if constexpr (F::kFp8) {
         if (ok) sk = *reinterpret_cast<const float*>(stg + (i % C::NSTAGE) * F::kStage + page_scale_offset_fp8(et));
@@ -576,7 +585,7 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
         const int last = st + ((issued - 1 - st) / C::NSTAGE) * C::NSTAGE;   // last page loaded into st
         mbar_wait(bar_full(st), (uint32_t)(last / C::NSTAGE) & 1u);
       }
-      if (mmas > 0) mbar_wait(bar_done((mmas - 1) % C::NACC), (uint32_t)((mmas - 1) / C::NACC) & 1u);
+      if (mmas > 0) mbar_wait(bar_done(mmas - 1), (uint32_t)((mmas - 1) / C::LDONE) & 1u);
     }
     __syncthreads();
   }
@@ -665,9 +674,15 @@ struct RowsCfg {
   static constexpr int OFF_WS = OFF_W + 2 * W_STRIDE;                    // FP8: w' times the row's scale
   static constexpr int OFF_SFW = OFF_WS + (F::kFp8 ? 2 * W_STRIDE : 0);
   static constexpr int OFF_GD = round_up(OFF_SFW + NCB * 32 * 4, 16);   // two group descriptors
-  // barriers: full and free per stage, empty per accumulator, qfull and qfree per query
-  // buffer, ready per scale set; FP8: scales read (per stage), scaled w' ready
-  static constexpr int B_FULL = 0, B_FREE = NSTAGE, B_EMPTY = 2 * NSTAGE, B_QFULL = B_EMPTY + NACC;
+  // barriers: full and free per stage, empty per accumulator and MMA warp, qfull and qfree per
+  // query buffer, ready per scale set; FP8: scales read (per stage), scaled w' ready.
+  // Accumulator c's release after tile j goes to the barrier of the MMA warp that issues tile
+  // j + NACC, so each empty barrier's phases are consumed in order by one MMA warp: with one
+  // barrier per accumulator, an MMA warp that takes every other tile skips every other phase
+  // and a parity wait could pass on a phase two rounds old (the epilogue then still reading
+  // the accumulator), which large groups of slow epilogues (16 query rows a tile) hit
+  static constexpr int NEMPTY = NACC * NMMA;
+  static constexpr int B_FULL = 0, B_FREE = NSTAGE, B_EMPTY = 2 * NSTAGE, B_QFULL = B_EMPTY + NEMPTY;
   static constexpr int B_QFREE = B_QFULL + 2, B_READY = B_QFREE + 2, B_SREAD = B_READY + NSC;
   static constexpr int B_WS = B_SREAD + (F::kFp8 ? NSTAGE : 0);
   static constexpr int NBAR = B_WS + (F::kFp8 ? 2 : 0);
@@ -707,7 +722,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
   const uint32_t bar0 = smem_u32(smem + C::OFF_BAR);
   auto bar_full = [&](int st) { return bar0 + 8u * (uint32_t)(C::B_FULL + st); };
   auto bar_free = [&](int st) { return bar0 + 8u * (uint32_t)(C::B_FREE + st); };
-  auto bar_empty = [&](int c) { return bar0 + 8u * (uint32_t)(C::B_EMPTY + c); };
+  auto bar_empty = [&](int c, int m) { return bar0 + 8u * (uint32_t)(C::B_EMPTY + c * NMMA + m); };
   auto bar_qfull = [&](int q) { return bar0 + 8u * (uint32_t)(C::B_QFULL + q); };
   auto bar_qfree = [&](int q) { return bar0 + 8u * (uint32_t)(C::B_QFREE + q); };
   auto bar_ready = [&](int sc) { return bar0 + 8u * (uint32_t)(C::B_READY + sc); };
@@ -715,7 +730,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
   auto bar_wsready = [&](int q) { return bar0 + 8u * (uint32_t)(C::B_WS + q); };
   if (warp == 0) {
     for (int i = lane; i < C::NBAR; i += 32) {
-      const bool empty_bar = i >= C::B_EMPTY && i < C::B_EMPTY + C::NACC;
+      const bool empty_bar = i >= C::B_EMPTY && i < C::B_EMPTY + C::NEMPTY;
       const bool qfree_bar = i >= C::B_QFREE && i < C::B_QFREE + 2;
       const bool ready_bar = i >= C::B_READY && i < C::B_READY + C::NSC;
       const bool sread_bar = F::kFp8 && i >= C::B_SREAD && i < C::B_SREAD + C::NSTAGE;
@@ -945,6 +960,7 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
     RingPos<C::NSTAGE> rst(jt);
     RingPos<C::NACC> rc(jt);
     RingPos<C::NSC> rsc(jt);
+    uint32_t eph = 0u;   // bit c: parity of this warp's next wait on accumulator c's barrier
     for (int k = 0; !failed; ++k) {
       const int qb = k & 1;
       if (!warp_wait(bar_qfull(qb), (uint32_t)(k >> 1) & 1u, wait_ns)) {
@@ -963,12 +979,15 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
         // the tile's scale set is ready (the scale warps arrive only after they have seen the
         // tile's copy land, so the tile is in place too) and accumulator c has been drained by
         // the epilogue of tile jt - NACC (the accumulator's previous round)
-        const bool ok = warp_wait2(bar_ready(sc), rsc.phase, bar_empty(c), rc.phase ^ 1u, jt >= (uint32_t)C::NACC,
-                                   wait_ns);
+        // (this warp's barrier for accumulator c: its phases are the releases of the tiles
+        // before this warp's tiles on c, in order; bit c of eph is the next one's parity)
+        const bool reuse = jt >= (uint32_t)C::NACC;
+        const bool ok = warp_wait2(bar_ready(sc), rsc.phase, bar_empty(c, mid), (eph >> c) & 1u, reuse, wait_ns);
         if (!ok) {
           failed = true;
           break;
         }
+        if (reuse) eph ^= 1u << c;
         if (lane == 0) {
           tc_fence_after();
           const uint32_t pa = stg0 + (uint32_t)(st * F::kStage);
@@ -1062,7 +1081,8 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
           tmem_ld32_wait(cur);
           if (h + 1 == NH) {
             tc_fence_before();
-            warp_arrive(bar_empty(c));   // accumulator c may take tile jt + NACC
+            // accumulator c may take tile jt + NACC (issued by MMA warp (jt + NACC) % NMMA)
+            warp_arrive(bar_empty(c, (int)((jt + (uint32_t)C::NACC) % (uint32_t)NMMA)));
           }
 #pragma unroll
           for (int u = 0; u < 32; u += 4) {

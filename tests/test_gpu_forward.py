@@ -119,12 +119,18 @@ def _sample_rows(wl: Workload, n_rand: int, seed: int):
     return rows
 
 
-# prefill_t4096: 16384 rows over 4096 keys, the many-rows top-k with 16 keys per thread
+# prefill_t4096: 16384 rows over 4096 keys, the many-rows top-k with 16 keys per thread.
+# h8_t8192 / h32_t6144: 16 and 4 query rows per score tile over long rows (groups of up to
+# 64 tiles): slow epilogues that let an MMA warp run rounds ahead of an accumulator's
+# releases (each accumulator's release barrier is per MMA warp, so no parity wait is ambiguous)
 _SAMPLED = {"prefill": WORKLOADS["prefill"], "large_prefill": WORKLOADS["large_prefill"],
-            "prefill_t4096": dataclasses.replace(WORKLOADS["prefill"], name="prefill_t4096", S=16384, topk=1024)}
+            "prefill_t4096": dataclasses.replace(WORKLOADS["prefill"], name="prefill_t4096", S=16384, topk=1024),
+            "h8_t8192": dataclasses.replace(WORKLOADS["large_prefill"], name="h8_t8192", B=1, H=8),
+            "h32_t6144": dataclasses.replace(WORKLOADS["large_prefill"], name="h32_t6144", B=1, S=24576, H=32)}
 
 
-@pytest.mark.parametrize("name,n_rand", [("prefill", 40), ("large_prefill", 24), ("prefill_t4096", 24)])
+@pytest.mark.parametrize("name,n_rand", [("prefill", 40), ("large_prefill", 24), ("prefill_t4096", 24),
+                                         ("h8_t8192", 16), ("h32_t6144", 16)])
 def test_forward_prefill_sampled(X, name, n_rand):
     wl = _SAMPLED[name]
     table = C.gpu_table(wl.max_pos)
