@@ -1244,10 +1244,11 @@ cudaError_t launch_rows(ScoreArgs a, cudaStream_t stream) {
                            a);
 }
 
-// The several-row kernel's epilogue warpgroups and MMA warps. The model's 64 heads (two query
-// rows per group) take a third epilogue warpgroup: 2048-key prefill scores 92.5 against
-// 96.7 us, 8192-key rows 2.293 against 2.493 ms.
-constexpr int kRowsEpi = 2, kRowsEpi64 = 3, kRowsMma = 2;
+// The several-row kernel's epilogue warpgroups and MMA warps: three epilogue warpgroups for
+// every head count (64 heads: 2048-key prefill scores 85.6 against 93.9 us with two, 8192-key
+// rows 2.058 against 2.392 ms; 8, 32 and 128 heads over 8192-key rows 10-14 % faster than
+// with two), two MMA warps (a third: 2.069 ms).
+constexpr int kRowsEpi = 3, kRowsMma = 2;
 
 template <class F>
 cudaError_t launch_scores_fmt(const ScoreArgs& a, cudaStream_t stream) {
@@ -1261,7 +1262,7 @@ cudaError_t launch_scores_fmt(const ScoreArgs& a, cudaStream_t stream) {
       case 8: return launch_rows<8, 16, kRowsEpi, kRowsMma, F>(a, stream);
       case 16: return launch_rows<16, 8, kRowsEpi, kRowsMma, F>(a, stream);
       case 32: return launch_rows<32, 4, kRowsEpi, kRowsMma, F>(a, stream);
-      case 64: return launch_rows<64, 2, kRowsEpi64, kRowsMma, F>(a, stream);
+      case 64: return launch_rows<64, 2, kRowsEpi, kRowsMma, F>(a, stream);
       case 128: return launch_rows<128, 1, kRowsEpi, kRowsMma, F>(a, stream);
       default: return cudaErrorInvalidValue;
     }
