@@ -385,50 +385,123 @@ __global__ void __launch_bounds__(kHeadDim) publish_multi_kernel(PublishArgs a, 
     if (e < a.Din) lat[kk][e] = bf16_to_f32(key_latent(a, key0 + kk)[e]);
   }
   __syncthreads();
-  for (int kk = 0; kk < nk; ++kk) {
-    long long slot;
-    int pos;
-    if (!key_target(a, key0 + kk, true, slot, pos)) continue;   // the same for every thread
-    uint32_t knorm_bits = 0;
-    float2 cs = make_float2(1.f, 0.f);
-    key_tail_inputs(a, pos, tid, knorm_bits, cs);
-    // k_pre[tid] = sum_e wk[tid][e] * latent[e]: four TwoSum-carried partial sums over the
-    // element pairs of each 8-element chunk, combined in order (linear_out<1, 128>'s order)
-    float sacc[4], cacc[4];
+  if constexpr (kKeysPerCta == 2) {
+    // two keys at a time: their dot products interleaved (eight independent TwoSum chains in
+    // flight instead of four, each key's own arithmetic and order unchanged), then each key's
+    // norm, rotation and quantiser in turn. This pays for CTAs of two keys (2048 keys: 25.3 ->
+    // 23.3 us) but not for CTAs of four or eight (16384 keys: 123 -> 136-147 us), which keep
+    // one key at a time
+    constexpr int NQ = 2;
+    for (int kk = 0; kk < nk; kk += NQ) {
+      const int nq = min(NQ, nk - kk);
+      long long slot[NQ];
+      int pos[NQ];
+      bool live[NQ];   // the same in every thread
 #pragma unroll
-    for (int k = 0; k < 4; ++k) sacc[k] = cacc[k] = 0.f;
+      for (int q = 0; q < NQ; ++q) live[q] = q < nq && key_target(a, key0 + kk + q, true, slot[q], pos[q]);
+      // the norm weight and rotation entries, loaded ahead of the dot products
+      uint32_t knorm_bits[NQ];
+      float2 cs[NQ];
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {
-      if (8 * u < a.Din) {
-        const uint32_t ww[4] = {w8[u].x, w8[u].y, w8[u].z, w8[u].w};
+      for (int q = 0; q < NQ; ++q) {
+        knorm_bits[q] = 0u;
+        cs[q] = make_float2(1.f, 0.f);
+        if (live[q]) key_tail_inputs(a, pos[q], tid, knorm_bits[q], cs[q]);
+      }
+      // k_pre[tid] = sum_e wk[tid][e] * latent[e]: four TwoSum-carried partial sums per key over
+      // the element pairs of each 8-element chunk, combined in order (linear_out<1, 128>'s order)
+      float sacc[NQ][4], cacc[NQ][4];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float p0 = __fmul_rn(bf16_to_f32(ww[k] & 0xFFFFu), lat[kk][8 * u + 2 * k]);
-          const float p1 = __fmul_rn(bf16_to_f32(ww[k] >> 16), lat[kk][8 * u + 2 * k + 1]);
-          float t, e;
-          two_sum(sacc[k], p0, t, e);
-          sacc[k] = t;
-          cacc[k] = __fadd_rn(cacc[k], e);
-          two_sum(sacc[k], p1, t, e);
-          sacc[k] = t;
-          cacc[k] = __fadd_rn(cacc[k], e);
+      for (int q = 0; q < NQ; ++q)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sacc[q][k] = cacc[q][k] = 0.f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        if (8 * u < a.Din) {
+          const uint32_t ww[4] = {w8[u].x, w8[u].y, w8[u].z, w8[u].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float w0 = bf16_to_f32(ww[k] & 0xFFFFu), w1 = bf16_to_f32(ww[k] >> 16);
+#pragma unroll
+            for (int q = 0; q < NQ; ++q) {
+              const float p0 = __fmul_rn(w0, lat[kk + q][8 * u + 2 * k]);   // kk + q < KPC (KPC a multiple of NQ)
+              const float p1 = __fmul_rn(w1, lat[kk + q][8 * u + 2 * k + 1]);
+              float t, e;
+              two_sum(sacc[q][k], p0, t, e);
+              sacc[q][k] = t;
+              cacc[q][k] = __fadd_rn(cacc[q][k], e);
+              two_sum(sacc[q][k], p1, t, e);
+              sacc[q][k] = t;
+              cacc[q][k] = __fadd_rn(cacc[q][k], e);
+            }
+          }
         }
       }
-    }
-    float hi = sacc[0], lo = cacc[0];
 #pragma unroll
-    for (int k = 1; k < 4; ++k) {
-      float t, e;
-      two_sum(hi, sacc[k], t, e);
-      hi = t;
-      lo = __fadd_rn(__fadd_rn(lo, cacc[k]), e);
+      for (int q = 0; q < NQ; ++q) {
+        if (!live[q]) continue;
+        float hi = sacc[q][0], lo = cacc[q][0];
+#pragma unroll
+        for (int k = 1; k < 4; ++k) {
+          float t, e;
+          two_sum(hi, sacc[q][k], t, e);
+          hi = t;
+          lo = __fadd_rn(__fadd_rn(lo, cacc[q][k]), e);
+        }
+        float t, e;
+        two_sum(hi, lo, t, e);
+        __syncthreads();   // the previous key's outputs have been read
+        kx[tid] = bf16_to_f32(f32pair_to_bf16_rne(t, e));
+        __syncthreads();
+        finish_key(a, slot[q], kx, knorm_bits[q], cs[q]);
+      }
     }
-    float t, e;
-    two_sum(hi, lo, t, e);
-    __syncthreads();   // the previous key's outputs have been read
-    kx[tid] = bf16_to_f32(f32pair_to_bf16_rne(t, e));
-    __syncthreads();
-    finish_key(a, slot, kx, knorm_bits, cs);
+  } else {
+    for (int kk = 0; kk < nk; ++kk) {
+      long long slot;
+      int pos;
+      if (!key_target(a, key0 + kk, true, slot, pos)) continue;   // the same for every thread
+      uint32_t knorm_bits = 0;
+      float2 cs = make_float2(1.f, 0.f);
+      key_tail_inputs(a, pos, tid, knorm_bits, cs);
+      // k_pre[tid] = sum_e wk[tid][e] * latent[e]: four TwoSum-carried partial sums over the
+      // element pairs of each 8-element chunk, combined in order (linear_out<1, 128>'s order)
+      float sacc[4], cacc[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sacc[k] = cacc[k] = 0.f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        if (8 * u < a.Din) {
+          const uint32_t ww[4] = {w8[u].x, w8[u].y, w8[u].z, w8[u].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float p0 = __fmul_rn(bf16_to_f32(ww[k] & 0xFFFFu), lat[kk][8 * u + 2 * k]);
+            const float p1 = __fmul_rn(bf16_to_f32(ww[k] >> 16), lat[kk][8 * u + 2 * k + 1]);
+            float t, e;
+            two_sum(sacc[k], p0, t, e);
+            sacc[k] = t;
+            cacc[k] = __fadd_rn(cacc[k], e);
+            two_sum(sacc[k], p1, t, e);
+            sacc[k] = t;
+            cacc[k] = __fadd_rn(cacc[k], e);
+          }
+        }
+      }
+      float hi = sacc[0], lo = cacc[0];
+#pragma unroll
+      for (int k = 1; k < 4; ++k) {
+        float t, e;
+        two_sum(hi, sacc[k], t, e);
+        hi = t;
+        lo = __fadd_rn(__fadd_rn(lo, cacc[k]), e);
+      }
+      float t, e;
+      two_sum(hi, lo, t, e);
+      __syncthreads();   // the previous key's outputs have been read
+      kx[tid] = bf16_to_f32(f32pair_to_bf16_rne(t, e));
+      __syncthreads();
+      finish_key(a, slot, kx, knorm_bits, cs);
+    }
   }
 }
 

@@ -193,7 +193,7 @@ __device__ void select_top(const uint32_t (&key)[KPT], int k_eff, int32_t* out, 
   const int tid = threadIdx.x;
   const int base = tid * kpt;
   const bool live = base < span;
-  for (int i = tid; i < 2 * kHistBins; i += NT) (&sh.hist[0][0])[i] = 0u;
+  for (int i = tid; i < 2 * kHistBins / 4; i += NT) reinterpret_cast<uint4*>(&sh.hist[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
   __syncthreads();
 
   auto search = [&](const uint32_t* h, uint32_t need) {
@@ -226,7 +226,7 @@ __device__ void select_top(const uint32_t (&key)[KPT], int k_eff, int32_t* out, 
       const uint32_t dm = p == 1 ? 0x7FFu : 0x3FFu;
       uint32_t* h = sh.hist[p & 1];
       if (p == 2) {   // pass 0's histogram, read by its search before the last barrier
-        for (int i = tid; i < kHistBins; i += NT) h[i] = 0u;
+        for (int i = tid; i < kHistBins / 4; i += NT) reinterpret_cast<uint4*>(h)[i] = make_uint4(0u, 0u, 0u, 0u);
         __syncthreads();
       }
       if (live) {
