@@ -226,27 +226,6 @@ __device__ __forceinline__ bool warp_wait2(uint32_t bar1, uint32_t par1, uint32_
   return __all_sync(0xffffffffu, ok1 && ok2);
 }
 
-// The same for up to four phases (phase k only when needk).
-__device__ __forceinline__ bool warp_wait4(uint32_t b0, uint32_t p0, bool n0, uint32_t b1, uint32_t p1, bool n1,
-                                           uint32_t b2, uint32_t p2, bool n2, uint32_t b3, uint32_t p3, bool n3,
-                                           uint64_t limit_ns) {
-  bool ok0 = !n0 || mbar_try_wait(b0, p0);
-  bool ok1 = !n1 || mbar_try_wait(b1, p1);
-  bool ok2 = !n2 || mbar_try_wait(b2, p2);
-  bool ok3 = !n3 || mbar_try_wait(b3, p3);
-  if (!(ok0 && ok1 && ok2 && ok3)) {
-    const uint64_t t0 = global_ns();
-    while (!(ok0 && ok1 && ok2 && ok3)) {
-      if (!ok0) ok0 = mbar_try_wait(b0, p0);
-      if (!ok1) ok1 = mbar_try_wait(b1, p1);
-      if (!ok2) ok2 = mbar_try_wait(b2, p2);
-      if (!ok3) ok3 = mbar_try_wait(b3, p3);
-      if (!(ok0 && ok1 && ok2 && ok3) && global_ns() - t0 > limit_ns) break;
-    }
-  }
-  return __all_sync(0xffffffffu, ok0 && ok1 && ok2 && ok3);
-}
-
 template <int H, int QG, int EPI, class F>
 __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
                                   ScoreCfg<H, QG, EPI, F>::TMEM_COLS <= 256 && ScoreCfg<H, QG, EPI, F>::THREADS <= 256
@@ -609,10 +588,10 @@ __global__ void __launch_bounds__(ScoreCfg<H, QG, EPI, F>::THREADS,
 //     polls that stage's barrier (the MMA that last read it has completed) and issues its copy;
 //   * scale warpgroup (warps 0-3): per group, rewrites the query rows into the B operand
 //     (core-matrix order, one of two buffers) and stores their scales in tensor memory (one
-//     of two sets); per tile, once the tile has landed and the MMA that last read the scale
-//     set j % NSC has completed, the four warps store the tile's A scales there (each warp its
-//     own lane quadrant) and signal the set's "ready" mbarrier, two tiles per poll. The sets
-//     form a ring of their own, so the scale warps run ahead of the accumulators;
+//     of two sets); per tile, once the tile has landed, the four warps store the tile's A
+//     scales into the scale set of its stage (each warp its own lane quadrant; the MMA that last
+//     read the set completed before the stage was refilled) and signal the set's "ready"
+//     mbarrier, two tiles per poll, so the scale warps run ahead of the accumulators;
 //   * NMMA MMA warps, warp m taking tiles m, m + NMMA, ...: once the tile's scale set is
 //     ready and its accumulator (j % NACC) has been drained, one thread issues the two
 //     block-scaled MMAs and commits to the stage's mbarrier, which frees the stage for the
@@ -652,10 +631,11 @@ struct RowsCfg {
   static constexpr int SB = round_up(NCB, 4);
   static constexpr int NSTAGE = F::kFp8 ? 8 : 12;
   static constexpr int PBATCH = 4;   // tiles the producer requests per poll of the stage barriers
-  // NSC key-scale sets (8 columns each) in a ring of their own: a tile's A scales go into set
-  // j % NSC once the MMA that last read the set has completed, so the scale warps run ahead of
-  // the accumulators (NSC < NSTAGE keeps the stage barriers unambiguous for that wait)
-  static constexpr int NSC = 6;
+  // NSC key-scale sets (8 columns each), one per stage: tile j's A scales go into set
+  // j % NSTAGE, last read by the MMA of tile j - NSTAGE, which had completed before the
+  // producer refilled the stage with tile j; so once tile j has landed its set is free, and
+  // the scale warps wait on the tile's barrier alone
+  static constexpr int NSC = NSTAGE;
   // NACC accumulators (MXFP4: then the NSC A scale sets and two B scale sets, one per query
   // buffer; FP8: no scale sets)
   static constexpr int NACC = F::kFp8 ? (512 / NP < 4 ? 512 / NP : 4)
@@ -696,7 +676,7 @@ struct RowsCfg {
   static_assert(NBAR <= 64, "barriers are initialised by the lanes of two passes of one warp");
   static_assert(QFREE_COUNT < (1 << 20), "mbarrier arrival count");
   static_assert(NSTAGE > NACC, "the epilogue waits on a stage's barrier for its accumulator");
-  static_assert(NSTAGE > NSC, "the scale warps wait on a stage's barrier for a scale set");
+  static_assert(NSC == NSTAGE, "a tile's scale set is freed by the refill of its stage");
   static_assert(PBATCH <= 32 && PBATCH < NSTAGE, "a batch of stages, one lane each");
   static_assert(OFF_GD + 64 + NBAR * 8 + 16 + 1024 <= 227 * 1024, "shared memory budget");
 };
@@ -897,57 +877,46 @@ __global__ void __launch_bounds__(RowsCfg<H, QG, EPI, NMMA, F>::THREADS, 1) scor
           tmem_st_x1(tq + sfb + C::SB + jj, wd >> 16);
         }
       }
-      // ring positions kept as counters: tile j's stage rs and scale set rsc; tile j - NSC's
-      // stage rp (the MMA that last read set rsc, one round of the stage ring earlier). Two
-      // tiles per poll: the warps pay one poll's latency (a wait on completed barriers still
-      // costs ~180 cycles) and one loop's bookkeeping for both
-      RingPos<C::NSTAGE> rs(j), rp(j + (uint32_t)(C::NSTAGE - C::NSC));
-      RingPos<C::NSC> rsc(j);
+      // tile j's stage and scale set, kept as a counter (one set per stage). Two tiles per
+      // poll: the warps pay one poll's latency (a wait on completed barriers still costs ~180
+      // cycles) and one loop's bookkeeping for both
+      RingPos<C::NSTAGE> rs(j);
       for (int i = 0; i < d.nt;) {
         const bool two = i + 1 < d.nt;   // (warp-uniform)
-        RingPos<C::NSTAGE> rs1 = rs, rp1 = rp;
-        RingPos<C::NSC> rsc1 = rsc;
+        RingPos<C::NSTAGE> rs1 = rs;
         rs1.template advance<1>();
-        rp1.template advance<1>();
-        rsc1.template advance<1>();
         if (!failed) {   // after a failure no more waits; the next group start reports it
-          // the tiles have landed, and the MMAs that last read their scale sets have
-          // completed; each warp goes on by itself and arrives on the sets' "ready" barriers
-          if (!warp_wait4(bar_full(rs.slot), rs.phase, true, bar_free(rp.slot), rp.phase ^ 1u,
-                          j >= (uint32_t)C::NSC, bar_full(rs1.slot), rs1.phase, two, bar_free(rp1.slot),
-                          rp1.phase ^ 1u, two && j + 1 >= (uint32_t)C::NSC, wait_ns)) {
+          // the tiles have landed, so their scale sets are free; each warp goes on by itself
+          // and arrives on the sets' "ready" barriers
+          if (!warp_wait2(bar_full(rs.slot), rs.phase, bar_full(rs1.slot), rs1.phase, two, wait_ns)) {
             failed = true;
           } else {
             tc_fence_after();
             if constexpr (!F::kFp8) {   // the tiles' A scales
               const uint32_t w = *reinterpret_cast<const uint32_t*>(stg + rs.slot * F::kStage + page_scale_offset(key));
               const uint32_t lo = w & 0xFFFFu, hi = w >> 16;
-              tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * rsc.slot), lo, lo, lo, lo, hi, hi, hi, hi);
+              tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * rs.slot), lo, lo, lo, lo, hi, hi, hi, hi);
               if (two) {
                 const uint32_t w1 =
                     *reinterpret_cast<const uint32_t*>(stg + rs1.slot * F::kStage + page_scale_offset(key));
                 const uint32_t lo1 = w1 & 0xFFFFu, hi1 = w1 >> 16;
-                tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * rsc1.slot), lo1, lo1, lo1, lo1, hi1, hi1, hi1, hi1);
+                tmem_st_x8(tq + (uint32_t)(C::SFA_COL + 8 * rs1.slot), lo1, lo1, lo1, lo1, hi1, hi1, hi1, hi1);
               }
             }
             tmem_wait_st();   // (also the group's B scales, for its first tile)
             tc_fence_before();
-            warp_arrive(bar_ready(rsc.slot));
-            if (two) warp_arrive(bar_ready(rsc1.slot));
+            warp_arrive(bar_ready(rs.slot));
+            if (two) warp_arrive(bar_ready(rs1.slot));
           }
         }
         if (two) {
           i += 2;
           j += 2;
           rs.template advance<2>();
-          rp.template advance<2>();
-          rsc.template advance<2>();
         } else {
           i += 1;
           j += 1;
           rs = rs1;
-          rp = rp1;
-          rsc = rsc1;
         }
       }
     }
