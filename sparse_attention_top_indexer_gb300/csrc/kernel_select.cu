@@ -43,10 +43,12 @@ struct TopkKept {
 // short-context fill [0 .. vis).
 
 // Many rows per SM: the 256-thread builds are register-capped so that more rows share an SM
-// and hide more of each row's latency chain: 32 keys a thread at 64 registers (four CTAs;
-// large prefill 0.92 against 1.06 ms with three), 8 keys at 40 (six CTAs; the 2048-key
-// prefill 41.0 against 44.7 us with five).
-constexpr int topk_min_ctas(int NT, int KPT) { return NT != 256 ? 1 : KPT == 32 ? 4 : KPT == 8 ? 6 : 1; }
+// and hide more of each row's latency chain. 32 keys a thread at 40 registers (six CTAs; the
+// large prefill 0.621 ms against 0.679 with four CTAs at 64 registers and 0.627 with five at
+// 48, although the cap spills some keys to local memory, which stays in L1; eight CTAs at 32
+// registers spill more and take 0.755 ms); 8 keys at 32 registers (eight CTAs, no spills;
+// the 2048-key prefill 30.5 against 33.2 us with six).
+constexpr int topk_min_ctas(int NT, int KPT) { return NT != 256 ? 1 : KPT == 32 ? 6 : KPT == 8 ? 8 : 1; }
 
 template <int NT, int KPT>
 __global__ void __launch_bounds__(NT, topk_min_ctas(NT, KPT)) topk_kernel(const TopkArgs a) {
