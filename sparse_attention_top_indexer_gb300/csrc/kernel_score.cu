@@ -1209,8 +1209,11 @@ cudaError_t launch_rows(ScoreArgs a, cudaStream_t stream) {
   const long long groups = a.groups ? (long long)a.n_groups : (long long)((a.S + QG - 1) / QG) * a.B;
   if (groups <= 0) return cudaSuccess;
   const long long ctas = groups < sm_count() ? groups : sm_count();   // one persistent CTA per SM
-  return launch_overlapped(score_rows_kernel<H, QG, EPI, NMMA, F>, dim3((unsigned)ctas), dim3(C::THREADS), smem, stream,
-                           a);
+  // plain stream order: started early, the persistent CTAs measured slower steps (the large
+  // prefill 3.017 against 2.988 ms; their work runs for milliseconds, their start-up for
+  // microseconds)
+  return launch_kernel(false, score_rows_kernel<H, QG, EPI, NMMA, F>, dim3((unsigned)ctas), dim3(C::THREADS), smem,
+                       stream, a);
 }
 
 // The several-row kernel's epilogue warpgroups and MMA warps: three epilogue warpgroups for

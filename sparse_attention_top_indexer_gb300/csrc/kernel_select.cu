@@ -331,13 +331,16 @@ __global__ void __launch_bounds__(kSelThreads, 1) cand_topk_kernel(const CandArg
   select_top<kSelThreads, KPT>(key, k_eff, out, a.topk, a.offset, sh.sel, vis);
 }
 
+// The candidate-block kernels and the sparse top-k launch in plain stream order, without the
+// early start the other small grids take: the two-level decode step (8 rows over 32768 keys)
+// measured 45.9 against 51.0 us with it.
 template <int KPT>
 cudaError_t launch_cand_topk_kpt(const CandArgs& c, const TopkArgs& a, int nblk, cudaStream_t stream) {
   const dim3 grid(a.rows), block(kSelThreads);
-  if (nblk <= kSelThreads) return launch_overlapped(cand_topk_kernel<KPT, 1>, grid, block, 0, stream, c, a);
-  if (nblk <= 2 * kSelThreads) return launch_overlapped(cand_topk_kernel<KPT, 2>, grid, block, 0, stream, c, a);
-  if (nblk <= 4 * kSelThreads) return launch_overlapped(cand_topk_kernel<KPT, 4>, grid, block, 0, stream, c, a);
-  if (nblk <= 8 * kSelThreads) return launch_overlapped(cand_topk_kernel<KPT, 8>, grid, block, 0, stream, c, a);
+  if (nblk <= kSelThreads) return launch_kernel(false, cand_topk_kernel<KPT, 1>, grid, block, 0, stream, c, a);
+  if (nblk <= 2 * kSelThreads) return launch_kernel(false, cand_topk_kernel<KPT, 2>, grid, block, 0, stream, c, a);
+  if (nblk <= 4 * kSelThreads) return launch_kernel(false, cand_topk_kernel<KPT, 4>, grid, block, 0, stream, c, a);
+  if (nblk <= 8 * kSelThreads) return launch_kernel(false, cand_topk_kernel<KPT, 8>, grid, block, 0, stream, c, a);
   return cudaErrorInvalidValue;
 }
 
@@ -359,9 +362,9 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
   if (a.sparse) {   // kept positions only: at most cbk * cbs of them
     const long long E = (long long)a.cbk * a.cbs;
     if (a.cand == nullptr || E > (long long)kSelThreads * 8) return cudaErrorInvalidValue;
-    if (E <= 256 * 8) return launch_overlapped(topk_sparse_kernel<256, 8>, grid, dim3(256), 0, stream, a);
-    if (E <= 512 * 8) return launch_overlapped(topk_sparse_kernel<512, 8>, grid, dim3(512), 0, stream, a);
-    return launch_overlapped(topk_sparse_kernel<kSelThreads, 8>, grid, dim3(kSelThreads), 0, stream, a);
+    if (E <= 256 * 8) return launch_kernel(false, topk_sparse_kernel<256, 8>, grid, dim3(256), 0, stream, a);
+    if (E <= 512 * 8) return launch_kernel(false, topk_sparse_kernel<512, 8>, grid, dim3(512), 0, stream, a);
+    return launch_kernel(false, topk_sparse_kernel<kSelThreads, 8>, grid, dim3(kSelThreads), 0, stream, a);
   }
   if (a.rows >= 4096 && a.T > 256 * 8 && a.T <= 256 * 32) {
     // many rows (prefill): 256 threads per row with up to 32 keys each, so several rows
@@ -384,10 +387,10 @@ cudaError_t launch_topk(const TopkArgs& a, cudaStream_t stream) {
 template <int PPT>
 cudaError_t launch_cand_ppt(const CandArgs& a, int nblk, cudaStream_t stream) {
   const dim3 grid(a.rows), block(kSelThreads);
-  if (nblk <= kSelThreads) return launch_overlapped(cand_kernel<PPT, 1>, grid, block, 0, stream, a);
-  if (nblk <= 2 * kSelThreads) return launch_overlapped(cand_kernel<PPT, 2>, grid, block, 0, stream, a);
-  if (nblk <= 4 * kSelThreads) return launch_overlapped(cand_kernel<PPT, 4>, grid, block, 0, stream, a);
-  if (nblk <= 8 * kSelThreads) return launch_overlapped(cand_kernel<PPT, 8>, grid, block, 0, stream, a);
+  if (nblk <= kSelThreads) return launch_kernel(false, cand_kernel<PPT, 1>, grid, block, 0, stream, a);
+  if (nblk <= 2 * kSelThreads) return launch_kernel(false, cand_kernel<PPT, 2>, grid, block, 0, stream, a);
+  if (nblk <= 4 * kSelThreads) return launch_kernel(false, cand_kernel<PPT, 4>, grid, block, 0, stream, a);
+  if (nblk <= 8 * kSelThreads) return launch_kernel(false, cand_kernel<PPT, 8>, grid, block, 0, stream, a);
   return cudaErrorInvalidValue;
 }
 

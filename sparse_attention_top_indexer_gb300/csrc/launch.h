@@ -11,11 +11,13 @@ struct IndexerDims;   // include/indexer.h
 
 namespace indexer {
 
-// Launches `kernel` with programmatic stream serialisation (the kernel calls pdl_wait()
-// before touching global memory; see device_common.cuh).
+// Launches `kernel` in stream order. With `overlap`, by programmatic stream serialisation: the
+// kernel may start while the one before it still runs, and calls pdl_wait() before touching
+// global memory (see device_common.cuh); without, it starts once the kernel before it is done
+// (its pdl_wait() then returns at once).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                              Args&&... args) {
+cudaError_t launch_kernel(bool overlap, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                          cudaStream_t stream, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
@@ -23,10 +25,24 @@ cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[0].val.programmaticStreamSerializationAllowed = overlap ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
+// The overlap pays for short, latency-bound grids (a decode step: 17.9 against 18.7 us with
+// no overlap anywhere). A grid of more CTAs than this runs many waves, its start-up is a
+// small share of its time, and the early start measured a loss (the large prefill's key
+// publish, query prep and top-k launched without it: 3.029 -> 3.017 ms a step), so such
+// grids launch in plain stream order.
+constexpr long long kOverlapMaxCtas = 1024;
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_overlapped(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  const bool overlap = (long long)grid.x * grid.y * grid.z <= kOverlapMaxCtas;
+  return launch_kernel(overlap, kernel, grid, block, smem, stream, static_cast<Args&&>(args)...);
 }
 
 constexpr int kMaxRopeHalf = 64;
