@@ -296,12 +296,13 @@ __device__ __forceinline__ uint2 quant_q_slice_fp8(uint4 raw, int j, const float
 }
 
 // ----------------------------------------------------------------------------- launch overlap
-// Every kernel of the library is launched with programmatic stream serialisation: it may
-// start while the kernel before it on the stream is still running. pdl_allow_next() lets
-// the next kernel start in turn; pdl_wait() blocks until every earlier kernel on the
-// stream has completed and its memory is visible, and each kernel calls it before its
-// first global-memory access (read or write), so only shared-memory set-up overlaps.
-// Both are no-ops for a kernel launched without that attribute.
+// The library's small, latency-bound grids are launched with programmatic stream
+// serialisation (launch.h): such a kernel may start while the kernel before it on the stream
+// is still running. pdl_allow_next() lets the next kernel start in turn; pdl_wait() blocks
+// until every earlier kernel on the stream has completed and its memory is visible, and each
+// kernel calls it before its first global-memory access (read or write), so only
+// shared-memory set-up overlaps. Both are no-ops for a kernel launched without that
+// attribute (the long grids), which starts once the kernel before it is done.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_allow_next() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
